@@ -1,0 +1,164 @@
+"""numpy wrapper around the plain-C oracle (``pulse_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+All arrays are numpy: FP32 master weights as ``float32``, BF16 weights,
+patch values and masks as ``uint16`` bit patterns, patch indices as
+``uint32``. Functions that update ``prev`` or ``w`` do so in place, like the
+CUDA entry points they check.
+
+Multi-tensor forms run the single-tensor definition over the tensors in list
+order; each tensor has its own patch segment with tensor-local indices (the
+whole-model, single-launch form described in the humansand.ai summary,
+section "Pipeline'i GPU'lara tasimak", computes exactly this).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pulse_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared library with gcc -O2 (no CUDA)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-Werror",
+                        "-shared", "-fPIC", "-o", tmp, _SRC], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            U64 = ctypes.c_uint64
+            lib.oracle_bf16_rne.argtypes = [ctypes.c_uint32]
+            lib.oracle_bf16_rne.restype = ctypes.c_uint16
+            lib.oracle_bf16_rne_array.argtypes = [P, P, U64]
+            lib.oracle_bf16_rne_array.restype = None
+            lib.oracle_encode.argtypes = [P, P, U64, P, P]
+            lib.oracle_encode.restype = U64
+            lib.oracle_count_changed.argtypes = [P, P, U64]
+            lib.oracle_count_changed.restype = U64
+            lib.oracle_apply.argtypes = [P, P, P, U64]
+            lib.oracle_apply.restype = None
+            lib.oracle_xor_mask.argtypes = [P, P, U64, P]
+            lib.oracle_xor_mask.restype = None
+            lib.oracle_xor_apply.argtypes = [P, P, U64]
+            lib.oracle_xor_apply.restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _check(a: np.ndarray, dtype, name: str, writable: bool = False):
+    if not isinstance(a, np.ndarray) or a.dtype != dtype or a.ndim != 1:
+        raise TypeError(f"{name}: expected a 1-D numpy {np.dtype(dtype).name} array")
+    if not a.flags.c_contiguous:
+        raise TypeError(f"{name}: must be contiguous")
+    if writable and not a.flags.writeable:
+        raise TypeError(f"{name}: must be writable")
+
+
+def bf16_rne(bits) -> np.ndarray | int:
+    """RNE cast of FP32 bit patterns (uint32 array or int) to BF16 bits."""
+    lib = _load()
+    if isinstance(bits, (int, np.integer)):
+        return int(lib.oracle_bf16_rne(int(bits) & 0xFFFFFFFF))
+    a = np.ascontiguousarray(bits, dtype=np.uint32).reshape(-1)
+    out = np.empty(a.size, dtype=np.uint16)
+    lib.oracle_bf16_rne_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def encode(master: np.ndarray, prev: np.ndarray):
+    """Returns (idx[k] uint32, val[k] uint16); refreshes ``prev`` in place."""
+    _check(master, np.float32, "master")
+    _check(prev, np.uint16, "prev", writable=True)
+    if master.size != prev.size:
+        raise ValueError("master and prev differ in length")
+    n = master.size
+    idx = np.empty(max(n, 1), dtype=np.uint32)
+    val = np.empty(max(n, 1), dtype=np.uint16)
+    k = _load().oracle_encode(_ptr(master), _ptr(prev), n, _ptr(idx), _ptr(val))
+    return idx[:k].copy(), val[:k].copy()
+
+
+def count_changed(master: np.ndarray, prev: np.ndarray) -> int:
+    _check(master, np.float32, "master")
+    _check(prev, np.uint16, "prev")
+    return int(_load().oracle_count_changed(_ptr(master), _ptr(prev), master.size))
+
+
+def apply(w: np.ndarray, idx: np.ndarray, val: np.ndarray) -> None:
+    """w[idx[j]] = val[j] for j in order, in place."""
+    _check(w, np.uint16, "w", writable=True)
+    _check(idx, np.uint32, "idx")
+    _check(val, np.uint16, "val")
+    if idx.size != val.size:
+        raise ValueError("idx and val differ in length")
+    if idx.size and int(idx.max()) >= w.size:
+        raise IndexError("patch index out of range")
+    _load().oracle_apply(_ptr(w), _ptr(idx), _ptr(val), idx.size)
+
+
+def xor_mask(master: np.ndarray, prev: np.ndarray) -> np.ndarray:
+    """Returns mask = rne(master) ^ prev; refreshes ``prev`` in place."""
+    _check(master, np.float32, "master")
+    _check(prev, np.uint16, "prev", writable=True)
+    if master.size != prev.size:
+        raise ValueError("master and prev differ in length")
+    mask = np.empty(master.size, dtype=np.uint16)
+    _load().oracle_xor_mask(_ptr(master), _ptr(prev), master.size, _ptr(mask))
+    return mask
+
+
+def xor_apply(w: np.ndarray, mask: np.ndarray) -> None:
+    """w ^= mask, in place."""
+    _check(w, np.uint16, "w", writable=True)
+    _check(mask, np.uint16, "mask")
+    if w.size != mask.size:
+        raise ValueError("w and mask differ in length")
+    _load().oracle_xor_apply(_ptr(w), _ptr(mask), w.size)
+
+
+# ------------------------------------------------------------ multi-tensor
+
+def encode_multi(masters, prevs):
+    """List-order encode; returns a list of (idx, val) segments."""
+    return [encode(m, p) for m, p in zip(masters, prevs)]
+
+
+def apply_multi(ws, patches) -> None:
+    for w, (idx, val) in zip(ws, patches):
+        apply(w, idx, val)
+
+
+def xor_mask_multi(masters, prevs):
+    return [xor_mask(m, p) for m, p in zip(masters, prevs)]
+
+
+def xor_apply_multi(ws, masks) -> None:
+    for w, m in zip(ws, masks):
+        xor_apply(w, m)
