@@ -1,0 +1,535 @@
+"""Benchmark of the weight-delta hot path: whole-model encode + apply.
+
+Default workload: the Llama-3-8B-shaped tensor set (291 tensors,
+8,030,261,248 FP32 master params, N(0, 0.02) weights, RMSNorm 1 + N(0, 0.01)),
+one Adam-sized step eta = 3e-6, synthetic data drawn on the device.
+
+One step = pulse_encode_multi (FP32 -> BF16 RNE, bitwise compare,
+order-preserving compaction, prev refresh) + pulse_apply_multi_device
+(scatter into the sampler's BF16 weights), one launch each over the whole
+model. Before every step prev and the sampler weights are restored from a
+pristine copy (untimed), so every timed step encodes the same real update.
+Inputs (48 GB) are far larger than L2 (129 MB), so no L2 flush is needed.
+
+Printed: one JSON line with params/s (value), the roofline of the encode
+kernel against measured HBM copy bandwidth, the XOR-mask path, an
+end-to-end number through host buffers, the CPU oracle baseline, and the
+SM clocks sampled during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "encode+apply params/s"
+UNIT = "params/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "encode_multi_llama3_8b.md")
+ENCODE_SRC = os.path.join(ROOT, "rl_post_trainer_gb300", "csrc", "encode.cu")
+
+
+# ------------------------------------------------------------- utilities
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per encode launch recorded under profiles/, if the kernel
+    source is unchanged since that capture (sha256 of encode.cu)."""
+    try:
+        text = open(PROFILE_SUMMARY, encoding="utf-8").read()
+        src_hash = hashlib.sha256(open(ENCODE_SRC, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("encode.cu sha256") != src_hash:
+        return None
+    try:
+        return float(fields["traffic_bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() in ("active", "1"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------- workload
+
+class Workload:
+    """Device buffers of one model: trainer (master, prev), sampler (w),
+    patch segments, XOR buffers, and a pristine copy of the initial view."""
+
+    def __init__(self, specs, seed, eta, dev, xor=True):
+        import rl_post_trainer_gb300 as pulse
+        self.specs = specs
+        self.n = workloads.total_params(specs)
+        pairs = workloads.torch_model(specs, seed, eta, dev)
+        self.master = [m for m, _ in pairs]
+        self.prev0 = [p for _, p in pairs]
+        self.prev = [p.clone() for p in self.prev0]
+        self.w = [p.clone() for p in self.prev0]
+        self.idx = [torch.empty(s.numel, dtype=torch.int32, device=dev) for s in specs]
+        self.val = [torch.empty(s.numel, dtype=torch.int16, device=dev) for s in specs]
+        self.plan = pulse.Plan([pulse.TensorSlot(s.numel, master=self.master[i], prev=self.prev[i],
+                                                 w=self.w[i], idx=self.idx[i], val=self.val[i])
+                                for i, s in enumerate(specs)])
+        self.counts = torch.zeros(len(specs), dtype=torch.int64, device=dev)
+        self.xor = xor
+        if xor:
+            self.prev_x = [p.clone() for p in self.prev0]
+            self.w_x = [p.clone() for p in self.prev0]
+            self.mask = [torch.empty(s.numel, dtype=torch.int16, device=dev) for s in specs]
+            self.xplan = pulse.Plan([pulse.TensorSlot(s.numel, master=self.master[i],
+                                                      prev=self.prev_x[i], w=self.w_x[i],
+                                                      mask=self.mask[i])
+                                     for i, s in enumerate(specs)])
+
+    def restore(self):
+        for p, w, p0 in zip(self.prev, self.w, self.prev0):
+            p.copy_(p0)
+            w.copy_(p0)
+
+    def restore_xor(self):
+        for p, w, p0 in zip(self.prev_x, self.w_x, self.prev0):
+            p.copy_(p0)
+            w.copy_(p0)
+
+    def sectors_touched(self, counts_np) -> int:
+        """Distinct 32-byte sectors of the BF16 arrays holding a changed element
+        (buffers are 512-byte aligned, so sector = index // 16)."""
+        total = 0
+        for t, k in enumerate(counts_np):
+            k = int(k)
+            if k == 0:
+                continue
+            s = self.idx[t][:k].to(torch.int64) // 16
+            total += 1 + int((s[1:] != s[:-1]).sum().item())
+        return total
+
+
+def barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+
+
+def _reduce(x: float, op, dist_on) -> float:
+    if not dist_on:
+        return x
+    on_gpu = torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
+    torch.distributed.all_reduce(t, op=op)
+    return float(t.item())
+
+
+def max_over_ranks(x: float, dist_on) -> float:
+    """Slowest rank's time: the job is done when every rank is done."""
+    return _reduce(x, torch.distributed.ReduceOp.MAX if dist_on else None, dist_on)
+
+
+def sum_over_ranks(x: float, dist_on) -> float:
+    """Work of all ranks (weak scaling: each rank runs its own model replica)."""
+    return _reduce(x, torch.distributed.ReduceOp.SUM if dist_on else None, dist_on)
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(specs, seed, eta, max_params, dev):
+    """First tensors of the model (list order) up to max_params, host copies
+    of (master, prev0) drawn with the same generator as the device workload."""
+    chosen, total = [], 0
+    for s in specs:
+        if chosen and total + s.numel > max_params:
+            break
+        chosen.append(s)
+        total += s.numel
+    if dev is not None:
+        pairs = workloads.torch_model(chosen, seed, eta, dev)
+        host = [(m.cpu().numpy(), p.cpu().numpy().view(np.uint16)) for m, p in pairs]
+        del pairs
+    else:
+        rng = np.random.default_rng(seed)
+        host = []
+        for s in chosen:
+            w0 = workloads.np_init(s, rng)
+            host.append((workloads.np_update(w0, eta, rng), workloads.np_bf16_view_torch(w0)))
+    return chosen, host, total
+
+
+def time_oracle(host_pairs, threads):
+    """Wall time of oracle encode + apply over the sample (tensors spread over
+    `threads` host threads; the oracle code itself is single-threaded)."""
+    import oracle
+    oracle.build()
+    work = [(m, p.copy(), p.copy()) for m, p in host_pairs]
+
+    def one(item):
+        m, prev, w = item
+        idx, val = oracle.encode(m, prev)
+        oracle.apply(w, idx, val)
+        return idx.size
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        ks = list(ex.map(one, work))
+    return time.perf_counter() - t0, sum(ks)
+
+
+# ----------------------------------------------------------------- arms
+
+def run_reference(args, cfg, specs, rank, world, dist_on):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    cores = host_cores()
+    chosen, host, total = oracle_sample(specs, cfg["seed"], cfg["eta"], args.cpu_sample_params, dev)
+    threads = max(1, min(cores, len(chosen)))
+    for _ in range(args.warmup):
+        time_oracle(host, threads)
+    times, ks = [], []
+    for _ in range(args.steps):
+        t, k = time_oracle(host, threads)
+        times.append(t)
+        ks.append(k)
+    tt = sum(times)
+    value = total * args.steps / tt
+    sample = (f"first {len(chosen)} tensors of {cfg['name']} ({total} of "
+              f"{workloads.total_params(specs)} params), encode+apply, {threads} threads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic",
+        "config": {"workload": cfg["name"], "params": workloads.total_params(specs),
+                   "tensors": len(specs), "eta": cfg["eta"], "sample_params": total},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "density": float(np.mean(ks)) / total,
+    }
+
+
+def run_ours(args, cfg, specs, rank, world, dist_on):
+    import rl_post_trainer_gb300 as pulse
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = Workload(specs, cfg["seed"] + 1000 * rank, cfg["eta"], dev, xor=not args.no_xor)
+    n = wl.n
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        wl.plan.encode(wl.counts)
+        if ev is not None:
+            ev[1].record(stream)
+        wl.plan.apply(wl.counts)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        wl.restore()
+        step()
+    torch.cuda.synchronize()
+    if wl.plan.get_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    counts_np = wl.counts.cpu().numpy()
+    k = int(counts_np.sum())
+
+    t_enc, t_app = [], []
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        for _ in range(args.steps):
+            wl.restore()
+            torch.cuda.synchronize()
+            barrier(dist_on)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            step(ev)
+            torch.cuda.synchronize()
+            barrier(dist_on)
+            t_enc.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+            t_app.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+    if wl.plan.get_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+    # the sampler holds the trainer's new view after every step
+    for t in range(len(specs)):
+        if not torch.equal(wl.w[t], wl.prev[t]):
+            raise RuntimeError(f"sampler weights differ from the trainer view (tensor {t})")
+
+    step_s = max_over_ranks(sum(t_enc) + sum(t_app), dist_on)
+    total_params = sum_over_ranks(float(n), dist_on)
+    value = total_params * args.steps / step_s
+    enc_s = float(np.mean(t_enc))
+    app_s = float(np.mean(t_app))
+    S = wl.sectors_touched(counts_np)
+    enc_alg = 6.0 * n + 8.0 * k
+    enc_sec = 6.0 * n + 32.0 * S + 6.0 * k
+    app_alg = 8.0 * k
+    app_sec = 6.0 * k + 32.0 * S
+    app_rmw = 6.0 * k + 64.0 * S
+    peak, peak_kind = measured_peak_gbs()
+    achieved = enc_alg / enc_s / 1e9
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * step_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic",
+        "config": {"workload": cfg["name"], "params": n, "tensors": len(specs), "eta": cfg["eta"],
+                   "density": k / n, "patch_entries": k, "parallelism": f"replicas{world}",
+                   "l2": "inputs (48 GB) larger than L2; prev and w restored untimed before each step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "kernel": "encode_kernel<multi>", "peak_kind": peak_kind,
+                     "bytes_model": "6n+8k"},
+        "encode": {"ms": 1e3 * enc_s, "params_per_s": n / enc_s,
+                   "gbs_algorithmic": enc_alg / enc_s / 1e9, "gbs_sector": enc_sec / enc_s / 1e9,
+                   "frac_measured_peak": enc_alg / enc_s / 1e9 / peak,
+                   "frac_nominal_8tbs": enc_alg / enc_s / 1e9 / NOMINAL_HBM_GBS,
+                   "frac_sector_measured_peak": enc_sec / enc_s / 1e9 / peak,
+                   "frac_sector_nominal_8tbs": enc_sec / enc_s / 1e9 / NOMINAL_HBM_GBS},
+        "apply": {"ms": 1e3 * app_s, "params_per_s": n / app_s,
+                  "gbs_algorithmic": app_alg / app_s / 1e9, "gbs_sector": app_sec / app_s / 1e9,
+                  "gbs_sector_rmw": app_rmw / app_s / 1e9,
+                  "frac_sector_rmw_measured_peak": app_rmw / app_s / 1e9 / peak,
+                  "frac_sector_rmw_nominal_8tbs": app_rmw / app_s / 1e9 / NOMINAL_HBM_GBS},
+        "sectors_touched": S,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+    if wl.xor:
+        tm, ta = [], []
+        for _ in range(max(1, args.steps)):
+            wl.restore_xor()
+            torch.cuda.synchronize()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            wl.xplan.xor_mask()
+            ev[1].record(stream)
+            wl.xplan.xor_apply()
+            ev[2].record(stream)
+            torch.cuda.synchronize()
+            tm.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+            ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+        xm, xa = float(np.mean(tm)), float(np.mean(ta))
+        xm_bytes = 8.0 * n + 32.0 * S
+        xa_bytes = 2.0 * n + 64.0 * S
+        out["xor"] = {"mask_ms": 1e3 * xm, "apply_ms": 1e3 * xa,
+                      "params_per_s": n / (xm + xa),
+                      "mask_gbs_sector": xm_bytes / xm / 1e9,
+                      "mask_frac_measured_peak": xm_bytes / xm / 1e9 / peak,
+                      "apply_gbs_sector_rmw": xa_bytes / xa / 1e9,
+                      "apply_frac_measured_peak": xa_bytes / xa / 1e9 / peak}
+        for t in range(len(specs)):
+            if not torch.equal(wl.w_x[t], wl.prev[t]):
+                raise RuntimeError(f"XOR path disagrees with the patch path (tensor {t})")
+        del wl.prev_x, wl.w_x, wl.mask
+        wl.xplan.close()
+
+    if not args.no_e2e:
+        out["e2e"] = e2e(args, wl, counts_np, dist_on)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = host_cores()
+        chosen, host, total = oracle_sample(specs, cfg["seed"], cfg["eta"], args.cpu_sample_params, dev)
+        threads = max(1, min(cores, len(chosen)))
+        t, _ = time_oracle(host, threads)
+        out["cpu_baseline"] = {
+            "value": total / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {len(chosen)} tensors ({total} params) of {cfg['name']}, "
+                      f"encode+apply, one oracle call per tensor on {threads} threads"}
+    return out
+
+
+def e2e(args, wl, counts_np, dist_on):
+    """Same metric through the public API with HOST buffers: every step copies
+    the new FP32 master from pinned host memory, encodes, reads the patch back
+    to pinned host memory (the wire), copies it to the sampler and applies."""
+    try:
+        host_master = []
+        for m in wl.master:
+            h = torch.empty(m.shape, dtype=m.dtype, pin_memory=True)
+            h.copy_(m)
+            host_master.append(h)
+        cap = [int(c * 1.05) + 1024 for c in counts_np]
+        h_idx = [torch.empty(c, dtype=torch.int32, pin_memory=True) for c in cap]
+        h_val = [torch.empty(c, dtype=torch.int16, pin_memory=True) for c in cap]
+    except RuntimeError as exc:  # not enough pinnable host memory
+        return {"value": None, "unit": UNIT, "error": str(exc)[:200]}
+    n = wl.n
+    T = len(wl.specs)
+
+    def one_step():
+        for m, hm in zip(wl.master, host_master):
+            m.copy_(hm, non_blocking=True)
+        wl.plan.encode(wl.counts)
+        ks = wl.counts.cpu().tolist()
+        for t in range(T):
+            k = ks[t]
+            if k > cap[t]:
+                raise RuntimeError("patch larger than the staging buffer")
+            h_idx[t][:k].copy_(wl.idx[t][:k], non_blocking=True)
+            h_val[t][:k].copy_(wl.val[t][:k], non_blocking=True)
+        torch.cuda.synchronize()
+        for t in range(T):
+            k = ks[t]
+            wl.idx[t][:k].copy_(h_idx[t][:k], non_blocking=True)
+            wl.val[t][:k].copy_(h_val[t][:k], non_blocking=True)
+        wl.plan.apply(ks)
+        torch.cuda.synchronize()
+        return sum(ks)
+
+    for _ in range(min(args.warmup, 1)):
+        wl.restore()
+        one_step()
+    times, ktot = [], 0
+    for _ in range(args.steps):
+        wl.restore()
+        torch.cuda.synchronize()
+        barrier(dist_on)
+        t0 = time.perf_counter()
+        ktot = one_step()
+        times.append(time.perf_counter() - t0)
+        barrier(dist_on)
+    tt = max_over_ranks(sum(times), dist_on)
+    total_params = sum_over_ranks(float(n), dist_on)
+    return {"value": total_params * args.steps / tt, "unit": UNIT,
+            "h2d_bytes_per_step": int(4 * n + 6 * ktot + 8 * T),
+            "d2h_bytes_per_step": int(6 * ktot + 8 * T),
+            "ms_per_step": 1e3 * tt / args.steps}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-xor", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-params", type=float, default=1.2e9)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = dict(workloads.CONFIGS[args.config])
+    if cfg["eta"] is None:
+        cfg["eta"] = workloads.ETA_DEFAULT
+    specs = cfg["specs"]()
+
+    if args.impl == "reference":
+        # the oracle runs on rank 0's host cores; other ranks have no work
+        if rank == 0:
+            out = run_reference(args, cfg, specs, rank, world, False)
+            print(json.dumps(out), flush=True)
+        return
+
+    dist_on = world > 1
+    if dist_on:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend=backend)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    out = run_ours(args, cfg, specs, rank, world, dist_on)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,246 @@
+/*
+ * pulse.h -- C ABI of the GB300 (sm_103a) compute-visible weight-delta
+ * library: trainer-side encode of a BF16 patch or XOR mask from FP32 master
+ * weights, and sampler-side apply of that patch or mask.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [TALK]  "Taking Reinforcement Learning Cross Datacenter" -- Nan Jiang,
+ *          Modal (talk transcript): 07:24-08:20 the forward pass reads a BF16
+ *          view of the FP32 master weights, spacing ~theta/128, visibility
+ *          boundary ~theta/256; 10:49-11:30 project to the serving dtype,
+ *          compare version t-1 with t, the patch is changed positions plus
+ *          replacement bits plus metadata, applied as selective overrides or
+ *          as XOR, reconstructing the served version bitwise.
+ *  [PULSE] "Riepilogo Tecnico" of arXiv 2602.03839 (PULSE), section
+ *          "Metodologia: PULSE -- 1. PULSESync": compare consecutive BF16
+ *          checkpoints, send the indices and new values of the changed
+ *          parameters, the sampler applies them to its BF16 weights; absolute
+ *          values make the result bit-identical to a full checkpoint.
+ *  [XOR]   humansand.ai summary "GPU agirlik isinlanmasi RL sampler'larini
+ *          4 saniyenin altinda ...", sections "XOR maskeleri ile delta
+ *          senkronizasyonu" (mask = XOR of pre- and post-step weights, same
+ *          size as the weights, XOR-ed in place by the sampler) and
+ *          "Pipeline'i GPU'lara tasimak" (one kernel launch covers the whole
+ *          model, with tiling and address-map metadata prepared on the CPU).
+ *  [PPLX]  "Weight transfer for RL post-training in under 2 seconds"
+ *          (Perplexity), section "Statyczny harmonogram": the transfer
+ *          schedule is computed once at initialisation and replayed each step.
+ *
+ * Conventions shared by every entry point:
+ *  - BF16 data (prev, w, val, mask) is passed as uint16_t bit patterns.
+ *  - Unless a parameter says "host", every pointer is DEVICE memory of the
+ *    CUDA device that is current on the calling thread. The caller owns all
+ *    buffers and keeps them alive until `stream` has passed the call.
+ *  - All calls are asynchronous on `stream` (0 = legacy default stream) and
+ *    return a status code synchronously. A non-zero status from argument
+ *    checking means nothing was launched. Device-side errors (a wait that
+ *    gave up, an out-of-range patch index) are recorded in a device error
+ *    word and reported by pulse_get_error / pulse_plan_get_error.
+ *  - Element counts n are < 2^32 (patch indices are uint32, tensor-local).
+ *  - The cast is IEEE round-to-nearest-even; subnormals are kept; values past
+ *    the largest finite BF16 round to infinity; every NaN becomes 0x7FC0.
+ *  - "Changed" compares 16-bit patterns, so +0 -> -0 is a change.
+ *  - Output buffers must not overlap input buffers; prev and w are updated in
+ *    place.
+ *  - No call prints, aborts, traps or throws.
+ */
+#ifndef PULSE_H
+#define PULSE_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define PULSE_OK           0  /* success */
+#define PULSE_ERR_INVALID  1  /* null pointer where one is required, bad count, overlap */
+#define PULSE_ERR_RANGE    2  /* an element count is >= 2^32 */
+#define PULSE_ERR_CUDA     3  /* a CUDA runtime call or kernel launch failed */
+#define PULSE_ERR_TIMEOUT  4  /* device: a bounded wait gave up; outputs of that call are invalid */
+#define PULSE_ERR_INDEX    5  /* device: a checked apply met an index >= n and skipped it */
+#define PULSE_ERR_NOMEM    6  /* workspace allocation failed */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *pulse_error_string(int status);
+
+/* Elements per encode tile (compile-time constant of this build). */
+uint32_t pulse_encode_tile_elems(void);
+
+/*
+ * pulse_encode -- trainer-side encode of one tensor. [TALK] 10:49-11:08,
+ * [PULSE] "1. PULSESync".
+ *
+ * For every i in [0, n): b = RNE_bf16(master_f32[i]); if b differs bitwise
+ * from prev_bf16[i], the pair (i, b) is part of the patch and prev_bf16[i]
+ * is set to b. The patch is written densely, in ascending index order:
+ * idx_out[0..k) = changed positions, val_out[0..k) = their new absolute BF16
+ * bits; *count_out = k (device uint64). prev_bf16 ends equal to the new view.
+ *
+ *   master_f32  device, n floats, read only
+ *   prev_bf16   device, n uint16, read and updated in place
+ *   idx_out     device, room for n uint32 (the worst case, all changed)
+ *   val_out     device, room for n uint16
+ *   count_out   device, one uint64
+ *
+ * n == 0 writes *count_out = 0 and launches only that write. Uses a library
+ * workspace per (device, stream), allocated on first use and grown on demand
+ * (growth synchronises `stream`); concurrent calls on one stream are ordered
+ * by the stream, calls on different streams use different workspaces.
+ * Errors: PULSE_ERR_INVALID (null pointer when n > 0), PULSE_ERR_RANGE
+ * (n >= 2^32), PULSE_ERR_NOMEM, PULSE_ERR_CUDA; device: PULSE_ERR_TIMEOUT.
+ */
+int pulse_encode(const float *master_f32, uint16_t *prev_bf16, uint64_t n,
+                 uint32_t *idx_out, uint16_t *val_out, uint64_t *count_out,
+                 cudaStream_t stream);
+
+/*
+ * pulse_apply -- sampler-side patch apply. [TALK] 11:08-11:30 ("selective
+ * overrides"), [PULSE] "1. PULSESync".
+ *
+ * For j in [0, count): w_bf16[idx[j]] = val[j]. With the patch of an encode
+ * (ascending, distinct indices) the result does not depend on order. The
+ * caller guarantees idx[j] < size of w_bf16; use pulse_apply_checked when it
+ * cannot.
+ *
+ *   w_bf16  device, updated in place
+ *   idx     device, count uint32;  val  device, count uint16
+ *   count   HOST value (the receiver knows the patch length)
+ * count == 0 launches nothing. Errors: PULSE_ERR_INVALID, PULSE_ERR_CUDA.
+ */
+int pulse_apply(uint16_t *w_bf16, const uint32_t *idx, const uint16_t *val,
+                uint64_t count, cudaStream_t stream);
+
+/*
+ * pulse_apply_checked -- as pulse_apply, for a w_bf16 of n elements; an entry
+ * with idx[j] >= n is skipped and PULSE_ERR_INDEX is recorded in the device
+ * error word of (device, stream), read by pulse_get_error.
+ */
+int pulse_apply_checked(uint16_t *w_bf16, uint64_t n, const uint32_t *idx,
+                        const uint16_t *val, uint64_t count, cudaStream_t stream);
+
+/*
+ * pulse_xor_mask -- trainer-side XOR mask of one tensor. [XOR] "XOR maskeleri
+ * ile delta senkronizasyonu".
+ *
+ * For every i in [0, n): b = RNE_bf16(master_f32[i]); mask_out[i] =
+ * b ^ prev_bf16[i]; prev_bf16[i] = b. Non-zero mask words are exactly the
+ * positions pulse_encode would list.
+ *   master_f32 device n floats; prev_bf16 device n uint16 (in/out);
+ *   mask_out device n uint16.
+ * n == 0 launches nothing. Errors: PULSE_ERR_INVALID, PULSE_ERR_RANGE,
+ * PULSE_ERR_CUDA.
+ */
+int pulse_xor_mask(const float *master_f32, uint16_t *prev_bf16, uint64_t n,
+                   uint16_t *mask_out, cudaStream_t stream);
+
+/*
+ * pulse_xor_apply -- sampler-side XOR apply. [XOR] same section: w ^= mask
+ * on raw bits; applying the same mask twice restores the original.
+ *   w_bf16 device n uint16 (in/out); mask device n uint16.
+ * n == 0 launches nothing. Errors: PULSE_ERR_INVALID, PULSE_ERR_RANGE,
+ * PULSE_ERR_CUDA.
+ */
+int pulse_xor_apply(uint16_t *w_bf16, const uint16_t *mask, uint64_t n,
+                    cudaStream_t stream);
+
+/*
+ * Device error word of the (current device, stream) workspace used by the
+ * single-tensor calls. Synchronises `stream`, then returns and clears the
+ * recorded error: PULSE_OK, PULSE_ERR_TIMEOUT or PULSE_ERR_INDEX (timeout
+ * wins if both were recorded), or PULSE_ERR_CUDA if the synchronisation
+ * itself failed.
+ */
+int pulse_get_error(cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Multi-tensor plans. [XOR] "Pipeline'i GPU'lara tasimak": the tile and
+ * address map of a whole model is prepared on the host and one kernel launch
+ * covers every tensor; [PPLX] "Statyczny harmonogram": the plan is built once
+ * and replayed each step.
+ *
+ * One pulse_tensor per model tensor, in a fixed list order. Fields a given
+ * operation does not use may be NULL:
+ *   encode_multi     master, prev, idx, val
+ *   apply_multi      w, idx, val
+ *   xor_mask_multi   master, prev, mask
+ *   xor_apply_multi  w, mask
+ * idx/val of tensor t hold that tensor's own patch segment (room for n
+ * entries; indices are local to the tensor). n may be 0.
+ * ---------------------------------------------------------------------- */
+typedef struct pulse_tensor {
+    const float *master;  /* device, n floats (trainer) */
+    uint16_t *prev;       /* device, n uint16 (trainer, in/out) */
+    uint16_t *w;          /* device, n uint16 (sampler, in/out) */
+    uint64_t n;           /* elements, < 2^32 */
+    uint32_t *idx;        /* device, room for n uint32 (patch segment) */
+    uint16_t *val;        /* device, room for n uint16 (patch segment) */
+    uint16_t *mask;       /* device, n uint16 (XOR mask) */
+} pulse_tensor;
+
+typedef struct pulse_plan pulse_plan;
+
+/*
+ * Build a plan for `ntensors` tensors (host array `tensors`, copied). Builds
+ * the tile tables on the host, uploads them, and allocates the plan's
+ * workspace on the current device; synchronous. *plan_out receives the
+ * handle. Errors: PULSE_ERR_INVALID (null arguments, ntensors < 1),
+ * PULSE_ERR_RANGE (some n >= 2^32), PULSE_ERR_NOMEM, PULSE_ERR_CUDA.
+ */
+int pulse_plan_create(const pulse_tensor *tensors, int ntensors, pulse_plan **plan_out);
+
+/* Free a plan (synchronises the device first). NULL is accepted. */
+int pulse_plan_destroy(pulse_plan *plan);
+
+/* Number of tensors and total encode tiles of a plan (0 on a NULL plan). */
+int pulse_plan_num_tensors(const pulse_plan *plan);
+uint64_t pulse_plan_num_tiles(const pulse_plan *plan);
+
+/*
+ * Encode every tensor of the plan in one launch; counts_out (device,
+ * ntensors uint64) receives each tensor's patch length k_t. Per tensor the
+ * result equals pulse_encode on that tensor. Errors: PULSE_ERR_INVALID (a
+ * required field is NULL in the plan), PULSE_ERR_CUDA; device:
+ * PULSE_ERR_TIMEOUT.
+ */
+int pulse_encode_multi(pulse_plan *plan, uint64_t *counts_out, cudaStream_t stream);
+
+/*
+ * Apply every tensor's patch segment in one launch. counts_host (HOST,
+ * ntensors uint64) gives each segment's length; it is copied before the call
+ * returns. Entries with idx >= n of their tensor are skipped and recorded as
+ * PULSE_ERR_INDEX in the plan's error word.
+ */
+int pulse_apply_multi(pulse_plan *plan, const uint64_t *counts_host, cudaStream_t stream);
+
+/* As pulse_apply_multi with the counts in DEVICE memory (e.g. counts_out of
+ * pulse_encode_multi), so no host round trip is needed. */
+int pulse_apply_multi_device(pulse_plan *plan, const uint64_t *counts_dev, cudaStream_t stream);
+
+/* XOR mask / XOR apply over every tensor of the plan, one launch each. */
+int pulse_xor_mask_multi(pulse_plan *plan, cudaStream_t stream);
+int pulse_xor_apply_multi(pulse_plan *plan, cudaStream_t stream);
+
+/* Synchronise the device, then return and clear the plan's device error word
+ * (PULSE_OK, PULSE_ERR_TIMEOUT or PULSE_ERR_INDEX). */
+int pulse_plan_get_error(pulse_plan *plan);
+
+/*
+ * Test hook for the look-back watchdog (not for production use). Runs
+ * pulse_encode with a wait limit of `wait_limit_ns` nanoseconds while tile 0
+ * is never processed, so tile 1 waits for a predecessor that never
+ * publishes. Expected outcome: the wait gives up, PULSE_ERR_TIMEOUT is
+ * recorded for pulse_get_error(stream), every write stays inside the
+ * caller's buffers, and the context stays usable. Needs n > one tile.
+ */
+int pulse_debug_encode_orphan_tile(const float *master_f32, uint16_t *prev_bf16, uint64_t n,
+                                   uint32_t *idx_out, uint16_t *val_out, uint64_t *count_out,
+                                   uint64_t wait_limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PULSE_H */

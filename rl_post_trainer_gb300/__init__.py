@@ -1,0 +1,19 @@
+"""GB300-native compute-visible weight-delta sync (PULSESync-style encode/apply).
+
+The compute path is the CUDA library ``libpulse.so`` (C ABI in
+``include/pulse.h``); :mod:`.pulse` is its thin Python binding.
+"""
+from .pulse import (  # noqa: F401
+    Plan,
+    PulseError,
+    TensorSlot,
+    apply,
+    encode,
+    error_string,
+    get_error,
+    lib,
+    library_path,
+    tile_elems,
+    xor_apply,
+    xor_mask,
+)

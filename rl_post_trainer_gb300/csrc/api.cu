@@ -1,0 +1,442 @@
+// api.cu -- the C ABI declared in include/pulse.h: argument checks, the
+// per-(device, stream) workspace of the single-tensor calls, and multi-tensor
+// plans (tile tables built once on the host and replayed every step, as in
+// the static schedule of "Weight transfer for RL post-training in under 2
+// seconds", section "Statyczny harmonogram", and the CPU-prepared tiling and
+// address map of the humansand.ai summary, section "Pipeline'i GPU'lara
+// tasimak").
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <utility>
+#include <vector>
+
+#include "pulse.h"
+#include "pulse_device.cuh"
+#include "pulse_internal.h"
+
+namespace pulse {
+
+int sm_count(int device) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(device);
+  if (it != cache.end()) return it->second;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms < 1)
+    sms = 1;
+  cache[device] = sms;
+  return sms;
+}
+
+namespace {
+
+constexpr uint64_t kMaxElems = 0xFFFFFFFFull;      // n < 2^32 (uint32 indices)
+constexpr uint64_t kMaxTiles = 0x7FFFFFFFull;      // tile tickets are uint32
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s per bounded wait
+constexpr size_t kCounterBytes = 256;               // ticket, finished, error (+ padding)
+constexpr int kMaxTensorsPerApplyLaunch = 16384;     // bound on the apply kernel's smem table
+
+uint64_t div_up(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PULSE_OK : PULSE_ERR_CUDA; }
+
+// Allocate (or grow) a workspace to hold `tiles` look-back words. Growing
+// synchronises `stream` so no running launch still uses the old arrays.
+int workspace_reserve(Workspace& ws, uint64_t tiles, cudaStream_t stream) {
+  if (ws.counters == nullptr) {
+    if (cudaMalloc(&ws.counters, kCounterBytes) != cudaSuccess) return PULSE_ERR_NOMEM;
+    if (cudaMemsetAsync(ws.counters, 0, kCounterBytes, stream) != cudaSuccess) return PULSE_ERR_CUDA;
+  }
+  if (tiles > ws.capacity_tiles) {
+    uint64_t cap = ws.capacity_tiles ? ws.capacity_tiles : 4096;
+    while (cap < tiles) cap *= 2;
+    if (ws.status != nullptr) {
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return PULSE_ERR_CUDA;
+      cudaFree(ws.status);
+      ws.status = nullptr;
+      ws.capacity_tiles = 0;
+    }
+    if (cudaMalloc(&ws.status, cap * sizeof(uint64_t)) != cudaSuccess) return PULSE_ERR_NOMEM;
+    if (cudaMemsetAsync(ws.status, 0, cap * sizeof(uint64_t), stream) != cudaSuccess)
+      return PULSE_ERR_CUDA;
+    ws.capacity_tiles = cap;
+  }
+  return PULSE_OK;
+}
+
+// Next launch epoch; when the 30-bit epoch wraps, clear the status words so
+// no stale word can match a reused epoch.
+int workspace_next_epoch(Workspace& ws, cudaStream_t stream, uint32_t* epoch) {
+  ws.epoch += 1;
+  if (ws.epoch > kEpochMask) {
+    if (cudaMemsetAsync(ws.status, 0, ws.capacity_tiles * sizeof(uint64_t), stream) != cudaSuccess)
+      return PULSE_ERR_CUDA;
+    ws.epoch = 1;
+  }
+  *epoch = ws.epoch;
+  return PULSE_OK;
+}
+
+void workspace_free(Workspace& ws) {
+  if (ws.status) cudaFree(ws.status);
+  if (ws.counters) cudaFree(ws.counters);
+  ws = Workspace{};
+}
+
+// Reads and clears the error word (caller has synchronised the stream).
+int workspace_take_error(Workspace& ws, cudaStream_t stream) {
+  if (ws.counters == nullptr) return PULSE_OK;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, ws.counters + 2, sizeof word, cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaMemsetAsync(ws.counters + 2, 0, sizeof(uint32_t), stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  if (word & kErrTimeout) return PULSE_ERR_TIMEOUT;
+  if (word & kErrIndex) return PULSE_ERR_INDEX;
+  return PULSE_OK;
+}
+
+// ---- per-(device, stream) workspaces of the single-tensor entry points
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, Workspace*> g_ws;
+
+Workspace* stream_workspace(int device, cudaStream_t stream) {
+  auto key = std::make_pair(device, reinterpret_cast<uintptr_t>(stream));
+  auto it = g_ws.find(key);
+  if (it != g_ws.end()) return it->second;
+  Workspace* ws = new (std::nothrow) Workspace();
+  if (ws == nullptr) return nullptr;
+  ws->device = device;
+  g_ws[key] = ws;
+  return ws;
+}
+
+TensorDesc make_desc(const pulse_tensor& t, uint64_t tile_begin) {
+  TensorDesc d{};
+  d.master = t.master;
+  d.prev = t.prev;
+  d.w = t.w;
+  d.idx = t.idx;
+  d.val = t.val;
+  d.mask = t.mask;
+  d.n = t.n;
+  d.tile_begin = tile_begin;
+  d.bulk_ok = (t.master && t.prev && aligned(t.master, 16) && aligned(t.prev, 16)) ? 1u : 0u;
+  d.vec_ok = 0;
+  if (t.master && t.prev && t.mask && aligned(t.master, 16) && aligned(t.prev, 8) &&
+      aligned(t.mask, 8))
+    d.vec_ok |= kVecMask;
+  if (t.w && t.mask && aligned(t.w, 8) && aligned(t.mask, 8)) d.vec_ok |= kVecApply;
+  return d;
+}
+
+int xor_grid(int device, uint64_t tiles) {
+  const uint64_t cap = uint64_t(sm_count(device)) * 8u;  // 8 x 256 threads per SM
+  return int(tiles < cap ? tiles : cap);
+}
+
+int encode_impl(const float* master, uint16_t* prev, uint64_t n, uint32_t* idx, uint16_t* val,
+                uint64_t* count_out, uint32_t first_ticket, uint64_t wait_ns,
+                cudaStream_t stream) {
+  if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (count_out == nullptr) return PULSE_ERR_INVALID;
+  if (n > 0 && (master == nullptr || prev == nullptr || idx == nullptr || val == nullptr))
+    return PULSE_ERR_INVALID;
+  if (n == 0) return cuda_status(cudaMemsetAsync(count_out, 0, sizeof(uint64_t), stream));
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  const uint64_t tiles = div_up(n, kEncTile);
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  Workspace* ws = stream_workspace(device, stream);
+  if (ws == nullptr) return PULSE_ERR_NOMEM;
+  int st = workspace_reserve(*ws, tiles, stream);
+  if (st != PULSE_OK) return st;
+  EncodeLaunch a{};
+  pulse_tensor t{};
+  t.master = master;
+  t.prev = prev;
+  t.n = n;
+  t.idx = idx;
+  t.val = val;
+  a.one = make_desc(t, 0);
+  a.tensors = nullptr;
+  a.tile_begin = nullptr;
+  a.ntensors = 1;
+  a.total_tiles = tiles;
+  a.status = ws->status;
+  a.counters = ws->counters;
+  a.counts_out = count_out;
+  a.first_ticket = first_ticket;
+  a.wait_limit_ns = wait_ns;
+  st = workspace_next_epoch(*ws, stream, &a.epoch);
+  if (st != PULSE_OK) return st;
+  const uint64_t cap = uint64_t(encode_grid_size(device));
+  const int grid = int(tiles < cap ? tiles : cap);
+  return cuda_status(launch_encode(a, false, grid, stream));
+}
+
+}  // namespace
+}  // namespace pulse
+
+using namespace pulse;
+
+// ------------------------------------------------------------------ plans
+
+struct pulse_plan {
+  int device = 0;
+  int ntensors = 0;
+  uint64_t total_tiles = 0;
+  bool can_encode = false, can_apply = false, can_xor_mask = false, can_xor_apply = false;
+  std::vector<TensorDesc> host_desc;
+  TensorDesc* desc = nullptr;       // device copy
+  uint64_t* tile_begin = nullptr;   // device, ntensors + 1
+  uint64_t* counts = nullptr;       // device, ntensors (host-count apply staging)
+  Workspace ws;
+};
+
+extern "C" {
+
+const char* pulse_error_string(int status) {
+  switch (status) {
+    case PULSE_OK: return "PULSE_OK";
+    case PULSE_ERR_INVALID: return "PULSE_ERR_INVALID: invalid argument";
+    case PULSE_ERR_RANGE: return "PULSE_ERR_RANGE: element count must be below 2^32";
+    case PULSE_ERR_CUDA: return "PULSE_ERR_CUDA: CUDA runtime call or launch failed";
+    case PULSE_ERR_TIMEOUT: return "PULSE_ERR_TIMEOUT: a bounded device wait gave up";
+    case PULSE_ERR_INDEX: return "PULSE_ERR_INDEX: patch index out of range (entry skipped)";
+    case PULSE_ERR_NOMEM: return "PULSE_ERR_NOMEM: workspace allocation failed";
+    default: return "PULSE_ERR_UNKNOWN";
+  }
+}
+
+uint32_t pulse_encode_tile_elems(void) { return uint32_t(kEncTile); }
+
+int pulse_encode(const float* master_f32, uint16_t* prev_bf16, uint64_t n, uint32_t* idx_out,
+                 uint16_t* val_out, uint64_t* count_out, cudaStream_t stream) {
+  return encode_impl(master_f32, prev_bf16, n, idx_out, val_out, count_out, 0u, kDefaultWaitNs,
+                     stream);
+}
+
+int pulse_debug_encode_orphan_tile(const float* master_f32, uint16_t* prev_bf16, uint64_t n,
+                                   uint32_t* idx_out, uint16_t* val_out, uint64_t* count_out,
+                                   uint64_t wait_limit_ns, cudaStream_t stream) {
+  if (n <= uint64_t(kEncTile)) return PULSE_ERR_INVALID;
+  return encode_impl(master_f32, prev_bf16, n, idx_out, val_out, count_out, 1u, wait_limit_ns,
+                     stream);
+}
+
+int pulse_apply(uint16_t* w_bf16, const uint32_t* idx, const uint16_t* val, uint64_t count,
+                cudaStream_t stream) {
+  if (count == 0) return PULSE_OK;
+  if (w_bf16 == nullptr || idx == nullptr || val == nullptr) return PULSE_ERR_INVALID;
+  return cuda_status(launch_apply(w_bf16, 0, false, idx, val, count, nullptr, stream));
+}
+
+int pulse_apply_checked(uint16_t* w_bf16, uint64_t n, const uint32_t* idx, const uint16_t* val,
+                        uint64_t count, cudaStream_t stream) {
+  if (count == 0) return PULSE_OK;
+  if (w_bf16 == nullptr || idx == nullptr || val == nullptr) return PULSE_ERR_INVALID;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  uint32_t* err = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    Workspace* ws = stream_workspace(device, stream);
+    if (ws == nullptr) return PULSE_ERR_NOMEM;
+    const int st = workspace_reserve(*ws, 0, stream);
+    if (st != PULSE_OK) return st;
+    err = ws->counters + 2;
+  }
+  return cuda_status(launch_apply(w_bf16, n, true, idx, val, count, err, stream));
+}
+
+int pulse_xor_mask(const float* master_f32, uint16_t* prev_bf16, uint64_t n, uint16_t* mask_out,
+                   cudaStream_t stream) {
+  if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (n == 0) return PULSE_OK;
+  if (master_f32 == nullptr || prev_bf16 == nullptr || mask_out == nullptr) return PULSE_ERR_INVALID;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  pulse_tensor t{};
+  t.master = master_f32;
+  t.prev = prev_bf16;
+  t.mask = mask_out;
+  t.n = n;
+  const TensorDesc d = make_desc(t, 0);
+  const uint64_t tiles = div_up(n, kXorTile);
+  return cuda_status(launch_xor_mask(d, nullptr, nullptr, 1, tiles, false, xor_grid(device, tiles), stream));
+}
+
+int pulse_xor_apply(uint16_t* w_bf16, const uint16_t* mask, uint64_t n, cudaStream_t stream) {
+  if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (n == 0) return PULSE_OK;
+  if (w_bf16 == nullptr || mask == nullptr) return PULSE_ERR_INVALID;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  pulse_tensor t{};
+  t.w = w_bf16;
+  t.mask = const_cast<uint16_t*>(mask);
+  t.n = n;
+  const TensorDesc d = make_desc(t, 0);
+  const uint64_t tiles = div_up(n, kXorTile);
+  return cuda_status(launch_xor_apply(d, nullptr, nullptr, 1, tiles, false, xor_grid(device, tiles), stream));
+}
+
+int pulse_get_error(cudaStream_t stream) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PULSE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  auto it = g_ws.find(std::make_pair(device, reinterpret_cast<uintptr_t>(stream)));
+  if (it == g_ws.end()) return PULSE_OK;
+  return workspace_take_error(*it->second, stream);
+}
+
+int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** plan_out) {
+  if (plan_out == nullptr) return PULSE_ERR_INVALID;
+  *plan_out = nullptr;
+  if (tensors == nullptr || ntensors < 1) return PULSE_ERR_INVALID;
+  pulse_plan* p = new (std::nothrow) pulse_plan();
+  if (p == nullptr) return PULSE_ERR_NOMEM;
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return PULSE_ERR_CUDA;
+  }
+  p->ntensors = ntensors;
+  p->can_encode = p->can_apply = p->can_xor_mask = p->can_xor_apply = true;
+  std::vector<uint64_t> tb(size_t(ntensors) + 1, 0);
+  p->host_desc.reserve(size_t(ntensors));
+  uint64_t tiles = 0;
+  for (int i = 0; i < ntensors; ++i) {
+    const pulse_tensor& t = tensors[i];
+    if (t.n >= kMaxElems + 1) {
+      delete p;
+      return PULSE_ERR_RANGE;
+    }
+    tb[size_t(i)] = tiles;
+    p->host_desc.push_back(make_desc(t, tiles));
+    tiles += div_up(t.n, kEncTile);
+    if (t.n > 0) {
+      p->can_encode = p->can_encode && t.master && t.prev && t.idx && t.val;
+      p->can_apply = p->can_apply && t.w && t.idx && t.val;
+      p->can_xor_mask = p->can_xor_mask && t.master && t.prev && t.mask;
+      p->can_xor_apply = p->can_xor_apply && t.w && t.mask;
+    }
+  }
+  tb[size_t(ntensors)] = tiles;
+  if (tiles > kMaxTiles) {
+    delete p;
+    return PULSE_ERR_RANGE;
+  }
+  p->total_tiles = tiles;
+  const size_t desc_bytes = sizeof(TensorDesc) * size_t(ntensors);
+  const size_t tb_bytes = sizeof(uint64_t) * (size_t(ntensors) + 1);
+  int st = PULSE_OK;
+  if (cudaMalloc(&p->desc, desc_bytes) != cudaSuccess ||
+      cudaMalloc(&p->tile_begin, tb_bytes) != cudaSuccess ||
+      cudaMalloc(&p->counts, sizeof(uint64_t) * size_t(ntensors)) != cudaSuccess) {
+    st = PULSE_ERR_NOMEM;
+  } else if (cudaMemcpy(p->desc, p->host_desc.data(), desc_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+             cudaMemcpy(p->tile_begin, tb.data(), tb_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+             cudaMemset(p->counts, 0, sizeof(uint64_t) * size_t(ntensors)) != cudaSuccess) {
+    st = PULSE_ERR_CUDA;
+  } else {
+    st = workspace_reserve(p->ws, tiles, nullptr);
+    if (st == PULSE_OK && cudaDeviceSynchronize() != cudaSuccess) st = PULSE_ERR_CUDA;
+  }
+  if (st != PULSE_OK) {
+    pulse_plan_destroy(p);
+    return st;
+  }
+  *plan_out = p;
+  return PULSE_OK;
+}
+
+int pulse_plan_destroy(pulse_plan* plan) {
+  if (plan == nullptr) return PULSE_OK;
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (plan->desc) cudaFree(plan->desc);
+  if (plan->tile_begin) cudaFree(plan->tile_begin);
+  if (plan->counts) cudaFree(plan->counts);
+  workspace_free(plan->ws);
+  delete plan;
+  return cuda_status(e);
+}
+
+int pulse_plan_num_tensors(const pulse_plan* plan) { return plan ? plan->ntensors : 0; }
+
+uint64_t pulse_plan_num_tiles(const pulse_plan* plan) { return plan ? plan->total_tiles : 0; }
+
+int pulse_encode_multi(pulse_plan* plan, uint64_t* counts_out, cudaStream_t stream) {
+  if (plan == nullptr || counts_out == nullptr || !plan->can_encode) return PULSE_ERR_INVALID;
+  if (plan->total_tiles == 0)
+    return cuda_status(cudaMemsetAsync(counts_out, 0, sizeof(uint64_t) * size_t(plan->ntensors), stream));
+  EncodeLaunch a{};
+  a.tensors = plan->desc;
+  a.tile_begin = plan->tile_begin;
+  a.ntensors = plan->ntensors;
+  a.total_tiles = plan->total_tiles;
+  a.status = plan->ws.status;
+  a.counters = plan->ws.counters;
+  a.counts_out = counts_out;
+  a.first_ticket = 0;
+  a.wait_limit_ns = kDefaultWaitNs;
+  const int st = workspace_next_epoch(plan->ws, stream, &a.epoch);
+  if (st != PULSE_OK) return st;
+  const uint64_t cap = uint64_t(encode_grid_size(plan->device));
+  const int grid = int(plan->total_tiles < cap ? plan->total_tiles : cap);
+  return cuda_status(launch_encode(a, true, grid, stream));
+}
+
+int pulse_apply_multi_device(pulse_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {
+  if (plan == nullptr || counts_dev == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
+  const int grid = sm_count(plan->device) * 8;
+  for (int t0 = 0; t0 < plan->ntensors; t0 += kMaxTensorsPerApplyLaunch) {
+    const int nt = plan->ntensors - t0 < kMaxTensorsPerApplyLaunch ? plan->ntensors - t0
+                                                                   : kMaxTensorsPerApplyLaunch;
+    const cudaError_t e = launch_apply_multi(plan->desc + t0, nt, counts_dev + t0,
+                                             plan->ws.counters + 2, grid, stream);
+    if (e != cudaSuccess) return PULSE_ERR_CUDA;
+  }
+  return PULSE_OK;
+}
+
+int pulse_apply_multi(pulse_plan* plan, const uint64_t* counts_host, cudaStream_t stream) {
+  if (plan == nullptr || counts_host == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
+  // From pageable memory the copy is staged before this call returns, so the
+  // caller may reuse counts_host at once.
+  if (cudaMemcpyAsync(plan->counts, counts_host, sizeof(uint64_t) * size_t(plan->ntensors),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  return pulse_apply_multi_device(plan, plan->counts, stream);
+}
+
+int pulse_xor_mask_multi(pulse_plan* plan, cudaStream_t stream) {
+  if (plan == nullptr || !plan->can_xor_mask) return PULSE_ERR_INVALID;
+  if (plan->total_tiles == 0) return PULSE_OK;
+  return cuda_status(launch_xor_mask(plan->host_desc[0], plan->desc, plan->tile_begin,
+                                     plan->ntensors, plan->total_tiles, true,
+                                     xor_grid(plan->device, plan->total_tiles), stream));
+}
+
+int pulse_xor_apply_multi(pulse_plan* plan, cudaStream_t stream) {
+  if (plan == nullptr || !plan->can_xor_apply) return PULSE_ERR_INVALID;
+  if (plan->total_tiles == 0) return PULSE_OK;
+  return cuda_status(launch_xor_apply(plan->host_desc[0], plan->desc, plan->tile_begin,
+                                      plan->ntensors, plan->total_tiles, true,
+                                      xor_grid(plan->device, plan->total_tiles), stream));
+}
+
+int pulse_plan_get_error(pulse_plan* plan) {
+  if (plan == nullptr) return PULSE_ERR_INVALID;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PULSE_ERR_CUDA;
+  return workspace_take_error(plan->ws, nullptr);
+}
+
+}  // extern "C"

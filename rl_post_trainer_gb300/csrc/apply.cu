@@ -1,0 +1,161 @@
+// apply.cu -- sampler-side patch apply: w[idx[j]] = val[j].
+//
+// "Taking Reinforcement Learning Cross Datacenter", talk 11:08-11:30
+// (selective overrides reconstruct the served version bitwise) and the PULSE
+// summary, section "Metodologia: PULSE -- 1. PULSESync" (the sampler applies
+// the sparse patch of absolute values directly to its BF16 weights).
+//
+// The patch is read once as a stream (128-bit index loads, 64-bit value
+// loads, evict-first) and scattered with 2-byte stores; an encode patch is in
+// ascending index order, so one warp's stores land in a narrow window of w
+// and L2 merges them into whole sectors before they reach HBM.
+#include "pulse_device.cuh"
+#include "pulse_internal.h"
+
+namespace pulse {
+namespace {
+
+constexpr int kGroups = kApplyPerThread / 4;  // 4-entry groups per thread per tile
+
+template <bool CHECKED>
+__device__ __forceinline__ void scatter1(uint16_t* w, uint64_t n, uint32_t i, uint16_t v,
+                                         uint32_t* err) {
+  if (CHECKED && uint64_t(i) >= n) {
+    record_error(err, kErrIndex);
+    return;
+  }
+  w[i] = v;
+}
+
+// Apply entries [0, count) of one segment, tile `tile` of kApplyTile entries.
+template <bool CHECKED>
+__device__ __forceinline__ void apply_tile(uint16_t* w, uint64_t n, const uint32_t* idx,
+                                           const uint16_t* val, uint64_t count, uint64_t tile,
+                                           bool vec, uint32_t* err) {
+  const int tid = threadIdx.x;
+  const uint64_t base = tile * kApplyTile;
+  if (vec && base + kApplyTile <= count) {
+    uint4 iv[kGroups];
+    uint2 vv[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      const uint64_t off = base + uint64_t(g * kApplyThreads + tid) * 4u;
+      iv[g] = ld_stream_u4_ro(idx + off);
+      vv[g] = ld_stream_u2_ro(val + off);
+    }
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      scatter1<CHECKED>(w, n, iv[g].x, uint16_t(vv[g].x & 0xFFFFu), err);
+      scatter1<CHECKED>(w, n, iv[g].y, uint16_t(vv[g].x >> 16), err);
+      scatter1<CHECKED>(w, n, iv[g].z, uint16_t(vv[g].y & 0xFFFFu), err);
+      scatter1<CHECKED>(w, n, iv[g].w, uint16_t(vv[g].y >> 16), err);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kApplyPerThread; ++k) {
+      const uint64_t j = base + uint64_t(k) * kApplyThreads + tid;
+      if (j < count) scatter1<CHECKED>(w, n, idx[j], val[j], err);
+    }
+  }
+}
+
+template <bool CHECKED>
+__global__ void __launch_bounds__(kApplyThreads)
+    apply_kernel(uint16_t* w, uint64_t n, const uint32_t* idx, const uint16_t* val,
+                 uint64_t count, uint32_t* err) {
+  const uint64_t ntiles = (count + kApplyTile - 1) / kApplyTile;
+  const bool vec = (reinterpret_cast<uintptr_t>(idx) % 16u == 0) &&
+                   (reinterpret_cast<uintptr_t>(val) % 8u == 0);
+  for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x)
+    apply_tile<CHECKED>(w, n, idx, val, count, t, vec, err);
+}
+
+// Whole-model apply: the segment lengths live in device memory, so the tile
+// map (tiles per tensor, prefix over the tensor list) is rebuilt by every CTA
+// in shared memory at the start of the launch.
+__global__ void __launch_bounds__(kApplyThreads)
+    apply_multi_kernel(const TensorDesc* tensors, int ntensors, const uint64_t* counts,
+                       uint32_t* err) {
+  extern __shared__ uint64_t tile_begin[];  // ntensors + 1
+  __shared__ uint64_t warp_tot[kApplyThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (ntensors + kApplyThreads - 1) / kApplyThreads;
+  const int t0 = tid * per;
+  uint64_t mine = 0;
+  for (int t = t0; t < t0 + per && t < ntensors; ++t) {
+    uint64_t c = counts[t];
+    if (c > tensors[t].n) c = tensors[t].n;  // a segment never exceeds its tensor
+    mine += (c + kApplyTile - 1) / kApplyTile;
+  }
+  uint64_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  uint64_t warp_off = 0;
+  for (int k = 0; k < warp; ++k) warp_off += warp_tot[k];
+  uint64_t run = warp_off + incl - mine;
+  for (int t = t0; t < t0 + per && t < ntensors; ++t) {
+    tile_begin[t] = run;
+    uint64_t c = counts[t];
+    if (c > tensors[t].n) c = tensors[t].n;
+    run += (c + kApplyTile - 1) / kApplyTile;
+  }
+  if (tid == kApplyThreads - 1) tile_begin[ntensors] = warp_off + incl;
+  __syncthreads();
+  if (tid == 0) {
+    for (int t = 0; t < ntensors; ++t)
+      if (counts[t] > tensors[t].n) record_error(err, kErrIndex);
+  }
+
+  const uint64_t total = tile_begin[ntensors];
+  for (uint64_t g = blockIdx.x; g < total; g += gridDim.x) {
+    int lo = 0, hi = ntensors;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_begin[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    const TensorDesc& d = tensors[lo];
+    uint64_t c = counts[lo];
+    if (c > d.n) c = d.n;
+    const bool vec = (reinterpret_cast<uintptr_t>(d.idx) % 16u == 0) &&
+                     (reinterpret_cast<uintptr_t>(d.val) % 8u == 0);
+    apply_tile<true>(d.w, d.n, d.idx, d.val, c, g - tile_begin[lo], vec, err);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_apply(uint16_t* w, uint64_t n, bool checked, const uint32_t* idx,
+                         const uint16_t* val, uint64_t count, uint32_t* error_word,
+                         cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t ntiles = (count + kApplyTile - 1) / kApplyTile;
+  const uint64_t cap = uint64_t(sm_count(dev)) * 8u;
+  const int grid = int(ntiles < cap ? ntiles : cap);
+  if (grid == 0) return cudaSuccess;
+  if (checked)
+    apply_kernel<true><<<grid, kApplyThreads, 0, stream>>>(w, n, idx, val, count, error_word);
+  else
+    apply_kernel<false><<<grid, kApplyThreads, 0, stream>>>(w, n, idx, val, count, error_word);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply_multi(const TensorDesc* tensors, int ntensors, const uint64_t* counts_dev,
+                               uint32_t* error_word, int grid, cudaStream_t stream) {
+  const size_t smem = size_t(ntensors + 1) * sizeof(uint64_t);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(apply_multi_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+  }
+  apply_multi_kernel<<<grid, kApplyThreads, smem, stream>>>(tensors, ntensors, counts_dev,
+                                                           error_word);
+  return cudaGetLastError();
+}
+
+}  // namespace pulse

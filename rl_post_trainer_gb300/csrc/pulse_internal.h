@@ -1,0 +1,86 @@
+// pulse_internal.h -- descriptors and launchers shared by the library's
+// translation units (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pulse {
+
+// ---------------------------------------------------------------- encode
+// Tile geometry: kEncThreads threads x kEncRounds rounds x 4 elements.
+constexpr int kEncThreads = 256;
+constexpr int kEncRounds = 4;
+constexpr int kEncTile = kEncThreads * kEncRounds * 4;  // 4096 elements
+constexpr int kEncStages = 3;                             // bulk-copy ring depth
+
+// Device view of one tensor for the encode / XOR-mask / apply kernels.
+struct TensorDesc {
+  const float* master;
+  uint16_t* prev;
+  uint16_t* w;
+  uint32_t* idx;
+  uint16_t* val;
+  uint16_t* mask;
+  uint64_t n;
+  uint64_t tile_begin;  // first global encode tile of this tensor
+  uint32_t bulk_ok;     // master and prev 16-byte aligned: encode may bulk-copy tiles
+  uint32_t vec_ok;      // kVecMask | kVecApply bits: XOR kernels may use vector accesses
+};
+constexpr uint32_t kVecMask = 2u;   // master 16-byte, prev and mask 8-byte aligned
+constexpr uint32_t kVecApply = 4u;  // w and mask 8-byte aligned
+
+// Library-owned scratch of one launch context (a stream, or a plan).
+struct Workspace {
+  uint64_t* status = nullptr;    // one look-back word per tile
+  uint32_t* counters = nullptr;  // [0] tile ticket, [1] CTAs finished, [2] error word
+  uint64_t capacity_tiles = 0;
+  uint32_t epoch = 0;            // host-side launch counter (30 bits used)
+  int device = -1;
+};
+
+struct EncodeLaunch {
+  TensorDesc one;                // single-tensor mode
+  const TensorDesc* tensors;     // multi-tensor mode: device array
+  const uint64_t* tile_begin;    // multi-tensor mode: ntensors + 1 entries (device)
+  int ntensors;                  // 1 in single-tensor mode
+  uint64_t total_tiles;
+  uint64_t* status;
+  uint32_t* counters;
+  uint64_t* counts_out;          // ntensors device uint64
+  uint32_t epoch;
+  uint32_t first_ticket;         // 0, or 1 for the watchdog test hook
+  uint64_t wait_limit_ns;
+};
+
+int encode_grid_size(int device);
+cudaError_t launch_encode(const EncodeLaunch& a, bool multi, int grid, cudaStream_t stream);
+
+// ---------------------------------------------------------------- apply
+constexpr int kApplyThreads = 256;
+constexpr int kApplyPerThread = 8;                          // entries per thread per tile
+constexpr int kApplyTile = kApplyThreads * kApplyPerThread;  // 2048 entries
+
+cudaError_t launch_apply(uint16_t* w, uint64_t n, bool checked, const uint32_t* idx,
+                         const uint16_t* val, uint64_t count, uint32_t* error_word,
+                         cudaStream_t stream);
+cudaError_t launch_apply_multi(const TensorDesc* tensors, int ntensors,
+                               const uint64_t* counts_dev, uint32_t* error_word,
+                               int grid, cudaStream_t stream);
+
+// ---------------------------------------------------------------- XOR
+constexpr int kXorThreads = 256;
+constexpr int kXorRounds = 4;
+constexpr int kXorTile = kXorThreads * kXorRounds * 4;  // 4096 elements (== kEncTile)
+static_assert(kXorTile == kEncTile, "XOR kernels reuse the encode tile table");
+
+cudaError_t launch_xor_mask(const TensorDesc& one, const TensorDesc* tensors,
+                            const uint64_t* tile_begin, int ntensors, uint64_t total_tiles,
+                            bool multi, int grid, cudaStream_t stream);
+cudaError_t launch_xor_apply(const TensorDesc& one, const TensorDesc* tensors,
+                             const uint64_t* tile_begin, int ntensors, uint64_t total_tiles,
+                             bool multi, int grid, cudaStream_t stream);
+
+int sm_count(int device);
+
+}  // namespace pulse

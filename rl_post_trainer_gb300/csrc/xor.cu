@@ -1,0 +1,151 @@
+// xor.cu -- dense XOR-mask encode and in-place XOR apply.
+//
+// humansand.ai summary "GPU agirlik isinlanmasi RL sampler'larini 4
+// saniyenin altinda ...", section "XOR maskeleri ile delta
+// senkronizasyonu": the trainer XORs its pre-step and post-step weights into
+// a mask the size of the weights (1-bits mark changed bits); a sampler that
+// holds the old weights XORs the mask in and holds exactly the new weights.
+// Section "Pipeline'i GPU'lara tasimak": one launch covers the whole model,
+// from a tile/address map prepared on the host.
+//
+// Both kernels stream their inputs once with 128/64-bit coalesced loads,
+// issuing every load of a tile before any arithmetic. xor_mask writes the
+// mask with streaming stores and writes prev back only in 8-byte groups that
+// changed; xor_apply reads w only where the mask is non-zero, so at low
+// density it moves little more than the mask itself.
+#include "pulse_device.cuh"
+#include "pulse_internal.h"
+
+namespace pulse {
+namespace {
+
+__device__ __forceinline__ int find_tensor_x(const uint64_t* tile_begin, int ntensors,
+                                             uint64_t g) {
+  int lo = 0, hi = ntensors;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(tile_begin + mid) <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint32_t pack_pair(uint32_t lo, uint32_t hi) { return lo | (hi << 16); }
+
+template <bool MULTI>
+__global__ void __launch_bounds__(kXorThreads)
+    xor_mask_kernel(const __grid_constant__ TensorDesc one, const TensorDesc* tensors,
+                    const uint64_t* tile_begin, int ntensors, uint64_t total_tiles) {
+  const int tid = threadIdx.x;
+  for (uint64_t g = blockIdx.x; g < total_tiles; g += gridDim.x) {
+    const TensorDesc& d = MULTI ? tensors[find_tensor_x(tile_begin, ntensors, g)] : one;
+    const uint64_t base = (g - d.tile_begin) * kXorTile;
+    const uint64_t rem = d.n - base;
+    const uint32_t len = uint32_t(rem < uint64_t(kXorTile) ? rem : uint64_t(kXorTile));
+    if ((d.vec_ok & kVecMask) && len == uint32_t(kXorTile)) {
+      uint4 mv[kXorRounds];
+      uint2 pv[kXorRounds];
+#pragma unroll
+      for (int j = 0; j < kXorRounds; ++j) {
+        const uint64_t off = base + uint64_t(j * kXorThreads + tid) * 4u;
+        mv[j] = ld_stream_u4_ro(d.master + off);
+        pv[j] = ld_u2_no_l1(d.prev + off);
+      }
+#pragma unroll
+      for (int j = 0; j < kXorRounds; ++j) {
+        const uint64_t off = base + uint64_t(j * kXorThreads + tid) * 4u;
+        const uint32_t b0 = bf16_rne_bits(mv[j].x), b1 = bf16_rne_bits(mv[j].y);
+        const uint32_t b2 = bf16_rne_bits(mv[j].z), b3 = bf16_rne_bits(mv[j].w);
+        const uint2 nb = make_uint2(pack_pair(b0, b1), pack_pair(b2, b3));
+        const uint2 mk = make_uint2(nb.x ^ pv[j].x, nb.y ^ pv[j].y);
+        __stcs(reinterpret_cast<uint2*>(d.mask + off), mk);
+        if ((mk.x | mk.y) != 0u) *reinterpret_cast<uint2*>(d.prev + off) = nb;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kXorRounds; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t li = uint32_t(j * kXorThreads + tid) * 4u + uint32_t(e);
+          if (li < len) {
+            const uint32_t b = bf16_rne_bits(__float_as_uint(d.master[base + li]));
+            const uint32_t p = d.prev[base + li];
+            d.mask[base + li] = uint16_t(b ^ p);
+            if (b != p) d.prev[base + li] = uint16_t(b);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <bool MULTI>
+__global__ void __launch_bounds__(kXorThreads)
+    xor_apply_kernel(const __grid_constant__ TensorDesc one, const TensorDesc* tensors,
+                     const uint64_t* tile_begin, int ntensors, uint64_t total_tiles) {
+  const int tid = threadIdx.x;
+  for (uint64_t g = blockIdx.x; g < total_tiles; g += gridDim.x) {
+    const TensorDesc& d = MULTI ? tensors[find_tensor_x(tile_begin, ntensors, g)] : one;
+    const uint64_t base = (g - d.tile_begin) * kXorTile;
+    const uint64_t rem = d.n - base;
+    const uint32_t len = uint32_t(rem < uint64_t(kXorTile) ? rem : uint64_t(kXorTile));
+    if ((d.vec_ok & kVecApply) && len == uint32_t(kXorTile)) {
+      uint2 mk[kXorRounds];
+#pragma unroll
+      for (int j = 0; j < kXorRounds; ++j)
+        mk[j] = ld_stream_u2_ro(d.mask + base + uint64_t(j * kXorThreads + tid) * 4u);
+      uint2 wv[kXorRounds] = {};
+#pragma unroll
+      for (int j = 0; j < kXorRounds; ++j) {
+        if ((mk[j].x | mk[j].y) != 0u)
+          wv[j] = ld_u2_no_l1(d.w + base + uint64_t(j * kXorThreads + tid) * 4u);
+      }
+#pragma unroll
+      for (int j = 0; j < kXorRounds; ++j) {
+        if ((mk[j].x | mk[j].y) != 0u) {
+          *reinterpret_cast<uint2*>(d.w + base + uint64_t(j * kXorThreads + tid) * 4u) =
+              make_uint2(wv[j].x ^ mk[j].x, wv[j].y ^ mk[j].y);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kXorRounds; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t li = uint32_t(j * kXorThreads + tid) * 4u + uint32_t(e);
+          if (li < len) {
+            const uint16_t m = d.mask[base + li];
+            if (m != 0) d.w[base + li] = uint16_t(d.w[base + li] ^ m);
+          }
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_xor_mask(const TensorDesc& one, const TensorDesc* tensors,
+                            const uint64_t* tile_begin, int ntensors, uint64_t total_tiles,
+                            bool multi, int grid, cudaStream_t stream) {
+  if (multi)
+    xor_mask_kernel<true><<<grid, kXorThreads, 0, stream>>>(one, tensors, tile_begin, ntensors,
+                                                            total_tiles);
+  else
+    xor_mask_kernel<false><<<grid, kXorThreads, 0, stream>>>(one, tensors, tile_begin, ntensors,
+                                                             total_tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_xor_apply(const TensorDesc& one, const TensorDesc* tensors,
+                             const uint64_t* tile_begin, int ntensors, uint64_t total_tiles,
+                             bool multi, int grid, cudaStream_t stream) {
+  if (multi)
+    xor_apply_kernel<true><<<grid, kXorThreads, 0, stream>>>(one, tensors, tile_begin, ntensors,
+                                                             total_tiles);
+  else
+    xor_apply_kernel<false><<<grid, kXorThreads, 0, stream>>>(one, tensors, tile_begin, ntensors,
+                                                              total_tiles);
+  return cudaGetLastError();
+}
+
+}  // namespace pulse

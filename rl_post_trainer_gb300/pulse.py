@@ -1,0 +1,322 @@
+"""Python binding of libpulse (include/pulse.h): argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; this module only
+checks tensor types, allocates outputs with torch, and passes raw device
+pointers plus torch's current CUDA stream through ctypes. There is no CPU
+fallback: if the library is not built, every call raises.
+
+Dtypes: FP32 master weights are ``torch.float32``; BF16 views, patch values
+and masks may be ``torch.bfloat16``, ``torch.int16`` or ``torch.uint16``
+(their bit patterns are used); patch indices are ``torch.int32`` holding
+uint32 values; counts are ``torch.int64`` holding uint64 values.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import _build
+
+PULSE_OK = 0
+PULSE_ERR_INVALID = 1
+PULSE_ERR_RANGE = 2
+PULSE_ERR_CUDA = 3
+PULSE_ERR_TIMEOUT = 4
+PULSE_ERR_INDEX = 5
+PULSE_ERR_NOMEM = 6
+
+_U16 = (torch.bfloat16, torch.int16, torch.uint16)
+_lib = None
+
+
+class PulseError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {error_string(status)}")
+
+
+class PulseTensor(ctypes.Structure):
+    _fields_ = [
+        ("master", ctypes.c_void_p),
+        ("prev", ctypes.c_void_p),
+        ("w", ctypes.c_void_p),
+        ("n", ctypes.c_uint64),
+        ("idx", ctypes.c_void_p),
+        ("val", ctypes.c_void_p),
+        ("mask", ctypes.c_void_p),
+    ]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libpulse.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(path)
+        P, U64, I = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int
+        sigs = {
+            "pulse_error_string": ([I], ctypes.c_char_p),
+            "pulse_encode_tile_elems": ([], ctypes.c_uint32),
+            "pulse_encode": ([P, P, U64, P, P, P, P], I),
+            "pulse_apply": ([P, P, P, U64, P], I),
+            "pulse_apply_checked": ([P, U64, P, P, U64, P], I),
+            "pulse_xor_mask": ([P, P, U64, P, P], I),
+            "pulse_xor_apply": ([P, P, U64, P], I),
+            "pulse_get_error": ([P], I),
+            "pulse_plan_create": ([ctypes.POINTER(PulseTensor), I, ctypes.POINTER(P)], I),
+            "pulse_plan_destroy": ([P], I),
+            "pulse_plan_num_tensors": ([P], I),
+            "pulse_plan_num_tiles": ([P], U64),
+            "pulse_encode_multi": ([P, P, P], I),
+            "pulse_apply_multi": ([P, P, P], I),
+            "pulse_apply_multi_device": ([P, P, P], I),
+            "pulse_xor_mask_multi": ([P, P], I),
+            "pulse_xor_apply_multi": ([P, P], I),
+            "pulse_plan_get_error": ([P], I),
+            "pulse_debug_encode_orphan_tile": ([P, P, U64, P, P, P, U64, P], I),
+        }
+        for name, (args, res) in sigs.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def error_string(status: int) -> str:
+    return lib().pulse_error_string(int(status)).decode()
+
+
+def _raise(status: int, where: str):
+    if status != PULSE_OK:
+        raise PulseError(status, where)
+
+
+def tile_elems() -> int:
+    return int(lib().pulse_encode_tile_elems())
+
+
+def _stream(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtypes, device=None, numel=None, min_numel=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_cuda:
+        raise TypeError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise TypeError(f"{name}: must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name}: {t.numel()} elements, need at least {min_numel}")
+
+
+# ------------------------------------------------------------ single tensor
+
+def encode(master: torch.Tensor, prev: torch.Tensor, idx_out: Optional[torch.Tensor] = None,
+           val_out: Optional[torch.Tensor] = None, count_out: Optional[torch.Tensor] = None):
+    """pulse_encode: returns (idx, val, count); refreshes ``prev`` in place.
+
+    ``idx``/``val`` have room for n entries; the patch is their first
+    ``count`` entries (``count`` is a 1-element device int64 tensor).
+    """
+    _need(master, "master", (torch.float32,))
+    dev = master.device
+    n = master.numel()
+    _need(prev, "prev", _U16, dev, n)
+    if idx_out is None:
+        idx_out = torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+    if val_out is None:
+        val_out = torch.empty(max(n, 1), dtype=torch.int16, device=dev)
+    if count_out is None:
+        count_out = torch.empty(1, dtype=torch.int64, device=dev)
+    _need(idx_out, "idx_out", (torch.int32, torch.uint32), dev, min_numel=n)
+    _need(val_out, "val_out", _U16, dev, min_numel=n)
+    _need(count_out, "count_out", (torch.int64, torch.uint64), dev, min_numel=1)
+    with torch.cuda.device(dev):
+        st = lib().pulse_encode(_ptr(master), _ptr(prev), n, _ptr(idx_out), _ptr(val_out),
+                                _ptr(count_out), _stream(dev))
+    _raise(st, "pulse_encode")
+    return idx_out, val_out, count_out
+
+
+def apply(w: torch.Tensor, idx: torch.Tensor, val: torch.Tensor, count: int, checked: bool = False):
+    """pulse_apply / pulse_apply_checked: w[idx[j]] = val[j] for j < count."""
+    _need(w, "w", _U16)
+    dev = w.device
+    count = int(count)
+    _need(idx, "idx", (torch.int32, torch.uint32), dev, min_numel=count)
+    _need(val, "val", _U16, dev, min_numel=count)
+    with torch.cuda.device(dev):
+        if checked:
+            st = lib().pulse_apply_checked(_ptr(w), w.numel(), _ptr(idx), _ptr(val), count, _stream(dev))
+        else:
+            st = lib().pulse_apply(_ptr(w), _ptr(idx), _ptr(val), count, _stream(dev))
+    _raise(st, "pulse_apply")
+    return w
+
+
+def xor_mask(master: torch.Tensor, prev: torch.Tensor, mask_out: Optional[torch.Tensor] = None):
+    """pulse_xor_mask: returns the mask; refreshes ``prev`` in place."""
+    _need(master, "master", (torch.float32,))
+    dev = master.device
+    n = master.numel()
+    _need(prev, "prev", _U16, dev, n)
+    if mask_out is None:
+        mask_out = torch.empty(n, dtype=torch.int16, device=dev)
+    _need(mask_out, "mask_out", _U16, dev, n)
+    with torch.cuda.device(dev):
+        st = lib().pulse_xor_mask(_ptr(master), _ptr(prev), n, _ptr(mask_out), _stream(dev))
+    _raise(st, "pulse_xor_mask")
+    return mask_out
+
+
+def xor_apply(w: torch.Tensor, mask: torch.Tensor):
+    """pulse_xor_apply: w ^= mask in place."""
+    _need(w, "w", _U16)
+    _need(mask, "mask", _U16, w.device, w.numel())
+    with torch.cuda.device(w.device):
+        st = lib().pulse_xor_apply(_ptr(w), _ptr(mask), w.numel(), _stream(w.device))
+    _raise(st, "pulse_xor_apply")
+    return w
+
+
+def get_error(device: Optional[torch.device] = None) -> int:
+    """pulse_get_error on torch's current stream: syncs it, returns and clears the code."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        return int(lib().pulse_get_error(_stream(dev)))
+
+
+def debug_encode_orphan_tile(master, prev, idx_out, val_out, count_out, wait_limit_ns: int) -> int:
+    """Test hook for the look-back watchdog (see include/pulse.h). Returns the status."""
+    dev = master.device
+    with torch.cuda.device(dev):
+        return int(lib().pulse_debug_encode_orphan_tile(
+            _ptr(master), _ptr(prev), master.numel(), _ptr(idx_out), _ptr(val_out),
+            _ptr(count_out), int(wait_limit_ns), _stream(dev)))
+
+
+# ------------------------------------------------------------- multi-tensor
+
+class TensorSlot:
+    """Buffers of one model tensor for a Plan (any field may be None)."""
+
+    def __init__(self, n: int, master=None, prev=None, w=None, idx=None, val=None, mask=None):
+        self.n = int(n)
+        self.master, self.prev, self.w = master, prev, w
+        self.idx, self.val, self.mask = idx, val, mask
+
+
+class Plan:
+    """pulse_plan: tile tables of a fixed tensor list, built once, replayed per step."""
+
+    def __init__(self, slots: Sequence[TensorSlot], device: Optional[torch.device] = None):
+        if len(slots) == 0:
+            raise ValueError("a plan needs at least one tensor")
+        self.slots = list(slots)  # keeps the buffers alive while the plan exists
+        dev = device
+        arr = (PulseTensor * len(slots))()
+        for i, s in enumerate(slots):
+            for name, t in (("master", s.master), ("prev", s.prev), ("w", s.w), ("idx", s.idx),
+                            ("val", s.val), ("mask", s.mask)):
+                if t is None:
+                    continue
+                if dev is None:
+                    dev = t.device
+                if name == "master":
+                    _need(t, name, (torch.float32,), dev, s.n)
+                elif name == "idx":
+                    _need(t, name, (torch.int32, torch.uint32), dev, min_numel=s.n)
+                elif name == "val":
+                    _need(t, name, _U16, dev, min_numel=s.n)
+                else:
+                    _need(t, name, _U16, dev, s.n)
+            arr[i] = PulseTensor(_ptr(s.master), _ptr(s.prev), _ptr(s.w), s.n, _ptr(s.idx),
+                                 _ptr(s.val), _ptr(s.mask))
+        if dev is None:
+            raise ValueError("a plan needs at least one device buffer")
+        self.device = dev
+        self.ntensors = len(slots)
+        handle = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            st = lib().pulse_plan_create(arr, len(slots), ctypes.byref(handle))
+        _raise(st, "pulse_plan_create")
+        self._h = handle
+
+    @property
+    def num_tiles(self) -> int:
+        return int(lib().pulse_plan_num_tiles(self._h))
+
+    def encode(self, counts_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        if counts_out is None:
+            counts_out = torch.empty(self.ntensors, dtype=torch.int64, device=self.device)
+        _need(counts_out, "counts_out", (torch.int64, torch.uint64), self.device, min_numel=self.ntensors)
+        with torch.cuda.device(self.device):
+            st = lib().pulse_encode_multi(self._h, _ptr(counts_out), _stream(self.device))
+        _raise(st, "pulse_encode_multi")
+        return counts_out
+
+    def apply(self, counts):
+        """counts: a device int64 tensor (no host round trip) or host integers."""
+        with torch.cuda.device(self.device):
+            if isinstance(counts, torch.Tensor) and counts.is_cuda:
+                _need(counts, "counts", (torch.int64, torch.uint64), self.device, min_numel=self.ntensors)
+                st = lib().pulse_apply_multi_device(self._h, _ptr(counts), _stream(self.device))
+            else:
+                host = (ctypes.c_uint64 * self.ntensors)(*[int(c) for c in counts])
+                st = lib().pulse_apply_multi(self._h, host, _stream(self.device))
+        _raise(st, "pulse_apply_multi")
+
+    def xor_mask(self):
+        with torch.cuda.device(self.device):
+            st = lib().pulse_xor_mask_multi(self._h, _stream(self.device))
+        _raise(st, "pulse_xor_mask_multi")
+
+    def xor_apply(self):
+        with torch.cuda.device(self.device):
+            st = lib().pulse_xor_apply_multi(self._h, _stream(self.device))
+        _raise(st, "pulse_xor_apply_multi")
+
+    def get_error(self) -> int:
+        with torch.cuda.device(self.device):
+            return int(lib().pulse_plan_get_error(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            with torch.cuda.device(self.device):
+                lib().pulse_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

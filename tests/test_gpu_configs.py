@@ -1,0 +1,220 @@
+"""GPU vs oracle on the five workloads at full size, in the launch
+configuration the benchmark times (one multi-tensor plan per model).
+
+1. one tensor of 2^20 FP32 weights, eta = 3e-6 (single-tensor entry points);
+2. one Llama-style decoder layer, 9 tensors, 218,112,000 params;
+3. a Llama-3-8B-shaped model, 291 tensors, 8,030,261,248 params;
+4. one flat 2^28 tensor at seven update scales (density sweep);
+5. a 20-step chain on a Qwen2.5-1.5B-shaped model, both modes.
+
+Comparisons are bit-exact: patch indices and values in order, counts,
+refreshed prev, XOR masks, and the sampler's weights after apply.
+"""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rl_post_trainer_gb300 as pulse
+import workloads
+from pulse_testutil import host_f32, host_u16, host_u32, patch_of
+
+pytestmark = pytest.mark.gpu
+
+WORKERS = max(1, min(8, (os.cpu_count() or 2) // 2))
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    return torch.device("cuda", 0)
+
+
+class Model:
+    """Trainer and sampler buffers of one model, one allocation per tensor."""
+
+    def __init__(self, specs, seed, eta, dev, keep_prev0=True, xor=True):
+        pairs = workloads.torch_model(specs, seed, eta, dev)
+        self.specs = specs
+        self.master = [m for m, _ in pairs]
+        self.prev = [p for _, p in pairs]
+        self.prev0 = [p.clone() for p in self.prev] if keep_prev0 else None
+        self.w = [p.clone() for p in self.prev]
+        self.idx = [torch.empty(max(s.numel, 1), dtype=torch.int32, device=dev) for s in specs]
+        self.val = [torch.empty(max(s.numel, 1), dtype=torch.int16, device=dev) for s in specs]
+        if xor:
+            self.prev_x = [p.clone() for p in self.prev]
+            self.w_x = [p.clone() for p in self.prev]
+            self.mask = [torch.empty(s.numel, dtype=torch.int16, device=dev) for s in specs]
+        slots = [pulse.TensorSlot(s.numel, master=self.master[i], prev=self.prev[i], w=self.w[i],
+                                  idx=self.idx[i], val=self.val[i]) for i, s in enumerate(specs)]
+        self.plan = pulse.Plan(slots)
+        if xor:
+            xslots = [pulse.TensorSlot(s.numel, master=self.master[i], prev=self.prev_x[i],
+                                       w=self.w_x[i], mask=self.mask[i]) for i, s in enumerate(specs)]
+            self.xplan = pulse.Plan(xslots)
+
+    def close(self):
+        self.plan.close()
+        if hasattr(self, "xplan"):
+            self.xplan.close()
+
+
+def _check_tensor(model, t, counts, check_xor, prev_before=None):
+    """Oracle on the host copy of tensor t's inputs vs the GPU outputs."""
+    master = host_f32(model.master[t])
+    p0 = host_u16(model.prev0[t] if prev_before is None else prev_before[t])
+    o_prev = p0.copy()
+    o_idx, o_val = oracle.encode(master, o_prev)
+    k = int(counts[t])
+    assert k == o_idx.size, (t, k, o_idx.size)
+    g_idx, g_val, _ = patch_of(model.idx[t], model.val[t], k)
+    np.testing.assert_array_equal(g_idx, o_idx)
+    np.testing.assert_array_equal(g_val, o_val)
+    np.testing.assert_array_equal(host_u16(model.prev[t]), o_prev)
+    w_np = p0.copy()
+    oracle.apply(w_np, o_idx, o_val)
+    np.testing.assert_array_equal(host_u16(model.w[t]), w_np)
+    if check_xor:
+        xp = p0.copy()
+        o_mask = oracle.xor_mask(master, xp)
+        np.testing.assert_array_equal(host_u16(model.mask[t]), o_mask)
+        np.testing.assert_array_equal(host_u16(model.prev_x[t]), xp)
+        wx = p0.copy()
+        oracle.xor_apply(wx, o_mask)
+        np.testing.assert_array_equal(host_u16(model.w_x[t]), wx)
+    return k
+
+
+def _run_model_step(model, xor=True):
+    counts = model.plan.encode()
+    model.plan.apply(counts)
+    if xor:
+        model.xplan.xor_mask()
+        model.xplan.xor_apply()
+    torch.cuda.synchronize()
+    assert model.plan.get_error() == 0
+    if xor:
+        assert model.xplan.get_error() == 0
+    return counts.cpu().numpy()
+
+
+def test_config1_single_tensor_2p20():
+    dev = _dev()
+    spec = workloads.single(1 << 20)[0]
+    (m, p0), = workloads.torch_model([spec], seed=0, eta=workloads.ETA_DEFAULT, device=dev)
+    prev = p0.clone()
+    idx, val, cnt = pulse.encode(m, prev)
+    w = p0.clone()
+    pulse.apply(w, idx, val, int(cnt.item()))
+    prev_x = p0.clone()
+    mask = pulse.xor_mask(m, prev_x)
+    w_x = p0.clone()
+    pulse.xor_apply(w_x, mask)
+    torch.cuda.synchronize()
+    master_np, p0_np = host_f32(m), host_u16(p0)
+    o_prev = p0_np.copy()
+    o_idx, o_val = oracle.encode(master_np, o_prev)
+    g_idx, g_val, k = patch_of(idx, val, cnt)
+    np.testing.assert_array_equal(g_idx, o_idx)
+    np.testing.assert_array_equal(g_val, o_val)
+    np.testing.assert_array_equal(host_u16(prev), o_prev)
+    np.testing.assert_array_equal(host_u16(w), o_prev)
+    xp = p0_np.copy()
+    np.testing.assert_array_equal(host_u16(mask), oracle.xor_mask(master_np, xp))
+    np.testing.assert_array_equal(host_u16(w_x), xp)
+    density = k / spec.numel
+    assert 0.05 < density < 0.12, density      # N(0, 0.02) weights at eta = 3e-6: about 8%
+
+
+def test_config2_llama_layer_multi_tensor():
+    dev = _dev()
+    cfg = workloads.CONFIGS[2]
+    specs = cfg["specs"]()
+    assert workloads.total_params(specs) == 218_112_000 and len(specs) == 9
+    model = Model(specs, cfg["seed"], cfg["eta"], dev)
+    counts = _run_model_step(model)
+    with ThreadPoolExecutor(WORKERS) as ex:
+        ks = list(ex.map(lambda t: _check_tensor(model, t, counts, True), range(len(specs))))
+    assert sum(ks) > 0
+    model.close()
+
+
+def test_config3_llama3_8b_full_model():
+    dev = _dev()
+    cfg = workloads.CONFIGS[3]
+    specs = cfg["specs"]()
+    assert workloads.total_params(specs) == 8_030_261_248 and len(specs) == 291
+    model = Model(specs, cfg["seed"], cfg["eta"], dev)
+    counts = _run_model_step(model)
+    order = sorted(range(len(specs)), key=lambda t: -specs[t].numel)   # big tensors first
+    with ThreadPoolExecutor(WORKERS) as ex:
+        ks = list(ex.map(lambda t: _check_tensor(model, t, counts, True), order))
+    total = sum(ks)
+    density = total / workloads.total_params(specs)
+    assert 0.05 < density < 0.12, density
+    model.close()
+
+
+def test_config4_density_sweep_2p28():
+    dev = _dev()
+    n = 1 << 28
+    spec = workloads.single(n)[0]
+    gen = workloads.torch_generator(dev, 3)
+    w0 = torch.empty(n, dtype=torch.float32, device=dev)
+    workloads.torch_init_(w0, spec, gen)
+    p0 = torch.empty(n, dtype=torch.int16, device=dev)
+    workloads.torch_bf16_view_(p0, w0)
+    w0_np, p0_np = host_f32(w0), host_u16(p0)
+    idx = torch.empty(n, dtype=torch.int32, device=dev)
+    val = torch.empty(n, dtype=torch.int16, device=dev)
+    last = -1.0
+    for i, eta in enumerate(workloads.ETA_SWEEP):
+        m = w0.clone()
+        workloads.torch_update_(m, eta, workloads.torch_generator(dev, workloads.sweep_seed(i)))
+        prev = p0.clone()
+        _, _, cnt = pulse.encode(m, prev, idx_out=idx, val_out=val)
+        w = p0.clone()
+        pulse.apply(w, idx, val, int(cnt.item()))
+        torch.cuda.synchronize()
+        m_np = host_f32(m)
+        o_prev = p0_np.copy()
+        o_idx, o_val = oracle.encode(m_np, o_prev)
+        g_idx, g_val, k = patch_of(idx, val, cnt)
+        assert k == o_idx.size, eta
+        np.testing.assert_array_equal(g_idx, o_idx)
+        np.testing.assert_array_equal(g_val, o_val)
+        np.testing.assert_array_equal(host_u16(prev), o_prev)
+        np.testing.assert_array_equal(host_u16(w), o_prev)
+        density = k / n
+        assert density > last        # the visible fraction grows with the update scale
+        last = density
+        del m, prev, w
+    assert pulse.get_error(dev) == 0
+
+
+def test_config5_qwen_chain_20_steps_both_modes():
+    dev = _dev()
+    cfg = workloads.CONFIGS[5]
+    specs = cfg["specs"]()
+    assert workloads.total_params(specs) == 1_543_714_304 and len(specs) == 338
+    model = Model(specs, cfg["seed"], cfg["eta"], dev, keep_prev0=True)
+    for step in range(workloads.CHAIN_STEPS):
+        if step > 0:
+            workloads.torch_step_(model.master, step)
+            for t in range(len(specs)):
+                model.prev0[t].copy_(model.prev[t])      # trainer view before this step
+        counts = _run_model_step(model)
+        for t in range(len(specs)):
+            full = model.master[t].to(torch.bfloat16).view(torch.int16)   # a full checkpoint's bits
+            assert torch.equal(model.w[t], model.prev[t]), (step, t)
+            assert torch.equal(model.w_x[t], model.prev_x[t]), (step, t)
+            assert torch.equal(model.prev[t], full), (step, t)
+            assert torch.equal(model.prev_x[t], full), (step, t)
+        if step in (0, 9, workloads.CHAIN_STEPS - 1):
+            with ThreadPoolExecutor(WORKERS) as ex:
+                list(ex.map(lambda t: _check_tensor(model, t, counts, True), range(len(specs))))
+    model.close()

@@ -194,3 +194,34 @@ def torch_bf16_view_(prev_u16, master_f32):
     import torch
     prev_u16.copy_(master_f32.to(torch.bfloat16).view(torch.int16))
     return prev_u16
+
+
+def torch_model(specs: Sequence[TensorSpec], seed: int, eta: float, device,
+                chunk: int = 1 << 26):
+    """Draws one training step on the device for every tensor, in list order.
+
+    Per tensor: w0 (initial master, FP32) then z; returns a list of
+    (master = w0 + eta * z, prev0 = torch's BF16 cast of w0) pairs, flat,
+    one allocation each (int16 holds the BF16 bit patterns of prev0).
+    """
+    import torch
+    gen = torch_generator(device, seed)
+    out = []
+    for spec in specs:
+        m = torch.empty(spec.numel, dtype=torch.float32, device=device)
+        torch_init_(m, spec, gen)
+        p = torch.empty(spec.numel, dtype=torch.int16, device=device)
+        torch_bf16_view_(p, m)
+        torch_update_(m, eta, gen, chunk)
+        out.append((m, p))
+    return out
+
+
+def torch_step_(masters, step: int, eta: float = ETA_DEFAULT, chunk: int = 1 << 26):
+    """One more Adam-sized step of a chain: master += eta * z, z drawn from
+    seed CHAIN_SEED_BASE + step, tensors in list order."""
+    if not masters:
+        return
+    gen = torch_generator(masters[0].device, CHAIN_SEED_BASE + step)
+    for m in masters:
+        torch_update_(m, eta, gen, chunk)
