@@ -7,21 +7,27 @@
 // summary, section "Metodologia: PULSE -- 1. PULSESync"), refreshing the
 // previous view in place.
 //
-// Kernel structure (one launch covers one tensor or a whole model):
-//  * persistent CTAs (SMs x resident CTAs); each takes tiles from a global
-//    ticket counter, so every tile's predecessors belong to CTAs that are
-//    already running and the look-back below always makes progress;
-//  * a kEncStages-deep ring of shared-memory stages filled by bulk copies
-//    (cp.async.bulk + mbarrier transaction counts): while a CTA resolves one
-//    tile's global offset, the next tiles are already streaming in;
-//  * per tile: 4 elements per thread per round, warp ballots give each
-//    thread's rank inside its warp, one warp scans the (round, warp) counts,
-//    and a single-pass decoupled look-back (Merrill & Garland, "Single-pass
-//    Parallel Prefix Scan with Decoupled Look-back", 2016) turns tile counts
-//    into global offsets; the look-back warp reads 128 predecessor words per
-//    step so the chain keeps up at HBM rates;
-//  * epilogue: (index, value) pairs at their global positions, and the new
-//    BF16 values written back to prev in 8-byte groups that hold a change.
+// One launch covers one tensor or a whole model. Persistent, warp-specialized
+// CTAs:
+//  * producer warp: takes tile tickets from a global counter (so a tile's
+//    predecessors always belong to CTAs that are already running) and fills
+//    a kEncStages-deep shared-memory ring with bulk copies (cp.async.bulk,
+//    completion counted in mbarrier transaction bytes);
+//  * 8 compute warps: per 4096-element tile, cast + compare 4 consecutive
+//    elements per thread per round, write changed BF16 values back to prev
+//    at once (8-byte groups), rank changed elements with warp ballots and a
+//    scan of the (round, warp) counts (one CTA barrier per tile), publish the
+//    tile's count immediately, and park the tile's compacted patch (12-bit
+//    local index + value, 4 bytes per entry) in a shared-memory entry ring;
+//  * kEncLookbackWarps look-back warps: each takes a different parked tile,
+//    resolves its global offset with a single-pass decoupled look-back
+//    (Merrill & Garland, "Single-pass Parallel Prefix Scan with Decoupled
+//    Look-back", 2016) reading kEncLookbackPerLane x 32 predecessor words per
+//    round trip, publishes the inclusive prefix, copies the parked entries to
+//    the patch with contiguous coalesced stores, and frees the slot. An L2
+//    round trip to the status words costs microseconds while HBM is
+//    saturated, so up to kEncParked tiles per CTA wait in the ring while the
+//    compute warps stream on.
 // Every wait is bounded; a wait that gives up records PULSE_ERR_TIMEOUT and
 // the kernel still finishes with all writes inside the caller's buffers.
 #include "pulse_device.cuh"
@@ -30,31 +36,65 @@
 namespace pulse {
 namespace {
 
-constexpr int kWarps = kEncThreads / 32;
-constexpr int kPairs = kEncRounds * kWarps;  // (round, warp) pairs in tile order
-static_assert(kPairs == 32, "one warp scans the (round, warp) counts");
-constexpr int kLookbackPerLane = 4;          // 128 predecessor words per step
+constexpr int kWarps = kEncThreads / 32;             // compute warps
+constexpr int kProducerWarp = kWarps;
+constexpr int kFirstLookbackWarp = kWarps + 1;
+static_assert(kEncRounds == 4, "four rounds pack into the bytes of one word");
+static_assert(kWarps == 8, "the cross-warp scan runs over 8 lanes");
+constexpr int kLookbackPerLane = kEncLookbackPerLane;
+// parked-tile slots: a multiple of the look-back warps (slot p is always
+// handled by look-back warp p % kEncLookbackWarps), at least kEncParked
+constexpr int kPendSlots =
+    ((kEncParked > kEncLookbackWarps ? kEncParked : kEncLookbackWarps) + kEncLookbackWarps - 1) /
+    kEncLookbackWarps * kEncLookbackWarps;
+constexpr int kComputeBarrier = 1;                   // named barrier of the compute warps
+constexpr uint32_t kRingMask = uint32_t(kEncRing) - 1u;
 
 constexpr uint32_t kStageMasterBytes = kEncTile * 4;
 constexpr uint32_t kStagePrevBytes = kEncTile * 2;
 constexpr uint32_t kStageBytes = kStageMasterBytes + kStagePrevBytes;
-constexpr size_t kDynSmem = size_t(kEncStages) * kStageBytes + 128;  // +128 for alignment
+constexpr size_t kDynSmem = size_t(kEncStages) * kStageBytes + size_t(kEncRing) * 4 + 128;
 
 enum : uint32_t { kModeEnd = 0, kModeBulk = 1, kModeGeneric = 2 };
 
+// Everything the compute warps need about a tile, written by the producer
+// (which reads the tensor descriptor anyway) so the compute path touches no
+// global descriptor memory.
 struct StageMeta {
   uint32_t tile;    // global tile id
   uint32_t tensor;  // tensor index (0 in single-tensor mode)
   uint32_t mode;
-  uint32_t pad;
+  uint32_t len;     // elements in the tile
+  uint64_t base;    // first element of the tile within its tensor
+  uint64_t first;   // first global tile of the tensor
+  uint64_t n;       // elements of the tensor
+  const float* master;
+  uint16_t* prev;
+  uint32_t* idx;
+  uint16_t* val;
+};
+
+struct ParkedMeta {
+  uint32_t tile;
+  uint32_t tensor;
+  uint32_t agg;     // changed elements in the tile
+  uint32_t last;    // 1: last tile of its tensor; 2: no more tiles for this look-back warp
+  uint64_t first;   // first global tile of the tensor
+  uint64_t n;       // elements of the tensor
+  uint32_t ring_start;
+  uint32_t base;    // first element of the tile within its tensor
+  uint32_t* idx;
+  uint16_t* val;
 };
 
 struct __align__(16) EncodeShared {
-  uint64_t bar[kEncStages];
+  uint64_t full[kEncStages];       // producer -> compute: stage filled
+  uint64_t empty[kEncStages];      // compute -> producer: stage consumed
+  uint64_t agg_ready[kPendSlots];  // compute -> look-back: tile parked and counted
+  uint64_t slot_free[kPendSlots];  // look-back -> compute: tile copied out
   StageMeta meta[kEncStages];
-  uint32_t pair_count[kPairs];
-  uint32_t pair_offset[kPairs];
-  uint32_t tile_prefix;
+  ParkedMeta parked[kPendSlots];
+  uint32_t warp_tot[2][kWarps];  // per warp: changed elements per round, one byte each
 };
 
 __device__ __forceinline__ int find_tensor(const uint64_t* tile_begin, int ntensors, uint64_t g) {
@@ -82,37 +122,57 @@ __device__ __forceinline__ void bulk_g2s_plain(void* smem_dst, const void* gmem_
       : "memory");
 }
 
-// Thread 0: take the next tile ticket and start filling stage s.
-template <bool MULTI>
-__device__ __forceinline__ void produce(const EncodeLaunch& a, EncodeShared& sh, uint8_t* stages,
-                                        int s, uint64_t pol_stream) {
-  const uint32_t ticket = atomicAdd(a.counters + 0, 1u) + a.first_ticket;
-  StageMeta m;
-  m.tile = ticket;
-  m.pad = 0;
-  if (ticket >= a.total_tiles) {
-    m.tensor = 0;
-    m.mode = kModeEnd;
-    sh.meta[s] = m;
-    return;
+__device__ __forceinline__ void compute_barrier() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kComputeBarrier), "n"(kEncThreads) : "memory");
+}
+
+// Named barrier of the compute warps that also ORs a predicate across them:
+// every loop-exit decision goes through it, so the 8 compute warps always
+// leave their loop together and no named barrier is ever left short.
+__device__ __forceinline__ bool compute_barrier_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(v)), "n"(kComputeBarrier), "n"(kEncThreads)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait for the producer and look-back warps, which are rarely on the
+// critical path: poll, sleeping kEncBackoffNs between polls so waiting warps
+// leave the issue slots to the compute warps. Same failure contract as
+// wait_or_flag below.
+__device__ __forceinline__ bool helper_wait(uint64_t* bar, uint32_t parity, const EncodeLaunch& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0; it < (1u << 28); ++it) {
+    if (kEncBackoffNs) __nanosleep(kEncBackoffNs);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (ld_volatile_u32(a.counters + 2) & kErrTimeout) return false;
+      if (global_timer_ns() - t0 > a.wait_limit_ns) break;
+    }
   }
-  const uint32_t t = MULTI ? static_cast<uint32_t>(find_tensor(a.tile_begin, a.ntensors, ticket)) : 0u;
-  const TensorDesc& d = desc_of<MULTI>(a, t);
-  const uint64_t base = (uint64_t(ticket) - d.tile_begin) * kEncTile;
-  const uint64_t len = d.n - base < uint64_t(kEncTile) ? d.n - base : uint64_t(kEncTile);
-  m.tensor = t;
-  if (d.bulk_ok && len == uint64_t(kEncTile)) {
-    m.mode = kModeBulk;
-    uint8_t* st = stages + size_t(s) * kStageBytes;
-    mbar_arrive_expect_tx(&sh.bar[s], kStageBytes);
-    bulk_g2s(st, d.master + base, kStageMasterBytes, &sh.bar[s], pol_stream);
-    // prev is written back soon after, so it keeps the default L2 policy
-    bulk_g2s_plain(st + kStageMasterBytes, d.prev + base, kStagePrevBytes, &sh.bar[s]);
-  } else {
-    m.mode = kModeGeneric;  // tail or unaligned tile: threads load from global
-    mbar_arrive(&sh.bar[s]);
-  }
-  sh.meta[s] = m;
+  record_error(a.counters + 2, kErrTimeout);
+  return false;
+}
+
+// Bounded mbarrier wait. Returns false if it gave up (the error is recorded);
+// once any wait of the launch has given up, later waits give up at once, so
+// a failed launch ends quickly. Callers stop after a failed wait; every
+// write they may still make stays in bounds.
+__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, const EncodeLaunch& a) {
+#pragma unroll 1
+  for (int i = 0; i < 64; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  if (ld_volatile_u32(a.counters + 2) & kErrTimeout) return false;
+  if (mbar_wait_bounded(bar, parity, a.wait_limit_ns)) return true;
+  record_error(a.counters + 2, kErrTimeout);
+  return false;
 }
 
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
@@ -121,45 +181,19 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
   return v;
 }
 
-// Spin (bounded) until the status word of `tile` is published in this epoch.
-// On timeout: record the error and report an inclusive prefix of 0, which
-// keeps every later offset at or below the true one (in bounds).
-__device__ __forceinline__ uint64_t wait_status(const EncodeLaunch& a, uint64_t tile) {
-  const uint64_t* p = a.status + tile;
-  uint64_t w = ld_relaxed_u64(p);
-  if (status_flag(w, a.epoch) != 0u) return w;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 0; it < (1u << 28); ++it) {
-    __nanosleep(40);
-    w = ld_relaxed_u64(p);
-    if (status_flag(w, a.epoch) != 0u) return w;
-    if ((it & 63u) == 63u) {
-      if (global_timer_ns() - t0 > a.wait_limit_ns ||
-          (ld_volatile_u32(a.counters + 2) & kErrTimeout)) {
-        break;
-      }
-    }
-  }
-  record_error(a.counters + 2, kErrTimeout);
-  return make_status(kFlagPrefix, a.epoch, 0u);
-}
-
-// Warp 0: publish this tile's count, find its exclusive prefix within the
-// tensor, publish the inclusive prefix.
-__device__ __forceinline__ uint32_t look_back(const EncodeLaunch& a, uint64_t g, uint64_t first,
-                                              uint32_t agg, int lane) {
+// Look-back warp: exclusive prefix of tile g within its tensor (its own
+// aggregate is already published). Reads kLookbackPerLane x 32 predecessor
+// words per round trip, nearest first; waits only on unpublished words that
+// lie before the nearest inclusive prefix; publishes g's inclusive prefix.
+__device__ __forceinline__ uint32_t resolve_prefix(const EncodeLaunch& a, uint64_t g,
+                                                   uint64_t first, uint32_t agg, int lane) {
   uint64_t* st = a.status;
-  if (g == first) {
-    if (lane == 0) st_relaxed_u64(st + g, make_status(kFlagPrefix, a.epoch, agg));
-    return 0u;
-  }
-  if (lane == 0) st_relaxed_u64(st + g, make_status(kFlagAggregate, a.epoch, agg));
+  if (g == first) return 0u;  // published as an inclusive prefix already
+  constexpr int kNone = 1 << 30;
   uint32_t prefix = 0;
   int64_t pos = int64_t(g) - 1;
+  bool gave_up = false;
   for (;;) {
-    // issue all window loads first (one round trip), then wait on any word
-    // that is not published yet; tiles before the tensor's first tile read
-    // as an inclusive prefix of 0
     uint64_t w[kLookbackPerLane];
 #pragma unroll
     for (int q = 0; q < kLookbackPerLane; ++q) {
@@ -167,37 +201,342 @@ __device__ __forceinline__ uint32_t look_back(const EncodeLaunch& a, uint64_t g,
       w[q] = tile >= int64_t(first) ? ld_relaxed_u64(st + tile)
                                     : make_status(kFlagPrefix, a.epoch, 0u);
     }
-    uint32_t vals[kLookbackPerLane];
-    int first_p = kLookbackPerLane;
+    int dp = kNone;  // window distance of the nearest inclusive prefix
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 0;; ++spin) {
+      int my_p = kNone, my_x = kNone;
 #pragma unroll
-    for (int q = 0; q < kLookbackPerLane; ++q) {
-      if (status_flag(w[q], a.epoch) == 0u)
-        w[q] = wait_status(a, uint64_t(pos - (lane * kLookbackPerLane + q)));
-      vals[q] = status_value(w[q]);
-      if (first_p == kLookbackPerLane && status_flag(w[q], a.epoch) == kFlagPrefix) first_p = q;
-    }
-    const uint32_t has_p = __ballot_sync(0xFFFFFFFFu, first_p < kLookbackPerLane);
-    uint32_t s = 0;
-    if (has_p) {
-      const int lp = __ffs(has_p) - 1;
+      for (int q = kLookbackPerLane - 1; q >= 0; --q) {
+        const uint32_t f = status_flag(w[q], a.epoch);
+        if (f == kFlagPrefix) my_p = lane * kLookbackPerLane + q;
+        if (f == 0u) my_x = lane * kLookbackPerLane + q;
+      }
+      dp = __reduce_min_sync(0xFFFFFFFFu, my_p);
+      const int dx = __reduce_min_sync(0xFFFFFFFFu, my_x);
+      if (dx == kNone || dx > dp) break;  // every word up to the nearest prefix is published
+      if (gave_up || (spin & 63u) == 63u) {
+        const bool late = gave_up || spin > (1u << 26) ||
+                          global_timer_ns() - t0 > a.wait_limit_ns ||
+                          (ld_volatile_u32(a.counters + 2) & kErrTimeout);
+        if (__any_sync(0xFFFFFFFFu, late)) {
+          // give up: unpublished words read as an inclusive prefix of 0, which
+          // keeps every offset at or below the true one (writes stay in bounds)
+          if (lane == 0) record_error(a.counters + 2, kErrTimeout);
+          gave_up = true;
+#pragma unroll
+          for (int q = 0; q < kLookbackPerLane; ++q)
+            if (status_flag(w[q], a.epoch) == 0u) w[q] = make_status(kFlagPrefix, a.epoch, 0u);
+          continue;
+        }
+      }
+      __nanosleep(32);
 #pragma unroll
       for (int q = 0; q < kLookbackPerLane; ++q) {
-        if (lane < lp || (lane == lp && q <= first_p)) s += vals[q];
+        if (status_flag(w[q], a.epoch) == 0u)
+          w[q] = ld_relaxed_u64(st + (pos - (lane * kLookbackPerLane + q)));
       }
-      prefix += warp_sum(s);
-      break;
     }
+    uint32_t sum = 0;
 #pragma unroll
-    for (int q = 0; q < kLookbackPerLane; ++q) s += vals[q];
-    prefix += warp_sum(s);
+    for (int q = 0; q < kLookbackPerLane; ++q)
+      if (lane * kLookbackPerLane + q <= dp) sum += status_value(w[q]);
+    prefix += warp_sum(sum);
+    if (dp != kNone) break;
     pos -= 32 * kLookbackPerLane;
   }
   if (lane == 0) st_relaxed_u64(st + g, make_status(kFlagPrefix, a.epoch, prefix + agg));
   return prefix;
 }
 
+// ------------------------------------------------------------ producer warp
 template <bool MULTI>
-__global__ void __launch_bounds__(kEncThreads) encode_kernel(const __grid_constant__ EncodeLaunch a) {
+__device__ __forceinline__ void producer_loop(const EncodeLaunch& a, EncodeShared& sh,
+                                              uint8_t* stages) {
+  const uint64_t pol_stream = l2_policy_evict_first();
+  uint32_t ticket_fills_done = 0;  // stage fills issued (the END marker included)
+  for (uint32_t it = 0;; ++it) {
+    const int s = int(it % kEncStages);
+    if (it >= uint32_t(kEncStages) && !helper_wait(&sh.empty[s], ((it / kEncStages) - 1) & 1u, a))
+      break;
+    ticket_fills_done = it + 1;
+    const uint32_t ticket = atomicAdd(a.counters + 0, 1u) + a.first_ticket;
+    StageMeta m{};
+    m.tile = ticket;
+    if (ticket >= a.total_tiles) {
+      m.mode = kModeEnd;
+      sh.meta[s] = m;
+      mbar_arrive(&sh.full[s]);
+      break;
+    }
+    const uint32_t t = MULTI ? uint32_t(find_tensor(a.tile_begin, a.ntensors, ticket)) : 0u;
+    const TensorDesc& d = desc_of<MULTI>(a, t);
+    const uint64_t base = (uint64_t(ticket) - d.tile_begin) * kEncTile;
+    const uint64_t len = d.n - base < uint64_t(kEncTile) ? d.n - base : uint64_t(kEncTile);
+    m.tensor = t;
+    m.len = uint32_t(len);
+    m.base = base;
+    m.first = d.tile_begin;
+    m.n = d.n;
+    m.master = d.master;
+    m.prev = d.prev;
+    m.idx = d.idx;
+    m.val = d.val;
+    if (d.bulk_ok && len == uint64_t(kEncTile)) {
+      m.mode = kModeBulk;
+      sh.meta[s] = m;
+      uint8_t* st = stages + size_t(s) * kStageBytes;
+      mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
+      bulk_g2s(st, d.master + base, kStageMasterBytes, &sh.full[s], pol_stream);
+      // prev is written back soon after, so it keeps the default L2 policy
+      bulk_g2s_plain(st + kStageMasterBytes, d.prev + base, kStagePrevBytes, &sh.full[s]);
+    } else {
+      m.mode = kModeGeneric;  // tail or unaligned tile: compute threads load from global
+      sh.meta[s] = m;
+      mbar_arrive(&sh.full[s]);
+    }
+  }
+  // No bulk copy may still be in flight when the CTA exits: wait (bounded)
+  // for the last fill of every stage.
+  const uint32_t fills = ticket_fills_done;
+  for (uint32_t f = fills > uint32_t(kEncStages) ? fills - kEncStages : 0u; f < fills; ++f)
+    mbar_wait_bounded(&sh.full[f % kEncStages], (f / kEncStages) & 1u, a.wait_limit_ns);
+  // The last CTA to stop taking tickets rewinds the ticket and finish
+  // counters for the next launch on this workspace.
+  __threadfence();
+  const uint32_t finished = atomicAdd(a.counters + 1, 1u);
+  if (finished == gridDim.x - 1) {
+    atomicExch(a.counters + 0, 0u);
+    atomicExch(a.counters + 1, 0u);
+  }
+}
+
+// ---------------------------------------------------------- look-back warps
+// Look-back warp w handles parked tiles w, w + W, w + 2W, ... of its CTA
+// (W = kEncLookbackWarps), each in its own slot: resolve the tile's global
+// offset, publish its inclusive prefix, then copy its parked entries to the
+// patch (entry k to position offset + k: contiguous, coalesced stores) and
+// free the slot.
+__device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShared& sh,
+                                              const uint32_t* ring, int w, int lane, bool multi) {
+  for (uint32_t i = uint32_t(w);; i += kEncLookbackWarps) {
+    const int q = int(i % kPendSlots);
+    const bool ok = helper_wait(&sh.agg_ready[q], (i / kPendSlots) & 1u, a);
+    // the warp leaves together: everything below uses full-warp collectives
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    const ParkedMeta pm = sh.parked[q];
+    if (pm.last == 2u) break;
+    const uint32_t prefix = resolve_prefix(a, pm.tile, pm.first, pm.agg, lane);
+    if (lane == 0 && pm.last == 1u) a.counts_out[multi ? pm.tensor : 0] = uint64_t(prefix) + pm.agg;
+    for (uint32_t k = uint32_t(lane); k < pm.agg; k += 32) {
+      const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
+      const uint64_t pos = uint64_t(prefix) + k;
+      // pos < n always holds when every wait succeeded; the test keeps the
+      // writes of a launch that gave up on a wait inside the buffers
+      if (pos < pm.n) {
+        pm.idx[pos] = pm.base + (ent & 0xFFFFu);
+        pm.val[pos] = uint16_t(ent >> 16);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.slot_free[q]);
+  }
+}
+
+// ------------------------------------------------------------ compute warps
+template <bool MULTI>
+__device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared& sh,
+                                             uint8_t* stages, uint32_t* ring, int tid, int lane,
+                                             int warp) {
+  // uniform across the compute threads
+  uint32_t posted = 0, freed = 0, ring_head = 0, ring_tail = 0;
+  bool failed = false;  // this thread saw a wait give up
+  for (uint32_t it = 0;; ++it) {
+    const int s = int(it % kEncStages);
+    failed |= !wait_or_flag(&sh.full[s], (it / kEncStages) & 1u, a);
+    const StageMeta m = sh.meta[s];
+    const bool live = m.mode != kModeEnd;
+    const uint64_t base = m.base;
+    const uint32_t len = m.len;
+
+    // ---- cast + compare: 4 consecutive elements per thread per round
+    uint32_t nb[kEncRounds][2];  // new BF16 values, two per word (low half = lower index)
+    uint32_t flags = 0;          // bit (j*4 + e): element e of round j changed
+    const float4* sm = reinterpret_cast<const float4*>(stages + size_t(s) * kStageBytes);
+    const uint2* sp = reinterpret_cast<const uint2*>(stages + size_t(s) * kStageBytes + kStageMasterBytes);
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      float4 mv;
+      uint2 pv;
+      if (m.mode == kModeBulk) {
+        mv = sm[j * kEncThreads + tid];
+        pv = sp[j * kEncThreads + tid];
+      } else {
+        // tail or unaligned tile; elements past the end read as +0 with a +0
+        // view, which never counts as a change (len is 0 for the end marker)
+        const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
+        float mm[4];
+        uint32_t pp[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool valid = li + e < len;
+          mm[e] = valid ? m.master[base + li + e] : 0.0f;
+          pp[e] = valid ? uint32_t(m.prev[base + li + e]) : 0u;
+        }
+        mv = make_float4(mm[0], mm[1], mm[2], mm[3]);
+        pv = make_uint2(pp[0] | (pp[1] << 16), pp[2] | (pp[3] << 16));
+      }
+      uint32_t b01 = cvt_bf16x2_rn(mv.x, mv.y);
+      uint32_t b23 = cvt_bf16x2_rn(mv.z, mv.w);
+      if (any_nan2(mv.x, mv.y) || any_nan2(mv.z, mv.w)) {
+        b01 = canon_nan_pair(b01, mv.x, mv.y);
+        b23 = canon_nan_pair(b23, mv.z, mv.w);
+      }
+      nb[j][0] = b01;
+      nb[j][1] = b23;
+      const uint32_t d01 = b01 ^ pv.x, d23 = b23 ^ pv.y;  // bitwise compare, two at a time
+      const uint32_t f = uint32_t((d01 & 0xFFFFu) != 0u) | (uint32_t(d01 > 0xFFFFu) << 1) |
+                         (uint32_t((d23 & 0xFFFFu) != 0u) << 2) | (uint32_t(d23 > 0xFFFFu) << 3);
+      flags |= f << (4 * j);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[s]);  // this warp is done with stage s
+
+    // ---- refresh prev now: it does not depend on the tile's global offset
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      const uint32_t f = (flags >> (j * 4)) & 0xFu;
+      if (f == 0u) continue;
+      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
+      if (m.mode == kModeBulk) {
+        *reinterpret_cast<uint2*>(m.prev + base + li) = make_uint2(nb[j][0], nb[j][1]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((f >> e) & 1u) m.prev[base + li + e] = uint16_t((nb[j][e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
+      }
+    }
+
+    // ---- rank the changed elements. Within a warp: one scan of the four
+    // per-round counts packed into bytes (a byte never exceeds 32 x 4 = 128).
+    uint32_t cnts = 0;
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) cnts |= uint32_t(__popc((flags >> (4 * j)) & 0xFu)) << (8 * j);
+    uint32_t incl = cnts;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t excl = incl - cnts;
+    const int pc = int(it & 1u);
+    if (lane == 31) sh.warp_tot[pc][warp] = incl;
+    // the one CTA barrier of the iteration; it also decides, for every compute
+    // warp at once, whether the loop ends
+    if (compute_barrier_or(failed || !live)) break;
+    // Across warps, in tile order (round-major, then warp): every warp scans
+    // the 8 packed warp totals, widened to 16-bit fields (rounds 0/2 and 1/3;
+    // a field never exceeds 8 x 128 = 1024).
+    const uint32_t t = lane < kWarps ? sh.warp_tot[pc][lane] : 0u;
+    const uint32_t t02 = t & 0x00FF00FFu, t13 = (t >> 8) & 0x00FF00FFu;
+    uint32_t s02 = t02, s13 = t13;
+#pragma unroll
+    for (int o = 1; o < kWarps; o <<= 1) {
+      const uint32_t v02 = __shfl_up_sync(0xFFFFFFFFu, s02, o);
+      const uint32_t v13 = __shfl_up_sync(0xFFFFFFFFu, s13, o);
+      if (lane >= o) { s02 += v02; s13 += v13; }
+    }
+    const uint32_t b02 = __shfl_sync(0xFFFFFFFFu, s02 - t02, warp);  // warps before this one
+    const uint32_t b13 = __shfl_sync(0xFFFFFFFFu, s13 - t13, warp);
+    const uint32_t a02 = __shfl_sync(0xFFFFFFFFu, s02, kWarps - 1);   // all warps
+    const uint32_t a13 = __shfl_sync(0xFFFFFFFFu, s13, kWarps - 1);
+    const uint32_t tot0 = a02 & 0xFFFFu, tot1 = a13 & 0xFFFFu, tot2 = a02 >> 16, tot3 = a13 >> 16;
+    uint32_t round_off[kEncRounds];  // this thread's first entry in each round, within the tile
+    round_off[0] = (b02 & 0xFFFFu) + (excl & 0xFFu);
+    round_off[1] = tot0 + (b13 & 0xFFFFu) + ((excl >> 8) & 0xFFu);
+    round_off[2] = tot0 + tot1 + (b02 >> 16) + ((excl >> 16) & 0xFFu);
+    round_off[3] = tot0 + tot1 + tot2 + (b13 >> 16) + (excl >> 24);
+    const uint32_t agg = tot0 + tot1 + tot2 + tot3;
+    if (tid == 0) {
+      // publish the count at once; a tensor's first tile is its own prefix
+      st_relaxed_u64(a.status + m.tile,
+                     make_status(uint64_t(m.tile) == m.first ? kFlagPrefix : kFlagAggregate,
+                                 a.epoch, agg));
+    }
+
+    // ---- room for the tile: a free parked slot and agg ring entries; slots
+    // are reclaimed in order once their look-back warp has copied them out
+    bool reclaimed = false;
+    while (posted - freed >= uint32_t(kPendSlots) || ring_head + agg - ring_tail > uint32_t(kEncRing)) {
+      if (freed == posted) break;  // nothing left to reclaim (reachable only after an error)
+      const int fq = int(freed % kPendSlots);
+      failed |= !wait_or_flag(&sh.slot_free[fq], (freed / kPendSlots) & 1u, a);
+      ring_tail += sh.parked[fq].agg;
+      ++freed;
+      reclaimed = true;
+    }
+    if (reclaimed) compute_barrier();  // every thread has read the reclaimed slots
+
+    // ---- park the compacted tile: (local index | value << 16) per entry
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      const uint32_t f = (flags >> (j * 4)) & 0xFu;
+      if (f == 0u) continue;
+      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
+      uint32_t r = ring_head + round_off[j];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((f >> e) & 1u) {
+          const uint32_t value = (nb[j][e >> 1] >> ((e & 1) * 16)) & 0xFFFFu;
+          ring[r & kRingMask] = (li + uint32_t(e)) | (value << 16);
+          ++r;
+        }
+      }
+    }
+    const int q = int(posted % kPendSlots);
+    if (tid == 0) {
+      ParkedMeta pm;
+      pm.tile = m.tile;
+      pm.tensor = m.tensor;
+      pm.agg = agg;
+      pm.last = (base + len == m.n) ? 1u : 0u;
+      pm.first = m.first;
+      pm.n = m.n;
+      pm.ring_start = ring_head;
+      pm.base = uint32_t(base);
+      pm.idx = m.idx;
+      pm.val = m.val;
+      sh.parked[q] = pm;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.agg_ready[q]);  // 8 arrivals: every warp's entries are in
+    ++posted;
+    ring_head += agg;
+  }
+  // no more tiles (the compute warps left the loop together): wait until
+  // every parked tile is copied out, then send each look-back warp its end
+  // marker
+  while (freed < posted) {
+    const int fq = int(freed % kPendSlots);
+    wait_or_flag(&sh.slot_free[fq], (freed / kPendSlots) & 1u, a);
+    ++freed;
+  }
+  compute_barrier();
+  for (int k = 0; k < kEncLookbackWarps; ++k) {
+    const uint32_t i = posted + uint32_t(k);
+    const int q = int(i % kPendSlots);
+    if (tid == 0) {
+      ParkedMeta pm{};
+      pm.last = 2u;
+      sh.parked[q] = pm;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.agg_ready[q]);
+  }
+}
+
+template <bool MULTI>
+__global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
+    encode_kernel(const __grid_constant__ EncodeLaunch a) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ EncodeShared sh;
   const int tid = threadIdx.x;
@@ -205,150 +544,40 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(const __grid_consta
   const int warp = tid >> 5;
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~uintptr_t(127));
-  const uint64_t pol_stream = l2_policy_evict_first();
+  uint32_t* ring = reinterpret_cast<uint32_t*>(stages + size_t(kEncStages) * kStageBytes);
 
   if constexpr (MULTI) {
     // tensors with no elements have no tiles: their count is 0
     if (blockIdx.x == 0) {
-      for (int t = tid; t < a.ntensors; t += kEncThreads)
+      for (int t = tid; t < a.ntensors; t += kEncBlockThreads)
         if (a.tensors[t].n == 0) a.counts_out[t] = 0;
     }
   }
   if (tid == 0) {
 #pragma unroll
-    for (int s = 0; s < kEncStages; ++s) mbar_init(&sh.bar[s], 1);
+    for (int s = 0; s < kEncStages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], kWarps);
+      sh.meta[s] = StageMeta{};
+      sh.meta[s].mode = kModeEnd;
+    }
+#pragma unroll
+    for (int q = 0; q < kPendSlots; ++q) {
+      mbar_init(&sh.agg_ready[q], kWarps);
+      mbar_init(&sh.slot_free[q], 1);
+      sh.parked[q] = ParkedMeta{};
+      sh.parked[q].last = 2u;
+    }
     fence_mbar_init();
   }
-  __syncthreads();
-  if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < kEncStages; ++s) produce<MULTI>(a, sh, stages, s, pol_stream);
-  }
-  __syncthreads();
+  __syncthreads();  // the last CTA-wide barrier: roles split below
 
-  uint32_t phase = 0;
-  for (uint32_t it = 0;; ++it) {
-    const int s = int(it % kEncStages);
-    const StageMeta m = sh.meta[s];
-    if (m.mode == kModeEnd) break;
-    const TensorDesc& d = desc_of<MULTI>(a, m.tensor);
-    const uint64_t first_tile = d.tile_begin;
-    const uint64_t base = (uint64_t(m.tile) - first_tile) * kEncTile;
-    const uint64_t n = d.n;
-    const uint32_t len = uint32_t(n - base < uint64_t(kEncTile) ? n - base : uint64_t(kEncTile));
-
-    if (!mbar_wait_bounded(&sh.bar[s], (phase >> s) & 1u, a.wait_limit_ns)) {
-      record_error(a.counters + 2, kErrTimeout);
-      mbar_wait_bounded(&sh.bar[s], (phase >> s) & 1u, a.wait_limit_ns);
-    }
-    phase ^= 1u << s;
-
-    // ---- cast + compare: 4 consecutive elements per thread per round
-    uint32_t nb[kEncRounds][2];  // new BF16 values, two per word (low = lower index)
-    uint32_t flags = 0;          // bit (j*4 + e): element e of round j changed
-    const float4* sm = reinterpret_cast<const float4*>(stages + size_t(s) * kStageBytes);
-    const uint2* sp = reinterpret_cast<const uint2*>(stages + size_t(s) * kStageBytes + kStageMasterBytes);
-#pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
-      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
-      uint32_t mu[4], pu[4];
-      bool valid[4];
-      if (m.mode == kModeBulk) {
-        const float4 mv = sm[j * kEncThreads + tid];
-        const uint2 pv = sp[j * kEncThreads + tid];
-        mu[0] = __float_as_uint(mv.x); mu[1] = __float_as_uint(mv.y);
-        mu[2] = __float_as_uint(mv.z); mu[3] = __float_as_uint(mv.w);
-        pu[0] = pv.x & 0xFFFFu; pu[1] = pv.x >> 16; pu[2] = pv.y & 0xFFFFu; pu[3] = pv.y >> 16;
-        valid[0] = valid[1] = valid[2] = valid[3] = true;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          valid[e] = li + e < len;
-          mu[e] = valid[e] ? __float_as_uint(d.master[base + li + e]) : 0u;
-          pu[e] = valid[e] ? uint32_t(d.prev[base + li + e]) : 0u;
-        }
-      }
-      uint32_t b[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        b[e] = bf16_rne_bits(mu[e]);
-        if (valid[e] && b[e] != pu[e]) flags |= 1u << (j * 4 + e);
-      }
-      nb[j][0] = b[0] | (b[1] << 16);
-      nb[j][1] = b[2] | (b[3] << 16);
-    }
-    __syncthreads();  // stage s consumed by every thread
-    if (tid == 0) produce<MULTI>(a, sh, stages, s, pol_stream);
-
-    // ---- ranks: within warp by ballots, across (round, warp) by one scan
-    uint32_t before[kEncRounds];
-#pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
-      uint32_t cnt = 0, bef = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (flags >> (j * 4 + e)) & 1u);
-        cnt += __popc(bal);
-        bef += __popc(bal & lanemask_lt());
-      }
-      before[j] = bef;
-      if (lane == 0) sh.pair_count[j * kWarps + warp] = cnt;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t c = sh.pair_count[lane];
-      uint32_t incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      sh.pair_offset[lane] = incl - c;
-      const uint32_t agg = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      const uint32_t prefix = look_back(a, m.tile, first_tile, agg, lane);
-      if (lane == 0) {
-        sh.tile_prefix = prefix;
-        if (base + len == n) a.counts_out[MULTI ? m.tensor : 0] = uint64_t(prefix) + agg;
-      }
-    }
-    __syncthreads();
-
-    // ---- emit the patch entries and refresh prev
-    const uint32_t prefix = sh.tile_prefix;
-#pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
-      const uint32_t f = (flags >> (j * 4)) & 0xFu;
-      if (f == 0u) continue;
-      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
-      uint32_t pos = prefix + sh.pair_offset[j * kWarps + warp] + before[j];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if ((f >> e) & 1u) {
-          d.idx[pos] = uint32_t(base) + li + uint32_t(e);
-          d.val[pos] = uint16_t((nb[j][e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
-          ++pos;
-        }
-      }
-      if (m.mode == kModeBulk) {
-        *reinterpret_cast<uint2*>(d.prev + base + li) = make_uint2(nb[j][0], nb[j][1]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((f >> e) & 1u) d.prev[base + li + e] = uint16_t((nb[j][e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
-      }
-    }
-  }
-
-  // The last CTA to finish rewinds the ticket and finish counters for the
-  // next launch on this workspace.
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t finished = atomicAdd(a.counters + 1, 1u);
-    if (finished == gridDim.x - 1) {
-      atomicExch(a.counters + 0, 0u);
-      atomicExch(a.counters + 1, 0u);
-    }
+  if (warp < kWarps) {
+    compute_loop<MULTI>(a, sh, stages, ring, tid, lane, warp);
+  } else if (warp == kProducerWarp) {
+    if (lane == 0) producer_loop<MULTI>(a, sh, stages);
+  } else {
+    lookback_loop(a, sh, ring, warp - kFirstLookbackWarp, lane, MULTI);
   }
 }
 
@@ -358,7 +587,7 @@ int encode_blocks_per_sm() {
     cudaFuncSetAttribute(encode_kernel<MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          int(kDynSmem));
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, encode_kernel<MULTI>, kEncThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, encode_kernel<MULTI>, kEncBlockThreads,
                                                       kDynSmem) != cudaSuccess || b < 1)
       b = 1;
     return b;
@@ -378,10 +607,10 @@ int encode_grid_size(int device) {
 cudaError_t launch_encode(const EncodeLaunch& a, bool multi, int grid, cudaStream_t stream) {
   if (multi) {
     encode_blocks_per_sm<true>();
-    encode_kernel<true><<<grid, kEncThreads, kDynSmem, stream>>>(a);
+    encode_kernel<true><<<grid, kEncBlockThreads, kDynSmem, stream>>>(a);
   } else {
     encode_blocks_per_sm<false>();
-    encode_kernel<false><<<grid, kEncThreads, kDynSmem, stream>>>(a);
+    encode_kernel<false><<<grid, kEncBlockThreads, kDynSmem, stream>>>(a);
   }
   return cudaGetLastError();
 }

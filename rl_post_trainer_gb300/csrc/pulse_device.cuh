@@ -29,6 +29,33 @@ __device__ __forceinline__ uint32_t bf16_rne_bits(uint32_t u) {
   return ((u & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC0u : rounded;
 }
 
+// Two FP32 values -> one packed BF16 pair with the hardware convert, round to
+// nearest even: low half from `lo`, high half from `hi`. Finite and infinite
+// inputs match bf16_rne_bits exactly; NaN inputs are not canonicalised here
+// (see canon_nan_pair).
+__device__ __forceinline__ uint32_t cvt_bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// True if either input is NaN (one compare for two elements).
+__device__ __forceinline__ bool any_nan2(float a, float b) {
+  uint32_t r;
+  asm("{\n\t.reg .pred p;\n\tsetp.nan.f32 p, %1, %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b));
+  return r != 0u;
+}
+
+// Replace the half of a packed BF16 pair whose FP32 source is NaN by the
+// canonical quiet NaN 0x7FC0 (rare path).
+__device__ __forceinline__ uint32_t canon_nan_pair(uint32_t b, float lo, float hi) {
+  if (lo != lo) b = (b & 0xFFFF0000u) | 0x7FC0u;
+  if (hi != hi) b = (b & 0x0000FFFFu) | 0x7FC00000u;
+  return b;
+}
+
 // ------------------------------------------------------------ time / errors
 
 __device__ __forceinline__ uint64_t global_timer_ns() {

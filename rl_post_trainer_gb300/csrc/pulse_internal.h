@@ -8,11 +8,43 @@
 namespace pulse {
 
 // ---------------------------------------------------------------- encode
-// Tile geometry: kEncThreads threads x kEncRounds rounds x 4 elements.
+// Tile geometry: kEncThreads compute threads x kEncRounds rounds x 4
+// elements. Each CTA adds one producer warp and kEncLookbackWarps look-back
+// warps.
 constexpr int kEncThreads = 256;
 constexpr int kEncRounds = 4;
 constexpr int kEncTile = kEncThreads * kEncRounds * 4;  // 4096 elements
-constexpr int kEncStages = 3;                             // bulk-copy ring depth
+#ifndef PULSE_ENC_STAGES
+#define PULSE_ENC_STAGES 2
+#endif
+#ifndef PULSE_ENC_LOOKBACK_WARPS
+#define PULSE_ENC_LOOKBACK_WARPS 1
+#endif
+#ifndef PULSE_ENC_PARKED
+#define PULSE_ENC_PARKED 8
+#endif
+#ifndef PULSE_ENC_RING
+#define PULSE_ENC_RING 4096
+#endif
+#ifndef PULSE_ENC_MIN_BLOCKS
+#define PULSE_ENC_MIN_BLOCKS 3
+#endif
+#ifndef PULSE_ENC_LOOKBACK
+#define PULSE_ENC_LOOKBACK 8
+#endif
+#ifndef PULSE_ENC_BACKOFF_NS
+#define PULSE_ENC_BACKOFF_NS 128
+#endif
+constexpr int kEncStages = PULSE_ENC_STAGES;                // bulk-copy ring depth
+constexpr int kEncLookbackWarps = PULSE_ENC_LOOKBACK_WARPS;  // concurrent look-backs per CTA
+constexpr int kEncParked = PULSE_ENC_PARKED;                // parked tiles per CTA awaiting copy-out
+constexpr int kEncRing = PULSE_ENC_RING;                    // parked patch entries per CTA
+constexpr int kEncMinBlocks = PULSE_ENC_MIN_BLOCKS;          // resident CTAs per SM
+constexpr int kEncLookbackPerLane = PULSE_ENC_LOOKBACK;     // look-back words per lane per round trip
+constexpr uint32_t kEncBackoffNs = PULSE_ENC_BACKOFF_NS;    // sleep between polls of waiting helper warps
+constexpr int kEncBlockThreads = kEncThreads + 32 * (1 + kEncLookbackWarps);
+static_assert((kEncRing & (kEncRing - 1)) == 0 && kEncRing >= kEncTile,
+              "the parked-entry ring is a power of two holding at least one full tile");
 
 // Device view of one tensor for the encode / XOR-mask / apply kernels.
 struct TensorDesc {
