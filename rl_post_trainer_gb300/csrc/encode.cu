@@ -95,7 +95,9 @@ struct __align__(16) EncodeShared {
   StageMeta meta[kEncStages];
   ParkedMeta parked[kPendSlots];
   uint32_t warp_tot[2][kWarps];  // per warp: changed elements per round, one byte each
+  uint32_t ring_tail;            // ring entries before this position are copied out
 };
+static_assert(kEncLookbackWarps == 1, "parked tiles are freed in order by one look-back warp");
 
 __device__ __forceinline__ int find_tensor(const uint64_t* tile_begin, int ntensors, uint64_t g) {
   // largest t with tile_begin[t] <= g; tile_begin[ntensors] = total > g
@@ -142,17 +144,14 @@ __device__ __forceinline__ bool compute_barrier_or(bool v) {
   return r != 0;
 }
 
-// Bounded wait for the producer and look-back warps, which are rarely on the
-// critical path: poll, sleeping kEncBackoffNs between polls so waiting warps
-// leave the issue slots to the compute warps. Same failure contract as
-// wait_or_flag below.
+// Bounded wait for the producer and look-back warps. The hardware suspends
+// the waiting warp between tries, so waiting warps leave the issue slots to
+// the compute warps. Same failure contract as wait_or_flag below.
 __device__ __forceinline__ bool helper_wait(uint64_t* bar, uint32_t parity, const EncodeLaunch& a) {
-  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 28); ++it) {
-    if (kEncBackoffNs) __nanosleep(kEncBackoffNs);
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((it & 15u) == 15u) {
       if (ld_volatile_u32(a.counters + 2) & kErrTimeout) return false;
       if (global_timer_ns() - t0 > a.wait_limit_ns) break;
     }
@@ -166,9 +165,10 @@ __device__ __forceinline__ bool helper_wait(uint64_t* bar, uint32_t parity, cons
 // a failed launch ends quickly. Callers stop after a failed wait; every
 // write they may still make stays in bounds.
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, const EncodeLaunch& a) {
+  // the hardware suspends the warp for up to 20 us per try
 #pragma unroll 1
-  for (int i = 0; i < 64; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  for (int i = 0; i < 4; ++i)
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   if (ld_volatile_u32(a.counters + 2) & kErrTimeout) return false;
   if (mbar_wait_bounded(bar, parity, a.wait_limit_ns)) return true;
   record_error(a.counters + 2, kErrTimeout);
@@ -185,22 +185,31 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
 // aggregate is already published). Reads kLookbackPerLane x 32 predecessor
 // words per round trip, nearest first; waits only on unpublished words that
 // lie before the nearest inclusive prefix; publishes g's inclusive prefix.
+// Issue the loads of one look-back window: the kLookbackPerLane x 32 status
+// words before `pos`, nearest first; words before the tensor's first tile
+// read as an inclusive prefix of 0.
+__device__ __forceinline__ void load_window(const EncodeLaunch& a, int64_t pos, uint64_t first,
+                                            int lane, uint64_t (&w)[kLookbackPerLane]) {
+#pragma unroll
+  for (int q = 0; q < kLookbackPerLane; ++q) {
+    const int64_t tile = pos - (lane * kLookbackPerLane + q);
+    w[q] = tile >= int64_t(first) ? ld_relaxed_u64(a.status + tile)
+                                  : make_status(kFlagPrefix, a.epoch, 0u);
+  }
+}
+
+// `w` holds the first window (load_window at g - 1), already in flight.
 __device__ __forceinline__ uint32_t resolve_prefix(const EncodeLaunch& a, uint64_t g,
-                                                   uint64_t first, uint32_t agg, int lane) {
+                                                   uint64_t first, uint32_t agg, int lane,
+                                                   uint64_t (&w)[kLookbackPerLane]) {
   uint64_t* st = a.status;
   if (g == first) return 0u;  // published as an inclusive prefix already
   constexpr int kNone = 1 << 30;
   uint32_t prefix = 0;
   int64_t pos = int64_t(g) - 1;
   bool gave_up = false;
-  for (;;) {
-    uint64_t w[kLookbackPerLane];
-#pragma unroll
-    for (int q = 0; q < kLookbackPerLane; ++q) {
-      const int64_t tile = pos - (lane * kLookbackPerLane + q);
-      w[q] = tile >= int64_t(first) ? ld_relaxed_u64(st + tile)
-                                    : make_status(kFlagPrefix, a.epoch, 0u);
-    }
+  for (bool first_window = true;; first_window = false) {
+    if (!first_window) load_window(a, pos, first, lane, w);
     int dp = kNone;  // window distance of the nearest inclusive prefix
     const uint64_t t0 = global_timer_ns();
     for (uint32_t spin = 0;; ++spin) {
@@ -249,30 +258,45 @@ __device__ __forceinline__ uint32_t resolve_prefix(const EncodeLaunch& a, uint64
 }
 
 // ------------------------------------------------------------ producer warp
+// One thread. The next tile ticket is requested one fill ahead, so the
+// atomic's round trip overlaps the wait for a free stage; consecutive tickets
+// usually fall in the same tensor, so its descriptor is kept in registers and
+// the tile -> tensor search runs only when a ticket leaves it.
 template <bool MULTI>
 __device__ __forceinline__ void producer_loop(const EncodeLaunch& a, EncodeShared& sh,
                                               uint8_t* stages) {
   const uint64_t pol_stream = l2_policy_evict_first();
   uint32_t ticket_fills_done = 0;  // stage fills issued (the END marker included)
+  uint32_t ticket = atomicAdd(a.counters + 0, 1u) + a.first_ticket;
+  uint32_t cur_t = 0;                      // cached tensor (multi-tensor mode)
+  uint64_t cur_begin = 1, cur_end = 0;     // its global tile range; empty until loaded
+  TensorDesc d = a.one;
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kEncStages);
+    const bool end = ticket >= a.total_tiles;
+    const uint32_t next = end ? ticket : atomicAdd(a.counters + 0, 1u) + a.first_ticket;
     if (it >= uint32_t(kEncStages) && !helper_wait(&sh.empty[s], ((it / kEncStages) - 1) & 1u, a))
       break;
     ticket_fills_done = it + 1;
-    const uint32_t ticket = atomicAdd(a.counters + 0, 1u) + a.first_ticket;
     StageMeta m{};
     m.tile = ticket;
-    if (ticket >= a.total_tiles) {
+    if (end) {
       m.mode = kModeEnd;
       sh.meta[s] = m;
       mbar_arrive(&sh.full[s]);
       break;
     }
-    const uint32_t t = MULTI ? uint32_t(find_tensor(a.tile_begin, a.ntensors, ticket)) : 0u;
-    const TensorDesc& d = desc_of<MULTI>(a, t);
+    if constexpr (MULTI) {
+      if (uint64_t(ticket) < cur_begin || uint64_t(ticket) >= cur_end) {
+        cur_t = uint32_t(find_tensor(a.tile_begin, a.ntensors, ticket));
+        d = a.tensors[cur_t];
+        cur_begin = d.tile_begin;
+        cur_end = __ldg(a.tile_begin + cur_t + 1);
+      }
+    }
     const uint64_t base = (uint64_t(ticket) - d.tile_begin) * kEncTile;
     const uint64_t len = d.n - base < uint64_t(kEncTile) ? d.n - base : uint64_t(kEncTile);
-    m.tensor = t;
+    m.tensor = cur_t;
     m.len = uint32_t(len);
     m.base = base;
     m.first = d.tile_begin;
@@ -294,6 +318,7 @@ __device__ __forceinline__ void producer_loop(const EncodeLaunch& a, EncodeShare
       sh.meta[s] = m;
       mbar_arrive(&sh.full[s]);
     }
+    ticket = next;
   }
   // No bulk copy may still be in flight when the CTA exits: wait (bounded)
   // for the last fill of every stage.
@@ -312,33 +337,75 @@ __device__ __forceinline__ void producer_loop(const EncodeLaunch& a, EncodeShare
 
 // ---------------------------------------------------------- look-back warps
 // Look-back warp w handles parked tiles w, w + W, w + 2W, ... of its CTA
-// (W = kEncLookbackWarps), each in its own slot: resolve the tile's global
-// offset, publish its inclusive prefix, then copy its parked entries to the
-// patch (entry k to position offset + k: contiguous, coalesced stores) and
-// free the slot.
+// (W = kEncLookbackWarps), each in its own slot. It takes every such tile
+// that is already counted, up to kLookbackBatch, issues all their look-back
+// windows at once (one L2 round trip for the batch), then for each tile:
+// resolves its global offset, publishes its inclusive prefix, copies its
+// parked entries to the patch (entry k to position offset + k: contiguous,
+// coalesced stores) and frees the slot.
+constexpr int kLookbackBatch = 4;
+
 __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShared& sh,
                                               const uint32_t* ring, int w, int lane, bool multi) {
-  for (uint32_t i = uint32_t(w);; i += kEncLookbackWarps) {
-    const int q = int(i % kPendSlots);
-    const bool ok = helper_wait(&sh.agg_ready[q], (i / kPendSlots) & 1u, a);
+  for (uint32_t i = uint32_t(w);;) {
+    const bool ok = helper_wait(&sh.agg_ready[i % kPendSlots], (i / kPendSlots) & 1u, a);
     // the warp leaves together: everything below uses full-warp collectives
     if (!__all_sync(0xFFFFFFFFu, ok)) break;
-    const ParkedMeta pm = sh.parked[q];
-    if (pm.last == 2u) break;
-    const uint32_t prefix = resolve_prefix(a, pm.tile, pm.first, pm.agg, lane);
-    if (lane == 0 && pm.last == 1u) a.counts_out[multi ? pm.tensor : 0] = uint64_t(prefix) + pm.agg;
-    for (uint32_t k = uint32_t(lane); k < pm.agg; k += 32) {
-      const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
-      const uint64_t pos = uint64_t(prefix) + k;
-      // pos < n always holds when every wait succeeded; the test keeps the
-      // writes of a launch that gave up on a wait inside the buffers
-      if (pos < pm.n) {
-        pm.idx[pos] = pm.base + (ent & 0xFFFFu);
-        pm.val[pos] = uint16_t(ent >> 16);
+    // how many more of this warp's tiles are already parked (lane 0 decides)
+    int more = 0;
+    if (lane == 0) {
+      for (int b = 1; b < kLookbackBatch; ++b) {
+        const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
+        if (!mbar_test_wait(&sh.agg_ready[ii % kPendSlots], (ii / kPendSlots) & 1u)) break;
+        more = b;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.slot_free[q]);
+    more = __shfl_sync(0xFFFFFFFFu, more, 0);
+    int nb = 0;
+    bool end = false;
+    uint64_t win[kLookbackBatch][kLookbackPerLane];
+#pragma unroll
+    for (int b = 0; b < kLookbackBatch; ++b) {
+      if (b > more || end) continue;
+      const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
+      const int q = int(ii % kPendSlots);
+      if (b > 0) mbar_test_wait(&sh.agg_ready[q], (ii / kPendSlots) & 1u);  // acquire for every lane
+      const ParkedMeta& pm = sh.parked[q];
+      if (pm.last == 2u) {
+        end = true;
+        continue;
+      }
+      if (pm.tile != pm.first) load_window(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
+      nb = b + 1;
+    }
+#pragma unroll
+    for (int b = 0; b < kLookbackBatch; ++b) {
+      if (b >= nb) continue;
+      const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
+      const int q = int(ii % kPendSlots);
+      const ParkedMeta pm = sh.parked[q];
+      const uint32_t prefix = resolve_prefix(a, pm.tile, pm.first, pm.agg, lane, win[b]);
+      if (lane == 0 && pm.last == 1u) a.counts_out[multi ? pm.tensor : 0] = uint64_t(prefix) + pm.agg;
+      for (uint32_t k = uint32_t(lane); k < pm.agg; k += 32) {
+        const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
+        const uint64_t pos = uint64_t(prefix) + k;
+        // pos < n always holds when every wait succeeded; the test keeps the
+        // writes of a launch that gave up on a wait inside the buffers
+        if (pos < pm.n) {
+          pm.idx[pos] = pm.base + (ent & 0xFFFFu);
+          pm.val[pos] = uint16_t(ent >> 16);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        // tiles are copied out in order: everything before this tile's end is free
+        __threadfence_block();
+        *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) = pm.ring_start + pm.agg;
+        mbar_arrive(&sh.slot_free[q]);
+      }
+    }
+    if (end) break;
+    i += uint32_t(nb * kEncLookbackWarps);
   }
 }
 
@@ -348,7 +415,7 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
                                              uint8_t* stages, uint32_t* ring, int tid, int lane,
                                              int warp) {
   // uniform across the compute threads
-  uint32_t posted = 0, freed = 0, ring_head = 0, ring_tail = 0;
+  uint32_t posted = 0, ring_head = 0;
   bool failed = false;  // this thread saw a wait give up
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kEncStages);
@@ -361,18 +428,16 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
     // ---- cast + compare: 4 consecutive elements per thread per round
     uint32_t nb[kEncRounds][2];  // new BF16 values, two per word (low half = lower index)
     uint32_t flags = 0;          // bit (j*4 + e): element e of round j changed
+    uint32_t nan_seen = 0;
     const float4* sm = reinterpret_cast<const float4*>(stages + size_t(s) * kStageBytes);
     const uint2* sp = reinterpret_cast<const uint2*>(stages + size_t(s) * kStageBytes + kStageMasterBytes);
-#pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
-      float4 mv;
-      uint2 pv;
+    // tail or unaligned tile: elements past the end read as +0 with a +0 view,
+    // which never counts as a change (len is 0 for the end marker)
+    auto load_round = [&](int j, float4& mv, uint2& pv) {
       if (m.mode == kModeBulk) {
         mv = sm[j * kEncThreads + tid];
         pv = sp[j * kEncThreads + tid];
       } else {
-        // tail or unaligned tile; elements past the end read as +0 with a +0
-        // view, which never counts as a change (len is 0 for the end marker)
         const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
         float mm[4];
         uint32_t pp[4];
@@ -385,18 +450,34 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
         mv = make_float4(mm[0], mm[1], mm[2], mm[3]);
         pv = make_uint2(pp[0] | (pp[1] << 16), pp[2] | (pp[3] << 16));
       }
-      uint32_t b01 = cvt_bf16x2_rn(mv.x, mv.y);
-      uint32_t b23 = cvt_bf16x2_rn(mv.z, mv.w);
-      if (any_nan2(mv.x, mv.y) || any_nan2(mv.z, mv.w)) {
-        b01 = canon_nan_pair(b01, mv.x, mv.y);
-        b23 = canon_nan_pair(b23, mv.z, mv.w);
+    };
+    auto compare_round = [&](int j, const uint2& pv) {
+      const uint32_t d01 = nb[j][0] ^ pv.x, d23 = nb[j][1] ^ pv.y;  // bitwise, two at a time
+      return uint32_t((d01 << 16) != 0u) | (uint32_t(d01 > 0xFFFFu) << 1) |
+             (uint32_t((d23 << 16) != 0u) << 2) | (uint32_t(d23 > 0xFFFFu) << 3);
+    };
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      float4 mv;
+      uint2 pv;
+      load_round(j, mv, pv);
+      nb[j][0] = cvt_bf16x2_rn(mv.x, mv.y);
+      nb[j][1] = cvt_bf16x2_rn(mv.z, mv.w);
+      nan_seen |= any_nan4(mv.x, mv.y, mv.z, mv.w);
+      flags |= compare_round(j, pv) << (4 * j);
+    }
+    if (nan_seen) {
+      // rare: redo this thread's rounds with NaN mapped to the canonical 0x7FC0
+      flags = 0;
+#pragma unroll
+      for (int j = 0; j < kEncRounds; ++j) {
+        float4 mv;
+        uint2 pv;
+        load_round(j, mv, pv);
+        nb[j][0] = canon_nan_pair(cvt_bf16x2_rn(mv.x, mv.y), mv.x, mv.y);
+        nb[j][1] = canon_nan_pair(cvt_bf16x2_rn(mv.z, mv.w), mv.z, mv.w);
+        flags |= compare_round(j, pv) << (4 * j);
       }
-      nb[j][0] = b01;
-      nb[j][1] = b23;
-      const uint32_t d01 = b01 ^ pv.x, d23 = b23 ^ pv.y;  // bitwise compare, two at a time
-      const uint32_t f = uint32_t((d01 & 0xFFFFu) != 0u) | (uint32_t(d01 > 0xFFFFu) << 1) |
-                         (uint32_t((d23 & 0xFFFFu) != 0u) << 2) | (uint32_t(d23 > 0xFFFFu) << 3);
-      flags |= f << (4 * j);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);  // this warp is done with stage s
@@ -463,36 +544,42 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
                                  a.epoch, agg));
     }
 
-    // ---- room for the tile: a free parked slot and agg ring entries; slots
-    // are reclaimed in order once their look-back warp has copied them out
-    bool reclaimed = false;
-    while (posted - freed >= uint32_t(kPendSlots) || ring_head + agg - ring_tail > uint32_t(kEncRing)) {
-      if (freed == posted) break;  // nothing left to reclaim (reachable only after an error)
-      const int fq = int(freed % kPendSlots);
-      failed |= !wait_or_flag(&sh.slot_free[fq], (freed / kPendSlots) & 1u, a);
-      ring_tail += sh.parked[fq].agg;
-      ++freed;
-      reclaimed = true;
-    }
-    if (reclaimed) compute_barrier();  // every thread has read the reclaimed slots
-
-    // ---- park the compacted tile: (local index | value << 16) per entry
-#pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
-      const uint32_t f = (flags >> (j * 4)) & 0xFu;
-      if (f == 0u) continue;
-      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
-      uint32_t r = ring_head + round_off[j];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if ((f >> e) & 1u) {
-          const uint32_t value = (nb[j][e >> 1] >> ((e & 1) * 16)) & 0xFFFFu;
-          ring[r & kRingMask] = (li + uint32_t(e)) | (value << 16);
-          ++r;
+    // ---- room for the tile: its parked slot must have been copied out (the
+    // look-back warp frees slots in order) and the ring must hold agg more
+    // entries. Each thread checks for itself; no CTA barrier is needed.
+    const int q = int(posted % kPendSlots);
+    if (posted >= uint32_t(kPendSlots))
+      failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kPendSlots) / kPendSlots) & 1u, a);
+    if (ring_head + agg - *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) > uint32_t(kEncRing)) {
+      const uint64_t t0 = global_timer_ns();
+      while (ring_head + agg - *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) > uint32_t(kEncRing)) {
+        __nanosleep(64);
+        if (global_timer_ns() - t0 > a.wait_limit_ns ||
+            (ld_volatile_u32(a.counters + 2) & kErrTimeout)) {
+          record_error(a.counters + 2, kErrTimeout);
+          failed = true;
+          break;
         }
       }
     }
-    const int q = int(posted % kPendSlots);
+
+    // ---- park the compacted tile: (local index | value << 16) per entry,
+    // visiting only the set flag bits
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      uint32_t f = (flags >> (j * 4)) & 0xFu;
+      if (f == 0u) continue;
+      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
+      uint32_t r = ring_head + round_off[j];
+      do {
+        const uint32_t e = uint32_t(__ffs(f)) - 1u;
+        f &= f - 1u;
+        const uint32_t word = (e & 2u) ? nb[j][1] : nb[j][0];
+        const uint32_t value = (e & 1u) ? (word >> 16) : (word & 0xFFFFu);
+        ring[r & kRingMask] = (li + e) | (value << 16);
+        ++r;
+      } while (f != 0u);
+    }
     if (tid == 0) {
       ParkedMeta pm;
       pm.tile = m.tile;
@@ -515,11 +602,8 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
   // no more tiles (the compute warps left the loop together): wait until
   // every parked tile is copied out, then send each look-back warp its end
   // marker
-  while (freed < posted) {
-    const int fq = int(freed % kPendSlots);
-    wait_or_flag(&sh.slot_free[fq], (freed / kPendSlots) & 1u, a);
-    ++freed;
-  }
+  for (uint32_t e = posted > uint32_t(kPendSlots) ? posted - kPendSlots : 0u; e < posted; ++e)
+    wait_or_flag(&sh.slot_free[e % kPendSlots], (e / kPendSlots) & 1u, a);
   compute_barrier();
   for (int k = 0; k < kEncLookbackWarps; ++k) {
     const uint32_t i = posted + uint32_t(k);
@@ -568,6 +652,7 @@ __global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
       sh.parked[q] = ParkedMeta{};
       sh.parked[q].last = 2u;
     }
+    sh.ring_tail = 0;
     fence_mbar_init();
   }
   __syncthreads();  // the last CTA-wide barrier: roles split below

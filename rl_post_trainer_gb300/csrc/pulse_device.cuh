@@ -48,6 +48,16 @@ __device__ __forceinline__ bool any_nan2(float a, float b) {
   return r != 0u;
 }
 
+// True if any of four inputs is NaN (two chained compares).
+__device__ __forceinline__ uint32_t any_nan4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .pred p;\n\tsetp.nan.f32 p, %1, %2;\n\tsetp.nan.or.f32 p, %3, %4, p;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
 // Replace the half of a packed BF16 pair whose FP32 source is NaN by the
 // canonical quiet NaN 0x7FC0 (rare path).
 __device__ __forceinline__ uint32_t canon_nan_pair(uint32_t b, float lo, float hi) {
@@ -144,14 +154,43 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// As mbar_try_wait, but lets the hardware suspend the waiting thread for up
+// to `hint_ns` nanoseconds (or until the phase completes) instead of
+// returning at once, so waiting warps do not take issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Bounded wait for phase `parity` of `bar`. Returns false if it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 15u && global_timer_ns() - t0 > limit_ns) return false;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return false;
 }

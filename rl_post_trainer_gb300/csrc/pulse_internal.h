@@ -30,18 +30,15 @@ constexpr int kEncTile = kEncThreads * kEncRounds * 4;  // 4096 elements
 #define PULSE_ENC_MIN_BLOCKS 3
 #endif
 #ifndef PULSE_ENC_LOOKBACK
-#define PULSE_ENC_LOOKBACK 8
+#define PULSE_ENC_LOOKBACK 2
 #endif
-#ifndef PULSE_ENC_BACKOFF_NS
-#define PULSE_ENC_BACKOFF_NS 128
-#endif
+
 constexpr int kEncStages = PULSE_ENC_STAGES;                // bulk-copy ring depth
 constexpr int kEncLookbackWarps = PULSE_ENC_LOOKBACK_WARPS;  // concurrent look-backs per CTA
 constexpr int kEncParked = PULSE_ENC_PARKED;                // parked tiles per CTA awaiting copy-out
 constexpr int kEncRing = PULSE_ENC_RING;                    // parked patch entries per CTA
 constexpr int kEncMinBlocks = PULSE_ENC_MIN_BLOCKS;          // resident CTAs per SM
 constexpr int kEncLookbackPerLane = PULSE_ENC_LOOKBACK;     // look-back words per lane per round trip
-constexpr uint32_t kEncBackoffNs = PULSE_ENC_BACKOFF_NS;    // sleep between polls of waiting helper warps
 constexpr int kEncBlockThreads = kEncThreads + 32 * (1 + kEncLookbackWarps);
 static_assert((kEncRing & (kEncRing - 1)) == 0 && kEncRing >= kEncTile,
               "the parked-entry ring is a power of two holding at least one full tile");
