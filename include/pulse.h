@@ -228,6 +228,39 @@ int pulse_xor_apply_multi(pulse_plan *plan, cudaStream_t stream);
 int pulse_plan_get_error(pulse_plan *plan);
 
 /*
+ * pulse_encode_noalloc -- pulse_encode for callers that must not allocate
+ * device memory. The pages describe no counterpart; this entry point exists
+ * for integration only.
+ *
+ * pulse_encode allocates its look-back scratch with cudaMalloc the first time
+ * a (device, stream) pair is seen and grows it for larger tensors. Callers
+ * that cannot allocate at that point -- engines that give all device memory
+ * to their own pool at start-up, runtimes that forbid allocation once serving
+ * has begun, code that must not let an allocation synchronise the device --
+ * use this variant: it computes exactly what pulse_encode computes, with the
+ * same arguments, but keeps its scratch in one fixed device array inside the
+ * library (512 KB + 256 bytes, held by every GPU that loads the library until
+ * the process exits) and calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *
+ *  - n may be at most PULSE_NOALLOC_MAX_ELEMS (2^28); larger n returns
+ *    PULSE_ERR_RANGE and launches nothing.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the array and it keeps the previous call's contents;
+ *    each call clears the counters it needs. Calls whose work may overlap on
+ *    the GPU (different streams without ordering) race on the array: order
+ *    them.
+ *  - Device-side errors are not kept for pulse_get_error: a wait that gave
+ *    up is reported as *count_out == UINT64_MAX (outputs invalid).
+ */
+#define PULSE_NOALLOC_MAX_ELEMS 268435456ull
+int pulse_encode_noalloc(const float *master_f32, uint16_t *prev_bf16, uint64_t n,
+                         uint32_t *idx_out, uint16_t *val_out, uint64_t *count_out,
+                         cudaStream_t stream);
+
+/*
  * Test hook for the look-back watchdog (not for production use). Runs
  * pulse_encode with a wait limit of `wait_limit_ns` nanoseconds while tile 0
  * is never processed, so tile 1 waits for a predecessor that never

@@ -9,6 +9,7 @@ from .pulse import (  # noqa: F401
     TensorSlot,
     apply,
     encode,
+    encode_noalloc,
     error_string,
     get_error,
     lib,

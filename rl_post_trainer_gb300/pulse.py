@@ -85,6 +85,7 @@ def lib():
             "pulse_xor_apply_multi": ([P, P], I),
             "pulse_plan_get_error": ([P], I),
             "pulse_debug_encode_orphan_tile": ([P, P, U64, P, P, P, U64, P], I),
+            "pulse_encode_noalloc": ([P, P, U64, P, P, P, P], I),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -158,6 +159,26 @@ def encode(master: torch.Tensor, prev: torch.Tensor, idx_out: Optional[torch.Ten
         st = lib().pulse_encode(_ptr(master), _ptr(prev), n, _ptr(idx_out), _ptr(val_out),
                                 _ptr(count_out), _stream(dev))
     _raise(st, "pulse_encode")
+    return idx_out, val_out, count_out
+
+
+def encode_noalloc(master: torch.Tensor, prev: torch.Tensor, idx_out: torch.Tensor,
+                   val_out: torch.Tensor, count_out: torch.Tensor):
+    """pulse_encode_noalloc: as encode, for callers that must not allocate device
+    memory (the library uses a fixed internal scratch array instead of a
+    cudaMalloc'd workspace). The caller passes every output buffer; n is at most
+    2^28. A count of 2^64 - 1 means a device wait gave up."""
+    _need(master, "master", (torch.float32,))
+    dev = master.device
+    n = master.numel()
+    _need(prev, "prev", _U16, dev, n)
+    _need(idx_out, "idx_out", (torch.int32, torch.uint32), dev, min_numel=n)
+    _need(val_out, "val_out", _U16, dev, min_numel=n)
+    _need(count_out, "count_out", (torch.int64, torch.uint64), dev, min_numel=1)
+    with torch.cuda.device(dev):
+        st = lib().pulse_encode_noalloc(_ptr(master), _ptr(prev), n, _ptr(idx_out), _ptr(val_out),
+                                        _ptr(count_out), _stream(dev))
+    _raise(st, "pulse_encode_noalloc")
     return idx_out, val_out, count_out
 
 
