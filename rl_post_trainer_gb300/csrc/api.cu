@@ -137,7 +137,7 @@ TensorDesc make_desc(const pulse_tensor& t, uint64_t tile_begin) {
 }
 
 int xor_grid(int device, uint64_t tiles) {
-  const uint64_t cap = uint64_t(sm_count(device)) * 8u;  // 8 x 256 threads per SM
+  const uint64_t cap = uint64_t(sm_count(device)) * uint64_t(2048 / kXorThreads);  // 2048 threads per SM
   return int(tiles < cap ? tiles : cap);
 }
 

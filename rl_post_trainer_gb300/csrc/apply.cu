@@ -8,7 +8,12 @@
 // The patch is read once as a stream (128-bit index loads, 64-bit value
 // loads, evict-first) and scattered with 2-byte stores; an encode patch is in
 // ascending index order, so one warp's stores land in a narrow window of w
-// and L2 merges them into whole sectors before they reach HBM.
+// and L2 merges them into whole sectors before they reach HBM. A 2-byte
+// store covers only part of a 32-byte sector, so L2 must fetch the rest of
+// the sector from HBM; the kernel first prefetches every target sector of
+// its entries into L2 (prefetch.global.L2) and only then stores, so those
+// fetches run as many parallel reads instead of write-miss fills (measured
+// on the 8B-parameter patch: 9.46 ms -> 6.69 ms).
 #include "pulse_device.cuh"
 #include "pulse_internal.h"
 
@@ -16,6 +21,15 @@ namespace pulse {
 namespace {
 
 constexpr int kGroups = kApplyPerThread / 4;  // 4-entry groups per thread per tile
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+template <bool CHECKED>
+__device__ __forceinline__ void prefetch1(const uint16_t* w, uint64_t n, uint32_t i) {
+  if (!CHECKED || uint64_t(i) < n) prefetch_l2(w + i);
+}
 
 template <bool CHECKED>
 __device__ __forceinline__ void scatter1(uint16_t* w, uint64_t n, uint32_t i, uint16_t v,
@@ -45,16 +59,30 @@ __device__ __forceinline__ void apply_tile(uint16_t* w, uint64_t n, const uint32
     }
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
+      prefetch1<CHECKED>(w, n, iv[g].x);
+      prefetch1<CHECKED>(w, n, iv[g].y);
+      prefetch1<CHECKED>(w, n, iv[g].z);
+      prefetch1<CHECKED>(w, n, iv[g].w);
+    }
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
       scatter1<CHECKED>(w, n, iv[g].x, uint16_t(vv[g].x & 0xFFFFu), err);
       scatter1<CHECKED>(w, n, iv[g].y, uint16_t(vv[g].x >> 16), err);
       scatter1<CHECKED>(w, n, iv[g].z, uint16_t(vv[g].y & 0xFFFFu), err);
       scatter1<CHECKED>(w, n, iv[g].w, uint16_t(vv[g].y >> 16), err);
     }
   } else {
+    uint32_t ii[kApplyPerThread];
 #pragma unroll
     for (int k = 0; k < kApplyPerThread; ++k) {
       const uint64_t j = base + uint64_t(k) * kApplyThreads + tid;
-      if (j < count) scatter1<CHECKED>(w, n, idx[j], val[j], err);
+      ii[k] = j < count ? idx[j] : 0u;
+      if (j < count) prefetch1<CHECKED>(w, n, ii[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < kApplyPerThread; ++k) {
+      const uint64_t j = base + uint64_t(k) * kApplyThreads + tid;
+      if (j < count) scatter1<CHECKED>(w, n, ii[k], val[j], err);
     }
   }
 }

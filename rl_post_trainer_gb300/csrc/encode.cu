@@ -343,7 +343,50 @@ __device__ __forceinline__ void producer_loop(const EncodeLaunch& a, EncodeShare
 // resolves its global offset, publishes its inclusive prefix, copies its
 // parked entries to the patch (entry k to position offset + k: contiguous,
 // coalesced stores) and frees the slot.
-constexpr int kLookbackBatch = 4;
+constexpr int kLookbackBatch = kEncLookbackBatch;
+
+// Copy a parked tile's entries to the patch: entry k goes to position
+// prefix + k. A head of up to 3 entries brings the position to a multiple of
+// 4; then each lane moves 4 consecutive entries with one 16-byte index store
+// and one 8-byte value store; the tail goes one entry at a time. Positions at
+// or past n are never written (they only arise after a wait gave up).
+__device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix,
+                                         const uint32_t* ring, int lane) {
+  const uint32_t agg = pm.agg;
+  const bool vec = (reinterpret_cast<uintptr_t>(pm.idx) % 16u == 0) &&
+                   (reinterpret_cast<uintptr_t>(pm.val) % 8u == 0) &&
+                   uint64_t(prefix) + agg <= pm.n;
+  uint32_t head = vec ? ((4u - (prefix & 3u)) & 3u) : agg;
+  if (head > agg) head = agg;
+  const uint32_t body = vec ? ((agg - head) & ~3u) : 0u;
+  for (uint32_t k = uint32_t(lane); k < head; k += 32) {
+    const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
+    const uint64_t pos = uint64_t(prefix) + k;
+    if (pos < pm.n) {
+      pm.idx[pos] = pm.base + (ent & 0xFFFFu);
+      pm.val[pos] = uint16_t(ent >> 16);
+    }
+  }
+  for (uint32_t k = head + uint32_t(lane) * 4u; k < head + body; k += 128u) {
+    uint32_t e[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) e[q] = ring[(pm.ring_start + k + uint32_t(q)) & kRingMask];
+    const uint64_t pos = uint64_t(prefix) + k;  // a multiple of 4
+    *reinterpret_cast<uint4*>(pm.idx + pos) =
+        make_uint4(pm.base + (e[0] & 0xFFFFu), pm.base + (e[1] & 0xFFFFu),
+                   pm.base + (e[2] & 0xFFFFu), pm.base + (e[3] & 0xFFFFu));
+    *reinterpret_cast<uint2*>(pm.val + pos) =
+        make_uint2((e[0] >> 16) | (e[1] & 0xFFFF0000u), (e[2] >> 16) | (e[3] & 0xFFFF0000u));
+  }
+  for (uint32_t k = head + body + uint32_t(lane); k < agg; k += 32) {
+    const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
+    const uint64_t pos = uint64_t(prefix) + k;
+    if (pos < pm.n) {
+      pm.idx[pos] = pm.base + (ent & 0xFFFFu);
+      pm.val[pos] = uint16_t(ent >> 16);
+    }
+  }
+}
 
 __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShared& sh,
                                               const uint32_t* ring, int w, int lane, bool multi) {
@@ -386,16 +429,7 @@ __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShare
       const ParkedMeta pm = sh.parked[q];
       const uint32_t prefix = resolve_prefix(a, pm.tile, pm.first, pm.agg, lane, win[b]);
       if (lane == 0 && pm.last == 1u) a.counts_out[multi ? pm.tensor : 0] = uint64_t(prefix) + pm.agg;
-      for (uint32_t k = uint32_t(lane); k < pm.agg; k += 32) {
-        const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
-        const uint64_t pos = uint64_t(prefix) + k;
-        // pos < n always holds when every wait succeeded; the test keeps the
-        // writes of a launch that gave up on a wait inside the buffers
-        if (pos < pm.n) {
-          pm.idx[pos] = pm.base + (ent & 0xFFFFu);
-          pm.val[pos] = uint16_t(ent >> 16);
-        }
-      }
+      copy_out(pm, prefix, ring, lane);
       __syncwarp();
       if (lane == 0) {
         // tiles are copied out in order: everything before this tile's end is free

@@ -32,6 +32,9 @@ constexpr int kEncTile = kEncThreads * kEncRounds * 4;  // 4096 elements
 #ifndef PULSE_ENC_LOOKBACK
 #define PULSE_ENC_LOOKBACK 2
 #endif
+#ifndef PULSE_ENC_LB_BATCH
+#define PULSE_ENC_LB_BATCH 4
+#endif
 
 constexpr int kEncStages = PULSE_ENC_STAGES;                // bulk-copy ring depth
 constexpr int kEncLookbackWarps = PULSE_ENC_LOOKBACK_WARPS;  // concurrent look-backs per CTA
@@ -39,6 +42,7 @@ constexpr int kEncParked = PULSE_ENC_PARKED;                // parked tiles per 
 constexpr int kEncRing = PULSE_ENC_RING;                    // parked patch entries per CTA
 constexpr int kEncMinBlocks = PULSE_ENC_MIN_BLOCKS;          // resident CTAs per SM
 constexpr int kEncLookbackPerLane = PULSE_ENC_LOOKBACK;     // look-back words per lane per round trip
+constexpr int kEncLookbackBatch = PULSE_ENC_LB_BATCH;        // parked tiles resolved per round trip
 constexpr int kEncBlockThreads = kEncThreads + 32 * (1 + kEncLookbackWarps);
 static_assert((kEncRing & (kEncRing - 1)) == 0 && kEncRing >= kEncTile,
               "the parked-entry ring is a power of two holding at least one full tile");
@@ -86,8 +90,14 @@ int encode_grid_size(int device);
 cudaError_t launch_encode(const EncodeLaunch& a, bool multi, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- apply
+#ifndef PULSE_APPLY_PER_THREAD
+#define PULSE_APPLY_PER_THREAD 8
+#endif
+#ifndef PULSE_XOR_ROUNDS
+#define PULSE_XOR_ROUNDS 8
+#endif
 constexpr int kApplyThreads = 256;
-constexpr int kApplyPerThread = 8;                          // entries per thread per tile
+constexpr int kApplyPerThread = PULSE_APPLY_PER_THREAD;     // entries per thread per tile
 constexpr int kApplyTile = kApplyThreads * kApplyPerThread;  // 2048 entries
 
 cudaError_t launch_apply(uint16_t* w, uint64_t n, bool checked, const uint32_t* idx,
@@ -98,10 +108,10 @@ cudaError_t launch_apply_multi(const TensorDesc* tensors, int ntensors,
                                int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- XOR
-constexpr int kXorThreads = 256;
-constexpr int kXorRounds = 4;
-constexpr int kXorTile = kXorThreads * kXorRounds * 4;  // 4096 elements (== kEncTile)
-static_assert(kXorTile == kEncTile, "XOR kernels reuse the encode tile table");
+constexpr int kXorRounds = PULSE_XOR_ROUNDS;            // 4-element loads in flight per thread
+constexpr int kXorTile = kEncTile;                        // XOR kernels reuse the encode tile table
+constexpr int kXorThreads = kXorTile / (4 * kXorRounds);  // one tile per CTA pass
+static_assert(kXorThreads * kXorRounds * 4 == kXorTile && kXorThreads >= 32, "tile geometry");
 
 cudaError_t launch_xor_mask(const TensorDesc& one, const TensorDesc* tensors,
                             const uint64_t* tile_begin, int ntensors, uint64_t total_tiles,
