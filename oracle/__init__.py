@@ -2,9 +2,9 @@
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg use it; the product library never does. The
-arithmetic lives in ``pulse_oracle.c`` (plain C, scalar loops, ascending
-index order); this module compiles it with gcc and wraps it for numpy arrays.
-It imports nothing from the CUDA package.
+arithmetic lives in ``pulse_oracle.c`` (BF16 view) and ``mx_oracle.c``
+(MXFP8 view): plain C, scalar loops, ascending index order; this module
+compiles them with gcc and wraps them for numpy arrays. It imports nothing from the CUDA package.
 """
 from .oracle import (  # noqa: F401
     build,
@@ -18,4 +18,12 @@ from .oracle import (  # noqa: F401
     apply_multi,
     xor_mask_multi,
     xor_apply_multi,
+    MX_BLOCK,
+    e4m3_rne,
+    mx_block_scale,
+    mx_blocks,
+    mxfp8_quantize,
+    mxfp8_encode,
+    apply_u8,
+    mxfp8_apply,
 )

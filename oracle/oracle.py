@@ -22,7 +22,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "pulse_oracle.c")
+_SRCS = [os.path.join(_HERE, "pulse_oracle.c"), os.path.join(_HERE, "mx_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
@@ -34,11 +34,11 @@ def build(force: bool = False) -> str:
     """Compile the oracle into a shared library with gcc -O2 (no CUDA)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+             or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(s) for s in _SRCS))
     if force or stale:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
         subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-Werror",
-                        "-shared", "-fPIC", "-o", tmp, _SRC], check=True)
+                        "-shared", "-fPIC", "-o", tmp, *_SRCS, "-lm"], check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -64,6 +64,16 @@ def _load():
             lib.oracle_xor_mask.restype = None
             lib.oracle_xor_apply.argtypes = [P, P, U64]
             lib.oracle_xor_apply.restype = None
+            lib.oracle_e4m3_rne.argtypes = [ctypes.c_double]
+            lib.oracle_e4m3_rne.restype = ctypes.c_uint8
+            lib.oracle_mx_block_scale.argtypes = [P, U64]
+            lib.oracle_mx_block_scale.restype = ctypes.c_uint8
+            lib.oracle_mxfp8_quantize.argtypes = [P, U64, P, P]
+            lib.oracle_mxfp8_quantize.restype = None
+            lib.oracle_mxfp8_encode.argtypes = [P, P, P, U64, P, P, P, P, P]
+            lib.oracle_mxfp8_encode.restype = None
+            lib.oracle_apply_u8.argtypes = [P, P, P, U64]
+            lib.oracle_apply_u8.restype = None
             _lib = lib
     return _lib
 
@@ -162,3 +172,75 @@ def xor_mask_multi(masters, prevs):
 def xor_apply_multi(ws, masks) -> None:
     for w, m in zip(ws, masks):
         xor_apply(w, m)
+
+
+# ------------------------------------------------- MXFP8 serving view
+
+MX_BLOCK = 32
+
+
+def e4m3_rne(y) -> int:
+    """E4M3 code of one finite value y (a Python float), RNE, clamped to 448."""
+    return int(_load().oracle_e4m3_rne(float(y)))
+
+
+def mx_block_scale(block: np.ndarray) -> int:
+    """E8M0 scale byte of one block of 1..32 FP32 values."""
+    _check(block, np.float32, "block")
+    if not 1 <= block.size <= MX_BLOCK:
+        raise ValueError("a block holds 1..32 values")
+    return int(_load().oracle_mx_block_scale(_ptr(block), block.size))
+
+
+def mx_blocks(n: int) -> int:
+    return (n + MX_BLOCK - 1) // MX_BLOCK
+
+
+def mxfp8_quantize(master: np.ndarray):
+    """Returns the MXFP8 view (codes uint8[n], scales uint8[ceil(n/32)])."""
+    _check(master, np.float32, "master")
+    n = master.size
+    codes = np.empty(n, dtype=np.uint8)
+    scales = np.empty(mx_blocks(n), dtype=np.uint8)
+    _load().oracle_mxfp8_quantize(_ptr(master), n, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def mxfp8_encode(master: np.ndarray, prev_codes: np.ndarray, prev_scales: np.ndarray):
+    """Returns (idx uint32, val uint8, sidx uint32, sval uint8); refreshes
+    ``prev_codes`` and ``prev_scales`` in place."""
+    _check(master, np.float32, "master")
+    _check(prev_codes, np.uint8, "prev_codes", writable=True)
+    _check(prev_scales, np.uint8, "prev_scales", writable=True)
+    n = master.size
+    if prev_codes.size != n or prev_scales.size != mx_blocks(n):
+        raise ValueError("view arrays do not match the master's length")
+    nb = mx_blocks(n)
+    idx = np.empty(max(n, 1), dtype=np.uint32)
+    val = np.empty(max(n, 1), dtype=np.uint8)
+    sidx = np.empty(max(nb, 1), dtype=np.uint32)
+    sval = np.empty(max(nb, 1), dtype=np.uint8)
+    counts = np.zeros(2, dtype=np.uint64)
+    _load().oracle_mxfp8_encode(_ptr(master), _ptr(prev_codes), _ptr(prev_scales), n,
+                                _ptr(idx), _ptr(val), _ptr(sidx), _ptr(sval), _ptr(counts))
+    k, ks = int(counts[0]), int(counts[1])
+    return idx[:k].copy(), val[:k].copy(), sidx[:ks].copy(), sval[:ks].copy()
+
+
+def apply_u8(w: np.ndarray, idx: np.ndarray, val: np.ndarray) -> None:
+    """w[idx[j]] = val[j] for j in order, in place (one byte segment)."""
+    _check(w, np.uint8, "w", writable=True)
+    _check(idx, np.uint32, "idx")
+    _check(val, np.uint8, "val")
+    if idx.size != val.size:
+        raise ValueError("idx and val differ in length")
+    if idx.size and int(idx.max()) >= w.size:
+        raise IndexError("patch index out of range")
+    _load().oracle_apply_u8(_ptr(w), _ptr(idx), _ptr(val), idx.size)
+
+
+def mxfp8_apply(codes: np.ndarray, scales: np.ndarray, patch) -> None:
+    """Apply both segments of an MXFP8 patch (idx, val, sidx, sval) in place."""
+    idx, val, sidx, sval = patch
+    apply_u8(codes, idx, val)
+    apply_u8(scales, sidx, sval)
