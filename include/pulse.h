@@ -22,6 +22,8 @@
  *          size as the weights, XOR-ed in place by the sampler) and
  *          "Pipeline'i GPU'lara tasimak" (one kernel launch covers the whole
  *          model, with tiling and address-map metadata prepared on the CPU).
+ *  [MX]    OCP "Microscaling Formats (MX) Specification" v1.0 (not one of
+ *          the pages): the MXFP8 format of the lower-precision view.
  *  [PPLX]  "Weight transfer for RL post-training in under 2 seconds"
  *          (Perplexity), section "Statyczny harmonogram": the transfer
  *          schedule is computed once at initialisation and replayed each step.
@@ -226,6 +228,106 @@ int pulse_xor_apply_multi(pulse_plan *plan, cudaStream_t stream);
 /* Synchronise the device, then return and clear the plan's device error word
  * (PULSE_OK, PULSE_ERR_TIMEOUT or PULSE_ERR_INDEX). */
 int pulse_plan_get_error(pulse_plan *plan);
+
+/* ------------------------------------------------------------------------
+ * MXFP8 serving view. [TALK] 13:06-14:40: rollouts are often served below
+ * BF16 (FP8, MXFP4, NVFP4); a plain float format hides updates below about
+ * theta / 2^(mantissa bits + 1), and with a shared group scale a scale
+ * change moves the whole group. [PULSE] "Potenziale Futuro": FP8 and MX
+ * views should be sparser still. [MX] OCP "Microscaling Formats (MX)
+ * Specification" v1.0 fixes the format (the pages do not):
+ *
+ *  - blocks of 32 consecutive elements of a tensor (the last block may be
+ *    shorter) share one E8M0 scale byte s, value 2^(s - 127);
+ *    s = floor(log2(max |v| over the block)) - 8 + 127, limited to
+ *    [0, 254]; a block whose maximum is 0 gets s = 0; a block holding a NaN
+ *    or an infinity gets s = 0xFF (NaN) and every code 0x7F;
+ *  - each element's code is the E4M3 encoding (OCP 8-bit float: bias 7, no
+ *    infinities, 0x7F/0xFF NaN, largest normal 448) of v / 2^(s - 127),
+ *    rounded to nearest even, magnitudes past 448 clamped to 448, sign kept
+ *    (-0 -> 0x80), subnormals kept.
+ *
+ * A view is two arrays: codes (n uint8) and scales (ceil(n / 32) uint8). An
+ * MXFP8 patch has two segments, each in ascending index order: changed codes
+ * (element index uint32, new code uint8) and changed scales (block index
+ * uint32, new scale uint8). n < 2^32 as everywhere.
+ * ---------------------------------------------------------------------- */
+#define PULSE_MX_BLOCK 32
+
+/*
+ * pulse_mx_quantize -- the MXFP8 view of one tensor (to initialise a
+ * trainer's previous view or a receiver).
+ *   master_f32  device, n floats;  codes_out device, n uint8;
+ *   scales_out  device, ceil(n / 32) uint8.
+ * n == 0 launches nothing. Errors: PULSE_ERR_INVALID, PULSE_ERR_RANGE,
+ * PULSE_ERR_CUDA.
+ */
+int pulse_mx_quantize(const float *master_f32, uint64_t n, uint8_t *codes_out,
+                      uint8_t *scales_out, cudaStream_t stream);
+
+/*
+ * pulse_mx_encode -- trainer-side encode of the MXFP8 view of one tensor.
+ * Computes the new view of master_f32, compares it bitwise with
+ * (prev_codes, prev_scales), writes both patch segments and refreshes both
+ * previous arrays in place:
+ *   idx_out[0..k)  / val_out[0..k)    changed codes (room for n entries)
+ *   sidx_out[0..ks) / sval_out[0..ks) changed scales (room for ceil(n/32))
+ *   counts_out     device, two uint64: {k, ks}
+ * master_f32, prev_codes and prev_scales 16-byte aligned take the fast
+ * path; any alignment is correct. Uses a library workspace per (device,
+ * stream), separate from pulse_encode's, allocated on first use; each call
+ * also clears that workspace's tile status words (one memset). n == 0 writes
+ * counts {0, 0}. Errors: PULSE_ERR_INVALID, PULSE_ERR_RANGE, PULSE_ERR_NOMEM,
+ * PULSE_ERR_CUDA; device: PULSE_ERR_TIMEOUT (pulse_get_error).
+ */
+int pulse_mx_encode(const float *master_f32, uint8_t *prev_codes, uint8_t *prev_scales,
+                    uint64_t n, uint32_t *idx_out, uint8_t *val_out, uint32_t *sidx_out,
+                    uint8_t *sval_out, uint64_t *counts_out, cudaStream_t stream);
+
+/*
+ * pulse_mx_apply -- sampler-side apply of both segments of an MXFP8 patch to
+ * a view of n elements: codes[idx[j]] = val[j] for j < count, then
+ * scales[sidx[j]] = sval[j] for j < scount (counts are HOST values). Entries
+ * past the view (idx >= n, sidx >= ceil(n/32)) are skipped and recorded as
+ * PULSE_ERR_INDEX for pulse_get_error(stream).
+ */
+int pulse_mx_apply(uint8_t *codes, uint8_t *scales, uint64_t n, const uint32_t *idx,
+                   const uint8_t *val, uint64_t count, const uint32_t *sidx,
+                   const uint8_t *sval, uint64_t scount, cudaStream_t stream);
+
+/*
+ * MXFP8 multi-tensor plans: as pulse_plan, one launch for the whole model.
+ * Fields an operation does not use may be NULL:
+ *   mx_encode_multi  master, prev_codes, prev_scales, idx, val, sidx, sval
+ *   mx_apply_multi   codes, scales, idx, val, sidx, sval
+ * Counts are 2 x ntensors uint64 in list order: {k_0, ks_0, k_1, ks_1, ...}.
+ * At most 8192 tensors per plan.
+ */
+typedef struct pulse_mx_tensor {
+    const float *master;   /* device, n floats (trainer) */
+    uint8_t *prev_codes;   /* device, n uint8 (trainer, in/out) */
+    uint8_t *prev_scales;  /* device, ceil(n/32) uint8 (trainer, in/out) */
+    uint8_t *codes;        /* device, n uint8 (sampler, in/out) */
+    uint8_t *scales;       /* device, ceil(n/32) uint8 (sampler, in/out) */
+    uint64_t n;            /* elements, < 2^32 */
+    uint32_t *idx;         /* device, room for n uint32 (code segment) */
+    uint8_t *val;          /* device, room for n uint8 */
+    uint32_t *sidx;        /* device, room for ceil(n/32) uint32 (scale segment) */
+    uint8_t *sval;         /* device, room for ceil(n/32) uint8 */
+} pulse_mx_tensor;
+
+typedef struct pulse_mx_plan pulse_mx_plan;
+
+int pulse_mx_plan_create(const pulse_mx_tensor *tensors, int ntensors, pulse_mx_plan **plan_out);
+int pulse_mx_plan_destroy(pulse_mx_plan *plan);
+int pulse_mx_plan_num_tensors(const pulse_mx_plan *plan);
+/* counts_out: device, 2 x ntensors uint64. */
+int pulse_mx_encode_multi(pulse_mx_plan *plan, uint64_t *counts_out, cudaStream_t stream);
+/* counts_host: HOST, 2 x ntensors uint64 (copied before return). */
+int pulse_mx_apply_multi(pulse_mx_plan *plan, const uint64_t *counts_host, cudaStream_t stream);
+/* counts_dev: DEVICE, 2 x ntensors uint64 (e.g. counts_out of pulse_mx_encode_multi). */
+int pulse_mx_apply_multi_device(pulse_mx_plan *plan, const uint64_t *counts_dev, cudaStream_t stream);
+int pulse_mx_plan_get_error(pulse_mx_plan *plan);
 
 /*
  * pulse_encode_noalloc -- pulse_encode for callers that must not allocate

@@ -4,6 +4,9 @@ The compute path is the CUDA library ``libpulse.so`` (C ABI in
 ``include/pulse.h``); :mod:`.pulse` is its thin Python binding.
 """
 from .pulse import (  # noqa: F401
+    MX_BLOCK,
+    MxPlan,
+    MxTensorSlot,
     Plan,
     PulseError,
     TensorSlot,
@@ -14,6 +17,10 @@ from .pulse import (  # noqa: F401
     get_error,
     lib,
     library_path,
+    mx_apply,
+    mx_blocks,
+    mx_encode,
+    mx_quantize,
     tile_elems,
     xor_apply,
     xor_mask,

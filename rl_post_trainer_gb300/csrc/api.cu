@@ -181,6 +181,62 @@ int encode_impl(const float* master, uint16_t* prev, uint64_t n, uint32_t* idx, 
   return cuda_status(launch_encode(a, false, grid, stream));
 }
 
+// ---- MXFP8 view: workspaces of the single-tensor calls. Their status words
+// use the packed layout without an epoch and are cleared before every
+// launch, so they are never shared with the BF16 calls' workspaces.
+std::map<std::pair<int, uintptr_t>, Workspace*> g_mx_ws;
+
+Workspace* stream_mx_workspace(int device, cudaStream_t stream) {
+  auto key = std::make_pair(device, reinterpret_cast<uintptr_t>(stream));
+  auto it = g_mx_ws.find(key);
+  if (it != g_mx_ws.end()) return it->second;
+  Workspace* ws = new (std::nothrow) Workspace();
+  if (ws == nullptr) return nullptr;
+  ws->device = device;
+  g_mx_ws[key] = ws;
+  return ws;
+}
+
+MxTensorDesc make_mx_desc(const pulse_mx_tensor& t, uint64_t tile_begin) {
+  MxTensorDesc d{};
+  d.master = t.master;
+  d.prev_codes = t.prev_codes;
+  d.prev_scales = t.prev_scales;
+  d.idx = t.idx;
+  d.val = t.val;
+  d.sidx = t.sidx;
+  d.sval = t.sval;
+  d.n = t.n;
+  d.tile_begin = tile_begin;
+  d.bulk_ok = (t.master && t.prev_codes && t.prev_scales && aligned(t.master, 16) &&
+               aligned(t.prev_codes, 16) && aligned(t.prev_scales, 16))
+                  ? 1u
+                  : 0u;
+  return d;
+}
+
+// Clear the status words of `tiles` tiles, then launch the MXFP8 encode.
+int launch_encode_mx_ws(MxLaunch& a, Workspace& ws, bool multi, int device, cudaStream_t stream) {
+  int st = workspace_reserve(ws, a.total_tiles, stream);
+  if (st != PULSE_OK) return st;
+  if (cudaMemsetAsync(ws.status, 0, a.total_tiles * sizeof(uint64_t), stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  a.status = ws.status;
+  a.counters = ws.counters;
+  a.epoch = 0;
+  const uint64_t cap = uint64_t(encode_mx_grid_size(device));
+  const int grid = int(a.total_tiles < cap ? a.total_tiles : cap);
+  return cuda_status(launch_encode_mx(a, multi, grid, stream));
+}
+
+int take_error_pair(Workspace* a, Workspace* b, cudaStream_t stream) {
+  const int ea = a ? workspace_take_error(*a, stream) : PULSE_OK;
+  const int eb = b ? workspace_take_error(*b, stream) : PULSE_OK;
+  if (ea == PULSE_ERR_CUDA || eb == PULSE_ERR_CUDA) return PULSE_ERR_CUDA;
+  if (ea == PULSE_ERR_TIMEOUT || eb == PULSE_ERR_TIMEOUT) return PULSE_ERR_TIMEOUT;
+  return ea != PULSE_OK ? ea : eb;
+}
+
 }  // namespace
 }  // namespace pulse
 
@@ -197,6 +253,19 @@ struct pulse_plan {
   TensorDesc* desc = nullptr;       // device copy
   uint64_t* tile_begin = nullptr;   // device, ntensors + 1
   uint64_t* counts = nullptr;       // device, ntensors (host-count apply staging)
+  Workspace ws;
+};
+
+struct pulse_mx_plan {
+  int device = 0;
+  int ntensors = 0;
+  uint64_t total_tiles = 0;
+  bool can_encode = false, can_apply = false;
+  std::vector<MxTensorDesc> host_desc;
+  MxTensorDesc* desc = nullptr;     // device copy
+  uint64_t* tile_begin = nullptr;   // device, ntensors + 1
+  ByteSegment* segs = nullptr;      // device, 2 x ntensors: codes then scales of each tensor
+  uint64_t* counts = nullptr;       // device, 2 x ntensors (host-count apply staging)
   Workspace ws;
 };
 
@@ -293,9 +362,11 @@ int pulse_get_error(cudaStream_t stream) {
   if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return PULSE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_ws_mu);
-  auto it = g_ws.find(std::make_pair(device, reinterpret_cast<uintptr_t>(stream)));
-  if (it == g_ws.end()) return PULSE_OK;
-  return workspace_take_error(*it->second, stream);
+  const auto key = std::make_pair(device, reinterpret_cast<uintptr_t>(stream));
+  auto it = g_ws.find(key);
+  auto mt = g_mx_ws.find(key);
+  return take_error_pair(it == g_ws.end() ? nullptr : it->second,
+                         mt == g_mx_ws.end() ? nullptr : mt->second, stream);
 }
 
 int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** plan_out) {
@@ -434,6 +505,191 @@ int pulse_xor_apply_multi(pulse_plan* plan, cudaStream_t stream) {
 }
 
 int pulse_plan_get_error(pulse_plan* plan) {
+  if (plan == nullptr) return PULSE_ERR_INVALID;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PULSE_ERR_CUDA;
+  return workspace_take_error(plan->ws, nullptr);
+}
+
+// ------------------------------------------------------------ MXFP8 view
+
+int pulse_mx_quantize(const float* master_f32, uint64_t n, uint8_t* codes_out, uint8_t* scales_out,
+                      cudaStream_t stream) {
+  if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (n == 0) return PULSE_OK;
+  if (master_f32 == nullptr || codes_out == nullptr || scales_out == nullptr) return PULSE_ERR_INVALID;
+  return cuda_status(launch_mx_quantize(master_f32, n, codes_out, scales_out, stream));
+}
+
+int pulse_mx_encode(const float* master_f32, uint8_t* prev_codes, uint8_t* prev_scales, uint64_t n,
+                    uint32_t* idx_out, uint8_t* val_out, uint32_t* sidx_out, uint8_t* sval_out,
+                    uint64_t* counts_out, cudaStream_t stream) {
+  if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (counts_out == nullptr) return PULSE_ERR_INVALID;
+  if (n > 0 && (master_f32 == nullptr || prev_codes == nullptr || prev_scales == nullptr ||
+                idx_out == nullptr || val_out == nullptr || sidx_out == nullptr || sval_out == nullptr))
+    return PULSE_ERR_INVALID;
+  if (n == 0) return cuda_status(cudaMemsetAsync(counts_out, 0, 2 * sizeof(uint64_t), stream));
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  pulse_mx_tensor t{};
+  t.master = master_f32;
+  t.prev_codes = prev_codes;
+  t.prev_scales = prev_scales;
+  t.n = n;
+  t.idx = idx_out;
+  t.val = val_out;
+  t.sidx = sidx_out;
+  t.sval = sval_out;
+  MxLaunch a{};
+  a.one = make_mx_desc(t, 0);
+  a.ntensors = 1;
+  a.total_tiles = div_up(n, kEncTile);
+  a.counts_out = counts_out;
+  a.first_ticket = 0;
+  a.wait_limit_ns = kDefaultWaitNs;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  Workspace* ws = stream_mx_workspace(device, stream);
+  if (ws == nullptr) return PULSE_ERR_NOMEM;
+  return launch_encode_mx_ws(a, *ws, false, device, stream);
+}
+
+int pulse_mx_apply(uint8_t* codes, uint8_t* scales, uint64_t n, const uint32_t* idx,
+                   const uint8_t* val, uint64_t count, const uint32_t* sidx, const uint8_t* sval,
+                   uint64_t scount, cudaStream_t stream) {
+  if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (count == 0 && scount == 0) return PULSE_OK;
+  if (count > 0 && (codes == nullptr || idx == nullptr || val == nullptr)) return PULSE_ERR_INVALID;
+  if (scount > 0 && (scales == nullptr || sidx == nullptr || sval == nullptr)) return PULSE_ERR_INVALID;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  uint32_t* err = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    Workspace* ws = stream_mx_workspace(device, stream);
+    if (ws == nullptr) return PULSE_ERR_NOMEM;
+    const int st = workspace_reserve(*ws, 0, stream);
+    if (st != PULSE_OK) return st;
+    err = ws->counters + 2;
+  }
+  if (launch_apply_u8(codes, n, true, idx, val, count, err, stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  return cuda_status(
+      launch_apply_u8(scales, div_up(n, kMxBlock), true, sidx, sval, scount, err, stream));
+}
+
+int pulse_mx_plan_create(const pulse_mx_tensor* tensors, int ntensors, pulse_mx_plan** plan_out) {
+  if (plan_out == nullptr) return PULSE_ERR_INVALID;
+  *plan_out = nullptr;
+  if (tensors == nullptr || ntensors < 1 || ntensors > kMaxTensorsPerApplyLaunch / 2)
+    return PULSE_ERR_INVALID;
+  pulse_mx_plan* p = new (std::nothrow) pulse_mx_plan();
+  if (p == nullptr) return PULSE_ERR_NOMEM;
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return PULSE_ERR_CUDA;
+  }
+  p->ntensors = ntensors;
+  p->can_encode = p->can_apply = true;
+  std::vector<uint64_t> tb(size_t(ntensors) + 1, 0);
+  std::vector<ByteSegment> segs(2 * size_t(ntensors));
+  p->host_desc.reserve(size_t(ntensors));
+  uint64_t tiles = 0;
+  for (int i = 0; i < ntensors; ++i) {
+    const pulse_mx_tensor& t = tensors[i];
+    if (t.n >= kMaxElems + 1) {
+      delete p;
+      return PULSE_ERR_RANGE;
+    }
+    tb[size_t(i)] = tiles;
+    p->host_desc.push_back(make_mx_desc(t, tiles));
+    tiles += div_up(t.n, kEncTile);
+    segs[2 * size_t(i)] = ByteSegment{t.codes, t.idx, t.val, t.n};
+    segs[2 * size_t(i) + 1] = ByteSegment{t.scales, t.sidx, t.sval, div_up(t.n, kMxBlock)};
+    if (t.n > 0) {
+      p->can_encode = p->can_encode && t.master && t.prev_codes && t.prev_scales && t.idx &&
+                      t.val && t.sidx && t.sval;
+      p->can_apply = p->can_apply && t.codes && t.scales && t.idx && t.val && t.sidx && t.sval;
+    }
+  }
+  tb[size_t(ntensors)] = tiles;
+  if (tiles > kMaxTiles) {
+    delete p;
+    return PULSE_ERR_RANGE;
+  }
+  p->total_tiles = tiles;
+  const size_t desc_bytes = sizeof(MxTensorDesc) * size_t(ntensors);
+  const size_t tb_bytes = sizeof(uint64_t) * (size_t(ntensors) + 1);
+  const size_t seg_bytes = sizeof(ByteSegment) * segs.size();
+  const size_t cnt_bytes = sizeof(uint64_t) * segs.size();
+  int st = PULSE_OK;
+  if (cudaMalloc(&p->desc, desc_bytes) != cudaSuccess ||
+      cudaMalloc(&p->tile_begin, tb_bytes) != cudaSuccess ||
+      cudaMalloc(&p->segs, seg_bytes) != cudaSuccess ||
+      cudaMalloc(&p->counts, cnt_bytes) != cudaSuccess) {
+    st = PULSE_ERR_NOMEM;
+  } else if (cudaMemcpy(p->desc, p->host_desc.data(), desc_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+             cudaMemcpy(p->tile_begin, tb.data(), tb_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+             cudaMemcpy(p->segs, segs.data(), seg_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+             cudaMemset(p->counts, 0, cnt_bytes) != cudaSuccess) {
+    st = PULSE_ERR_CUDA;
+  } else {
+    st = workspace_reserve(p->ws, tiles, nullptr);
+    if (st == PULSE_OK && cudaDeviceSynchronize() != cudaSuccess) st = PULSE_ERR_CUDA;
+  }
+  if (st != PULSE_OK) {
+    pulse_mx_plan_destroy(p);
+    return st;
+  }
+  *plan_out = p;
+  return PULSE_OK;
+}
+
+int pulse_mx_plan_destroy(pulse_mx_plan* plan) {
+  if (plan == nullptr) return PULSE_OK;
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (plan->desc) cudaFree(plan->desc);
+  if (plan->tile_begin) cudaFree(plan->tile_begin);
+  if (plan->segs) cudaFree(plan->segs);
+  if (plan->counts) cudaFree(plan->counts);
+  workspace_free(plan->ws);
+  delete plan;
+  return cuda_status(e);
+}
+
+int pulse_mx_plan_num_tensors(const pulse_mx_plan* plan) { return plan ? plan->ntensors : 0; }
+
+int pulse_mx_encode_multi(pulse_mx_plan* plan, uint64_t* counts_out, cudaStream_t stream) {
+  if (plan == nullptr || counts_out == nullptr || !plan->can_encode) return PULSE_ERR_INVALID;
+  if (plan->total_tiles == 0)
+    return cuda_status(
+        cudaMemsetAsync(counts_out, 0, 2 * sizeof(uint64_t) * size_t(plan->ntensors), stream));
+  MxLaunch a{};
+  a.tensors = plan->desc;
+  a.tile_begin = plan->tile_begin;
+  a.ntensors = plan->ntensors;
+  a.total_tiles = plan->total_tiles;
+  a.counts_out = counts_out;
+  a.first_ticket = 0;
+  a.wait_limit_ns = kDefaultWaitNs;
+  return launch_encode_mx_ws(a, plan->ws, true, plan->device, stream);
+}
+
+int pulse_mx_apply_multi_device(pulse_mx_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {
+  if (plan == nullptr || counts_dev == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
+  const int grid = sm_count(plan->device) * 8;
+  return cuda_status(launch_apply_u8_multi(plan->segs, 2 * plan->ntensors, counts_dev,
+                                           plan->ws.counters + 2, grid, stream));
+}
+
+int pulse_mx_apply_multi(pulse_mx_plan* plan, const uint64_t* counts_host, cudaStream_t stream) {
+  if (plan == nullptr || counts_host == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
+  if (cudaMemcpyAsync(plan->counts, counts_host, 2 * sizeof(uint64_t) * size_t(plan->ntensors),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  return pulse_mx_apply_multi_device(plan, plan->counts, stream);
+}
+
+int pulse_mx_plan_get_error(pulse_mx_plan* plan) {
   if (plan == nullptr) return PULSE_ERR_INVALID;
   if (cudaDeviceSynchronize() != cudaSuccess) return PULSE_ERR_CUDA;
   return workspace_take_error(plan->ws, nullptr);

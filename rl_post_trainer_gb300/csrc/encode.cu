@@ -30,32 +30,17 @@
 //    compute warps stream on.
 // Every wait is bounded; a wait that gives up records PULSE_ERR_TIMEOUT and
 // the kernel still finishes with all writes inside the caller's buffers.
-#include "pulse_device.cuh"
-#include "pulse_internal.h"
+#include "encode_common.cuh"
 
 namespace pulse {
 namespace {
 
-constexpr int kWarps = kEncThreads / 32;             // compute warps
-constexpr int kProducerWarp = kWarps;
-constexpr int kFirstLookbackWarp = kWarps + 1;
-static_assert(kEncRounds == 4, "four rounds pack into the bytes of one word");
-static_assert(kWarps == 8, "the cross-warp scan runs over 8 lanes");
-constexpr int kLookbackPerLane = kEncLookbackPerLane;
-// parked-tile slots: a multiple of the look-back warps (slot p is always
-// handled by look-back warp p % kEncLookbackWarps), at least kEncParked
-constexpr int kPendSlots =
-    ((kEncParked > kEncLookbackWarps ? kEncParked : kEncLookbackWarps) + kEncLookbackWarps - 1) /
-    kEncLookbackWarps * kEncLookbackWarps;
-constexpr int kComputeBarrier = 1;                   // named barrier of the compute warps
-constexpr uint32_t kRingMask = uint32_t(kEncRing) - 1u;
+using namespace enc;
 
 constexpr uint32_t kStageMasterBytes = kEncTile * 4;
 constexpr uint32_t kStagePrevBytes = kEncTile * 2;
 constexpr uint32_t kStageBytes = kStageMasterBytes + kStagePrevBytes;
 constexpr size_t kDynSmem = size_t(kEncStages) * kStageBytes + size_t(kEncRing) * 4 + 128;
-
-enum : uint32_t { kModeEnd = 0, kModeBulk = 1, kModeGeneric = 2 };
 
 // Everything the compute warps need about a tile, written by the producer
 // (which reads the tensor descriptor anyway) so the compute path touches no
@@ -99,162 +84,10 @@ struct __align__(16) EncodeShared {
 };
 static_assert(kEncLookbackWarps == 1, "parked tiles are freed in order by one look-back warp");
 
-__device__ __forceinline__ int find_tensor(const uint64_t* tile_begin, int ntensors, uint64_t g) {
-  // largest t with tile_begin[t] <= g; tile_begin[ntensors] = total > g
-  int lo = 0, hi = ntensors;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(tile_begin + mid) <= g) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 template <bool MULTI>
 __device__ __forceinline__ const TensorDesc& desc_of(const EncodeLaunch& a, uint32_t t) {
   if constexpr (MULTI) return a.tensors[t];
   else return a.one;
-}
-
-__device__ __forceinline__ void bulk_g2s_plain(void* smem_dst, const void* gmem_src,
-                                               uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(smem_dst)),
-      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void compute_barrier() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kComputeBarrier), "n"(kEncThreads) : "memory");
-}
-
-// Named barrier of the compute warps that also ORs a predicate across them:
-// every loop-exit decision goes through it, so the 8 compute warps always
-// leave their loop together and no named barrier is ever left short.
-__device__ __forceinline__ bool compute_barrier_or(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(uint32_t(v)), "n"(kComputeBarrier), "n"(kEncThreads)
-      : "memory");
-  return r != 0;
-}
-
-// Bounded wait for the producer and look-back warps. The hardware suspends
-// the waiting warp between tries, so waiting warps leave the issue slots to
-// the compute warps. Same failure contract as wait_or_flag below.
-__device__ __forceinline__ bool helper_wait(uint64_t* bar, uint32_t parity, const EncodeLaunch& a) {
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 0; it < (1u << 28); ++it) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if ((it & 15u) == 15u) {
-      if (ld_volatile_u32(a.counters + 2) & kErrTimeout) return false;
-      if (global_timer_ns() - t0 > a.wait_limit_ns) break;
-    }
-  }
-  record_error(a.counters + 2, kErrTimeout);
-  return false;
-}
-
-// Bounded mbarrier wait. Returns false if it gave up (the error is recorded);
-// once any wait of the launch has given up, later waits give up at once, so
-// a failed launch ends quickly. Callers stop after a failed wait; every
-// write they may still make stays in bounds.
-__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, const EncodeLaunch& a) {
-  // the hardware suspends the warp for up to 20 us per try
-#pragma unroll 1
-  for (int i = 0; i < 4; ++i)
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-  if (ld_volatile_u32(a.counters + 2) & kErrTimeout) return false;
-  if (mbar_wait_bounded(bar, parity, a.wait_limit_ns)) return true;
-  record_error(a.counters + 2, kErrTimeout);
-  return false;
-}
-
-__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
-
-// Look-back warp: exclusive prefix of tile g within its tensor (its own
-// aggregate is already published). Reads kLookbackPerLane x 32 predecessor
-// words per round trip, nearest first; waits only on unpublished words that
-// lie before the nearest inclusive prefix; publishes g's inclusive prefix.
-// Issue the loads of one look-back window: the kLookbackPerLane x 32 status
-// words before `pos`, nearest first; words before the tensor's first tile
-// read as an inclusive prefix of 0.
-__device__ __forceinline__ void load_window(const EncodeLaunch& a, int64_t pos, uint64_t first,
-                                            int lane, uint64_t (&w)[kLookbackPerLane]) {
-#pragma unroll
-  for (int q = 0; q < kLookbackPerLane; ++q) {
-    const int64_t tile = pos - (lane * kLookbackPerLane + q);
-    w[q] = tile >= int64_t(first) ? ld_relaxed_u64(a.status + tile)
-                                  : make_status(kFlagPrefix, a.epoch, 0u);
-  }
-}
-
-// `w` holds the first window (load_window at g - 1), already in flight.
-__device__ __forceinline__ uint32_t resolve_prefix(const EncodeLaunch& a, uint64_t g,
-                                                   uint64_t first, uint32_t agg, int lane,
-                                                   uint64_t (&w)[kLookbackPerLane]) {
-  uint64_t* st = a.status;
-  if (g == first) return 0u;  // published as an inclusive prefix already
-  constexpr int kNone = 1 << 30;
-  uint32_t prefix = 0;
-  int64_t pos = int64_t(g) - 1;
-  bool gave_up = false;
-  for (bool first_window = true;; first_window = false) {
-    if (!first_window) load_window(a, pos, first, lane, w);
-    int dp = kNone;  // window distance of the nearest inclusive prefix
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t spin = 0;; ++spin) {
-      int my_p = kNone, my_x = kNone;
-#pragma unroll
-      for (int q = kLookbackPerLane - 1; q >= 0; --q) {
-        const uint32_t f = status_flag(w[q], a.epoch);
-        if (f == kFlagPrefix) my_p = lane * kLookbackPerLane + q;
-        if (f == 0u) my_x = lane * kLookbackPerLane + q;
-      }
-      dp = __reduce_min_sync(0xFFFFFFFFu, my_p);
-      const int dx = __reduce_min_sync(0xFFFFFFFFu, my_x);
-      if (dx == kNone || dx > dp) break;  // every word up to the nearest prefix is published
-      if (gave_up || (spin & 63u) == 63u) {
-        const bool late = gave_up || spin > (1u << 26) ||
-                          global_timer_ns() - t0 > a.wait_limit_ns ||
-                          (ld_volatile_u32(a.counters + 2) & kErrTimeout);
-        if (__any_sync(0xFFFFFFFFu, late)) {
-          // give up: unpublished words read as an inclusive prefix of 0, which
-          // keeps every offset at or below the true one (writes stay in bounds)
-          if (lane == 0) record_error(a.counters + 2, kErrTimeout);
-          gave_up = true;
-#pragma unroll
-          for (int q = 0; q < kLookbackPerLane; ++q)
-            if (status_flag(w[q], a.epoch) == 0u) w[q] = make_status(kFlagPrefix, a.epoch, 0u);
-          continue;
-        }
-      }
-      __nanosleep(32);
-#pragma unroll
-      for (int q = 0; q < kLookbackPerLane; ++q) {
-        if (status_flag(w[q], a.epoch) == 0u)
-          w[q] = ld_relaxed_u64(st + (pos - (lane * kLookbackPerLane + q)));
-      }
-    }
-    uint32_t sum = 0;
-#pragma unroll
-    for (int q = 0; q < kLookbackPerLane; ++q)
-      if (lane * kLookbackPerLane + q <= dp) sum += status_value(w[q]);
-    prefix += warp_sum(sum);
-    if (dp != kNone) break;
-    pos -= 32 * kLookbackPerLane;
-  }
-  if (lane == 0) st_relaxed_u64(st + g, make_status(kFlagPrefix, a.epoch, prefix + agg));
-  return prefix;
 }
 
 // ------------------------------------------------------------ producer warp
@@ -343,8 +176,6 @@ __device__ __forceinline__ void producer_loop(const EncodeLaunch& a, EncodeShare
 // resolves its global offset, publishes its inclusive prefix, copies its
 // parked entries to the patch (entry k to position offset + k: contiguous,
 // coalesced stores) and frees the slot.
-constexpr int kLookbackBatch = kEncLookbackBatch;
-
 // Copy a parked tile's entries to the patch: entry k goes to position
 // prefix + k. A head of up to 3 entries brings the position to a multiple of
 // 4; then each lane moves 4 consecutive entries with one 16-byte index store
@@ -418,7 +249,7 @@ __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShare
         end = true;
         continue;
       }
-      if (pm.tile != pm.first) load_window(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
+      if (pm.tile != pm.first) load_window<StatusEpoch>(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
       nb = b + 1;
     }
 #pragma unroll
@@ -427,7 +258,7 @@ __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShare
       const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
       const int q = int(ii % kPendSlots);
       const ParkedMeta pm = sh.parked[q];
-      const uint32_t prefix = resolve_prefix(a, pm.tile, pm.first, pm.agg, lane, win[b]);
+      const uint32_t prefix = resolve_prefix<StatusEpoch>(a, pm.tile, pm.first, pm.agg, lane, win[b]);
       if (lane == 0 && pm.last == 1u) a.counts_out[multi ? pm.tensor : 0] = uint64_t(prefix) + pm.agg;
       copy_out(pm, prefix, ring, lane);
       __syncwarp();

@@ -1,0 +1,689 @@
+// encode_mx.cu -- the MXFP8 serving view: quantize, and the fused
+// quantize + compare + order-preserving compaction of what changed.
+//
+// Lower-precision serving ("Taking Reinforcement Learning Cross Datacenter",
+// talk 13:06-14:40: rollouts served in FP8 / MXFP4 / NVFP4; a plain float
+// format hides updates below about theta / 2^(mantissa bits + 1); with a
+// shared group scale, a scale change moves a whole group) and the PULSE
+// summary ("Potenziale Futuro": FP8 and MX views should be sparser still).
+// The view is MXFP8 as the OCP Microscaling (MX) v1.0 specification defines
+// it, the block-scaled FP8 that Blackwell tensor cores read directly: blocks
+// of 32 consecutive elements share one E8M0 scale 2^e with
+// e = floor(log2 max|v|) - 8 (limited to [-127, 127]); each element is the
+// E4M3 encoding (round to nearest even, magnitudes past 448 clamped to 448)
+// of v / 2^e. A block holding a NaN or an infinity gets the NaN scale 0xFF
+// and the code 0x7F everywhere; an all-zero block gets the scale 2^-127.
+//
+// The patch has two segments per tensor, each in ascending index order:
+// changed codes (element index, new code) and changed scales (block index,
+// new scale). Encode refreshes both previous arrays in place.
+//
+// Kernel: the BF16 encode's persistent warp-specialized CTA (producer warp
+// with bulk copies into a 2-stage ring, 8 compute warps, one look-back warp
+// that resolves parked tiles with a decoupled look-back and copies them out).
+// Per 4096-element tile the compute warps handle 4 consecutive elements per
+// thread per round, so one 32-element block spans 8 consecutive lanes: the
+// block maximum is 3 butterfly shuffles, the scale is read from the maximum's
+// exponent bits, and the elements are scaled by an exact power of two and
+// converted with the hardware's saturating E4M3 convert. The tile's status
+// word carries both counts (codes in the low 32 bits, scales above), so one
+// look-back yields both segment offsets.
+#include "encode_common.cuh"
+
+namespace pulse {
+namespace {
+
+using namespace enc;
+
+constexpr int kTileBlocks = kEncTile / kMxBlock;                   // 128
+constexpr uint32_t kStageMasterBytes = kEncTile * 4;               // 16 KB
+constexpr uint32_t kStageCodeBytes = kEncTile;                     // 4 KB
+constexpr uint32_t kStageScaleBytes = kTileBlocks;                 // 128 B
+constexpr uint32_t kStageBytes = kStageMasterBytes + kStageCodeBytes + kStageScaleBytes;
+static_assert(kStageBytes % 128 == 0, "stages stay 128-byte aligned");
+constexpr size_t kDynSmem = size_t(kEncStages) * kStageBytes + size_t(kEncRing) * 4 + 128;
+static_assert(kEncTile % (kMxBlock * 8) == 0, "a warp round covers whole blocks");
+
+// ---------------------------------------------------------- MXFP8 arithmetic
+
+// Largest |v| bit pattern (sign cleared) over the 32-element block this
+// thread's 4 elements belong to: the block spans lanes (lane & ~7) .. +7.
+// For non-NaN values the unsigned order of these patterns is the order of
+// the magnitudes; any NaN makes the result exceed 0x7F800000. All 32 lanes
+// must call.
+__device__ __forceinline__ uint32_t block_amax_bits(const float4& v) {
+  uint32_t a = max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+                   max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu));
+  a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+  a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+  a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+  return a;
+}
+
+// E8M0 scale byte from the block maximum: with E the maximum's biased FP32
+// exponent, floor(log2 max) - 8 + 127 = E - 135 + 127 = E - 8 for normal
+// maxima; zero and subnormal maxima (E = 0), and normals with E <= 8, give
+// an exponent at or below -127, which is raised to -127 (byte 0). Any
+// infinity or NaN in the block gives the NaN scale 0xFF.
+__device__ __forceinline__ uint32_t mx_scale_byte(uint32_t amax_bits) {
+  if (amax_bits >= 0x7F800000u) return 0xFFu;
+  const uint32_t e = amax_bits >> 23;
+  return e > 8u ? e - 8u : 0u;
+}
+
+// Saturating round-to-nearest-even FP32 -> E4M3 of two values; `hi` lands in
+// the upper byte of the result.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Codes of 4 consecutive elements (element 0 in the low byte) under scale
+// byte `scale`. The factor 2^(127 - scale) is a normal FP32 power of two
+// (scale <= 246), so each product is exact unless it falls below 2^-126, and
+// such a value rounds to a zero code either way.
+__device__ __forceinline__ uint32_t mx_codes4(const float4& v, uint32_t scale) {
+  if (scale == 0xFFu) return 0x7F7F7F7Fu;
+  const float f = __uint_as_float((254u - scale) << 23);
+  return cvt_e4m3x2(__fmul_rn(v.y, f), __fmul_rn(v.x, f)) |
+         (cvt_e4m3x2(__fmul_rn(v.w, f), __fmul_rn(v.z, f)) << 16);
+}
+
+// One bit per byte of a and b that differs (bit e for byte e).
+__device__ __forceinline__ uint32_t byte_diff_bits(uint32_t a, uint32_t b) {
+  const uint32_t m = __vcmpne4(a, b);
+  return ((m >> 7) & 1u) | ((m >> 14) & 2u) | ((m >> 21) & 4u) | ((m >> 28) & 8u);
+}
+
+// -------------------------------------------------------------- shared state
+
+struct StageMeta {
+  uint32_t tile;
+  uint32_t tensor;
+  uint32_t mode;
+  uint32_t len;  // elements in the tile
+  uint64_t base;
+  uint64_t first;
+  uint64_t n;
+  const float* master;
+  uint8_t* prev_codes;
+  uint8_t* prev_scales;
+  uint32_t* idx;
+  uint8_t* val;
+  uint32_t* sidx;
+  uint8_t* sval;
+};
+
+struct ParkedMeta {
+  uint32_t tile;
+  uint32_t tensor;
+  uint32_t agg_c;  // changed codes in the tile
+  uint32_t agg_s;  // changed scales in the tile
+  uint32_t last;   // 1: last tile of its tensor; 2: no more tiles for this look-back warp
+  uint32_t ring_start;
+  uint64_t first;
+  uint64_t n;
+  uint64_t base;
+  uint32_t* idx;
+  uint8_t* val;
+  uint32_t* sidx;
+  uint8_t* sval;
+};
+
+struct __align__(16) MxShared {
+  uint64_t full[kEncStages];
+  uint64_t empty[kEncStages];
+  uint64_t agg_ready[kPendSlots];
+  uint64_t slot_free[kPendSlots];
+  StageMeta meta[kEncStages];
+  ParkedMeta parked[kPendSlots];
+  uint32_t warp_tot[2][kWarps];   // per warp: changed codes per round, one byte each
+  uint32_t warp_stot[2][kWarps];  // per warp: changed scales per round, one byte each
+  uint32_t ring_tail;
+  uint16_t sring[kPendSlots][kTileBlocks];  // parked scale entries: block | scale << 8
+};
+static_assert(kEncLookbackWarps == 1, "parked tiles are freed in order by one look-back warp");
+
+// ------------------------------------------------------------ producer warp
+template <bool MULTI>
+__device__ __forceinline__ void producer_loop(const MxLaunch& a, MxShared& sh, uint8_t* stages) {
+  const uint64_t pol_stream = l2_policy_evict_first();
+  uint32_t fills_done = 0;
+  uint32_t ticket = atomicAdd(a.counters + 0, 1u) + a.first_ticket;
+  uint32_t cur_t = 0;
+  uint64_t cur_begin = 1, cur_end = 0;
+  MxTensorDesc d = a.one;
+  for (uint32_t it = 0;; ++it) {
+    const int s = int(it % kEncStages);
+    const bool end = ticket >= a.total_tiles;
+    const uint32_t next = end ? ticket : atomicAdd(a.counters + 0, 1u) + a.first_ticket;
+    if (it >= uint32_t(kEncStages) && !helper_wait(&sh.empty[s], ((it / kEncStages) - 1) & 1u, a))
+      break;
+    fills_done = it + 1;
+    StageMeta m{};
+    m.tile = ticket;
+    if (end) {
+      m.mode = kModeEnd;
+      sh.meta[s] = m;
+      mbar_arrive(&sh.full[s]);
+      break;
+    }
+    if constexpr (MULTI) {
+      if (uint64_t(ticket) < cur_begin || uint64_t(ticket) >= cur_end) {
+        cur_t = uint32_t(find_tensor(a.tile_begin, a.ntensors, ticket));
+        d = a.tensors[cur_t];
+        cur_begin = d.tile_begin;
+        cur_end = __ldg(a.tile_begin + cur_t + 1);
+      }
+    }
+    const uint64_t base = (uint64_t(ticket) - d.tile_begin) * kEncTile;
+    const uint64_t len = d.n - base < uint64_t(kEncTile) ? d.n - base : uint64_t(kEncTile);
+    m.tensor = cur_t;
+    m.len = uint32_t(len);
+    m.base = base;
+    m.first = d.tile_begin;
+    m.n = d.n;
+    m.master = d.master;
+    m.prev_codes = d.prev_codes;
+    m.prev_scales = d.prev_scales;
+    m.idx = d.idx;
+    m.val = d.val;
+    m.sidx = d.sidx;
+    m.sval = d.sval;
+    if (d.bulk_ok && len == uint64_t(kEncTile)) {
+      m.mode = kModeBulk;
+      sh.meta[s] = m;
+      uint8_t* st = stages + size_t(s) * kStageBytes;
+      mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
+      bulk_g2s(st, d.master + base, kStageMasterBytes, &sh.full[s], pol_stream);
+      bulk_g2s_plain(st + kStageMasterBytes, d.prev_codes + base, kStageCodeBytes, &sh.full[s]);
+      bulk_g2s_plain(st + kStageMasterBytes + kStageCodeBytes, d.prev_scales + base / kMxBlock,
+                     kStageScaleBytes, &sh.full[s]);
+    } else {
+      m.mode = kModeGeneric;
+      sh.meta[s] = m;
+      mbar_arrive(&sh.full[s]);
+    }
+    ticket = next;
+  }
+  for (uint32_t f = fills_done > uint32_t(kEncStages) ? fills_done - kEncStages : 0u; f < fills_done; ++f)
+    mbar_wait_bounded(&sh.full[f % kEncStages], (f / kEncStages) & 1u, a.wait_limit_ns);
+  __threadfence();
+  const uint32_t finished = atomicAdd(a.counters + 1, 1u);
+  if (finished == gridDim.x - 1) {
+    atomicExch(a.counters + 0, 0u);
+    atomicExch(a.counters + 1, 0u);
+  }
+}
+
+// ---------------------------------------------------------- look-back warp
+
+// Copy a parked tile's code entries to positions prefix_c + k (16-byte index
+// and 4-byte code stores after a head of up to 3 entries) and its scale
+// entries to positions prefix_s + k. Positions past the segment's capacity
+// are never written (they only arise after a wait gave up).
+__device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix_c, uint32_t prefix_s,
+                                         const uint32_t* ring, const uint16_t* sring, int lane) {
+  const uint32_t agg = pm.agg_c;
+  const uint32_t base = uint32_t(pm.base);
+  const bool vec = (reinterpret_cast<uintptr_t>(pm.idx) % 16u == 0) &&
+                   (reinterpret_cast<uintptr_t>(pm.val) % 4u == 0) &&
+                   uint64_t(prefix_c) + agg <= pm.n;
+  uint32_t head = vec ? ((4u - (prefix_c & 3u)) & 3u) : agg;
+  if (head > agg) head = agg;
+  const uint32_t body = vec ? ((agg - head) & ~3u) : 0u;
+  for (uint32_t k = uint32_t(lane); k < head; k += 32) {
+    const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
+    const uint64_t pos = uint64_t(prefix_c) + k;
+    if (pos < pm.n) {
+      pm.idx[pos] = base + (ent & 0xFFFFu);
+      pm.val[pos] = uint8_t(ent >> 16);
+    }
+  }
+  for (uint32_t k = head + uint32_t(lane) * 4u; k < head + body; k += 128u) {
+    uint32_t e[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) e[q] = ring[(pm.ring_start + k + uint32_t(q)) & kRingMask];
+    const uint64_t pos = uint64_t(prefix_c) + k;
+    *reinterpret_cast<uint4*>(pm.idx + pos) =
+        make_uint4(base + (e[0] & 0xFFFFu), base + (e[1] & 0xFFFFu), base + (e[2] & 0xFFFFu),
+                   base + (e[3] & 0xFFFFu));
+    *reinterpret_cast<uint32_t*>(pm.val + pos) =
+        ((e[0] >> 16) & 0xFFu) | (((e[1] >> 16) & 0xFFu) << 8) | (((e[2] >> 16) & 0xFFu) << 16) |
+        (((e[3] >> 16) & 0xFFu) << 24);
+  }
+  for (uint32_t k = head + body + uint32_t(lane); k < agg; k += 32) {
+    const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
+    const uint64_t pos = uint64_t(prefix_c) + k;
+    if (pos < pm.n) {
+      pm.idx[pos] = base + (ent & 0xFFFFu);
+      pm.val[pos] = uint8_t(ent >> 16);
+    }
+  }
+  const uint64_t nblocks = (pm.n + kMxBlock - 1) / kMxBlock;
+  const uint32_t block_base = uint32_t(pm.base / kMxBlock);
+  for (uint32_t k = uint32_t(lane); k < pm.agg_s; k += 32) {
+    const uint32_t ent = sring[k];
+    const uint64_t pos = uint64_t(prefix_s) + k;
+    if (pos < nblocks) {
+      pm.sidx[pos] = block_base + (ent & 0xFFu);
+      pm.sval[pos] = uint8_t(ent >> 8);
+    }
+  }
+}
+
+__device__ __forceinline__ void lookback_loop(const MxLaunch& a, MxShared& sh, const uint32_t* ring,
+                                              int w, int lane, bool multi) {
+  for (uint32_t i = uint32_t(w);;) {
+    const bool ok = helper_wait(&sh.agg_ready[i % kPendSlots], (i / kPendSlots) & 1u, a);
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    int more = 0;
+    if (lane == 0) {
+      for (int b = 1; b < kLookbackBatch; ++b) {
+        const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
+        if (!mbar_test_wait(&sh.agg_ready[ii % kPendSlots], (ii / kPendSlots) & 1u)) break;
+        more = b;
+      }
+    }
+    more = __shfl_sync(0xFFFFFFFFu, more, 0);
+    int nb = 0;
+    bool end = false;
+    uint64_t win[kLookbackBatch][kLookbackPerLane];
+#pragma unroll
+    for (int b = 0; b < kLookbackBatch; ++b) {
+      if (b > more || end) continue;
+      const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
+      const int q = int(ii % kPendSlots);
+      if (b > 0) mbar_test_wait(&sh.agg_ready[q], (ii / kPendSlots) & 1u);  // acquire for every lane
+      const ParkedMeta& pm = sh.parked[q];
+      if (pm.last == 2u) {
+        end = true;
+        continue;
+      }
+      if (pm.tile != pm.first)
+        load_window<StatusPacked>(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
+      nb = b + 1;
+    }
+#pragma unroll
+    for (int b = 0; b < kLookbackBatch; ++b) {
+      if (b >= nb) continue;
+      const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
+      const int q = int(ii % kPendSlots);
+      const ParkedMeta pm = sh.parked[q];
+      const uint64_t agg = uint64_t(pm.agg_c) | (uint64_t(pm.agg_s) << 32);
+      const uint64_t prefix = resolve_prefix<StatusPacked>(a, pm.tile, pm.first, agg, lane, win[b]);
+      const uint32_t prefix_c = uint32_t(prefix), prefix_s = uint32_t(prefix >> 32);
+      if (lane == 0 && pm.last == 1u) {
+        const uint32_t t = multi ? pm.tensor : 0u;
+        a.counts_out[2 * t] = uint64_t(prefix_c) + pm.agg_c;
+        a.counts_out[2 * t + 1] = uint64_t(prefix_s) + pm.agg_s;
+      }
+      copy_out(pm, prefix_c, prefix_s, ring, sh.sring[q], lane);
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) = pm.ring_start + pm.agg_c;
+        mbar_arrive(&sh.slot_free[q]);
+      }
+    }
+    if (end) break;
+    i += uint32_t(nb * kEncLookbackWarps);
+  }
+}
+
+// ------------------------------------------------------------ compute warps
+template <bool MULTI>
+__device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, uint8_t* stages,
+                                             uint32_t* ring, int tid, int lane, int warp) {
+  uint32_t posted = 0, ring_head = 0;
+  bool failed = false;
+  const bool leader = (lane & 7) == 0;  // lane that owns its block's scale
+  for (uint32_t it = 0;; ++it) {
+    const int s = int(it % kEncStages);
+    failed |= !wait_or_flag(&sh.full[s], (it / kEncStages) & 1u, a);
+    const StageMeta m = sh.meta[s];
+    const bool live = m.mode != kModeEnd;
+    const uint64_t base = m.base;
+    const uint32_t len = m.len;
+    const uint8_t* stage = stages + size_t(s) * kStageBytes;
+
+    // ---- quantize + compare: 4 consecutive elements per thread per round
+    uint32_t nc[kEncRounds];  // new codes, element 0 in the low byte
+    uint32_t ns = 0;          // byte j: new scale of this thread's block in round j
+    uint32_t flags = 0;       // bit (j*4 + e): code e of round j changed
+    uint32_t sflags = 0;      // bit j: the block of round j changed its scale (leaders only)
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
+      const uint32_t lb = li / kMxBlock;  // block within the tile
+      float4 mv;
+      uint32_t pc, ps = 0;
+      if (m.mode == kModeBulk) {
+        mv = reinterpret_cast<const float4*>(stage)[j * kEncThreads + tid];
+        pc = reinterpret_cast<const uint32_t*>(stage + kStageMasterBytes)[j * kEncThreads + tid];
+        if (leader) ps = stage[kStageMasterBytes + kStageCodeBytes + lb];
+      } else {
+        // tail or unaligned tile: elements past the end read as +0 (no effect
+        // on the block maximum) and are never reported
+        float mm[4];
+        uint32_t pp = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool valid = li + e < len;
+          mm[e] = valid ? m.master[base + li + e] : 0.0f;
+          pp |= (valid ? uint32_t(m.prev_codes[base + li + e]) : 0u) << (8 * e);
+        }
+        mv = make_float4(mm[0], mm[1], mm[2], mm[3]);
+        pc = pp;
+        if (leader && lb * kMxBlock < len) ps = m.prev_scales[(base / kMxBlock) + lb];
+      }
+      const uint32_t sb = mx_scale_byte(block_amax_bits(mv));
+      nc[j] = mx_codes4(mv, sb);
+      ns |= sb << (8 * j);
+      uint32_t f = byte_diff_bits(nc[j], pc);
+      if (m.mode != kModeBulk) {
+        const uint32_t nvalid = li >= len ? 0u : (len - li >= 4u ? 4u : len - li);
+        f &= (1u << nvalid) - 1u;
+      }
+      flags |= f << (4 * j);
+      if (leader && lb * kMxBlock < len && sb != ps) sflags |= 1u << j;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[s]);
+
+    // ---- refresh the previous view now
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      const uint32_t f = (flags >> (j * 4)) & 0xFu;
+      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
+      if (f != 0u) {
+        if (m.mode == kModeBulk) {
+          *reinterpret_cast<uint32_t*>(m.prev_codes + base + li) = nc[j];
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if ((f >> e) & 1u) m.prev_codes[base + li + e] = uint8_t(nc[j] >> (8 * e));
+        }
+      }
+      if ((sflags >> j) & 1u) m.prev_scales[base / kMxBlock + li / kMxBlock] = uint8_t(ns >> (8 * j));
+    }
+
+    // ---- rank: codes as in the BF16 encode (byte-packed warp scan of the
+    // four per-round counts); scales by one ballot per round (at most 4 per
+    // warp and round: one per block)
+    uint32_t cnts = 0;
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) cnts |= uint32_t(__popc((flags >> (4 * j)) & 0xFu)) << (8 * j);
+    uint32_t incl = cnts;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t excl = incl - cnts;
+    uint32_t stot = 0;   // byte j: changed scales of this warp in round j
+    uint32_t srank = 0;  // byte j: changed scales of earlier lanes of this warp in round j
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (sflags >> j) & 1u);
+      stot |= uint32_t(__popc(bal)) << (8 * j);
+      srank |= uint32_t(__popc(bal & lt)) << (8 * j);
+    }
+    const int pc = int(it & 1u);
+    if (lane == 31) sh.warp_tot[pc][warp] = incl;
+    if (lane == 0) sh.warp_stot[pc][warp] = stot;
+    if (compute_barrier_or(failed || !live)) break;
+
+    // codes across warps: 16-bit fields (rounds 0/2 and 1/3), as in the BF16 encode
+    const uint32_t t = lane < kWarps ? sh.warp_tot[pc][lane] : 0u;
+    const uint32_t t02 = t & 0x00FF00FFu, t13 = (t >> 8) & 0x00FF00FFu;
+    // scales across warps: 4 byte fields, each at most 8 x 4 = 32
+    const uint32_t ts = lane < kWarps ? sh.warp_stot[pc][lane] : 0u;
+    uint32_t s02 = t02, s13 = t13, ss = ts;
+#pragma unroll
+    for (int o = 1; o < kWarps; o <<= 1) {
+      const uint32_t v02 = __shfl_up_sync(0xFFFFFFFFu, s02, o);
+      const uint32_t v13 = __shfl_up_sync(0xFFFFFFFFu, s13, o);
+      const uint32_t vs = __shfl_up_sync(0xFFFFFFFFu, ss, o);
+      if (lane >= o) { s02 += v02; s13 += v13; ss += vs; }
+    }
+    const uint32_t b02 = __shfl_sync(0xFFFFFFFFu, s02 - t02, warp);
+    const uint32_t b13 = __shfl_sync(0xFFFFFFFFu, s13 - t13, warp);
+    const uint32_t bs = __shfl_sync(0xFFFFFFFFu, ss - ts, warp);
+    const uint32_t a02 = __shfl_sync(0xFFFFFFFFu, s02, kWarps - 1);
+    const uint32_t a13 = __shfl_sync(0xFFFFFFFFu, s13, kWarps - 1);
+    const uint32_t as = __shfl_sync(0xFFFFFFFFu, ss, kWarps - 1);
+    const uint32_t tot0 = a02 & 0xFFFFu, tot1 = a13 & 0xFFFFu, tot2 = a02 >> 16, tot3 = a13 >> 16;
+    uint32_t round_off[kEncRounds];
+    round_off[0] = (b02 & 0xFFFFu) + (excl & 0xFFu);
+    round_off[1] = tot0 + (b13 & 0xFFFFu) + ((excl >> 8) & 0xFFu);
+    round_off[2] = tot0 + tot1 + (b02 >> 16) + ((excl >> 16) & 0xFFu);
+    round_off[3] = tot0 + tot1 + tot2 + (b13 >> 16) + (excl >> 24);
+    const uint32_t agg_c = tot0 + tot1 + tot2 + tot3;
+    const uint32_t stot0 = as & 0xFFu, stot1 = (as >> 8) & 0xFFu, stot2 = (as >> 16) & 0xFFu,
+                   stot3 = as >> 24;
+    const uint32_t agg_s = stot0 + stot1 + stot2 + stot3;
+    if (tid == 0) {
+      const uint64_t v = uint64_t(agg_c) | (uint64_t(agg_s) << 32);
+      st_relaxed_u64(a.status + m.tile,
+                     StatusPacked::make(uint64_t(m.tile) == m.first ? kFlagPrefix : kFlagAggregate,
+                                        0u, v));
+    }
+
+    // ---- room: the parked slot must be free and the ring must hold agg_c more
+    const int q = int(posted % kPendSlots);
+    if (posted >= uint32_t(kPendSlots))
+      failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kPendSlots) / kPendSlots) & 1u, a);
+    if (ring_head + agg_c - *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) > uint32_t(kEncRing)) {
+      const uint64_t t0 = global_timer_ns();
+      while (ring_head + agg_c - *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) >
+             uint32_t(kEncRing)) {
+        __nanosleep(64);
+        if (global_timer_ns() - t0 > a.wait_limit_ns ||
+            (ld_volatile_u32(a.counters + 2) & kErrTimeout)) {
+          record_error(a.counters + 2, kErrTimeout);
+          failed = true;
+          break;
+        }
+      }
+    }
+
+    // ---- park the compacted tile
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      uint32_t f = (flags >> (j * 4)) & 0xFu;
+      if (f == 0u) continue;
+      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
+      uint32_t r = ring_head + round_off[j];
+      do {
+        const uint32_t e = uint32_t(__ffs(f)) - 1u;
+        f &= f - 1u;
+        ring[r & kRingMask] = (li + e) | (((nc[j] >> (8 * e)) & 0xFFu) << 16);
+        ++r;
+      } while (f != 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kEncRounds; ++j) {
+      if (!((sflags >> j) & 1u)) continue;
+      const uint32_t before = (j > 0 ? stot0 : 0u) + (j > 1 ? stot1 : 0u) + (j > 2 ? stot2 : 0u);
+      const uint32_t pos = before + ((bs >> (8 * j)) & 0xFFu) + ((srank >> (8 * j)) & 0xFFu);
+      const uint32_t lb = (uint32_t(j * kEncThreads + tid) * 4u) / kMxBlock;
+      sh.sring[q][pos] = uint16_t(lb | (((ns >> (8 * j)) & 0xFFu) << 8));
+    }
+    if (tid == 0) {
+      ParkedMeta pm;
+      pm.tile = m.tile;
+      pm.tensor = m.tensor;
+      pm.agg_c = agg_c;
+      pm.agg_s = agg_s;
+      pm.last = (base + len == m.n) ? 1u : 0u;
+      pm.ring_start = ring_head;
+      pm.first = m.first;
+      pm.n = m.n;
+      pm.base = base;
+      pm.idx = m.idx;
+      pm.val = m.val;
+      pm.sidx = m.sidx;
+      pm.sval = m.sval;
+      sh.parked[q] = pm;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.agg_ready[q]);
+    ++posted;
+    ring_head += agg_c;
+  }
+  for (uint32_t e = posted > uint32_t(kPendSlots) ? posted - kPendSlots : 0u; e < posted; ++e)
+    wait_or_flag(&sh.slot_free[e % kPendSlots], (e / kPendSlots) & 1u, a);
+  compute_barrier();
+  for (int k = 0; k < kEncLookbackWarps; ++k) {
+    const uint32_t i = posted + uint32_t(k);
+    const int q = int(i % kPendSlots);
+    if (tid == 0) {
+      ParkedMeta pm{};
+      pm.last = 2u;
+      sh.parked[q] = pm;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.agg_ready[q]);
+  }
+}
+
+template <bool MULTI>
+__global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
+    encode_mx_kernel(const __grid_constant__ MxLaunch a) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ MxShared sh;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~uintptr_t(127));
+  uint32_t* ring = reinterpret_cast<uint32_t*>(stages + size_t(kEncStages) * kStageBytes);
+
+  if constexpr (MULTI) {
+    if (blockIdx.x == 0) {
+      for (int t = tid; t < a.ntensors; t += kEncBlockThreads) {
+        if (a.tensors[t].n == 0) {
+          a.counts_out[2 * t] = 0;
+          a.counts_out[2 * t + 1] = 0;
+        }
+      }
+    }
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < kEncStages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], kWarps);
+      sh.meta[s] = StageMeta{};
+      sh.meta[s].mode = kModeEnd;
+    }
+#pragma unroll
+    for (int q = 0; q < kPendSlots; ++q) {
+      mbar_init(&sh.agg_ready[q], kWarps);
+      mbar_init(&sh.slot_free[q], 1);
+      sh.parked[q] = ParkedMeta{};
+      sh.parked[q].last = 2u;
+    }
+    sh.ring_tail = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp < kWarps) {
+    compute_loop<MULTI>(a, sh, stages, ring, tid, lane, warp);
+  } else if (warp == kProducerWarp) {
+    if (lane == 0) producer_loop<MULTI>(a, sh, stages);
+  } else {
+    lookback_loop(a, sh, ring, warp - kFirstLookbackWarp, lane, MULTI);
+  }
+}
+
+template <bool MULTI>
+int encode_mx_blocks_per_sm() {
+  static int cached = [] {
+    cudaFuncSetAttribute(encode_mx_kernel<MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         int(kDynSmem));
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, encode_mx_kernel<MULTI>,
+                                                      kEncBlockThreads, kDynSmem) != cudaSuccess ||
+        b < 1)
+      b = 1;
+    return b;
+  }();
+  return cached;
+}
+
+// ------------------------------------------------------------ quantize
+// The MXFP8 view of one tensor (initial state of the trainer's previous view
+// and of a receiver). 4 consecutive elements per thread; a warp covers 4
+// whole blocks, so block b of the warp is lanes 8b .. 8b+7.
+constexpr int kQuantThreads = 256;
+
+__global__ void __launch_bounds__(kQuantThreads)
+    mx_quantize_kernel(const float* __restrict__ master, uint64_t n, uint8_t* __restrict__ codes,
+                       uint8_t* __restrict__ scales) {
+  const bool vec = (reinterpret_cast<uintptr_t>(master) % 16u == 0) &&
+                   (reinterpret_cast<uintptr_t>(codes) % 4u == 0);
+  const uint64_t groups = (n + 3) / 4;
+  const uint64_t stride = uint64_t(gridDim.x) * kQuantThreads;
+  // every lane of a warp runs the same number of iterations (shuffles below)
+  const uint64_t warp_first = (uint64_t(blockIdx.x) * kQuantThreads + (threadIdx.x & ~31u));
+  const int lane = threadIdx.x & 31;
+  for (uint64_t g0 = warp_first; g0 < groups; g0 += stride) {
+    const uint64_t i = (g0 + lane) * 4u;
+    float4 v;
+    if (vec && i + 4 <= n) {
+      v = *reinterpret_cast<const float4*>(master + i);
+    } else {
+      v.x = i + 0 < n ? master[i + 0] : 0.0f;
+      v.y = i + 1 < n ? master[i + 1] : 0.0f;
+      v.z = i + 2 < n ? master[i + 2] : 0.0f;
+      v.w = i + 3 < n ? master[i + 3] : 0.0f;
+    }
+    const uint32_t sb = mx_scale_byte(block_amax_bits(v));
+    const uint32_t c = mx_codes4(v, sb);
+    if (vec && i + 4 <= n) {
+      *reinterpret_cast<uint32_t*>(codes + i) = c;
+    } else {
+      for (int e = 0; e < 4; ++e)
+        if (i + e < n) codes[i + e] = uint8_t(c >> (8 * e));
+    }
+    if ((lane & 7) == 0 && i < n) scales[i / kMxBlock] = uint8_t(sb);
+  }
+}
+
+}  // namespace
+
+int encode_mx_grid_size(int device) {
+  const int a = encode_mx_blocks_per_sm<true>(), b = encode_mx_blocks_per_sm<false>();
+  return sm_count(device) * (a < b ? a : b);
+}
+
+cudaError_t launch_encode_mx(const MxLaunch& a, bool multi, int grid, cudaStream_t stream) {
+  if (multi) {
+    encode_mx_blocks_per_sm<true>();
+    encode_mx_kernel<true><<<grid, kEncBlockThreads, kDynSmem, stream>>>(a);
+  } else {
+    encode_mx_blocks_per_sm<false>();
+    encode_mx_kernel<false><<<grid, kEncBlockThreads, kDynSmem, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quantize(const float* master, uint64_t n, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t warps = (n + 127) / 128;
+  const uint64_t blocks = (warps + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
+  const uint64_t cap = uint64_t(sm_count(dev)) * 8u;
+  const int grid = int(blocks < cap ? blocks : cap);
+  if (grid == 0) return cudaSuccess;
+  mx_quantize_kernel<<<grid, kQuantThreads, 0, stream>>>(master, n, codes, scales);
+  return cudaGetLastError();
+}
+
+}  // namespace pulse

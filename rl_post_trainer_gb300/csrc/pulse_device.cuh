@@ -213,7 +213,7 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
-// Streaming 128/64-bit global loads that do not allocate in L1. The `_ro`
+// Streaming 128/64/32-bit global loads that do not allocate in L1. The `_ro`
 // forms use the read-only path and are only for buffers nothing writes
 // during the kernel; the others are for in/out buffers.
 __device__ __forceinline__ uint4 ld_stream_u4_ro(const void* p) {
@@ -228,6 +228,11 @@ __device__ __forceinline__ uint2 ld_stream_u2_ro(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
                : "=r"(v.x), "=r"(v.y)
                : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u1_ro(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 __device__ __forceinline__ uint2 ld_u2_no_l1(const void* p) {

@@ -89,6 +89,44 @@ struct EncodeLaunch {
 int encode_grid_size(int device);
 cudaError_t launch_encode(const EncodeLaunch& a, bool multi, int grid, cudaStream_t stream);
 
+// ------------------------------------------------------- MXFP8 view encode
+// Same CTA layout and tile as the BF16 encode; a tile holds kEncTile / 32
+// blocks of 32 elements sharing one E8M0 scale.
+constexpr int kMxBlock = 32;
+
+struct MxTensorDesc {
+  const float* master;
+  uint8_t* prev_codes;   // n E4M3 codes, in/out
+  uint8_t* prev_scales;  // ceil(n / 32) E8M0 scales, in/out
+  uint32_t* idx;         // code segment: element indices
+  uint8_t* val;          //               new codes
+  uint32_t* sidx;        // scale segment: block indices
+  uint8_t* sval;         //                new scales
+  uint64_t n;
+  uint64_t tile_begin;   // first global encode tile of this tensor
+  uint32_t bulk_ok;      // master, prev_codes, prev_scales 16-byte aligned
+  uint32_t reserved;
+};
+
+struct MxLaunch {
+  MxTensorDesc one;              // single-tensor mode
+  const MxTensorDesc* tensors;   // multi-tensor mode: device array
+  const uint64_t* tile_begin;    // multi-tensor mode: ntensors + 1 entries (device)
+  int ntensors;
+  uint64_t total_tiles;
+  uint64_t* status;              // cleared (all zero) before the launch
+  uint32_t* counters;
+  uint64_t* counts_out;          // 2 x ntensors device uint64: codes, scales per tensor
+  uint32_t epoch;                // unused (the packed status words carry no epoch)
+  uint32_t first_ticket;
+  uint64_t wait_limit_ns;
+};
+
+int encode_mx_grid_size(int device);
+cudaError_t launch_encode_mx(const MxLaunch& a, bool multi, int grid, cudaStream_t stream);
+cudaError_t launch_mx_quantize(const float* master, uint64_t n, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t stream);
+
 // ---------------------------------------------------------------- apply
 #ifndef PULSE_APPLY_PER_THREAD
 #define PULSE_APPLY_PER_THREAD 8
@@ -106,6 +144,19 @@ cudaError_t launch_apply(uint16_t* w, uint64_t n, bool checked, const uint32_t* 
 cudaError_t launch_apply_multi(const TensorDesc* tensors, int ntensors,
                                const uint64_t* counts_dev, uint32_t* error_word,
                                int grid, cudaStream_t stream);
+
+// One byte-valued patch segment (an MXFP8 code or scale array).
+struct ByteSegment {
+  uint8_t* w;
+  uint32_t* idx;
+  uint8_t* val;
+  uint64_t n;
+};
+cudaError_t launch_apply_u8(uint8_t* w, uint64_t n, bool checked, const uint32_t* idx,
+                            const uint8_t* val, uint64_t count, uint32_t* error_word,
+                            cudaStream_t stream);
+cudaError_t launch_apply_u8_multi(const ByteSegment* segs, int nsegs, const uint64_t* counts_dev,
+                                  uint32_t* error_word, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- XOR
 constexpr int kXorRounds = PULSE_XOR_ROUNDS;            // 4-element loads in flight per thread

@@ -50,6 +50,30 @@ class PulseTensor(ctypes.Structure):
     ]
 
 
+class PulseMxTensor(ctypes.Structure):
+    _fields_ = [
+        ("master", ctypes.c_void_p),
+        ("prev_codes", ctypes.c_void_p),
+        ("prev_scales", ctypes.c_void_p),
+        ("codes", ctypes.c_void_p),
+        ("scales", ctypes.c_void_p),
+        ("n", ctypes.c_uint64),
+        ("idx", ctypes.c_void_p),
+        ("val", ctypes.c_void_p),
+        ("sidx", ctypes.c_void_p),
+        ("sval", ctypes.c_void_p),
+    ]
+
+
+MX_BLOCK = 32
+_U8 = (torch.uint8, torch.int8)
+
+
+def mx_blocks(n: int) -> int:
+    """Scale bytes of an n-element MXFP8 view."""
+    return (int(n) + MX_BLOCK - 1) // MX_BLOCK
+
+
 def library_path() -> str:
     return _build.LIB
 
@@ -86,6 +110,16 @@ def lib():
             "pulse_plan_get_error": ([P], I),
             "pulse_debug_encode_orphan_tile": ([P, P, U64, P, P, P, U64, P], I),
             "pulse_encode_noalloc": ([P, P, U64, P, P, P, P], I),
+            "pulse_mx_quantize": ([P, U64, P, P, P], I),
+            "pulse_mx_encode": ([P, P, P, U64, P, P, P, P, P, P], I),
+            "pulse_mx_apply": ([P, P, U64, P, P, U64, P, P, U64, P], I),
+            "pulse_mx_plan_create": ([ctypes.POINTER(PulseMxTensor), I, ctypes.POINTER(P)], I),
+            "pulse_mx_plan_destroy": ([P], I),
+            "pulse_mx_plan_num_tensors": ([P], I),
+            "pulse_mx_encode_multi": ([P, P, P], I),
+            "pulse_mx_apply_multi": ([P, P, P], I),
+            "pulse_mx_apply_multi_device": ([P, P, P], I),
+            "pulse_mx_plan_get_error": ([P], I),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -328,6 +362,179 @@ class Plan:
         if getattr(self, "_h", None) is not None and self._h.value:
             with torch.cuda.device(self.device):
                 lib().pulse_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+# ------------------------------------------------------------ MXFP8 view
+
+def mx_quantize(master: torch.Tensor, codes_out: Optional[torch.Tensor] = None,
+                scales_out: Optional[torch.Tensor] = None):
+    """pulse_mx_quantize: returns the MXFP8 view (codes uint8[n], scales uint8[ceil(n/32)])."""
+    _need(master, "master", (torch.float32,))
+    dev = master.device
+    n = master.numel()
+    if codes_out is None:
+        codes_out = torch.empty(n, dtype=torch.uint8, device=dev)
+    if scales_out is None:
+        scales_out = torch.empty(mx_blocks(n), dtype=torch.uint8, device=dev)
+    _need(codes_out, "codes_out", _U8, dev, n)
+    _need(scales_out, "scales_out", _U8, dev, mx_blocks(n))
+    with torch.cuda.device(dev):
+        st = lib().pulse_mx_quantize(_ptr(master), n, _ptr(codes_out), _ptr(scales_out), _stream(dev))
+    _raise(st, "pulse_mx_quantize")
+    return codes_out, scales_out
+
+
+def mx_encode(master: torch.Tensor, prev_codes: torch.Tensor, prev_scales: torch.Tensor,
+              idx_out=None, val_out=None, sidx_out=None, sval_out=None, counts_out=None):
+    """pulse_mx_encode: returns (idx, val, sidx, sval, counts); refreshes the
+    previous view in place. ``counts`` is a 2-element device int64 tensor
+    {changed codes, changed scales}; each segment is the first count entries
+    of its buffers."""
+    _need(master, "master", (torch.float32,))
+    dev = master.device
+    n = master.numel()
+    nb = mx_blocks(n)
+    _need(prev_codes, "prev_codes", _U8, dev, n)
+    _need(prev_scales, "prev_scales", _U8, dev, nb)
+    if idx_out is None:
+        idx_out = torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+    if val_out is None:
+        val_out = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    if sidx_out is None:
+        sidx_out = torch.empty(max(nb, 1), dtype=torch.int32, device=dev)
+    if sval_out is None:
+        sval_out = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+    if counts_out is None:
+        counts_out = torch.empty(2, dtype=torch.int64, device=dev)
+    _need(idx_out, "idx_out", (torch.int32, torch.uint32), dev, min_numel=n)
+    _need(val_out, "val_out", _U8, dev, min_numel=n)
+    _need(sidx_out, "sidx_out", (torch.int32, torch.uint32), dev, min_numel=nb)
+    _need(sval_out, "sval_out", _U8, dev, min_numel=nb)
+    _need(counts_out, "counts_out", (torch.int64, torch.uint64), dev, min_numel=2)
+    with torch.cuda.device(dev):
+        st = lib().pulse_mx_encode(_ptr(master), _ptr(prev_codes), _ptr(prev_scales), n,
+                                   _ptr(idx_out), _ptr(val_out), _ptr(sidx_out), _ptr(sval_out),
+                                   _ptr(counts_out), _stream(dev))
+    _raise(st, "pulse_mx_encode")
+    return idx_out, val_out, sidx_out, sval_out, counts_out
+
+
+def mx_apply(codes: torch.Tensor, scales: torch.Tensor, idx, val, count: int, sidx, sval,
+             scount: int):
+    """pulse_mx_apply: codes[idx[j]] = val[j] (j < count), scales[sidx[j]] = sval[j] (j < scount)."""
+    _need(codes, "codes", _U8)
+    dev = codes.device
+    n = codes.numel()
+    _need(scales, "scales", _U8, dev, mx_blocks(n))
+    count, scount = int(count), int(scount)
+    _need(idx, "idx", (torch.int32, torch.uint32), dev, min_numel=count)
+    _need(val, "val", _U8, dev, min_numel=count)
+    _need(sidx, "sidx", (torch.int32, torch.uint32), dev, min_numel=scount)
+    _need(sval, "sval", _U8, dev, min_numel=scount)
+    with torch.cuda.device(dev):
+        st = lib().pulse_mx_apply(_ptr(codes), _ptr(scales), n, _ptr(idx), _ptr(val), count,
+                                  _ptr(sidx), _ptr(sval), scount, _stream(dev))
+    _raise(st, "pulse_mx_apply")
+
+
+class MxTensorSlot:
+    """Buffers of one model tensor for an MxPlan (any field may be None)."""
+
+    def __init__(self, n: int, master=None, prev_codes=None, prev_scales=None, codes=None,
+                 scales=None, idx=None, val=None, sidx=None, sval=None):
+        self.n = int(n)
+        self.master, self.prev_codes, self.prev_scales = master, prev_codes, prev_scales
+        self.codes, self.scales = codes, scales
+        self.idx, self.val, self.sidx, self.sval = idx, val, sidx, sval
+
+
+class MxPlan:
+    """pulse_mx_plan: the MXFP8 view of a fixed tensor list, one launch per step.
+
+    Counts are 2 x ntensors int64 in list order: {codes_0, scales_0, codes_1, ...}."""
+
+    def __init__(self, slots: Sequence[MxTensorSlot], device: Optional[torch.device] = None):
+        if len(slots) == 0:
+            raise ValueError("a plan needs at least one tensor")
+        self.slots = list(slots)
+        dev = device
+        arr = (PulseMxTensor * len(slots))()
+        for i, s in enumerate(slots):
+            nb = mx_blocks(s.n)
+            checks = (("master", s.master, (torch.float32,), s.n, None),
+                      ("prev_codes", s.prev_codes, _U8, s.n, None),
+                      ("prev_scales", s.prev_scales, _U8, nb, None),
+                      ("codes", s.codes, _U8, s.n, None),
+                      ("scales", s.scales, _U8, nb, None),
+                      ("idx", s.idx, (torch.int32, torch.uint32), None, s.n),
+                      ("val", s.val, _U8, None, s.n),
+                      ("sidx", s.sidx, (torch.int32, torch.uint32), None, nb),
+                      ("sval", s.sval, _U8, None, nb))
+            for name, t, dtypes, numel, min_numel in checks:
+                if t is None:
+                    continue
+                if dev is None:
+                    dev = t.device
+                _need(t, name, dtypes, dev, numel, min_numel)
+            arr[i] = PulseMxTensor(_ptr(s.master), _ptr(s.prev_codes), _ptr(s.prev_scales),
+                                   _ptr(s.codes), _ptr(s.scales), s.n, _ptr(s.idx), _ptr(s.val),
+                                   _ptr(s.sidx), _ptr(s.sval))
+        if dev is None:
+            raise ValueError("a plan needs at least one device buffer")
+        self.device = dev
+        self.ntensors = len(slots)
+        handle = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            st = lib().pulse_mx_plan_create(arr, len(slots), ctypes.byref(handle))
+        _raise(st, "pulse_mx_plan_create")
+        self._h = handle
+
+    def encode(self, counts_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        if counts_out is None:
+            counts_out = torch.empty(2 * self.ntensors, dtype=torch.int64, device=self.device)
+        _need(counts_out, "counts_out", (torch.int64, torch.uint64), self.device,
+              min_numel=2 * self.ntensors)
+        with torch.cuda.device(self.device):
+            st = lib().pulse_mx_encode_multi(self._h, _ptr(counts_out), _stream(self.device))
+        _raise(st, "pulse_mx_encode_multi")
+        return counts_out
+
+    def apply(self, counts):
+        """counts: a device int64 tensor (no host round trip) or 2 x ntensors host integers."""
+        with torch.cuda.device(self.device):
+            if isinstance(counts, torch.Tensor) and counts.is_cuda:
+                _need(counts, "counts", (torch.int64, torch.uint64), self.device,
+                      min_numel=2 * self.ntensors)
+                st = lib().pulse_mx_apply_multi_device(self._h, _ptr(counts), _stream(self.device))
+            else:
+                vals = [int(c) for c in counts]
+                if len(vals) != 2 * self.ntensors:
+                    raise ValueError(f"expected {2 * self.ntensors} counts, got {len(vals)}")
+                host = (ctypes.c_uint64 * len(vals))(*vals)
+                st = lib().pulse_mx_apply_multi(self._h, host, _stream(self.device))
+        _raise(st, "pulse_mx_apply_multi")
+
+    def get_error(self) -> int:
+        with torch.cuda.device(self.device):
+            return int(lib().pulse_mx_plan_get_error(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            with torch.cuda.device(self.device):
+                lib().pulse_mx_plan_destroy(self._h)
             self._h = ctypes.c_void_p()
 
     def __del__(self):

@@ -90,3 +90,25 @@ def test_binding_rejects_cpu_tensors(lib):
         pulse.encode(m, p)
     with pytest.raises(TypeError):
         pulse.xor_mask(m, p)
+
+
+def test_mx_host_side_argument_checks_launch_nothing(lib):
+    P = ctypes.c_void_p
+    E = pulse.pulse
+    assert lib.pulse_mx_quantize(P(0), 0, P(0), P(0), P(0)) == E.PULSE_OK
+    assert lib.pulse_mx_quantize(P(0), 7, P(0), P(0), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_quantize(P(0), 1 << 32, P(0), P(0), P(0)) == E.PULSE_ERR_RANGE
+    assert lib.pulse_mx_encode(P(0), P(0), P(0), 5, P(0), P(0), P(0), P(0), P(0), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_encode(P(0), P(0), P(0), 5, P(0), P(0), P(0), P(0), P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_encode(P(0), P(0), P(0), 1 << 32, P(0), P(0), P(0), P(0), P(8), P(0)) == E.PULSE_ERR_RANGE
+    assert lib.pulse_mx_apply(P(0), P(0), 10, P(0), P(0), 0, P(0), P(0), 0, P(0)) == E.PULSE_OK
+    assert lib.pulse_mx_apply(P(0), P(0), 10, P(0), P(0), 2, P(0), P(0), 0, P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_apply(P(0), P(0), 10, P(0), P(0), 0, P(0), P(0), 1, P(0)) == E.PULSE_ERR_INVALID
+    h = P()
+    assert lib.pulse_mx_plan_create(None, 0, ctypes.byref(h)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_plan_create(None, 1, None) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_encode_multi(None, P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_apply_multi(None, P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_apply_multi_device(None, P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_plan_destroy(None) == E.PULSE_OK
+    assert lib.pulse_mx_plan_num_tensors(None) == 0

@@ -217,6 +217,23 @@ def torch_model(specs: Sequence[TensorSpec], seed: int, eta: float, device,
     return out
 
 
+def torch_model_states(specs: Sequence[TensorSpec], seed: int, eta: float, device,
+                       chunk: int = 1 << 26):
+    """The same draws as ``torch_model`` (per tensor: w0, then z), returned as
+    (w0, master = w0 + eta * z) pairs of FP32 tensors, for views other than
+    BF16 that are built from w0 by the code under test."""
+    import torch
+    gen = torch_generator(device, seed)
+    out = []
+    for spec in specs:
+        w0 = torch.empty(spec.numel, dtype=torch.float32, device=device)
+        torch_init_(w0, spec, gen)
+        m = w0.clone()
+        torch_update_(m, eta, gen, chunk)
+        out.append((w0, m))
+    return out
+
+
 def torch_step_(masters, step: int, eta: float = ETA_DEFAULT, chunk: int = 1 << 26):
     """One more Adam-sized step of a chain: master += eta * z, z drawn from
     seed CHAIN_SEED_BASE + step, tensors in list order."""
