@@ -12,7 +12,8 @@ pristine copy (untimed), so every timed step encodes the same real update.
 Inputs (48 GB) are far larger than L2 (129 MB), so no L2 flush is needed.
 
 Printed: one JSON line with params/s (value), the roofline of the encode
-kernel against measured HBM copy bandwidth, the XOR-mask path, an
+kernel against measured HBM copy bandwidth, the XOR-mask path, the MXFP8
+serving view of the same step (its own encode + apply), an
 end-to-end number through host buffers, the CPU oracle baseline, and the
 SM clocks sampled during the timed region.
 
@@ -414,6 +415,9 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
         del wl.prev_x, wl.w_x, wl.mask
         wl.xplan.close()
 
+    if not args.no_mx:
+        out["mxfp8"] = run_mx(args, cfg, specs, wl, dev, rank, peak)
+
     if not args.no_e2e:
         out["e2e"] = e2e(args, wl, counts_np, dist_on)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -426,6 +430,110 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
             "sample": f"first {len(chosen)} tensors ({total} params) of {cfg['name']}, "
                       f"encode+apply, one oracle call per tensor on {threads} threads"}
     return out
+
+
+def run_mx(args, cfg, specs, wl, dev, rank, peak):
+    """The MXFP8 serving view of the same model and step: whole-model
+    pulse_mx_encode_multi + pulse_mx_apply_multi_device, timed like the BF16
+    step (previous view and receiver restored untimed before each step). The
+    BF16 patch buffers are reused for the code segments."""
+    import rl_post_trainer_gb300 as pulse
+    n = wl.n
+    stream = torch.cuda.current_stream(dev)
+    # the view before the step: the same generator sequence as the workload
+    # (per tensor: w0, then z), quantizing each w0 as it is drawn
+    gen = workloads.torch_generator(dev, cfg["seed"] + 1000 * rank)
+    c0, s0 = [], []
+    tmp = torch.empty(max(s.numel for s in specs), dtype=torch.float32, device=dev)
+    for spec in specs:
+        w0 = tmp[:spec.numel]
+        workloads.torch_init_(w0, spec, gen)
+        c, sc = pulse.mx_quantize(w0)
+        c0.append(c)
+        s0.append(sc)
+        workloads.torch_update_(w0, cfg["eta"], gen)   # advances the generator past z
+    del tmp
+    prev_c = [c.clone() for c in c0]
+    prev_s = [x.clone() for x in s0]
+    codes = [c.clone() for c in c0]
+    scales = [x.clone() for x in s0]
+    nb = [pulse.mx_blocks(s.numel) for s in specs]
+    sidx = [torch.empty(max(b, 1), dtype=torch.int32, device=dev) for b in nb]
+    sval = [torch.empty(max(b, 1), dtype=torch.uint8, device=dev) for b in nb]
+    plan = pulse.MxPlan([pulse.MxTensorSlot(s.numel, master=wl.master[i], prev_codes=prev_c[i],
+                                            prev_scales=prev_s[i], codes=codes[i], scales=scales[i],
+                                            idx=wl.idx[i], val=wl.val[i].view(torch.uint8),
+                                            sidx=sidx[i], sval=sval[i])
+                         for i, s in enumerate(specs)])
+    counts = torch.zeros(2 * len(specs), dtype=torch.int64, device=dev)
+
+    def restore():
+        for a, b in zip(prev_c, c0):
+            a.copy_(b)
+        for a, b in zip(prev_s, s0):
+            a.copy_(b)
+        for a, b in zip(codes, c0):
+            a.copy_(b)
+        for a, b in zip(scales, s0):
+            a.copy_(b)
+
+    for _ in range(args.warmup):
+        restore()
+        plan.encode(counts)
+        plan.apply(counts)
+    torch.cuda.synchronize()
+    te, ta = [], []
+    for _ in range(args.steps):
+        restore()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        plan.encode(counts)
+        ev[1].record(stream)
+        plan.apply(counts)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        te.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+        ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+    if plan.get_error() != 0:
+        raise RuntimeError("device error in the MXFP8 steps")
+    for t in range(len(specs)):
+        if not (torch.equal(codes[t], prev_c[t]) and torch.equal(scales[t], prev_s[t])):
+            raise RuntimeError(f"MXFP8 receiver differs from the trainer view (tensor {t})")
+    cn = counts.cpu().numpy()
+    k, ks = int(cn[0::2].sum()), int(cn[1::2].sum())
+    # distinct 32-byte sectors holding a changed code / scale (1-byte arrays,
+    # allocations 512-byte aligned: sector = index // 32)
+    sc_codes = sc_scales = 0
+    for t in range(len(specs)):
+        for cnt, arr in ((int(cn[2 * t]), wl.idx[t]), (int(cn[2 * t + 1]), sidx[t])):
+            if cnt:
+                sec = arr[:cnt].to(torch.int64) // 32
+                val = 1 + int((sec[1:] != sec[:-1]).sum().item())
+                if arr is sidx[t]:
+                    sc_scales += val
+                else:
+                    sc_codes += val
+    nblocks = float(sum(nb))
+    e_s, a_s = float(np.mean(te)), float(np.mean(ta))
+    enc_alg = 5.0 * n + nblocks + 6.0 * k + 6.0 * ks
+    enc_sec = 5.0 * n + nblocks + 32.0 * (sc_codes + sc_scales) + 5.0 * k + 5.0 * ks
+    app_rmw = 5.0 * (k + ks) + 64.0 * (sc_codes + sc_scales)
+    plan.close()
+    return {
+        "format": "MXFP8 (E4M3 codes, E8M0 scale per 32 elements)",
+        "encode_ms": 1e3 * e_s, "apply_ms": 1e3 * a_s,
+        "params_per_s": n / (e_s + a_s),
+        "code_density": k / n, "scale_density": ks / nblocks,
+        "code_entries": k, "scale_entries": ks,
+        "encode_gbs_algorithmic": enc_alg / e_s / 1e9,
+        "encode_gbs_sector": enc_sec / e_s / 1e9,
+        "encode_frac_measured_peak": enc_alg / e_s / 1e9 / peak,
+        "encode_frac_sector_measured_peak": enc_sec / e_s / 1e9 / peak,
+        "apply_gbs_sector_rmw": app_rmw / a_s / 1e9,
+        "bytes_model": "encode 5n + n/32 + 6k + 6ks (sector: 5n + n/32 + 32S + 5k + 5ks)",
+        "gpu_launches": 2 * args.steps,
+    }
 
 
 def e2e(args, wl, counts_np, dist_on):
@@ -494,6 +602,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-xor", action="store_true")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8-view leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-params", type=float, default=1.2e9)

@@ -42,34 +42,8 @@ constexpr uint32_t kStageScaleBytes = kTileBlocks;                 // 128 B
 constexpr uint32_t kStageBytes = kStageMasterBytes + kStageCodeBytes + kStageScaleBytes;
 static_assert(kStageBytes % 128 == 0, "stages stay 128-byte aligned");
 constexpr size_t kDynSmem = size_t(kEncStages) * kStageBytes + size_t(kEncRing) * 4 + 128;
-static_assert(kEncTile % (kMxBlock * 8) == 0, "a warp round covers whole blocks");
 
 // ---------------------------------------------------------- MXFP8 arithmetic
-
-// Largest |v| bit pattern (sign cleared) over the 32-element block this
-// thread's 4 elements belong to: the block spans lanes (lane & ~7) .. +7.
-// For non-NaN values the unsigned order of these patterns is the order of
-// the magnitudes; any NaN makes the result exceed 0x7F800000. All 32 lanes
-// must call.
-__device__ __forceinline__ uint32_t block_amax_bits(const float4& v) {
-  uint32_t a = max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
-                   max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu));
-  a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-  a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-  a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-  return a;
-}
-
-// E8M0 scale byte from the block maximum: with E the maximum's biased FP32
-// exponent, floor(log2 max) - 8 + 127 = E - 135 + 127 = E - 8 for normal
-// maxima; zero and subnormal maxima (E = 0), and normals with E <= 8, give
-// an exponent at or below -127, which is raised to -127 (byte 0). Any
-// infinity or NaN in the block gives the NaN scale 0xFF.
-__device__ __forceinline__ uint32_t mx_scale_byte(uint32_t amax_bits) {
-  if (amax_bits >= 0x7F800000u) return 0xFFu;
-  const uint32_t e = amax_bits >> 23;
-  return e > 8u ? e - 8u : 0u;
-}
 
 // Saturating round-to-nearest-even FP32 -> E4M3 of two values; `hi` lands in
 // the upper byte of the result.
@@ -85,15 +59,9 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
 // such a value rounds to a zero code either way.
 __device__ __forceinline__ uint32_t mx_codes4(const float4& v, uint32_t scale) {
   if (scale == 0xFFu) return 0x7F7F7F7Fu;
-  const float f = __uint_as_float((254u - scale) << 23);
+  const float f = __uint_as_float(0x7F000000u - (scale << 23));  // (254 - scale) << 23
   return cvt_e4m3x2(__fmul_rn(v.y, f), __fmul_rn(v.x, f)) |
          (cvt_e4m3x2(__fmul_rn(v.w, f), __fmul_rn(v.z, f)) << 16);
-}
-
-// One bit per byte of a and b that differs (bit e for byte e).
-__device__ __forceinline__ uint32_t byte_diff_bits(uint32_t a, uint32_t b) {
-  const uint32_t m = __vcmpne4(a, b);
-  return ((m >> 7) & 1u) | ((m >> 14) & 2u) | ((m >> 21) & 4u) | ((m >> 28) & 8u);
 }
 
 // -------------------------------------------------------------- shared state
@@ -333,60 +301,119 @@ __device__ __forceinline__ void lookback_loop(const MxLaunch& a, MxShared& sh, c
 }
 
 // ------------------------------------------------------------ compute warps
+// Per tile each compute thread handles kMxRounds rounds of kMxPerThread
+// consecutive elements, so a 32-element block spans 4 consecutive lanes.
+constexpr int kMxPerThread = 8;
+constexpr int kMxRounds = kEncTile / (kEncThreads * kMxPerThread);  // 2
+static_assert(kMxRounds == 2, "two rounds pack into the 16-bit fields of one word");
+constexpr int kLanesPerBlock = kMxBlock / kMxPerThread;             // 4
+
+// Largest magnitude of 8 values; NaN if any of them is NaN.
+__device__ __forceinline__ float abs_max_nan(float a, float b) {
+  float r;
+  asm("{\n\t.reg .f32 x, y;\n\tabs.f32 x, %1;\n\tabs.f32 y, %2;\n\t"
+      "max.NaN.f32 %0, x, y;\n\t}" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// E8M0 scale byte of the block this thread's 8 elements belong to (lanes
+// 4b .. 4b+3 hold block b). The block maximum is a non-negative float or NaN
+// (max.NaN propagates NaN), so its bit pattern's exponent field E is 255
+// exactly for a non-finite block. All 32 lanes must call.
+__device__ __forceinline__ uint32_t block_scale8(const float4& a, const float4& b) {
+  float m = max_nan(max_nan(abs_max_nan(a.x, a.y), abs_max_nan(a.z, a.w)),
+                    max_nan(abs_max_nan(b.x, b.y), abs_max_nan(b.z, b.w)));
+  m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+  const uint32_t e = __float_as_uint(m) >> 23;  // sign is clear
+  return e == 255u ? 0xFFu : (e > 8u ? e - 8u : 0u);
+}
+
+// One 0x80 per byte of x that is non-zero (x = new ^ old codes).
+__device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
+  return (((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x) & 0x80808080u;
+}
+
+// Eight change flags in element order (bit e = element e) from the 0x80
+// bytes of nonzero_bytes for elements 0-3 (z0) and 4-7 (z1). After the
+// shifts the flags sit at bits 8e (e < 4) and 8(e - 4) + 4; multiplying by
+// 1 + 2^7 + 2^14 + 2^21 copies bit p to p, p+7, p+14 and p+21, and for these
+// eight p all copies land on distinct bits (so nothing carries), with the
+// copy of element e's flag at bit 21 + e.
+__device__ __forceinline__ uint32_t gather_flags8(uint32_t z0, uint32_t z1) {
+  return ((((z0 >> 7) | (z1 >> 3)) * 0x00204081u) >> 21) & 0xFFu;
+}
+
 template <bool MULTI>
 __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, uint8_t* stages,
                                              uint32_t* ring, int tid, int lane, int warp) {
   uint32_t posted = 0, ring_head = 0;
   bool failed = false;
-  const bool leader = (lane & 7) == 0;  // lane that owns its block's scale
+  const bool leader = (lane & (kLanesPerBlock - 1)) == 0;  // lane that owns its block's scale
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kEncStages);
     failed |= !wait_or_flag(&sh.full[s], (it / kEncStages) & 1u, a);
     const StageMeta m = sh.meta[s];
     const bool live = m.mode != kModeEnd;
+    const bool bulk = m.mode == kModeBulk;
     const uint64_t base = m.base;
     const uint32_t len = m.len;
     const uint8_t* stage = stages + size_t(s) * kStageBytes;
 
-    // ---- quantize + compare: 4 consecutive elements per thread per round
-    uint32_t nc[kEncRounds];  // new codes, element 0 in the low byte
-    uint32_t ns = 0;          // byte j: new scale of this thread's block in round j
-    uint32_t flags = 0;       // bit (j*4 + e): code e of round j changed
-    uint32_t sflags = 0;      // bit j: the block of round j changed its scale (leaders only)
+    // ---- quantize + compare: 8 consecutive elements per thread per round
+    uint32_t nc[kMxRounds][2];  // new codes, element 0 in the low byte of word 0
+    uint32_t ns = 0;            // byte j: new scale of this thread's block in round j
+    uint32_t flags = 0;         // bit 8j + e: element e of round j changed
+    uint32_t sflags = 0;        // bit j: the block of round j changed its scale (leaders only)
 #pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
-      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
-      const uint32_t lb = li / kMxBlock;  // block within the tile
-      float4 mv;
-      uint32_t pc, ps = 0;
-      if (m.mode == kModeBulk) {
-        mv = reinterpret_cast<const float4*>(stage)[j * kEncThreads + tid];
-        pc = reinterpret_cast<const uint32_t*>(stage + kStageMasterBytes)[j * kEncThreads + tid];
+    for (int j = 0; j < kMxRounds; ++j) {
+      const uint32_t slot = uint32_t(j * kEncThreads + tid);  // 8-element group within the tile
+      const uint32_t li = slot * kMxPerThread;
+      const uint32_t lb = slot / kLanesPerBlock;              // block within the tile
+      float4 v0, v1;
+      uint2 pc;
+      uint32_t ps = 0;
+      if (bulk) {
+        const float4* sm = reinterpret_cast<const float4*>(stage);
+        v0 = sm[2 * slot];
+        v1 = sm[2 * slot + 1];
+        pc = reinterpret_cast<const uint2*>(stage + kStageMasterBytes)[slot];
         if (leader) ps = stage[kStageMasterBytes + kStageCodeBytes + lb];
       } else {
         // tail or unaligned tile: elements past the end read as +0 (no effect
         // on the block maximum) and are never reported
-        float mm[4];
-        uint32_t pp = 0;
+        float mm[kMxPerThread];
+        uint32_t pp[2] = {0u, 0u};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < kMxPerThread; ++e) {
           const bool valid = li + e < len;
           mm[e] = valid ? m.master[base + li + e] : 0.0f;
-          pp |= (valid ? uint32_t(m.prev_codes[base + li + e]) : 0u) << (8 * e);
+          pp[e >> 2] |= (valid ? uint32_t(m.prev_codes[base + li + e]) : 0u) << (8 * (e & 3));
         }
-        mv = make_float4(mm[0], mm[1], mm[2], mm[3]);
-        pc = pp;
+        v0 = make_float4(mm[0], mm[1], mm[2], mm[3]);
+        v1 = make_float4(mm[4], mm[5], mm[6], mm[7]);
+        pc = make_uint2(pp[0], pp[1]);
         if (leader && lb * kMxBlock < len) ps = m.prev_scales[(base / kMxBlock) + lb];
       }
-      const uint32_t sb = mx_scale_byte(block_amax_bits(mv));
-      nc[j] = mx_codes4(mv, sb);
+      const uint32_t sb = block_scale8(v0, v1);
+      nc[j][0] = mx_codes4(v0, sb);
+      nc[j][1] = mx_codes4(v1, sb);
       ns |= sb << (8 * j);
-      uint32_t f = byte_diff_bits(nc[j], pc);
-      if (m.mode != kModeBulk) {
-        const uint32_t nvalid = li >= len ? 0u : (len - li >= 4u ? 4u : len - li);
-        f &= (1u << nvalid) - 1u;
+      uint32_t z0 = nonzero_bytes(nc[j][0] ^ pc.x), z1 = nonzero_bytes(nc[j][1] ^ pc.y);
+      if (!bulk) {
+        // keep only elements inside the tile
+        const uint32_t nvalid = li >= len ? 0u : (len - li >= 8u ? 8u : len - li);
+        const uint64_t keep =  // one 0xFF byte per valid element
+            nvalid >= 8u ? ~uint64_t(0) : (uint64_t(1) << (8 * nvalid)) - 1u;
+        z0 &= uint32_t(keep);
+        z1 &= uint32_t(keep >> 32);
       }
-      flags |= f << (4 * j);
+      flags |= gather_flags8(z0, z1) << (8 * j);
       if (leader && lb * kMxBlock < len && sb != ps) sflags |= 1u << j;
     }
     __syncwarp();
@@ -394,27 +421,25 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
 
     // ---- refresh the previous view now
 #pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
-      const uint32_t f = (flags >> (j * 4)) & 0xFu;
-      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
+    for (int j = 0; j < kMxRounds; ++j) {
+      const uint32_t f = (flags >> (8 * j)) & 0xFFu;
+      const uint32_t li = uint32_t(j * kEncThreads + tid) * kMxPerThread;
       if (f != 0u) {
-        if (m.mode == kModeBulk) {
-          *reinterpret_cast<uint32_t*>(m.prev_codes + base + li) = nc[j];
+        if (bulk) {
+          *reinterpret_cast<uint2*>(m.prev_codes + base + li) = make_uint2(nc[j][0], nc[j][1]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if ((f >> e) & 1u) m.prev_codes[base + li + e] = uint8_t(nc[j] >> (8 * e));
+          for (int e = 0; e < kMxPerThread; ++e)
+            if ((f >> e) & 1u)
+              m.prev_codes[base + li + e] = uint8_t(nc[j][e >> 2] >> (8 * (e & 3)));
         }
       }
       if ((sflags >> j) & 1u) m.prev_scales[base / kMxBlock + li / kMxBlock] = uint8_t(ns >> (8 * j));
     }
 
-    // ---- rank: codes as in the BF16 encode (byte-packed warp scan of the
-    // four per-round counts); scales by one ballot per round (at most 4 per
-    // warp and round: one per block)
-    uint32_t cnts = 0;
-#pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) cnts |= uint32_t(__popc((flags >> (4 * j)) & 0xFu)) << (8 * j);
+    // ---- rank. Codes: one warp scan of the two per-round counts in 16-bit
+    // fields (a field never exceeds 32 x 8 = 256). Scales: one ballot per round.
+    const uint32_t cnts = uint32_t(__popc(flags & 0xFFu)) | (uint32_t(__popc(flags & 0xFF00u)) << 16);
     uint32_t incl = cnts;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -422,49 +447,37 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
       if (lane >= o) incl += v;
     }
     const uint32_t excl = incl - cnts;
-    uint32_t stot = 0;   // byte j: changed scales of this warp in round j
-    uint32_t srank = 0;  // byte j: changed scales of earlier lanes of this warp in round j
     const uint32_t lt = lanemask_lt();
-#pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
-      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (sflags >> j) & 1u);
-      stot |= uint32_t(__popc(bal)) << (8 * j);
-      srank |= uint32_t(__popc(bal & lt)) << (8 * j);
-    }
+    const uint32_t bal0 = __ballot_sync(0xFFFFFFFFu, sflags & 1u);
+    const uint32_t bal1 = __ballot_sync(0xFFFFFFFFu, sflags & 2u);
+    const uint32_t stot = uint32_t(__popc(bal0)) | (uint32_t(__popc(bal1)) << 8);
+    const uint32_t srank = uint32_t(__popc(bal0 & lt)) | (uint32_t(__popc(bal1 & lt)) << 8);
     const int pc = int(it & 1u);
     if (lane == 31) sh.warp_tot[pc][warp] = incl;
     if (lane == 0) sh.warp_stot[pc][warp] = stot;
     if (compute_barrier_or(failed || !live)) break;
 
-    // codes across warps: 16-bit fields (rounds 0/2 and 1/3), as in the BF16 encode
+    // across warps, in tile order (round-major, then warp): codes in 16-bit
+    // fields (at most 8 x 256 = 2048), scales in bytes (at most 8 x 8 = 64)
     const uint32_t t = lane < kWarps ? sh.warp_tot[pc][lane] : 0u;
-    const uint32_t t02 = t & 0x00FF00FFu, t13 = (t >> 8) & 0x00FF00FFu;
-    // scales across warps: 4 byte fields, each at most 8 x 4 = 32
     const uint32_t ts = lane < kWarps ? sh.warp_stot[pc][lane] : 0u;
-    uint32_t s02 = t02, s13 = t13, ss = ts;
+    uint32_t sc = t, ss = ts;
 #pragma unroll
     for (int o = 1; o < kWarps; o <<= 1) {
-      const uint32_t v02 = __shfl_up_sync(0xFFFFFFFFu, s02, o);
-      const uint32_t v13 = __shfl_up_sync(0xFFFFFFFFu, s13, o);
+      const uint32_t vc = __shfl_up_sync(0xFFFFFFFFu, sc, o);
       const uint32_t vs = __shfl_up_sync(0xFFFFFFFFu, ss, o);
-      if (lane >= o) { s02 += v02; s13 += v13; ss += vs; }
+      if (lane >= o) { sc += vc; ss += vs; }
     }
-    const uint32_t b02 = __shfl_sync(0xFFFFFFFFu, s02 - t02, warp);
-    const uint32_t b13 = __shfl_sync(0xFFFFFFFFu, s13 - t13, warp);
+    const uint32_t bc = __shfl_sync(0xFFFFFFFFu, sc - t, warp);   // warps before this one
     const uint32_t bs = __shfl_sync(0xFFFFFFFFu, ss - ts, warp);
-    const uint32_t a02 = __shfl_sync(0xFFFFFFFFu, s02, kWarps - 1);
-    const uint32_t a13 = __shfl_sync(0xFFFFFFFFu, s13, kWarps - 1);
+    const uint32_t ac = __shfl_sync(0xFFFFFFFFu, sc, kWarps - 1);  // all warps
     const uint32_t as = __shfl_sync(0xFFFFFFFFu, ss, kWarps - 1);
-    const uint32_t tot0 = a02 & 0xFFFFu, tot1 = a13 & 0xFFFFu, tot2 = a02 >> 16, tot3 = a13 >> 16;
-    uint32_t round_off[kEncRounds];
-    round_off[0] = (b02 & 0xFFFFu) + (excl & 0xFFu);
-    round_off[1] = tot0 + (b13 & 0xFFFFu) + ((excl >> 8) & 0xFFu);
-    round_off[2] = tot0 + tot1 + (b02 >> 16) + ((excl >> 16) & 0xFFu);
-    round_off[3] = tot0 + tot1 + tot2 + (b13 >> 16) + (excl >> 24);
-    const uint32_t agg_c = tot0 + tot1 + tot2 + tot3;
-    const uint32_t stot0 = as & 0xFFu, stot1 = (as >> 8) & 0xFFu, stot2 = (as >> 16) & 0xFFu,
-                   stot3 = as >> 24;
-    const uint32_t agg_s = stot0 + stot1 + stot2 + stot3;
+    const uint32_t tot0 = ac & 0xFFFFu, tot1 = ac >> 16;
+    const uint32_t round_off0 = (bc & 0xFFFFu) + (excl & 0xFFFFu);
+    const uint32_t round_off1 = tot0 + (bc >> 16) + (excl >> 16);
+    const uint32_t agg_c = tot0 + tot1;
+    const uint32_t stot0 = as & 0xFFu;
+    const uint32_t agg_s = stot0 + ((as >> 8) & 0xFFu);
     if (tid == 0) {
       const uint64_t v = uint64_t(agg_c) | (uint64_t(agg_s) << 32);
       st_relaxed_u64(a.status + m.tile,
@@ -492,24 +505,24 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
 
     // ---- park the compacted tile
 #pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
-      uint32_t f = (flags >> (j * 4)) & 0xFu;
+    for (int j = 0; j < kMxRounds; ++j) {
+      uint32_t f = (flags >> (8 * j)) & 0xFFu;
       if (f == 0u) continue;
-      const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
-      uint32_t r = ring_head + round_off[j];
+      const uint32_t li = uint32_t(j * kEncThreads + tid) * kMxPerThread;
+      uint32_t r = ring_head + (j == 0 ? round_off0 : round_off1);
       do {
         const uint32_t e = uint32_t(__ffs(f)) - 1u;
         f &= f - 1u;
-        ring[r & kRingMask] = (li + e) | (((nc[j] >> (8 * e)) & 0xFFu) << 16);
+        const uint32_t word = (e & 4u) ? nc[j][1] : nc[j][0];
+        ring[r & kRingMask] = (li + e) | (((word >> (8 * (e & 3))) & 0xFFu) << 16);
         ++r;
       } while (f != 0u);
     }
 #pragma unroll
-    for (int j = 0; j < kEncRounds; ++j) {
+    for (int j = 0; j < kMxRounds; ++j) {
       if (!((sflags >> j) & 1u)) continue;
-      const uint32_t before = (j > 0 ? stot0 : 0u) + (j > 1 ? stot1 : 0u) + (j > 2 ? stot2 : 0u);
-      const uint32_t pos = before + ((bs >> (8 * j)) & 0xFFu) + ((srank >> (8 * j)) & 0xFFu);
-      const uint32_t lb = (uint32_t(j * kEncThreads + tid) * 4u) / kMxBlock;
+      const uint32_t pos = (j > 0 ? stot0 : 0u) + ((bs >> (8 * j)) & 0xFFu) + ((srank >> (8 * j)) & 0xFFu);
+      const uint32_t lb = uint32_t(j * kEncThreads + tid) / kLanesPerBlock;
       sh.sring[q][pos] = uint16_t(lb | (((ns >> (8 * j)) & 0xFFu) << 8));
     }
     if (tid == 0) {
@@ -618,40 +631,44 @@ int encode_mx_blocks_per_sm() {
 
 // ------------------------------------------------------------ quantize
 // The MXFP8 view of one tensor (initial state of the trainer's previous view
-// and of a receiver). 4 consecutive elements per thread; a warp covers 4
-// whole blocks, so block b of the warp is lanes 8b .. 8b+7.
+// and of a receiver), with the encode's arithmetic: 8 consecutive elements
+// per thread, so block b of a warp's 256 elements is lanes 4b .. 4b+3.
 constexpr int kQuantThreads = 256;
 
 __global__ void __launch_bounds__(kQuantThreads)
     mx_quantize_kernel(const float* __restrict__ master, uint64_t n, uint8_t* __restrict__ codes,
                        uint8_t* __restrict__ scales) {
   const bool vec = (reinterpret_cast<uintptr_t>(master) % 16u == 0) &&
-                   (reinterpret_cast<uintptr_t>(codes) % 4u == 0);
-  const uint64_t groups = (n + 3) / 4;
+                   (reinterpret_cast<uintptr_t>(codes) % 8u == 0);
+  const uint64_t groups = (n + kMxPerThread - 1) / kMxPerThread;
   const uint64_t stride = uint64_t(gridDim.x) * kQuantThreads;
   // every lane of a warp runs the same number of iterations (shuffles below)
-  const uint64_t warp_first = (uint64_t(blockIdx.x) * kQuantThreads + (threadIdx.x & ~31u));
+  const uint64_t warp_first = uint64_t(blockIdx.x) * kQuantThreads + (threadIdx.x & ~31u);
   const int lane = threadIdx.x & 31;
   for (uint64_t g0 = warp_first; g0 < groups; g0 += stride) {
-    const uint64_t i = (g0 + lane) * 4u;
-    float4 v;
-    if (vec && i + 4 <= n) {
-      v = *reinterpret_cast<const float4*>(master + i);
+    const uint64_t i = (g0 + lane) * kMxPerThread;
+    const bool full = vec && i + kMxPerThread <= n;
+    float v[kMxPerThread];
+    if (full) {
+      const float4 a = *reinterpret_cast<const float4*>(master + i);
+      const float4 b = *reinterpret_cast<const float4*>(master + i + 4);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     } else {
-      v.x = i + 0 < n ? master[i + 0] : 0.0f;
-      v.y = i + 1 < n ? master[i + 1] : 0.0f;
-      v.z = i + 2 < n ? master[i + 2] : 0.0f;
-      v.w = i + 3 < n ? master[i + 3] : 0.0f;
+#pragma unroll
+      for (int e = 0; e < kMxPerThread; ++e) v[e] = i + e < n ? master[i + e] : 0.0f;
     }
-    const uint32_t sb = mx_scale_byte(block_amax_bits(v));
-    const uint32_t c = mx_codes4(v, sb);
-    if (vec && i + 4 <= n) {
-      *reinterpret_cast<uint32_t*>(codes + i) = c;
+    const float4 a = make_float4(v[0], v[1], v[2], v[3]);
+    const float4 b = make_float4(v[4], v[5], v[6], v[7]);
+    const uint32_t sb = block_scale8(a, b);
+    const uint32_t c0 = mx_codes4(a, sb), c1 = mx_codes4(b, sb);
+    if (full) {
+      *reinterpret_cast<uint2*>(codes + i) = make_uint2(c0, c1);
     } else {
-      for (int e = 0; e < 4; ++e)
-        if (i + e < n) codes[i + e] = uint8_t(c >> (8 * e));
+      for (int e = 0; e < kMxPerThread; ++e)
+        if (i + e < n) codes[i + e] = uint8_t((e < 4 ? c0 : c1) >> (8 * (e & 3)));
     }
-    if ((lane & 7) == 0 && i < n) scales[i / kMxBlock] = uint8_t(sb);
+    if ((lane & (kLanesPerBlock - 1)) == 0 && i < n) scales[i / kMxBlock] = uint8_t(sb);
   }
 }
 
@@ -677,7 +694,7 @@ cudaError_t launch_mx_quantize(const float* master, uint64_t n, uint8_t* codes, 
                                cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  const uint64_t warps = (n + 127) / 128;
+  const uint64_t warps = (n + 32 * kMxPerThread - 1) / (32 * kMxPerThread);
   const uint64_t blocks = (warps + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
   const uint64_t cap = uint64_t(sm_count(dev)) * 8u;
   const int grid = int(blocks < cap ? blocks : cap);
