@@ -45,7 +45,8 @@ UNIT = "params/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "encode_multi_llama3_8b.md")
-ENCODE_SRC = os.path.join(ROOT, "rl_post_trainer_gb300", "csrc", "encode.cu")
+ENCODE_SRCS = [os.path.join(ROOT, "rl_post_trainer_gb300", "csrc", f)
+               for f in ("encode.cu", "encode_common.cuh")]
 
 
 # ------------------------------------------------------------- utilities
@@ -69,10 +70,14 @@ def measured_peak_gbs():
 
 def profiled_traffic():
     """dram bytes per encode launch recorded under profiles/, if the kernel
-    source is unchanged since that capture (sha256 of encode.cu)."""
+    source is unchanged since that capture (sha256 of encode.cu followed by
+    encode_common.cuh)."""
     try:
         text = open(PROFILE_SUMMARY, encoding="utf-8").read()
-        src_hash = hashlib.sha256(open(ENCODE_SRC, "rb").read()).hexdigest()
+        h = hashlib.sha256()
+        for path in ENCODE_SRCS:
+            h.update(open(path, "rb").read())
+        src_hash = h.hexdigest()
     except OSError:
         return None
     fields = {}
@@ -80,7 +85,7 @@ def profiled_traffic():
         if line.startswith("- ") and ":" in line:
             k, v = line[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    if fields.get("encode.cu sha256") != src_hash:
+    if fields.get("encode source sha256") != src_hash:
         return None
     try:
         return float(fields["traffic_bytes_per_launch_full"])
