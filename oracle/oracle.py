@@ -22,7 +22,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "pulse_oracle.c"), os.path.join(_HERE, "mx_oracle.c")]
+_SRCS = [os.path.join(_HERE, f) for f in ("pulse_oracle.c", "mx_oracle.c", "compose_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
@@ -74,6 +74,10 @@ def _load():
             lib.oracle_mxfp8_encode.restype = None
             lib.oracle_apply_u8.argtypes = [P, P, P, U64]
             lib.oracle_apply_u8.restype = None
+            lib.oracle_compose.argtypes = [P, P, U64, P, P, U64, P, P]
+            lib.oracle_compose.restype = U64
+            lib.oracle_compose_u8.argtypes = [P, P, U64, P, P, U64, P, P]
+            lib.oracle_compose_u8.restype = U64
             _lib = lib
     return _lib
 
@@ -244,3 +248,37 @@ def mxfp8_apply(codes: np.ndarray, scales: np.ndarray, patch) -> None:
     idx, val, sidx, sval = patch
     apply_u8(codes, idx, val)
     apply_u8(scales, sidx, sval)
+
+
+# ---------------------------------------------------- patch-chain composition
+
+def compose(a, b):
+    """One patch equal to patch ``a`` followed by patch ``b`` (each an (idx,
+    val) pair with strictly ascending idx): the union of the indices, the
+    later value on a shared index. Values uint16 or uint8 (both the same)."""
+    ia, va = a
+    ib, vb = b
+    _check(ia, np.uint32, "idx_a")
+    _check(ib, np.uint32, "idx_b")
+    if va.dtype != vb.dtype or va.dtype not in (np.uint16, np.uint8):
+        raise TypeError("values must both be uint16 or both uint8")
+    _check(va, va.dtype, "val_a")
+    _check(vb, vb.dtype, "val_b")
+    if ia.size != va.size or ib.size != vb.size:
+        raise ValueError("idx and val differ in length")
+    cap = max(ia.size + ib.size, 1)
+    idx = np.empty(cap, dtype=np.uint32)
+    val = np.empty(cap, dtype=va.dtype)
+    fn = _load().oracle_compose if va.dtype == np.uint16 else _load().oracle_compose_u8
+    k = fn(_ptr(ia), _ptr(va), ia.size, _ptr(ib), _ptr(vb), ib.size, _ptr(idx), _ptr(val))
+    return idx[:k].copy(), val[:k].copy()
+
+
+def compose_chain(patches):
+    """Left fold of compose over a list of patches (oldest first)."""
+    if not patches:
+        raise ValueError("empty chain")
+    out = patches[0]
+    for p in patches[1:]:
+        out = compose(out, p)
+    return out
