@@ -24,6 +24,8 @@
  *          model, with tiling and address-map metadata prepared on the CPU).
  *  [MX]    OCP "Microscaling Formats (MX) Specification" v1.0 (not one of
  *          the pages): the MXFP8 format of the lower-precision view.
+ *  [KR]    Korean write-up of the talk, section "Cross-Globe RL을 위한
+ *          Version-Aware Rollout Architecture" (sidecar catch-up).
  *  [PPLX]  "Weight transfer for RL post-training in under 2 seconds"
  *          (Perplexity), section "Statyczny harmonogram": the transfer
  *          schedule is computed once at initialisation and replayed each step.
@@ -228,6 +230,60 @@ int pulse_xor_apply_multi(pulse_plan *plan, cudaStream_t stream);
 /* Synchronise the device, then return and clear the plan's device error word
  * (PULSE_OK, PULSE_ERR_TIMEOUT or PULSE_ERR_INDEX). */
 int pulse_plan_get_error(pulse_plan *plan);
+
+/* ------------------------------------------------------------------------
+ * Patch-chain composition. [TALK] 16:40-17:04: a sidecar whose engine is
+ * behind applies the missing transitions; [PULSE] "1. PULSESync": patch
+ * values are absolute. So patch A followed by patch B equals ONE patch:
+ * every index listed by A or B, with B's value where both list it (the later
+ * patch wins), in ascending order. A chain of m patches composes by folding
+ * left; applying the result once equals applying the m patches in order.
+ * Preconditions: within each input, indices strictly ascending (what encode
+ * produces); output buffers hold count_a + count_b entries and overlap no
+ * input. Counts in are HOST values, count out is DEVICE memory.
+ * ---------------------------------------------------------------------- */
+
+/*
+ * pulse_compose -- compose two BF16 patches (16-bit values).
+ *   idx_a/val_a  device, count_a entries (the earlier patch)
+ *   idx_b/val_b  device, count_b entries (the later patch)
+ *   idx_out/val_out device, room for count_a + count_b entries
+ *   count_out    device uint64: entries written
+ * Uses a library workspace per (device, stream) (allocated on first use and
+ * grown on demand; growth synchronises `stream`). Errors: PULSE_ERR_INVALID,
+ * PULSE_ERR_RANGE (a count >= 2^32), PULSE_ERR_NOMEM, PULSE_ERR_CUDA; device:
+ * PULSE_ERR_TIMEOUT (pulse_get_error).
+ */
+int pulse_compose(const uint32_t *idx_a, const uint16_t *val_a, uint64_t count_a,
+                  const uint32_t *idx_b, const uint16_t *val_b, uint64_t count_b,
+                  uint32_t *idx_out, uint16_t *val_out, uint64_t *count_out,
+                  cudaStream_t stream);
+
+/* pulse_compose_u8 -- the same for 8-bit values (an MXFP8 code or scale segment). */
+int pulse_compose_u8(const uint32_t *idx_a, const uint8_t *val_a, uint64_t count_a,
+                     const uint32_t *idx_b, const uint8_t *val_b, uint64_t count_b,
+                     uint32_t *idx_out, uint8_t *val_out, uint64_t *count_out,
+                     cudaStream_t stream);
+
+/*
+ * pulse_compose_multi -- compose the segments of a whole model in one pass
+ * (one partition launch + one compose launch). segs: HOST array of nsegs
+ * segment pairs (copied before the call returns); value_bytes: 2 (BF16
+ * patches) or 1 (MXFP8 segments); counts_out: DEVICE, nsegs uint64.
+ */
+typedef struct pulse_compose_segment {
+    const uint32_t *idx_a;   /* device, count_a entries */
+    const void *val_a;
+    uint64_t count_a;        /* host value */
+    const uint32_t *idx_b;   /* device, count_b entries */
+    const void *val_b;
+    uint64_t count_b;        /* host value */
+    uint32_t *idx_out;       /* device, room for count_a + count_b */
+    void *val_out;
+} pulse_compose_segment;
+
+int pulse_compose_multi(const pulse_compose_segment *segs, int nsegs, int value_bytes,
+                        uint64_t *counts_out, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * MXFP8 serving view. [TALK] 13:06-14:40: rollouts are often served below

@@ -11,6 +11,8 @@ from .pulse import (  # noqa: F401
     PulseError,
     TensorSlot,
     apply,
+    compose,
+    compose_multi,
     encode,
     encode_noalloc,
     error_string,

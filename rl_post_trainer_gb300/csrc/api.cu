@@ -229,6 +229,92 @@ int launch_encode_mx_ws(MxLaunch& a, Workspace& ws, bool multi, int device, cuda
   return cuda_status(launch_encode_mx(a, multi, grid, stream));
 }
 
+// ---- compose: per-(device, stream) workspace with the merge-path splits and
+// the segment table of multi-segment calls.
+struct CmpWorkspace {
+  Workspace ws;
+  uint32_t* splits = nullptr;
+  uint64_t split_cap = 0;
+  CmpSegment* segs = nullptr;
+  uint64_t* tile_begin = nullptr;
+  int table_cap = 0;
+};
+std::map<std::pair<int, uintptr_t>, CmpWorkspace*> g_cmp_ws;
+
+CmpWorkspace* stream_cmp_workspace(int device, cudaStream_t stream) {
+  auto key = std::make_pair(device, reinterpret_cast<uintptr_t>(stream));
+  auto it = g_cmp_ws.find(key);
+  if (it != g_cmp_ws.end()) return it->second;
+  CmpWorkspace* ws = new (std::nothrow) CmpWorkspace();
+  if (ws == nullptr) return nullptr;
+  ws->ws.device = device;
+  g_cmp_ws[key] = ws;
+  return ws;
+}
+
+// Grow the split array / segment table (growth synchronises `stream`).
+int cmp_reserve(CmpWorkspace& w, uint64_t tiles, int nsegs, cudaStream_t stream) {
+  int st = workspace_reserve(w.ws, tiles, stream);
+  if (st != PULSE_OK) return st;
+  if (tiles > w.split_cap) {
+    uint64_t cap = w.split_cap ? w.split_cap : 4096;
+    while (cap < tiles) cap *= 2;
+    if (w.splits != nullptr) {
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return PULSE_ERR_CUDA;
+      cudaFree(w.splits);
+      w.splits = nullptr;
+      w.split_cap = 0;
+    }
+    if (cudaMalloc(&w.splits, cap * sizeof(uint32_t)) != cudaSuccess) return PULSE_ERR_NOMEM;
+    w.split_cap = cap;
+  }
+  if (nsegs > w.table_cap) {
+    int cap = w.table_cap ? w.table_cap : 64;
+    while (cap < nsegs) cap *= 2;
+    if (w.segs != nullptr || w.tile_begin != nullptr) {
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return PULSE_ERR_CUDA;
+      if (w.segs) cudaFree(w.segs);
+      if (w.tile_begin) cudaFree(w.tile_begin);
+      w.segs = nullptr;
+      w.tile_begin = nullptr;
+      w.table_cap = 0;
+    }
+    if (cudaMalloc(&w.segs, sizeof(CmpSegment) * size_t(cap)) != cudaSuccess ||
+        cudaMalloc(&w.tile_begin, sizeof(uint64_t) * (size_t(cap) + 1)) != cudaSuccess)
+      return PULSE_ERR_NOMEM;
+    w.table_cap = cap;
+  }
+  return PULSE_OK;
+}
+
+int compose_one(const uint32_t* idx_a, const void* val_a, uint64_t count_a, const uint32_t* idx_b,
+                const void* val_b, uint64_t count_b, uint32_t* idx_out, void* val_out,
+                uint64_t* count_out, int value_bytes, cudaStream_t stream) {
+  if (count_out == nullptr) return PULSE_ERR_INVALID;
+  if (count_a >= kMaxElems + 1 || count_b >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if ((count_a > 0 && (idx_a == nullptr || val_a == nullptr)) ||
+      (count_b > 0 && (idx_b == nullptr || val_b == nullptr)) ||
+      (count_a + count_b > 0 && (idx_out == nullptr || val_out == nullptr)))
+    return PULSE_ERR_INVALID;
+  if (count_a + count_b == 0) return cuda_status(cudaMemsetAsync(count_out, 0, sizeof(uint64_t), stream));
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  const uint64_t tiles = compose_tiles(count_a + count_b);
+  if (tiles > kMaxTiles) return PULSE_ERR_RANGE;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  CmpWorkspace* w = stream_cmp_workspace(device, stream);
+  if (w == nullptr) return PULSE_ERR_NOMEM;
+  int st = cmp_reserve(*w, tiles, 0, stream);
+  if (st != PULSE_OK) return st;
+  uint32_t epoch = 0;
+  st = workspace_next_epoch(w->ws, stream, &epoch);
+  if (st != PULSE_OK) return st;
+  CmpSegment one{idx_a, val_a, count_a, idx_b, val_b, count_b, idx_out, val_out, 0};
+  return cuda_status(launch_compose(nullptr, one, nullptr, 1, tiles, w->splits, w->ws.status,
+                                    w->ws.counters, count_out, epoch, kDefaultWaitNs, value_bytes,
+                                    stream));
+}
+
 int take_error_pair(Workspace* a, Workspace* b, cudaStream_t stream) {
   const int ea = a ? workspace_take_error(*a, stream) : PULSE_OK;
   const int eb = b ? workspace_take_error(*b, stream) : PULSE_OK;
@@ -365,8 +451,13 @@ int pulse_get_error(cudaStream_t stream) {
   const auto key = std::make_pair(device, reinterpret_cast<uintptr_t>(stream));
   auto it = g_ws.find(key);
   auto mt = g_mx_ws.find(key);
-  return take_error_pair(it == g_ws.end() ? nullptr : it->second,
-                         mt == g_mx_ws.end() ? nullptr : mt->second, stream);
+  auto ct = g_cmp_ws.find(key);
+  const int e1 = take_error_pair(it == g_ws.end() ? nullptr : it->second,
+                                 mt == g_mx_ws.end() ? nullptr : mt->second, stream);
+  const int e2 = take_error_pair(ct == g_cmp_ws.end() ? nullptr : &ct->second->ws, nullptr, stream);
+  if (e1 == PULSE_ERR_CUDA || e2 == PULSE_ERR_CUDA) return PULSE_ERR_CUDA;
+  if (e1 == PULSE_ERR_TIMEOUT || e2 == PULSE_ERR_TIMEOUT) return PULSE_ERR_TIMEOUT;
+  return e1 != PULSE_OK ? e1 : e2;
 }
 
 int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** plan_out) {
@@ -508,6 +599,69 @@ int pulse_plan_get_error(pulse_plan* plan) {
   if (plan == nullptr) return PULSE_ERR_INVALID;
   if (cudaDeviceSynchronize() != cudaSuccess) return PULSE_ERR_CUDA;
   return workspace_take_error(plan->ws, nullptr);
+}
+
+// ------------------------------------------------------------ compose
+
+int pulse_compose(const uint32_t* idx_a, const uint16_t* val_a, uint64_t count_a,
+                  const uint32_t* idx_b, const uint16_t* val_b, uint64_t count_b,
+                  uint32_t* idx_out, uint16_t* val_out, uint64_t* count_out, cudaStream_t stream) {
+  return compose_one(idx_a, val_a, count_a, idx_b, val_b, count_b, idx_out, val_out, count_out, 2,
+                     stream);
+}
+
+int pulse_compose_u8(const uint32_t* idx_a, const uint8_t* val_a, uint64_t count_a,
+                     const uint32_t* idx_b, const uint8_t* val_b, uint64_t count_b,
+                     uint32_t* idx_out, uint8_t* val_out, uint64_t* count_out, cudaStream_t stream) {
+  return compose_one(idx_a, val_a, count_a, idx_b, val_b, count_b, idx_out, val_out, count_out, 1,
+                     stream);
+}
+
+int pulse_compose_multi(const pulse_compose_segment* segs, int nsegs, int value_bytes,
+                        uint64_t* counts_out, cudaStream_t stream) {
+  if (segs == nullptr || nsegs < 1 || counts_out == nullptr) return PULSE_ERR_INVALID;
+  if (value_bytes != 1 && value_bytes != 2) return PULSE_ERR_INVALID;
+  std::vector<CmpSegment> table(static_cast<size_t>(nsegs));
+  std::vector<uint64_t> tb(static_cast<size_t>(nsegs) + 1);
+  uint64_t tiles = 0;
+  for (int i = 0; i < nsegs; ++i) {
+    const pulse_compose_segment& g = segs[i];
+    if (g.count_a >= kMaxElems + 1 || g.count_b >= kMaxElems + 1) return PULSE_ERR_RANGE;
+    if ((g.count_a > 0 && (g.idx_a == nullptr || g.val_a == nullptr)) ||
+        (g.count_b > 0 && (g.idx_b == nullptr || g.val_b == nullptr)) ||
+        (g.count_a + g.count_b > 0 && (g.idx_out == nullptr || g.val_out == nullptr)))
+      return PULSE_ERR_INVALID;
+    tb[size_t(i)] = tiles;
+    table[size_t(i)] = CmpSegment{g.idx_a, g.val_a, g.count_a, g.idx_b, g.val_b, g.count_b,
+                                  g.idx_out, g.val_out, tiles};
+    tiles += compose_tiles(g.count_a + g.count_b);
+  }
+  tb[size_t(nsegs)] = tiles;
+  if (tiles > kMaxTiles) return PULSE_ERR_RANGE;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  CmpWorkspace* w = stream_cmp_workspace(device, stream);
+  if (w == nullptr) return PULSE_ERR_NOMEM;
+  int st = cmp_reserve(*w, tiles, nsegs, stream);
+  if (st != PULSE_OK) return st;
+  // empty segments have no tile: their count is 0; the others are written
+  // by their last tile
+  if (cudaMemsetAsync(counts_out, 0, sizeof(uint64_t) * size_t(nsegs), stream) != cudaSuccess ||
+      cudaMemcpyAsync(w->segs, table.data(), sizeof(CmpSegment) * size_t(nsegs),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(w->tile_begin, tb.data(), sizeof(uint64_t) * (size_t(nsegs) + 1),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  // (copies from pageable memory are staged before cudaMemcpyAsync returns,
+  // so the host tables may go out of scope now)
+  if (tiles == 0) return PULSE_OK;
+  uint32_t epoch = 0;
+  st = workspace_next_epoch(w->ws, stream, &epoch);
+  if (st != PULSE_OK) return st;
+  return cuda_status(launch_compose(w->segs, table[0], w->tile_begin, nsegs, tiles, w->splits,
+                                    w->ws.status, w->ws.counters, counts_out, epoch,
+                                    kDefaultWaitNs, value_bytes, stream));
 }
 
 // ------------------------------------------------------------ MXFP8 view

@@ -127,6 +127,29 @@ cudaError_t launch_encode_mx(const MxLaunch& a, bool multi, int grid, cudaStream
 cudaError_t launch_mx_quantize(const float* master, uint64_t n, uint8_t* codes, uint8_t* scales,
                                cudaStream_t stream);
 
+// ---------------------------------------------------------------- compose
+// One pair of patch segments to compose (values 1 or 2 bytes wide) and its
+// output; tile_begin is the segment's first global compose tile.
+struct CmpSegment {
+  const uint32_t* idx_a;
+  const void* val_a;
+  uint64_t count_a;
+  const uint32_t* idx_b;
+  const void* val_b;
+  uint64_t count_b;
+  uint32_t* idx_out;
+  void* val_out;
+  uint64_t tile_begin;
+};
+
+uint64_t compose_tiles(uint64_t entries);
+// segs_dev == nullptr: single-segment mode using `one`.
+cudaError_t launch_compose(const CmpSegment* segs_dev, const CmpSegment& one,
+                           const uint64_t* tile_begin_dev, int nsegs, uint64_t total_tiles,
+                           uint32_t* splits, uint64_t* status, uint32_t* counters,
+                           uint64_t* counts_out, uint32_t epoch, uint64_t wait_limit_ns,
+                           int value_bytes, cudaStream_t stream);
+
 // ---------------------------------------------------------------- apply
 #ifndef PULSE_APPLY_PER_THREAD
 #define PULSE_APPLY_PER_THREAD 8

@@ -74,6 +74,19 @@ def mx_blocks(n: int) -> int:
     return (int(n) + MX_BLOCK - 1) // MX_BLOCK
 
 
+class PulseComposeSegment(ctypes.Structure):
+    _fields_ = [
+        ("idx_a", ctypes.c_void_p),
+        ("val_a", ctypes.c_void_p),
+        ("count_a", ctypes.c_uint64),
+        ("idx_b", ctypes.c_void_p),
+        ("val_b", ctypes.c_void_p),
+        ("count_b", ctypes.c_uint64),
+        ("idx_out", ctypes.c_void_p),
+        ("val_out", ctypes.c_void_p),
+    ]
+
+
 def library_path() -> str:
     return _build.LIB
 
@@ -110,6 +123,9 @@ def lib():
             "pulse_plan_get_error": ([P], I),
             "pulse_debug_encode_orphan_tile": ([P, P, U64, P, P, P, U64, P], I),
             "pulse_encode_noalloc": ([P, P, U64, P, P, P, P], I),
+            "pulse_compose": ([P, P, U64, P, P, U64, P, P, P, P], I),
+            "pulse_compose_u8": ([P, P, U64, P, P, U64, P, P, P, P], I),
+            "pulse_compose_multi": ([ctypes.POINTER(PulseComposeSegment), I, I, P, P], I),
             "pulse_mx_quantize": ([P, U64, P, P, P], I),
             "pulse_mx_encode": ([P, P, P, U64, P, P, P, P, P, P], I),
             "pulse_mx_apply": ([P, P, U64, P, P, U64, P, P, U64, P], I),
@@ -548,3 +564,79 @@ class MxPlan:
 
     def __exit__(self, *exc):
         self.close()
+
+
+# ------------------------------------------------------- patch composition
+
+def _value_kind(t: torch.Tensor) -> int:
+    if t.dtype in _U16:
+        return 2
+    if t.dtype in _U8:
+        return 1
+    raise TypeError(f"patch values must be 16-bit or 8-bit, not {t.dtype}")
+
+
+def compose(idx_a: torch.Tensor, val_a: torch.Tensor, count_a: int,
+            idx_b: torch.Tensor, val_b: torch.Tensor, count_b: int,
+            idx_out: Optional[torch.Tensor] = None, val_out: Optional[torch.Tensor] = None,
+            count_out: Optional[torch.Tensor] = None):
+    """pulse_compose / pulse_compose_u8: one patch equal to patch A (the first
+    count_a entries of idx_a/val_a) followed by patch B. Returns (idx, val,
+    count); the result is the first ``count`` entries (device int64)."""
+    _need(idx_a, "idx_a", (torch.int32, torch.uint32))
+    dev = idx_a.device
+    count_a, count_b = int(count_a), int(count_b)
+    vb = _value_kind(val_a)
+    if _value_kind(val_b) != vb:
+        raise TypeError("val_a and val_b differ in width")
+    _need(idx_a, "idx_a", (torch.int32, torch.uint32), dev, min_numel=count_a)
+    _need(val_a, "val_a", (val_a.dtype,), dev, min_numel=count_a)
+    _need(idx_b, "idx_b", (torch.int32, torch.uint32), dev, min_numel=count_b)
+    _need(val_b, "val_b", (val_b.dtype,), dev, min_numel=count_b)
+    cap = max(count_a + count_b, 1)
+    if idx_out is None:
+        idx_out = torch.empty(cap, dtype=torch.int32, device=dev)
+    if val_out is None:
+        val_out = torch.empty(cap, dtype=val_a.dtype, device=dev)
+    if count_out is None:
+        count_out = torch.empty(1, dtype=torch.int64, device=dev)
+    _need(idx_out, "idx_out", (torch.int32, torch.uint32), dev, min_numel=count_a + count_b)
+    _need(val_out, "val_out", _U16 if vb == 2 else _U8, dev, min_numel=count_a + count_b)
+    _need(count_out, "count_out", (torch.int64, torch.uint64), dev, min_numel=1)
+    fn = lib().pulse_compose if vb == 2 else lib().pulse_compose_u8
+    with torch.cuda.device(dev):
+        st = fn(_ptr(idx_a), _ptr(val_a), count_a, _ptr(idx_b), _ptr(val_b), count_b,
+                _ptr(idx_out), _ptr(val_out), _ptr(count_out), _stream(dev))
+    _raise(st, "pulse_compose")
+    return idx_out, val_out, count_out
+
+
+def compose_multi(segments, counts_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """pulse_compose_multi. ``segments``: a list of (idx_a, val_a, count_a,
+    idx_b, val_b, count_b, idx_out, val_out) with host counts; all values of
+    one width. Returns counts_out (device int64, one per segment)."""
+    if not segments:
+        raise ValueError("no segments")
+    dev = segments[0][0].device
+    vb = _value_kind(segments[0][1])
+    arr = (PulseComposeSegment * len(segments))()
+    for i, (ia, va, ka, ib, vbv, kb, io, vo) in enumerate(segments):
+        ka, kb = int(ka), int(kb)
+        for name, t in (("val_a", va), ("val_b", vbv), ("val_out", vo)):
+            if _value_kind(t) != vb:
+                raise TypeError(f"segment {i}: {name} differs in width")
+        _need(ia, "idx_a", (torch.int32, torch.uint32), dev, min_numel=ka)
+        _need(va, "val_a", (va.dtype,), dev, min_numel=ka)
+        _need(ib, "idx_b", (torch.int32, torch.uint32), dev, min_numel=kb)
+        _need(vbv, "val_b", (vbv.dtype,), dev, min_numel=kb)
+        _need(io, "idx_out", (torch.int32, torch.uint32), dev, min_numel=ka + kb)
+        _need(vo, "val_out", (vo.dtype,), dev, min_numel=ka + kb)
+        arr[i] = PulseComposeSegment(_ptr(ia), _ptr(va), ka, _ptr(ib), _ptr(vbv), kb,
+                                     _ptr(io), _ptr(vo))
+    if counts_out is None:
+        counts_out = torch.empty(len(segments), dtype=torch.int64, device=dev)
+    _need(counts_out, "counts_out", (torch.int64, torch.uint64), dev, min_numel=len(segments))
+    with torch.cuda.device(dev):
+        st = lib().pulse_compose_multi(arr, len(segments), vb, _ptr(counts_out), _stream(dev))
+    _raise(st, "pulse_compose_multi")
+    return counts_out

@@ -112,3 +112,19 @@ def test_mx_host_side_argument_checks_launch_nothing(lib):
     assert lib.pulse_mx_apply_multi_device(None, P(8), P(0)) == E.PULSE_ERR_INVALID
     assert lib.pulse_mx_plan_destroy(None) == E.PULSE_OK
     assert lib.pulse_mx_plan_num_tensors(None) == 0
+
+
+def test_compose_host_side_argument_checks_launch_nothing(lib):
+    P = ctypes.c_void_p
+    E = pulse.pulse
+    assert lib.pulse_compose(P(0), P(0), 0, P(0), P(0), 0, P(0), P(0), P(0), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_compose(P(0), P(0), 3, P(0), P(0), 0, P(0), P(0), P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_compose(P(8), P(8), 3, P(0), P(0), 0, P(0), P(0), P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_compose(P(8), P(8), 1 << 32, P(0), P(0), 0, P(8), P(8), P(8), P(0)) == E.PULSE_ERR_RANGE
+    assert lib.pulse_compose_u8(P(0), P(0), 0, P(0), P(0), 2, P(0), P(0), P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_compose_multi(None, 1, 2, P(8), P(0)) == E.PULSE_ERR_INVALID
+    seg = (pulse.pulse.PulseComposeSegment * 1)()
+    assert lib.pulse_compose_multi(seg, 1, 3, P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_compose_multi(seg, 0, 2, P(8), P(0)) == E.PULSE_ERR_INVALID
+    seg[0].count_a = 5
+    assert lib.pulse_compose_multi(seg, 1, 2, P(8), P(0)) == E.PULSE_ERR_INVALID
