@@ -425,6 +425,8 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
 
     if not args.no_e2e:
         out["e2e"] = e2e(args, wl, counts_np, dist_on)
+    if not args.no_compose:
+        out["compose"] = run_compose(args, wl, dev)   # advances the masters: runs last
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = host_cores()
         chosen, host, total = oracle_sample(specs, cfg["seed"], cfg["eta"], args.cpu_sample_params, dev)
@@ -541,6 +543,113 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak):
     }
 
 
+def run_compose(args, wl, dev, versions: int = 4):
+    """Sidecar catch-up over `versions` missing versions of the whole model:
+    encode `versions` consecutive steps (untimed), then time (a) composing
+    the chain into one patch (pulse_compose_multi, folded left) plus one
+    apply, against (b) applying the patches one after another."""
+    import rl_post_trainer_gb300 as pulse
+    specs = wl.specs
+    T = len(specs)
+    stream = torch.cuda.current_stream(dev)
+    wl.restore()
+    chain = []   # per version: (idx list, val list, host counts)
+    for v in range(versions):
+        if v > 0:
+            workloads.torch_step_(wl.master, 500 + v)
+        wl.plan.encode(wl.counts)
+        ks = wl.counts.cpu().tolist()
+        chain.append(([wl.idx[t][:ks[t]].clone() for t in range(T)],
+                      [wl.val[t][:ks[t]].clone() for t in range(T)], ks))
+    final_view = [p.clone() for p in wl.prev]
+    # ping-pong outputs sized for the largest possible composition
+    cap = [sum(c[2][t] for c in chain) for t in range(T)]
+    outs = [([torch.empty(max(cap[t], 1), dtype=torch.int32, device=dev) for t in range(T)],
+             [torch.empty(max(cap[t], 1), dtype=torch.int16, device=dev) for t in range(T)])
+            for _ in range(2)]
+    apply_plan = pulse.Plan([pulse.TensorSlot(s.numel, w=wl.w[t], idx=wl.idx[t], val=wl.val[t])
+                             for t, s in enumerate(specs)])
+
+    fold_bytes = []
+
+    def compose_chain():
+        cur_i, cur_v, cur_k = chain[0]
+        fold_bytes.clear()
+        for v in range(1, versions):
+            oi, ov = outs[v % 2]
+            nxt_i, nxt_v, nxt_k = chain[v]
+            segs = [(cur_i[t], cur_v[t], cur_k[t], nxt_i[t], nxt_v[t], nxt_k[t], oi[t], ov[t])
+                    for t in range(T)]
+            counts = pulse.compose_multi(segs)
+            out_k = counts.cpu().tolist()     # host counts feed the next fold
+            fold_bytes.append(6 * (sum(cur_k) + sum(nxt_k) + sum(out_k)))
+            cur_i, cur_v, cur_k = oi, ov, out_k
+        return cur_i, cur_v, cur_k
+
+    last_i, last_v = outs[(versions - 1) % 2]
+    composed_plan = pulse.Plan([pulse.TensorSlot(s.numel, w=wl.w[t], idx=last_i[t], val=last_v[t])
+                                for t, s in enumerate(specs)])
+
+    def apply_seq():
+        for idx_l, val_l, ks in chain:
+            for t in range(T):
+                wl.idx[t][:ks[t]].copy_(idx_l[t])
+                wl.val[t][:ks[t]].copy_(val_l[t])
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            apply_plan.apply(ks)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            yield e0.elapsed_time(e1) * 1e-3
+
+    t_cmp, t_app1, t_seq = [], [], []
+    reps = max(1, min(args.steps, 3))
+    for r in range(reps + 1):          # the first round is a warm-up
+        for w, p0 in zip(wl.w, wl.prev0):
+            w.copy_(p0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ci, cv, ck = compose_chain()
+        torch.cuda.synchronize()
+        tc = time.perf_counter() - t0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        composed_plan.apply(ck)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ta = e0.elapsed_time(e1) * 1e-3
+        for t in range(T):
+            if not torch.equal(wl.w[t], final_view[t]):
+                raise RuntimeError(f"composed catch-up differs from the final view (tensor {t})")
+        for w, p0 in zip(wl.w, wl.prev0):
+            w.copy_(p0)
+        ts = sum(apply_seq())
+        for t in range(T):
+            if not torch.equal(wl.w[t], final_view[t]):
+                raise RuntimeError(f"sequential catch-up differs from the final view (tensor {t})")
+        if r > 0:
+            t_cmp.append(tc)
+            t_app1.append(ta)
+            t_seq.append(ts)
+    if pulse.get_error(dev) != 0:
+        raise RuntimeError("device error in the compose leg")
+    apply_plan.close()
+    composed_plan.close()
+    k_in = [sum(c[2]) for c in chain]
+    k_out = sum(ck)
+    moved = sum(fold_bytes)   # every fold reads both inputs and writes its output
+    tcm, tam, tsm = float(np.mean(t_cmp)), float(np.mean(t_app1)), float(np.mean(t_seq))
+    return {
+        "versions": versions, "patch_entries": k_in, "composed_entries": k_out,
+        "compose_ms": 1e3 * tcm, "apply_composed_ms": 1e3 * tam,
+        "catch_up_composed_ms": 1e3 * (tcm + tam), "catch_up_sequential_ms": 1e3 * tsm,
+        "compose_bytes": moved, "compose_gbs": moved / tcm / 1e9,
+        "timing": "compose: host wall time of the folds (includes the host counts read "
+                  "between folds); applies: CUDA events",
+    }
+
+
 def e2e(args, wl, counts_np, dist_on):
     """Same metric through the public API with HOST buffers: every step copies
     the new FP32 master from pinned host memory, encodes, reads the patch back
@@ -608,6 +717,7 @@ def main():
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-xor", action="store_true")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8-view leg")
+    ap.add_argument("--no-compose", action="store_true", help="skip the patch-chain leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-params", type=float, default=1.2e9)

@@ -171,8 +171,10 @@ int pulse_get_error(cudaStream_t stream);
  *   apply_multi      w, idx, val
  *   xor_mask_multi   master, prev, mask
  *   xor_apply_multi  w, mask
- * idx/val of tensor t hold that tensor's own patch segment (room for n
- * entries; indices are local to the tensor). n may be 0.
+ * idx/val of tensor t hold that tensor's own patch segment (indices local to
+ * the tensor): room for n entries where encode_multi writes them or where
+ * apply_multi_device reads device counts; for apply_multi with host counts,
+ * room for the count applied is enough. n may be 0.
  * ---------------------------------------------------------------------- */
 typedef struct pulse_tensor {
     const float *master;  /* device, n floats (trainer) */

@@ -265,7 +265,8 @@ int cmp_reserve(CmpWorkspace& w, uint64_t tiles, int nsegs, cudaStream_t stream)
       w.splits = nullptr;
       w.split_cap = 0;
     }
-    if (cudaMalloc(&w.splits, cap * sizeof(uint32_t)) != cudaSuccess) return PULSE_ERR_NOMEM;
+    // two words per tile: the merge-path split, and the tile's segment
+    if (cudaMalloc(&w.splits, 2 * cap * sizeof(uint32_t)) != cudaSuccess) return PULSE_ERR_NOMEM;
     w.split_cap = cap;
   }
   if (nsegs > w.table_cap) {
@@ -310,9 +311,9 @@ int compose_one(const uint32_t* idx_a, const void* val_a, uint64_t count_a, cons
   st = workspace_next_epoch(w->ws, stream, &epoch);
   if (st != PULSE_OK) return st;
   CmpSegment one{idx_a, val_a, count_a, idx_b, val_b, count_b, idx_out, val_out, 0};
-  return cuda_status(launch_compose(nullptr, one, nullptr, 1, tiles, w->splits, w->ws.status,
-                                    w->ws.counters, count_out, epoch, kDefaultWaitNs, value_bytes,
-                                    stream));
+  return cuda_status(launch_compose(nullptr, one, nullptr, 1, tiles, w->splits,
+                                    w->splits + w->split_cap, w->ws.status, w->ws.counters,
+                                    count_out, epoch, kDefaultWaitNs, value_bytes, stream));
 }
 
 int take_error_pair(Workspace* a, Workspace* b, cudaStream_t stream) {
@@ -660,8 +661,8 @@ int pulse_compose_multi(const pulse_compose_segment* segs, int nsegs, int value_
   st = workspace_next_epoch(w->ws, stream, &epoch);
   if (st != PULSE_OK) return st;
   return cuda_status(launch_compose(w->segs, table[0], w->tile_begin, nsegs, tiles, w->splits,
-                                    w->ws.status, w->ws.counters, counts_out, epoch,
-                                    kDefaultWaitNs, value_bytes, stream));
+                                    w->splits + w->split_cap, w->ws.status, w->ws.counters,
+                                    counts_out, epoch, kDefaultWaitNs, value_bytes, stream));
 }
 
 // ------------------------------------------------------------ MXFP8 view

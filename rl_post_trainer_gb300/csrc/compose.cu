@@ -23,8 +23,14 @@
 namespace pulse {
 namespace {
 
+#ifndef PULSE_CMP_PER_THREAD
+#define PULSE_CMP_PER_THREAD 8
+#endif
+#ifndef PULSE_CMP_MIN_BLOCKS
+#define PULSE_CMP_MIN_BLOCKS 6
+#endif
 constexpr int kCmpThreads = 256;
-constexpr int kCmpPerThread = 8;
+constexpr int kCmpPerThread = PULSE_CMP_PER_THREAD;
 constexpr int kCmpTile = kCmpThreads * kCmpPerThread;  // merged positions per tile
 constexpr int kCmpWarps = kCmpThreads / 32;
 
@@ -35,6 +41,7 @@ struct CmpLaunch {
   int nsegs;
   uint64_t total_tiles;
   const uint32_t* splits;  // per tile: A entries before the tile's first merged position
+  const uint32_t* tile_seg;  // per tile: its segment (multi-segment mode)
   uint64_t* status;
   uint32_t* counters;
   uint64_t* counts_out;
@@ -73,11 +80,14 @@ __device__ __forceinline__ uint32_t merge_split_shared(const uint32_t* A, uint32
 
 template <bool MULTI>
 __global__ void __launch_bounds__(256)
-    compose_partition_kernel(const CmpLaunch a, uint32_t* splits) {
+    compose_partition_kernel(const CmpLaunch a, uint32_t* splits, uint32_t* tile_seg) {
   const uint64_t g = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (g >= a.total_tiles) return;
   int t = 0;
-  if constexpr (MULTI) t = enc::find_tensor(a.tile_begin, a.nsegs, g);
+  if constexpr (MULTI) {
+    t = enc::find_tensor(a.tile_begin, a.nsegs, g);
+    tile_seg[g] = uint32_t(t);
+  }
   const CmpSegment& s = seg_of<MULTI>(a, t);
   const uint64_t d = (g - s.tile_begin) * kCmpTile;
   splits[g] = uint32_t(merge_split_global(s.idx_a, s.count_a, s.idx_b, s.count_b, d));
@@ -97,7 +107,7 @@ struct __align__(16) CmpShared {
 };
 
 template <class V, bool MULTI>
-__global__ void __launch_bounds__(kCmpThreads)
+__global__ void __launch_bounds__(kCmpThreads, PULSE_CMP_MIN_BLOCKS)
     compose_kernel(const __grid_constant__ CmpLaunch a) {
   __shared__ CmpShared<V> sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -106,7 +116,7 @@ __global__ void __launch_bounds__(kCmpThreads)
   const uint64_t g = sh.ticket;  // tiles are taken in ticket order: predecessors already run
 
   int t = 0;
-  if constexpr (MULTI) t = enc::find_tensor(a.tile_begin, a.nsegs, g);
+  if constexpr (MULTI) t = int(a.tile_seg[g]);
   const CmpSegment& s = seg_of<MULTI>(a, t);
   const uint64_t first = s.tile_begin;
   const uint64_t total = s.count_a + s.count_b;
@@ -140,12 +150,15 @@ __global__ void __launch_bounds__(kCmpThreads)
   }
   __syncthreads();
 
-  // ---- merge 8 positions per thread
+  // ---- merge kCmpPerThread positions per thread; a position is dropped when
+  // the next merged position has the same index. The position after a
+  // thread's last one is the smaller of the next unconsumed A and B entries
+  // (or, past the tile, the first position of the next tile).
   const uint32_t n = na + nb;
   const uint32_t dd = uint32_t(tid) * kCmpPerThread;
   uint32_t mi[kCmpPerThread];
   V mv[kCmpPerThread];
-  uint32_t cnt = 0;
+  uint32_t keep = 0;  // bit e: merged position dd + e is kept
   if (dd < n) {
     uint32_t x = merge_split_shared(sh.ia, na, sh.ib, nb, dd);
     uint32_t y = dd - x;
@@ -159,22 +172,22 @@ __global__ void __launch_bounds__(kCmpThreads)
         y += take_a ? 0u : 1u;
       }
     }
-  }
-  __syncthreads();  // staged ranges no longer read: reuse ia for the merged indices
+    uint32_t after = sh.next_idx;
+    bool has_after = sh.has_next != 0;
+    if (x < na || y < nb) {
+      after = (y >= nb || (x < na && sh.ia[x] <= sh.ib[y])) ? sh.ia[x] : sh.ib[y];
+      has_after = true;
+    }
 #pragma unroll
-  for (int e = 0; e < kCmpPerThread; ++e)
-    if (dd + e < n) sh.ia[dd + e] = mi[e];
-  __syncthreads();
-  uint32_t keep = 0;  // bit e: merged position dd + e is kept
-#pragma unroll
-  for (int e = 0; e < kCmpPerThread; ++e) {
-    const uint32_t p = dd + e;
-    if (p < n) {
-      const bool dup = p + 1 < n ? sh.ia[p + 1] == mi[e] : (sh.has_next && sh.next_idx == mi[e]);
-      if (!dup) keep |= 1u << e;
+    for (int e = 0; e < kCmpPerThread; ++e) {
+      if (dd + e < n) {
+        const bool last = e + 1 == kCmpPerThread || dd + e + 1 == n;
+        const bool dup = last ? (has_after && after == mi[e]) : mi[e + 1 < kCmpPerThread ? e + 1 : e] == mi[e];
+        if (!dup) keep |= 1u << e;
+      }
     }
   }
-  cnt = uint32_t(__popc(keep));
+  const uint32_t cnt = uint32_t(__popc(keep));
 
   // ---- block scan of kept counts
   uint32_t incl = cnt;
@@ -241,7 +254,8 @@ uint64_t compose_tiles(uint64_t entries) { return (entries + kCmpTile - 1) / kCm
 
 cudaError_t launch_compose(const CmpSegment* segs_dev, const CmpSegment& one,
                            const uint64_t* tile_begin_dev, int nsegs, uint64_t total_tiles,
-                           uint32_t* splits, uint64_t* status, uint32_t* counters,
+                           uint32_t* splits, uint32_t* tile_seg, uint64_t* status,
+                           uint32_t* counters,
                            uint64_t* counts_out, uint32_t epoch, uint64_t wait_limit_ns,
                            int value_bytes, cudaStream_t stream) {
   if (total_tiles == 0) return cudaSuccess;
@@ -252,6 +266,7 @@ cudaError_t launch_compose(const CmpSegment* segs_dev, const CmpSegment& one,
   a.nsegs = nsegs;
   a.total_tiles = total_tiles;
   a.splits = splits;
+  a.tile_seg = tile_seg;
   a.status = status;
   a.counters = counters;
   a.counts_out = counts_out;
@@ -259,8 +274,8 @@ cudaError_t launch_compose(const CmpSegment* segs_dev, const CmpSegment& one,
   a.wait_limit_ns = wait_limit_ns;
   const bool multi = segs_dev != nullptr;
   const unsigned pgrid = unsigned((total_tiles + 255) / 256);
-  if (multi) compose_partition_kernel<true><<<pgrid, 256, 0, stream>>>(a, splits);
-  else compose_partition_kernel<false><<<pgrid, 256, 0, stream>>>(a, splits);
+  if (multi) compose_partition_kernel<true><<<pgrid, 256, 0, stream>>>(a, splits, tile_seg);
+  else compose_partition_kernel<false><<<pgrid, 256, 0, stream>>>(a, splits, tile_seg);
   const unsigned grid = unsigned(total_tiles);
   if (value_bytes == 2) {
     if (multi) compose_kernel<uint16_t, true><<<grid, kCmpThreads, 0, stream>>>(a);

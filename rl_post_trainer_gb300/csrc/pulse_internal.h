@@ -146,7 +146,8 @@ uint64_t compose_tiles(uint64_t entries);
 // segs_dev == nullptr: single-segment mode using `one`.
 cudaError_t launch_compose(const CmpSegment* segs_dev, const CmpSegment& one,
                            const uint64_t* tile_begin_dev, int nsegs, uint64_t total_tiles,
-                           uint32_t* splits, uint64_t* status, uint32_t* counters,
+                           uint32_t* splits, uint32_t* tile_seg, uint64_t* status,
+                           uint32_t* counters,
                            uint64_t* counts_out, uint32_t epoch, uint64_t wait_limit_ns,
                            int value_bytes, cudaStream_t stream);
 

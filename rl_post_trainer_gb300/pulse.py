@@ -316,12 +316,15 @@ class Plan:
                     continue
                 if dev is None:
                     dev = t.device
+                # patch segments need room for n entries where encode writes
+                # them; an apply-only segment needs room for the counts applied
+                room = s.n if s.master is not None else None
                 if name == "master":
                     _need(t, name, (torch.float32,), dev, s.n)
                 elif name == "idx":
-                    _need(t, name, (torch.int32, torch.uint32), dev, min_numel=s.n)
+                    _need(t, name, (torch.int32, torch.uint32), dev, min_numel=room)
                 elif name == "val":
-                    _need(t, name, _U16, dev, min_numel=s.n)
+                    _need(t, name, _U16, dev, min_numel=room)
                 else:
                     _need(t, name, _U16, dev, s.n)
             arr[i] = PulseTensor(_ptr(s.master), _ptr(s.prev), _ptr(s.w), s.n, _ptr(s.idx),
@@ -330,6 +333,8 @@ class Plan:
             raise ValueError("a plan needs at least one device buffer")
         self.device = dev
         self.ntensors = len(slots)
+        self._room = [min(s.idx.numel(), s.val.numel()) if s.idx is not None and s.val is not None
+                      else 0 for s in slots]
         handle = ctypes.c_void_p()
         with torch.cuda.device(dev):
             st = lib().pulse_plan_create(arr, len(slots), ctypes.byref(handle))
@@ -354,9 +359,15 @@ class Plan:
         with torch.cuda.device(self.device):
             if isinstance(counts, torch.Tensor) and counts.is_cuda:
                 _need(counts, "counts", (torch.int64, torch.uint64), self.device, min_numel=self.ntensors)
+                if any(r < s.n for r, s in zip(self._room, self.slots)):
+                    raise ValueError("device counts need patch segments with room for n entries")
                 st = lib().pulse_apply_multi_device(self._h, _ptr(counts), _stream(self.device))
             else:
-                host = (ctypes.c_uint64 * self.ntensors)(*[int(c) for c in counts])
+                vals = [int(c) for c in counts]
+                for t, (c, r) in enumerate(zip(vals, self._room)):
+                    if c > r:
+                        raise ValueError(f"tensor {t}: count {c} exceeds its patch segment ({r})")
+                host = (ctypes.c_uint64 * self.ntensors)(*vals)
                 st = lib().pulse_apply_multi(self._h, host, _stream(self.device))
         _raise(st, "pulse_apply_multi")
 
