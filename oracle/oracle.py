@@ -22,7 +22,8 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, f) for f in ("pulse_oracle.c", "mx_oracle.c", "compose_oracle.c")]
+_SRCS = [os.path.join(_HERE, f) for f in ("pulse_oracle.c", "mx_oracle.c", "compose_oracle.c",
+                                          "loco_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
@@ -37,8 +38,10 @@ def build(force: bool = False) -> str:
              or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(s) for s in _SRCS))
     if force or stale:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        # -ffp-contract=off: every FP32 operation rounds on its own (no FMA)
         subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-Werror",
-                        "-shared", "-fPIC", "-o", tmp, *_SRCS, "-lm"], check=True)
+                        "-ffp-contract=off", "-shared", "-fPIC", "-o", tmp, *_SRCS, "-lm"],
+                       check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -78,6 +81,10 @@ def _load():
             lib.oracle_compose.restype = U64
             lib.oracle_compose_u8.argtypes = [P, P, U64, P, P, U64, P, P]
             lib.oracle_compose_u8.restype = U64
+            lib.oracle_loco_gate.argtypes = [P, P, P, U64, P, P]
+            lib.oracle_loco_gate.restype = U64
+            lib.oracle_loco_accumulate.argtypes = [P, P, P, U64]
+            lib.oracle_loco_accumulate.restype = None
             _lib = lib
     return _lib
 
@@ -282,3 +289,32 @@ def compose_chain(patches):
     for p in patches[1:]:
         out = compose(out, p)
     return out
+
+
+# ------------------------------------------------- PULSELoCo gate (sender)
+
+def loco_gate(global_w: np.ndarray, local_w: np.ndarray, err: np.ndarray):
+    """Returns (idx uint32, val float32) of the entries that pass the
+    visibility gate; updates ``err`` (float32) in place."""
+    _check(global_w, np.float32, "global")
+    _check(local_w, np.float32, "local")
+    _check(err, np.float32, "err", writable=True)
+    n = global_w.size
+    if local_w.size != n or err.size != n:
+        raise ValueError("global, local and err differ in length")
+    idx = np.empty(max(n, 1), dtype=np.uint32)
+    val = np.empty(max(n, 1), dtype=np.float32)
+    k = _load().oracle_loco_gate(_ptr(global_w), _ptr(local_w), _ptr(err), n, _ptr(idx), _ptr(val))
+    return idx[:k].copy(), val[:k].copy()
+
+
+def loco_accumulate(acc: np.ndarray, idx: np.ndarray, val: np.ndarray) -> None:
+    """acc[idx[j]] += val[j] in order, FP32, in place."""
+    _check(acc, np.float32, "acc", writable=True)
+    _check(idx, np.uint32, "idx")
+    _check(val, np.float32, "val")
+    if idx.size != val.size:
+        raise ValueError("idx and val differ in length")
+    if idx.size and int(idx.max()) >= acc.size:
+        raise IndexError("index out of range")
+    _load().oracle_loco_accumulate(_ptr(acc), _ptr(idx), _ptr(val), idx.size)
