@@ -234,6 +234,65 @@ int pulse_xor_apply_multi(pulse_plan *plan, cudaStream_t stream);
 int pulse_plan_get_error(pulse_plan *plan);
 
 /* ------------------------------------------------------------------------
+ * PULSELoCo sender gate and receiver accumulation. [PULSE] "Metodologia:
+ * PULSE -- 2. PULSELoCo": trainers run H local steps from a shared global
+ * checkpoint, form FP32 pseudo-gradients, and synchronise only the entries
+ * that would change the BF16 view; the rest stay in an FP32 error-feedback
+ * buffer for the next round. Per element (each FP32 operation rounded once,
+ * no fused multiply-add):
+ *     d = local - global;  u = d + err;  (a NaN u is the quiet NaN 0x7FC00000)
+ *     sent  iff  RNE_bf16(global + u) != RNE_bf16(global)  (bitwise; NaN -> 0x7FC0)
+ *     sent: entry (i, u) and err = +0;  not sent: err = u.
+ * Sent entries are written in ascending index order.
+ * ---------------------------------------------------------------------- */
+
+/*
+ * pulse_loco_gate -- one tensor.
+ *   global_w, local_w  device, n floats (read only)
+ *   err                device, n floats, in/out (the error-feedback buffer)
+ *   idx_out / val_out  device, room for n uint32 / n floats
+ *   count_out          device uint64: entries sent
+ * 16-byte aligned global_w/local_w/err take the fast path. Uses the same
+ * per-(device, stream) workspace as pulse_encode. n == 0 writes count 0.
+ * Errors: PULSE_ERR_INVALID, PULSE_ERR_RANGE, PULSE_ERR_NOMEM, PULSE_ERR_CUDA;
+ * device: PULSE_ERR_TIMEOUT (pulse_get_error).
+ */
+int pulse_loco_gate(const float *global_w, const float *local_w, float *err, uint64_t n,
+                    uint32_t *idx_out, float *val_out, uint64_t *count_out, cudaStream_t stream);
+
+/*
+ * pulse_loco_accumulate -- receiver: acc[idx[j]] += val[j] (FP32) for
+ * j < count (HOST value). Within one call indices must be distinct (what the
+ * gate produces); entries with idx >= n are skipped and PULSE_ERR_INDEX is
+ * recorded for pulse_get_error(stream).
+ */
+int pulse_loco_accumulate(float *acc, uint64_t n, const uint32_t *idx, const float *val,
+                          uint64_t count, cudaStream_t stream);
+
+/* Multi-tensor form (one launch per operation for a whole model). Fields an
+ * operation does not use may be NULL: gate_multi needs global_w, local_w,
+ * err, idx, val; accumulate_multi needs acc, idx, val. */
+typedef struct pulse_loco_tensor {
+    const float *global_w;  /* device, n */
+    const float *local_w;   /* device, n */
+    float *err;             /* device, n, in/out */
+    uint64_t n;             /* elements, < 2^32 */
+    uint32_t *idx;          /* device, room for n (sent indices) */
+    float *val;             /* device, room for n (sent values) */
+    float *acc;             /* device, n (receiver accumulator) */
+} pulse_loco_tensor;
+
+typedef struct pulse_loco_plan pulse_loco_plan;
+
+int pulse_loco_plan_create(const pulse_loco_tensor *tensors, int ntensors, pulse_loco_plan **plan_out);
+int pulse_loco_plan_destroy(pulse_loco_plan *plan);
+/* counts_out: device, ntensors uint64. */
+int pulse_loco_gate_multi(pulse_loco_plan *plan, uint64_t *counts_out, cudaStream_t stream);
+/* counts_dev: device, ntensors uint64 (e.g. the counts_out of a gate). */
+int pulse_loco_accumulate_multi(pulse_loco_plan *plan, const uint64_t *counts_dev, cudaStream_t stream);
+int pulse_loco_plan_get_error(pulse_loco_plan *plan);
+
+/* ------------------------------------------------------------------------
  * Patch-chain composition. [TALK] 16:40-17:04: a sidecar whose engine is
  * behind applies the missing transitions; [PULSE] "1. PULSESync": patch
  * values are absolute. So patch A followed by patch B equals ONE patch:

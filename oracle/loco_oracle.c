@@ -20,7 +20,9 @@
  * Readings (listed with their reasons in the design notes):
  *  - pseudo-gradient d = local - global (the parameter change), FP32;
  *  - candidate u = d + err (error feedback added before the gate), FP32,
- *    each operation rounded to nearest even, no fused multiply-add;
+ *    each operation rounded to nearest even, no fused multiply-add; a NaN u
+ *    is the quiet NaN 0x7FC00000 (the payload of a NaN result differs
+ *    between processors, so it is fixed, as the BF16 view fixes it);
  *  - gate: u passes iff RNE_bf16(global + u) differs bitwise from
  *    RNE_bf16(global) (the update would change the BF16 view of the shared
  *    checkpoint), with the BF16 cast of the BF16 encode (every NaN -> 0x7FC0);
@@ -42,6 +44,14 @@ static uint32_t bits_of(float f)
     uint32_t u;
     memcpy(&u, &f, sizeof u);
     return u;
+}
+
+static float canonical_nan(void)
+{
+    const uint32_t q = 0x7FC00000u;
+    float f;
+    memcpy(&f, &q, sizeof f);
+    return f;
 }
 
 /* FP32 bits -> BF16 bits, round to nearest even, every NaN -> 0x7FC0
@@ -69,6 +79,8 @@ uint64_t oracle_loco_gate(const float *global, const float *local, float *err, u
         /* built with -ffp-contract=off: each operation rounds once */
         float d = local[i] - global[i];
         float u = d + err[i];
+        if (u != u)
+            u = canonical_nan();
         float s = global[i] + u;
         if (bf16_view(s) != bf16_view(global[i])) {
             idx_out[k] = (uint32_t)i;

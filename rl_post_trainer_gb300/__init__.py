@@ -5,6 +5,8 @@ The compute path is the CUDA library ``libpulse.so`` (C ABI in
 """
 from .pulse import (  # noqa: F401
     MX_BLOCK,
+    LocoPlan,
+    LocoTensorSlot,
     MxPlan,
     MxTensorSlot,
     Plan,
@@ -19,6 +21,8 @@ from .pulse import (  # noqa: F401
     get_error,
     lib,
     library_path,
+    loco_accumulate,
+    loco_gate,
     mx_apply,
     mx_blocks,
     mx_encode,

@@ -343,6 +343,16 @@ struct pulse_plan {
   Workspace ws;
 };
 
+struct pulse_loco_plan {
+  int device = 0;
+  int ntensors = 0;
+  uint64_t total_tiles = 0;
+  bool can_gate = false, can_accumulate = false;
+  LocoTensorDesc* desc = nullptr;   // device
+  uint64_t* tile_begin = nullptr;   // device, ntensors + 1
+  Workspace ws;
+};
+
 struct pulse_mx_plan {
   int device = 0;
   int ntensors = 0;
@@ -597,6 +607,181 @@ int pulse_xor_apply_multi(pulse_plan* plan, cudaStream_t stream) {
 }
 
 int pulse_plan_get_error(pulse_plan* plan) {
+  if (plan == nullptr) return PULSE_ERR_INVALID;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PULSE_ERR_CUDA;
+  return workspace_take_error(plan->ws, nullptr);
+}
+
+// ------------------------------------------------------------ PULSELoCo
+
+namespace {
+LocoTensorDesc make_loco_desc(const pulse_loco_tensor& t, uint64_t tile_begin) {
+  LocoTensorDesc d{};
+  d.global = t.global_w;
+  d.local = t.local_w;
+  d.err = t.err;
+  d.idx = t.idx;
+  d.val = t.val;
+  d.acc = t.acc;
+  d.n = t.n;
+  d.tile_begin = tile_begin;
+  d.bulk_ok = (t.global_w && t.local_w && t.err && aligned(t.global_w, 16) &&
+               aligned(t.local_w, 16) && aligned(t.err, 16))
+                  ? 1u
+                  : 0u;
+  return d;
+}
+}  // namespace
+
+int pulse_loco_gate(const float* global_w, const float* local_w, float* err, uint64_t n,
+                    uint32_t* idx_out, float* val_out, uint64_t* count_out, cudaStream_t stream) {
+  if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (count_out == nullptr) return PULSE_ERR_INVALID;
+  if (n > 0 && (global_w == nullptr || local_w == nullptr || err == nullptr || idx_out == nullptr ||
+                val_out == nullptr))
+    return PULSE_ERR_INVALID;
+  if (n == 0) return cuda_status(cudaMemsetAsync(count_out, 0, sizeof(uint64_t), stream));
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  const uint64_t tiles = loco_tiles(n);
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  Workspace* ws = stream_workspace(device, stream);
+  if (ws == nullptr) return PULSE_ERR_NOMEM;
+  int st = workspace_reserve(*ws, tiles, stream);
+  if (st != PULSE_OK) return st;
+  pulse_loco_tensor t{};
+  t.global_w = global_w;
+  t.local_w = local_w;
+  t.err = err;
+  t.n = n;
+  t.idx = idx_out;
+  t.val = val_out;
+  LocoLaunch a{};
+  a.one = make_loco_desc(t, 0);
+  a.ntensors = 1;
+  a.total_tiles = tiles;
+  a.status = ws->status;
+  a.counters = ws->counters;
+  a.counts_out = count_out;
+  a.wait_limit_ns = kDefaultWaitNs;
+  st = workspace_next_epoch(*ws, stream, &a.epoch);
+  if (st != PULSE_OK) return st;
+  const uint64_t cap = uint64_t(loco_grid_size(device));
+  return cuda_status(launch_loco_gate(a, false, int(tiles < cap ? tiles : cap), stream));
+}
+
+int pulse_loco_accumulate(float* acc, uint64_t n, const uint32_t* idx, const float* val,
+                          uint64_t count, cudaStream_t stream) {
+  if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (count == 0) return PULSE_OK;
+  if (acc == nullptr || idx == nullptr || val == nullptr) return PULSE_ERR_INVALID;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  uint32_t* err = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    Workspace* ws = stream_workspace(device, stream);
+    if (ws == nullptr) return PULSE_ERR_NOMEM;
+    const int st = workspace_reserve(*ws, 0, stream);
+    if (st != PULSE_OK) return st;
+    err = ws->counters + 2;
+  }
+  return cuda_status(launch_loco_accumulate(acc, n, idx, val, count, err, stream));
+}
+
+int pulse_loco_plan_create(const pulse_loco_tensor* tensors, int ntensors, pulse_loco_plan** plan_out) {
+  if (plan_out == nullptr) return PULSE_ERR_INVALID;
+  *plan_out = nullptr;
+  if (tensors == nullptr || ntensors < 1 || ntensors > kMaxTensorsPerApplyLaunch) return PULSE_ERR_INVALID;
+  pulse_loco_plan* p = new (std::nothrow) pulse_loco_plan();
+  if (p == nullptr) return PULSE_ERR_NOMEM;
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return PULSE_ERR_CUDA;
+  }
+  p->ntensors = ntensors;
+  p->can_gate = p->can_accumulate = true;
+  std::vector<LocoTensorDesc> desc;
+  std::vector<uint64_t> tb(size_t(ntensors) + 1, 0);
+  uint64_t tiles = 0;
+  for (int i = 0; i < ntensors; ++i) {
+    const pulse_loco_tensor& t = tensors[i];
+    if (t.n >= kMaxElems + 1) {
+      delete p;
+      return PULSE_ERR_RANGE;
+    }
+    tb[size_t(i)] = tiles;
+    desc.push_back(make_loco_desc(t, tiles));
+    tiles += loco_tiles(t.n);
+    if (t.n > 0) {
+      p->can_gate = p->can_gate && t.global_w && t.local_w && t.err && t.idx && t.val;
+      p->can_accumulate = p->can_accumulate && t.acc && t.idx && t.val;
+    }
+  }
+  tb[size_t(ntensors)] = tiles;
+  if (tiles > kMaxTiles) {
+    delete p;
+    return PULSE_ERR_RANGE;
+  }
+  p->total_tiles = tiles;
+  int st = PULSE_OK;
+  if (cudaMalloc(&p->desc, sizeof(LocoTensorDesc) * desc.size()) != cudaSuccess ||
+      cudaMalloc(&p->tile_begin, sizeof(uint64_t) * tb.size()) != cudaSuccess) {
+    st = PULSE_ERR_NOMEM;
+  } else if (cudaMemcpy(p->desc, desc.data(), sizeof(LocoTensorDesc) * desc.size(),
+                        cudaMemcpyHostToDevice) != cudaSuccess ||
+             cudaMemcpy(p->tile_begin, tb.data(), sizeof(uint64_t) * tb.size(),
+                        cudaMemcpyHostToDevice) != cudaSuccess) {
+    st = PULSE_ERR_CUDA;
+  } else {
+    st = workspace_reserve(p->ws, tiles, nullptr);
+    if (st == PULSE_OK && cudaDeviceSynchronize() != cudaSuccess) st = PULSE_ERR_CUDA;
+  }
+  if (st != PULSE_OK) {
+    pulse_loco_plan_destroy(p);
+    return st;
+  }
+  *plan_out = p;
+  return PULSE_OK;
+}
+
+int pulse_loco_plan_destroy(pulse_loco_plan* plan) {
+  if (plan == nullptr) return PULSE_OK;
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (plan->desc) cudaFree(plan->desc);
+  if (plan->tile_begin) cudaFree(plan->tile_begin);
+  workspace_free(plan->ws);
+  delete plan;
+  return cuda_status(e);
+}
+
+int pulse_loco_gate_multi(pulse_loco_plan* plan, uint64_t* counts_out, cudaStream_t stream) {
+  if (plan == nullptr || counts_out == nullptr || !plan->can_gate) return PULSE_ERR_INVALID;
+  if (plan->total_tiles == 0)
+    return cuda_status(cudaMemsetAsync(counts_out, 0, sizeof(uint64_t) * size_t(plan->ntensors), stream));
+  LocoLaunch a{};
+  a.tensors = plan->desc;
+  a.tile_begin = plan->tile_begin;
+  a.ntensors = plan->ntensors;
+  a.total_tiles = plan->total_tiles;
+  a.status = plan->ws.status;
+  a.counters = plan->ws.counters;
+  a.counts_out = counts_out;
+  a.wait_limit_ns = kDefaultWaitNs;
+  const int st = workspace_next_epoch(plan->ws, stream, &a.epoch);
+  if (st != PULSE_OK) return st;
+  const uint64_t cap = uint64_t(loco_grid_size(plan->device));
+  return cuda_status(launch_loco_gate(a, true, int(plan->total_tiles < cap ? plan->total_tiles : cap), stream));
+}
+
+int pulse_loco_accumulate_multi(pulse_loco_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {
+  if (plan == nullptr || counts_dev == nullptr || !plan->can_accumulate) return PULSE_ERR_INVALID;
+  return cuda_status(launch_loco_accumulate_multi(plan->desc, plan->ntensors, counts_dev,
+                                                  plan->ws.counters + 2, sm_count(plan->device) * 8,
+                                                  stream));
+}
+
+int pulse_loco_plan_get_error(pulse_loco_plan* plan) {
   if (plan == nullptr) return PULSE_ERR_INVALID;
   if (cudaDeviceSynchronize() != cudaSuccess) return PULSE_ERR_CUDA;
   return workspace_take_error(plan->ws, nullptr);

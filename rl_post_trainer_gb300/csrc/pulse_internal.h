@@ -127,6 +127,43 @@ cudaError_t launch_encode_mx(const MxLaunch& a, bool multi, int grid, cudaStream
 cudaError_t launch_mx_quantize(const float* master, uint64_t n, uint8_t* codes, uint8_t* scales,
                                cudaStream_t stream);
 
+// ---------------------------------------------------------------- PULSELoCo
+struct LocoTensorDesc {
+  const float* global;  // shared checkpoint
+  const float* local;   // this worker's parameters after its local steps
+  float* err;           // FP32 error feedback, in/out
+  uint32_t* idx;        // sent entries: indices
+  float* val;           //               values
+  float* acc;           // receiver accumulator (accumulate)
+  uint64_t n;
+  uint64_t tile_begin;  // first global gate tile of this tensor
+  uint32_t bulk_ok;     // global, local, err 16-byte aligned
+  uint32_t reserved;
+};
+
+struct LocoLaunch {
+  LocoTensorDesc one;
+  const LocoTensorDesc* tensors;
+  const uint64_t* tile_begin;
+  int ntensors;
+  uint64_t total_tiles;
+  uint64_t* status;
+  uint32_t* counters;
+  uint64_t* counts_out;
+  uint32_t epoch;
+  uint32_t first_ticket;
+  uint64_t wait_limit_ns;
+};
+
+uint64_t loco_tiles(uint64_t n);
+int loco_grid_size(int device);
+cudaError_t launch_loco_gate(const LocoLaunch& a, bool multi, int grid, cudaStream_t stream);
+cudaError_t launch_loco_accumulate(float* acc, uint64_t n, const uint32_t* idx, const float* val,
+                                   uint64_t count, uint32_t* err, cudaStream_t stream);
+cudaError_t launch_loco_accumulate_multi(const LocoTensorDesc* tensors, int ntensors,
+                                         const uint64_t* counts, uint32_t* err, int grid,
+                                         cudaStream_t stream);
+
 // ---------------------------------------------------------------- compose
 // One pair of patch segments to compose (values 1 or 2 bytes wide) and its
 // output; tile_begin is the segment's first global compose tile.

@@ -87,6 +87,18 @@ class PulseComposeSegment(ctypes.Structure):
     ]
 
 
+class PulseLocoTensor(ctypes.Structure):
+    _fields_ = [
+        ("global_w", ctypes.c_void_p),
+        ("local_w", ctypes.c_void_p),
+        ("err", ctypes.c_void_p),
+        ("n", ctypes.c_uint64),
+        ("idx", ctypes.c_void_p),
+        ("val", ctypes.c_void_p),
+        ("acc", ctypes.c_void_p),
+    ]
+
+
 def library_path() -> str:
     return _build.LIB
 
@@ -126,6 +138,13 @@ def lib():
             "pulse_compose": ([P, P, U64, P, P, U64, P, P, P, P], I),
             "pulse_compose_u8": ([P, P, U64, P, P, U64, P, P, P, P], I),
             "pulse_compose_multi": ([ctypes.POINTER(PulseComposeSegment), I, I, P, P], I),
+            "pulse_loco_gate": ([P, P, P, U64, P, P, P, P], I),
+            "pulse_loco_accumulate": ([P, U64, P, P, U64, P], I),
+            "pulse_loco_plan_create": ([ctypes.POINTER(PulseLocoTensor), I, ctypes.POINTER(P)], I),
+            "pulse_loco_plan_destroy": ([P], I),
+            "pulse_loco_gate_multi": ([P, P, P], I),
+            "pulse_loco_accumulate_multi": ([P, P, P], I),
+            "pulse_loco_plan_get_error": ([P], I),
             "pulse_mx_quantize": ([P, U64, P, P, P], I),
             "pulse_mx_encode": ([P, P, P, U64, P, P, P, P, P, P], I),
             "pulse_mx_apply": ([P, P, U64, P, P, U64, P, P, U64, P], I),
@@ -651,3 +670,126 @@ def compose_multi(segments, counts_out: Optional[torch.Tensor] = None) -> torch.
         st = lib().pulse_compose_multi(arr, len(segments), vb, _ptr(counts_out), _stream(dev))
     _raise(st, "pulse_compose_multi")
     return counts_out
+
+
+# ------------------------------------------------------------- PULSELoCo
+
+def loco_gate(global_w: torch.Tensor, local_w: torch.Tensor, err: torch.Tensor,
+              idx_out: Optional[torch.Tensor] = None, val_out: Optional[torch.Tensor] = None,
+              count_out: Optional[torch.Tensor] = None):
+    """pulse_loco_gate: returns (idx, val, count) of the entries sent; updates
+    ``err`` (the FP32 error-feedback buffer) in place."""
+    _need(global_w, "global_w", (torch.float32,))
+    dev = global_w.device
+    n = global_w.numel()
+    _need(local_w, "local_w", (torch.float32,), dev, n)
+    _need(err, "err", (torch.float32,), dev, n)
+    if idx_out is None:
+        idx_out = torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+    if val_out is None:
+        val_out = torch.empty(max(n, 1), dtype=torch.float32, device=dev)
+    if count_out is None:
+        count_out = torch.empty(1, dtype=torch.int64, device=dev)
+    _need(idx_out, "idx_out", (torch.int32, torch.uint32), dev, min_numel=n)
+    _need(val_out, "val_out", (torch.float32,), dev, min_numel=n)
+    _need(count_out, "count_out", (torch.int64, torch.uint64), dev, min_numel=1)
+    with torch.cuda.device(dev):
+        st = lib().pulse_loco_gate(_ptr(global_w), _ptr(local_w), _ptr(err), n, _ptr(idx_out),
+                                   _ptr(val_out), _ptr(count_out), _stream(dev))
+    _raise(st, "pulse_loco_gate")
+    return idx_out, val_out, count_out
+
+
+def loco_accumulate(acc: torch.Tensor, idx: torch.Tensor, val: torch.Tensor, count: int):
+    """pulse_loco_accumulate: acc[idx[j]] += val[j] for j < count (FP32)."""
+    _need(acc, "acc", (torch.float32,))
+    dev = acc.device
+    count = int(count)
+    _need(idx, "idx", (torch.int32, torch.uint32), dev, min_numel=count)
+    _need(val, "val", (torch.float32,), dev, min_numel=count)
+    with torch.cuda.device(dev):
+        st = lib().pulse_loco_accumulate(_ptr(acc), acc.numel(), _ptr(idx), _ptr(val), count,
+                                         _stream(dev))
+    _raise(st, "pulse_loco_accumulate")
+    return acc
+
+
+class LocoTensorSlot:
+    """Buffers of one model tensor for a LocoPlan (any field may be None)."""
+
+    def __init__(self, n: int, global_w=None, local_w=None, err=None, idx=None, val=None, acc=None):
+        self.n = int(n)
+        self.global_w, self.local_w, self.err = global_w, local_w, err
+        self.idx, self.val, self.acc = idx, val, acc
+
+
+class LocoPlan:
+    """pulse_loco_plan: the gate / accumulation of a whole model, one launch each."""
+
+    def __init__(self, slots: Sequence[LocoTensorSlot], device: Optional[torch.device] = None):
+        if len(slots) == 0:
+            raise ValueError("a plan needs at least one tensor")
+        self.slots = list(slots)
+        dev = device
+        arr = (PulseLocoTensor * len(slots))()
+        for i, s in enumerate(slots):
+            for name, t, dtypes, numel, room in (
+                    ("global_w", s.global_w, (torch.float32,), s.n, None),
+                    ("local_w", s.local_w, (torch.float32,), s.n, None),
+                    ("err", s.err, (torch.float32,), s.n, None),
+                    ("idx", s.idx, (torch.int32, torch.uint32), None, s.n),
+                    ("val", s.val, (torch.float32,), None, s.n),
+                    ("acc", s.acc, (torch.float32,), s.n, None)):
+                if t is None:
+                    continue
+                if dev is None:
+                    dev = t.device
+                _need(t, name, dtypes, dev, numel, room)
+            arr[i] = PulseLocoTensor(_ptr(s.global_w), _ptr(s.local_w), _ptr(s.err), s.n,
+                                     _ptr(s.idx), _ptr(s.val), _ptr(s.acc))
+        if dev is None:
+            raise ValueError("a plan needs at least one device buffer")
+        self.device = dev
+        self.ntensors = len(slots)
+        handle = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            st = lib().pulse_loco_plan_create(arr, len(slots), ctypes.byref(handle))
+        _raise(st, "pulse_loco_plan_create")
+        self._h = handle
+
+    def gate(self, counts_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        if counts_out is None:
+            counts_out = torch.empty(self.ntensors, dtype=torch.int64, device=self.device)
+        _need(counts_out, "counts_out", (torch.int64, torch.uint64), self.device, min_numel=self.ntensors)
+        with torch.cuda.device(self.device):
+            st = lib().pulse_loco_gate_multi(self._h, _ptr(counts_out), _stream(self.device))
+        _raise(st, "pulse_loco_gate_multi")
+        return counts_out
+
+    def accumulate(self, counts: torch.Tensor):
+        _need(counts, "counts", (torch.int64, torch.uint64), self.device, min_numel=self.ntensors)
+        with torch.cuda.device(self.device):
+            st = lib().pulse_loco_accumulate_multi(self._h, _ptr(counts), _stream(self.device))
+        _raise(st, "pulse_loco_accumulate_multi")
+
+    def get_error(self) -> int:
+        with torch.cuda.device(self.device):
+            return int(lib().pulse_loco_plan_get_error(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            with torch.cuda.device(self.device):
+                lib().pulse_loco_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

@@ -128,3 +128,18 @@ def test_compose_host_side_argument_checks_launch_nothing(lib):
     assert lib.pulse_compose_multi(seg, 0, 2, P(8), P(0)) == E.PULSE_ERR_INVALID
     seg[0].count_a = 5
     assert lib.pulse_compose_multi(seg, 1, 2, P(8), P(0)) == E.PULSE_ERR_INVALID
+
+
+def test_loco_host_side_argument_checks_launch_nothing(lib):
+    P = ctypes.c_void_p
+    E = pulse.pulse
+    assert lib.pulse_loco_gate(P(0), P(0), P(0), 4, P(0), P(0), P(0), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_loco_gate(P(0), P(0), P(0), 4, P(0), P(0), P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_loco_gate(P(0), P(0), P(0), 1 << 32, P(0), P(0), P(8), P(0)) == E.PULSE_ERR_RANGE
+    assert lib.pulse_loco_accumulate(P(0), 4, P(0), P(0), 0, P(0)) == E.PULSE_OK
+    assert lib.pulse_loco_accumulate(P(0), 4, P(0), P(0), 2, P(0)) == E.PULSE_ERR_INVALID
+    h = P()
+    assert lib.pulse_loco_plan_create(None, 1, ctypes.byref(h)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_loco_gate_multi(None, P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_loco_accumulate_multi(None, P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_loco_plan_destroy(None) == E.PULSE_OK

@@ -2,9 +2,9 @@
 
 What fixes the expected results here is independent of the oracle's code:
   * numpy FP32 arithmetic (IEEE, one rounding per operation) for the
-    pseudo-gradient and the error-feedback sum, and torch's CPU BF16 cast
-    (every NaN read as 0x7FC0) for the visibility test, on random and
-    special-value inputs;
+    pseudo-gradient and the error-feedback sum (a NaN sum stored as the quiet
+    NaN 0x7FC00000), and torch's CPU BF16 cast (every NaN read as 0x7FC0)
+    for the visibility test, on random and special-value inputs;
   * conservation: for every entry, the value sent (or 0) plus the new error
     equals pseudo-gradient + old error, bit for bit (nothing is lost or
     created, PULSE summary "2. PULSELoCo": what does not pass is kept);
@@ -31,6 +31,7 @@ def _bf16(x: np.ndarray) -> np.ndarray:
 def _expected(g, w, e):
     with np.errstate(all="ignore"):
         u = (w - g) + e                      # numpy float32: one rounding per op
+        u[np.isnan(u)] = np.uint32(0x7FC00000).view(np.float32)   # the quiet NaN
         s = g + u
     passed = _bf16(s) != _bf16(g)
     idx = np.nonzero(passed)[0].astype(np.uint32)
