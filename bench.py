@@ -182,6 +182,13 @@ class Workload:
                                                       mask=self.mask[i])
                                      for i, s in enumerate(specs)])
 
+    def release_views(self):
+        """Drop the BF16 views and the BF16 plan (legs that only need the
+        FP32 masters and the index buffers run after this)."""
+        self.plan.close()
+        self.prev = self.prev0 = self.w = []
+        torch.cuda.empty_cache()
+
     def restore(self):
         for p, w, p0 in zip(self.prev, self.w, self.prev0):
             p.copy_(p0)
@@ -426,7 +433,11 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
     if not args.no_e2e:
         out["e2e"] = e2e(args, wl, counts_np, dist_on)
     if not args.no_compose:
-        out["compose"] = run_compose(args, wl, dev)   # advances the masters: runs last
+        out["compose"] = run_compose(args, wl, dev)   # advances the masters
+    if not args.no_loco:
+        wl.release_views()
+        out["loco"] = run_loco(args, cfg, specs, wl, dev, rank, peak,
+                               local_steps=1 if args.no_compose else 4)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = host_cores()
         chosen, host, total = oracle_sample(specs, cfg["seed"], cfg["eta"], args.cpu_sample_params, dev)
@@ -650,6 +661,73 @@ def run_compose(args, wl, dev, versions: int = 4):
     }
 
 
+def run_loco(args, cfg, specs, wl, dev, rank, peak, local_steps):
+    """The PULSELoCo sender gate over the whole model (pulse_loco_gate_multi)
+    and the receiver's accumulation (pulse_loco_accumulate_multi): global =
+    the starting weights w0 (the same generator draws), local = the current
+    master (`local_steps` Adam-sized steps past w0), error buffer zero. The error buffer and the accumulator
+    are restored untimed before each step. Reuses the BF16 patch index
+    buffers for the sent indices."""
+    import rl_post_trainer_gb300 as pulse
+    n = wl.n
+    stream = torch.cuda.current_stream(dev)
+    gen = workloads.torch_generator(dev, cfg["seed"] + 1000 * rank)
+    glob, err, val, acc = [], [], [], []
+    for spec in specs:
+        w0 = torch.empty(spec.numel, dtype=torch.float32, device=dev)
+        workloads.torch_init_(w0, spec, gen)
+        glob.append(w0)
+        workloads.torch_update_(w0.clone(), cfg["eta"], gen)   # advances past this tensor's z
+        err.append(torch.zeros(spec.numel, dtype=torch.float32, device=dev))
+        val.append(torch.empty(spec.numel, dtype=torch.float32, device=dev))
+        acc.append(w0.clone())
+    plan = pulse.LocoPlan([pulse.LocoTensorSlot(s.numel, global_w=glob[t], local_w=wl.master[t],
+                                                err=err[t], idx=wl.idx[t], val=val[t], acc=acc[t])
+                           for t, s in enumerate(specs)])
+    counts = torch.zeros(len(specs), dtype=torch.int64, device=dev)
+
+    def restore():
+        for e in err:
+            e.zero_()
+        for a_, g_ in zip(acc, glob):
+            a_.copy_(g_)
+
+    for _ in range(args.warmup):
+        restore()
+        plan.gate(counts)
+        plan.accumulate(counts)
+    torch.cuda.synchronize()
+    tg, ta = [], []
+    for _ in range(args.steps):
+        restore()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        plan.gate(counts)
+        ev[1].record(stream)
+        plan.accumulate(counts)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        tg.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+        ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+    if plan.get_error() != 0:
+        raise RuntimeError("device error in the PULSELoCo steps")
+    k = int(counts.sum().item())
+    plan.close()
+    g_s, a_s = float(np.mean(tg)), float(np.mean(ta))
+    gate_bytes = 16.0 * n + 8.0 * k      # read global, local, err; write err; sent entries
+    acc_bytes = 16.0 * k                 # read idx, val, acc; write acc (entry-granular)
+    return {
+        "local_steps": local_steps,
+        "gate_ms": 1e3 * g_s, "accumulate_ms": 1e3 * a_s, "sent": k, "sent_fraction": k / n,
+        "gate_params_per_s": n / g_s, "gate_gbs": gate_bytes / g_s / 1e9,
+        "gate_frac_measured_peak": gate_bytes / g_s / 1e9 / peak,
+        "accumulate_gbs_entry": acc_bytes / a_s / 1e9,
+        "bytes_model": "gate 16n + 8k; accumulate 16k (entry-granular)",
+        "gpu_launches": 2 * args.steps,
+    }
+
+
 def e2e(args, wl, counts_np, dist_on):
     """Same metric through the public API with HOST buffers: every step copies
     the new FP32 master from pinned host memory, encodes, reads the patch back
@@ -718,6 +796,7 @@ def main():
     ap.add_argument("--no-xor", action="store_true")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8-view leg")
     ap.add_argument("--no-compose", action="store_true", help="skip the patch-chain leg")
+    ap.add_argument("--no-loco", action="store_true", help="skip the PULSELoCo leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-params", type=float, default=1.2e9)
