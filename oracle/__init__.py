@@ -3,8 +3,8 @@
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg use it; the product library never does. The
 arithmetic lives in ``pulse_oracle.c`` (BF16 view), ``mx_oracle.c``
-(MXFP8 view), ``compose_oracle.c`` (patch chains) and ``loco_oracle.c``
-(PULSELoCo gate): plain C, scalar loops, ascending index order; this module
+(MXFP8 view), ``compose_oracle.c`` (patch chains), ``loco_oracle.c``
+(PULSELoCo gate) and ``pack_oracle.c`` (index packing): plain C, scalar loops, ascending index order; this module
 compiles them with gcc and wraps them for numpy arrays. It imports nothing from the CUDA package.
 """
 from .oracle import (  # noqa: F401
@@ -31,4 +31,8 @@ from .oracle import (  # noqa: F401
     compose_chain,
     loco_gate,
     loco_accumulate,
+    PACK_BLOCK,
+    PACK_CHUNK,
+    pack_indices,
+    unpack_indices,
 )

@@ -23,7 +23,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRCS = [os.path.join(_HERE, f) for f in ("pulse_oracle.c", "mx_oracle.c", "compose_oracle.c",
-                                          "loco_oracle.c")]
+                                          "loco_oracle.c", "pack_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
@@ -85,6 +85,10 @@ def _load():
             lib.oracle_loco_gate.restype = U64
             lib.oracle_loco_accumulate.argtypes = [P, P, P, U64]
             lib.oracle_loco_accumulate.restype = None
+            lib.oracle_pack_indices.argtypes = [P, U64, P, P, P, P]
+            lib.oracle_pack_indices.restype = U64
+            lib.oracle_unpack_indices.argtypes = [P, P, P, P, U64, P]
+            lib.oracle_unpack_indices.restype = None
             _lib = lib
     return _lib
 
@@ -318,3 +322,37 @@ def loco_accumulate(acc: np.ndarray, idx: np.ndarray, val: np.ndarray) -> None:
     if idx.size and int(idx.max()) >= acc.size:
         raise IndexError("index out of range")
     _load().oracle_loco_accumulate(_ptr(acc), _ptr(idx), _ptr(val), idx.size)
+
+
+# ------------------------------------------------------ index packing
+
+PACK_BLOCK = 128
+PACK_CHUNK = 4096   # entries per independently decodable chunk (32 blocks)
+
+
+def pack_indices(idx: np.ndarray):
+    """Returns (firsts uint32[B], widths uint8[B], chunk_off uint64[C],
+    payload uint8[...]) for strictly ascending uint32 indices."""
+    _check(idx, np.uint32, "idx")
+    k = idx.size
+    nb = (k + PACK_BLOCK - 1) // PACK_BLOCK
+    nc = (k + PACK_CHUNK - 1) // PACK_CHUNK
+    firsts = np.zeros(max(nb, 1), dtype=np.uint32)
+    widths = np.zeros(max(nb, 1), dtype=np.uint8)
+    chunk_off = np.zeros(max(nc, 1), dtype=np.uint64)
+    payload = np.zeros(max(nb * 512, 1), dtype=np.uint8)
+    size = _load().oracle_pack_indices(_ptr(idx), k, _ptr(firsts), _ptr(widths), _ptr(chunk_off),
+                                       _ptr(payload))
+    return firsts[:nb].copy(), widths[:nb].copy(), chunk_off[:nc].copy(), payload[:size].copy()
+
+
+def unpack_indices(firsts, widths, chunk_off, payload, k: int) -> np.ndarray:
+    _check(firsts, np.uint32, "firsts")
+    _check(widths, np.uint8, "widths")
+    _check(chunk_off, np.uint64, "chunk_off")
+    _check(payload, np.uint8, "payload")
+    out = np.empty(max(int(k), 1), dtype=np.uint32)
+    pl = payload if payload.size else np.zeros(1, np.uint8)
+    _load().oracle_unpack_indices(_ptr(firsts), _ptr(widths), _ptr(chunk_off), _ptr(pl), int(k),
+                                  _ptr(out))
+    return out[:int(k)].copy()
