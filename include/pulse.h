@@ -293,6 +293,52 @@ int pulse_loco_accumulate_multi(pulse_loco_plan *plan, const uint64_t *counts_de
 int pulse_loco_plan_get_error(pulse_loco_plan *plan);
 
 /* ------------------------------------------------------------------------
+ * Codec-friendly index packing. [PULSE] "1. PULSESync -- Compressione":
+ * patches are further compressed with general codecs (zstd); [XOR]
+ * "Pipeline'i GPU'lara tasimak": byte-oriented LZ4 on the GPU, and
+ * trainer-side compression latency matters. The pages leave the index
+ * representation open; this format (a reading of this library) turns the
+ * strictly ascending uint32 indices of a patch segment into small packed
+ * gaps before such a codec:
+ *  - blocks of PULSE_PACK_BLOCK = 128 entries (the last may be shorter);
+ *    firsts[i] = block i's first index;
+ *  - gap of slot s = idx[128 i + s + 1] - idx[128 i + s] - 1;
+ *    widths[i] = bit length of the block's largest gap (0 if none);
+ *  - block i's payload = 16 * widths[i] bytes: slot s in bits
+ *    [s w, s w + w) of a little-endian bit string (bit t = bit t % 8 of
+ *    byte t / 8), unused bits 0; payloads back to back in block order;
+ *  - chunks of 32 blocks (PULSE_PACK_CHUNK = 4096 entries):
+ *    chunk_off[c] = byte offset of block 32 c's payload, so each chunk
+ *    decodes independently.
+ * ---------------------------------------------------------------------- */
+#define PULSE_PACK_BLOCK 128
+#define PULSE_PACK_CHUNK 4096
+
+/*
+ * pulse_pack_indices -- pack count indices (DEVICE, strictly ascending).
+ *   firsts     device, ceil(count / 128) uint32
+ *   widths     device, ceil(count / 128) uint8
+ *   chunk_off  device, ceil(count / 4096) uint64
+ *   payload    device, 16-byte aligned, room for 512 * ceil(count / 128)
+ *              bytes (the widest case)
+ *   payload_bytes  device uint64: payload bytes written
+ * Uses the per-(device, stream) workspace of pulse_encode. count == 0 writes
+ * payload_bytes = 0. Errors: PULSE_ERR_INVALID, PULSE_ERR_RANGE,
+ * PULSE_ERR_NOMEM, PULSE_ERR_CUDA; device: PULSE_ERR_TIMEOUT.
+ */
+int pulse_pack_indices(const uint32_t *idx, uint64_t count, uint32_t *firsts, uint8_t *widths,
+                       uint64_t *chunk_off, uint8_t *payload, uint64_t *payload_bytes,
+                       cudaStream_t stream);
+
+/*
+ * pulse_unpack_indices -- the inverse: rebuild count indices (count is a
+ * HOST value) into idx_out (device, count uint32). payload 4-byte aligned.
+ */
+int pulse_unpack_indices(const uint32_t *firsts, const uint8_t *widths, const uint64_t *chunk_off,
+                         const uint8_t *payload, uint64_t count, uint32_t *idx_out,
+                         cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Patch-chain composition. [TALK] 16:40-17:04: a sidecar whose engine is
  * behind applies the missing transitions; [PULSE] "1. PULSESync": patch
  * values are absolute. So patch A followed by patch B equals ONE patch:

@@ -27,6 +27,8 @@ from .pulse import (  # noqa: F401
     mx_blocks,
     mx_encode,
     mx_quantize,
+    pack_indices,
+    unpack_indices,
     tile_elems,
     xor_apply,
     xor_mask,

@@ -787,6 +787,45 @@ int pulse_loco_plan_get_error(pulse_loco_plan* plan) {
   return workspace_take_error(plan->ws, nullptr);
 }
 
+// ------------------------------------------------------------ index packing
+
+int pulse_pack_indices(const uint32_t* idx, uint64_t count, uint32_t* firsts, uint8_t* widths,
+                       uint64_t* chunk_off, uint8_t* payload, uint64_t* payload_bytes,
+                       cudaStream_t stream) {
+  if (count >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (payload_bytes == nullptr) return PULSE_ERR_INVALID;
+  if (count > 0 && (idx == nullptr || firsts == nullptr || widths == nullptr ||
+                    chunk_off == nullptr || payload == nullptr))
+    return PULSE_ERR_INVALID;
+  if (count > 0 && !aligned(payload, 16)) return PULSE_ERR_INVALID;
+  if (count == 0) return cuda_status(cudaMemsetAsync(payload_bytes, 0, sizeof(uint64_t), stream));
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  const uint64_t chunks = pack_chunks(count);
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  Workspace* ws = stream_workspace(device, stream);
+  if (ws == nullptr) return PULSE_ERR_NOMEM;
+  int st = workspace_reserve(*ws, chunks, stream);
+  if (st != PULSE_OK) return st;
+  uint32_t epoch = 0;
+  st = workspace_next_epoch(*ws, stream, &epoch);
+  if (st != PULSE_OK) return st;
+  return cuda_status(launch_pack(idx, count, firsts, widths, chunk_off, payload, payload_bytes,
+                                 ws->status, ws->counters, epoch, kDefaultWaitNs, stream));
+}
+
+int pulse_unpack_indices(const uint32_t* firsts, const uint8_t* widths, const uint64_t* chunk_off,
+                         const uint8_t* payload, uint64_t count, uint32_t* idx_out,
+                         cudaStream_t stream) {
+  if (count >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (count == 0) return PULSE_OK;
+  if (firsts == nullptr || widths == nullptr || chunk_off == nullptr || payload == nullptr ||
+      idx_out == nullptr)
+    return PULSE_ERR_INVALID;
+  if (!aligned(payload, 4)) return PULSE_ERR_INVALID;
+  return cuda_status(launch_unpack(firsts, widths, chunk_off, payload, count, idx_out, stream));
+}
+
 // ------------------------------------------------------------ compose
 
 int pulse_compose(const uint32_t* idx_a, const uint16_t* val_a, uint64_t count_a,

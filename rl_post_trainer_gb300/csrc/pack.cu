@@ -1,0 +1,254 @@
+// pack.cu -- codec-friendly packing of patch indices and its inverse.
+//
+// The pages compress patches with byte-oriented general codecs (PULSE
+// summary, "1. PULSESync -- Compressione": zstd; humansand.ai summary,
+// "Pipeline'i GPU'lara tasimak": LZ4 on nvCOMP, no entropy stage) and note
+// that trainer-side compression latency can eat the gain. This step turns
+// the ascending indices into small bit-packed gaps on the GPU, before such a
+// codec:
+//  * blocks of 128 entries: firsts[i] = first index, widths[i] = bit length
+//    of the largest gap (gap = next - previous - 1), payload = 16 * width
+//    bytes holding the 127 gaps as one little-endian bit string;
+//  * chunks of 32 blocks (4096 entries): chunk_off[c] = byte offset of the
+//    chunk's first payload, so every chunk decodes on its own.
+//
+// Pack: one CTA per chunk, in ticket order; each warp measures and packs 4
+// blocks (bits OR-ed into shared-memory words); the chunk's payload offset is
+// the exclusive prefix of the chunk sizes, found with the decoupled look-back
+// shared with the encode kernels (warp 0), counted in 16-byte units.
+// Unpack: one CTA per chunk; each warp extracts a block's gaps and rebuilds
+// its indices with a warp scan.
+#include "encode_common.cuh"
+
+namespace pulse {
+namespace {
+
+constexpr int kPackBlock = 128;
+constexpr int kPackChunkBlocks = 32;
+constexpr int kPackChunk = kPackBlock * kPackChunkBlocks;  // 4096 entries
+constexpr int kPackThreads = 256;
+constexpr int kPackWarps = kPackThreads / 32;
+constexpr int kBlocksPerWarp = kPackChunkBlocks / kPackWarps;  // 4
+
+struct PackLaunch {
+  const uint32_t* idx;
+  uint64_t count;
+  uint32_t* firsts;
+  uint8_t* widths;
+  uint64_t* chunk_off;
+  uint8_t* payload;
+  uint64_t* payload_bytes;
+  uint64_t total_chunks;
+  uint64_t* status;
+  uint32_t* counters;
+  uint32_t epoch;
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ uint32_t bit_width(uint32_t v) { return v ? 32u - __clz(v) : 0u; }
+
+__global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constant__ PackLaunch a) {
+  __shared__ uint32_t words[kPackWarps][kPackBlock];  // one block's packed words per warp
+  __shared__ uint32_t width_of[kPackChunkBlocks];
+  __shared__ uint32_t ticket, prefix16;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) ticket = atomicAdd(a.counters + 0, 1u);
+  __syncthreads();
+  const uint64_t c = ticket;  // chunks are taken in ticket order: predecessors already run
+  const uint64_t chunk_first = c * kPackChunk;
+
+  // ---- widths and firsts; the gaps stay in registers
+  uint32_t gap[kBlocksPerWarp][4];
+  uint32_t cnt_blk[kBlocksPerWarp];
+#pragma unroll
+  for (int q = 0; q < kBlocksPerWarp; ++q) {
+    const int lb = warp * kBlocksPerWarp + q;
+    const uint64_t start = chunk_first + uint64_t(lb) * kPackBlock;
+    const uint32_t cnt = start < a.count ? uint32_t(a.count - start < kPackBlock ? a.count - start : kPackBlock) : 0u;
+    cnt_blk[q] = cnt;
+    uint32_t v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+      v[e] = j < cnt ? a.idx[start + j] : 0u;
+    }
+    const uint32_t before = __shfl_up_sync(0xFFFFFFFFu, v[3], 1);  // lane - 1's last entry
+    uint32_t mx = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+      const uint32_t prev = e == 0 ? before : v[e - 1];
+      gap[q][e] = (j >= 1 && j < cnt) ? v[e] - prev - 1u : 0u;
+      mx = max(mx, gap[q][e]);
+    }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if (lane == 0) {
+      width_of[lb] = cnt ? bit_width(mx) : 0u;
+      if (cnt) {
+        a.firsts[start / kPackBlock] = v[0];
+        a.widths[start / kPackBlock] = uint8_t(bit_width(mx));
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- the chunk's payload offset (16-byte units): look-back by warp 0
+  if (warp == 0) {
+    const uint32_t wl = width_of[lane];
+    const uint32_t agg = __reduce_add_sync(0xFFFFFFFFu, wl);
+    if (lane == 0) st_relaxed_u64(a.status + c, make_status(c == 0 ? kFlagPrefix : kFlagAggregate, a.epoch, agg));
+    uint32_t p = 0;
+    if (c != 0) {
+      uint64_t win[enc::kLookbackPerLane];
+      enc::load_window<enc::StatusEpoch>(a, int64_t(c) - 1, 0, lane, win);
+      p = enc::resolve_prefix<enc::StatusEpoch>(a, c, 0, agg, lane, win);
+    }
+    if (lane == 0) {
+      prefix16 = p;
+      a.chunk_off[c] = uint64_t(p) * 16u;
+      if (c + 1 == a.total_chunks) *a.payload_bytes = (uint64_t(p) + agg) * 16u;
+    }
+  }
+  __syncthreads();
+
+  // ---- pack each block's gaps into words and write them out
+  uint32_t off16 = prefix16;
+  for (int q = 0; q < warp * kBlocksPerWarp; ++q) off16 += width_of[q];
+#pragma unroll
+  for (int q = 0; q < kBlocksPerWarp; ++q) {
+    const int lb = warp * kBlocksPerWarp + q;
+    const uint32_t b = width_of[lb];
+    if (b != 0u) {  // warp-uniform
+      const uint32_t nwords = 4u * b;
+      for (uint32_t w = lane; w < nwords; w += 32) words[warp][w] = 0u;
+      __syncwarp();
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+        if (j >= 1 && j < cnt_blk[q] && gap[q][e] != 0u) {
+          const uint32_t bit = (j - 1u) * b;
+          const uint32_t w0 = bit >> 5, sh = bit & 31u;
+          atomicOr(&words[warp][w0], gap[q][e] << sh);
+          if (sh + b > 32u) atomicOr(&words[warp][w0 + 1], gap[q][e] >> (32u - sh));
+        }
+      }
+      __syncwarp();
+      uint32_t* dst = reinterpret_cast<uint32_t*>(a.payload + uint64_t(off16) * 16u);
+      for (uint32_t w = lane; w < nwords; w += 32) dst[w] = words[warp][w];
+      __syncwarp();
+    }
+    off16 += b;
+  }
+
+  // the last CTA to finish rewinds the ticket and finish counters
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t done = atomicAdd(a.counters + 1, 1u);
+    if (done == gridDim.x - 1) {
+      atomicExch(a.counters + 0, 0u);
+      atomicExch(a.counters + 1, 0u);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kPackThreads)
+    unpack_kernel(const uint32_t* __restrict__ firsts, const uint8_t* __restrict__ widths,
+                  const uint64_t* __restrict__ chunk_off, const uint8_t* __restrict__ payload,
+                  uint64_t count, uint32_t* __restrict__ idx_out) {
+  __shared__ uint32_t words[kPackWarps][kPackBlock + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint64_t c = blockIdx.x;
+  const uint64_t chunk_first = c * kPackChunk;
+  const uint64_t nblocks = (count + kPackBlock - 1) / kPackBlock;
+  // widths of the chunk's blocks and their exclusive prefix (16-byte units)
+  const uint64_t gb_lane = c * kPackChunkBlocks + uint64_t(lane);
+  const uint32_t wl = gb_lane < nblocks ? widths[gb_lane] : 0u;
+  uint32_t incl = wl;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const uint64_t base_off = chunk_off[c];
+#pragma unroll
+  for (int q = 0; q < kBlocksPerWarp; ++q) {
+    const int lb = warp * kBlocksPerWarp + q;
+    const uint32_t b = __shfl_sync(0xFFFFFFFFu, wl, lb);
+    const uint32_t pre = __shfl_sync(0xFFFFFFFFu, incl - wl, lb);
+    const uint64_t start = chunk_first + uint64_t(lb) * kPackBlock;
+    if (start >= count) break;  // warp-uniform
+    const uint32_t cnt = uint32_t(count - start < kPackBlock ? count - start : kPackBlock);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(payload + base_off + uint64_t(pre) * 16u);
+    for (uint32_t w = lane; w < 4u * b; w += 32) words[warp][w] = src[w];
+    if (lane == 0) words[warp][4u * b] = 0u;  // a zero word past the end for two-word reads
+    __syncwarp();
+    // x_j = gap_j + 1 for j >= 1, x_0 = 0; idx_j = first + inclusive sum of x
+    uint32_t x[4];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+      uint32_t g = 0;
+      if (j >= 1 && j < cnt && b != 0u) {
+        const uint32_t bit = (j - 1u) * b;
+        const uint32_t w0 = bit >> 5, sh = bit & 31u;
+        const uint64_t two = uint64_t(words[warp][w0]) | (uint64_t(words[warp][w0 + 1]) << 32);
+        g = uint32_t((two >> sh) & ((b == 32u) ? 0xFFFFFFFFull : ((1ull << b) - 1ull)));
+      }
+      x[e] = (j >= 1 && j < cnt) ? g + 1u : 0u;
+      sum += x[e];
+    }
+    uint32_t run = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, run, o);
+      if (lane >= o) run += v;
+    }
+    uint32_t cur = firsts[start / kPackBlock] + (run - sum);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+      cur += x[e];
+      if (j < cnt) idx_out[start + j] = cur;
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+uint64_t pack_chunks(uint64_t count) { return (count + kPackChunk - 1) / kPackChunk; }
+
+cudaError_t launch_pack(const uint32_t* idx, uint64_t count, uint32_t* firsts, uint8_t* widths,
+                        uint64_t* chunk_off, uint8_t* payload, uint64_t* payload_bytes,
+                        uint64_t* status, uint32_t* counters, uint32_t epoch,
+                        uint64_t wait_limit_ns, cudaStream_t stream) {
+  PackLaunch a{};
+  a.idx = idx;
+  a.count = count;
+  a.firsts = firsts;
+  a.widths = widths;
+  a.chunk_off = chunk_off;
+  a.payload = payload;
+  a.payload_bytes = payload_bytes;
+  a.total_chunks = pack_chunks(count);
+  a.status = status;
+  a.counters = counters;
+  a.epoch = epoch;
+  a.wait_limit_ns = wait_limit_ns;
+  if (a.total_chunks == 0) return cudaSuccess;
+  pack_kernel<<<unsigned(a.total_chunks), kPackThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const uint32_t* firsts, const uint8_t* widths, const uint64_t* chunk_off,
+                          const uint8_t* payload, uint64_t count, uint32_t* idx_out,
+                          cudaStream_t stream) {
+  const uint64_t chunks = pack_chunks(count);
+  if (chunks == 0) return cudaSuccess;
+  unpack_kernel<<<unsigned(chunks), kPackThreads, 0, stream>>>(firsts, widths, chunk_off, payload,
+                                                               count, idx_out);
+  return cudaGetLastError();
+}
+
+}  // namespace pulse

@@ -164,6 +164,16 @@ cudaError_t launch_loco_accumulate_multi(const LocoTensorDesc* tensors, int nten
                                          const uint64_t* counts, uint32_t* err, int grid,
                                          cudaStream_t stream);
 
+// ---------------------------------------------------------------- index packing
+uint64_t pack_chunks(uint64_t count);
+cudaError_t launch_pack(const uint32_t* idx, uint64_t count, uint32_t* firsts, uint8_t* widths,
+                        uint64_t* chunk_off, uint8_t* payload, uint64_t* payload_bytes,
+                        uint64_t* status, uint32_t* counters, uint32_t epoch,
+                        uint64_t wait_limit_ns, cudaStream_t stream);
+cudaError_t launch_unpack(const uint32_t* firsts, const uint8_t* widths, const uint64_t* chunk_off,
+                          const uint8_t* payload, uint64_t count, uint32_t* idx_out,
+                          cudaStream_t stream);
+
 // ---------------------------------------------------------------- compose
 // One pair of patch segments to compose (values 1 or 2 bytes wide) and its
 // output; tile_begin is the segment's first global compose tile.

@@ -145,6 +145,8 @@ def lib():
             "pulse_loco_gate_multi": ([P, P, P], I),
             "pulse_loco_accumulate_multi": ([P, P, P], I),
             "pulse_loco_plan_get_error": ([P], I),
+            "pulse_pack_indices": ([P, U64, P, P, P, P, P, P], I),
+            "pulse_unpack_indices": ([P, P, P, P, U64, P, P], I),
             "pulse_mx_quantize": ([P, U64, P, P, P], I),
             "pulse_mx_encode": ([P, P, P, U64, P, P, P, P, P, P], I),
             "pulse_mx_apply": ([P, P, U64, P, P, U64, P, P, U64, P], I),
@@ -793,3 +795,52 @@ class LocoPlan:
 
     def __exit__(self, *exc):
         self.close()
+
+
+# ------------------------------------------------------------ index packing
+
+PACK_BLOCK = 128
+PACK_CHUNK = 4096
+
+
+def pack_indices(idx: torch.Tensor, count: int):
+    """pulse_pack_indices on the first ``count`` entries of ``idx``. Returns
+    (firsts, widths, chunk_off, payload, payload_bytes); the packed payload is
+    the first ``payload_bytes`` bytes (device int64 tensor) of ``payload``."""
+    _need(idx, "idx", (torch.int32, torch.uint32))
+    dev = idx.device
+    count = int(count)
+    _need(idx, "idx", (torch.int32, torch.uint32), dev, min_numel=count)
+    nb = (count + PACK_BLOCK - 1) // PACK_BLOCK
+    nc = (count + PACK_CHUNK - 1) // PACK_CHUNK
+    firsts = torch.empty(max(nb, 1), dtype=torch.int32, device=dev)
+    widths = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+    chunk_off = torch.empty(max(nc, 1), dtype=torch.int64, device=dev)
+    payload = torch.empty(max(512 * nb, 16), dtype=torch.uint8, device=dev)
+    payload_bytes = torch.empty(1, dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().pulse_pack_indices(_ptr(idx), count, _ptr(firsts), _ptr(widths), _ptr(chunk_off),
+                                      _ptr(payload), _ptr(payload_bytes), _stream(dev))
+    _raise(st, "pulse_pack_indices")
+    return firsts, widths, chunk_off, payload, payload_bytes
+
+
+def unpack_indices(firsts: torch.Tensor, widths: torch.Tensor, chunk_off: torch.Tensor,
+                   payload: torch.Tensor, count: int, idx_out: Optional[torch.Tensor] = None):
+    """pulse_unpack_indices: the ``count`` indices of a packed segment."""
+    dev = firsts.device
+    count = int(count)
+    nb = (count + PACK_BLOCK - 1) // PACK_BLOCK
+    nc = (count + PACK_CHUNK - 1) // PACK_CHUNK
+    _need(firsts, "firsts", (torch.int32, torch.uint32), dev, min_numel=nb)
+    _need(widths, "widths", _U8, dev, min_numel=nb)
+    _need(chunk_off, "chunk_off", (torch.int64, torch.uint64), dev, min_numel=nc)
+    _need(payload, "payload", _U8, dev)
+    if idx_out is None:
+        idx_out = torch.empty(max(count, 1), dtype=torch.int32, device=dev)
+    _need(idx_out, "idx_out", (torch.int32, torch.uint32), dev, min_numel=count)
+    with torch.cuda.device(dev):
+        st = lib().pulse_unpack_indices(_ptr(firsts), _ptr(widths), _ptr(chunk_off), _ptr(payload),
+                                        count, _ptr(idx_out), _stream(dev))
+    _raise(st, "pulse_unpack_indices")
+    return idx_out
