@@ -385,8 +385,10 @@ class Plan:
                 st = lib().pulse_apply_multi_device(self._h, _ptr(counts), _stream(self.device))
             else:
                 vals = [int(c) for c in counts]
+                # the library reads min(count, n) entries (a larger count is
+                # clamped and reported as PULSE_ERR_INDEX)
                 for t, (c, r) in enumerate(zip(vals, self._room)):
-                    if c > r:
+                    if min(c, self.slots[t].n) > r:
                         raise ValueError(f"tensor {t}: count {c} exceeds its patch segment ({r})")
                 host = (ctypes.c_uint64 * self.ntensors)(*vals)
                 st = lib().pulse_apply_multi(self._h, host, _stream(self.device))
