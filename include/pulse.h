@@ -214,10 +214,14 @@ uint64_t pulse_plan_num_tiles(const pulse_plan *plan);
 int pulse_encode_multi(pulse_plan *plan, uint64_t *counts_out, cudaStream_t stream);
 
 /*
- * Apply every tensor's patch segment in one launch. counts_host (HOST,
- * ntensors uint64) gives each segment's length; it is copied before the call
- * returns. Entries with idx >= n of their tensor are skipped and recorded as
- * PULSE_ERR_INDEX in the plan's error word.
+ * Apply every tensor's patch segment (one partition launch and one apply
+ * launch for the whole model). counts_host (HOST, ntensors uint64) gives each
+ * segment's length; it is copied before the call returns. Each segment must
+ * list ascending indices (what encode writes): the tensor is cut into chunks,
+ * each chunk's entries are found by binary search, and a chunk with many
+ * entries is read-modified-written in shared memory and its changed 32-byte
+ * sectors written back whole. Entries outside their chunk or with idx >= n
+ * are skipped and recorded as PULSE_ERR_INDEX in the plan's error word.
  */
 int pulse_apply_multi(pulse_plan *plan, const uint64_t *counts_host, cudaStream_t stream);
 

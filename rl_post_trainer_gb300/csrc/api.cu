@@ -340,6 +340,11 @@ struct pulse_plan {
   TensorDesc* desc = nullptr;       // device copy
   uint64_t* tile_begin = nullptr;   // device, ntensors + 1
   uint64_t* counts = nullptr;       // device, ntensors (host-count apply staging)
+  // chunk-owned apply: chunk tables (built once) and the per-call partition
+  uint64_t total_chunks = 0;
+  uint64_t* chunk_begin = nullptr;  // device, ntensors + 1
+  uint32_t* chunk_tensor = nullptr; // device, total_chunks
+  uint32_t* chunk_first = nullptr;  // device, total_chunks (scratch)
   Workspace ws;
 };
 
@@ -521,8 +526,32 @@ int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** pl
     st = PULSE_ERR_CUDA;
   } else {
     st = workspace_reserve(p->ws, tiles, nullptr);
-    if (st == PULSE_OK && cudaDeviceSynchronize() != cudaSuccess) st = PULSE_ERR_CUDA;
   }
+  if (st == PULSE_OK && p->can_apply) {
+    // chunk tables of the chunk-owned apply
+    std::vector<uint64_t> cb(size_t(ntensors) + 1, 0);
+    uint64_t chunks = 0;
+    for (int i = 0; i < ntensors; ++i) {
+      cb[size_t(i)] = chunks;
+      chunks += div_up(tensors[i].n, uint64_t(kApplyChunk));
+    }
+    cb[size_t(ntensors)] = chunks;
+    std::vector<uint32_t> ct(size_t(chunks > 0 ? chunks : 1), 0);
+    for (int i = 0; i < ntensors; ++i)
+      for (uint64_t g = cb[size_t(i)]; g < cb[size_t(i) + 1]; ++g) ct[size_t(g)] = uint32_t(i);
+    p->total_chunks = chunks;
+    if (cudaMalloc(&p->chunk_begin, sizeof(uint64_t) * cb.size()) != cudaSuccess ||
+        cudaMalloc(&p->chunk_tensor, sizeof(uint32_t) * ct.size()) != cudaSuccess ||
+        cudaMalloc(&p->chunk_first, sizeof(uint32_t) * ct.size()) != cudaSuccess) {
+      st = PULSE_ERR_NOMEM;
+    } else if (cudaMemcpy(p->chunk_begin, cb.data(), sizeof(uint64_t) * cb.size(),
+                          cudaMemcpyHostToDevice) != cudaSuccess ||
+               cudaMemcpy(p->chunk_tensor, ct.data(), sizeof(uint32_t) * ct.size(),
+                          cudaMemcpyHostToDevice) != cudaSuccess) {
+      st = PULSE_ERR_CUDA;
+    }
+  }
+  if (st == PULSE_OK && cudaDeviceSynchronize() != cudaSuccess) st = PULSE_ERR_CUDA;
   if (st != PULSE_OK) {
     pulse_plan_destroy(p);
     return st;
@@ -537,6 +566,9 @@ int pulse_plan_destroy(pulse_plan* plan) {
   if (plan->desc) cudaFree(plan->desc);
   if (plan->tile_begin) cudaFree(plan->tile_begin);
   if (plan->counts) cudaFree(plan->counts);
+  if (plan->chunk_begin) cudaFree(plan->chunk_begin);
+  if (plan->chunk_tensor) cudaFree(plan->chunk_tensor);
+  if (plan->chunk_first) cudaFree(plan->chunk_first);
   workspace_free(plan->ws);
   delete plan;
   return cuda_status(e);
@@ -569,6 +601,10 @@ int pulse_encode_multi(pulse_plan* plan, uint64_t* counts_out, cudaStream_t stre
 
 int pulse_apply_multi_device(pulse_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {
   if (plan == nullptr || counts_dev == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
+  if (plan->chunk_first != nullptr)
+    return cuda_status(launch_apply_chunks(plan->desc, plan->chunk_begin, plan->chunk_tensor,
+                                           plan->chunk_first, counts_dev, plan->total_chunks,
+                                           plan->ws.counters + 2, kDefaultWaitNs, stream));
   const int grid = sm_count(plan->device) * 8;
   for (int t0 = 0; t0 < plan->ntensors; t0 += kMaxTensorsPerApplyLaunch) {
     const int nt = plan->ntensors - t0 < kMaxTensorsPerApplyLaunch ? plan->ntensors - t0

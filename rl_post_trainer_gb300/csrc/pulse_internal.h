@@ -216,6 +216,26 @@ cudaError_t launch_apply_multi(const TensorDesc* tensors, int ntensors,
                                const uint64_t* counts_dev, uint32_t* error_word,
                                int grid, cudaStream_t stream);
 
+// Chunk-owned whole-model apply (ascending segments): kApplyChunk elements
+// per chunk; chunk_begin[t] = first global chunk of tensor t (ntensors + 1),
+// chunk_tensor[g] = tensor of chunk g, chunk_first[g] = scratch (total_chunks).
+#ifndef PULSE_APPLY_CHUNK
+#define PULSE_APPLY_CHUNK 8192
+#endif
+#ifndef PULSE_APPLY_DENSE_MIN
+#define PULSE_APPLY_DENSE_MIN 64
+#endif
+#ifndef PULSE_APPLY_CHUNK_CTAS
+#define PULSE_APPLY_CHUNK_CTAS 6
+#endif
+constexpr int kApplyChunkCtas = PULSE_APPLY_CHUNK_CTAS;  // resident chunk-apply CTAs per SM
+constexpr int kApplyChunk = PULSE_APPLY_CHUNK;
+constexpr uint32_t kApplyDenseMin = PULSE_APPLY_DENSE_MIN;
+cudaError_t launch_apply_chunks(const TensorDesc* tensors, const uint64_t* chunk_begin,
+                                const uint32_t* chunk_tensor, uint32_t* chunk_first,
+                                const uint64_t* counts_dev, uint64_t total_chunks,
+                                uint32_t* error_word, uint64_t wait_limit_ns, cudaStream_t stream);
+
 // One byte-valued patch segment (an MXFP8 code or scale array).
 struct ByteSegment {
   uint8_t* w;
