@@ -803,10 +803,17 @@ def run_loco(args, cfg, specs, wl, dev, rank, peak, local_steps):
     }
 
 
-def e2e(args, wl, counts_np, dist_on):
+def e2e(args, wl, counts_np, dist_on, groups: int = 16):
     """Same metric through the public API with HOST buffers: every step copies
     the new FP32 master from pinned host memory, encodes, reads the patch back
-    to pinned host memory (the wire), copies it to the sampler and applies."""
+    to pinned host memory (the wire), copies it to the sampler and applies.
+
+    The model is cut into `groups` groups of tensors of about equal size, one
+    plan each, so the transfers overlap the work of other groups: masters go
+    up on one stream; each group's encode waits for its masters, its count
+    comes down at once, and as soon as the host has it the group's patch goes
+    down and back up and is applied on other streams."""
+    import rl_post_trainer_gb300 as pulse
     try:
         host_master = []
         for m in wl.master:
@@ -820,26 +827,60 @@ def e2e(args, wl, counts_np, dist_on):
         return {"value": None, "unit": UNIT, "error": str(exc)[:200]}
     n = wl.n
     T = len(wl.specs)
+    dev = wl.master[0].device
+    # groups of consecutive tensors with about n / groups params each
+    bounds, acc, target = [0], 0, n / groups
+    for t, s_ in enumerate(wl.specs):
+        acc += s_.numel
+        if acc >= target * len(bounds) and t + 1 < T:
+            bounds.append(t + 1)
+    bounds.append(T)
+    G = len(bounds) - 1
+    plans = [pulse.Plan([pulse.TensorSlot(wl.specs[t].numel, master=wl.master[t], prev=wl.prev[t],
+                                          w=wl.w[t], idx=wl.idx[t], val=wl.val[t])
+                         for t in range(bounds[g], bounds[g + 1])]) for g in range(G)]
+    counts_d = [torch.zeros(bounds[g + 1] - bounds[g], dtype=torch.int64, device=dev) for g in range(G)]
+    counts_h = [torch.zeros(bounds[g + 1] - bounds[g], dtype=torch.int64, pin_memory=True) for g in range(G)]
+    s_in, s_enc, s_out, s_back = (torch.cuda.Stream(dev) for _ in range(4))
 
     def one_step():
-        for m, hm in zip(wl.master, host_master):
-            m.copy_(hm, non_blocking=True)
-        wl.plan.encode(wl.counts)
-        ks = wl.counts.cpu().tolist()
-        for t in range(T):
-            k = ks[t]
-            if k > cap[t]:
-                raise RuntimeError("patch larger than the staging buffer")
-            h_idx[t][:k].copy_(wl.idx[t][:k], non_blocking=True)
-            h_val[t][:k].copy_(wl.val[t][:k], non_blocking=True)
+        ev_in = [torch.cuda.Event() for _ in range(G)]
+        ev_cnt = [torch.cuda.Event() for _ in range(G)]
+        ev_out = [torch.cuda.Event() for _ in range(G)]
+        with torch.cuda.stream(s_in):
+            for g in range(G):
+                for t in range(bounds[g], bounds[g + 1]):
+                    wl.master[t].copy_(host_master[t], non_blocking=True)
+                ev_in[g].record(s_in)
+        with torch.cuda.stream(s_enc):
+            for g in range(G):
+                s_enc.wait_event(ev_in[g])
+                plans[g].encode(counts_d[g])
+                counts_h[g].copy_(counts_d[g], non_blocking=True)
+                ev_cnt[g].record(s_enc)
+        ktot = 0
+        for g in range(G):
+            ev_cnt[g].synchronize()
+            ks = counts_h[g].tolist()
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cnt[g])
+                for j, t in enumerate(range(bounds[g], bounds[g + 1])):
+                    k = ks[j]
+                    if k > cap[t]:
+                        raise RuntimeError("patch larger than the staging buffer")
+                    h_idx[t][:k].copy_(wl.idx[t][:k], non_blocking=True)
+                    h_val[t][:k].copy_(wl.val[t][:k], non_blocking=True)
+                ev_out[g].record(s_out)
+            with torch.cuda.stream(s_back):
+                s_back.wait_event(ev_out[g])
+                for j, t in enumerate(range(bounds[g], bounds[g + 1])):
+                    k = ks[j]
+                    wl.idx[t][:k].copy_(h_idx[t][:k], non_blocking=True)
+                    wl.val[t][:k].copy_(h_val[t][:k], non_blocking=True)
+                plans[g].apply(ks)
+            ktot += sum(ks)
         torch.cuda.synchronize()
-        for t in range(T):
-            k = ks[t]
-            wl.idx[t][:k].copy_(h_idx[t][:k], non_blocking=True)
-            wl.val[t][:k].copy_(h_val[t][:k], non_blocking=True)
-        wl.plan.apply(ks)
-        torch.cuda.synchronize()
-        return sum(ks)
+        return ktot
 
     for _ in range(min(args.warmup, 1)):
         wl.restore()
@@ -853,12 +894,19 @@ def e2e(args, wl, counts_np, dist_on):
         ktot = one_step()
         times.append(time.perf_counter() - t0)
         barrier(dist_on)
+    for t in range(T):
+        if not torch.equal(wl.w[t], wl.prev[t]):
+            raise RuntimeError(f"e2e: sampler weights differ from the trainer view (tensor {t})")
+    for p_ in plans:
+        p_.close()
     tt = max_over_ranks(sum(times), dist_on)
     total_params = sum_over_ranks(float(n), dist_on)
     return {"value": total_params * args.steps / tt, "unit": UNIT,
             "h2d_bytes_per_step": int(4 * n + 6 * ktot + 8 * T),
             "d2h_bytes_per_step": int(6 * ktot + 8 * T),
-            "ms_per_step": 1e3 * tt / args.steps}
+            "ms_per_step": 1e3 * tt / args.steps, "groups": G,
+            "pipeline": "per-group plans; masters up on one stream, encode + counts down on a "
+                        "second, patches down on a third, up again and applied on a fourth"}
 
 
 def main():
