@@ -203,7 +203,7 @@ cudaError_t launch_compose(const CmpSegment* segs_dev, const CmpSegment& one,
 #define PULSE_APPLY_PER_THREAD 8
 #endif
 #ifndef PULSE_XOR_ROUNDS
-#define PULSE_XOR_ROUNDS 8
+#define PULSE_XOR_ROUNDS 4
 #endif
 constexpr int kApplyThreads = 256;
 constexpr int kApplyPerThread = PULSE_APPLY_PER_THREAD;     // entries per thread per tile
