@@ -561,7 +561,8 @@ def run_compose(args, wl, dev, versions: int = 4):
     """Sidecar catch-up over `versions` missing versions of the whole model:
     encode `versions` consecutive steps (untimed), then time (a) composing
     the chain into one patch (pulse_compose_multi, folded left) plus one
-    apply, against (b) applying the patches one after another."""
+    apply, (b) applying the patches one after another, and (c) the chained
+    apply (pulse_apply_chain_multi: every version in one pass over w)."""
     import rl_post_trainer_gb300 as pulse
     specs = wl.specs
     T = len(specs)
@@ -604,6 +605,18 @@ def run_compose(args, wl, dev, versions: int = 4):
     composed_plan = pulse.Plan([pulse.TensorSlot(s.numel, w=wl.w[t], idx=last_i[t], val=last_v[t])
                                 for t, s in enumerate(specs)])
 
+    chain_plan = pulse.Plan([pulse.TensorSlot(s.numel, w=wl.w[t]) for t, s in enumerate(specs)])
+    chain_refs = chain_plan.prepare_chain([[(c[0][t], c[1][t], c[2][t]) for t in range(T)]
+                                           for c in chain])
+
+    def apply_chained():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        chain_plan.apply_chain(chain_refs)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3
+
     def apply_seq():
         for idx_l, val_l, ks in chain:
             for t in range(T):
@@ -617,7 +630,7 @@ def run_compose(args, wl, dev, versions: int = 4):
             torch.cuda.synchronize()
             yield e0.elapsed_time(e1) * 1e-3
 
-    t_cmp, t_app1, t_seq = [], [], []
+    t_cmp, t_app1, t_seq, t_chain = [], [], [], []
     reps = max(1, min(args.steps, 3))
     for r in range(reps + 1):          # the first round is a warm-up
         for w, p0 in zip(wl.w, wl.prev0):
@@ -642,25 +655,48 @@ def run_compose(args, wl, dev, versions: int = 4):
         for t in range(T):
             if not torch.equal(wl.w[t], final_view[t]):
                 raise RuntimeError(f"sequential catch-up differs from the final view (tensor {t})")
+        for w, p0 in zip(wl.w, wl.prev0):
+            w.copy_(p0)
+        torch.cuda.synchronize()
+        tch = apply_chained()
+        for t in range(T):
+            if not torch.equal(wl.w[t], final_view[t]):
+                raise RuntimeError(f"chained catch-up differs from the final view (tensor {t})")
         if r > 0:
             t_cmp.append(tc)
             t_app1.append(ta)
             t_seq.append(ts)
+            t_chain.append(tch)
     if pulse.get_error(dev) != 0:
         raise RuntimeError("device error in the compose leg")
+    if chain_plan.get_error() != 0:
+        raise RuntimeError("device error in the chained apply")
+    # sectors of w that any version touches: the composed patch's distinct idx / 16
+    s_union = 0
+    for t in range(T):
+        if ck[t] > 0:
+            sec = ci[t][:ck[t]] // 16
+            s_union += 1 + int(torch.count_nonzero(sec[1:] != sec[:-1]))
     apply_plan.close()
     composed_plan.close()
+    chain_plan.close()
     k_in = [sum(c[2]) for c in chain]
     k_out = sum(ck)
     moved = sum(fold_bytes)   # every fold reads both inputs and writes its output
     tcm, tam, tsm = float(np.mean(t_cmp)), float(np.mean(t_app1)), float(np.mean(t_seq))
+    tchm = float(np.mean(t_chain))
+    chain_bytes = 6 * sum(k_in) + 64 * s_union
     return {
         "versions": versions, "patch_entries": k_in, "composed_entries": k_out,
         "compose_ms": 1e3 * tcm, "apply_composed_ms": 1e3 * tam,
         "catch_up_composed_ms": 1e3 * (tcm + tam), "catch_up_sequential_ms": 1e3 * tsm,
         "compose_bytes": moved, "compose_gbs": moved / tcm / 1e9,
+        "catch_up_chained_ms": 1e3 * tchm, "sectors_union": s_union,
+        "chained_bytes_model": "6 * sum(k) + 64 * S_union", "chained_bytes": chain_bytes,
+        "chained_gbs": chain_bytes / tchm / 1e9,
         "timing": "compose: host wall time of the folds (includes the host counts read "
-                  "between folds); applies: CUDA events",
+                  "between folds); applies: CUDA events; chained: one pulse_apply_chain_multi "
+                  "call on a prepared chain (partition + apply launch), CUDA events",
     }
 
 

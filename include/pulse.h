@@ -229,6 +229,37 @@ int pulse_apply_multi(pulse_plan *plan, const uint64_t *counts_host, cudaStream_
  * pulse_encode_multi), so no host round trip is needed. */
 int pulse_apply_multi_device(pulse_plan *plan, const uint64_t *counts_dev, cudaStream_t stream);
 
+/*
+ * pulse_apply_chain_multi -- bring the plan's w forward by several versions
+ * at once. [TALK] 16:40-17:04: a sidecar whose engine is behind applies the
+ * transitions it missed, in order; [PULSE] "1. PULSESync": patch values are
+ * absolute, so the later patch wins where two list the same index.
+ *   patches   HOST array of nversions x ntensors references, version-major:
+ *             patches[v * ntensors + t] is tensor t's patch of the v-th
+ *             version applied (oldest first); copied before the call returns
+ *   nversions >= 1
+ * The result equals pulse_apply_multi with each version's segments, one
+ * version after the other. Each segment must list ascending indices (what
+ * encode writes). One pass over w per 16 versions: a chunk of w is loaded
+ * once, receives every version's entries in version order, and its changed
+ * 32-byte sectors are written back once. Needs w for every tensor with n > 0
+ * (idx, val and master of the plan are not used). Growing the call's
+ * internal tables synchronises `stream`; one stream at a time per plan.
+ * Errors: PULSE_ERR_INVALID (NULL plan or patches, nversions < 1, a plan
+ * tensor without w, count > 0 with NULL idx or val), PULSE_ERR_RANGE (a
+ * count >= 2^32), PULSE_ERR_NOMEM, PULSE_ERR_CUDA; device (plan error word):
+ * PULSE_ERR_INDEX (count > n, clamped; entries outside their chunk, skipped),
+ * PULSE_ERR_TIMEOUT.
+ */
+typedef struct pulse_patch_ref {
+    const uint32_t *idx;  /* device, count entries, ascending, local to the tensor */
+    const uint16_t *val;  /* device, count entries (BF16 bit patterns) */
+    uint64_t count;       /* host value */
+} pulse_patch_ref;
+
+int pulse_apply_chain_multi(pulse_plan *plan, const pulse_patch_ref *patches, int nversions,
+                            cudaStream_t stream);
+
 /* XOR mask / XOR apply over every tensor of the plan, one launch each. */
 int pulse_xor_mask_multi(pulse_plan *plan, cudaStream_t stream);
 int pulse_xor_apply_multi(pulse_plan *plan, cudaStream_t stream);

@@ -10,6 +10,7 @@ from .pulse import (  # noqa: F401
     MxPlan,
     MxTensorSlot,
     Plan,
+    PreparedChain,
     PulseError,
     TensorSlot,
     apply,

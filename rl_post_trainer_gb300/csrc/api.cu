@@ -336,6 +336,7 @@ struct pulse_plan {
   int ntensors = 0;
   uint64_t total_tiles = 0;
   bool can_encode = false, can_apply = false, can_xor_mask = false, can_xor_apply = false;
+  bool can_chain = false;  // every tensor with n > 0 has w: chained applies are possible
   std::vector<TensorDesc> host_desc;
   TensorDesc* desc = nullptr;       // device copy
   uint64_t* tile_begin = nullptr;   // device, ntensors + 1
@@ -345,6 +346,10 @@ struct pulse_plan {
   uint64_t* chunk_begin = nullptr;  // device, ntensors + 1
   uint32_t* chunk_tensor = nullptr; // device, total_chunks
   uint32_t* chunk_first = nullptr;  // device, total_chunks (scratch)
+  // chained apply: per-call patch table and partition scratch (grown on demand)
+  ChainSeg* chain_segs = nullptr;   // device, chain_seg_cap entries
+  uint64_t chain_seg_cap = 0;
+  uint32_t* chain_first = nullptr;  // device, kChainMaxVersions x total_chunks (first use)
   Workspace ws;
 };
 
@@ -487,7 +492,7 @@ int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** pl
     return PULSE_ERR_CUDA;
   }
   p->ntensors = ntensors;
-  p->can_encode = p->can_apply = p->can_xor_mask = p->can_xor_apply = true;
+  p->can_encode = p->can_apply = p->can_xor_mask = p->can_xor_apply = p->can_chain = true;
   std::vector<uint64_t> tb(size_t(ntensors) + 1, 0);
   p->host_desc.reserve(size_t(ntensors));
   uint64_t tiles = 0;
@@ -503,6 +508,7 @@ int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** pl
     if (t.n > 0) {
       p->can_encode = p->can_encode && t.master && t.prev && t.idx && t.val;
       p->can_apply = p->can_apply && t.w && t.idx && t.val;
+      p->can_chain = p->can_chain && t.w;
       p->can_xor_mask = p->can_xor_mask && t.master && t.prev && t.mask;
       p->can_xor_apply = p->can_xor_apply && t.w && t.mask;
     }
@@ -527,8 +533,8 @@ int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** pl
   } else {
     st = workspace_reserve(p->ws, tiles, nullptr);
   }
-  if (st == PULSE_OK && p->can_apply) {
-    // chunk tables of the chunk-owned apply
+  if (st == PULSE_OK && p->can_chain) {
+    // chunk tables of the chunk-owned (and chained) apply
     std::vector<uint64_t> cb(size_t(ntensors) + 1, 0);
     uint64_t chunks = 0;
     for (int i = 0; i < ntensors; ++i) {
@@ -569,6 +575,8 @@ int pulse_plan_destroy(pulse_plan* plan) {
   if (plan->chunk_begin) cudaFree(plan->chunk_begin);
   if (plan->chunk_tensor) cudaFree(plan->chunk_tensor);
   if (plan->chunk_first) cudaFree(plan->chunk_first);
+  if (plan->chain_segs) cudaFree(plan->chain_segs);
+  if (plan->chain_first) cudaFree(plan->chain_first);
   workspace_free(plan->ws);
   delete plan;
   return cuda_status(e);
@@ -624,6 +632,52 @@ int pulse_apply_multi(pulse_plan* plan, const uint64_t* counts_host, cudaStream_
                       cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return PULSE_ERR_CUDA;
   return pulse_apply_multi_device(plan, plan->counts, stream);
+}
+
+int pulse_apply_chain_multi(pulse_plan* plan, const pulse_patch_ref* patches, int nversions,
+                            cudaStream_t stream) {
+  if (plan == nullptr || patches == nullptr || nversions < 1 || !plan->can_chain)
+    return PULSE_ERR_INVALID;
+  const uint64_t nseg = uint64_t(nversions) * uint64_t(plan->ntensors);
+  std::vector<ChainSeg> segs(static_cast<size_t>(nseg));
+  for (uint64_t i = 0; i < nseg; ++i) {
+    const pulse_patch_ref& r = patches[i];
+    if (r.count >= kMaxElems + 1) return PULSE_ERR_RANGE;
+    if (r.count > 0 && (r.idx == nullptr || r.val == nullptr)) return PULSE_ERR_INVALID;
+    segs[size_t(i)] = ChainSeg{r.idx, r.val, r.count};
+  }
+  if (plan->total_chunks == 0) return PULSE_OK;
+  // grow the patch table; replacing a buffer waits for the work that reads it
+  if (nseg > plan->chain_seg_cap) {
+    uint64_t cap = plan->chain_seg_cap ? plan->chain_seg_cap : 256;
+    while (cap < nseg) cap *= 2;
+    if (plan->chain_segs != nullptr) {
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return PULSE_ERR_CUDA;
+      cudaFree(plan->chain_segs);
+      plan->chain_segs = nullptr;
+      plan->chain_seg_cap = 0;
+    }
+    if (cudaMalloc(&plan->chain_segs, sizeof(ChainSeg) * size_t(cap)) != cudaSuccess)
+      return PULSE_ERR_NOMEM;
+    plan->chain_seg_cap = cap;
+  }
+  if (plan->chain_first == nullptr &&
+      cudaMalloc(&plan->chain_first, sizeof(uint32_t) * size_t(plan->total_chunks) *
+                                         size_t(kChainMaxVersions)) != cudaSuccess)
+    return PULSE_ERR_NOMEM;
+  // from pageable memory the copy is staged before this call returns
+  if (cudaMemcpyAsync(plan->chain_segs, segs.data(), sizeof(ChainSeg) * size_t(nseg),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  for (int v0 = 0; v0 < nversions; v0 += kChainMaxVersions) {
+    const int nv = nversions - v0 < kChainMaxVersions ? nversions - v0 : kChainMaxVersions;
+    const cudaError_t e = launch_apply_chain(
+        plan->desc, plan->chunk_begin, plan->chunk_tensor, plan->chain_first,
+        plan->chain_segs + size_t(v0) * size_t(plan->ntensors), plan->ntensors, nv,
+        plan->total_chunks, plan->ws.counters + 2, kDefaultWaitNs, stream);
+    if (e != cudaSuccess) return PULSE_ERR_CUDA;
+  }
+  return PULSE_OK;
 }
 
 int pulse_xor_mask_multi(pulse_plan* plan, cudaStream_t stream) {

@@ -226,7 +226,6 @@ cudaError_t launch_apply_multi_t(const Seg* segs, int nsegs, const uint64_t* cou
 // directly. Entries outside their chunk (a patch that is not ascending, or
 // an index past the tensor) are skipped and reported as PULSE_ERR_INDEX.
 constexpr int kChunk = kApplyChunk;                 // elements per chunk (16 KB of BF16)
-constexpr int kChunkThreads = 256;
 constexpr int kChunkSectors = kChunk * 2 / 32;      // 512
 constexpr uint32_t kDenseMin = kApplyDenseMin;      // entries from which a chunk goes dense
 
@@ -256,146 +255,330 @@ __global__ void __launch_bounds__(256)
   chunk_first[g] = lower_bound_u32(d.idx, uint32_t(c), uint32_t(start));
 }
 
-// Chunk g's entry range [e0, e1) and whether it goes dense.
-struct ChunkWork {
-  uint64_t g;
-  uint32_t t;
-  uint64_t e0, e1, base;
-  uint32_t len;
-  bool dense;
-};
-
-__device__ __forceinline__ ChunkWork chunk_work(const TensorDesc* tensors, const uint64_t* chunk_begin,
-                                                const uint32_t* chunk_tensor,
-                                                const uint32_t* chunk_first, const uint64_t* counts,
-                                                uint64_t g) {
-  ChunkWork c;
-  c.g = g;
-  c.t = chunk_tensor[g];
-  const TensorDesc& d = tensors[c.t];
-  uint64_t cnt = counts[c.t];
-  if (cnt > d.n) cnt = d.n;
-  c.e0 = chunk_first[g];
-  c.e1 = g + 1 < chunk_begin[c.t + 1] ? chunk_first[g + 1] : cnt;
-  if (c.e1 < c.e0) c.e1 = c.e0;
-  c.base = (g - chunk_begin[c.t]) * kChunk;
-  c.len = uint32_t(d.n - c.base < uint64_t(kChunk) ? d.n - c.base : uint64_t(kChunk));
-  c.dense = c.e1 - c.e0 >= kDenseMin && (reinterpret_cast<uintptr_t>(d.w) % 16u == 0);
-  return c;
+// ------------------------------------------------------------ chained apply
+// A receiver that is several versions behind applies the patches of versions
+// v0 < v1 < ... in order (talk 16:40-17:04, the sidecar catching up). Each
+// patch lists absolute values, so applying them in order equals applying
+// their composition once; the chained form gets there without composing:
+// one pass over w in which every chunk is loaded once, receives the entries
+// of every version in version order (a barrier of the storing warps between
+// versions: the later patch wins) and writes its changed sectors back once.
+__global__ void __launch_bounds__(256)
+    chain_partition_kernel(const TensorDesc* tensors, const uint64_t* chunk_begin,
+                           const uint32_t* chunk_tensor, const ChainSeg* segs, int ntensors,
+                           int nversions, uint64_t total_chunks, uint32_t* chain_first,
+                           uint32_t* err) {
+  const uint64_t x = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (x >= total_chunks * uint64_t(nversions)) return;
+  const uint32_t v = uint32_t(x / total_chunks);
+  const uint64_t g = x - uint64_t(v) * total_chunks;
+  const uint32_t t = chunk_tensor[g];
+  const ChainSeg s = segs[size_t(v) * size_t(ntensors) + t];
+  uint64_t c = s.count;
+  if (c > tensors[t].n) {
+    if (g == chunk_begin[t]) record_error(err, kErrIndex);  // once per tensor and version
+    c = tensors[t].n;
+  }
+  const uint64_t start = (g - chunk_begin[t]) * kChunk;
+  chain_first[x] = lower_bound_u32(s.idx, uint32_t(c), uint32_t(start));
 }
 
-constexpr int kPrefetchEntries = 4;  // entries per thread loaded before the chunk lands
+// ------------------------------------------------ chunk-owned apply kernel
+// One kernel serves the whole-model apply (one version, counts on the
+// device) and the chained apply (1..kChainMaxVersions versions). Warp
+// roles per CTA:
+//  * producer warp: for the CTA's next chunk, reads the entry range of every
+//    version (from the partition), asks L2 to prefetch those entries, writes
+//    the chunk's description into the buffer's shared slot and, when the
+//    chunk goes dense, bulk-copies its w into the buffer; it runs up to
+//    kCwBuf chunks ahead of the workers (full / empty mbarriers per buffer),
+//    so none of this sits on the workers' path;
+//  * 8 worker warps: per chunk, for each version in order, load the entries
+//    (kCwPre per thread and version in flight at once, for kCwGroup
+//    versions) and store them into the shared copy of the chunk (flagging
+//    the changed 32-byte sectors) or, for a sparse chunk, straight to w; a
+//    named barrier between versions makes the later patch win; then write
+//    the changed sectors back whole.
+constexpr int kCwWorkers = 256;                    // 8 worker warps
+constexpr int kCwThreads = kCwWorkers + 32;        // + the producer warp
+constexpr int kCwBuf = 2;                          // chunks staged per CTA
+constexpr int kCwBarrier = 1;                      // the workers' named barrier
+constexpr uint32_t kModeNone = 0, kModeDirect = 1, kModeDense = 2, kModeEnd = 3;
 
-__global__ void __launch_bounds__(kChunkThreads, kApplyChunkCtas)
-    apply_chunk_kernel(const TensorDesc* tensors, const uint64_t* chunk_begin,
-                       const uint32_t* chunk_tensor, const uint32_t* chunk_first,
-                       const uint64_t* counts, uint64_t total_chunks, uint32_t* err,
-                       uint64_t wait_limit_ns) {
-  __shared__ __align__(128) uint16_t wsm[2][kChunk];  // double buffer
+struct ChunkSlot {
+  uint16_t* w;     // the chunk's first element
+  uint64_t base;   // tensor-local index of that element
+  uint32_t len;    // elements in the chunk
+  uint32_t mode;
+  uint32_t e0[kChainMaxVersions], e1[kChainMaxVersions];
+  const uint32_t* idx[kChainMaxVersions];
+  const uint16_t* val[kChainMaxVersions];
+};
+
+// Where the segment of version v of tensor t comes from.
+struct CwArgs {
+  const TensorDesc* tensors;
+  const uint64_t* chunk_begin;
+  const uint32_t* chunk_tensor;
+  const uint32_t* first;   // nversions x total_chunks: first entry of each chunk
+  const ChainSeg* segs;    // chained: nversions x ntensors; else null
+  const uint64_t* counts;  // whole-model apply: device counts; else null
+  int ntensors;
+  int nversions;
+  uint64_t total_chunks;
+  uint32_t* err;
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ void worker_barrier() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kCwBarrier), "n"(kCwWorkers) : "memory");
+}
+
+// Named barrier of the workers that also ORs a predicate over them (every
+// loop exit goes through it, so the workers always leave together).
+__device__ __forceinline__ bool worker_barrier_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(v)), "n"(kCwBarrier), "n"(kCwWorkers)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that gives up at once when another wait of the launch has
+// given up (the error word holds kErrTimeout).
+__device__ __forceinline__ bool cw_wait(uint64_t* bar, uint32_t parity, const CwArgs& a) {
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i)
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+  if (ld_volatile_u32(a.err) & kErrTimeout) return false;
+  if (mbar_wait_bounded(bar, parity, a.wait_limit_ns)) return true;
+  record_error(a.err, kErrTimeout);
+  return false;
+}
+
+// GROUP: versions whose entries are in flight together; PRE: entries per
+// thread and version loaded at once; CTAS: resident CTAs per SM.
+template <int GROUP, int PRE, int CTAS>
+__global__ void __launch_bounds__(kCwThreads, CTAS) chunk_apply_kernel(const CwArgs a) {
+  constexpr int kCwGroup = GROUP, kCwPre = PRE;
+  __shared__ __align__(128) uint16_t wsm[kCwBuf][kChunk];
   __shared__ __align__(16) uint8_t dirty[kChunkSectors];  // one flag byte per 32-byte sector
-  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ ChunkSlot slot[kCwBuf];
+  __shared__ __align__(8) uint64_t full[kCwBuf], empty[kCwBuf];
   const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int b = 0; b < kCwBuf; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], 1);
+    }
     fence_mbar_init();
   }
+  for (int k = tid; k < kChunkSectors; k += kCwThreads) dirty[k] = 0u;
   __syncthreads();
-  const uint64_t pol = l2_policy_evict_first();
-  uint32_t phases = 0;  // bit b: parity of buffer b's next phase
-  // issue the bulk copy of a dense chunk's body into buffer b (thread 0)
-  auto stage = [&](const ChunkWork& c, int b) {
-    if (tid == 0 && c.dense) {
-      const TensorDesc& d = tensors[c.t];
-      const uint32_t body = c.len & ~7u;
-      mbar_arrive_expect_tx(&bar[b], body * 2u);
-      if (body) bulk_g2s(wsm[b], d.w + c.base, body * 2u, &bar[b], pol);
-    }
-  };
-  uint64_t g = blockIdx.x;
-  ChunkWork cur{};
-  if (g < total_chunks) {
-    cur = chunk_work(tensors, chunk_begin, chunk_tensor, chunk_first, counts, g);
-    stage(cur, 0);
-  }
-  for (int b = 0; g < total_chunks; g += gridDim.x, b ^= 1) {
-    // the next chunk of this CTA starts loading into the other buffer now
-    const uint64_t gn = g + gridDim.x;
-    ChunkWork nxt{};
-    if (gn < total_chunks) {
-      nxt = chunk_work(tensors, chunk_begin, chunk_tensor, chunk_first, counts, gn);
-      stage(nxt, b ^ 1);
-    }
-    const TensorDesc& d = tensors[cur.t];
-    if (cur.e1 > cur.e0 && !cur.dense) {
-      for (uint64_t j = cur.e0 + tid; j < cur.e1; j += kChunkThreads) {
-        const uint32_t i = d.idx[j];
-        if (uint64_t(i) < cur.base || uint64_t(i) >= cur.base + cur.len) {
-          record_error(err, kErrIndex);
-          continue;
+
+  if (warp == kCwWorkers / 32) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = l2_policy_evict_first();
+    // lane 0: 1 + round of buffer b's latest phase when a bulk copy completes
+    // it, else 0 (a parity wait is only meaningful for the latest phase)
+    uint32_t armed[kCwBuf] = {};
+    for (uint32_t i = 0;; ++i) {
+      const int b = int(i % kCwBuf);
+      const uint32_t round = i / kCwBuf;
+      if (round > 0 && !cw_wait(&empty[b], (round - 1) & 1u, a)) break;
+      const uint64_t g = blockIdx.x + uint64_t(i) * gridDim.x;
+      ChunkSlot& sl = slot[b];
+      // a new phase on buffer b follows the workers' release of its last one,
+      // so an earlier bulk copy into b has landed
+      armed[b] = 0;
+      if (g >= a.total_chunks) {
+        if (lane == 0) {
+          sl.mode = kModeEnd;
+          mbar_arrive(&full[b]);
         }
-        d.w[i] = d.val[j];
-      }
-    } else if (cur.dense) {
-      // entries of this chunk, loaded while its copy is in flight
-      uint32_t pi[kPrefetchEntries];
-      uint16_t pv[kPrefetchEntries];
-#pragma unroll
-      for (int q = 0; q < kPrefetchEntries; ++q) {
-        const uint64_t j = cur.e0 + uint64_t(q) * kChunkThreads + tid;
-        pi[q] = j < cur.e1 ? d.idx[j] : 0u;
-        pv[q] = j < cur.e1 ? d.val[j] : uint16_t(0);
-      }
-      for (uint32_t k = tid; k < uint32_t(kChunkSectors) / 4u; k += kChunkThreads)
-        reinterpret_cast<uint32_t*>(dirty)[k] = 0u;
-      const uint32_t body = cur.len & ~7u;
-      for (uint32_t k = body + tid; k < cur.len; k += kChunkThreads) wsm[b][k] = d.w[cur.base + k];
-      const uint32_t par = (phases >> b) & 1u;
-      const bool ok = mbar_wait_bounded(&bar[b], par, wait_limit_ns);
-      phases ^= 1u << b;
-      if (!__syncthreads_and(ok)) {
-        // a copy did not land in time: report, give both buffers one more
-        // bounded wait (no copy may still write shared memory at exit), stop
-        if (tid == 0) record_error(err, kErrTimeout);
-        mbar_wait_bounded(&bar[b], par, wait_limit_ns);
-        if (nxt.dense) mbar_wait_bounded(&bar[b ^ 1], (phases >> (b ^ 1)) & 1u, wait_limit_ns);
         break;
       }
+      const uint32_t t = a.chunk_tensor[g];
+      const TensorDesc& d = a.tensors[t];
+      const uint64_t n = d.n;
+      const uint64_t base = (g - a.chunk_begin[t]) * kChunk;
+      const uint32_t len = uint32_t(n - base < uint64_t(kChunk) ? n - base : uint64_t(kChunk));
+      const bool last_of_tensor = g + 1 >= a.chunk_begin[t + 1];
+      uint32_t e0 = 0, e1 = 0;
+      if (lane < a.nversions) {
+        const uint32_t* ip;
+        const uint16_t* vp;
+        uint64_t cnt;
+        if (a.segs != nullptr) {
+          const ChainSeg sg = a.segs[size_t(lane) * size_t(a.ntensors) + t];
+          ip = sg.idx;
+          vp = sg.val;
+          cnt = sg.count;
+        } else {
+          ip = d.idx;
+          vp = d.val;
+          cnt = a.counts[t];
+        }
+        if (cnt > n) cnt = n;
+        const uint32_t* f = a.first + uint64_t(lane) * a.total_chunks;
+        e0 = f[g];
+        e1 = last_of_tensor ? uint32_t(cnt) : f[g + 1];
+        if (e1 < e0) e1 = e0;
+        if (e1 > e0) {
+          l2_prefetch_range(ip + e0, uint64_t(e1 - e0) * 4u);
+          l2_prefetch_range(vp + e0, uint64_t(e1 - e0) * 2u);
+        }
+        sl.e0[lane] = e0;
+        sl.e1[lane] = e1;
+        sl.idx[lane] = ip;
+        sl.val[lane] = vp;
+      }
+      const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, e1 - e0);
+      const bool dense = total >= kDenseMin && (reinterpret_cast<uintptr_t>(d.w) % 16u == 0);
+      const uint32_t body = len & ~7u;
+      if (dense && lane < int(len - body)) wsm[b][body + lane] = d.w[base + body + lane];
+      if (lane == 0) {
+        sl.w = d.w + base;
+        sl.base = base;
+        sl.len = len;
+        sl.mode = total == 0 ? kModeNone : (dense ? kModeDense : kModeDirect);
+      }
+      __syncwarp();  // every lane's slot and tail writes precede the arrival
+      if (lane == 0) {
+        if (dense && body > 0) {
+          mbar_arrive_expect_tx(&full[b], body * 2u);
+          bulk_g2s(wsm[b], d.w + base, body * 2u, &full[b], pol);
+          armed[b] = round + 1;
+        } else {
+          mbar_arrive(&full[b]);
+        }
+      }
+    }
+    // no bulk copy may still be writing shared memory when the CTA exits
+    // (normally the workers have waited for every one; this matters only
+    // when a wait gave up)
+    if (lane == 0)
+      for (int b = 0; b < kCwBuf; ++b)
+        if (armed[b] != 0 && !mbar_wait_bounded(&full[b], (armed[b] - 1) & 1u, a.wait_limit_ns))
+          record_error(a.err, kErrTimeout);
+    return;
+  }
+
+  // --------------------------------------------------------------- workers
+  for (uint32_t i = 0;; ++i) {
+    const int b = int(i % kCwBuf);
+    const uint32_t round = i / kCwBuf;
+    const bool ok = cw_wait(&full[b], round & 1u, a);
+    if (worker_barrier_or(!ok)) break;
+    const ChunkSlot& sl = slot[b];
+    const uint32_t m = sl.mode;
+    if (m == kModeEnd) break;
+    if (m != kModeNone) {
+      const bool dense = m == kModeDense;
+      uint16_t* w = sl.w;
+      const uint64_t base = sl.base;
+      const uint32_t len = sl.len;
       auto put = [&](uint32_t i, uint16_t v) {
-        if (uint64_t(i) < cur.base || uint64_t(i) >= cur.base + cur.len) {
-          record_error(err, kErrIndex);
+        const uint64_t li = uint64_t(i) - base;  // wraps to a huge value below base
+        if (li >= len) {
+          record_error(a.err, kErrIndex);
           return;
         }
-        const uint32_t li = uint32_t(i - cur.base);
-        wsm[b][li] = v;
-        dirty[li >> 4] = 1u;  // plain store: every writer stores the same value
-      };
-#pragma unroll
-      for (int q = 0; q < kPrefetchEntries; ++q) {
-        const uint64_t j = cur.e0 + uint64_t(q) * kChunkThreads + tid;
-        if (j < cur.e1) put(pi[q], pv[q]);
-      }
-      for (uint64_t j = cur.e0 + uint64_t(kPrefetchEntries) * kChunkThreads + tid; j < cur.e1;
-           j += kChunkThreads)
-        put(d.idx[j], d.val[j]);
-      __syncthreads();
-      // write back the changed sectors: 16 elements = two 16-byte stores each
-      for (uint32_t sct = tid; sct < uint32_t(kChunkSectors); sct += kChunkThreads) {
-        if (!dirty[sct]) continue;
-        const uint32_t first = sct * 16u;
-        if (first + 16u <= cur.len) {
-          const uint4* src = reinterpret_cast<const uint4*>(wsm[b] + first);
-          uint4* dst = reinterpret_cast<uint4*>(d.w + cur.base + first);
-          dst[0] = src[0];
-          dst[1] = src[1];
+        if (dense) {
+          wsm[b][li] = v;
+          dirty[li >> 4] = 1u;
         } else {
-          for (uint32_t k = first; k < cur.len; ++k) d.w[cur.base + k] = wsm[b][k];
+          w[li] = v;
+        }
+      };
+      for (int v0 = 0; v0 < a.nversions; v0 += kCwGroup) {
+        uint32_t pi[kCwGroup][kCwPre];
+        uint16_t pv[kCwGroup][kCwPre];
+#pragma unroll
+        for (int u = 0; u < kCwGroup; ++u) {
+          const int v = v0 + u;
+          const int vc = v < a.nversions ? v : 0;  // every shared read stays in bounds
+          const uint32_t e0 = sl.e0[vc];
+          const uint32_t e1 = v < a.nversions ? sl.e1[vc] : e0;
+          const uint32_t* ip = sl.idx[vc];
+          const uint16_t* vp = sl.val[vc];
+#pragma unroll
+          for (int q = 0; q < kCwPre; ++q) {
+            const uint32_t j = e0 + uint32_t(q * kCwWorkers + tid);
+            pi[u][q] = j < e1 ? ip[j] : 0u;
+            pv[u][q] = j < e1 ? vp[j] : uint16_t(0);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kCwGroup; ++u) {
+          const int v = v0 + u;
+          if (v >= a.nversions) break;  // uniform
+          const uint32_t e0 = sl.e0[v], e1 = sl.e1[v];
+#pragma unroll
+          for (int q = 0; q < kCwPre; ++q)
+            if (e0 + uint32_t(q * kCwWorkers + tid) < e1) put(pi[u][q], pv[u][q]);
+          const uint32_t* ip = sl.idx[v];
+          const uint16_t* vp = sl.val[v];
+          for (uint32_t j = e0 + uint32_t(kCwPre * kCwWorkers + tid); j < e1; j += kCwWorkers)
+            put(ip[j], vp[j]);
+          worker_barrier();  // the next version's stores land after these
         }
       }
-      __syncthreads();  // buffer b and the dirty bits are reused
+      if (dense) {
+        // changed sectors back whole (two 16-byte stores each), flags cleared
+        for (uint32_t sct = tid; sct < uint32_t(kChunkSectors); sct += kCwWorkers) {
+          if (!dirty[sct]) continue;
+          dirty[sct] = 0u;
+          const uint32_t f = sct * 16u;
+          if (f + 16u <= len) {
+            const uint4* src = reinterpret_cast<const uint4*>(wsm[b] + f);
+            uint4* dst = reinterpret_cast<uint4*>(w + f);
+            dst[0] = src[0];
+            dst[1] = src[1];
+          } else {
+            for (uint32_t k = f; k < len; ++k) w[k] = wsm[b][k];
+          }
+        }
+        // the buffer is next written by a bulk copy: order this thread's
+        // shared-memory accesses before it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
     }
-    cur = nxt;
+    worker_barrier();  // buffer b, its slot and the flags are free again
+    if (tid == 0) mbar_arrive(&empty[b]);
   }
+}
+
+// whole-model apply (one version) and chained apply (up to 16 versions)
+#ifndef PULSE_CW_PRE_ONE
+#define PULSE_CW_PRE_ONE 4
+#endif
+#ifndef PULSE_CW_CTAS_ONE
+#define PULSE_CW_CTAS_ONE 5
+#endif
+#ifndef PULSE_CW_CTAS_CHAIN
+#define PULSE_CW_CTAS_CHAIN 4
+#endif
+constexpr int kCwPreOne = PULSE_CW_PRE_ONE, kCwCtasOne = PULSE_CW_CTAS_ONE;
+constexpr int kCwGroupChain = 4, kCwPreChain = 3, kCwCtasChain = PULSE_CW_CTAS_CHAIN;
+
+// Resident CTAs per SM of a persistent kernel (static shared memory only),
+// so that every CTA of the grid is resident from the start.
+template <class K>
+int resident_per_sm(K kernel, int threads, int cap) {
+  // shared memory is the limit: ask for the largest carveout
+  cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       int(cudaSharedmemCarveoutMaxShared));
+  int b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, 0) != cudaSuccess || b < 1)
+    b = 1;
+  return b < cap ? b : cap;
 }
 
 }  // namespace
@@ -409,11 +592,36 @@ cudaError_t launch_apply_chunks(const TensorDesc* tensors, const uint64_t* chunk
   cudaGetDevice(&dev);
   apply_partition_kernel<<<unsigned((total_chunks + 255) / 256), 256, 0, stream>>>(
       tensors, chunk_begin, chunk_tensor, counts_dev, total_chunks, chunk_first, error_word);
-  const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(kApplyChunkCtas);
+  auto kernel = chunk_apply_kernel<1, kCwPreOne, kCwCtasOne>;
+  static const int per_sm = resident_per_sm(kernel, kCwThreads, kCwCtasOne);
+  const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(per_sm);
   const unsigned grid = unsigned(total_chunks < cap ? total_chunks : cap);
-  apply_chunk_kernel<<<grid, kChunkThreads, 0, stream>>>(tensors, chunk_begin, chunk_tensor,
-                                                         chunk_first, counts_dev, total_chunks,
-                                                         error_word, wait_limit_ns);
+  const CwArgs args{tensors, chunk_begin, chunk_tensor, chunk_first, nullptr, counts_dev,
+                    0,       1,           total_chunks, error_word, wait_limit_ns};
+  kernel<<<grid, kCwThreads, 0, stream>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply_chain(const TensorDesc* tensors, const uint64_t* chunk_begin,
+                               const uint32_t* chunk_tensor, uint32_t* chain_first,
+                               const ChainSeg* segs, int ntensors, int nversions,
+                               uint64_t total_chunks, uint32_t* error_word, uint64_t wait_limit_ns,
+                               cudaStream_t stream) {
+  if (total_chunks == 0 || nversions < 1) return cudaSuccess;
+  if (nversions > kChainMaxVersions) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t parts = total_chunks * uint64_t(nversions);
+  chain_partition_kernel<<<unsigned((parts + 255) / 256), 256, 0, stream>>>(
+      tensors, chunk_begin, chunk_tensor, segs, ntensors, nversions, total_chunks, chain_first,
+      error_word);
+  auto kernel = chunk_apply_kernel<kCwGroupChain, kCwPreChain, kCwCtasChain>;
+  static const int per_sm = resident_per_sm(kernel, kCwThreads, kCwCtasChain);
+  const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(per_sm);
+  const unsigned grid = unsigned(total_chunks < cap ? total_chunks : cap);
+  const CwArgs args{tensors,  chunk_begin,  chunk_tensor, chain_first, segs, nullptr,
+                    ntensors, nversions,    total_chunks, error_word,  wait_limit_ns};
+  kernel<<<grid, kCwThreads, 0, stream>>>(args);
   return cudaGetLastError();
 }
 

@@ -213,6 +213,17 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
+// Bulk prefetch of the whole 16-byte units inside [p, p + bytes) into L2 (no
+// byte outside the range is touched; the ragged ends are left to the loads).
+__device__ __forceinline__ void l2_prefetch_range(const void* p, uint64_t bytes) {
+  const uint64_t a = reinterpret_cast<uint64_t>(p);
+  const uint64_t lo = (a + 15u) & ~uint64_t(15);
+  const uint64_t hi = (a + bytes) & ~uint64_t(15);
+  if (hi > lo)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"(uint32_t(hi - lo))
+                 : "memory");
+}
+
 // Streaming 128/64/32-bit global loads that do not allocate in L1. The `_ro`
 // forms use the read-only path and are only for buffers nothing writes
 // during the kernel; the others are for in/out buffers.

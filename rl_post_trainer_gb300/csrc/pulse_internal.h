@@ -225,16 +225,29 @@ cudaError_t launch_apply_multi(const TensorDesc* tensors, int ntensors,
 #ifndef PULSE_APPLY_DENSE_MIN
 #define PULSE_APPLY_DENSE_MIN 64
 #endif
-#ifndef PULSE_APPLY_CHUNK_CTAS
-#define PULSE_APPLY_CHUNK_CTAS 6
-#endif
-constexpr int kApplyChunkCtas = PULSE_APPLY_CHUNK_CTAS;  // resident chunk-apply CTAs per SM
 constexpr int kApplyChunk = PULSE_APPLY_CHUNK;
 constexpr uint32_t kApplyDenseMin = PULSE_APPLY_DENSE_MIN;
 cudaError_t launch_apply_chunks(const TensorDesc* tensors, const uint64_t* chunk_begin,
                                 const uint32_t* chunk_tensor, uint32_t* chunk_first,
                                 const uint64_t* counts_dev, uint64_t total_chunks,
                                 uint32_t* error_word, uint64_t wait_limit_ns, cudaStream_t stream);
+
+// Chained apply: one tensor's patch of one version (ascending indices).
+struct ChainSeg {
+  const uint32_t* idx;
+  const uint16_t* val;
+  uint64_t count;
+};
+// Versions one chained-apply launch takes (longer chains take several
+// launches, in order, on the same stream).
+constexpr int kChainMaxVersions = 16;
+// segs: nversions x ntensors, version-major; chain_first: scratch of
+// nversions x total_chunks words. nversions in [1, kChainMaxVersions].
+cudaError_t launch_apply_chain(const TensorDesc* tensors, const uint64_t* chunk_begin,
+                               const uint32_t* chunk_tensor, uint32_t* chain_first,
+                               const ChainSeg* segs, int ntensors, int nversions,
+                               uint64_t total_chunks, uint32_t* error_word, uint64_t wait_limit_ns,
+                               cudaStream_t stream);
 
 // One byte-valued patch segment (an MXFP8 code or scale array).
 struct ByteSegment {

@@ -87,6 +87,14 @@ class PulseComposeSegment(ctypes.Structure):
     ]
 
 
+class PulsePatchRef(ctypes.Structure):
+    _fields_ = [
+        ("idx", ctypes.c_void_p),
+        ("val", ctypes.c_void_p),
+        ("count", ctypes.c_uint64),
+    ]
+
+
 class PulseLocoTensor(ctypes.Structure):
     _fields_ = [
         ("global_w", ctypes.c_void_p),
@@ -130,6 +138,7 @@ def lib():
             "pulse_encode_multi": ([P, P, P], I),
             "pulse_apply_multi": ([P, P, P], I),
             "pulse_apply_multi_device": ([P, P, P], I),
+            "pulse_apply_chain_multi": ([P, ctypes.POINTER(PulsePatchRef), I, P], I),
             "pulse_xor_mask_multi": ([P, P], I),
             "pulse_xor_apply_multi": ([P, P], I),
             "pulse_plan_get_error": ([P], I),
@@ -321,6 +330,14 @@ class TensorSlot:
         self.idx, self.val, self.mask = idx, val, mask
 
 
+class PreparedChain:
+    """A chain of patch versions checked and marshalled for one Plan."""
+
+    def __init__(self, plan, refs, nversions: int, keep):
+        self.plan, self.refs, self.nversions = plan, refs, int(nversions)
+        self._keep = keep  # the patch tensors stay alive with the references
+
+
 class Plan:
     """pulse_plan: tile tables of a fixed tensor list, built once, replayed per step."""
 
@@ -393,6 +410,42 @@ class Plan:
                 host = (ctypes.c_uint64 * self.ntensors)(*vals)
                 st = lib().pulse_apply_multi(self._h, host, _stream(self.device))
         _raise(st, "pulse_apply_multi")
+
+    def prepare_chain(self, patches) -> "PreparedChain":
+        """Check and marshal a chain once: patches[v][t] = (idx, val, count)
+        of tensor t in the v-th version to apply (oldest first); counts are
+        host integers. The result can be passed to apply_chain any number of
+        times while the patch buffers stay alive."""
+        nv = len(patches)
+        if nv < 1:
+            raise ValueError("a chain needs at least one version")
+        arr = (PulsePatchRef * (nv * self.ntensors))()
+        keep = []
+        for v, row in enumerate(patches):
+            if len(row) != self.ntensors:
+                raise ValueError(f"version {v}: {len(row)} segments for {self.ntensors} tensors")
+            for t, (idx, val, count) in enumerate(row):
+                c = int(count)
+                use = min(c, self.slots[t].n)
+                if use > 0:
+                    _need(idx, "idx", (torch.int32, torch.uint32), self.device, min_numel=use)
+                    _need(val, "val", _U16, self.device, min_numel=use)
+                    keep.append((idx, val))
+                arr[v * self.ntensors + t] = PulsePatchRef(_ptr(idx) if c > 0 else None,
+                                                           _ptr(val) if c > 0 else None, c)
+        return PreparedChain(self, arr, nv, keep)
+
+    def apply_chain(self, patches):
+        """pulse_apply_chain_multi: bring w forward by every version of the
+        chain (a PreparedChain, or the nested list prepare_chain takes) in
+        one pass; equals apply() of each version in turn."""
+        prep = patches if isinstance(patches, PreparedChain) else self.prepare_chain(patches)
+        if prep.plan is not self:
+            raise ValueError("the chain was prepared for another plan")
+        with torch.cuda.device(self.device):
+            st = lib().pulse_apply_chain_multi(self._h, prep.refs, prep.nversions,
+                                               _stream(self.device))
+        _raise(st, "pulse_apply_chain_multi")
 
     def xor_mask(self):
         with torch.cuda.device(self.device):

@@ -75,6 +75,9 @@ def test_host_side_argument_checks_launch_nothing(lib):
     assert lib.pulse_encode_multi(None, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_apply_multi(None, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_apply_multi_device(None, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
+    refs = (pulse.pulse.PulsePatchRef * 1)()
+    assert lib.pulse_apply_chain_multi(None, refs, 1, P(0)) == pulse.pulse.PULSE_ERR_INVALID
+    assert lib.pulse_apply_chain_multi(None, None, 1, P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_xor_mask_multi(None, P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_xor_apply_multi(None, P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_plan_get_error(None) == pulse.pulse.PULSE_ERR_INVALID
