@@ -22,7 +22,6 @@ SM clocks sampled during the timed region.
 from __future__ import annotations
 
 import argparse
-import ctypes
 import hashlib
 import json
 import os
@@ -702,52 +701,25 @@ def run_compose(args, wl, dev, versions: int = 4):
 
 def run_pack(args, wl, counts_np, dev):
     """Codec-friendly packing of the step's patch indices (every tensor's
-    segment; pulse_pack_indices per segment), and the receiver's unpack,
-    checked to round-trip. Times cover all segments (CUDA events)."""
+    segment in one pulse_pack_indices_multi launch), and the receiver's
+    unpack (one pulse_unpack_indices_multi launch), checked to round-trip.
+    CUDA events around each call."""
     import rl_post_trainer_gb300 as pulse
     stream = torch.cuda.current_stream(dev)
     wl.restore()
     wl.plan.encode(wl.counts)          # the step's patch into wl.idx / wl.val
     ks = wl.counts.cpu().tolist()
     T = len(ks)
-    outs = []
-    for k in ks:
-        nb = (k + 127) // 128
-        nc = (k + 4095) // 4096
-        outs.append((torch.empty(max(nb, 1), dtype=torch.int32, device=dev),
-                     torch.empty(max(nb, 1), dtype=torch.uint8, device=dev),
-                     torch.empty(max(nc, 1), dtype=torch.int64, device=dev),
-                     torch.empty(max(512 * nb, 16), dtype=torch.uint8, device=dev),
-                     torch.empty(1, dtype=torch.int64, device=dev),
-                     torch.empty(max(k, 1), dtype=torch.int32, device=dev)))
-    L = pulse.lib()
-    P = ctypes.c_void_p
-    s = P(stream.cuda_stream)
-
-    def pack_all():
-        for t in range(T):
-            f, w, c, p, nbytes, _ = outs[t]
-            st = L.pulse_pack_indices(P(wl.idx[t].data_ptr()), ks[t], P(f.data_ptr()), P(w.data_ptr()),
-                                      P(c.data_ptr()), P(p.data_ptr()), P(nbytes.data_ptr()), s)
-            if st != 0:
-                raise RuntimeError(f"pulse_pack_indices: {st}")
-
-    def unpack_all():
-        for t in range(T):
-            f, w, c, p, _, back = outs[t]
-            st = L.pulse_unpack_indices(P(f.data_ptr()), P(w.data_ptr()), P(c.data_ptr()),
-                                        P(p.data_ptr()), ks[t], P(back.data_ptr()), s)
-            if st != 0:
-                raise RuntimeError(f"pulse_unpack_indices: {st}")
+    job = pulse.PackJob([(wl.idx[t], ks[t]) for t in range(T)])
 
     tp, tu = [], []
     for r in range(args.warmup + args.steps):
         torch.cuda.synchronize()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         ev[0].record(stream)
-        pack_all()
+        job.pack()
         ev[1].record(stream)
-        unpack_all()
+        job.unpack()
         ev[2].record(stream)
         torch.cuda.synchronize()
         if r >= args.warmup:
@@ -756,10 +728,10 @@ def run_pack(args, wl, counts_np, dev):
     if pulse.get_error(dev) != 0:
         raise RuntimeError("device error in the packing leg")
     for t in range(T):
-        if ks[t] and not torch.equal(outs[t][5][:ks[t]], wl.idx[t][:ks[t]]):
+        if ks[t] and not torch.equal(job.unpacked[t][:ks[t]], wl.idx[t][:ks[t]]):
             raise RuntimeError(f"unpack differs from the patch indices (tensor {t})")
     k = sum(ks)
-    payload = sum(int(o[4].item()) for o in outs)
+    payload = int(job.payload_bytes.sum().item())
     headers = sum(5 * ((kk + 127) // 128) + 8 * ((kk + 4095) // 4096) for kk in ks)
     tpm, tum = float(np.mean(tp)), float(np.mean(tu))
     return {
@@ -768,7 +740,7 @@ def run_pack(args, wl, counts_np, dev):
         "patch_bytes_raw": 6 * k, "patch_bytes_packed": payload + headers + 2 * k,
         "pack_ms": 1e3 * tpm, "unpack_ms": 1e3 * tum,
         "pack_gbs_in": 4.0 * k / tpm / 1e9, "unpack_gbs_out": 4.0 * k / tum / 1e9,
-        "launches": 2 * T, "timing": "all 291 segments, one call each, CUDA events",
+        "launches": 2, "timing": f"all {T} segments in one pack and one unpack launch, CUDA events",
     }
 
 

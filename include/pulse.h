@@ -373,6 +373,34 @@ int pulse_unpack_indices(const uint32_t *firsts, const uint8_t *widths, const ui
                          const uint8_t *payload, uint64_t count, uint32_t *idx_out,
                          cudaStream_t stream);
 
+/*
+ * pulse_pack_indices_multi -- pack the index segments of a whole model in
+ * one launch (every chunk of every segment). segs: HOST array of nsegs
+ * segments, copied before the call returns; each is packed exactly as
+ * pulse_pack_indices packs it (idx is read). payload_bytes: DEVICE, nsegs
+ * uint64: segment s's payload size (0 for an empty segment). Uses the
+ * per-(device, stream) workspace of pulse_encode; growing it synchronises
+ * `stream`. Errors: PULSE_ERR_INVALID (NULL segs or payload_bytes, nsegs < 1,
+ * a NULL or misaligned buffer of a non-empty segment), PULSE_ERR_RANGE (a
+ * count >= 2^32), PULSE_ERR_NOMEM, PULSE_ERR_CUDA; device: PULSE_ERR_TIMEOUT.
+ *
+ * pulse_unpack_indices_multi -- the inverse over the same segment table:
+ * rebuilds each segment's count indices into its idx (written), one launch.
+ * payload 4-byte aligned.
+ */
+typedef struct pulse_pack_segment {
+    uint32_t *idx;        /* device, count indices: read by pack, written by unpack */
+    uint64_t count;       /* host value */
+    uint32_t *firsts;     /* device, ceil(count / 128) */
+    uint8_t *widths;      /* device, ceil(count / 128) */
+    uint64_t *chunk_off;  /* device, ceil(count / 4096) */
+    uint8_t *payload;     /* device, room for 512 * ceil(count / 128) bytes */
+} pulse_pack_segment;
+
+int pulse_pack_indices_multi(const pulse_pack_segment *segs, int nsegs, uint64_t *payload_bytes,
+                             cudaStream_t stream);
+int pulse_unpack_indices_multi(const pulse_pack_segment *segs, int nsegs, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------
  * Patch-chain composition. [TALK] 16:40-17:04: a sidecar whose engine is
  * behind applies the missing transitions; [PULSE] "1. PULSESync": patch

@@ -9,6 +9,7 @@ from .pulse import (  # noqa: F401
     LocoTensorSlot,
     MxPlan,
     MxTensorSlot,
+    PackJob,
     Plan,
     PreparedChain,
     PulseError,

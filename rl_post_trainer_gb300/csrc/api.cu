@@ -916,6 +916,122 @@ int pulse_unpack_indices(const uint32_t* firsts, const uint8_t* widths, const ui
   return cuda_status(launch_unpack(firsts, widths, chunk_off, payload, count, idx_out, stream));
 }
 
+namespace {
+// Segment tables of the multi-segment pack calls, per (device, stream); the
+// look-back scratch is the stream's encode workspace.
+struct PackTables {
+  PackSegment* segs = nullptr;
+  uint64_t* begin = nullptr;
+  int cap = 0;
+};
+std::map<std::pair<int, uintptr_t>, PackTables*> g_pack_tables;
+
+// Check a host segment table, build the device-side one and the chunk
+// offsets; `unpack` selects the unpack alignment rule.
+int pack_table(const pulse_pack_segment* segs, int nsegs, uint64_t* payload_bytes, bool unpack,
+               std::vector<PackSegment>& table, std::vector<uint64_t>& begin) {
+  if (segs == nullptr || nsegs < 1) return PULSE_ERR_INVALID;
+  table.resize(static_cast<size_t>(nsegs));
+  begin.resize(static_cast<size_t>(nsegs) + 1);
+  uint64_t chunks = 0;
+  for (int i = 0; i < nsegs; ++i) {
+    const pulse_pack_segment& g = segs[i];
+    if (g.count >= kMaxElems + 1) return PULSE_ERR_RANGE;
+    if (g.count > 0 && (g.idx == nullptr || g.firsts == nullptr || g.widths == nullptr ||
+                        g.chunk_off == nullptr || g.payload == nullptr))
+      return PULSE_ERR_INVALID;
+    if (g.count > 0 && !aligned(g.payload, unpack ? 4 : 16)) return PULSE_ERR_INVALID;
+    begin[size_t(i)] = chunks;
+    table[size_t(i)] = PackSegment{g.idx,     g.count,   g.firsts,
+                                   g.widths,  g.chunk_off, g.payload,
+                                   payload_bytes == nullptr ? nullptr : payload_bytes + i, chunks};
+    chunks += pack_chunks(g.count);
+  }
+  begin[size_t(nsegs)] = chunks;
+  return chunks > kMaxTiles ? PULSE_ERR_RANGE : PULSE_OK;
+}
+
+// Upload the tables (growth synchronises `stream`).
+int pack_upload(int device, cudaStream_t stream, const std::vector<PackSegment>& table,
+                const std::vector<uint64_t>& begin, PackTables** out) {
+  auto key = std::make_pair(device, reinterpret_cast<uintptr_t>(stream));
+  PackTables*& t = g_pack_tables[key];
+  if (t == nullptr) t = new (std::nothrow) PackTables();
+  if (t == nullptr) return PULSE_ERR_NOMEM;
+  const int nsegs = int(table.size());
+  if (nsegs > t->cap) {
+    int cap = t->cap ? t->cap : 64;
+    while (cap < nsegs) cap *= 2;
+    if (t->segs != nullptr || t->begin != nullptr) {
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return PULSE_ERR_CUDA;
+      if (t->segs) cudaFree(t->segs);
+      if (t->begin) cudaFree(t->begin);
+      t->segs = nullptr;
+      t->begin = nullptr;
+      t->cap = 0;
+    }
+    if (cudaMalloc(&t->segs, sizeof(PackSegment) * size_t(cap)) != cudaSuccess ||
+        cudaMalloc(&t->begin, sizeof(uint64_t) * (size_t(cap) + 1)) != cudaSuccess)
+      return PULSE_ERR_NOMEM;
+    t->cap = cap;
+  }
+  // (copies from pageable memory are staged before cudaMemcpyAsync returns)
+  if (cudaMemcpyAsync(t->segs, table.data(), sizeof(PackSegment) * table.size(),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(t->begin, begin.data(), sizeof(uint64_t) * begin.size(),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  *out = t;
+  return PULSE_OK;
+}
+}  // namespace
+
+int pulse_pack_indices_multi(const pulse_pack_segment* segs, int nsegs, uint64_t* payload_bytes,
+                             cudaStream_t stream) {
+  if (payload_bytes == nullptr) return PULSE_ERR_INVALID;
+  std::vector<PackSegment> table;
+  std::vector<uint64_t> begin;
+  int st = pack_table(segs, nsegs, payload_bytes, false, table, begin);
+  if (st != PULSE_OK) return st;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  // empty segments have no chunk: their size is 0; the others are written
+  // by their last chunk
+  if (cudaMemsetAsync(payload_bytes, 0, sizeof(uint64_t) * size_t(nsegs), stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  const uint64_t chunks = begin.back();
+  if (chunks == 0) return PULSE_OK;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  Workspace* ws = stream_workspace(device, stream);
+  if (ws == nullptr) return PULSE_ERR_NOMEM;
+  st = workspace_reserve(*ws, chunks, stream);
+  if (st != PULSE_OK) return st;
+  PackTables* t = nullptr;
+  st = pack_upload(device, stream, table, begin, &t);
+  if (st != PULSE_OK) return st;
+  uint32_t epoch = 0;
+  st = workspace_next_epoch(*ws, stream, &epoch);
+  if (st != PULSE_OK) return st;
+  return cuda_status(launch_pack_multi(t->segs, t->begin, nsegs, chunks, ws->status, ws->counters,
+                                       epoch, kDefaultWaitNs, stream));
+}
+
+int pulse_unpack_indices_multi(const pulse_pack_segment* segs, int nsegs, cudaStream_t stream) {
+  std::vector<PackSegment> table;
+  std::vector<uint64_t> begin;
+  int st = pack_table(segs, nsegs, nullptr, true, table, begin);
+  if (st != PULSE_OK) return st;
+  const uint64_t chunks = begin.back();
+  if (chunks == 0) return PULSE_OK;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  PackTables* t = nullptr;
+  st = pack_upload(device, stream, table, begin, &t);
+  if (st != PULSE_OK) return st;
+  return cuda_status(launch_unpack_multi(t->segs, t->begin, nsegs, chunks, stream));
+}
+
 // ------------------------------------------------------------ compose
 
 int pulse_compose(const uint32_t* idx_a, const uint16_t* val_a, uint64_t count_a,

@@ -31,13 +31,10 @@ constexpr int kPackWarps = kPackThreads / 32;
 constexpr int kBlocksPerWarp = kPackChunkBlocks / kPackWarps;  // 4
 
 struct PackLaunch {
-  const uint32_t* idx;
-  uint64_t count;
-  uint32_t* firsts;
-  uint8_t* widths;
-  uint64_t* chunk_off;
-  uint8_t* payload;
-  uint64_t* payload_bytes;
+  PackSegment one;             // single-segment mode (chunk_begin 0)
+  const PackSegment* segs;     // multi-segment mode: device table
+  const uint64_t* chunk_begin; // multi-segment mode: nsegs + 1 entries (device)
+  int nsegs;
   uint64_t total_chunks;
   uint64_t* status;
   uint32_t* counters;
@@ -45,8 +42,16 @@ struct PackLaunch {
   uint64_t wait_limit_ns;
 };
 
+// The segment that global chunk c belongs to.
+template <bool MULTI>
+__device__ __forceinline__ PackSegment segment_of(const PackLaunch& a, uint64_t c) {
+  if (!MULTI) return a.one;
+  return a.segs[enc::find_tensor(a.chunk_begin, a.nsegs, c)];
+}
+
 __device__ __forceinline__ uint32_t bit_width(uint32_t v) { return v ? 32u - __clz(v) : 0u; }
 
+template <bool MULTI>
 __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constant__ PackLaunch a) {
   __shared__ uint32_t words[kPackWarps][kPackBlock];  // one block's packed words per warp
   __shared__ uint32_t width_of[kPackChunkBlocks];
@@ -55,7 +60,9 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constan
   if (tid == 0) ticket = atomicAdd(a.counters + 0, 1u);
   __syncthreads();
   const uint64_t c = ticket;  // chunks are taken in ticket order: predecessors already run
-  const uint64_t chunk_first = c * kPackChunk;
+  const PackSegment sg = segment_of<MULTI>(a, c);
+  const uint64_t lc = c - sg.chunk_begin;  // chunk within the segment
+  const uint64_t chunk_first = lc * kPackChunk;
 
   // ---- widths and firsts; the gaps stay in registers
   uint32_t gap[kBlocksPerWarp][4];
@@ -64,13 +71,13 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constan
   for (int q = 0; q < kBlocksPerWarp; ++q) {
     const int lb = warp * kBlocksPerWarp + q;
     const uint64_t start = chunk_first + uint64_t(lb) * kPackBlock;
-    const uint32_t cnt = start < a.count ? uint32_t(a.count - start < kPackBlock ? a.count - start : kPackBlock) : 0u;
+    const uint32_t cnt = start < sg.count ? uint32_t(sg.count - start < kPackBlock ? sg.count - start : kPackBlock) : 0u;
     cnt_blk[q] = cnt;
     uint32_t v[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
-      v[e] = j < cnt ? a.idx[start + j] : 0u;
+      v[e] = j < cnt ? sg.idx[start + j] : 0u;
     }
     const uint32_t before = __shfl_up_sync(0xFFFFFFFFu, v[3], 1);  // lane - 1's last entry
     uint32_t mx = 0;
@@ -85,8 +92,8 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constan
     if (lane == 0) {
       width_of[lb] = cnt ? bit_width(mx) : 0u;
       if (cnt) {
-        a.firsts[start / kPackBlock] = v[0];
-        a.widths[start / kPackBlock] = uint8_t(bit_width(mx));
+        sg.firsts[start / kPackBlock] = v[0];
+        sg.widths[start / kPackBlock] = uint8_t(bit_width(mx));
       }
     }
   }
@@ -96,17 +103,20 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constan
   if (warp == 0) {
     const uint32_t wl = width_of[lane];
     const uint32_t agg = __reduce_add_sync(0xFFFFFFFFu, wl);
-    if (lane == 0) st_relaxed_u64(a.status + c, make_status(c == 0 ? kFlagPrefix : kFlagAggregate, a.epoch, agg));
+    // the look-back restarts at each segment's first chunk
+    const uint64_t first = sg.chunk_begin;
+    if (lane == 0)
+      st_relaxed_u64(a.status + c, make_status(c == first ? kFlagPrefix : kFlagAggregate, a.epoch, agg));
     uint32_t p = 0;
-    if (c != 0) {
+    if (c != first) {
       uint64_t win[enc::kLookbackPerLane];
-      enc::load_window<enc::StatusEpoch>(a, int64_t(c) - 1, 0, lane, win);
-      p = enc::resolve_prefix<enc::StatusEpoch>(a, c, 0, agg, lane, win);
+      enc::load_window<enc::StatusEpoch>(a, int64_t(c) - 1, first, lane, win);
+      p = enc::resolve_prefix<enc::StatusEpoch>(a, c, first, agg, lane, win);
     }
     if (lane == 0) {
       prefix16 = p;
-      a.chunk_off[c] = uint64_t(p) * 16u;
-      if (c + 1 == a.total_chunks) *a.payload_bytes = (uint64_t(p) + agg) * 16u;
+      sg.chunk_off[lc] = uint64_t(p) * 16u;
+      if ((lc + 1) * kPackChunk >= sg.count) *sg.payload_bytes = (uint64_t(p) + agg) * 16u;
     }
   }
   __syncthreads();
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constan
         }
       }
       __syncwarp();
-      uint32_t* dst = reinterpret_cast<uint32_t*>(a.payload + uint64_t(off16) * 16u);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(sg.payload + uint64_t(off16) * 16u);
       for (uint32_t w = lane; w < nwords; w += 32) dst[w] = words[warp][w];
       __syncwarp();
     }
@@ -151,17 +161,22 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constan
   }
 }
 
-__global__ void __launch_bounds__(kPackThreads)
-    unpack_kernel(const uint32_t* __restrict__ firsts, const uint8_t* __restrict__ widths,
-                  const uint64_t* __restrict__ chunk_off, const uint8_t* __restrict__ payload,
-                  uint64_t count, uint32_t* __restrict__ idx_out) {
+template <bool MULTI>
+__global__ void __launch_bounds__(kPackThreads) unpack_kernel(const __grid_constant__ PackLaunch a) {
   __shared__ uint32_t words[kPackWarps][kPackBlock + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint64_t c = blockIdx.x;
-  const uint64_t chunk_first = c * kPackChunk;
+  const PackSegment sg = segment_of<MULTI>(a, c);
+  const uint64_t lc = c - sg.chunk_begin;  // chunk within the segment
+  const uint64_t chunk_first = lc * kPackChunk;
+  const uint64_t count = sg.count;
+  const uint32_t* __restrict__ firsts = sg.firsts;
+  const uint8_t* __restrict__ widths = sg.widths;
+  const uint8_t* __restrict__ payload = sg.payload;
+  uint32_t* __restrict__ idx_out = sg.idx;
   const uint64_t nblocks = (count + kPackBlock - 1) / kPackBlock;
   // widths of the chunk's blocks and their exclusive prefix (16-byte units)
-  const uint64_t gb_lane = c * kPackChunkBlocks + uint64_t(lane);
+  const uint64_t gb_lane = lc * kPackChunkBlocks + uint64_t(lane);
   const uint32_t wl = gb_lane < nblocks ? widths[gb_lane] : 0u;
   uint32_t incl = wl;
 #pragma unroll
@@ -169,7 +184,7 @@ __global__ void __launch_bounds__(kPackThreads)
     const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= o) incl += v;
   }
-  const uint64_t base_off = chunk_off[c];
+  const uint64_t base_off = sg.chunk_off[lc];
 #pragma unroll
   for (int q = 0; q < kBlocksPerWarp; ++q) {
     const int lb = warp * kBlocksPerWarp + q;
@@ -224,20 +239,33 @@ cudaError_t launch_pack(const uint32_t* idx, uint64_t count, uint32_t* firsts, u
                         uint64_t* status, uint32_t* counters, uint32_t epoch,
                         uint64_t wait_limit_ns, cudaStream_t stream) {
   PackLaunch a{};
-  a.idx = idx;
-  a.count = count;
-  a.firsts = firsts;
-  a.widths = widths;
-  a.chunk_off = chunk_off;
-  a.payload = payload;
-  a.payload_bytes = payload_bytes;
+  a.one = PackSegment{const_cast<uint32_t*>(idx), count, firsts, widths, chunk_off, payload,
+                      payload_bytes, 0};
+  a.nsegs = 1;
   a.total_chunks = pack_chunks(count);
   a.status = status;
   a.counters = counters;
   a.epoch = epoch;
   a.wait_limit_ns = wait_limit_ns;
   if (a.total_chunks == 0) return cudaSuccess;
-  pack_kernel<<<unsigned(a.total_chunks), kPackThreads, 0, stream>>>(a);
+  pack_kernel<false><<<unsigned(a.total_chunks), kPackThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_multi(const PackSegment* segs, const uint64_t* chunk_begin, int nsegs,
+                              uint64_t total_chunks, uint64_t* status, uint32_t* counters,
+                              uint32_t epoch, uint64_t wait_limit_ns, cudaStream_t stream) {
+  if (total_chunks == 0) return cudaSuccess;
+  PackLaunch a{};
+  a.segs = segs;
+  a.chunk_begin = chunk_begin;
+  a.nsegs = nsegs;
+  a.total_chunks = total_chunks;
+  a.status = status;
+  a.counters = counters;
+  a.epoch = epoch;
+  a.wait_limit_ns = wait_limit_ns;
+  pack_kernel<true><<<unsigned(total_chunks), kPackThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -246,8 +274,24 @@ cudaError_t launch_unpack(const uint32_t* firsts, const uint8_t* widths, const u
                           cudaStream_t stream) {
   const uint64_t chunks = pack_chunks(count);
   if (chunks == 0) return cudaSuccess;
-  unpack_kernel<<<unsigned(chunks), kPackThreads, 0, stream>>>(firsts, widths, chunk_off, payload,
-                                                               count, idx_out);
+  PackLaunch a{};
+  a.one = PackSegment{idx_out, count, const_cast<uint32_t*>(firsts), const_cast<uint8_t*>(widths),
+                      const_cast<uint64_t*>(chunk_off), const_cast<uint8_t*>(payload), nullptr, 0};
+  a.nsegs = 1;
+  a.total_chunks = chunks;
+  unpack_kernel<false><<<unsigned(chunks), kPackThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_multi(const PackSegment* segs, const uint64_t* chunk_begin, int nsegs,
+                                uint64_t total_chunks, cudaStream_t stream) {
+  if (total_chunks == 0) return cudaSuccess;
+  PackLaunch a{};
+  a.segs = segs;
+  a.chunk_begin = chunk_begin;
+  a.nsegs = nsegs;
+  a.total_chunks = total_chunks;
+  unpack_kernel<true><<<unsigned(total_chunks), kPackThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -165,7 +165,24 @@ cudaError_t launch_loco_accumulate_multi(const LocoTensorDesc* tensors, int nten
                                          cudaStream_t stream);
 
 // ---------------------------------------------------------------- index packing
+// One segment of indices to pack (or to rebuild: idx is then written).
+struct PackSegment {
+  uint32_t* idx;
+  uint64_t count;
+  uint32_t* firsts;
+  uint8_t* widths;
+  uint64_t* chunk_off;
+  uint8_t* payload;
+  uint64_t* payload_bytes;  // pack: this segment's device word
+  uint64_t chunk_begin;     // first global chunk of this segment
+};
 uint64_t pack_chunks(uint64_t count);
+// segs / chunk_begin: device tables (nsegs, nsegs + 1 entries).
+cudaError_t launch_pack_multi(const PackSegment* segs, const uint64_t* chunk_begin, int nsegs,
+                              uint64_t total_chunks, uint64_t* status, uint32_t* counters,
+                              uint32_t epoch, uint64_t wait_limit_ns, cudaStream_t stream);
+cudaError_t launch_unpack_multi(const PackSegment* segs, const uint64_t* chunk_begin, int nsegs,
+                                uint64_t total_chunks, cudaStream_t stream);
 cudaError_t launch_pack(const uint32_t* idx, uint64_t count, uint32_t* firsts, uint8_t* widths,
                         uint64_t* chunk_off, uint8_t* payload, uint64_t* payload_bytes,
                         uint64_t* status, uint32_t* counters, uint32_t epoch,

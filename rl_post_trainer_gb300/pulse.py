@@ -95,6 +95,17 @@ class PulsePatchRef(ctypes.Structure):
     ]
 
 
+class PulsePackSegment(ctypes.Structure):
+    _fields_ = [
+        ("idx", ctypes.c_void_p),
+        ("count", ctypes.c_uint64),
+        ("firsts", ctypes.c_void_p),
+        ("widths", ctypes.c_void_p),
+        ("chunk_off", ctypes.c_void_p),
+        ("payload", ctypes.c_void_p),
+    ]
+
+
 class PulseLocoTensor(ctypes.Structure):
     _fields_ = [
         ("global_w", ctypes.c_void_p),
@@ -156,6 +167,8 @@ def lib():
             "pulse_loco_plan_get_error": ([P], I),
             "pulse_pack_indices": ([P, U64, P, P, P, P, P, P], I),
             "pulse_unpack_indices": ([P, P, P, P, U64, P, P], I),
+            "pulse_pack_indices_multi": ([ctypes.POINTER(PulsePackSegment), I, P, P], I),
+            "pulse_unpack_indices_multi": ([ctypes.POINTER(PulsePackSegment), I, P], I),
             "pulse_mx_quantize": ([P, U64, P, P, P], I),
             "pulse_mx_encode": ([P, P, P, U64, P, P, P, P, P, P], I),
             "pulse_mx_apply": ([P, P, U64, P, P, U64, P, P, U64, P], I),
@@ -899,3 +912,60 @@ def unpack_indices(firsts: torch.Tensor, widths: torch.Tensor, chunk_off: torch.
                                         count, _ptr(idx_out), _stream(dev))
     _raise(st, "pulse_unpack_indices")
     return idx_out
+
+
+class PackJob:
+    """pulse_pack_indices_multi / pulse_unpack_indices_multi over a fixed list
+    of index segments: the output buffers and both segment tables are built
+    once; pack() and unpack() are one launch each for the whole list.
+
+    segments: list of (idx tensor, count) with strictly ascending indices.
+    After pack(): packed[s] = (firsts, widths, chunk_off, payload) of segment
+    s, payload_bytes[s] (device int64) its payload size. unpack() rebuilds
+    every segment into unpacked[s] (first count entries)."""
+
+    def __init__(self, segments):
+        if len(segments) == 0:
+            raise ValueError("a pack job needs at least one segment")
+        dev = None
+        self.counts, self.packed, self.unpacked, keep = [], [], [], []
+        n = len(segments)
+        self._pack_arr = (PulsePackSegment * n)()
+        self._unpack_arr = (PulsePackSegment * n)()
+        for i, (idx, count) in enumerate(segments):
+            count = int(count)
+            if dev is None:
+                dev = idx.device
+            _need(idx, "idx", (torch.int32, torch.uint32), dev, min_numel=count)
+            nb = (count + PACK_BLOCK - 1) // PACK_BLOCK
+            nc = (count + PACK_CHUNK - 1) // PACK_CHUNK
+            firsts = torch.empty(max(nb, 1), dtype=torch.int32, device=dev)
+            widths = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+            chunk_off = torch.empty(max(nc, 1), dtype=torch.int64, device=dev)
+            payload = torch.empty(max(512 * nb, 16), dtype=torch.uint8, device=dev)
+            out = torch.empty(max(count, 1), dtype=torch.int32, device=dev)
+            self.counts.append(count)
+            self.packed.append((firsts, widths, chunk_off, payload))
+            self.unpacked.append(out)
+            keep.append(idx)
+            self._pack_arr[i] = PulsePackSegment(_ptr(idx), count, _ptr(firsts), _ptr(widths),
+                                                 _ptr(chunk_off), _ptr(payload))
+            self._unpack_arr[i] = PulsePackSegment(_ptr(out), count, _ptr(firsts), _ptr(widths),
+                                                   _ptr(chunk_off), _ptr(payload))
+        self.device = dev
+        self.nsegs = n
+        self._keep = keep
+        self.payload_bytes = torch.zeros(n, dtype=torch.int64, device=dev)
+
+    def pack(self) -> torch.Tensor:
+        with torch.cuda.device(self.device):
+            st = lib().pulse_pack_indices_multi(self._pack_arr, self.nsegs, _ptr(self.payload_bytes),
+                                                _stream(self.device))
+        _raise(st, "pulse_pack_indices_multi")
+        return self.payload_bytes
+
+    def unpack(self):
+        with torch.cuda.device(self.device):
+            st = lib().pulse_unpack_indices_multi(self._unpack_arr, self.nsegs, _stream(self.device))
+        _raise(st, "pulse_unpack_indices_multi")
+        return self.unpacked

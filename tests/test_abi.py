@@ -75,6 +75,15 @@ def test_host_side_argument_checks_launch_nothing(lib):
     assert lib.pulse_encode_multi(None, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_apply_multi(None, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_apply_multi_device(None, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
+    segs = (pulse.pulse.PulsePackSegment * 1)()
+    assert lib.pulse_pack_indices_multi(None, 1, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
+    assert lib.pulse_pack_indices_multi(segs, 0, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
+    assert lib.pulse_pack_indices_multi(segs, 1, None, P(0)) == pulse.pulse.PULSE_ERR_INVALID
+    segs[0].count = 5  # a non-empty segment with NULL buffers
+    assert lib.pulse_pack_indices_multi(segs, 1, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
+    assert lib.pulse_unpack_indices_multi(segs, 1, P(0)) == pulse.pulse.PULSE_ERR_INVALID
+    segs[0].count = 1 << 32
+    assert lib.pulse_unpack_indices_multi(segs, 1, P(0)) == pulse.pulse.PULSE_ERR_RANGE
     refs = (pulse.pulse.PulsePatchRef * 1)()
     assert lib.pulse_apply_chain_multi(None, refs, 1, P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_apply_chain_multi(None, None, 1, P(0)) == pulse.pulse.PULSE_ERR_INVALID

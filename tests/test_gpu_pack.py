@@ -79,3 +79,68 @@ def test_pack_an_encode_patch():
     k = int(cnt.item())
     size = _check(host_u32(idx[:k]), dev)
     assert size < k   # under one byte per index at about 8 % density
+
+
+def _check_job(segs_np, dev, offsets=None):
+    """Pack a list of segments in one launch (PackJob) and compare every
+    segment's arrays with the oracle packing that segment alone; unpack
+    them all in one launch and compare with the input."""
+    tens = []
+    for i, a in enumerate(segs_np):
+        off = 0 if offsets is None else offsets[i]
+        buf = torch.zeros(a.size + off + 1, dtype=torch.int32, device=dev)
+        if a.size:
+            buf[off:off + a.size] = dev_u32(a, dev)
+        tens.append((buf[off:], a.size))
+    job = pulse.PackJob(tens)
+    sizes = job.pack()
+    outs = job.unpack()
+    torch.cuda.synchronize()
+    assert pulse.get_error(dev) == 0
+    sizes = sizes.cpu().tolist()
+    for a, (firsts, widths, chunk_off, payload), size, back in zip(segs_np, job.packed, sizes, outs):
+        of, ow, oc, op = oracle.pack_indices(a)
+        nb, nc = of.size, oc.size
+        assert size == op.size
+        np.testing.assert_array_equal(host_u32(firsts[:nb]), of)
+        np.testing.assert_array_equal(widths[:nb].cpu().numpy(), ow)
+        np.testing.assert_array_equal(chunk_off[:nc].cpu().numpy().view(np.uint64), oc)
+        np.testing.assert_array_equal(payload[:size].cpu().numpy(), op)
+        np.testing.assert_array_equal(host_u32(back[:a.size]), a)
+
+
+def test_pack_job_many_segments():
+    """Segments of every size edge (empty ones included) in one launch: the
+    look-back restarts at each segment's first chunk."""
+    dev = _dev()
+    rng = np.random.default_rng(77)
+    ks = [0, 1, 2, 127, 128, 129, 0, 4095, 4096, 4097, 3 * 4096 + 5, 100000, 0, 7]
+    segs = [_random_idx(rng, k, int(rng.choice([0, 11, 1000])), big=bool(i % 3 == 0))
+            for i, k in enumerate(ks)]
+    _check_job(segs, dev)
+
+
+def test_pack_job_unaligned_inputs_and_model_patch():
+    """A model's patch (one segment per tensor, from a GPU encode) with
+    index views that start at odd word offsets."""
+    dev = _dev()
+    rng = np.random.default_rng(5)
+    specs = workloads.llama_layer()
+    segs = []
+    for s in specs:
+        n = s.numel // 16
+        w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        prev = oracle.bf16_rne(w0.view(np.uint32)).astype(np.uint16)
+        w1 = (w0 + np.float32(3e-6) * rng.standard_normal(n).astype(np.float32)).astype(np.float32)
+        idx, _ = oracle.encode(w1, prev)
+        segs.append(idx)
+    _check_job(segs, dev, offsets=[i % 4 for i in range(len(segs))])
+
+
+def test_pack_job_all_empty():
+    dev = _dev()
+    job = pulse.PackJob([(torch.zeros(1, dtype=torch.int32, device=dev), 0)] * 3)
+    assert job.pack().cpu().tolist() == [0, 0, 0]
+    job.unpack()
+    torch.cuda.synchronize()
+    assert pulse.get_error(dev) == 0
