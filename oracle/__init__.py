@@ -3,7 +3,7 @@
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg use it; the product library never does. The
 arithmetic lives in ``pulse_oracle.c`` (BF16 view), ``mx_oracle.c``
-(MXFP8 view), ``compose_oracle.c`` (patch chains), ``loco_oracle.c``
+(MXFP8 view), ``mxfp4_oracle.c`` (MXFP4 view), ``compose_oracle.c`` (patch chains), ``loco_oracle.c``
 (PULSELoCo gate) and ``pack_oracle.c`` (index packing): plain C, scalar loops, ascending index order; this module
 compiles them with gcc and wraps them for numpy arrays. It imports nothing from the CUDA package.
 """
@@ -27,6 +27,12 @@ from .oracle import (  # noqa: F401
     mxfp8_encode,
     apply_u8,
     mxfp8_apply,
+    e2m1_rne,
+    mxfp4_block_scale,
+    mxfp4_code_bytes,
+    mxfp4_quantize,
+    mxfp4_encode,
+    mxfp4_apply,
     compose,
     compose_chain,
     loco_gate,

@@ -22,8 +22,8 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, f) for f in ("pulse_oracle.c", "mx_oracle.c", "compose_oracle.c",
-                                          "loco_oracle.c", "pack_oracle.c")]
+_SRCS = [os.path.join(_HERE, f) for f in ("pulse_oracle.c", "mx_oracle.c", "mxfp4_oracle.c",
+                                          "compose_oracle.c", "loco_oracle.c", "pack_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
@@ -75,6 +75,14 @@ def _load():
             lib.oracle_mxfp8_quantize.restype = None
             lib.oracle_mxfp8_encode.argtypes = [P, P, P, U64, P, P, P, P, P]
             lib.oracle_mxfp8_encode.restype = None
+            lib.oracle_e2m1_rne.argtypes = [ctypes.c_double]
+            lib.oracle_e2m1_rne.restype = ctypes.c_uint8
+            lib.oracle_mxfp4_block_scale.argtypes = [P, U64]
+            lib.oracle_mxfp4_block_scale.restype = ctypes.c_uint8
+            lib.oracle_mxfp4_quantize.argtypes = [P, U64, P, P]
+            lib.oracle_mxfp4_quantize.restype = None
+            lib.oracle_mxfp4_encode.argtypes = [P, P, P, U64, P, P, P, P, P]
+            lib.oracle_mxfp4_encode.restype = None
             lib.oracle_apply_u8.argtypes = [P, P, P, U64]
             lib.oracle_apply_u8.restype = None
             lib.oracle_compose.argtypes = [P, P, U64, P, P, U64, P, P]
@@ -256,6 +264,65 @@ def apply_u8(w: np.ndarray, idx: np.ndarray, val: np.ndarray) -> None:
 
 def mxfp8_apply(codes: np.ndarray, scales: np.ndarray, patch) -> None:
     """Apply both segments of an MXFP8 patch (idx, val, sidx, sval) in place."""
+    idx, val, sidx, sval = patch
+    apply_u8(codes, idx, val)
+    apply_u8(scales, sidx, sval)
+
+
+# ------------------------------------------------------------- MXFP4 view
+
+def e2m1_rne(y) -> int:
+    """E2M1 code (4 bits, bit 3 = sign) of one finite value y, RNE, clamped to 6."""
+    return int(_load().oracle_e2m1_rne(float(y)))
+
+
+def mxfp4_block_scale(block: np.ndarray) -> int:
+    """E8M0 scale byte of one MXFP4 block of 1..32 FP32 values."""
+    _check(block, np.float32, "block")
+    if not 1 <= block.size <= MX_BLOCK:
+        raise ValueError("a block holds 1..32 values")
+    return int(_load().oracle_mxfp4_block_scale(_ptr(block), block.size))
+
+
+def mxfp4_code_bytes(n: int) -> int:
+    """Bytes of an n-element MXFP4 code array (two codes per byte)."""
+    return (n + 1) // 2
+
+
+def mxfp4_quantize(master: np.ndarray):
+    """Returns the MXFP4 view (codes uint8[ceil(n/2)], element 2j in the low
+    nibble of byte j; scales uint8[ceil(n/32)])."""
+    _check(master, np.float32, "master")
+    n = master.size
+    codes = np.empty(mxfp4_code_bytes(n), dtype=np.uint8)
+    scales = np.empty(mx_blocks(n), dtype=np.uint8)
+    _load().oracle_mxfp4_quantize(_ptr(master), n, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def mxfp4_encode(master: np.ndarray, prev_codes: np.ndarray, prev_scales: np.ndarray):
+    """Returns (idx uint32, val uint8, sidx uint32, sval uint8): changed code
+    BYTES and changed scales; refreshes ``prev_codes`` and ``prev_scales``."""
+    _check(master, np.float32, "master")
+    _check(prev_codes, np.uint8, "prev_codes", writable=True)
+    _check(prev_scales, np.uint8, "prev_scales", writable=True)
+    n = master.size
+    if prev_codes.size != mxfp4_code_bytes(n) or prev_scales.size != mx_blocks(n):
+        raise ValueError("view arrays do not match the master's length")
+    nb, ncb = mx_blocks(n), mxfp4_code_bytes(n)
+    idx = np.empty(max(ncb, 1), dtype=np.uint32)
+    val = np.empty(max(ncb, 1), dtype=np.uint8)
+    sidx = np.empty(max(nb, 1), dtype=np.uint32)
+    sval = np.empty(max(nb, 1), dtype=np.uint8)
+    counts = np.zeros(2, dtype=np.uint64)
+    _load().oracle_mxfp4_encode(_ptr(master), _ptr(prev_codes), _ptr(prev_scales), n,
+                                _ptr(idx), _ptr(val), _ptr(sidx), _ptr(sval), _ptr(counts))
+    k, ks = int(counts[0]), int(counts[1])
+    return idx[:k].copy(), val[:k].copy(), sidx[:ks].copy(), sval[:ks].copy()
+
+
+def mxfp4_apply(codes: np.ndarray, scales: np.ndarray, patch) -> None:
+    """Apply both segments of an MXFP4 patch (byte idx, val, sidx, sval) in place."""
     idx, val, sidx, sval = patch
     apply_u8(codes, idx, val)
     apply_u8(scales, sidx, sval)
