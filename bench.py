@@ -428,7 +428,8 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
         wl.xplan.close()
 
     if not args.no_mx:
-        out["mxfp8"] = run_mx(args, cfg, specs, wl, dev, rank, peak)
+        out["mxfp8"] = run_mx(args, cfg, specs, wl, dev, rank, peak, pulse.MX_E4M3)
+        out["mxfp4"] = run_mx(args, cfg, specs, wl, dev, rank, peak, pulse.MX_E2M1)
 
     if not args.no_e2e:
         out["e2e"] = e2e(args, wl, counts_np, dist_on)
@@ -452,13 +453,15 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
     return out
 
 
-def run_mx(args, cfg, specs, wl, dev, rank, peak):
-    """The MXFP8 serving view of the same model and step: whole-model
-    pulse_mx_encode_multi + pulse_mx_apply_multi_device, timed like the BF16
-    step (previous view and receiver restored untimed before each step). The
-    BF16 patch buffers are reused for the code segments."""
+def run_mx(args, cfg, specs, wl, dev, rank, peak, fmt=0):
+    """An MX serving view (fmt 0: MXFP8, 1: MXFP4) of the same model and step:
+    whole-model pulse_mx_encode_multi + pulse_mx_apply_multi_device, timed
+    like the BF16 step (previous view and receiver restored untimed before
+    each step). The BF16 patch buffers are reused for the code segments."""
     import rl_post_trainer_gb300 as pulse
     n = wl.n
+    name = "MXFP8" if fmt == pulse.MX_E4M3 else "MXFP4"
+    epb = 1 if fmt == pulse.MX_E4M3 else 2   # elements per code byte
     stream = torch.cuda.current_stream(dev)
     # the view before the step: the same generator sequence as the workload
     # (per tensor: w0, then z), quantizing each w0 as it is drawn
@@ -468,7 +471,7 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak):
     for spec in specs:
         w0 = tmp[:spec.numel]
         workloads.torch_init_(w0, spec, gen)
-        c, sc = pulse.mx_quantize(w0)
+        c, sc = pulse.mx_quantize(w0, fmt=fmt)
         c0.append(c)
         s0.append(sc)
         workloads.torch_update_(w0, cfg["eta"], gen)   # advances the generator past z
@@ -484,7 +487,7 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak):
                                             prev_scales=prev_s[i], codes=codes[i], scales=scales[i],
                                             idx=wl.idx[i], val=wl.val[i].view(torch.uint8),
                                             sidx=sidx[i], sval=sval[i])
-                         for i, s in enumerate(specs)])
+                         for i, s in enumerate(specs)], fmt=fmt)
     counts = torch.zeros(2 * len(specs), dtype=torch.int64, device=dev)
 
     def restore():
@@ -516,10 +519,10 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak):
         te.append(ev[0].elapsed_time(ev[1]) * 1e-3)
         ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
     if plan.get_error() != 0:
-        raise RuntimeError("device error in the MXFP8 steps")
+        raise RuntimeError(f"device error in the {name} steps")
     for t in range(len(specs)):
         if not (torch.equal(codes[t], prev_c[t]) and torch.equal(scales[t], prev_s[t])):
-            raise RuntimeError(f"MXFP8 receiver differs from the trainer view (tensor {t})")
+            raise RuntimeError(f"{name} receiver differs from the trainer view (tensor {t})")
     cn = counts.cpu().numpy()
     k, ks = int(cn[0::2].sum()), int(cn[1::2].sum())
     # distinct 32-byte sectors holding a changed code / scale (1-byte arrays,
@@ -536,22 +539,26 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak):
                     sc_codes += val
     nblocks = float(sum(nb))
     e_s, a_s = float(np.mean(te)), float(np.mean(ta))
-    enc_alg = 5.0 * n + nblocks + 6.0 * k + 6.0 * ks
-    enc_sec = 5.0 * n + nblocks + 32.0 * (sc_codes + sc_scales) + 5.0 * k + 5.0 * ks
+    view = (4.0 + 1.0 / epb) * n + nblocks  # master read + previous view read
+    enc_alg = view + 6.0 * k + 6.0 * ks
+    enc_sec = view + 32.0 * (sc_codes + sc_scales) + 5.0 * k + 5.0 * ks
     app_rmw = 5.0 * (k + ks) + 64.0 * (sc_codes + sc_scales)
     plan.close()
+    model = "5n" if epb == 1 else "4.5n"
     return {
-        "format": "MXFP8 (E4M3 codes, E8M0 scale per 32 elements)",
+        "format": ("MXFP8 (E4M3 codes, E8M0 scale per 32 elements)" if epb == 1 else
+                   "MXFP4 (E2M1 codes two per byte, E8M0 scale per 32 elements; code entries "
+                   "are bytes)"),
         "encode_ms": 1e3 * e_s, "apply_ms": 1e3 * a_s,
         "params_per_s": n / (e_s + a_s),
-        "code_density": k / n, "scale_density": ks / nblocks,
+        "code_density": k / (n / epb), "scale_density": ks / nblocks,
         "code_entries": k, "scale_entries": ks,
         "encode_gbs_algorithmic": enc_alg / e_s / 1e9,
         "encode_gbs_sector": enc_sec / e_s / 1e9,
         "encode_frac_measured_peak": enc_alg / e_s / 1e9 / peak,
         "encode_frac_sector_measured_peak": enc_sec / e_s / 1e9 / peak,
         "apply_gbs_sector_rmw": app_rmw / a_s / 1e9,
-        "bytes_model": "encode 5n + n/32 + 6k + 6ks (sector: 5n + n/32 + 32S + 5k + 5ks)",
+        "bytes_model": f"encode {model} + n/32 + 6k + 6ks (sector: {model} + n/32 + 32S + 5k + 5ks)",
         "gpu_launches": 2 * args.steps,
     }
 
@@ -925,7 +932,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-xor", action="store_true")
-    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8-view leg")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8- and MXFP4-view legs")
     ap.add_argument("--no-compose", action="store_true", help="skip the patch-chain leg")
     ap.add_argument("--no-loco", action="store_true", help="skip the PULSELoCo leg")
     ap.add_argument("--no-pack", action="store_true", help="skip the index-packing leg")

@@ -555,6 +555,52 @@ int pulse_mx_apply_multi(pulse_mx_plan *plan, const uint64_t *counts_host, cudaS
 int pulse_mx_apply_multi_device(pulse_mx_plan *plan, const uint64_t *counts_dev, cudaStream_t stream);
 int pulse_mx_plan_get_error(pulse_mx_plan *plan);
 
+/* ------------------------------------------------------------------------
+ * MXFP4 serving view. [TALK] 13:06-14:40 names MXFP4 and NVFP4 serving: each
+ * weight is quantized against a shared group scale, and a scale change moves
+ * the whole group; [KR] same section; [PULSE] "Potenziale Futuro": MXFP4
+ * views should be sparser still. [MX] fixes the format:
+ *
+ *  - blocks of 32 consecutive elements share one E8M0 scale byte s exactly
+ *    as in the MXFP8 view but with the E2M1 maximum exponent:
+ *    s = floor(log2(max |v| over the block)) - 2 + 127, limited to
+ *    [0, 254]; an all-zero block gets s = 0; a block holding a NaN or an
+ *    infinity gets s = 0xFF and every code 0;
+ *  - each element's code is the E2M1 encoding (sign, 2 exponent bits with
+ *    bias 1, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) of
+ *    v / 2^(s - 127), rounded to nearest even, magnitudes past 6 clamped to
+ *    6, sign kept (a negative value rounding to zero gives code 0x8);
+ *  - codes are stored two per byte: element 2j in the low nibble of byte j,
+ *    element 2j + 1 in the high nibble; a tensor of odd length has a zero
+ *    high nibble in its last byte.
+ *
+ * A view is codes (ceil(n / 2) bytes) and scales (ceil(n / 32) bytes). Its
+ * patch lists changed code BYTES (byte index, new byte) and changed scales
+ * (block index, new byte), each ascending; applying it is the byte apply of
+ * the MXFP8 view. The _fmt forms below take the format and otherwise behave
+ * as the MXFP8 calls above, with "codes" and "code segment" counted in bytes
+ * (ceil(n / 2) for E2M1). The MXFP8 calls equal the _fmt calls with
+ * PULSE_MX_E4M3.
+ * ---------------------------------------------------------------------- */
+#define PULSE_MX_E4M3 0  /* MXFP8: one E4M3 code per byte */
+#define PULSE_MX_E2M1 1  /* MXFP4: two E2M1 codes per byte */
+
+/* Errors as the MXFP8 calls, plus PULSE_ERR_INVALID for an unknown format. */
+int pulse_mx_quantize_fmt(int format, const float *master_f32, uint64_t n, uint8_t *codes_out,
+                          uint8_t *scales_out, cudaStream_t stream);
+int pulse_mx_encode_fmt(int format, const float *master_f32, uint8_t *prev_codes,
+                        uint8_t *prev_scales, uint64_t n, uint32_t *idx_out, uint8_t *val_out,
+                        uint32_t *sidx_out, uint8_t *sval_out, uint64_t *counts_out,
+                        cudaStream_t stream);
+int pulse_mx_apply_fmt(int format, uint8_t *codes, uint8_t *scales, uint64_t n,
+                       const uint32_t *idx, const uint8_t *val, uint64_t count,
+                       const uint32_t *sidx, const uint8_t *sval, uint64_t scount,
+                       cudaStream_t stream);
+/* A plan of one format: prev_codes, codes, idx and val of each tensor hold
+ * code bytes (ceil(n / 2) for E2M1). */
+int pulse_mx_plan_create_fmt(const pulse_mx_tensor *tensors, int ntensors, int format,
+                             pulse_mx_plan **plan_out);
+
 /*
  * pulse_encode_noalloc -- pulse_encode for callers that must not allocate
  * device memory. The pages describe no counterpart; this entry point exists

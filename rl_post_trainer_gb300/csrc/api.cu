@@ -215,8 +215,9 @@ MxTensorDesc make_mx_desc(const pulse_mx_tensor& t, uint64_t tile_begin) {
   return d;
 }
 
-// Clear the status words of `tiles` tiles, then launch the MXFP8 encode.
-int launch_encode_mx_ws(MxLaunch& a, Workspace& ws, bool multi, int device, cudaStream_t stream) {
+// Clear the status words of `tiles` tiles, then launch the MX encode.
+int launch_encode_mx_ws(MxLaunch& a, int format, Workspace& ws, bool multi, int device,
+                        cudaStream_t stream) {
   int st = workspace_reserve(ws, a.total_tiles, stream);
   if (st != PULSE_OK) return st;
   if (cudaMemsetAsync(ws.status, 0, a.total_tiles * sizeof(uint64_t), stream) != cudaSuccess)
@@ -224,9 +225,9 @@ int launch_encode_mx_ws(MxLaunch& a, Workspace& ws, bool multi, int device, cuda
   a.status = ws.status;
   a.counters = ws.counters;
   a.epoch = 0;
-  const uint64_t cap = uint64_t(encode_mx_grid_size(device));
+  const uint64_t cap = uint64_t(encode_mx_grid_size(device, format));
   const int grid = int(a.total_tiles < cap ? a.total_tiles : cap);
-  return cuda_status(launch_encode_mx(a, multi, grid, stream));
+  return cuda_status(launch_encode_mx(a, format, multi, grid, stream));
 }
 
 // ---- compose: per-(device, stream) workspace with the merge-path splits and
@@ -365,6 +366,7 @@ struct pulse_loco_plan {
 
 struct pulse_mx_plan {
   int device = 0;
+  int format = PULSE_MX_E4M3;
   int ntensors = 0;
   uint64_t total_tiles = 0;
   bool can_encode = false, can_apply = false;
@@ -1097,17 +1099,31 @@ int pulse_compose_multi(const pulse_compose_segment* segs, int nsegs, int value_
 
 // ------------------------------------------------------------ MXFP8 view
 
-int pulse_mx_quantize(const float* master_f32, uint64_t n, uint8_t* codes_out, uint8_t* scales_out,
-                      cudaStream_t stream) {
+namespace {
+bool mx_format_ok(int format) { return format == PULSE_MX_E4M3 || format == PULSE_MX_E2M1; }
+// code bytes of an n-element view
+uint64_t mx_code_bytes(int format, uint64_t n) { return format == PULSE_MX_E2M1 ? div_up(n, 2) : n; }
+}  // namespace
+
+int pulse_mx_quantize_fmt(int format, const float* master_f32, uint64_t n, uint8_t* codes_out,
+                          uint8_t* scales_out, cudaStream_t stream) {
+  if (!mx_format_ok(format)) return PULSE_ERR_INVALID;
   if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
   if (n == 0) return PULSE_OK;
   if (master_f32 == nullptr || codes_out == nullptr || scales_out == nullptr) return PULSE_ERR_INVALID;
-  return cuda_status(launch_mx_quantize(master_f32, n, codes_out, scales_out, stream));
+  return cuda_status(launch_mx_quantize(format, master_f32, n, codes_out, scales_out, stream));
 }
 
-int pulse_mx_encode(const float* master_f32, uint8_t* prev_codes, uint8_t* prev_scales, uint64_t n,
-                    uint32_t* idx_out, uint8_t* val_out, uint32_t* sidx_out, uint8_t* sval_out,
-                    uint64_t* counts_out, cudaStream_t stream) {
+int pulse_mx_quantize(const float* master_f32, uint64_t n, uint8_t* codes_out, uint8_t* scales_out,
+                      cudaStream_t stream) {
+  return pulse_mx_quantize_fmt(PULSE_MX_E4M3, master_f32, n, codes_out, scales_out, stream);
+}
+
+int pulse_mx_encode_fmt(int format, const float* master_f32, uint8_t* prev_codes,
+                        uint8_t* prev_scales, uint64_t n, uint32_t* idx_out, uint8_t* val_out,
+                        uint32_t* sidx_out, uint8_t* sval_out, uint64_t* counts_out,
+                        cudaStream_t stream) {
+  if (!mx_format_ok(format)) return PULSE_ERR_INVALID;
   if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
   if (counts_out == nullptr) return PULSE_ERR_INVALID;
   if (n > 0 && (master_f32 == nullptr || prev_codes == nullptr || prev_scales == nullptr ||
@@ -1135,12 +1151,21 @@ int pulse_mx_encode(const float* master_f32, uint8_t* prev_codes, uint8_t* prev_
   std::lock_guard<std::mutex> lock(g_ws_mu);
   Workspace* ws = stream_mx_workspace(device, stream);
   if (ws == nullptr) return PULSE_ERR_NOMEM;
-  return launch_encode_mx_ws(a, *ws, false, device, stream);
+  return launch_encode_mx_ws(a, format, *ws, false, device, stream);
 }
 
-int pulse_mx_apply(uint8_t* codes, uint8_t* scales, uint64_t n, const uint32_t* idx,
-                   const uint8_t* val, uint64_t count, const uint32_t* sidx, const uint8_t* sval,
-                   uint64_t scount, cudaStream_t stream) {
+int pulse_mx_encode(const float* master_f32, uint8_t* prev_codes, uint8_t* prev_scales, uint64_t n,
+                    uint32_t* idx_out, uint8_t* val_out, uint32_t* sidx_out, uint8_t* sval_out,
+                    uint64_t* counts_out, cudaStream_t stream) {
+  return pulse_mx_encode_fmt(PULSE_MX_E4M3, master_f32, prev_codes, prev_scales, n, idx_out, val_out,
+                             sidx_out, sval_out, counts_out, stream);
+}
+
+int pulse_mx_apply_fmt(int format, uint8_t* codes, uint8_t* scales, uint64_t n,
+                       const uint32_t* idx, const uint8_t* val, uint64_t count,
+                       const uint32_t* sidx, const uint8_t* sval, uint64_t scount,
+                       cudaStream_t stream) {
+  if (!mx_format_ok(format)) return PULSE_ERR_INVALID;
   if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
   if (count == 0 && scount == 0) return PULSE_OK;
   if (count > 0 && (codes == nullptr || idx == nullptr || val == nullptr)) return PULSE_ERR_INVALID;
@@ -1156,15 +1181,25 @@ int pulse_mx_apply(uint8_t* codes, uint8_t* scales, uint64_t n, const uint32_t* 
     if (st != PULSE_OK) return st;
     err = ws->counters + 2;
   }
-  if (launch_apply_u8(codes, n, true, idx, val, count, err, stream) != cudaSuccess)
+  if (launch_apply_u8(codes, mx_code_bytes(format, n), true, idx, val, count, err, stream) !=
+      cudaSuccess)
     return PULSE_ERR_CUDA;
   return cuda_status(
       launch_apply_u8(scales, div_up(n, kMxBlock), true, sidx, sval, scount, err, stream));
 }
 
-int pulse_mx_plan_create(const pulse_mx_tensor* tensors, int ntensors, pulse_mx_plan** plan_out) {
+int pulse_mx_apply(uint8_t* codes, uint8_t* scales, uint64_t n, const uint32_t* idx,
+                   const uint8_t* val, uint64_t count, const uint32_t* sidx, const uint8_t* sval,
+                   uint64_t scount, cudaStream_t stream) {
+  return pulse_mx_apply_fmt(PULSE_MX_E4M3, codes, scales, n, idx, val, count, sidx, sval, scount,
+                            stream);
+}
+
+int pulse_mx_plan_create_fmt(const pulse_mx_tensor* tensors, int ntensors, int format,
+                             pulse_mx_plan** plan_out) {
   if (plan_out == nullptr) return PULSE_ERR_INVALID;
   *plan_out = nullptr;
+  if (!mx_format_ok(format)) return PULSE_ERR_INVALID;
   if (tensors == nullptr || ntensors < 1 || ntensors > kMaxTensorsPerApplyLaunch / 2)
     return PULSE_ERR_INVALID;
   pulse_mx_plan* p = new (std::nothrow) pulse_mx_plan();
@@ -1174,6 +1209,7 @@ int pulse_mx_plan_create(const pulse_mx_tensor* tensors, int ntensors, pulse_mx_
     return PULSE_ERR_CUDA;
   }
   p->ntensors = ntensors;
+  p->format = format;
   p->can_encode = p->can_apply = true;
   std::vector<uint64_t> tb(size_t(ntensors) + 1, 0);
   std::vector<ByteSegment> segs(2 * size_t(ntensors));
@@ -1188,7 +1224,7 @@ int pulse_mx_plan_create(const pulse_mx_tensor* tensors, int ntensors, pulse_mx_
     tb[size_t(i)] = tiles;
     p->host_desc.push_back(make_mx_desc(t, tiles));
     tiles += div_up(t.n, kEncTile);
-    segs[2 * size_t(i)] = ByteSegment{t.codes, t.idx, t.val, t.n};
+    segs[2 * size_t(i)] = ByteSegment{t.codes, t.idx, t.val, mx_code_bytes(format, t.n)};
     segs[2 * size_t(i) + 1] = ByteSegment{t.scales, t.sidx, t.sval, div_up(t.n, kMxBlock)};
     if (t.n > 0) {
       p->can_encode = p->can_encode && t.master && t.prev_codes && t.prev_scales && t.idx &&
@@ -1229,6 +1265,10 @@ int pulse_mx_plan_create(const pulse_mx_tensor* tensors, int ntensors, pulse_mx_
   return PULSE_OK;
 }
 
+int pulse_mx_plan_create(const pulse_mx_tensor* tensors, int ntensors, pulse_mx_plan** plan_out) {
+  return pulse_mx_plan_create_fmt(tensors, ntensors, PULSE_MX_E4M3, plan_out);
+}
+
 int pulse_mx_plan_destroy(pulse_mx_plan* plan) {
   if (plan == nullptr) return PULSE_OK;
   const cudaError_t e = cudaDeviceSynchronize();
@@ -1256,7 +1296,7 @@ int pulse_mx_encode_multi(pulse_mx_plan* plan, uint64_t* counts_out, cudaStream_
   a.counts_out = counts_out;
   a.first_ticket = 0;
   a.wait_limit_ns = kDefaultWaitNs;
-  return launch_encode_mx_ws(a, plan->ws, true, plan->device, stream);
+  return launch_encode_mx_ws(a, plan->format, plan->ws, true, plan->device, stream);
 }
 
 int pulse_mx_apply_multi_device(pulse_mx_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {

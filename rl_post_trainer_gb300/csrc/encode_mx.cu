@@ -37,11 +37,33 @@ using namespace enc;
 
 constexpr int kTileBlocks = kEncTile / kMxBlock;                   // 128
 constexpr uint32_t kStageMasterBytes = kEncTile * 4;               // 16 KB
-constexpr uint32_t kStageCodeBytes = kEncTile;                     // 4 KB
 constexpr uint32_t kStageScaleBytes = kTileBlocks;                 // 128 B
-constexpr uint32_t kStageBytes = kStageMasterBytes + kStageCodeBytes + kStageScaleBytes;
-static_assert(kStageBytes % 128 == 0, "stages stay 128-byte aligned");
-constexpr size_t kDynSmem = size_t(kEncStages) * kStageBytes + size_t(kEncRing) * 4 + 128;
+
+// Element formats: F = kFmtE4M3 (MXFP8, one code byte per element) or
+// kFmtE2M1 (MXFP4, two codes per byte, element 2j in the low nibble of byte
+// j). kEmax: exponent of the format's largest normal (448 = 1.75 * 2^8,
+// 6 = 1.5 * 2^2).
+template <int F>
+struct Fmt;
+template <>
+struct Fmt<kFmtE4M3> {
+  static constexpr uint32_t kEmax = 8;
+  static constexpr uint32_t kElemsPerByte = 1;
+};
+template <>
+struct Fmt<kFmtE2M1> {
+  static constexpr uint32_t kEmax = 2;
+  static constexpr uint32_t kElemsPerByte = 2;
+};
+// Stage layout of a tile for format F: master, previous code bytes,
+// previous scales.
+template <int F>
+struct Stage {
+  static constexpr uint32_t kCodeBytes = kEncTile / Fmt<F>::kElemsPerByte;
+  static constexpr uint32_t kBytes = kStageMasterBytes + kCodeBytes + kStageScaleBytes;
+  static constexpr size_t kDynSmem = size_t(kEncStages) * kBytes + size_t(kEncRing) * 4 + 128;
+  static_assert(kBytes % 128 == 0, "stages stay 128-byte aligned");
+};
 
 // ---------------------------------------------------------- MXFP8 arithmetic
 
@@ -62,6 +84,26 @@ __device__ __forceinline__ uint32_t mx_codes4(const float4& v, uint32_t scale) {
   const float f = __uint_as_float(0x7F000000u - (scale << 23));  // (254 - scale) << 23
   return cvt_e4m3x2(__fmul_rn(v.y, f), __fmul_rn(v.x, f)) |
          (cvt_e4m3x2(__fmul_rn(v.w, f), __fmul_rn(v.z, f)) << 16);
+}
+
+// Saturating round-to-nearest-even FP32 -> E2M1 of 8 values under scale byte
+// `scale`: byte j holds element 2j in its low nibble and 2j + 1 in its high
+// nibble. Same scaling argument as mx_codes4 (scale <= 252 here).
+__device__ __forceinline__ uint32_t fp4_codes8(const float4& a, const float4& b, uint32_t scale) {
+  if (scale == 0xFFu) return 0u;
+  const float f = __uint_as_float(0x7F000000u - (scale << 23));
+  uint32_t r;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+      : "=r"(r)
+      : "f"(__fmul_rn(a.x, f)), "f"(__fmul_rn(a.y, f)), "f"(__fmul_rn(a.z, f)),
+        "f"(__fmul_rn(a.w, f)), "f"(__fmul_rn(b.x, f)), "f"(__fmul_rn(b.y, f)),
+        "f"(__fmul_rn(b.z, f)), "f"(__fmul_rn(b.w, f)));
+  return r;
 }
 
 // -------------------------------------------------------------- shared state
@@ -86,13 +128,15 @@ struct StageMeta {
 struct ParkedMeta {
   uint32_t tile;
   uint32_t tensor;
-  uint32_t agg_c;  // changed codes in the tile
+  uint32_t agg_c;  // changed code bytes in the tile
   uint32_t agg_s;  // changed scales in the tile
   uint32_t last;   // 1: last tile of its tensor; 2: no more tiles for this look-back warp
   uint32_t ring_start;
   uint64_t first;
   uint64_t n;
   uint64_t base;
+  uint64_t code_base;  // code-byte index of the tile's first element
+  uint64_t code_cap;   // code bytes of the tensor (the code segment's room)
   uint32_t* idx;
   uint8_t* val;
   uint32_t* sidx;
@@ -114,8 +158,9 @@ struct __align__(16) MxShared {
 static_assert(kEncLookbackWarps == 1, "parked tiles are freed in order by one look-back warp");
 
 // ------------------------------------------------------------ producer warp
-template <bool MULTI>
+template <int F, bool MULTI>
 __device__ __forceinline__ void producer_loop(const MxLaunch& a, MxShared& sh, uint8_t* stages) {
+  constexpr uint32_t kStageBytes = Stage<F>::kBytes, kStageCodeBytes = Stage<F>::kCodeBytes;
   const uint64_t pol_stream = l2_policy_evict_first();
   uint32_t fills_done = 0;
   uint32_t ticket = atomicAdd(a.counters + 0, 1u) + a.first_ticket;
@@ -165,7 +210,8 @@ __device__ __forceinline__ void producer_loop(const MxLaunch& a, MxShared& sh, u
       uint8_t* st = stages + size_t(s) * kStageBytes;
       mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
       bulk_g2s(st, d.master + base, kStageMasterBytes, &sh.full[s], pol_stream);
-      bulk_g2s_plain(st + kStageMasterBytes, d.prev_codes + base, kStageCodeBytes, &sh.full[s]);
+      bulk_g2s_plain(st + kStageMasterBytes, d.prev_codes + base / Fmt<F>::kElemsPerByte,
+                     kStageCodeBytes, &sh.full[s]);
       bulk_g2s_plain(st + kStageMasterBytes + kStageCodeBytes, d.prev_scales + base / kMxBlock,
                      kStageScaleBytes, &sh.full[s]);
     } else {
@@ -194,17 +240,17 @@ __device__ __forceinline__ void producer_loop(const MxLaunch& a, MxShared& sh, u
 __device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix_c, uint32_t prefix_s,
                                          const uint32_t* ring, const uint16_t* sring, int lane) {
   const uint32_t agg = pm.agg_c;
-  const uint32_t base = uint32_t(pm.base);
+  const uint32_t base = uint32_t(pm.code_base);
   const bool vec = (reinterpret_cast<uintptr_t>(pm.idx) % 16u == 0) &&
                    (reinterpret_cast<uintptr_t>(pm.val) % 4u == 0) &&
-                   uint64_t(prefix_c) + agg <= pm.n;
+                   uint64_t(prefix_c) + agg <= pm.code_cap;
   uint32_t head = vec ? ((4u - (prefix_c & 3u)) & 3u) : agg;
   if (head > agg) head = agg;
   const uint32_t body = vec ? ((agg - head) & ~3u) : 0u;
   for (uint32_t k = uint32_t(lane); k < head; k += 32) {
     const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
     const uint64_t pos = uint64_t(prefix_c) + k;
-    if (pos < pm.n) {
+    if (pos < pm.code_cap) {
       pm.idx[pos] = base + (ent & 0xFFFFu);
       pm.val[pos] = uint8_t(ent >> 16);
     }
@@ -224,7 +270,7 @@ __device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix_c
   for (uint32_t k = head + body + uint32_t(lane); k < agg; k += 32) {
     const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
     const uint64_t pos = uint64_t(prefix_c) + k;
-    if (pos < pm.n) {
+    if (pos < pm.code_cap) {
       pm.idx[pos] = base + (ent & 0xFFFFu);
       pm.val[pos] = uint8_t(ent >> 16);
     }
@@ -322,16 +368,24 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 }
 
 // E8M0 scale byte of the block this thread's 8 elements belong to (lanes
-// 4b .. 4b+3 hold block b). The block maximum is a non-negative float or NaN
-// (max.NaN propagates NaN), so its bit pattern's exponent field E is 255
-// exactly for a non-finite block. All 32 lanes must call.
+// 4b .. 4b+3 hold block b), for an element format whose largest normal has
+// exponent EMAX. The block maximum is a non-negative float or NaN (max.NaN
+// propagates NaN), so its bit pattern's exponent field E is 255 exactly for
+// a non-finite block. All 32 lanes must call.
+template <uint32_t EMAX>
 __device__ __forceinline__ uint32_t block_scale8(const float4& a, const float4& b) {
   float m = max_nan(max_nan(abs_max_nan(a.x, a.y), abs_max_nan(a.z, a.w)),
                     max_nan(abs_max_nan(b.x, b.y), abs_max_nan(b.z, b.w)));
   m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
   m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
   const uint32_t e = __float_as_uint(m) >> 23;  // sign is clear
-  return e == 255u ? 0xFFu : (e > 8u ? e - 8u : 0u);
+  return e == 255u ? 0xFFu : (e > EMAX ? e - EMAX : 0u);
+}
+
+// Four change flags in byte order (bit b = byte b) from the 0x80 bytes of
+// nonzero_bytes: the same multiply as gather_flags8 with one word.
+__device__ __forceinline__ uint32_t gather_flags4(uint32_t z) {
+  return (((z >> 7) * 0x00204081u) >> 21) & 0xFu;
 }
 
 // One 0x80 per byte of x that is non-zero (x = new ^ old codes).
@@ -349,9 +403,13 @@ __device__ __forceinline__ uint32_t gather_flags8(uint32_t z0, uint32_t z1) {
   return ((((z0 >> 7) | (z1 >> 3)) * 0x00204081u) >> 21) & 0xFFu;
 }
 
-template <bool MULTI>
+template <int F, bool MULTI>
 __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, uint8_t* stages,
                                              uint32_t* ring, int tid, int lane, int warp) {
+  constexpr uint32_t kStageBytes = Stage<F>::kBytes, kStageCodeBytes = Stage<F>::kCodeBytes;
+  constexpr bool kFp4 = F == kFmtE2M1;
+  // code bytes per 8-element group, and change flags per round
+  constexpr uint32_t kGroupBytes = kMxPerThread / Fmt<F>::kElemsPerByte;
   uint32_t posted = 0, ring_head = 0;
   bool failed = false;
   const bool leader = (lane & (kLanesPerBlock - 1)) == 0;  // lane that owns its block's scale
@@ -366,9 +424,9 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
     const uint8_t* stage = stages + size_t(s) * kStageBytes;
 
     // ---- quantize + compare: 8 consecutive elements per thread per round
-    uint32_t nc[kMxRounds][2];  // new codes, element 0 in the low byte of word 0
+    uint32_t nc[kMxRounds][2];  // new code bytes, byte 0 in the low byte of word 0 (FP4: word 0 only)
     uint32_t ns = 0;            // byte j: new scale of this thread's block in round j
-    uint32_t flags = 0;         // bit 8j + e: element e of round j changed
+    uint32_t flags = 0;         // bit 8j + e: code byte e of round j changed
     uint32_t sflags = 0;        // bit j: the block of round j changed its scale (leaders only)
 #pragma unroll
     for (int j = 0; j < kMxRounds; ++j) {
@@ -376,44 +434,64 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
       const uint32_t li = slot * kMxPerThread;
       const uint32_t lb = slot / kLanesPerBlock;              // block within the tile
       float4 v0, v1;
-      uint2 pc;
+      uint2 pc = make_uint2(0u, 0u);
       uint32_t ps = 0;
       if (bulk) {
         const float4* sm = reinterpret_cast<const float4*>(stage);
         v0 = sm[2 * slot];
         v1 = sm[2 * slot + 1];
-        pc = reinterpret_cast<const uint2*>(stage + kStageMasterBytes)[slot];
+        if constexpr (kFp4)
+          pc.x = reinterpret_cast<const uint32_t*>(stage + kStageMasterBytes)[slot];
+        else
+          pc = reinterpret_cast<const uint2*>(stage + kStageMasterBytes)[slot];
         if (leader) ps = stage[kStageMasterBytes + kStageCodeBytes + lb];
       } else {
         // tail or unaligned tile: elements past the end read as +0 (no effect
-        // on the block maximum) and are never reported
+        // on the block maximum, code 0) and bytes past the end are never
+        // reported
         float mm[kMxPerThread];
-        uint32_t pp[2] = {0u, 0u};
 #pragma unroll
-        for (int e = 0; e < kMxPerThread; ++e) {
-          const bool valid = li + e < len;
-          mm[e] = valid ? m.master[base + li + e] : 0.0f;
-          pp[e >> 2] |= (valid ? uint32_t(m.prev_codes[base + li + e]) : 0u) << (8 * (e & 3));
+        for (int e = 0; e < kMxPerThread; ++e) mm[e] = li + e < len ? m.master[base + li + e] : 0.0f;
+        uint32_t pp[2] = {0u, 0u};
+        const uint64_t cb = (base + li) / Fmt<F>::kElemsPerByte;  // first code byte
+#pragma unroll
+        for (int e = 0; e < int(kGroupBytes); ++e) {
+          const bool valid = li + uint32_t(e) * Fmt<F>::kElemsPerByte < len;
+          pp[e >> 2] |= (valid ? uint32_t(m.prev_codes[cb + e]) : 0u) << (8 * (e & 3));
         }
         v0 = make_float4(mm[0], mm[1], mm[2], mm[3]);
         v1 = make_float4(mm[4], mm[5], mm[6], mm[7]);
         pc = make_uint2(pp[0], pp[1]);
         if (leader && lb * kMxBlock < len) ps = m.prev_scales[(base / kMxBlock) + lb];
       }
-      const uint32_t sb = block_scale8(v0, v1);
-      nc[j][0] = mx_codes4(v0, sb);
-      nc[j][1] = mx_codes4(v1, sb);
-      ns |= sb << (8 * j);
-      uint32_t z0 = nonzero_bytes(nc[j][0] ^ pc.x), z1 = nonzero_bytes(nc[j][1] ^ pc.y);
-      if (!bulk) {
-        // keep only elements inside the tile
-        const uint32_t nvalid = li >= len ? 0u : (len - li >= 8u ? 8u : len - li);
-        const uint64_t keep =  // one 0xFF byte per valid element
-            nvalid >= 8u ? ~uint64_t(0) : (uint64_t(1) << (8 * nvalid)) - 1u;
-        z0 &= uint32_t(keep);
-        z1 &= uint32_t(keep >> 32);
+      const uint32_t sb = block_scale8<Fmt<F>::kEmax>(v0, v1);
+      uint32_t f4;
+      if constexpr (kFp4) {
+        nc[j][0] = fp4_codes8(v0, v1, sb);
+        nc[j][1] = 0u;
+        uint32_t z = nonzero_bytes(nc[j][0] ^ pc.x);
+        if (!bulk) {
+          // keep only the code bytes inside the tile
+          const uint32_t nb = li >= len ? 0u : (len - li >= 8u ? 4u : (len - li + 1u) / 2u);
+          z &= nb >= 4u ? 0xFFFFFFFFu : (1u << (8 * nb)) - 1u;
+        }
+        f4 = gather_flags4(z);
+      } else {
+        nc[j][0] = mx_codes4(v0, sb);
+        nc[j][1] = mx_codes4(v1, sb);
+        uint32_t z0 = nonzero_bytes(nc[j][0] ^ pc.x), z1 = nonzero_bytes(nc[j][1] ^ pc.y);
+        if (!bulk) {
+          // keep only elements inside the tile
+          const uint32_t nvalid = li >= len ? 0u : (len - li >= 8u ? 8u : len - li);
+          const uint64_t keep =  // one 0xFF byte per valid element
+              nvalid >= 8u ? ~uint64_t(0) : (uint64_t(1) << (8 * nvalid)) - 1u;
+          z0 &= uint32_t(keep);
+          z1 &= uint32_t(keep >> 32);
+        }
+        f4 = gather_flags8(z0, z1);
       }
-      flags |= gather_flags8(z0, z1) << (8 * j);
+      ns |= sb << (8 * j);
+      flags |= f4 << (8 * j);
       if (leader && lb * kMxBlock < len && sb != ps) sflags |= 1u << j;
     }
     __syncwarp();
@@ -425,13 +503,16 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
       const uint32_t f = (flags >> (8 * j)) & 0xFFu;
       const uint32_t li = uint32_t(j * kEncThreads + tid) * kMxPerThread;
       if (f != 0u) {
+        const uint64_t cb = (base + li) / Fmt<F>::kElemsPerByte;  // first code byte
         if (bulk) {
-          *reinterpret_cast<uint2*>(m.prev_codes + base + li) = make_uint2(nc[j][0], nc[j][1]);
+          if constexpr (kFp4)
+            *reinterpret_cast<uint32_t*>(m.prev_codes + cb) = nc[j][0];
+          else
+            *reinterpret_cast<uint2*>(m.prev_codes + cb) = make_uint2(nc[j][0], nc[j][1]);
         } else {
 #pragma unroll
-          for (int e = 0; e < kMxPerThread; ++e)
-            if ((f >> e) & 1u)
-              m.prev_codes[base + li + e] = uint8_t(nc[j][e >> 2] >> (8 * (e & 3)));
+          for (int e = 0; e < int(kGroupBytes); ++e)
+            if ((f >> e) & 1u) m.prev_codes[cb + e] = uint8_t(nc[j][e >> 2] >> (8 * (e & 3)));
         }
       }
       if ((sflags >> j) & 1u) m.prev_scales[base / kMxBlock + li / kMxBlock] = uint8_t(ns >> (8 * j));
@@ -514,7 +595,8 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
         const uint32_t e = uint32_t(__ffs(f)) - 1u;
         f &= f - 1u;
         const uint32_t word = (e & 4u) ? nc[j][1] : nc[j][0];
-        ring[r & kRingMask] = (li + e) | (((word >> (8 * (e & 3))) & 0xFFu) << 16);
+        ring[r & kRingMask] =
+            (li / Fmt<F>::kElemsPerByte + e) | (((word >> (8 * (e & 3))) & 0xFFu) << 16);
         ++r;
       } while (f != 0u);
     }
@@ -536,6 +618,8 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
       pm.first = m.first;
       pm.n = m.n;
       pm.base = base;
+      pm.code_base = base / Fmt<F>::kElemsPerByte;
+      pm.code_cap = (m.n + Fmt<F>::kElemsPerByte - 1) / Fmt<F>::kElemsPerByte;
       pm.idx = m.idx;
       pm.val = m.val;
       pm.sidx = m.sidx;
@@ -563,9 +647,10 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
   }
 }
 
-template <bool MULTI>
+template <int F, bool MULTI>
 __global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
     encode_mx_kernel(const __grid_constant__ MxLaunch a) {
+  constexpr uint32_t kStageBytes = Stage<F>::kBytes;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ MxShared sh;
   const int tid = threadIdx.x;
@@ -606,22 +691,22 @@ __global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
   __syncthreads();
 
   if (warp < kWarps) {
-    compute_loop<MULTI>(a, sh, stages, ring, tid, lane, warp);
+    compute_loop<F, MULTI>(a, sh, stages, ring, tid, lane, warp);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_loop<MULTI>(a, sh, stages);
+    if (lane == 0) producer_loop<F, MULTI>(a, sh, stages);
   } else {
     lookback_loop(a, sh, ring, warp - kFirstLookbackWarp, lane, MULTI);
   }
 }
 
-template <bool MULTI>
+template <int F, bool MULTI>
 int encode_mx_blocks_per_sm() {
   static int cached = [] {
-    cudaFuncSetAttribute(encode_mx_kernel<MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         int(kDynSmem));
+    cudaFuncSetAttribute(encode_mx_kernel<F, MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         int(Stage<F>::kDynSmem));
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, encode_mx_kernel<MULTI>,
-                                                      kEncBlockThreads, kDynSmem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, encode_mx_kernel<F, MULTI>,
+                                                      kEncBlockThreads, Stage<F>::kDynSmem) != cudaSuccess ||
         b < 1)
       b = 1;
     return b;
@@ -630,16 +715,18 @@ int encode_mx_blocks_per_sm() {
 }
 
 // ------------------------------------------------------------ quantize
-// The MXFP8 view of one tensor (initial state of the trainer's previous view
+// The MX view of one tensor (initial state of the trainer's previous view
 // and of a receiver), with the encode's arithmetic: 8 consecutive elements
 // per thread, so block b of a warp's 256 elements is lanes 4b .. 4b+3.
 constexpr int kQuantThreads = 256;
 
+template <int F>
 __global__ void __launch_bounds__(kQuantThreads)
     mx_quantize_kernel(const float* __restrict__ master, uint64_t n, uint8_t* __restrict__ codes,
                        uint8_t* __restrict__ scales) {
+  constexpr uint32_t kGroupBytes = kMxPerThread / Fmt<F>::kElemsPerByte;
   const bool vec = (reinterpret_cast<uintptr_t>(master) % 16u == 0) &&
-                   (reinterpret_cast<uintptr_t>(codes) % 8u == 0);
+                   (reinterpret_cast<uintptr_t>(codes) % kGroupBytes == 0);
   const uint64_t groups = (n + kMxPerThread - 1) / kMxPerThread;
   const uint64_t stride = uint64_t(gridDim.x) * kQuantThreads;
   // every lane of a warp runs the same number of iterations (shuffles below)
@@ -660,13 +747,25 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
     const float4 a = make_float4(v[0], v[1], v[2], v[3]);
     const float4 b = make_float4(v[4], v[5], v[6], v[7]);
-    const uint32_t sb = block_scale8(a, b);
-    const uint32_t c0 = mx_codes4(a, sb), c1 = mx_codes4(b, sb);
-    if (full) {
-      *reinterpret_cast<uint2*>(codes + i) = make_uint2(c0, c1);
+    const uint32_t sb = block_scale8<Fmt<F>::kEmax>(a, b);
+    uint32_t c0, c1;
+    if constexpr (F == kFmtE2M1) {
+      c0 = fp4_codes8(a, b, sb);
+      c1 = 0u;
     } else {
-      for (int e = 0; e < kMxPerThread; ++e)
-        if (i + e < n) codes[i + e] = uint8_t((e < 4 ? c0 : c1) >> (8 * (e & 3)));
+      c0 = mx_codes4(a, sb);
+      c1 = mx_codes4(b, sb);
+    }
+    const uint64_t cb = i / Fmt<F>::kElemsPerByte;  // first code byte
+    if (full) {
+      if constexpr (F == kFmtE2M1)
+        *reinterpret_cast<uint32_t*>(codes + cb) = c0;
+      else
+        *reinterpret_cast<uint2*>(codes + cb) = make_uint2(c0, c1);
+    } else {
+      for (int e = 0; e < int(kGroupBytes); ++e)
+        if (i + uint64_t(e) * Fmt<F>::kElemsPerByte < n)
+          codes[cb + e] = uint8_t((e < 4 ? c0 : c1) >> (8 * (e & 3)));
     }
     if ((lane & (kLanesPerBlock - 1)) == 0 && i < n) scales[i / kMxBlock] = uint8_t(sb);
   }
@@ -674,24 +773,40 @@ __global__ void __launch_bounds__(kQuantThreads)
 
 }  // namespace
 
-int encode_mx_grid_size(int device) {
-  const int a = encode_mx_blocks_per_sm<true>(), b = encode_mx_blocks_per_sm<false>();
+int encode_mx_grid_size(int device, int format) {
+  int a, b;
+  if (format == kFmtE2M1) {
+    a = encode_mx_blocks_per_sm<kFmtE2M1, true>();
+    b = encode_mx_blocks_per_sm<kFmtE2M1, false>();
+  } else {
+    a = encode_mx_blocks_per_sm<kFmtE4M3, true>();
+    b = encode_mx_blocks_per_sm<kFmtE4M3, false>();
+  }
   return sm_count(device) * (a < b ? a : b);
 }
 
-cudaError_t launch_encode_mx(const MxLaunch& a, bool multi, int grid, cudaStream_t stream) {
+namespace {
+template <int F>
+cudaError_t launch_encode_mx_t(const MxLaunch& a, bool multi, int grid, cudaStream_t stream) {
   if (multi) {
-    encode_mx_blocks_per_sm<true>();
-    encode_mx_kernel<true><<<grid, kEncBlockThreads, kDynSmem, stream>>>(a);
+    encode_mx_blocks_per_sm<F, true>();
+    encode_mx_kernel<F, true><<<grid, kEncBlockThreads, Stage<F>::kDynSmem, stream>>>(a);
   } else {
-    encode_mx_blocks_per_sm<false>();
-    encode_mx_kernel<false><<<grid, kEncBlockThreads, kDynSmem, stream>>>(a);
+    encode_mx_blocks_per_sm<F, false>();
+    encode_mx_kernel<F, false><<<grid, kEncBlockThreads, Stage<F>::kDynSmem, stream>>>(a);
   }
   return cudaGetLastError();
 }
+}  // namespace
 
-cudaError_t launch_mx_quantize(const float* master, uint64_t n, uint8_t* codes, uint8_t* scales,
-                               cudaStream_t stream) {
+cudaError_t launch_encode_mx(const MxLaunch& a, int format, bool multi, int grid,
+                             cudaStream_t stream) {
+  return format == kFmtE2M1 ? launch_encode_mx_t<kFmtE2M1>(a, multi, grid, stream)
+                            : launch_encode_mx_t<kFmtE4M3>(a, multi, grid, stream);
+}
+
+cudaError_t launch_mx_quantize(int format, const float* master, uint64_t n, uint8_t* codes,
+                               uint8_t* scales, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t warps = (n + 32 * kMxPerThread - 1) / (32 * kMxPerThread);
@@ -699,7 +814,10 @@ cudaError_t launch_mx_quantize(const float* master, uint64_t n, uint8_t* codes, 
   const uint64_t cap = uint64_t(sm_count(dev)) * 8u;
   const int grid = int(blocks < cap ? blocks : cap);
   if (grid == 0) return cudaSuccess;
-  mx_quantize_kernel<<<grid, kQuantThreads, 0, stream>>>(master, n, codes, scales);
+  if (format == kFmtE2M1)
+    mx_quantize_kernel<kFmtE2M1><<<grid, kQuantThreads, 0, stream>>>(master, n, codes, scales);
+  else
+    mx_quantize_kernel<kFmtE4M3><<<grid, kQuantThreads, 0, stream>>>(master, n, codes, scales);
   return cudaGetLastError();
 }
 

@@ -89,17 +89,17 @@ struct EncodeLaunch {
 int encode_grid_size(int device);
 cudaError_t launch_encode(const EncodeLaunch& a, bool multi, int grid, cudaStream_t stream);
 
-// ------------------------------------------------------- MXFP8 view encode
+// ------------------------------------------------------- MX view encode
 // Same CTA layout and tile as the BF16 encode; a tile holds kEncTile / 32
 // blocks of 32 elements sharing one E8M0 scale.
 constexpr int kMxBlock = 32;
 
 struct MxTensorDesc {
   const float* master;
-  uint8_t* prev_codes;   // n E4M3 codes, in/out
+  uint8_t* prev_codes;   // code bytes (n for E4M3, ceil(n / 2) for E2M1), in/out
   uint8_t* prev_scales;  // ceil(n / 32) E8M0 scales, in/out
-  uint32_t* idx;         // code segment: element indices
-  uint8_t* val;          //               new codes
+  uint32_t* idx;         // code segment: code-byte indices
+  uint8_t* val;          //               new code bytes
   uint32_t* sidx;        // scale segment: block indices
   uint8_t* sval;         //                new scales
   uint64_t n;
@@ -122,10 +122,15 @@ struct MxLaunch {
   uint64_t wait_limit_ns;
 };
 
-int encode_mx_grid_size(int device);
-cudaError_t launch_encode_mx(const MxLaunch& a, bool multi, int grid, cudaStream_t stream);
-cudaError_t launch_mx_quantize(const float* master, uint64_t n, uint8_t* codes, uint8_t* scales,
-                               cudaStream_t stream);
+// Element formats of the MX views (values of the public PULSE_MX_* constants).
+constexpr int kFmtE4M3 = 0;  // MXFP8: one E4M3 code per byte
+constexpr int kFmtE2M1 = 1;  // MXFP4: two E2M1 codes per byte, element 2j in the low nibble
+
+int encode_mx_grid_size(int device, int format);
+cudaError_t launch_encode_mx(const MxLaunch& a, int format, bool multi, int grid,
+                             cudaStream_t stream);
+cudaError_t launch_mx_quantize(int format, const float* master, uint64_t n, uint8_t* codes,
+                               uint8_t* scales, cudaStream_t stream);
 
 // ---------------------------------------------------------------- PULSELoCo
 struct LocoTensorDesc {

@@ -66,12 +66,21 @@ class PulseMxTensor(ctypes.Structure):
 
 
 MX_BLOCK = 32
+MX_E4M3 = 0  # MXFP8 view: one E4M3 code per byte
+MX_E2M1 = 1  # MXFP4 view: two E2M1 codes per byte, element 2j in the low nibble
 _U8 = (torch.uint8, torch.int8)
 
 
 def mx_blocks(n: int) -> int:
-    """Scale bytes of an n-element MXFP8 view."""
+    """Scale bytes of an n-element MX view."""
     return (int(n) + MX_BLOCK - 1) // MX_BLOCK
+
+
+def mx_code_bytes(n: int, fmt: int = MX_E4M3) -> int:
+    """Code bytes of an n-element MX view of format ``fmt``."""
+    if fmt not in (MX_E4M3, MX_E2M1):
+        raise ValueError(f"unknown MX format {fmt}")
+    return int(n) if fmt == MX_E4M3 else (int(n) + 1) // 2
 
 
 class PulseComposeSegment(ctypes.Structure):
@@ -179,6 +188,10 @@ def lib():
             "pulse_mx_apply_multi": ([P, P, P], I),
             "pulse_mx_apply_multi_device": ([P, P, P], I),
             "pulse_mx_plan_get_error": ([P], I),
+            "pulse_mx_quantize_fmt": ([I, P, U64, P, P, P], I),
+            "pulse_mx_encode_fmt": ([I, P, P, P, U64, P, P, P, P, P, P], I),
+            "pulse_mx_apply_fmt": ([I, P, P, U64, P, P, U64, P, P, U64, P], I),
+            "pulse_mx_plan_create_fmt": ([ctypes.POINTER(PulseMxTensor), I, I, ctypes.POINTER(P)], I),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -496,64 +509,73 @@ class Plan:
 # ------------------------------------------------------------ MXFP8 view
 
 def mx_quantize(master: torch.Tensor, codes_out: Optional[torch.Tensor] = None,
-                scales_out: Optional[torch.Tensor] = None):
-    """pulse_mx_quantize: returns the MXFP8 view (codes uint8[n], scales uint8[ceil(n/32)])."""
+                scales_out: Optional[torch.Tensor] = None, fmt: int = MX_E4M3):
+    """pulse_mx_quantize_fmt: returns the MX view of format ``fmt`` (codes
+    uint8[mx_code_bytes(n, fmt)], scales uint8[ceil(n/32)])."""
     _need(master, "master", (torch.float32,))
     dev = master.device
     n = master.numel()
+    ncb = mx_code_bytes(n, fmt)
     if codes_out is None:
-        codes_out = torch.empty(n, dtype=torch.uint8, device=dev)
+        codes_out = torch.empty(ncb, dtype=torch.uint8, device=dev)
     if scales_out is None:
         scales_out = torch.empty(mx_blocks(n), dtype=torch.uint8, device=dev)
-    _need(codes_out, "codes_out", _U8, dev, n)
+    _need(codes_out, "codes_out", _U8, dev, ncb)
     _need(scales_out, "scales_out", _U8, dev, mx_blocks(n))
     with torch.cuda.device(dev):
-        st = lib().pulse_mx_quantize(_ptr(master), n, _ptr(codes_out), _ptr(scales_out), _stream(dev))
-    _raise(st, "pulse_mx_quantize")
+        st = lib().pulse_mx_quantize_fmt(fmt, _ptr(master), n, _ptr(codes_out), _ptr(scales_out),
+                                         _stream(dev))
+    _raise(st, "pulse_mx_quantize_fmt")
     return codes_out, scales_out
 
 
 def mx_encode(master: torch.Tensor, prev_codes: torch.Tensor, prev_scales: torch.Tensor,
-              idx_out=None, val_out=None, sidx_out=None, sval_out=None, counts_out=None):
-    """pulse_mx_encode: returns (idx, val, sidx, sval, counts); refreshes the
-    previous view in place. ``counts`` is a 2-element device int64 tensor
-    {changed codes, changed scales}; each segment is the first count entries
-    of its buffers."""
+              idx_out=None, val_out=None, sidx_out=None, sval_out=None, counts_out=None,
+              fmt: int = MX_E4M3):
+    """pulse_mx_encode_fmt: returns (idx, val, sidx, sval, counts); refreshes
+    the previous view in place. ``counts`` is a 2-element device int64 tensor
+    {changed code bytes, changed scales}; each segment is the first count
+    entries of its buffers."""
     _need(master, "master", (torch.float32,))
     dev = master.device
     n = master.numel()
     nb = mx_blocks(n)
-    _need(prev_codes, "prev_codes", _U8, dev, n)
+    ncb = mx_code_bytes(n, fmt)
+    _need(prev_codes, "prev_codes", _U8, dev, ncb)
     _need(prev_scales, "prev_scales", _U8, dev, nb)
     if idx_out is None:
-        idx_out = torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+        idx_out = torch.empty(max(ncb, 1), dtype=torch.int32, device=dev)
     if val_out is None:
-        val_out = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        val_out = torch.empty(max(ncb, 1), dtype=torch.uint8, device=dev)
     if sidx_out is None:
         sidx_out = torch.empty(max(nb, 1), dtype=torch.int32, device=dev)
     if sval_out is None:
         sval_out = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
     if counts_out is None:
         counts_out = torch.empty(2, dtype=torch.int64, device=dev)
-    _need(idx_out, "idx_out", (torch.int32, torch.uint32), dev, min_numel=n)
-    _need(val_out, "val_out", _U8, dev, min_numel=n)
+    _need(idx_out, "idx_out", (torch.int32, torch.uint32), dev, min_numel=ncb)
+    _need(val_out, "val_out", _U8, dev, min_numel=ncb)
     _need(sidx_out, "sidx_out", (torch.int32, torch.uint32), dev, min_numel=nb)
     _need(sval_out, "sval_out", _U8, dev, min_numel=nb)
     _need(counts_out, "counts_out", (torch.int64, torch.uint64), dev, min_numel=2)
     with torch.cuda.device(dev):
-        st = lib().pulse_mx_encode(_ptr(master), _ptr(prev_codes), _ptr(prev_scales), n,
-                                   _ptr(idx_out), _ptr(val_out), _ptr(sidx_out), _ptr(sval_out),
-                                   _ptr(counts_out), _stream(dev))
-    _raise(st, "pulse_mx_encode")
+        st = lib().pulse_mx_encode_fmt(fmt, _ptr(master), _ptr(prev_codes), _ptr(prev_scales), n,
+                                       _ptr(idx_out), _ptr(val_out), _ptr(sidx_out), _ptr(sval_out),
+                                       _ptr(counts_out), _stream(dev))
+    _raise(st, "pulse_mx_encode_fmt")
     return idx_out, val_out, sidx_out, sval_out, counts_out
 
 
 def mx_apply(codes: torch.Tensor, scales: torch.Tensor, idx, val, count: int, sidx, sval,
-             scount: int):
-    """pulse_mx_apply: codes[idx[j]] = val[j] (j < count), scales[sidx[j]] = sval[j] (j < scount)."""
+             scount: int, fmt: int = MX_E4M3, n: Optional[int] = None):
+    """pulse_mx_apply_fmt: codes[idx[j]] = val[j] (j < count), scales[sidx[j]] = sval[j]
+    (j < scount), on a view of ``n`` elements (default: every code byte full)."""
     _need(codes, "codes", _U8)
     dev = codes.device
-    n = codes.numel()
+    if n is None:
+        n = codes.numel() * (1 if fmt == MX_E4M3 else 2)
+    n = int(n)
+    _need(codes, "codes", _U8, dev, mx_code_bytes(n, fmt))
     _need(scales, "scales", _U8, dev, mx_blocks(n))
     count, scount = int(count), int(scount)
     _need(idx, "idx", (torch.int32, torch.uint32), dev, min_numel=count)
@@ -561,9 +583,9 @@ def mx_apply(codes: torch.Tensor, scales: torch.Tensor, idx, val, count: int, si
     _need(sidx, "sidx", (torch.int32, torch.uint32), dev, min_numel=scount)
     _need(sval, "sval", _U8, dev, min_numel=scount)
     with torch.cuda.device(dev):
-        st = lib().pulse_mx_apply(_ptr(codes), _ptr(scales), n, _ptr(idx), _ptr(val), count,
-                                  _ptr(sidx), _ptr(sval), scount, _stream(dev))
-    _raise(st, "pulse_mx_apply")
+        st = lib().pulse_mx_apply_fmt(fmt, _ptr(codes), _ptr(scales), n, _ptr(idx), _ptr(val), count,
+                                      _ptr(sidx), _ptr(sval), scount, _stream(dev))
+    _raise(st, "pulse_mx_apply_fmt")
 
 
 class MxTensorSlot:
@@ -578,25 +600,29 @@ class MxTensorSlot:
 
 
 class MxPlan:
-    """pulse_mx_plan: the MXFP8 view of a fixed tensor list, one launch per step.
+    """pulse_mx_plan: the MX view (format ``fmt``) of a fixed tensor list, one
+    launch per step.
 
     Counts are 2 x ntensors int64 in list order: {codes_0, scales_0, codes_1, ...}."""
 
-    def __init__(self, slots: Sequence[MxTensorSlot], device: Optional[torch.device] = None):
+    def __init__(self, slots: Sequence[MxTensorSlot], device: Optional[torch.device] = None,
+                 fmt: int = MX_E4M3):
         if len(slots) == 0:
             raise ValueError("a plan needs at least one tensor")
         self.slots = list(slots)
+        self.fmt = fmt
         dev = device
         arr = (PulseMxTensor * len(slots))()
         for i, s in enumerate(slots):
             nb = mx_blocks(s.n)
+            ncb = mx_code_bytes(s.n, fmt)
             checks = (("master", s.master, (torch.float32,), s.n, None),
-                      ("prev_codes", s.prev_codes, _U8, s.n, None),
+                      ("prev_codes", s.prev_codes, _U8, ncb, None),
                       ("prev_scales", s.prev_scales, _U8, nb, None),
-                      ("codes", s.codes, _U8, s.n, None),
+                      ("codes", s.codes, _U8, ncb, None),
                       ("scales", s.scales, _U8, nb, None),
-                      ("idx", s.idx, (torch.int32, torch.uint32), None, s.n),
-                      ("val", s.val, _U8, None, s.n),
+                      ("idx", s.idx, (torch.int32, torch.uint32), None, ncb),
+                      ("val", s.val, _U8, None, ncb),
                       ("sidx", s.sidx, (torch.int32, torch.uint32), None, nb),
                       ("sval", s.sval, _U8, None, nb))
             for name, t, dtypes, numel, min_numel in checks:
@@ -614,8 +640,8 @@ class MxPlan:
         self.ntensors = len(slots)
         handle = ctypes.c_void_p()
         with torch.cuda.device(dev):
-            st = lib().pulse_mx_plan_create(arr, len(slots), ctypes.byref(handle))
-        _raise(st, "pulse_mx_plan_create")
+            st = lib().pulse_mx_plan_create_fmt(arr, len(slots), fmt, ctypes.byref(handle))
+        _raise(st, "pulse_mx_plan_create_fmt")
         self._h = handle
 
     def encode(self, counts_out: Optional[torch.Tensor] = None) -> torch.Tensor:

@@ -109,6 +109,13 @@ def test_mx_host_side_argument_checks_launch_nothing(lib):
     E = pulse.pulse
     assert lib.pulse_mx_quantize(P(0), 0, P(0), P(0), P(0)) == E.PULSE_OK
     assert lib.pulse_mx_quantize(P(0), 7, P(0), P(0), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_quantize_fmt(2, P(8), 7, P(8), P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_quantize_fmt(1, P(0), 7, P(0), P(0), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_encode_fmt(5, P(8), P(8), P(8), 5, P(8), P(8), P(8), P(8), P(8), P(0)) \
+        == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_apply_fmt(-1, P(8), P(8), 5, P(8), P(8), 1, P(8), P(8), 1, P(0)) \
+        == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_plan_create_fmt(None, 1, 1, None) == E.PULSE_ERR_INVALID
     assert lib.pulse_mx_quantize(P(0), 1 << 32, P(0), P(0), P(0)) == E.PULSE_ERR_RANGE
     assert lib.pulse_mx_encode(P(0), P(0), P(0), 5, P(0), P(0), P(0), P(0), P(0), P(0)) == E.PULSE_ERR_INVALID
     assert lib.pulse_mx_encode(P(0), P(0), P(0), 5, P(0), P(0), P(0), P(0), P(8), P(0)) == E.PULSE_ERR_INVALID
