@@ -615,6 +615,19 @@ def run_compose(args, wl, dev, versions: int = 4):
     chain_refs = chain_plan.prepare_chain([[(c[0][t], c[1][t], c[2][t]) for t in range(T)]
                                            for c in chain])
 
+    kway_out = [(torch.empty(max(cap[t], 1), dtype=torch.int32, device=dev),
+                 torch.empty(max(cap[t], 1), dtype=torch.int16, device=dev)) for t in range(T)]
+    kway_prep = chain_plan.prepare_compose(chain_refs, kway_out)
+    kway_counts = torch.empty(T, dtype=torch.int64, device=dev)
+
+    def compose_kway():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        chain_plan.compose_chain(kway_prep, counts_out=kway_counts)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3
+
     def apply_chained():
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -636,7 +649,7 @@ def run_compose(args, wl, dev, versions: int = 4):
             torch.cuda.synchronize()
             yield e0.elapsed_time(e1) * 1e-3
 
-    t_cmp, t_app1, t_seq, t_chain = [], [], [], []
+    t_cmp, t_app1, t_seq, t_chain, t_kway = [], [], [], [], []
     reps = max(1, min(args.steps, 3))
     for r in range(reps + 1):          # the first round is a warm-up
         for w, p0 in zip(wl.w, wl.prev0):
@@ -668,11 +681,18 @@ def run_compose(args, wl, dev, versions: int = 4):
         for t in range(T):
             if not torch.equal(wl.w[t], final_view[t]):
                 raise RuntimeError(f"chained catch-up differs from the final view (tensor {t})")
+        tk = compose_kway()
+        kc = kway_counts.cpu().tolist()
+        for t in range(T):
+            if kc[t] != ck[t] or not (torch.equal(kway_out[t][0][:kc[t]], ci[t][:ck[t]]) and
+                                      torch.equal(kway_out[t][1][:kc[t]], cv[t][:ck[t]])):
+                raise RuntimeError(f"k-way composition differs from the folded one (tensor {t})")
         if r > 0:
             t_cmp.append(tc)
             t_app1.append(ta)
             t_seq.append(ts)
             t_chain.append(tch)
+            t_kway.append(tk)
     if pulse.get_error(dev) != 0:
         raise RuntimeError("device error in the compose leg")
     if chain_plan.get_error() != 0:
@@ -691,18 +711,25 @@ def run_compose(args, wl, dev, versions: int = 4):
     moved = sum(fold_bytes)   # every fold reads both inputs and writes its output
     tcm, tam, tsm = float(np.mean(t_cmp)), float(np.mean(t_app1)), float(np.mean(t_seq))
     tchm = float(np.mean(t_chain))
+    tkm = float(np.mean(t_kway))
+    kway_bytes = 6 * sum(k_in) + 6 * k_out
     chain_bytes = 6 * sum(k_in) + 64 * s_union
     return {
         "versions": versions, "patch_entries": k_in, "composed_entries": k_out,
         "compose_ms": 1e3 * tcm, "apply_composed_ms": 1e3 * tam,
         "catch_up_composed_ms": 1e3 * (tcm + tam), "catch_up_sequential_ms": 1e3 * tsm,
         "compose_bytes": moved, "compose_gbs": moved / tcm / 1e9,
+        "compose_kway_ms": 1e3 * tkm, "compose_kway_bytes": kway_bytes,
+        "compose_kway_gbs": kway_bytes / tkm / 1e9,
+        "catch_up_kway_composed_ms": 1e3 * (tkm + tam),
         "catch_up_chained_ms": 1e3 * tchm, "sectors_union": s_union,
         "chained_bytes_model": "6 * sum(k) + 64 * S_union", "chained_bytes": chain_bytes,
         "chained_gbs": chain_bytes / tchm / 1e9,
         "timing": "compose: host wall time of the folds (includes the host counts read "
                   "between folds); applies: CUDA events; chained: one pulse_apply_chain_multi "
-                  "call on a prepared chain (partition + apply launch), CUDA events",
+                  "call on a prepared chain (partition + apply launch), CUDA events; k-way: one "
+                  "pulse_compose_chain_multi call over all versions (partition + compose "
+                  "launch), CUDA events, checked equal to the folded composition",
     }
 
 

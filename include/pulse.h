@@ -260,6 +260,38 @@ typedef struct pulse_patch_ref {
 int pulse_apply_chain_multi(pulse_plan *plan, const pulse_patch_ref *patches, int nversions,
                             cudaStream_t stream);
 
+/*
+ * pulse_compose_chain_multi -- compose the patches of nversions consecutive
+ * versions (1 .. 16) of every tensor of the plan into ONE patch per tensor.
+ * [TALK] 16:40-17:04 (a sidecar catching up), [PULSE] "1. PULSESync" (values
+ * are absolute): the result lists every index any version lists, with the
+ * value of the latest version that lists it, in ascending order; applying it
+ * equals applying the versions in turn. Per tensor it equals folding
+ * pulse_compose over the versions, oldest first.
+ *   patches     HOST, nversions x ntensors references, version-major (as for
+ *               pulse_apply_chain_multi); each segment ascending
+ *   outs        HOST, ntensors: outs[t].idx / outs[t].val (device) receive
+ *               tensor t's composed segment; outs[t].room (host) must be at
+ *               least min(n, sum over versions of min(count, n))
+ *   counts_out  DEVICE, ntensors uint64: entries written per tensor
+ * One partition launch and one compose launch; the plan needs only the
+ * tensors' sizes (no buffer of the plan is read or written). Output buffers
+ * must not overlap the inputs. Errors: PULSE_ERR_INVALID (NULL argument,
+ * nversions outside 1..16, an output segment without room), PULSE_ERR_RANGE,
+ * PULSE_ERR_NOMEM, PULSE_ERR_CUDA; device (plan error word): PULSE_ERR_INDEX
+ * (count > n, clamped; an entry outside its chunk, skipped),
+ * PULSE_ERR_TIMEOUT.
+ */
+typedef struct pulse_patch_out {
+    uint32_t *idx;  /* device, room entries */
+    uint16_t *val;  /* device, room entries */
+    uint64_t room;  /* host value */
+} pulse_patch_out;
+
+int pulse_compose_chain_multi(pulse_plan *plan, const pulse_patch_ref *patches, int nversions,
+                              const pulse_patch_out *outs, uint64_t *counts_out,
+                              cudaStream_t stream);
+
 /* XOR mask / XOR apply over every tensor of the plan, one launch each. */
 int pulse_xor_mask_multi(pulse_plan *plan, cudaStream_t stream);
 int pulse_xor_apply_multi(pulse_plan *plan, cudaStream_t stream);

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpulse.so")
-SOURCES = ["api.cu", "encode.cu", "encode_mx.cu", "compose.cu", "loco.cu", "pack.cu", "apply.cu", "xor.cu", "encode_noalloc.cu"]
+SOURCES = ["api.cu", "encode.cu", "encode_mx.cu", "compose.cu", "compose_chunk.cu", "loco.cu", "pack.cu", "apply.cu", "xor.cu", "encode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

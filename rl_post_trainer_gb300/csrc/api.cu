@@ -351,6 +351,7 @@ struct pulse_plan {
   ChainSeg* chain_segs = nullptr;   // device, chain_seg_cap entries
   uint64_t chain_seg_cap = 0;
   uint32_t* chain_first = nullptr;  // device, kChainMaxVersions x total_chunks (first use)
+  CcOut* cc_outs = nullptr;         // device, ntensors (first k-way compose)
   Workspace ws;
 };
 
@@ -535,8 +536,8 @@ int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** pl
   } else {
     st = workspace_reserve(p->ws, tiles, nullptr);
   }
-  if (st == PULSE_OK && p->can_chain) {
-    // chunk tables of the chunk-owned (and chained) apply
+  if (st == PULSE_OK) {
+    // chunk tables of the chunk-owned apply, the chained apply and the k-way compose
     std::vector<uint64_t> cb(size_t(ntensors) + 1, 0);
     uint64_t chunks = 0;
     for (int i = 0; i < ntensors; ++i) {
@@ -579,6 +580,7 @@ int pulse_plan_destroy(pulse_plan* plan) {
   if (plan->chunk_first) cudaFree(plan->chunk_first);
   if (plan->chain_segs) cudaFree(plan->chain_segs);
   if (plan->chain_first) cudaFree(plan->chain_first);
+  if (plan->cc_outs) cudaFree(plan->cc_outs);
   workspace_free(plan->ws);
   delete plan;
   return cuda_status(e);
@@ -636,10 +638,11 @@ int pulse_apply_multi(pulse_plan* plan, const uint64_t* counts_host, cudaStream_
   return pulse_apply_multi_device(plan, plan->counts, stream);
 }
 
-int pulse_apply_chain_multi(pulse_plan* plan, const pulse_patch_ref* patches, int nversions,
-                            cudaStream_t stream) {
-  if (plan == nullptr || patches == nullptr || nversions < 1 || !plan->can_chain)
-    return PULSE_ERR_INVALID;
+namespace {
+// Check a chain's host references and upload them into the plan's table
+// (growth synchronises `stream`); allocates the partition scratch on first use.
+int upload_chain(pulse_plan* plan, const pulse_patch_ref* patches, int nversions,
+                 cudaStream_t stream) {
   const uint64_t nseg = uint64_t(nversions) * uint64_t(plan->ntensors);
   std::vector<ChainSeg> segs(static_cast<size_t>(nseg));
   for (uint64_t i = 0; i < nseg; ++i) {
@@ -671,6 +674,16 @@ int pulse_apply_chain_multi(pulse_plan* plan, const pulse_patch_ref* patches, in
   if (cudaMemcpyAsync(plan->chain_segs, segs.data(), sizeof(ChainSeg) * size_t(nseg),
                       cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return PULSE_ERR_CUDA;
+  return PULSE_OK;
+}
+}  // namespace
+
+int pulse_apply_chain_multi(pulse_plan* plan, const pulse_patch_ref* patches, int nversions,
+                            cudaStream_t stream) {
+  if (plan == nullptr || patches == nullptr || nversions < 1 || !plan->can_chain)
+    return PULSE_ERR_INVALID;
+  const int st = upload_chain(plan, patches, nversions, stream);
+  if (st != PULSE_OK || plan->total_chunks == 0) return st;
   for (int v0 = 0; v0 < nversions; v0 += kChainMaxVersions) {
     const int nv = nversions - v0 < kChainMaxVersions ? nversions - v0 : kChainMaxVersions;
     const cudaError_t e = launch_apply_chain(
@@ -680,6 +693,64 @@ int pulse_apply_chain_multi(pulse_plan* plan, const pulse_patch_ref* patches, in
     if (e != cudaSuccess) return PULSE_ERR_CUDA;
   }
   return PULSE_OK;
+}
+
+int pulse_compose_chain_multi(pulse_plan* plan, const pulse_patch_ref* patches, int nversions,
+                              const pulse_patch_out* outs, uint64_t* counts_out,
+                              cudaStream_t stream) {
+  if (plan == nullptr || patches == nullptr || outs == nullptr || counts_out == nullptr ||
+      nversions < 1 || nversions > kChainMaxVersions)
+    return PULSE_ERR_INVALID;
+  const int nt = plan->ntensors;
+  std::vector<CcOut> table(static_cast<size_t>(nt));
+  for (int t = 0; t < nt; ++t) {
+    // the composed segment holds at most min(n, sum of the versions' counts)
+    const uint64_t n = plan->host_desc[size_t(t)].n;
+    uint64_t need = 0;
+    for (int v = 0; v < nversions; ++v) {
+      const uint64_t c = patches[size_t(v) * size_t(nt) + size_t(t)].count;
+      need += c < n ? c : n;
+    }
+    if (need > n) need = n;
+    const pulse_patch_out& o = outs[t];
+    if (o.room < need || (need > 0 && (o.idx == nullptr || o.val == nullptr)))
+      return PULSE_ERR_INVALID;
+    table[size_t(t)] = CcOut{o.idx, o.val, o.room};
+  }
+  int st = upload_chain(plan, patches, nversions, stream);
+  if (st != PULSE_OK) return st;
+  // tensors without chunks (n == 0) keep a count of 0; the others are
+  // written by their last chunk
+  if (cudaMemsetAsync(counts_out, 0, sizeof(uint64_t) * size_t(nt), stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  if (plan->total_chunks == 0) return PULSE_OK;
+  if (plan->cc_outs == nullptr &&
+      cudaMalloc(&plan->cc_outs, sizeof(CcOut) * size_t(nt)) != cudaSuccess)
+    return PULSE_ERR_NOMEM;
+  if (cudaMemcpyAsync(plan->cc_outs, table.data(), sizeof(CcOut) * size_t(nt),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  if (launch_chain_partition(plan->desc, plan->chunk_begin, plan->chunk_tensor, plan->chain_segs,
+                             nt, nversions, plan->total_chunks, plan->chain_first,
+                             plan->ws.counters + 2, stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  CcArgs a{};
+  a.tensors = plan->desc;
+  a.chunk_begin = plan->chunk_begin;
+  a.chunk_tensor = plan->chunk_tensor;
+  a.first = plan->chain_first;
+  a.segs = plan->chain_segs;
+  a.outs = plan->cc_outs;
+  a.counts_out = counts_out;
+  a.ntensors = nt;
+  a.nversions = nversions;
+  a.total_chunks = plan->total_chunks;
+  a.status = plan->ws.status;
+  a.counters = plan->ws.counters;
+  a.wait_limit_ns = kDefaultWaitNs;
+  st = workspace_next_epoch(plan->ws, stream, &a.epoch);
+  if (st != PULSE_OK) return st;
+  return cuda_status(launch_compose_chunks(a, stream));
 }
 
 int pulse_xor_mask_multi(pulse_plan* plan, cudaStream_t stream) {

@@ -602,6 +602,19 @@ cudaError_t launch_apply_chunks(const TensorDesc* tensors, const uint64_t* chunk
   return cudaGetLastError();
 }
 
+cudaError_t launch_chain_partition(const TensorDesc* tensors, const uint64_t* chunk_begin,
+                                   const uint32_t* chunk_tensor, const ChainSeg* segs,
+                                   int ntensors, int nversions, uint64_t total_chunks,
+                                   uint32_t* chain_first, uint32_t* error_word,
+                                   cudaStream_t stream) {
+  const uint64_t parts = total_chunks * uint64_t(nversions);
+  if (parts == 0) return cudaSuccess;
+  chain_partition_kernel<<<unsigned((parts + 255) / 256), 256, 0, stream>>>(
+      tensors, chunk_begin, chunk_tensor, segs, ntensors, nversions, total_chunks, chain_first,
+      error_word);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_apply_chain(const TensorDesc* tensors, const uint64_t* chunk_begin,
                                const uint32_t* chunk_tensor, uint32_t* chain_first,
                                const ChainSeg* segs, int ntensors, int nversions,

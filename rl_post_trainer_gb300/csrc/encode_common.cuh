@@ -159,7 +159,8 @@ __device__ __forceinline__ void load_window(const L& a, int64_t pos, uint64_t fi
 // words per round trip, nearest first; waits only on unpublished words that
 // lie before the nearest inclusive prefix; publishes g's inclusive prefix.
 // `w` holds the first window (load_window at g - 1), already in flight.
-template <class S, class L>
+// kSleepNs: pause between polls of unpublished words.
+template <class S, class L, unsigned kSleepNs = 32>
 __device__ __forceinline__ typename S::value_t resolve_prefix(const L& a, uint64_t g,
                                                               uint64_t first,
                                                               typename S::value_t agg, int lane,
@@ -201,7 +202,7 @@ __device__ __forceinline__ typename S::value_t resolve_prefix(const L& a, uint64
           continue;
         }
       }
-      __nanosleep(32);
+      __nanosleep(kSleepNs);
 #pragma unroll
       for (int q = 0; q < kLookbackPerLane; ++q) {
         if (S::flag(w[q], a.epoch) == 0u)

@@ -271,6 +271,39 @@ cudaError_t launch_apply_chain(const TensorDesc* tensors, const uint64_t* chunk_
                                uint64_t total_chunks, uint32_t* error_word, uint64_t wait_limit_ns,
                                cudaStream_t stream);
 
+// Chain partition (shared by the chained apply and the k-way compose):
+// chain_first[v * total_chunks + g] = first entry of version v's segment at
+// or after chunk g's start (kApplyChunk elements per chunk).
+cudaError_t launch_chain_partition(const TensorDesc* tensors, const uint64_t* chunk_begin,
+                                   const uint32_t* chunk_tensor, const ChainSeg* segs,
+                                   int ntensors, int nversions, uint64_t total_chunks,
+                                   uint32_t* chain_first, uint32_t* error_word,
+                                   cudaStream_t stream);
+
+// k-way composition of a chain of patches (compose_chunk.cu).
+struct CcOut {
+  uint32_t* idx;  // composed segment of one tensor
+  uint16_t* val;
+  uint64_t cap;   // room in entries
+};
+struct CcArgs {
+  const TensorDesc* tensors;     // n of each tensor
+  const uint64_t* chunk_begin;   // ntensors + 1
+  const uint32_t* chunk_tensor;  // total_chunks
+  const uint32_t* first;         // chain partition: nversions x total_chunks
+  const ChainSeg* segs;          // nversions x ntensors, version-major (oldest first)
+  const CcOut* outs;             // ntensors
+  uint64_t* counts_out;          // ntensors (device), zeroed before the launch
+  int ntensors;
+  int nversions;                 // 1 .. kChainMaxVersions
+  uint64_t total_chunks;
+  uint64_t* status;              // one look-back word per chunk
+  uint32_t* counters;            // [0] ticket, [1] CTAs finished, [2] error word
+  uint32_t epoch;
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_compose_chunks(const CcArgs& a, cudaStream_t stream);
+
 // One byte-valued patch segment (an MXFP8 code or scale array).
 struct ByteSegment {
   uint8_t* w;

@@ -115,6 +115,14 @@ class PulsePackSegment(ctypes.Structure):
     ]
 
 
+class PulsePatchOut(ctypes.Structure):
+    _fields_ = [
+        ("idx", ctypes.c_void_p),
+        ("val", ctypes.c_void_p),
+        ("room", ctypes.c_uint64),
+    ]
+
+
 class PulseLocoTensor(ctypes.Structure):
     _fields_ = [
         ("global_w", ctypes.c_void_p),
@@ -159,6 +167,8 @@ def lib():
             "pulse_apply_multi": ([P, P, P], I),
             "pulse_apply_multi_device": ([P, P, P], I),
             "pulse_apply_chain_multi": ([P, ctypes.POINTER(PulsePatchRef), I, P], I),
+            "pulse_compose_chain_multi": ([P, ctypes.POINTER(PulsePatchRef), I,
+                                           ctypes.POINTER(PulsePatchOut), P, P], I),
             "pulse_xor_mask_multi": ([P, P], I),
             "pulse_xor_apply_multi": ([P, P], I),
             "pulse_plan_get_error": ([P], I),
@@ -359,9 +369,17 @@ class TensorSlot:
 class PreparedChain:
     """A chain of patch versions checked and marshalled for one Plan."""
 
-    def __init__(self, plan, refs, nversions: int, keep):
+    def __init__(self, plan, refs, nversions: int, keep, counts):
         self.plan, self.refs, self.nversions = plan, refs, int(nversions)
         self._keep = keep  # the patch tensors stay alive with the references
+        self.counts = counts  # counts[v][t], clamped to each tensor's size
+
+
+class PreparedCompose:
+    """A chain and its output segments marshalled for Plan.compose_chain."""
+
+    def __init__(self, chain: PreparedChain, outs, arr):
+        self.chain, self.outs, self.arr = chain, outs, arr
 
 
 class Plan:
@@ -459,7 +477,8 @@ class Plan:
                     keep.append((idx, val))
                 arr[v * self.ntensors + t] = PulsePatchRef(_ptr(idx) if c > 0 else None,
                                                            _ptr(val) if c > 0 else None, c)
-        return PreparedChain(self, arr, nv, keep)
+        counts = [[min(int(c), s.n) for (_, _, c), s in zip(row, self.slots)] for row in patches]
+        return PreparedChain(self, arr, nv, keep, counts)
 
     def apply_chain(self, patches):
         """pulse_apply_chain_multi: bring w forward by every version of the
@@ -472,6 +491,48 @@ class Plan:
             st = lib().pulse_apply_chain_multi(self._h, prep.refs, prep.nversions,
                                                _stream(self.device))
         _raise(st, "pulse_apply_chain_multi")
+
+    def prepare_compose(self, patches, outs=None) -> "PreparedCompose":
+        """Check and marshal a k-way composition once: the chain (a
+        PreparedChain or the nested list prepare_chain takes) and per tensor
+        (idx, val) device output buffers with room for min(n, sum of the
+        versions' counts) entries (allocated when ``outs`` is None)."""
+        prep = patches if isinstance(patches, PreparedChain) else self.prepare_chain(patches)
+        if prep.plan is not self:
+            raise ValueError("the chain was prepared for another plan")
+        if prep.nversions > 16:
+            raise ValueError("a composition takes at most 16 versions")
+        need = [min(s.n, sum(prep.counts[v][t] for v in range(prep.nversions)))
+                for t, s in enumerate(self.slots)]
+        if outs is None:
+            outs = [(torch.empty(max(r, 1), dtype=torch.int32, device=self.device),
+                     torch.empty(max(r, 1), dtype=torch.int16, device=self.device)) for r in need]
+        if len(outs) != self.ntensors:
+            raise ValueError(f"{len(outs)} output segments for {self.ntensors} tensors")
+        arr = (PulsePatchOut * self.ntensors)()
+        for t, ((oi, ov), r) in enumerate(zip(outs, need)):
+            _need(oi, "idx_out", (torch.int32, torch.uint32), self.device, min_numel=r)
+            _need(ov, "val_out", _U16, self.device, min_numel=r)
+            arr[t] = PulsePatchOut(_ptr(oi), _ptr(ov), min(oi.numel(), ov.numel()))
+        return PreparedCompose(prep, outs, arr)
+
+    def compose_chain(self, patches, outs=None, counts_out: Optional[torch.Tensor] = None):
+        """pulse_compose_chain_multi: one composed patch per tensor for a chain
+        of 1..16 versions (a PreparedCompose, or what prepare_compose takes).
+        Returns (outs, counts): per tensor (idx, val) buffers whose first
+        counts[t] entries are the composed segment (counts: device int64)."""
+        pc = patches if isinstance(patches, PreparedCompose) else self.prepare_compose(patches, outs)
+        if pc.chain.plan is not self:
+            raise ValueError("the composition was prepared for another plan")
+        if counts_out is None:
+            counts_out = torch.empty(self.ntensors, dtype=torch.int64, device=self.device)
+        _need(counts_out, "counts_out", (torch.int64, torch.uint64), self.device,
+              min_numel=self.ntensors)
+        with torch.cuda.device(self.device):
+            st = lib().pulse_compose_chain_multi(self._h, pc.chain.refs, pc.chain.nversions, pc.arr,
+                                                 _ptr(counts_out), _stream(self.device))
+        _raise(st, "pulse_compose_chain_multi")
+        return pc.outs, counts_out
 
     def xor_mask(self):
         with torch.cuda.device(self.device):

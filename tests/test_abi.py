@@ -85,6 +85,8 @@ def test_host_side_argument_checks_launch_nothing(lib):
     segs[0].count = 1 << 32
     assert lib.pulse_unpack_indices_multi(segs, 1, P(0)) == pulse.pulse.PULSE_ERR_RANGE
     refs = (pulse.pulse.PulsePatchRef * 1)()
+    outs = (pulse.pulse.PulsePatchOut * 1)()
+    assert lib.pulse_compose_chain_multi(None, refs, 1, outs, P(8), P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_apply_chain_multi(None, refs, 1, P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_apply_chain_multi(None, None, 1, P(0)) == pulse.pulse.PULSE_ERR_INVALID
     assert lib.pulse_xor_mask_multi(None, P(0)) == pulse.pulse.PULSE_ERR_INVALID

@@ -223,3 +223,85 @@ def test_prepared_chain_reused():
         with pulse.Plan([pulse.TensorSlot(n, w=w)]) as other:
             with pytest.raises(ValueError):
                 other.apply_chain(prep)
+
+
+# ------------------------------------------------------------ k-way compose
+
+def _compose(w_sizes, chains, dev, offset=0):
+    """GPU k-way composition of chains[t] (per tensor, oldest first); returns
+    per tensor (idx, val) of the composed segment and the plan's error word."""
+    slots = [pulse.TensorSlot(n, w=torch.zeros(max(n, 1), dtype=torch.int16, device=dev)[:n])
+             for n in w_sizes]
+    nv = len(chains[0])
+    patches = [[_dev_patch(chains[t][v], dev) for t in range(len(w_sizes))] for v in range(nv)]
+    with pulse.Plan(slots) as plan:
+        outs, counts = plan.compose_chain(patches)
+        torch.cuda.synchronize()
+        err = plan.get_error()
+        cnt = counts.cpu().tolist()
+        res = [(host_u32_(oi[:k]), host_u16(ov[:k])) for (oi, ov), k in zip(outs, cnt)]
+    return res, err
+
+
+def host_u32_(t):
+    return t.view(torch.int32).cpu().numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("nv", [1, 2, 4, 5, 16])
+def test_compose_chain_matches_oracle(nv):
+    dev = _dev()
+    rng = np.random.default_rng(500 + nv)
+    etas = ([3e-6, 1e-7, 1e-4, 3e-6, 3e-7] * 4)[:nv]
+    chains, finals, w0s = [], [], []
+    for n in SIZES:
+        w0, patches, last = _encode_chain(rng, n, etas)
+        chains.append(patches)
+        finals.append(last)
+        w0s.append(w0)
+    got, err = _compose(SIZES, chains, dev)
+    assert err == 0
+    for (gi, gv), chain, w0, last in zip(got, chains, w0s, finals):
+        oi, ov = oracle.compose_chain(chain)
+        np.testing.assert_array_equal(gi, oi)
+        np.testing.assert_array_equal(gv, ov)
+        w = w0.copy()
+        oracle.apply(w, gi, gv)
+        np.testing.assert_array_equal(w, last)  # one patch brings w0 to the last view
+
+
+def test_compose_chain_random_overlaps():
+    dev = _dev()
+    rng = np.random.default_rng(8)
+    sizes = [5 * CHUNK + 33, 70000, 9, CHUNK]
+    ks = [(4000, 20000, 60000), (30, 2, 0), (9, 9, 1), (CHUNK, CHUNK, CHUNK)]
+    chains = [[_rand_patch(rng, n, k) for k in kk] for n, kk in zip(sizes, ks)]
+    got, err = _compose(sizes, chains, dev)
+    assert err == 0
+    for (gi, gv), chain in zip(got, chains):
+        oi, ov = oracle.compose_chain(chain)
+        np.testing.assert_array_equal(gi, oi)
+        np.testing.assert_array_equal(gv, ov)
+
+
+def test_compose_chain_errors_and_limits():
+    dev = _dev()
+    n = 3 * CHUNK
+    gi = np.arange(0, n, 5, dtype=np.uint32)
+    good = (gi, np.ones(gi.size, np.uint16))
+    bad_idx = gi.copy()
+    bad_idx[10] = n - 1
+    _, err = _compose([n], [[good, (bad_idx, good[1])]], dev)
+    assert err == pulse.pulse.PULSE_ERR_INDEX
+    w = torch.zeros(10, dtype=torch.int16, device=dev)
+    with pulse.Plan([pulse.TensorSlot(10, w=w)]) as plan:
+        idx = torch.arange(12, dtype=torch.int32, device=dev)
+        val = torch.ones(12, dtype=torch.int16, device=dev)
+        outs, counts = plan.compose_chain([[(idx, val, 12)]])
+        torch.cuda.synchronize()
+        assert plan.get_error() == pulse.pulse.PULSE_ERR_INDEX
+        assert counts.cpu().tolist() == [10]
+        with pytest.raises(ValueError):   # more than 16 versions
+            plan.compose_chain([[(idx, val, 3)]] * 17)
+        small = [(torch.zeros(2, dtype=torch.int32, device=dev), torch.zeros(2, dtype=torch.int16, device=dev))]
+        with pytest.raises(ValueError):   # no room for the union
+            plan.compose_chain([[(idx, val, 5)], [(idx, val, 5)]], outs=small)
