@@ -3,7 +3,7 @@
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg use it; the product library never does. The
 arithmetic lives in ``pulse_oracle.c`` (BF16 view), ``mx_oracle.c``
-(MXFP8 view), ``mxfp4_oracle.c`` (MXFP4 view), ``compose_oracle.c`` (patch chains), ``loco_oracle.c``
+(MXFP8 view), ``mxfp4_oracle.c`` (MXFP4 view), ``nvfp4_oracle.c`` (NVFP4 view), ``compose_oracle.c`` (patch chains), ``loco_oracle.c``
 (PULSELoCo gate) and ``pack_oracle.c`` (index packing): plain C, scalar loops, ascending index order; this module
 compiles them with gcc and wraps them for numpy arrays. It imports nothing from the CUDA package.
 """
@@ -33,6 +33,11 @@ from .oracle import (  # noqa: F401
     mxfp4_quantize,
     mxfp4_encode,
     mxfp4_apply,
+    NV_BLOCK,
+    nv_blocks,
+    nvfp4_tensor_scale,
+    nvfp4_quantize,
+    nvfp4_encode,
     compose,
     compose_chain,
     loco_gate,

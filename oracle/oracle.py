@@ -23,7 +23,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRCS = [os.path.join(_HERE, f) for f in ("pulse_oracle.c", "mx_oracle.c", "mxfp4_oracle.c",
-                                          "compose_oracle.c", "loco_oracle.c", "pack_oracle.c")]
+                                          "nvfp4_oracle.c", "compose_oracle.c", "loco_oracle.c",
+                                          "pack_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
@@ -83,6 +84,12 @@ def _load():
             lib.oracle_mxfp4_quantize.restype = None
             lib.oracle_mxfp4_encode.argtypes = [P, P, P, U64, P, P, P, P, P]
             lib.oracle_mxfp4_encode.restype = None
+            lib.oracle_nvfp4_tensor_scale.argtypes = [P, U64]
+            lib.oracle_nvfp4_tensor_scale.restype = ctypes.c_float
+            lib.oracle_nvfp4_quantize.argtypes = [P, U64, P, P]
+            lib.oracle_nvfp4_quantize.restype = ctypes.c_float
+            lib.oracle_nvfp4_encode.argtypes = [P, P, P, U64, P, P, P, P, P]
+            lib.oracle_nvfp4_encode.restype = ctypes.c_float
             lib.oracle_apply_u8.argtypes = [P, P, P, U64]
             lib.oracle_apply_u8.restype = None
             lib.oracle_compose.argtypes = [P, P, U64, P, P, U64, P, P]
@@ -326,6 +333,54 @@ def mxfp4_apply(codes: np.ndarray, scales: np.ndarray, patch) -> None:
     idx, val, sidx, sval = patch
     apply_u8(codes, idx, val)
     apply_u8(scales, sidx, sval)
+
+
+# ------------------------------------------------------------- NVFP4 view
+
+NV_BLOCK = 16
+
+
+def nv_blocks(n: int) -> int:
+    return (n + NV_BLOCK - 1) // NV_BLOCK
+
+
+def nvfp4_tensor_scale(master: np.ndarray) -> float:
+    """S = (largest finite magnitude) / 2688, in FP32."""
+    _check(master, np.float32, "master")
+    return float(np.float32(_load().oracle_nvfp4_tensor_scale(_ptr(master), master.size)))
+
+
+def nvfp4_quantize(master: np.ndarray):
+    """Returns the NVFP4 view: (codes uint8[ceil(n/2)], block scales
+    uint8[ceil(n/16)] (E4M3), tensor scale as a numpy float32)."""
+    _check(master, np.float32, "master")
+    n = master.size
+    codes = np.empty(mxfp4_code_bytes(n), dtype=np.uint8)
+    scales = np.empty(nv_blocks(n), dtype=np.uint8)
+    S = _load().oracle_nvfp4_quantize(_ptr(master), n, _ptr(codes), _ptr(scales))
+    return codes, scales, np.float32(S)
+
+
+def nvfp4_encode(master: np.ndarray, prev_codes: np.ndarray, prev_scales: np.ndarray):
+    """Returns (idx, val, sidx, sval, tensor scale): changed code bytes,
+    changed block scales and the new tensor scale; refreshes the previous
+    view in place."""
+    _check(master, np.float32, "master")
+    _check(prev_codes, np.uint8, "prev_codes", writable=True)
+    _check(prev_scales, np.uint8, "prev_scales", writable=True)
+    n = master.size
+    if prev_codes.size != mxfp4_code_bytes(n) or prev_scales.size != nv_blocks(n):
+        raise ValueError("view arrays do not match the master's length")
+    nb, ncb = nv_blocks(n), mxfp4_code_bytes(n)
+    idx = np.empty(max(ncb, 1), dtype=np.uint32)
+    val = np.empty(max(ncb, 1), dtype=np.uint8)
+    sidx = np.empty(max(nb, 1), dtype=np.uint32)
+    sval = np.empty(max(nb, 1), dtype=np.uint8)
+    counts = np.zeros(2, dtype=np.uint64)
+    S = _load().oracle_nvfp4_encode(_ptr(master), _ptr(prev_codes), _ptr(prev_scales), n,
+                                    _ptr(idx), _ptr(val), _ptr(sidx), _ptr(sval), _ptr(counts))
+    k, ks = int(counts[0]), int(counts[1])
+    return idx[:k].copy(), val[:k].copy(), sidx[:ks].copy(), sval[:ks].copy(), np.float32(S)
 
 
 # ---------------------------------------------------- patch-chain composition
