@@ -430,6 +430,7 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
     if not args.no_mx:
         out["mxfp8"] = run_mx(args, cfg, specs, wl, dev, rank, peak, pulse.MX_E4M3)
         out["mxfp4"] = run_mx(args, cfg, specs, wl, dev, rank, peak, pulse.MX_E2M1)
+        out["nvfp4"] = run_mx(args, cfg, specs, wl, dev, rank, peak, pulse.MX_NVFP4)
 
     if not args.no_e2e:
         out["e2e"] = e2e(args, wl, counts_np, dist_on)
@@ -454,13 +455,15 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
 
 
 def run_mx(args, cfg, specs, wl, dev, rank, peak, fmt=0):
-    """An MX serving view (fmt 0: MXFP8, 1: MXFP4) of the same model and step:
-    whole-model pulse_mx_encode_multi + pulse_mx_apply_multi_device, timed
-    like the BF16 step (previous view and receiver restored untimed before
-    each step). The BF16 patch buffers are reused for the code segments."""
+    """A low-precision serving view (fmt 0: MXFP8, 1: MXFP4, 2: NVFP4) of the
+    same model and step: whole-model encode (pulse_mx_encode_multi, or
+    pulse_nvfp4_encode_multi: tensor maxima pass + encode) and
+    pulse_mx_apply_multi_device, timed like the BF16 step (previous view and
+    receiver restored untimed before each step). The BF16 patch buffers are
+    reused for the code segments."""
     import rl_post_trainer_gb300 as pulse
     n = wl.n
-    name = "MXFP8" if fmt == pulse.MX_E4M3 else "MXFP4"
+    name = {pulse.MX_E4M3: "MXFP8", pulse.MX_E2M1: "MXFP4", pulse.MX_NVFP4: "NVFP4"}[fmt]
     epb = 1 if fmt == pulse.MX_E4M3 else 2   # elements per code byte
     stream = torch.cuda.current_stream(dev)
     # the view before the step: the same generator sequence as the workload
@@ -471,7 +474,11 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak, fmt=0):
     for spec in specs:
         w0 = tmp[:spec.numel]
         workloads.torch_init_(w0, spec, gen)
-        c, sc = pulse.mx_quantize(w0, fmt=fmt)
+        if fmt == pulse.MX_NVFP4:
+            c, sc, _ = pulse.nvfp4_quantize(w0)
+            c, sc = c.clone(), sc.clone()
+        else:
+            c, sc = pulse.mx_quantize(w0, fmt=fmt)
         c0.append(c)
         s0.append(sc)
         workloads.torch_update_(w0, cfg["eta"], gen)   # advances the generator past z
@@ -480,7 +487,7 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak, fmt=0):
     prev_s = [x.clone() for x in s0]
     codes = [c.clone() for c in c0]
     scales = [x.clone() for x in s0]
-    nb = [pulse.mx_blocks(s.numel) for s in specs]
+    nb = [pulse.mx_scale_count(s.numel, fmt) for s in specs]
     sidx = [torch.empty(max(b, 1), dtype=torch.int32, device=dev) for b in nb]
     sval = [torch.empty(max(b, 1), dtype=torch.uint8, device=dev) for b in nb]
     plan = pulse.MxPlan([pulse.MxTensorSlot(s.numel, master=wl.master[i], prev_codes=prev_c[i],
@@ -539,16 +546,23 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak, fmt=0):
                     sc_codes += val
     nblocks = float(sum(nb))
     e_s, a_s = float(np.mean(te)), float(np.mean(ta))
-    view = (4.0 + 1.0 / epb) * n + nblocks  # master read + previous view read
+    # master read (twice for NVFP4: the tensor maxima first) + previous view read
+    view = (4.0 + 1.0 / epb) * n + nblocks + (4.0 * n if fmt == pulse.MX_NVFP4 else 0.0)
     enc_alg = view + 6.0 * k + 6.0 * ks
     enc_sec = view + 32.0 * (sc_codes + sc_scales) + 5.0 * k + 5.0 * ks
     app_rmw = 5.0 * (k + ks) + 64.0 * (sc_codes + sc_scales)
     plan.close()
-    model = "5n" if epb == 1 else "4.5n"
+    model = {pulse.MX_E4M3: "5n + n/32", pulse.MX_E2M1: "4.5n + n/32",
+             pulse.MX_NVFP4: "8.5n + n/16"}[fmt]
+    fmt_name = {
+        pulse.MX_E4M3: "MXFP8 (E4M3 codes, E8M0 scale per 32 elements)",
+        pulse.MX_E2M1: "MXFP4 (E2M1 codes two per byte, E8M0 scale per 32 elements; code entries "
+                       "are bytes)",
+        pulse.MX_NVFP4: "NVFP4 (E2M1 codes two per byte, E4M3 scale per 16 elements, FP32 scale "
+                        "per tensor; code entries are bytes; encode includes the tensor-maximum "
+                        "pass)"}[fmt]
     return {
-        "format": ("MXFP8 (E4M3 codes, E8M0 scale per 32 elements)" if epb == 1 else
-                   "MXFP4 (E2M1 codes two per byte, E8M0 scale per 32 elements; code entries "
-                   "are bytes)"),
+        "format": fmt_name,
         "encode_ms": 1e3 * e_s, "apply_ms": 1e3 * a_s,
         "params_per_s": n / (e_s + a_s),
         "code_density": k / (n / epb), "scale_density": ks / nblocks,
@@ -558,8 +572,8 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak, fmt=0):
         "encode_frac_measured_peak": enc_alg / e_s / 1e9 / peak,
         "encode_frac_sector_measured_peak": enc_sec / e_s / 1e9 / peak,
         "apply_gbs_sector_rmw": app_rmw / a_s / 1e9,
-        "bytes_model": f"encode {model} + n/32 + 6k + 6ks (sector: {model} + n/32 + 32S + 5k + 5ks)",
-        "gpu_launches": 2 * args.steps,
+        "bytes_model": f"encode {model} + 6k + 6ks (sector: {model} + 32S + 5k + 5ks)",
+        "gpu_launches": (3 if fmt == pulse.MX_NVFP4 else 2) * args.steps,
     }
 
 
@@ -959,7 +973,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-xor", action="store_true")
-    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8- and MXFP4-view legs")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8-, MXFP4- and NVFP4-view legs")
     ap.add_argument("--no-compose", action="store_true", help="skip the patch-chain leg")
     ap.add_argument("--no-loco", action="store_true", help="skip the PULSELoCo leg")
     ap.add_argument("--no-pack", action="store_true", help="skip the index-packing leg")

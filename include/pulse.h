@@ -617,7 +617,9 @@ int pulse_mx_plan_get_error(pulse_mx_plan *plan);
 #define PULSE_MX_E4M3 0  /* MXFP8: one E4M3 code per byte */
 #define PULSE_MX_E2M1 1  /* MXFP4: two E2M1 codes per byte */
 
-/* Errors as the MXFP8 calls, plus PULSE_ERR_INVALID for an unknown format. */
+/* Errors as the MXFP8 calls, plus PULSE_ERR_INVALID for an unknown format.
+ * The quantize and encode forms take PULSE_MX_E4M3 or PULSE_MX_E2M1 (NVFP4
+ * has its own entry points below); apply and plans take all three. */
 int pulse_mx_quantize_fmt(int format, const float *master_f32, uint64_t n, uint8_t *codes_out,
                           uint8_t *scales_out, cudaStream_t stream);
 int pulse_mx_encode_fmt(int format, const float *master_f32, uint8_t *prev_codes,
@@ -629,9 +631,52 @@ int pulse_mx_apply_fmt(int format, uint8_t *codes, uint8_t *scales, uint64_t n,
                        const uint32_t *sidx, const uint8_t *sval, uint64_t scount,
                        cudaStream_t stream);
 /* A plan of one format: prev_codes, codes, idx and val of each tensor hold
- * code bytes (ceil(n / 2) for E2M1). */
+ * code bytes (ceil(n / 2) for E2M1 and NVFP4); prev_scales, scales, sidx and
+ * sval hold block scales (ceil(n / 16) for NVFP4). */
 int pulse_mx_plan_create_fmt(const pulse_mx_tensor *tensors, int ntensors, int format,
                              pulse_mx_plan **plan_out);
+
+/* ------------------------------------------------------------------------
+ * NVFP4 serving view. [TALK] 13:06-14:00 names NVFP4 serving and its
+ * hierarchical scales; [XOR] section "Bildirilen sayilar" uses an NVFP4
+ * checkpoint as its workload (0.085 % of it changes per step). The pages do
+ * not define the format; this library reads it as the publicly described
+ * NVFP4 layout, with every scale step one FP32 operation rounded to nearest
+ * even, in this order:
+ *  - A = the tensor's largest finite magnitude; tensor scale S = A / 2688
+ *    (2688 = 448 * 6);
+ *  - blocks of 16 consecutive elements; a block holding a NaN or an infinity
+ *    gets scale byte 0x7F and codes 0; otherwise the block scale byte is the
+ *    E4M3 (round to nearest even, clamped to 448) of (max |v| / 6) / S, and
+ *    0 when S is 0;
+ *  - element codes: E2M1 (as in the MXFP4 view, two per byte, element 2j in
+ *    the low nibble) of v * (1 / (dec(scale byte) * S)); all 0 when the
+ *    scale byte is 0 or that product is 0 or its reciprocal is not finite.
+ * A view is codes (ceil(n / 2) bytes), block scales (ceil(n / 16) bytes)
+ * and S. A patch lists changed code bytes and changed block scales (as the
+ * MX patches) and carries the new S (4 bytes of metadata per tensor). Apply
+ * with pulse_mx_apply_fmt(PULSE_MX_NVFP4, ...) or an NVFP4 plan's
+ * pulse_mx_apply_multi*, and take S from the patch.
+ * ---------------------------------------------------------------------- */
+#define PULSE_MX_NVFP4 2  /* NVFP4: E2M1 codes, E4M3 scale per 16, FP32 scale per tensor */
+
+/* The NVFP4 view of one tensor; tscale_out: device, one float (S). Two
+ * launches (the tensor maximum, then the view). Errors as pulse_mx_quantize. */
+int pulse_nvfp4_quantize(const float *master_f32, uint64_t n, uint8_t *codes_out,
+                         uint8_t *scales_out, float *tscale_out, cudaStream_t stream);
+
+/* As pulse_mx_encode for the NVFP4 view; tscale_out (device, one float)
+ * receives the new view's S. The tensor maximum is one extra pass over
+ * master_f32 before the encode launch. */
+int pulse_nvfp4_encode(const float *master_f32, uint8_t *prev_codes, uint8_t *prev_scales,
+                       uint64_t n, uint32_t *idx_out, uint8_t *val_out, uint32_t *sidx_out,
+                       uint8_t *sval_out, uint64_t *counts_out, float *tscale_out,
+                       cudaStream_t stream);
+
+/* Whole-model NVFP4 encode on a plan created with PULSE_MX_NVFP4 (which
+ * pulse_mx_encode_multi refuses); tscales_out: device, ntensors floats. */
+int pulse_nvfp4_encode_multi(pulse_mx_plan *plan, uint64_t *counts_out, float *tscales_out,
+                             cudaStream_t stream);
 
 /*
  * pulse_encode_noalloc -- pulse_encode for callers that must not allocate

@@ -13,7 +13,8 @@
  *  [TALK]  "Taking Reinforcement Learning Cross Datacenter" -- Nan Jiang,
  *          Modal (talk transcript), 13:06-14:00: rollouts are served in NVFP4;
  *          NVFP4 has hierarchical scales, and the same sparsity is observed.
- *  [XOR]   humansand.ai summary "GPU agirlik isinlanmasi ...": the proxy
+ *  [XOR]   humansand.ai summary "GPU agirlik isinlanmasi ...", section
+ *          "Bildirilen sayilar": the proxy
  *          workload is an NVFP4 checkpoint of which 0.085 % changes per step.
  *  The pages name the format but do not define it. The reading below is the
  *  publicly described NVFP4 layout (NVIDIA's Blackwell microscaling format):

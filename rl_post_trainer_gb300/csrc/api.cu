@@ -37,6 +37,7 @@ constexpr uint64_t kMaxElems = 0xFFFFFFFFull;      // n < 2^32 (uint32 indices)
 constexpr uint64_t kMaxTiles = 0x7FFFFFFFull;      // tile tickets are uint32
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s per bounded wait
 constexpr size_t kCounterBytes = 256;               // ticket, finished, error (+ padding)
+constexpr int kAmaxWord = 8;  // counters word holding a single-tensor NVFP4 maximum
 constexpr int kMaxTensorsPerApplyLaunch = 16384;     // bound on the apply kernel's smem table
 
 uint64_t div_up(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
@@ -216,10 +217,20 @@ MxTensorDesc make_mx_desc(const pulse_mx_tensor& t, uint64_t tile_begin) {
 }
 
 // Clear the status words of `tiles` tiles, then launch the MX encode.
+// NVFP4 (amax_scratch: ntensors words): the tensor maxima first, into the
+// scratch the encode reads.
 int launch_encode_mx_ws(MxLaunch& a, int format, Workspace& ws, bool multi, int device,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, uint32_t* amax_scratch = nullptr) {
   int st = workspace_reserve(ws, a.total_tiles, stream);
   if (st != PULSE_OK) return st;
+  if (format == PULSE_MX_NVFP4) {
+    if (amax_scratch == nullptr) amax_scratch = ws.counters + kAmaxWord;
+    if (cudaMemsetAsync(amax_scratch, 0, sizeof(uint32_t) * size_t(a.ntensors), stream) !=
+            cudaSuccess ||
+        launch_mx_amax(a, multi, amax_scratch, stream) != cudaSuccess)
+      return PULSE_ERR_CUDA;
+    a.amax_bits = amax_scratch;
+  }
   if (cudaMemsetAsync(ws.status, 0, a.total_tiles * sizeof(uint64_t), stream) != cudaSuccess)
     return PULSE_ERR_CUDA;
   a.status = ws.status;
@@ -368,6 +379,7 @@ struct pulse_loco_plan {
 struct pulse_mx_plan {
   int device = 0;
   int format = PULSE_MX_E4M3;
+  uint32_t* amax = nullptr;         // NVFP4: device, ntensors (tensor maxima)
   int ntensors = 0;
   uint64_t total_tiles = 0;
   bool can_encode = false, can_apply = false;
@@ -1171,18 +1183,55 @@ int pulse_compose_multi(const pulse_compose_segment* segs, int nsegs, int value_
 // ------------------------------------------------------------ MXFP8 view
 
 namespace {
-bool mx_format_ok(int format) { return format == PULSE_MX_E4M3 || format == PULSE_MX_E2M1; }
-// code bytes of an n-element view
-uint64_t mx_code_bytes(int format, uint64_t n) { return format == PULSE_MX_E2M1 ? div_up(n, 2) : n; }
+bool mx_format_ok(int format) {
+  return format == PULSE_MX_E4M3 || format == PULSE_MX_E2M1 || format == PULSE_MX_NVFP4;
+}
+// code bytes and block scales of an n-element view
+uint64_t mx_code_bytes(int format, uint64_t n) { return format == PULSE_MX_E4M3 ? n : div_up(n, 2); }
+uint64_t mx_scale_count(int format, uint64_t n) {
+  return div_up(n, format == PULSE_MX_NVFP4 ? 16 : kMxBlock);
+}
 }  // namespace
 
 int pulse_mx_quantize_fmt(int format, const float* master_f32, uint64_t n, uint8_t* codes_out,
                           uint8_t* scales_out, cudaStream_t stream) {
-  if (!mx_format_ok(format)) return PULSE_ERR_INVALID;
+  if (!mx_format_ok(format) || format == PULSE_MX_NVFP4) return PULSE_ERR_INVALID;
   if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
   if (n == 0) return PULSE_OK;
   if (master_f32 == nullptr || codes_out == nullptr || scales_out == nullptr) return PULSE_ERR_INVALID;
-  return cuda_status(launch_mx_quantize(format, master_f32, n, codes_out, scales_out, stream));
+  return cuda_status(
+      launch_mx_quantize(format, master_f32, n, codes_out, scales_out, nullptr, nullptr, stream));
+}
+
+int pulse_nvfp4_quantize(const float* master_f32, uint64_t n, uint8_t* codes_out,
+                         uint8_t* scales_out, float* tscale_out, cudaStream_t stream) {
+  if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
+  if (tscale_out == nullptr) return PULSE_ERR_INVALID;
+  if (n == 0) return cuda_status(cudaMemsetAsync(tscale_out, 0, sizeof(float), stream));
+  if (master_f32 == nullptr || codes_out == nullptr || scales_out == nullptr) return PULSE_ERR_INVALID;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
+  uint32_t* amax = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    Workspace* ws = stream_mx_workspace(device, stream);
+    if (ws == nullptr) return PULSE_ERR_NOMEM;
+    const int st = workspace_reserve(*ws, 0, stream);
+    if (st != PULSE_OK) return st;
+    amax = ws->counters + kAmaxWord;
+  }
+  pulse_mx_tensor t{};
+  t.master = master_f32;
+  t.n = n;
+  MxLaunch a{};
+  a.one = make_mx_desc(t, 0);
+  a.ntensors = 1;
+  a.total_tiles = div_up(n, kEncTile);
+  if (cudaMemsetAsync(amax, 0, sizeof(uint32_t), stream) != cudaSuccess ||
+      launch_mx_amax(a, false, amax, stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
+  return cuda_status(launch_mx_quantize(PULSE_MX_NVFP4, master_f32, n, codes_out, scales_out, amax,
+                                        tscale_out, stream));
 }
 
 int pulse_mx_quantize(const float* master_f32, uint64_t n, uint8_t* codes_out, uint8_t* scales_out,
@@ -1190,17 +1239,21 @@ int pulse_mx_quantize(const float* master_f32, uint64_t n, uint8_t* codes_out, u
   return pulse_mx_quantize_fmt(PULSE_MX_E4M3, master_f32, n, codes_out, scales_out, stream);
 }
 
-int pulse_mx_encode_fmt(int format, const float* master_f32, uint8_t* prev_codes,
-                        uint8_t* prev_scales, uint64_t n, uint32_t* idx_out, uint8_t* val_out,
-                        uint32_t* sidx_out, uint8_t* sval_out, uint64_t* counts_out,
-                        cudaStream_t stream) {
-  if (!mx_format_ok(format)) return PULSE_ERR_INVALID;
+namespace {
+int mx_encode_one(int format, const float* master_f32, uint8_t* prev_codes, uint8_t* prev_scales,
+                  uint64_t n, uint32_t* idx_out, uint8_t* val_out, uint32_t* sidx_out,
+                  uint8_t* sval_out, uint64_t* counts_out, float* tscale_out, cudaStream_t stream) {
   if (n >= kMaxElems + 1) return PULSE_ERR_RANGE;
   if (counts_out == nullptr) return PULSE_ERR_INVALID;
   if (n > 0 && (master_f32 == nullptr || prev_codes == nullptr || prev_scales == nullptr ||
                 idx_out == nullptr || val_out == nullptr || sidx_out == nullptr || sval_out == nullptr))
     return PULSE_ERR_INVALID;
-  if (n == 0) return cuda_status(cudaMemsetAsync(counts_out, 0, 2 * sizeof(uint64_t), stream));
+  if (n == 0) {
+    if (tscale_out != nullptr &&
+        cudaMemsetAsync(tscale_out, 0, sizeof(float), stream) != cudaSuccess)
+      return PULSE_ERR_CUDA;
+    return cuda_status(cudaMemsetAsync(counts_out, 0, 2 * sizeof(uint64_t), stream));
+  }
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PULSE_ERR_CUDA;
   pulse_mx_tensor t{};
@@ -1219,10 +1272,30 @@ int pulse_mx_encode_fmt(int format, const float* master_f32, uint8_t* prev_codes
   a.counts_out = counts_out;
   a.first_ticket = 0;
   a.wait_limit_ns = kDefaultWaitNs;
+  a.tscale_out = tscale_out;
   std::lock_guard<std::mutex> lock(g_ws_mu);
   Workspace* ws = stream_mx_workspace(device, stream);
   if (ws == nullptr) return PULSE_ERR_NOMEM;
   return launch_encode_mx_ws(a, format, *ws, false, device, stream);
+}
+}  // namespace
+
+int pulse_mx_encode_fmt(int format, const float* master_f32, uint8_t* prev_codes,
+                        uint8_t* prev_scales, uint64_t n, uint32_t* idx_out, uint8_t* val_out,
+                        uint32_t* sidx_out, uint8_t* sval_out, uint64_t* counts_out,
+                        cudaStream_t stream) {
+  if (!mx_format_ok(format) || format == PULSE_MX_NVFP4) return PULSE_ERR_INVALID;
+  return mx_encode_one(format, master_f32, prev_codes, prev_scales, n, idx_out, val_out, sidx_out,
+                       sval_out, counts_out, nullptr, stream);
+}
+
+int pulse_nvfp4_encode(const float* master_f32, uint8_t* prev_codes, uint8_t* prev_scales,
+                       uint64_t n, uint32_t* idx_out, uint8_t* val_out, uint32_t* sidx_out,
+                       uint8_t* sval_out, uint64_t* counts_out, float* tscale_out,
+                       cudaStream_t stream) {
+  if (tscale_out == nullptr) return PULSE_ERR_INVALID;
+  return mx_encode_one(PULSE_MX_NVFP4, master_f32, prev_codes, prev_scales, n, idx_out, val_out,
+                       sidx_out, sval_out, counts_out, tscale_out, stream);
 }
 
 int pulse_mx_encode(const float* master_f32, uint8_t* prev_codes, uint8_t* prev_scales, uint64_t n,
@@ -1256,7 +1329,7 @@ int pulse_mx_apply_fmt(int format, uint8_t* codes, uint8_t* scales, uint64_t n,
       cudaSuccess)
     return PULSE_ERR_CUDA;
   return cuda_status(
-      launch_apply_u8(scales, div_up(n, kMxBlock), true, sidx, sval, scount, err, stream));
+      launch_apply_u8(scales, mx_scale_count(format, n), true, sidx, sval, scount, err, stream));
 }
 
 int pulse_mx_apply(uint8_t* codes, uint8_t* scales, uint64_t n, const uint32_t* idx,
@@ -1296,7 +1369,7 @@ int pulse_mx_plan_create_fmt(const pulse_mx_tensor* tensors, int ntensors, int f
     p->host_desc.push_back(make_mx_desc(t, tiles));
     tiles += div_up(t.n, kEncTile);
     segs[2 * size_t(i)] = ByteSegment{t.codes, t.idx, t.val, mx_code_bytes(format, t.n)};
-    segs[2 * size_t(i) + 1] = ByteSegment{t.scales, t.sidx, t.sval, div_up(t.n, kMxBlock)};
+    segs[2 * size_t(i) + 1] = ByteSegment{t.scales, t.sidx, t.sval, mx_scale_count(format, t.n)};
     if (t.n > 0) {
       p->can_encode = p->can_encode && t.master && t.prev_codes && t.prev_scales && t.idx &&
                       t.val && t.sidx && t.sval;
@@ -1317,7 +1390,9 @@ int pulse_mx_plan_create_fmt(const pulse_mx_tensor* tensors, int ntensors, int f
   if (cudaMalloc(&p->desc, desc_bytes) != cudaSuccess ||
       cudaMalloc(&p->tile_begin, tb_bytes) != cudaSuccess ||
       cudaMalloc(&p->segs, seg_bytes) != cudaSuccess ||
-      cudaMalloc(&p->counts, cnt_bytes) != cudaSuccess) {
+      cudaMalloc(&p->counts, cnt_bytes) != cudaSuccess ||
+      (format == PULSE_MX_NVFP4 &&
+       cudaMalloc(&p->amax, sizeof(uint32_t) * size_t(ntensors)) != cudaSuccess)) {
     st = PULSE_ERR_NOMEM;
   } else if (cudaMemcpy(p->desc, p->host_desc.data(), desc_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
              cudaMemcpy(p->tile_begin, tb.data(), tb_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
@@ -1347,6 +1422,7 @@ int pulse_mx_plan_destroy(pulse_mx_plan* plan) {
   if (plan->tile_begin) cudaFree(plan->tile_begin);
   if (plan->segs) cudaFree(plan->segs);
   if (plan->counts) cudaFree(plan->counts);
+  if (plan->amax) cudaFree(plan->amax);
   workspace_free(plan->ws);
   delete plan;
   return cuda_status(e);
@@ -1354,8 +1430,12 @@ int pulse_mx_plan_destroy(pulse_mx_plan* plan) {
 
 int pulse_mx_plan_num_tensors(const pulse_mx_plan* plan) { return plan ? plan->ntensors : 0; }
 
-int pulse_mx_encode_multi(pulse_mx_plan* plan, uint64_t* counts_out, cudaStream_t stream) {
-  if (plan == nullptr || counts_out == nullptr || !plan->can_encode) return PULSE_ERR_INVALID;
+namespace {
+int mx_encode_plan(pulse_mx_plan* plan, uint64_t* counts_out, float* tscales_out,
+                   cudaStream_t stream) {
+  if (tscales_out != nullptr &&
+      cudaMemsetAsync(tscales_out, 0, sizeof(float) * size_t(plan->ntensors), stream) != cudaSuccess)
+    return PULSE_ERR_CUDA;
   if (plan->total_tiles == 0)
     return cuda_status(
         cudaMemsetAsync(counts_out, 0, 2 * sizeof(uint64_t) * size_t(plan->ntensors), stream));
@@ -1367,7 +1447,24 @@ int pulse_mx_encode_multi(pulse_mx_plan* plan, uint64_t* counts_out, cudaStream_
   a.counts_out = counts_out;
   a.first_ticket = 0;
   a.wait_limit_ns = kDefaultWaitNs;
-  return launch_encode_mx_ws(a, plan->format, plan->ws, true, plan->device, stream);
+  a.tscale_out = tscales_out;
+  return launch_encode_mx_ws(a, plan->format, plan->ws, true, plan->device, stream, plan->amax);
+}
+}  // namespace
+
+int pulse_mx_encode_multi(pulse_mx_plan* plan, uint64_t* counts_out, cudaStream_t stream) {
+  if (plan == nullptr || counts_out == nullptr || !plan->can_encode ||
+      plan->format == PULSE_MX_NVFP4)
+    return PULSE_ERR_INVALID;
+  return mx_encode_plan(plan, counts_out, nullptr, stream);
+}
+
+int pulse_nvfp4_encode_multi(pulse_mx_plan* plan, uint64_t* counts_out, float* tscales_out,
+                             cudaStream_t stream) {
+  if (plan == nullptr || counts_out == nullptr || tscales_out == nullptr || !plan->can_encode ||
+      plan->format != PULSE_MX_NVFP4)
+    return PULSE_ERR_INVALID;
+  return mx_encode_plan(plan, counts_out, tscales_out, stream);
 }
 
 int pulse_mx_apply_multi_device(pulse_mx_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {

@@ -35,32 +35,42 @@ namespace {
 
 using namespace enc;
 
-constexpr int kTileBlocks = kEncTile / kMxBlock;                   // 128
 constexpr uint32_t kStageMasterBytes = kEncTile * 4;               // 16 KB
-constexpr uint32_t kStageScaleBytes = kTileBlocks;                 // 128 B
+constexpr int kMaxTileBlocks = kEncTile / 16;                      // blocks of the smallest size
 
 // Element formats: F = kFmtE4M3 (MXFP8, one code byte per element) or
 // kFmtE2M1 (MXFP4, two codes per byte, element 2j in the low nibble of byte
 // j). kEmax: exponent of the format's largest normal (448 = 1.75 * 2^8,
 // 6 = 1.5 * 2^2).
+// kBlock: elements per block scale. NVFP4 (kFmtNvfp4): E2M1 codes two per
+// byte under an E4M3 scale per 16 elements and an FP32 scale per tensor.
 template <int F>
 struct Fmt;
 template <>
 struct Fmt<kFmtE4M3> {
   static constexpr uint32_t kEmax = 8;
   static constexpr uint32_t kElemsPerByte = 1;
+  static constexpr uint32_t kBlock = 32;
 };
 template <>
 struct Fmt<kFmtE2M1> {
   static constexpr uint32_t kEmax = 2;
   static constexpr uint32_t kElemsPerByte = 2;
+  static constexpr uint32_t kBlock = 32;
+};
+template <>
+struct Fmt<kFmtNvfp4> {
+  static constexpr uint32_t kEmax = 0;  // unused: the block scale is an E4M3 value
+  static constexpr uint32_t kElemsPerByte = 2;
+  static constexpr uint32_t kBlock = 16;
 };
 // Stage layout of a tile for format F: master, previous code bytes,
 // previous scales.
 template <int F>
 struct Stage {
   static constexpr uint32_t kCodeBytes = kEncTile / Fmt<F>::kElemsPerByte;
-  static constexpr uint32_t kBytes = kStageMasterBytes + kCodeBytes + kStageScaleBytes;
+  static constexpr uint32_t kScaleBytes = kEncTile / Fmt<F>::kBlock;  // one per block
+  static constexpr uint32_t kBytes = kStageMasterBytes + kCodeBytes + kScaleBytes;
   static constexpr size_t kDynSmem = size_t(kEncStages) * kBytes + size_t(kEncRing) * 4 + 128;
   static_assert(kBytes % 128 == 0, "stages stay 128-byte aligned");
 };
@@ -113,6 +123,7 @@ struct StageMeta {
   uint32_t tensor;
   uint32_t mode;
   uint32_t len;  // elements in the tile
+  float tscale;  // NVFP4: the tensor's FP32 scale
   uint64_t base;
   uint64_t first;
   uint64_t n;
@@ -137,6 +148,8 @@ struct ParkedMeta {
   uint64_t base;
   uint64_t code_base;  // code-byte index of the tile's first element
   uint64_t code_cap;   // code bytes of the tensor (the code segment's room)
+  uint64_t scale_base; // block index of the tile's first element
+  uint64_t scale_cap;  // blocks of the tensor (the scale segment's room)
   uint32_t* idx;
   uint8_t* val;
   uint32_t* sidx;
@@ -153,7 +166,7 @@ struct __align__(16) MxShared {
   uint32_t warp_tot[2][kWarps];   // per warp: changed codes per round, one byte each
   uint32_t warp_stot[2][kWarps];  // per warp: changed scales per round, one byte each
   uint32_t ring_tail;
-  uint16_t sring[kPendSlots][kTileBlocks];  // parked scale entries: block | scale << 8
+  uint16_t sring[kPendSlots][kMaxTileBlocks];  // parked scale entries: block | scale << 8
 };
 static_assert(kEncLookbackWarps == 1, "parked tiles are freed in order by one look-back warp");
 
@@ -167,6 +180,11 @@ __device__ __forceinline__ void producer_loop(const MxLaunch& a, MxShared& sh, u
   uint32_t cur_t = 0;
   uint64_t cur_begin = 1, cur_end = 0;
   MxTensorDesc d = a.one;
+  // NVFP4: S = (largest finite magnitude of the tensor) / 2688, FP32
+  auto tensor_scale = [&](uint32_t t) {
+    return F == kFmtNvfp4 ? __fdiv_rn(__uint_as_float(a.amax_bits[t]), 2688.0f) : 0.0f;
+  };
+  float cur_s = tensor_scale(0);
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kEncStages);
     const bool end = ticket >= a.total_tiles;
@@ -188,12 +206,15 @@ __device__ __forceinline__ void producer_loop(const MxLaunch& a, MxShared& sh, u
         d = a.tensors[cur_t];
         cur_begin = d.tile_begin;
         cur_end = __ldg(a.tile_begin + cur_t + 1);
+        cur_s = tensor_scale(cur_t);
       }
     }
+    if (F == kFmtNvfp4 && uint64_t(ticket) == d.tile_begin) a.tscale_out[cur_t] = cur_s;
     const uint64_t base = (uint64_t(ticket) - d.tile_begin) * kEncTile;
     const uint64_t len = d.n - base < uint64_t(kEncTile) ? d.n - base : uint64_t(kEncTile);
     m.tensor = cur_t;
     m.len = uint32_t(len);
+    m.tscale = cur_s;
     m.base = base;
     m.first = d.tile_begin;
     m.n = d.n;
@@ -212,8 +233,8 @@ __device__ __forceinline__ void producer_loop(const MxLaunch& a, MxShared& sh, u
       bulk_g2s(st, d.master + base, kStageMasterBytes, &sh.full[s], pol_stream);
       bulk_g2s_plain(st + kStageMasterBytes, d.prev_codes + base / Fmt<F>::kElemsPerByte,
                      kStageCodeBytes, &sh.full[s]);
-      bulk_g2s_plain(st + kStageMasterBytes + kStageCodeBytes, d.prev_scales + base / kMxBlock,
-                     kStageScaleBytes, &sh.full[s]);
+      bulk_g2s_plain(st + kStageMasterBytes + kStageCodeBytes, d.prev_scales + base / Fmt<F>::kBlock,
+                     Stage<F>::kScaleBytes, &sh.full[s]);
     } else {
       m.mode = kModeGeneric;
       sh.meta[s] = m;
@@ -275,8 +296,8 @@ __device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix_c
       pm.val[pos] = uint8_t(ent >> 16);
     }
   }
-  const uint64_t nblocks = (pm.n + kMxBlock - 1) / kMxBlock;
-  const uint32_t block_base = uint32_t(pm.base / kMxBlock);
+  const uint64_t nblocks = pm.scale_cap;
+  const uint32_t block_base = uint32_t(pm.scale_base);
   for (uint32_t k = uint32_t(lane); k < pm.agg_s; k += 32) {
     const uint32_t ent = sring[k];
     const uint64_t pos = uint64_t(prefix_s) + k;
@@ -352,7 +373,6 @@ __device__ __forceinline__ void lookback_loop(const MxLaunch& a, MxShared& sh, c
 constexpr int kMxPerThread = 8;
 constexpr int kMxRounds = kEncTile / (kEncThreads * kMxPerThread);  // 2
 static_assert(kMxRounds == 2, "two rounds pack into the 16-bit fields of one word");
-constexpr int kLanesPerBlock = kMxBlock / kMxPerThread;             // 4
 
 // Largest magnitude of 8 values; NaN if any of them is NaN.
 __device__ __forceinline__ float abs_max_nan(float a, float b) {
@@ -382,6 +402,59 @@ __device__ __forceinline__ uint32_t block_scale8(const float4& a, const float4& 
   return e == 255u ? 0xFFu : (e > EMAX ? e - EMAX : 0u);
 }
 
+// ------------------------------------------------------------ NVFP4 pieces
+// Every step is one FP32 operation rounded to nearest even, in this order.
+
+// E4M3 code of a non-negative finite u: round to nearest even, values past
+// 448 clamped to 448 (the saturating hardware convert).
+__device__ __forceinline__ uint32_t e4m3_of(float u) {
+  return cvt_e4m3x2(0.0f, u) & 0xFFu;
+}
+
+// Value of an E4M3 code (exact: E4M3 -> f16 -> f32).
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(uint16_t(c)));
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(uint16_t(h2 & 0xFFFFu)));
+  return f;
+}
+
+// Block scale byte of the 16-element block this thread's 8 elements belong
+// to (lanes 2b, 2b+1 hold block b) under tensor scale ts: 0x7F for a block
+// holding a NaN or an infinity, 0 when ts is 0, else E4M3((amax / 6) / ts).
+// All 32 lanes must call.
+__device__ __forceinline__ uint32_t nv_block_scale8(const float4& a, const float4& b, float ts) {
+  float m = max_nan(max_nan(abs_max_nan(a.x, a.y), abs_max_nan(a.z, a.w)),
+                    max_nan(abs_max_nan(b.x, b.y), abs_max_nan(b.z, b.w)));
+  m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  if ((__float_as_uint(m) >> 23) == 255u) return 0x7Fu;
+  if (ts == 0.0f) return 0u;
+  return e4m3_of(__fdiv_rn(__fdiv_rn(m, 6.0f), ts));
+}
+
+// Codes of 8 elements under block scale byte d and tensor scale ts: the
+// E2M1 of v * (1 / (dec(d) * ts)); all 0 when the block has no usable scale.
+__device__ __forceinline__ uint32_t nv_codes8(const float4& a, const float4& b, uint32_t d, float ts) {
+  if (d == 0x7Fu || d == 0u) return 0u;
+  const float x = __fmul_rn(e4m3_value(d), ts);
+  if (x == 0.0f) return 0u;
+  const float r = __frcp_rn(x);
+  if (!isfinite(r)) return 0u;
+  uint32_t q;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+      : "=r"(q)
+      : "f"(__fmul_rn(a.x, r)), "f"(__fmul_rn(a.y, r)), "f"(__fmul_rn(a.z, r)),
+        "f"(__fmul_rn(a.w, r)), "f"(__fmul_rn(b.x, r)), "f"(__fmul_rn(b.y, r)),
+        "f"(__fmul_rn(b.z, r)), "f"(__fmul_rn(b.w, r)));
+  return q;
+}
+
 // Four change flags in byte order (bit b = byte b) from the 0x80 bytes of
 // nonzero_bytes: the same multiply as gather_flags8 with one word.
 __device__ __forceinline__ uint32_t gather_flags4(uint32_t z) {
@@ -407,7 +480,9 @@ template <int F, bool MULTI>
 __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, uint8_t* stages,
                                              uint32_t* ring, int tid, int lane, int warp) {
   constexpr uint32_t kStageBytes = Stage<F>::kBytes, kStageCodeBytes = Stage<F>::kCodeBytes;
-  constexpr bool kFp4 = F == kFmtE2M1;
+  constexpr bool kFp4 = F != kFmtE4M3;  // two codes per byte
+  constexpr uint32_t kBlock = Fmt<F>::kBlock;
+  constexpr int kLanesPerBlock = int(kBlock) / kMxPerThread;  // 4 or 2
   // code bytes per 8-element group, and change flags per round
   constexpr uint32_t kGroupBytes = kMxPerThread / Fmt<F>::kElemsPerByte;
   uint32_t posted = 0, ring_head = 0;
@@ -462,12 +537,19 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
         v0 = make_float4(mm[0], mm[1], mm[2], mm[3]);
         v1 = make_float4(mm[4], mm[5], mm[6], mm[7]);
         pc = make_uint2(pp[0], pp[1]);
-        if (leader && lb * kMxBlock < len) ps = m.prev_scales[(base / kMxBlock) + lb];
+        if (leader && lb * kBlock < len) ps = m.prev_scales[(base / kBlock) + lb];
       }
-      const uint32_t sb = block_scale8<Fmt<F>::kEmax>(v0, v1);
+      uint32_t sb;
+      if constexpr (F == kFmtNvfp4)
+        sb = nv_block_scale8(v0, v1, m.tscale);
+      else
+        sb = block_scale8<Fmt<F>::kEmax>(v0, v1);
       uint32_t f4;
       if constexpr (kFp4) {
-        nc[j][0] = fp4_codes8(v0, v1, sb);
+        if constexpr (F == kFmtNvfp4)
+          nc[j][0] = nv_codes8(v0, v1, sb, m.tscale);
+        else
+          nc[j][0] = fp4_codes8(v0, v1, sb);
         nc[j][1] = 0u;
         uint32_t z = nonzero_bytes(nc[j][0] ^ pc.x);
         if (!bulk) {
@@ -492,7 +574,7 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
       }
       ns |= sb << (8 * j);
       flags |= f4 << (8 * j);
-      if (leader && lb * kMxBlock < len && sb != ps) sflags |= 1u << j;
+      if (leader && lb * kBlock < len && sb != ps) sflags |= 1u << j;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
@@ -515,7 +597,7 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
             if ((f >> e) & 1u) m.prev_codes[cb + e] = uint8_t(nc[j][e >> 2] >> (8 * (e & 3)));
         }
       }
-      if ((sflags >> j) & 1u) m.prev_scales[base / kMxBlock + li / kMxBlock] = uint8_t(ns >> (8 * j));
+      if ((sflags >> j) & 1u) m.prev_scales[base / kBlock + li / kBlock] = uint8_t(ns >> (8 * j));
     }
 
     // ---- rank. Codes: one warp scan of the two per-round counts in 16-bit
@@ -620,6 +702,8 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
       pm.base = base;
       pm.code_base = base / Fmt<F>::kElemsPerByte;
       pm.code_cap = (m.n + Fmt<F>::kElemsPerByte - 1) / Fmt<F>::kElemsPerByte;
+      pm.scale_base = base / kBlock;
+      pm.scale_cap = (m.n + kBlock - 1) / kBlock;
       pm.idx = m.idx;
       pm.val = m.val;
       pm.sidx = m.sidx;
@@ -723,8 +807,13 @@ constexpr int kQuantThreads = 256;
 template <int F>
 __global__ void __launch_bounds__(kQuantThreads)
     mx_quantize_kernel(const float* __restrict__ master, uint64_t n, uint8_t* __restrict__ codes,
-                       uint8_t* __restrict__ scales) {
+                       uint8_t* __restrict__ scales, const uint32_t* __restrict__ amax_bits,
+                       float* __restrict__ tscale_out) {
   constexpr uint32_t kGroupBytes = kMxPerThread / Fmt<F>::kElemsPerByte;
+  constexpr uint32_t kBlock = Fmt<F>::kBlock;
+  constexpr int kLanesPerBlock = int(kBlock) / kMxPerThread;
+  const float ts = F == kFmtNvfp4 ? __fdiv_rn(__uint_as_float(*amax_bits), 2688.0f) : 0.0f;
+  if (F == kFmtNvfp4 && blockIdx.x == 0 && threadIdx.x == 0) *tscale_out = ts;
   const bool vec = (reinterpret_cast<uintptr_t>(master) % 16u == 0) &&
                    (reinterpret_cast<uintptr_t>(codes) % kGroupBytes == 0);
   const uint64_t groups = (n + kMxPerThread - 1) / kMxPerThread;
@@ -747,9 +836,15 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
     const float4 a = make_float4(v[0], v[1], v[2], v[3]);
     const float4 b = make_float4(v[4], v[5], v[6], v[7]);
-    const uint32_t sb = block_scale8<Fmt<F>::kEmax>(a, b);
-    uint32_t c0, c1;
-    if constexpr (F == kFmtE2M1) {
+    uint32_t sb, c0, c1;
+    if constexpr (F == kFmtNvfp4)
+      sb = nv_block_scale8(a, b, ts);
+    else
+      sb = block_scale8<Fmt<F>::kEmax>(a, b);
+    if constexpr (F == kFmtNvfp4) {
+      c0 = nv_codes8(a, b, sb, ts);
+      c1 = 0u;
+    } else if constexpr (F == kFmtE2M1) {
       c0 = fp4_codes8(a, b, sb);
       c1 = 0u;
     } else {
@@ -758,7 +853,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
     const uint64_t cb = i / Fmt<F>::kElemsPerByte;  // first code byte
     if (full) {
-      if constexpr (F == kFmtE2M1)
+      if constexpr (F != kFmtE4M3)
         *reinterpret_cast<uint32_t*>(codes + cb) = c0;
       else
         *reinterpret_cast<uint2*>(codes + cb) = make_uint2(c0, c1);
@@ -767,7 +862,55 @@ __global__ void __launch_bounds__(kQuantThreads)
         if (i + uint64_t(e) * Fmt<F>::kElemsPerByte < n)
           codes[cb + e] = uint8_t((e < 4 ? c0 : c1) >> (8 * (e & 3)));
     }
-    if ((lane & (kLanesPerBlock - 1)) == 0 && i < n) scales[i / kMxBlock] = uint8_t(sb);
+    if ((lane & (kLanesPerBlock - 1)) == 0 && i < n) scales[i / kBlock] = uint8_t(sb);
+  }
+}
+
+// ------------------------------------------------------------ tensor maxima
+// NVFP4's tensor scale needs each tensor's largest finite magnitude before
+// any block is encoded: one pass over the master, 4096-element tiles, a
+// block maximum per tile and one atomicMax per tile on the bit pattern (a
+// non-negative float orders like its bits). amax_bits is zeroed beforehand.
+constexpr int kAmaxThreads = 256;
+
+template <bool MULTI>
+__global__ void __launch_bounds__(kAmaxThreads)
+    mx_amax_kernel(const MxTensorDesc one, const MxTensorDesc* tensors, const uint64_t* tile_begin,
+                   int ntensors, uint64_t total_tiles, uint32_t* amax_bits) {
+  __shared__ uint32_t wmax[kAmaxThreads / 32];
+  const int tid = threadIdx.x;
+  for (uint64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    const int t = MULTI ? find_tensor(tile_begin, ntensors, tile) : 0;
+    const MxTensorDesc d = MULTI ? tensors[t] : one;
+    const uint64_t base = (tile - d.tile_begin) * kEncTile;
+    const uint32_t len = uint32_t(d.n - base < uint64_t(kEncTile) ? d.n - base : uint64_t(kEncTile));
+    const float* src = d.master + base;
+    const bool vec = (reinterpret_cast<uintptr_t>(src) % 16u) == 0;
+    float m = 0.0f;
+    for (uint32_t k = uint32_t(tid) * 4u; k < len; k += 4u * kAmaxThreads) {
+      float v[4];
+      if (vec && k + 4u <= len) {
+        const float4 q = *reinterpret_cast<const float4*>(src + k);
+        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = k + uint32_t(e) < len ? src[k + e] : 0.0f;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = fabsf(v[e]);
+        if (x <= 3.40282347e38f) m = fmaxf(m, x);  // finite values only (NaN fails the test)
+      }
+    }
+    const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
+    if ((tid & 31) == 0) wmax[tid >> 5] = wm;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t bm = 0;
+      for (int w = 0; w < kAmaxThreads / 32; ++w) bm = bm > wmax[w] ? bm : wmax[w];
+      atomicMax(amax_bits + t, bm);
+    }
+    __syncthreads();
   }
 }
 
@@ -775,7 +918,10 @@ __global__ void __launch_bounds__(kQuantThreads)
 
 int encode_mx_grid_size(int device, int format) {
   int a, b;
-  if (format == kFmtE2M1) {
+  if (format == kFmtNvfp4) {
+    a = encode_mx_blocks_per_sm<kFmtNvfp4, true>();
+    b = encode_mx_blocks_per_sm<kFmtNvfp4, false>();
+  } else if (format == kFmtE2M1) {
     a = encode_mx_blocks_per_sm<kFmtE2M1, true>();
     b = encode_mx_blocks_per_sm<kFmtE2M1, false>();
   } else {
@@ -801,12 +947,29 @@ cudaError_t launch_encode_mx_t(const MxLaunch& a, bool multi, int grid, cudaStre
 
 cudaError_t launch_encode_mx(const MxLaunch& a, int format, bool multi, int grid,
                              cudaStream_t stream) {
+  if (format == kFmtNvfp4) return launch_encode_mx_t<kFmtNvfp4>(a, multi, grid, stream);
   return format == kFmtE2M1 ? launch_encode_mx_t<kFmtE2M1>(a, multi, grid, stream)
                             : launch_encode_mx_t<kFmtE4M3>(a, multi, grid, stream);
 }
 
+cudaError_t launch_mx_amax(const MxLaunch& a, bool multi, uint32_t* amax_bits, cudaStream_t stream) {
+  if (a.total_tiles == 0) return cudaSuccess;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t cap = uint64_t(sm_count(dev)) * 8u;
+  const unsigned grid = unsigned(a.total_tiles < cap ? a.total_tiles : cap);
+  if (multi)
+    mx_amax_kernel<true><<<grid, kAmaxThreads, 0, stream>>>(a.one, a.tensors, a.tile_begin,
+                                                             a.ntensors, a.total_tiles, amax_bits);
+  else
+    mx_amax_kernel<false><<<grid, kAmaxThreads, 0, stream>>>(a.one, a.tensors, a.tile_begin,
+                                                              a.ntensors, a.total_tiles, amax_bits);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_mx_quantize(int format, const float* master, uint64_t n, uint8_t* codes,
-                               uint8_t* scales, cudaStream_t stream) {
+                               uint8_t* scales, const uint32_t* amax_bits, float* tscale_out,
+                               cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t warps = (n + 32 * kMxPerThread - 1) / (32 * kMxPerThread);
@@ -814,10 +977,15 @@ cudaError_t launch_mx_quantize(int format, const float* master, uint64_t n, uint
   const uint64_t cap = uint64_t(sm_count(dev)) * 8u;
   const int grid = int(blocks < cap ? blocks : cap);
   if (grid == 0) return cudaSuccess;
-  if (format == kFmtE2M1)
-    mx_quantize_kernel<kFmtE2M1><<<grid, kQuantThreads, 0, stream>>>(master, n, codes, scales);
+  if (format == kFmtNvfp4)
+    mx_quantize_kernel<kFmtNvfp4><<<grid, kQuantThreads, 0, stream>>>(master, n, codes, scales,
+                                                                      amax_bits, tscale_out);
+  else if (format == kFmtE2M1)
+    mx_quantize_kernel<kFmtE2M1><<<grid, kQuantThreads, 0, stream>>>(master, n, codes, scales,
+                                                                     amax_bits, tscale_out);
   else
-    mx_quantize_kernel<kFmtE4M3><<<grid, kQuantThreads, 0, stream>>>(master, n, codes, scales);
+    mx_quantize_kernel<kFmtE4M3><<<grid, kQuantThreads, 0, stream>>>(master, n, codes, scales,
+                                                                     amax_bits, tscale_out);
   return cudaGetLastError();
 }
 

@@ -120,17 +120,25 @@ struct MxLaunch {
   uint32_t epoch;                // unused (the packed status words carry no epoch)
   uint32_t first_ticket;
   uint64_t wait_limit_ns;
+  const uint32_t* amax_bits;     // NVFP4: per tensor, largest finite magnitude (float bits)
+  float* tscale_out;             // NVFP4: per tensor, the new view's tensor scale
 };
 
 // Element formats of the MX views (values of the public PULSE_MX_* constants).
 constexpr int kFmtE4M3 = 0;  // MXFP8: one E4M3 code per byte
 constexpr int kFmtE2M1 = 1;  // MXFP4: two E2M1 codes per byte, element 2j in the low nibble
+constexpr int kFmtNvfp4 = 2; // NVFP4: E2M1 codes as MXFP4, E4M3 scale per 16, FP32 per tensor
 
 int encode_mx_grid_size(int device, int format);
 cudaError_t launch_encode_mx(const MxLaunch& a, int format, bool multi, int grid,
                              cudaStream_t stream);
+// amax_bits / tscale_out: NVFP4 only (one tensor).
 cudaError_t launch_mx_quantize(int format, const float* master, uint64_t n, uint8_t* codes,
-                               uint8_t* scales, cudaStream_t stream);
+                               uint8_t* scales, const uint32_t* amax_bits, float* tscale_out,
+                               cudaStream_t stream);
+// Per-tensor largest finite magnitude of the launch's tensors into amax_bits
+// (zeroed by the caller), for the NVFP4 tensor scale.
+cudaError_t launch_mx_amax(const MxLaunch& a, bool multi, uint32_t* amax_bits, cudaStream_t stream);
 
 // ---------------------------------------------------------------- PULSELoCo
 struct LocoTensorDesc {

@@ -68,6 +68,7 @@ class PulseMxTensor(ctypes.Structure):
 MX_BLOCK = 32
 MX_E4M3 = 0  # MXFP8 view: one E4M3 code per byte
 MX_E2M1 = 1  # MXFP4 view: two E2M1 codes per byte, element 2j in the low nibble
+MX_NVFP4 = 2  # NVFP4 view: E2M1 codes as MXFP4, E4M3 scale per 16, FP32 scale per tensor
 _U8 = (torch.uint8, torch.int8)
 
 
@@ -78,9 +79,17 @@ def mx_blocks(n: int) -> int:
 
 def mx_code_bytes(n: int, fmt: int = MX_E4M3) -> int:
     """Code bytes of an n-element MX view of format ``fmt``."""
-    if fmt not in (MX_E4M3, MX_E2M1):
+    if fmt not in (MX_E4M3, MX_E2M1, MX_NVFP4):
         raise ValueError(f"unknown MX format {fmt}")
     return int(n) if fmt == MX_E4M3 else (int(n) + 1) // 2
+
+
+def mx_scale_count(n: int, fmt: int = MX_E4M3) -> int:
+    """Block scales of an n-element view of format ``fmt`` (16 elements per
+    scale for NVFP4, 32 for the MX formats)."""
+    mx_code_bytes(n, fmt)  # checks the format
+    block = 16 if fmt == MX_NVFP4 else MX_BLOCK
+    return (int(n) + block - 1) // block
 
 
 class PulseComposeSegment(ctypes.Structure):
@@ -202,6 +211,9 @@ def lib():
             "pulse_mx_encode_fmt": ([I, P, P, P, U64, P, P, P, P, P, P], I),
             "pulse_mx_apply_fmt": ([I, P, P, U64, P, P, U64, P, P, U64, P], I),
             "pulse_mx_plan_create_fmt": ([ctypes.POINTER(PulseMxTensor), I, I, ctypes.POINTER(P)], I),
+            "pulse_nvfp4_quantize": ([P, U64, P, P, P, P], I),
+            "pulse_nvfp4_encode": ([P, P, P, U64, P, P, P, P, P, P, P], I),
+            "pulse_nvfp4_encode_multi": ([P, P, P, P], I),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -637,7 +649,7 @@ def mx_apply(codes: torch.Tensor, scales: torch.Tensor, idx, val, count: int, si
         n = codes.numel() * (1 if fmt == MX_E4M3 else 2)
     n = int(n)
     _need(codes, "codes", _U8, dev, mx_code_bytes(n, fmt))
-    _need(scales, "scales", _U8, dev, mx_blocks(n))
+    _need(scales, "scales", _U8, dev, mx_scale_count(n, fmt))
     count, scount = int(count), int(scount)
     _need(idx, "idx", (torch.int32, torch.uint32), dev, min_numel=count)
     _need(val, "val", _U8, dev, min_numel=count)
@@ -647,6 +659,59 @@ def mx_apply(codes: torch.Tensor, scales: torch.Tensor, idx, val, count: int, si
         st = lib().pulse_mx_apply_fmt(fmt, _ptr(codes), _ptr(scales), n, _ptr(idx), _ptr(val), count,
                                       _ptr(sidx), _ptr(sval), scount, _stream(dev))
     _raise(st, "pulse_mx_apply_fmt")
+
+
+def nvfp4_quantize(master: torch.Tensor):
+    """pulse_nvfp4_quantize: the NVFP4 view (codes uint8[ceil(n/2)], block
+    scales uint8[ceil(n/16)], tensor scale: a 1-element device float32)."""
+    _need(master, "master", (torch.float32,))
+    dev = master.device
+    n = master.numel()
+    codes = torch.empty(max(mx_code_bytes(n, MX_NVFP4), 1), dtype=torch.uint8, device=dev)
+    scales = torch.empty(max(mx_scale_count(n, MX_NVFP4), 1), dtype=torch.uint8, device=dev)
+    ts = torch.empty(1, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().pulse_nvfp4_quantize(_ptr(master), n, _ptr(codes), _ptr(scales), _ptr(ts),
+                                        _stream(dev))
+    _raise(st, "pulse_nvfp4_quantize")
+    return codes[:mx_code_bytes(n, MX_NVFP4)], scales[:mx_scale_count(n, MX_NVFP4)], ts
+
+
+def nvfp4_encode(master: torch.Tensor, prev_codes: torch.Tensor, prev_scales: torch.Tensor,
+                 idx_out=None, val_out=None, sidx_out=None, sval_out=None, counts_out=None,
+                 tscale_out=None):
+    """pulse_nvfp4_encode: returns (idx, val, sidx, sval, counts, tscale);
+    refreshes the previous codes and block scales in place."""
+    _need(master, "master", (torch.float32,))
+    dev = master.device
+    n = master.numel()
+    nb, ncb = mx_scale_count(n, MX_NVFP4), mx_code_bytes(n, MX_NVFP4)
+    _need(prev_codes, "prev_codes", _U8, dev, ncb)
+    _need(prev_scales, "prev_scales", _U8, dev, nb)
+    if idx_out is None:
+        idx_out = torch.empty(max(ncb, 1), dtype=torch.int32, device=dev)
+    if val_out is None:
+        val_out = torch.empty(max(ncb, 1), dtype=torch.uint8, device=dev)
+    if sidx_out is None:
+        sidx_out = torch.empty(max(nb, 1), dtype=torch.int32, device=dev)
+    if sval_out is None:
+        sval_out = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+    if counts_out is None:
+        counts_out = torch.empty(2, dtype=torch.int64, device=dev)
+    if tscale_out is None:
+        tscale_out = torch.empty(1, dtype=torch.float32, device=dev)
+    _need(idx_out, "idx_out", (torch.int32, torch.uint32), dev, min_numel=ncb)
+    _need(val_out, "val_out", _U8, dev, min_numel=ncb)
+    _need(sidx_out, "sidx_out", (torch.int32, torch.uint32), dev, min_numel=nb)
+    _need(sval_out, "sval_out", _U8, dev, min_numel=nb)
+    _need(counts_out, "counts_out", (torch.int64, torch.uint64), dev, min_numel=2)
+    _need(tscale_out, "tscale_out", (torch.float32,), dev, min_numel=1)
+    with torch.cuda.device(dev):
+        st = lib().pulse_nvfp4_encode(_ptr(master), _ptr(prev_codes), _ptr(prev_scales), n,
+                                      _ptr(idx_out), _ptr(val_out), _ptr(sidx_out), _ptr(sval_out),
+                                      _ptr(counts_out), _ptr(tscale_out), _stream(dev))
+    _raise(st, "pulse_nvfp4_encode")
+    return idx_out, val_out, sidx_out, sval_out, counts_out, tscale_out
 
 
 class MxTensorSlot:
@@ -675,7 +740,7 @@ class MxPlan:
         dev = device
         arr = (PulseMxTensor * len(slots))()
         for i, s in enumerate(slots):
-            nb = mx_blocks(s.n)
+            nb = mx_scale_count(s.n, fmt)
             ncb = mx_code_bytes(s.n, fmt)
             checks = (("master", s.master, (torch.float32,), s.n, None),
                       ("prev_codes", s.prev_codes, _U8, ncb, None),
@@ -705,13 +770,25 @@ class MxPlan:
         _raise(st, "pulse_mx_plan_create_fmt")
         self._h = handle
 
-    def encode(self, counts_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    def encode(self, counts_out: Optional[torch.Tensor] = None,
+               tscales_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Whole-model encode; for an NVFP4 plan the new tensor scales go to
+        ``tscales_out`` (device float32, ntensors; kept as ``self.tscales``)."""
         if counts_out is None:
             counts_out = torch.empty(2 * self.ntensors, dtype=torch.int64, device=self.device)
         _need(counts_out, "counts_out", (torch.int64, torch.uint64), self.device,
               min_numel=2 * self.ntensors)
         with torch.cuda.device(self.device):
-            st = lib().pulse_mx_encode_multi(self._h, _ptr(counts_out), _stream(self.device))
+            if self.fmt == MX_NVFP4:
+                if tscales_out is None:
+                    tscales_out = torch.empty(self.ntensors, dtype=torch.float32, device=self.device)
+                _need(tscales_out, "tscales_out", (torch.float32,), self.device,
+                      min_numel=self.ntensors)
+                self.tscales = tscales_out
+                st = lib().pulse_nvfp4_encode_multi(self._h, _ptr(counts_out), _ptr(tscales_out),
+                                                    _stream(self.device))
+            else:
+                st = lib().pulse_mx_encode_multi(self._h, _ptr(counts_out), _stream(self.device))
         _raise(st, "pulse_mx_encode_multi")
         return counts_out
 

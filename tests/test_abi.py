@@ -118,6 +118,11 @@ def test_mx_host_side_argument_checks_launch_nothing(lib):
     assert lib.pulse_mx_apply_fmt(-1, P(8), P(8), 5, P(8), P(8), 1, P(8), P(8), 1, P(0)) \
         == E.PULSE_ERR_INVALID
     assert lib.pulse_mx_plan_create_fmt(None, 1, 1, None) == E.PULSE_ERR_INVALID
+    assert lib.pulse_mx_quantize_fmt(2, P(8), 7, P(8), P(8), P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_nvfp4_quantize(P(8), 7, P(8), P(8), None, P(0)) == E.PULSE_ERR_INVALID
+    assert lib.pulse_nvfp4_encode(P(8), P(8), P(8), 7, P(8), P(8), P(8), P(8), P(8), None, P(0)) \
+        == E.PULSE_ERR_INVALID
+    assert lib.pulse_nvfp4_encode_multi(None, P(8), P(8), P(0)) == E.PULSE_ERR_INVALID
     assert lib.pulse_mx_quantize(P(0), 1 << 32, P(0), P(0), P(0)) == E.PULSE_ERR_RANGE
     assert lib.pulse_mx_encode(P(0), P(0), P(0), 5, P(0), P(0), P(0), P(0), P(0), P(0)) == E.PULSE_ERR_INVALID
     assert lib.pulse_mx_encode(P(0), P(0), P(0), 5, P(0), P(0), P(0), P(0), P(8), P(0)) == E.PULSE_ERR_INVALID
