@@ -572,9 +572,6 @@ constexpr int kCwGroupChain = 4, kCwPreChain = 3, kCwCtasChain = PULSE_CW_CTAS_C
 // so that every CTA of the grid is resident from the start.
 template <class K>
 int resident_per_sm(K kernel, int threads, int cap) {
-  // shared memory is the limit: ask for the largest carveout
-  cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                       int(cudaSharedmemCarveoutMaxShared));
   int b = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, 0) != cudaSuccess || b < 1)
     b = 1;
