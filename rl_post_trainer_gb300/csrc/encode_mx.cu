@@ -66,13 +66,30 @@ struct Fmt<kFmtNvfp4> {
 };
 // Stage layout of a tile for format F: master, previous code bytes,
 // previous scales.
+// Stages in flight per CTA and parked-entry ring per format: a tile holds at
+// most kEncTile / elements-per-byte code entries, so the FP4 formats need
+// half the ring. (A third stage measured the same: the compute warps' per-tile
+// bookkeeping, not the prefetch depth, sets the pace.)
+#ifndef PULSE_MX8_STAGES
+#define PULSE_MX8_STAGES 2
+#endif
+#ifndef PULSE_MX4_STAGES
+#define PULSE_MX4_STAGES 2
+#endif
+constexpr int kMaxMxStages = 4;
+
 template <int F>
 struct Stage {
   static constexpr uint32_t kCodeBytes = kEncTile / Fmt<F>::kElemsPerByte;
   static constexpr uint32_t kScaleBytes = kEncTile / Fmt<F>::kBlock;  // one per block
   static constexpr uint32_t kBytes = kStageMasterBytes + kCodeBytes + kScaleBytes;
-  static constexpr size_t kDynSmem = size_t(kEncStages) * kBytes + size_t(kEncRing) * 4 + 128;
+  static constexpr int kStages = F == kFmtE4M3 ? PULSE_MX8_STAGES : PULSE_MX4_STAGES;
+  static constexpr uint32_t kRing = kCodeBytes;  // parked code entries per CTA
+  static constexpr uint32_t kRingMask = kRing - 1u;
+  static constexpr size_t kDynSmem = size_t(kStages) * kBytes + size_t(kRing) * 4 + 128;
   static_assert(kBytes % 128 == 0, "stages stay 128-byte aligned");
+  static_assert((kRing & (kRing - 1)) == 0, "the ring is a power of two");
+  static_assert(kStages >= 2 && kStages <= kMaxMxStages, "stage count");
 };
 
 // ---------------------------------------------------------- MXFP8 arithmetic
@@ -157,11 +174,11 @@ struct ParkedMeta {
 };
 
 struct __align__(16) MxShared {
-  uint64_t full[kEncStages];
-  uint64_t empty[kEncStages];
+  uint64_t full[kMaxMxStages];
+  uint64_t empty[kMaxMxStages];
   uint64_t agg_ready[kPendSlots];
   uint64_t slot_free[kPendSlots];
-  StageMeta meta[kEncStages];
+  StageMeta meta[kMaxMxStages];
   ParkedMeta parked[kPendSlots];
   uint32_t warp_tot[2][kWarps];   // per warp: changed codes per round, one byte each
   uint32_t warp_stot[2][kWarps];  // per warp: changed scales per round, one byte each
@@ -174,6 +191,7 @@ static_assert(kEncLookbackWarps == 1, "parked tiles are freed in order by one lo
 template <int F, bool MULTI>
 __device__ __forceinline__ void producer_loop(const MxLaunch& a, MxShared& sh, uint8_t* stages) {
   constexpr uint32_t kStageBytes = Stage<F>::kBytes, kStageCodeBytes = Stage<F>::kCodeBytes;
+  constexpr int kEncStages = Stage<F>::kStages;
   const uint64_t pol_stream = l2_policy_evict_first();
   uint32_t fills_done = 0;
   uint32_t ticket = atomicAdd(a.counters + 0, 1u) + a.first_ticket;
@@ -258,8 +276,10 @@ __device__ __forceinline__ void producer_loop(const MxLaunch& a, MxShared& sh, u
 // and 4-byte code stores after a head of up to 3 entries) and its scale
 // entries to positions prefix_s + k. Positions past the segment's capacity
 // are never written (they only arise after a wait gave up).
+template <int F>
 __device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix_c, uint32_t prefix_s,
                                          const uint32_t* ring, const uint16_t* sring, int lane) {
+  constexpr uint32_t kRingMask = Stage<F>::kRingMask;
   const uint32_t agg = pm.agg_c;
   const uint32_t base = uint32_t(pm.code_base);
   const bool vec = (reinterpret_cast<uintptr_t>(pm.idx) % 16u == 0) &&
@@ -308,6 +328,7 @@ __device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix_c
   }
 }
 
+template <int F>
 __device__ __forceinline__ void lookback_loop(const MxLaunch& a, MxShared& sh, const uint32_t* ring,
                                               int w, int lane, bool multi) {
   for (uint32_t i = uint32_t(w);;) {
@@ -354,7 +375,7 @@ __device__ __forceinline__ void lookback_loop(const MxLaunch& a, MxShared& sh, c
         a.counts_out[2 * t] = uint64_t(prefix_c) + pm.agg_c;
         a.counts_out[2 * t + 1] = uint64_t(prefix_s) + pm.agg_s;
       }
-      copy_out(pm, prefix_c, prefix_s, ring, sh.sring[q], lane);
+      copy_out<F>(pm, prefix_c, prefix_s, ring, sh.sring[q], lane);
       __syncwarp();
       if (lane == 0) {
         __threadfence_block();
@@ -480,6 +501,8 @@ template <int F, bool MULTI>
 __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, uint8_t* stages,
                                              uint32_t* ring, int tid, int lane, int warp) {
   constexpr uint32_t kStageBytes = Stage<F>::kBytes, kStageCodeBytes = Stage<F>::kCodeBytes;
+  constexpr int kEncStages = Stage<F>::kStages;
+  constexpr uint32_t kEncRing = Stage<F>::kRing, kRingMask = Stage<F>::kRingMask;
   constexpr bool kFp4 = F != kFmtE4M3;  // two codes per byte
   constexpr uint32_t kBlock = Fmt<F>::kBlock;
   constexpr int kLanesPerBlock = int(kBlock) / kMxPerThread;  // 4 or 2
@@ -735,6 +758,7 @@ template <int F, bool MULTI>
 __global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
     encode_mx_kernel(const __grid_constant__ MxLaunch a) {
   constexpr uint32_t kStageBytes = Stage<F>::kBytes;
+  constexpr int kEncStages = Stage<F>::kStages;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ MxShared sh;
   const int tid = threadIdx.x;
@@ -779,7 +803,7 @@ __global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_loop<F, MULTI>(a, sh, stages);
   } else {
-    lookback_loop(a, sh, ring, warp - kFirstLookbackWarp, lane, MULTI);
+    lookback_loop<F>(a, sh, ring, warp - kFirstLookbackWarp, lane, MULTI);
   }
 }
 
