@@ -52,7 +52,7 @@ __device__ __forceinline__ PackSegment segment_of(const PackLaunch& a, uint64_t 
 __device__ __forceinline__ uint32_t bit_width(uint32_t v) { return v ? 32u - __clz(v) : 0u; }
 
 template <bool MULTI>
-__global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constant__ PackLaunch a) {
+__global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const __grid_constant__ PackLaunch a) {
   __shared__ uint32_t words[kPackWarps][kPackBlock];  // one block's packed words per warp
   __shared__ uint32_t width_of[kPackChunkBlocks];
   __shared__ uint32_t ticket, prefix16;
