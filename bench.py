@@ -9,13 +9,17 @@ order-preserving compaction, prev refresh) + pulse_apply_multi_device
 (scatter into the sampler's BF16 weights), one launch each over the whole
 model. Before every step prev and the sampler weights are restored from a
 pristine copy (untimed), so every timed step encodes the same real update.
-Inputs (48 GB) are far larger than L2 (129 MB), so no L2 flush is needed.
+Inputs (48 GB) are far larger than L2 (129 MB), so no L2 flush is needed;
+a workload whose buffers fit in a few L2s (the single 2^20 tensor) gets a
+512 MB scratch write after the restore, before every step.
 
 Printed: one JSON line with params/s (value), the roofline of the encode
-kernel against measured HBM copy bandwidth, the XOR-mask path, the MXFP8
-serving view of the same step (its own encode + apply), an
-end-to-end number through host buffers, the CPU oracle baseline, and the
-SM clocks sampled during the timed region.
+kernel against measured HBM copy bandwidth, the XOR-mask path, the MXFP8,
+MXFP4 and NVFP4 serving views of the same step (their own encode + apply),
+the sidecar catch-up legs, index packing, PULSELoCo, an end-to-end number
+through host buffers, the CPU oracle baseline, and the SM clocks sampled
+during the timed region. The flat 2^28 workload (--config 4) adds the
+encode + apply cost at every update scale of the density sweep.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -43,6 +47,8 @@ import workloads  # noqa: E402
 METRIC = "encode+apply params/s"
 UNIT = "params/s"
 NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 1024 * 1024
+FLUSH_BYTES = 512 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "encode_multi_llama3_8b.md")
 ENCODE_SRCS = [os.path.join(ROOT, "rl_post_trainer_gb300", "csrc", f)
@@ -318,6 +324,16 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
     wl = Workload(specs, cfg["seed"] + 1000 * rank, cfg["eta"], dev, xor=not args.no_xor)
     n = wl.n
     stream = torch.cuda.current_stream(dev)
+    # trainer + sampler buffers of one step: master, prev, w, patch capacity
+    footprint = 14 * n
+    flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+             if footprint < 4 * L2_BYTES else None)
+    if flush is None:
+        l2_note = (f"inputs ({footprint / 1e9:.3g} GB) larger than L2; "
+                   "prev and w restored untimed before each step")
+    else:
+        l2_note = ("L2 flushed by a 512 MB write after the untimed restore of prev and w, "
+                   "before each encode + apply step")
 
     def step(ev=None):
         if ev is not None:
@@ -342,6 +358,8 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
         for _ in range(args.steps):
             wl.restore()
+            if flush is not None:
+                flush.fill_(1)
             torch.cuda.synchronize()
             barrier(dist_on)
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -377,7 +395,7 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
         "data": "synthetic",
         "config": {"workload": cfg["name"], "params": n, "tensors": len(specs), "eta": cfg["eta"],
                    "density": k / n, "patch_entries": k, "parallelism": f"replicas{world}",
-                   "l2": "inputs (48 GB) larger than L2; prev and w restored untimed before each step"},
+                   "l2": l2_note},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),
                      "kernel": "encode_kernel<multi>", "peak_kind": peak_kind,
@@ -394,7 +412,9 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
                   "frac_sector_rmw_measured_peak": app_rmw / app_s / 1e9 / peak,
                   "frac_sector_rmw_nominal_8tbs": app_rmw / app_s / 1e9 / NOMINAL_HBM_GBS},
         "sectors_touched": S,
-        "gpu_launches": 2 * args.steps,
+        # encode, then the apply's route, partition, chunk-owned and scatter
+        # launches (the route not taken returns at once)
+        "gpu_launches": 5 * args.steps,
         "clocks": clocks.summary(),
     }
 
@@ -427,6 +447,8 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
         del wl.prev_x, wl.w_x, wl.mask
         wl.xplan.close()
 
+    if cfg.get("sweep"):
+        out["sweep"] = run_sweep(args, specs, cfg["seed"], dev, peak)
     if not args.no_mx:
         out["mxfp8"] = run_mx(args, cfg, specs, wl, dev, rank, peak, pulse.MX_E4M3)
         out["mxfp4"] = run_mx(args, cfg, specs, wl, dev, rank, peak, pulse.MX_E2M1)
@@ -747,6 +769,67 @@ def run_compose(args, wl, dev, versions: int = 4):
     }
 
 
+def run_sweep(args, specs, seed, dev, peak):
+    """Encode + apply of one flat tensor at every update scale of the density
+    sweep: w0 from `seed`, the i-th scale's z from sweep_seed(i) (the draws of
+    the parity tests). prev and w restored untimed before every step; the
+    inputs (1.6 GB and up) are larger than L2. CUDA events, mean over steps."""
+    import rl_post_trainer_gb300 as pulse
+    (spec,) = specs
+    n = spec.numel
+    gen = workloads.torch_generator(dev, seed)
+    w0 = torch.empty(n, dtype=torch.float32, device=dev)
+    workloads.torch_init_(w0, spec, gen)
+    p0 = torch.empty(n, dtype=torch.int16, device=dev)
+    workloads.torch_bf16_view_(p0, w0)
+    m = torch.empty_like(w0)
+    prev, w = torch.empty_like(p0), torch.empty_like(p0)
+    idx = torch.empty(n, dtype=torch.int32, device=dev)
+    val = torch.empty(n, dtype=torch.int16, device=dev)
+    counts = torch.zeros(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    rows = []
+    with pulse.Plan([pulse.TensorSlot(n, master=m, prev=prev, w=w, idx=idx, val=val)]) as plan:
+        for i, eta in enumerate(workloads.ETA_SWEEP):
+            m.copy_(w0)
+            workloads.torch_update_(m, eta, workloads.torch_generator(dev, workloads.sweep_seed(i)))
+            te, ta = [], []
+            for it in range(args.warmup + args.steps):
+                prev.copy_(p0)
+                w.copy_(p0)
+                torch.cuda.synchronize()
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                ev[0].record(stream)
+                plan.encode(counts)
+                ev[1].record(stream)
+                plan.apply(counts)
+                ev[2].record(stream)
+                torch.cuda.synchronize()
+                if it >= args.warmup:
+                    te.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+                    ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+            if plan.get_error() != 0:
+                raise RuntimeError(f"device error in the sweep at eta={eta}")
+            if not torch.equal(w, prev):
+                raise RuntimeError(f"sampler weights differ from the trainer view at eta={eta}")
+            k = int(counts.item())
+            sec = idx[:k].to(torch.int64) // 16
+            S = 0 if k == 0 else 1 + int((sec[1:] != sec[:-1]).sum().item())
+            del sec
+            enc_s, app_s = float(np.mean(te)), float(np.mean(ta))
+            enc_sec = 6.0 * n + 32.0 * S + 6.0 * k
+            app_rmw = 6.0 * k + 64.0 * S
+            rows.append({"eta": eta, "density": k / n, "patch_entries": k, "sectors_touched": S,
+                         "encode_ms": 1e3 * enc_s, "apply_ms": 1e3 * app_s,
+                         "params_per_s": n / (enc_s + app_s),
+                         "encode_gbs_algorithmic": (6.0 * n + 8.0 * k) / enc_s / 1e9,
+                         "encode_frac_sector_measured_peak": enc_sec / enc_s / 1e9 / peak,
+                         "apply_frac_sector_rmw_measured_peak": app_rmw / app_s / 1e9 / peak})
+    return {"workload": f"one flat tensor of {n} params", "rows": rows,
+            "bytes_model": "encode 6n+8k (sector 6n+32S+6k); apply sector read-modify-write 6k+64S",
+            "gpu_launches": 5 * len(rows) * (args.warmup + args.steps)}
+
+
 def run_pack(args, wl, counts_np, dev):
     """Codec-friendly packing of the step's patch indices (every tensor's
     segment in one pulse_pack_indices_multi launch), and the receiver's
@@ -993,8 +1076,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = dict(workloads.CONFIGS[args.config])
-    if cfg["eta"] is None:
+    if cfg["eta"] is None:  # the density sweep: the headline at the default scale, then every scale
         cfg["eta"] = workloads.ETA_DEFAULT
+        cfg["sweep"] = True
     specs = cfg["specs"]()
 
     if args.impl == "reference":

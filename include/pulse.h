@@ -214,19 +214,28 @@ uint64_t pulse_plan_num_tiles(const pulse_plan *plan);
 int pulse_encode_multi(pulse_plan *plan, uint64_t *counts_out, cudaStream_t stream);
 
 /*
- * Apply every tensor's patch segment (one partition launch and one apply
- * launch for the whole model). counts_host (HOST, ntensors uint64) gives each
- * segment's length; it is copied before the call returns. Each segment must
- * list ascending indices (what encode writes): the tensor is cut into chunks,
- * each chunk's entries are found by binary search, and a chunk with many
- * entries is read-modified-written in shared memory and its changed 32-byte
- * sectors written back whole. Entries outside their chunk or with idx >= n
- * are skipped and recorded as PULSE_ERR_INDEX in the plan's error word.
+ * Apply every tensor's patch segment to the whole model. counts_host (HOST,
+ * ntensors uint64) gives each segment's length; it is copied before the call
+ * returns. Each segment must list ascending indices (what encode writes).
+ * The route follows from the counts (here on the host):
+ *  - k = sum of the counts, n = sum of the tensor sizes; when 64 k >= n the
+ *    tensor is cut into chunks, each chunk's entries are found by binary
+ *    search, and a chunk with many entries is read-modified-written in shared
+ *    memory and its changed 32-byte sectors written back whole;
+ *  - when 64 k < n (a sparse patch) the entries are scattered straight into
+ *    w (each target sector prefetched into L2 first), which moves only the
+ *    touched sectors.
+ * Entries with idx >= n are skipped and recorded as PULSE_ERR_INDEX in the
+ * plan's error word; on the chunk route so are entries outside their chunk
+ * (a segment that is not ascending), while the scatter route stores such
+ * entries in patch order.
  */
 int pulse_apply_multi(pulse_plan *plan, const uint64_t *counts_host, cudaStream_t stream);
 
 /* As pulse_apply_multi with the counts in DEVICE memory (e.g. counts_out of
- * pulse_encode_multi), so no host round trip is needed. */
+ * pulse_encode_multi), so no host round trip is needed: a one-CTA launch
+ * picks the route on the device and the launches of the route not taken
+ * return at once. */
 int pulse_apply_multi_device(pulse_plan *plan, const uint64_t *counts_dev, cudaStream_t stream);
 
 /*

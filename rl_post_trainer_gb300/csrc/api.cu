@@ -38,6 +38,7 @@ constexpr uint64_t kMaxTiles = 0x7FFFFFFFull;      // tile tickets are uint32
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s per bounded wait
 constexpr size_t kCounterBytes = 256;               // ticket, finished, error (+ padding)
 constexpr int kAmaxWord = 8;  // counters word holding a single-tensor NVFP4 maximum
+constexpr int kRouteWord = 12;  // counters word holding a whole-model apply's route
 constexpr int kMaxTensorsPerApplyLaunch = 16384;     // bound on the apply kernel's smem table
 
 uint64_t div_up(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
@@ -347,6 +348,7 @@ struct pulse_plan {
   int device = 0;
   int ntensors = 0;
   uint64_t total_tiles = 0;
+  uint64_t total_n = 0;             // elements over every tensor
   bool can_encode = false, can_apply = false, can_xor_mask = false, can_xor_apply = false;
   bool can_chain = false;  // every tensor with n > 0 has w: chained applies are possible
   std::vector<TensorDesc> host_desc;
@@ -520,6 +522,7 @@ int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** pl
     tb[size_t(i)] = tiles;
     p->host_desc.push_back(make_desc(t, tiles));
     tiles += div_up(t.n, kEncTile);
+    p->total_n += t.n;
     if (t.n > 0) {
       p->can_encode = p->can_encode && t.master && t.prev && t.idx && t.val;
       p->can_apply = p->can_apply && t.w && t.idx && t.val;
@@ -623,31 +626,56 @@ int pulse_encode_multi(pulse_plan* plan, uint64_t* counts_out, cudaStream_t stre
   return cuda_status(launch_encode(a, true, grid, stream));
 }
 
-int pulse_apply_multi_device(pulse_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {
-  if (plan == nullptr || counts_dev == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
-  if (plan->chunk_first != nullptr)
-    return cuda_status(launch_apply_chunks(plan->desc, plan->chunk_begin, plan->chunk_tensor,
-                                           plan->chunk_first, counts_dev, plan->total_chunks,
-                                           plan->ws.counters + 2, kDefaultWaitNs, stream));
+namespace {
+constexpr int kRouteDevice = -1, kRouteChunks = 0, kRouteScatter = 1;
+
+// Whole-model apply by the given route (kRouteDevice: decided on the device
+// from counts_dev; the launches of the route not taken return at once).
+int apply_multi_routed(pulse_plan* plan, const uint64_t* counts_dev, int how, cudaStream_t stream) {
+  if (plan->chunk_first == nullptr) how = kRouteScatter;  // no chunk tables
+  const uint32_t* run_if = nullptr;
+  if (how != kRouteScatter) {
+    uint32_t* route = how == kRouteDevice ? plan->ws.counters + kRouteWord : nullptr;
+    const cudaError_t e = launch_apply_chunks(
+        plan->desc, plan->ntensors, plan->total_n, plan->chunk_begin, plan->chunk_tensor,
+        plan->chunk_first, counts_dev, plan->total_chunks, route, plan->ws.counters + 2,
+        kDefaultWaitNs, stream);
+    if (e != cudaSuccess) return PULSE_ERR_CUDA;
+    if (how == kRouteChunks) return PULSE_OK;
+    run_if = route;
+  }
   const int grid = sm_count(plan->device) * 8;
   for (int t0 = 0; t0 < plan->ntensors; t0 += kMaxTensorsPerApplyLaunch) {
     const int nt = plan->ntensors - t0 < kMaxTensorsPerApplyLaunch ? plan->ntensors - t0
                                                                    : kMaxTensorsPerApplyLaunch;
     const cudaError_t e = launch_apply_multi(plan->desc + t0, nt, counts_dev + t0,
-                                             plan->ws.counters + 2, grid, stream);
+                                             plan->ws.counters + 2, grid, stream, run_if);
     if (e != cudaSuccess) return PULSE_ERR_CUDA;
   }
   return PULSE_OK;
 }
+}  // namespace
+
+int pulse_apply_multi_device(pulse_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {
+  if (plan == nullptr || counts_dev == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
+  return apply_multi_routed(plan, counts_dev, kRouteDevice, stream);
+}
 
 int pulse_apply_multi(pulse_plan* plan, const uint64_t* counts_host, cudaStream_t stream) {
   if (plan == nullptr || counts_host == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
+  // the route from the host counts, by the rule the device would apply
+  uint64_t k = 0;
+  for (int t = 0; t < plan->ntensors; ++t) {
+    const uint64_t n = plan->host_desc[size_t(t)].n;
+    k += counts_host[t] < n ? counts_host[t] : n;
+  }
+  const int how = kApplySparseRatio * k < plan->total_n ? kRouteScatter : kRouteChunks;
   // From pageable memory the copy is staged before this call returns, so the
   // caller may reuse counts_host at once.
   if (cudaMemcpyAsync(plan->counts, counts_host, sizeof(uint64_t) * size_t(plan->ntensors),
                       cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return PULSE_ERR_CUDA;
-  return pulse_apply_multi_device(plan, plan->counts, stream);
+  return apply_multi_routed(plan, plan->counts, how, stream);
 }
 
 namespace {

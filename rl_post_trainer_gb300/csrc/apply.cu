@@ -136,9 +136,11 @@ __global__ void __launch_bounds__(kApplyThreads)
 // is rebuilt by every CTA in shared memory at the start of the launch.
 template <class Seg>
 __global__ void __launch_bounds__(kApplyThreads)
-    apply_multi_kernel(const Seg* segs, int nsegs, const uint64_t* counts, uint32_t* err) {
+    apply_multi_kernel(const Seg* segs, int nsegs, const uint64_t* counts, uint32_t* err,
+                       const uint32_t* run_if) {
   extern __shared__ uint64_t tile_begin[];  // nsegs + 1
   __shared__ uint64_t warp_tot[kApplyThreads / 32];
+  if (run_if != nullptr && *run_if == 0u) return;  // the other route takes this patch
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (nsegs + kApplyThreads - 1) / kApplyThreads;
   const int t0 = tid * per;
@@ -204,14 +206,16 @@ cudaError_t launch_apply_t(V* w, uint64_t n, bool checked, const uint32_t* idx, 
 
 template <class Seg>
 cudaError_t launch_apply_multi_t(const Seg* segs, int nsegs, const uint64_t* counts_dev,
-                                 uint32_t* error_word, int grid, cudaStream_t stream) {
+                                 uint32_t* error_word, int grid, cudaStream_t stream,
+                                 const uint32_t* run_if) {
   const size_t smem = size_t(nsegs + 1) * sizeof(uint64_t);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(apply_multi_kernel<Seg>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
   }
-  apply_multi_kernel<Seg><<<grid, kApplyThreads, smem, stream>>>(segs, nsegs, counts_dev, error_word);
+  apply_multi_kernel<Seg><<<grid, kApplyThreads, smem, stream>>>(segs, nsegs, counts_dev, error_word,
+                                                                 run_if);
   return cudaGetLastError();
 }
 
@@ -238,12 +242,37 @@ __device__ __forceinline__ uint32_t lower_bound_u32(const uint32_t* a, uint32_t 
   return lo;
 }
 
+// One CTA: the route of a whole-model apply (1 = entry scatter for a sparse
+// patch, 0 = chunk-owned). Both routes give the same w for an ascending patch.
+__global__ void __launch_bounds__(256)
+    apply_route_kernel(const TensorDesc* tensors, int ntensors, const uint64_t* counts,
+                       uint64_t total_n, uint32_t* route) {
+  __shared__ uint64_t part[256 / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t k = 0;
+  for (int t = tid; t < ntensors; t += 256) {
+    const uint64_t c = counts[t], n = tensors[t].n;
+    k += c < n ? c : n;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) k += __shfl_xor_sync(0xFFFFFFFFu, k, o);
+  if (lane == 0) part[warp] = k;
+  __syncthreads();
+  if (tid == 0) {
+    uint64_t sum = 0;
+    for (int w = 0; w < 256 / 32; ++w) sum += part[w];
+    *route = kApplySparseRatio * sum < total_n ? 1u : 0u;
+  }
+}
+
 __global__ void __launch_bounds__(256)
     apply_partition_kernel(const TensorDesc* tensors, const uint64_t* chunk_begin,
                            const uint32_t* chunk_tensor, const uint64_t* counts,
-                           uint64_t total_chunks, uint32_t* chunk_first, uint32_t* err) {
+                           uint64_t total_chunks, uint32_t* chunk_first, uint32_t* err,
+                           const uint32_t* skip_if) {
   const uint64_t g = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (g >= total_chunks) return;
+  if (skip_if != nullptr && *skip_if != 0u) return;  // the sparse route takes this patch
   const uint32_t t = chunk_tensor[g];
   const TensorDesc& d = tensors[t];
   uint64_t c = counts[t];
@@ -328,6 +357,7 @@ struct CwArgs {
   uint64_t total_chunks;
   uint32_t* err;
   uint64_t wait_limit_ns;
+  const uint32_t* skip_if;  // null, or a device word: the launch does nothing when it is non-zero
 };
 
 __device__ __forceinline__ void worker_barrier() {
@@ -370,6 +400,8 @@ __global__ void __launch_bounds__(kCwThreads, CTAS) chunk_apply_kernel(const CwA
   __shared__ __align__(16) uint8_t dirty[kChunkSectors];  // one flag byte per 32-byte sector
   __shared__ ChunkSlot slot[kCwBuf];
   __shared__ __align__(8) uint64_t full[kCwBuf], empty[kCwBuf];
+  // the same word for every thread, written by an earlier launch: a uniform exit
+  if (a.skip_if != nullptr && *a.skip_if != 0u) return;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -523,10 +555,23 @@ __global__ void __launch_bounds__(kCwThreads, CTAS) chunk_apply_kernel(const CwA
 #pragma unroll
           for (int q = 0; q < kCwPre; ++q)
             if (e0 + uint32_t(q * kCwWorkers + tid) < e1) put(pi[u][q], pv[u][q]);
+          // the rest of a crowded chunk, kCwPre loads in flight per thread
           const uint32_t* ip = sl.idx[v];
           const uint16_t* vp = sl.val[v];
-          for (uint32_t j = e0 + uint32_t(kCwPre * kCwWorkers + tid); j < e1; j += kCwWorkers)
-            put(ip[j], vp[j]);
+          for (uint32_t j0 = e0 + uint32_t(kCwPre * kCwWorkers); j0 < e1;
+               j0 += uint32_t(kCwPre * kCwWorkers)) {
+            uint32_t xi[kCwPre];
+            uint16_t xv[kCwPre];
+#pragma unroll
+            for (int q = 0; q < kCwPre; ++q) {
+              const uint32_t j = j0 + uint32_t(q * kCwWorkers + tid);
+              xi[q] = j < e1 ? ip[j] : 0u;
+              xv[q] = j < e1 ? vp[j] : uint16_t(0);
+            }
+#pragma unroll
+            for (int q = 0; q < kCwPre; ++q)
+              if (j0 + uint32_t(q * kCwWorkers + tid) < e1) put(xi[q], xv[q]);
+          }
           worker_barrier();  // the next version's stores land after these
         }
       }
@@ -580,21 +625,24 @@ int resident_per_sm(K kernel, int threads, int cap) {
 
 }  // namespace
 
-cudaError_t launch_apply_chunks(const TensorDesc* tensors, const uint64_t* chunk_begin,
-                                const uint32_t* chunk_tensor, uint32_t* chunk_first,
-                                const uint64_t* counts_dev, uint64_t total_chunks,
-                                uint32_t* error_word, uint64_t wait_limit_ns, cudaStream_t stream) {
-  if (total_chunks == 0) return cudaSuccess;
+cudaError_t launch_apply_chunks(const TensorDesc* tensors, int ntensors, uint64_t total_n,
+                                const uint64_t* chunk_begin, const uint32_t* chunk_tensor,
+                                uint32_t* chunk_first, const uint64_t* counts_dev,
+                                uint64_t total_chunks, uint32_t* route, uint32_t* error_word,
+                                uint64_t wait_limit_ns, cudaStream_t stream) {
+  if (route != nullptr)
+    apply_route_kernel<<<1, 256, 0, stream>>>(tensors, ntensors, counts_dev, total_n, route);
+  if (total_chunks == 0) return cudaGetLastError();
   int dev = 0;
   cudaGetDevice(&dev);
   apply_partition_kernel<<<unsigned((total_chunks + 255) / 256), 256, 0, stream>>>(
-      tensors, chunk_begin, chunk_tensor, counts_dev, total_chunks, chunk_first, error_word);
+      tensors, chunk_begin, chunk_tensor, counts_dev, total_chunks, chunk_first, error_word, route);
   auto kernel = chunk_apply_kernel<1, kCwPreOne, kCwCtasOne>;
   static const int per_sm = resident_per_sm(kernel, kCwThreads, kCwCtasOne);
   const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(per_sm);
   const unsigned grid = unsigned(total_chunks < cap ? total_chunks : cap);
   const CwArgs args{tensors, chunk_begin, chunk_tensor, chunk_first, nullptr, counts_dev,
-                    0,       1,           total_chunks, error_word, wait_limit_ns};
+                    0,       1,           total_chunks, error_word, wait_limit_ns, route};
   kernel<<<grid, kCwThreads, 0, stream>>>(args);
   return cudaGetLastError();
 }
@@ -630,7 +678,7 @@ cudaError_t launch_apply_chain(const TensorDesc* tensors, const uint64_t* chunk_
   const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(per_sm);
   const unsigned grid = unsigned(total_chunks < cap ? total_chunks : cap);
   const CwArgs args{tensors,  chunk_begin,  chunk_tensor, chain_first, segs, nullptr,
-                    ntensors, nversions,    total_chunks, error_word,  wait_limit_ns};
+                    ntensors, nversions,    total_chunks, error_word,  wait_limit_ns, nullptr};
   kernel<<<grid, kCwThreads, 0, stream>>>(args);
   return cudaGetLastError();
 }
@@ -648,13 +696,14 @@ cudaError_t launch_apply_u8(uint8_t* w, uint64_t n, bool checked, const uint32_t
 }
 
 cudaError_t launch_apply_multi(const TensorDesc* tensors, int ntensors, const uint64_t* counts_dev,
-                               uint32_t* error_word, int grid, cudaStream_t stream) {
-  return launch_apply_multi_t(tensors, ntensors, counts_dev, error_word, grid, stream);
+                               uint32_t* error_word, int grid, cudaStream_t stream,
+                               const uint32_t* run_if) {
+  return launch_apply_multi_t(tensors, ntensors, counts_dev, error_word, grid, stream, run_if);
 }
 
 cudaError_t launch_apply_u8_multi(const ByteSegment* segs, int nsegs, const uint64_t* counts_dev,
                                   uint32_t* error_word, int grid, cudaStream_t stream) {
-  return launch_apply_multi_t(segs, nsegs, counts_dev, error_word, grid, stream);
+  return launch_apply_multi_t(segs, nsegs, counts_dev, error_word, grid, stream, nullptr);
 }
 
 }  // namespace pulse

@@ -329,10 +329,23 @@ __device__ __forceinline__ void cc_compute(const CcArgs& a, CcShared& sh, int ti
 #pragma unroll
         for (int q = 0; q < kCcPre; ++q)
           if (e0 + uint32_t(q * kEncThreads + tid) < e1) put(pi[u][q], pv[u][q], stamp);
+        // the rest of a crowded chunk, kCcPre loads in flight per thread
         const uint32_t* ip = m.idx[v];
         const uint16_t* vp = m.val[v];
-        for (uint32_t j = e0 + uint32_t(kCcPre * kEncThreads + tid); j < e1; j += kEncThreads)
-          put(ip[j], vp[j], stamp);
+        for (uint32_t j0 = e0 + uint32_t(kCcPre * kEncThreads); j0 < e1;
+             j0 += uint32_t(kCcPre * kEncThreads)) {
+          uint32_t xi[kCcPre];
+          uint16_t xv[kCcPre];
+#pragma unroll
+          for (int q = 0; q < kCcPre; ++q) {
+            const uint32_t j = j0 + uint32_t(q * kEncThreads + tid);
+            xi[q] = j < e1 ? ip[j] : 0u;
+            xv[q] = j < e1 ? vp[j] : uint16_t(0);
+          }
+#pragma unroll
+          for (int q = 0; q < kCcPre; ++q)
+            if (j0 + uint32_t(q * kEncThreads + tid) < e1) put(xi[q], xv[q], stamp);
+        }
       }
     }
     compute_barrier();  // every entry of the chunk is in the image

@@ -334,6 +334,45 @@ def test_multi_tensor_plan_parity(aligned):
     plan.close()
 
 
+@pytest.mark.parametrize("eta", [1e-8, 3e-7, 1e-6, 1e-4])
+@pytest.mark.parametrize("device_counts", [True, False])
+def test_multi_apply_both_routes(eta, device_counts):
+    """A whole-model apply takes the entry scatter when 64 k < n and the
+    chunk-owned kernel otherwise (1e-4 also fills chunks far past the
+    entries a thread loads at once); every route gives the oracle's view."""
+    dev = _cuda()
+    sizes = [3 * 8192 + 77, 1, 0, 65536 + 5, 8192, 200003]
+    masters, prevs = [], []
+    for i, n in enumerate(sizes):
+        m, p = (workloads.np_pair(n, seed=900 + i, eta=eta) if n
+                else (np.zeros(0, np.float32), np.zeros(0, np.uint16)))
+        masters.append(m)
+        prevs.append(p)
+    slots, keep = _slots_from_np(masters, prevs, dev, with_mask=False)
+    o_prevs = [p.copy() for p in prevs]
+    o_patches = oracle.encode_multi(masters, o_prevs)
+    k = sum(o_idx.size for o_idx, _ in o_patches)
+    sparse = 64 * k < sum(sizes)
+    assert sparse == (eta < 1e-6)  # the cases cover both routes
+    with pulse.Plan(slots) as plan:
+        counts = plan.encode()
+        plan.apply(counts if device_counts else counts.cpu().numpy().tolist())
+        torch.cuda.synchronize()
+        for t, s in enumerate(slots):
+            np.testing.assert_array_equal(host_u16(s.w), o_prevs[t])
+        assert plan.get_error() == 0
+        # the same patch again changes nothing; an index past its tensor is
+        # skipped and reported on either route
+        plan.apply(counts if device_counts else counts.cpu().numpy().tolist())
+        assert plan.get_error() == 0
+        if o_patches[0][0].size:
+            slots[0].idx[0] = sizes[0] + 100
+            plan.apply(counts)
+            assert plan.get_error() == pulse.pulse.PULSE_ERR_INDEX
+        for t, s in enumerate(slots[1:], start=1):
+            np.testing.assert_array_equal(host_u16(s.w), o_prevs[t])
+
+
 def test_multi_apply_host_counts_and_out_of_range_segment():
     dev = _cuda()
     sizes = [TILE + 3, 2 * TILE]
