@@ -897,45 +897,61 @@ __global__ void __launch_bounds__(kQuantThreads)
 // non-negative float orders like its bits). amax_bits is zeroed beforehand.
 constexpr int kAmaxThreads = 256;
 
+// Largest finite magnitude of every tensor (bit pattern of a non-negative
+// float, so unsigned order is float order). A CTA walks tiles blockIdx.x,
+// blockIdx.x + grid, ...; each thread keeps a running maximum while the tiles
+// stay in one tensor and a warp folds it into amax_bits[t] with one atomicMax
+// when the tensor changes and at the end. A full, aligned tile is read with
+// all four 16-byte loads of a thread in flight at once.
 template <bool MULTI>
 __global__ void __launch_bounds__(kAmaxThreads)
     mx_amax_kernel(const MxTensorDesc one, const MxTensorDesc* tensors, const uint64_t* tile_begin,
                    int ntensors, uint64_t total_tiles, uint32_t* amax_bits) {
-  __shared__ uint32_t wmax[kAmaxThreads / 32];
-  const int tid = threadIdx.x;
+  constexpr int kLoads = kEncTile / (4 * kAmaxThreads);  // float4 loads per thread per tile
+  static_assert(kLoads * 4 * kAmaxThreads == kEncTile, "a tile is whole float4 rounds");
+  const int tid = threadIdx.x, lane = tid & 31;
+  int cur = MULTI ? -1 : 0;
+  uint64_t cur_begin = 1, cur_end = 0;
+  MxTensorDesc d = one;
+  float m = 0.0f;  // this thread's maximum over the tiles of tensor `cur` seen so far
+  auto take = [&](float v) {
+    const float x = fabsf(v);
+    if (x <= 3.40282347e38f) m = fmaxf(m, x);  // finite values only (NaN fails the test)
+  };
+  auto flush = [&]() {  // uniform over the CTA: every thread walks the same tiles
+    const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
+    if (lane == 0 && cur >= 0 && wm != 0u) atomicMax(amax_bits + cur, wm);
+    m = 0.0f;
+  };
   for (uint64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-    const int t = MULTI ? find_tensor(tile_begin, ntensors, tile) : 0;
-    const MxTensorDesc d = MULTI ? tensors[t] : one;
+    if constexpr (MULTI) {
+      if (tile < cur_begin || tile >= cur_end) {
+        flush();
+        cur = find_tensor(tile_begin, ntensors, tile);
+        d = tensors[cur];
+        cur_begin = d.tile_begin;
+        cur_end = tile_begin[cur + 1];
+      }
+    }
     const uint64_t base = (tile - d.tile_begin) * kEncTile;
     const uint32_t len = uint32_t(d.n - base < uint64_t(kEncTile) ? d.n - base : uint64_t(kEncTile));
     const float* src = d.master + base;
-    const bool vec = (reinterpret_cast<uintptr_t>(src) % 16u) == 0;
-    float m = 0.0f;
-    for (uint32_t k = uint32_t(tid) * 4u; k < len; k += 4u * kAmaxThreads) {
-      float v[4];
-      if (vec && k + 4u <= len) {
-        const float4 q = *reinterpret_cast<const float4*>(src + k);
-        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-      } else {
+    if (len == uint32_t(kEncTile) && (reinterpret_cast<uintptr_t>(src) % 16u) == 0) {
+      uint4 q[kLoads];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = k + uint32_t(e) < len ? src[k + e] : 0.0f;
-      }
+      for (int r = 0; r < kLoads; ++r) q[r] = ld_stream_u4_ro(src + (r * kAmaxThreads + tid) * 4);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x = fabsf(v[e]);
-        if (x <= 3.40282347e38f) m = fmaxf(m, x);  // finite values only (NaN fails the test)
+      for (int r = 0; r < kLoads; ++r) {
+        take(__uint_as_float(q[r].x));
+        take(__uint_as_float(q[r].y));
+        take(__uint_as_float(q[r].z));
+        take(__uint_as_float(q[r].w));
       }
+    } else {
+      for (uint32_t k = uint32_t(tid); k < len; k += kAmaxThreads) take(src[k]);
     }
-    const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
-    if ((tid & 31) == 0) wmax[tid >> 5] = wm;
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t bm = 0;
-      for (int w = 0; w < kAmaxThreads / 32; ++w) bm = bm > wmax[w] ? bm : wmax[w];
-      atomicMax(amax_bits + t, bm);
-    }
-    __syncthreads();
   }
+  flush();
 }
 
 }  // namespace
