@@ -12,10 +12,14 @@
 //  * chunks of 32 blocks (4096 entries): chunk_off[c] = byte offset of the
 //    chunk's first payload, so every chunk decodes on its own.
 //
-// Pack: one CTA per chunk, in ticket order; each warp measures and packs 4
-// blocks (bits OR-ed into shared-memory words); the chunk's payload offset is
-// the exclusive prefix of the chunk sizes, found with the decoupled look-back
-// shared with the encode kernels (warp 0), counted in 16-byte units.
+// Pack: persistent CTAs (8 per SM) take chunks in ticket order, a ticket
+// when its chunk starts; each warp measures and packs 4 blocks (bits OR-ed
+// into shared-memory words); the chunk's payload offset is the exclusive
+// prefix of the chunk sizes, found with the decoupled look-back shared with
+// the encode kernels (warp 0), counted in 16-byte units.
+// The pack CTAs keep the segments' chunk ranges in shared memory (loaded
+// once per CTA when there are fewer than kSegCache segments), so finding a
+// chunk's segment costs no dependent global loads.
 // Unpack: one CTA per chunk; each warp extracts a block's gaps and rebuilds
 // its indices with a warp scan.
 #include "encode_common.cuh"
@@ -42,25 +46,47 @@ struct PackLaunch {
   uint64_t wait_limit_ns;
 };
 
-// The segment that global chunk c belongs to.
+constexpr int kSegCache = 1024;  // segments whose chunk ranges a CTA keeps in shared memory
+constexpr int kPackCtasPerSm = 8;
+
+// Copy the chunk ranges into shared memory when they fit (multi-segment).
 template <bool MULTI>
-__device__ __forceinline__ PackSegment segment_of(const PackLaunch& a, uint64_t c) {
+__device__ __forceinline__ void load_seg_begin(const PackLaunch& a, uint64_t* sbeg) {
+  if (MULTI && a.nsegs < kSegCache)
+    for (int k = threadIdx.x; k <= a.nsegs; k += kPackThreads) sbeg[k] = a.chunk_begin[k];
+}
+
+// The segment that global chunk c belongs to: the largest s with
+// chunk_begin[s] <= c (chunk_begin[nsegs] = total > c); sbeg: the shared
+// copy of chunk_begin, or null to search the global one.
+template <bool MULTI>
+__device__ __forceinline__ PackSegment segment_of(const PackLaunch& a, const uint64_t* sbeg,
+                                                  uint64_t c) {
   if (!MULTI) return a.one;
-  return a.segs[enc::find_tensor(a.chunk_begin, a.nsegs, c)];
+  if (sbeg == nullptr || a.nsegs >= kSegCache)
+    return a.segs[enc::find_tensor(a.chunk_begin, a.nsegs, c)];
+  int lo = 0, hi = a.nsegs;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sbeg[mid] <= c) lo = mid; else hi = mid - 1;
+  }
+  return a.segs[lo];
 }
 
 __device__ __forceinline__ uint32_t bit_width(uint32_t v) { return v ? 32u - __clz(v) : 0u; }
 
+struct PackSmem {
+  uint32_t words[kPackWarps][kPackBlock];  // one block's packed words per warp
+  uint32_t width_of[kPackChunkBlocks];
+  uint32_t prefix16;
+};
+
+// Pack chunk c (of segment sg): firsts, widths, the chunk's payload offset
+// (look-back) and its payload. Ends with every thread done with `sm`.
 template <bool MULTI>
-__global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const __grid_constant__ PackLaunch a) {
-  __shared__ uint32_t words[kPackWarps][kPackBlock];  // one block's packed words per warp
-  __shared__ uint32_t width_of[kPackChunkBlocks];
-  __shared__ uint32_t ticket, prefix16;
+__device__ __forceinline__ void pack_chunk(const PackLaunch& a, PackSmem& sm, uint64_t c,
+                                           const PackSegment& sg) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) ticket = atomicAdd(a.counters + 0, 1u);
-  __syncthreads();
-  const uint64_t c = ticket;  // chunks are taken in ticket order: predecessors already run
-  const PackSegment sg = segment_of<MULTI>(a, c);
   const uint64_t lc = c - sg.chunk_begin;  // chunk within the segment
   const uint64_t chunk_first = lc * kPackChunk;
 
@@ -90,7 +116,7 @@ __global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const __grid_cons
     }
     mx = __reduce_max_sync(0xFFFFFFFFu, mx);
     if (lane == 0) {
-      width_of[lb] = cnt ? bit_width(mx) : 0u;
+      sm.width_of[lb] = cnt ? bit_width(mx) : 0u;
       if (cnt) {
         sg.firsts[start / kPackBlock] = v[0];
         sg.widths[start / kPackBlock] = uint8_t(bit_width(mx));
@@ -101,7 +127,7 @@ __global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const __grid_cons
 
   // ---- the chunk's payload offset (16-byte units): look-back by warp 0
   if (warp == 0) {
-    const uint32_t wl = width_of[lane];
+    const uint32_t wl = sm.width_of[lane];
     const uint32_t agg = __reduce_add_sync(0xFFFFFFFFu, wl);
     // the look-back restarts at each segment's first chunk
     const uint64_t first = sg.chunk_begin;
@@ -114,7 +140,7 @@ __global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const __grid_cons
       p = enc::resolve_prefix<enc::StatusEpoch>(a, c, first, agg, lane, win);
     }
     if (lane == 0) {
-      prefix16 = p;
+      sm.prefix16 = p;
       sg.chunk_off[lc] = uint64_t(p) * 16u;
       if ((lc + 1) * kPackChunk >= sg.count) *sg.payload_bytes = (uint64_t(p) + agg) * 16u;
     }
@@ -122,15 +148,15 @@ __global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const __grid_cons
   __syncthreads();
 
   // ---- pack each block's gaps into words and write them out
-  uint32_t off16 = prefix16;
-  for (int q = 0; q < warp * kBlocksPerWarp; ++q) off16 += width_of[q];
+  uint32_t off16 = sm.prefix16;
+  for (int q = 0; q < warp * kBlocksPerWarp; ++q) off16 += sm.width_of[q];
 #pragma unroll
   for (int q = 0; q < kBlocksPerWarp; ++q) {
     const int lb = warp * kBlocksPerWarp + q;
-    const uint32_t b = width_of[lb];
+    const uint32_t b = sm.width_of[lb];
     if (b != 0u) {  // warp-uniform
       const uint32_t nwords = 4u * b;
-      for (uint32_t w = lane; w < nwords; w += 32) words[warp][w] = 0u;
+      for (uint32_t w = lane; w < nwords; w += 32) sm.words[warp][w] = 0u;
       __syncwarp();
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -138,16 +164,37 @@ __global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const __grid_cons
         if (j >= 1 && j < cnt_blk[q] && gap[q][e] != 0u) {
           const uint32_t bit = (j - 1u) * b;
           const uint32_t w0 = bit >> 5, sh = bit & 31u;
-          atomicOr(&words[warp][w0], gap[q][e] << sh);
-          if (sh + b > 32u) atomicOr(&words[warp][w0 + 1], gap[q][e] >> (32u - sh));
+          atomicOr(&sm.words[warp][w0], gap[q][e] << sh);
+          if (sh + b > 32u) atomicOr(&sm.words[warp][w0 + 1], gap[q][e] >> (32u - sh));
         }
       }
       __syncwarp();
       uint32_t* dst = reinterpret_cast<uint32_t*>(sg.payload + uint64_t(off16) * 16u);
-      for (uint32_t w = lane; w < nwords; w += 32) dst[w] = words[warp][w];
+      for (uint32_t w = lane; w < nwords; w += 32) dst[w] = sm.words[warp][w];
       __syncwarp();
     }
     off16 += b;
+  }
+  __syncthreads();  // the shared words and widths are free again
+}
+
+template <bool MULTI>
+__global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm)
+    pack_kernel(const __grid_constant__ PackLaunch a) {
+  __shared__ PackSmem sm;
+  __shared__ uint32_t ticket;
+  __shared__ uint64_t sbeg[MULTI ? kSegCache : 1];
+  const int tid = threadIdx.x;
+  load_seg_begin<MULTI>(a, sbeg);
+  // Chunks are taken in ticket order, so every smaller ticket is held by a
+  // running CTA. A ticket is taken only when its chunk starts: a ticket held
+  // ahead would keep its aggregate from the look-backs behind it meanwhile.
+  for (;;) {
+    if (tid == 0) ticket = atomicAdd(a.counters + 0, 1u);
+    __syncthreads();
+    const uint64_t c = ticket;
+    if (c >= a.total_chunks) break;  // the same shared word for every thread
+    pack_chunk<MULTI>(a, sm, c, segment_of<MULTI>(a, sbeg, c));  // ends in a CTA barrier
   }
 
   // the last CTA to finish rewinds the ticket and finish counters
@@ -161,12 +208,14 @@ __global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const __grid_cons
   }
 }
 
+struct UnpackSmem {
+  uint32_t words[kPackWarps][kPackBlock + 1];
+};
+
+// Rebuild the indices of chunk c (of segment sg).
 template <bool MULTI>
-__global__ void __launch_bounds__(kPackThreads) unpack_kernel(const __grid_constant__ PackLaunch a) {
-  __shared__ uint32_t words[kPackWarps][kPackBlock + 1];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint64_t c = blockIdx.x;
-  const PackSegment sg = segment_of<MULTI>(a, c);
+__device__ __forceinline__ void unpack_chunk(UnpackSmem& sm, uint64_t c, const PackSegment& sg) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint64_t lc = c - sg.chunk_begin;  // chunk within the segment
   const uint64_t chunk_first = lc * kPackChunk;
   const uint64_t count = sg.count;
@@ -194,8 +243,8 @@ __global__ void __launch_bounds__(kPackThreads) unpack_kernel(const __grid_const
     if (start >= count) break;  // warp-uniform
     const uint32_t cnt = uint32_t(count - start < kPackBlock ? count - start : kPackBlock);
     const uint32_t* src = reinterpret_cast<const uint32_t*>(payload + base_off + uint64_t(pre) * 16u);
-    for (uint32_t w = lane; w < 4u * b; w += 32) words[warp][w] = src[w];
-    if (lane == 0) words[warp][4u * b] = 0u;  // a zero word past the end for two-word reads
+    for (uint32_t w = lane; w < 4u * b; w += 32) sm.words[warp][w] = src[w];
+    if (lane == 0) sm.words[warp][4u * b] = 0u;  // a zero word past the end for two-word reads
     __syncwarp();
     // x_j = gap_j + 1 for j >= 1, x_0 = 0; idx_j = first + inclusive sum of x
     uint32_t x[4];
@@ -207,7 +256,7 @@ __global__ void __launch_bounds__(kPackThreads) unpack_kernel(const __grid_const
       if (j >= 1 && j < cnt && b != 0u) {
         const uint32_t bit = (j - 1u) * b;
         const uint32_t w0 = bit >> 5, sh = bit & 31u;
-        const uint64_t two = uint64_t(words[warp][w0]) | (uint64_t(words[warp][w0 + 1]) << 32);
+        const uint64_t two = uint64_t(sm.words[warp][w0]) | (uint64_t(sm.words[warp][w0 + 1]) << 32);
         g = uint32_t((two >> sh) & ((b == 32u) ? 0xFFFFFFFFull : ((1ull << b) - 1ull)));
       }
       x[e] = (j >= 1 && j < cnt) ? g + 1u : 0u;
@@ -230,6 +279,23 @@ __global__ void __launch_bounds__(kPackThreads) unpack_kernel(const __grid_const
   }
 }
 
+// One CTA per chunk (no ordering between chunks; as short-lived CTAs the
+// chunks overlap better than in a persistent loop).
+template <bool MULTI>
+__global__ void __launch_bounds__(kPackThreads) unpack_kernel(const __grid_constant__ PackLaunch a) {
+  __shared__ UnpackSmem sm;
+  const uint64_t c = blockIdx.x;
+  unpack_chunk<MULTI>(sm, c, segment_of<MULTI>(a, nullptr, c));
+}
+
+// Persistent pack grid: kPackCtasPerSm CTAs per SM, or fewer chunks.
+unsigned pack_grid(uint64_t chunks) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(kPackCtasPerSm);
+  return unsigned(chunks < cap ? chunks : cap);
+}
+
 }  // namespace
 
 uint64_t pack_chunks(uint64_t count) { return (count + kPackChunk - 1) / kPackChunk; }
@@ -248,7 +314,7 @@ cudaError_t launch_pack(const uint32_t* idx, uint64_t count, uint32_t* firsts, u
   a.epoch = epoch;
   a.wait_limit_ns = wait_limit_ns;
   if (a.total_chunks == 0) return cudaSuccess;
-  pack_kernel<false><<<unsigned(a.total_chunks), kPackThreads, 0, stream>>>(a);
+  pack_kernel<false><<<pack_grid(a.total_chunks), kPackThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -265,7 +331,7 @@ cudaError_t launch_pack_multi(const PackSegment* segs, const uint64_t* chunk_beg
   a.counters = counters;
   a.epoch = epoch;
   a.wait_limit_ns = wait_limit_ns;
-  pack_kernel<true><<<unsigned(total_chunks), kPackThreads, 0, stream>>>(a);
+  pack_kernel<true><<<pack_grid(total_chunks), kPackThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
