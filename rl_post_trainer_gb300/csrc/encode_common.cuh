@@ -140,31 +140,32 @@ struct StatusPacked {
   }
 };
 
-// Issue the loads of one look-back window: the kLookbackPerLane x 32 status
-// words before `pos`, nearest first; words before the tensor's first tile
-// read as an inclusive prefix of 0.
-template <class S, class L>
+// Issue the loads of one look-back window: the W x 32 status words before
+// `pos`, nearest first; words before the tensor's first tile read as an
+// inclusive prefix of 0.
+template <class S, class L, int W = kLookbackPerLane>
 __device__ __forceinline__ void load_window(const L& a, int64_t pos, uint64_t first, int lane,
-                                            uint64_t (&w)[kLookbackPerLane]) {
+                                            uint64_t (&w)[W]) {
 #pragma unroll
-  for (int q = 0; q < kLookbackPerLane; ++q) {
-    const int64_t tile = pos - (lane * kLookbackPerLane + q);
+  for (int q = 0; q < W; ++q) {
+    const int64_t tile = pos - (lane * W + q);
     w[q] = tile >= int64_t(first) ? ld_relaxed_u64(a.status + tile)
                                   : S::make(kFlagPrefix, a.epoch, 0u);
   }
 }
 
 // Look-back warp: exclusive prefix of tile g within its tensor (its own
-// aggregate is already published). Reads kLookbackPerLane x 32 predecessor
-// words per round trip, nearest first; waits only on unpublished words that
-// lie before the nearest inclusive prefix; publishes g's inclusive prefix.
-// `w` holds the first window (load_window at g - 1), already in flight.
-// kSleepNs: pause between polls of unpublished words.
-template <class S, class L, unsigned kSleepNs = 32>
+// aggregate is already published). Reads W x 32 predecessor words per round
+// trip, nearest first; waits only on unpublished words that lie before the
+// nearest inclusive prefix; publishes g's inclusive prefix. `w` holds the
+// first window (load_window at g - 1), already in flight. kSleepNs: pause
+// between polls of unpublished words.
+template <class S, class L, unsigned kSleepNs = 32, int W = kLookbackPerLane>
 __device__ __forceinline__ typename S::value_t resolve_prefix(const L& a, uint64_t g,
                                                               uint64_t first,
                                                               typename S::value_t agg, int lane,
-                                                              uint64_t (&w)[kLookbackPerLane]) {
+                                                              uint64_t (&w)[W]) {
+  constexpr int kLookbackPerLane = W;
   using V = typename S::value_t;
   uint64_t* st = a.status;
   if (g == first) return V(0);  // published as an inclusive prefix already
@@ -173,7 +174,7 @@ __device__ __forceinline__ typename S::value_t resolve_prefix(const L& a, uint64
   int64_t pos = int64_t(g) - 1;
   bool gave_up = false;
   for (bool first_window = true;; first_window = false) {
-    if (!first_window) load_window<S>(a, pos, first, lane, w);
+    if (!first_window) load_window<S, L, W>(a, pos, first, lane, w);
     int dp = kNone;  // window distance of the nearest inclusive prefix
     const uint64_t t0 = global_timer_ns();
     for (uint32_t spin = 0;; ++spin) {

@@ -47,6 +47,13 @@ struct PackLaunch {
 };
 
 constexpr int kSegCache = 1024;  // segments whose chunk ranges a CTA keeps in shared memory
+#ifndef PULSE_PACK_LOOKBACK
+#define PULSE_PACK_LOOKBACK 1
+#endif
+// Status words per lane and look-back round trip. The whole CTA waits for
+// its chunk's prefix, so the look-back's own latency is what counts: one word
+// per lane (32 predecessors per round trip) measured faster than 2, 4 or 8.
+constexpr int kPackLookback = PULSE_PACK_LOOKBACK;
 constexpr int kPackCtasPerSm = 8;
 
 // Copy the chunk ranges into shared memory when they fit (multi-segment).
@@ -135,9 +142,11 @@ __device__ __forceinline__ void pack_chunk(const PackLaunch& a, PackSmem& sm, ui
       st_relaxed_u64(a.status + c, make_status(c == first ? kFlagPrefix : kFlagAggregate, a.epoch, agg));
     uint32_t p = 0;
     if (c != first) {
-      uint64_t win[enc::kLookbackPerLane];
-      enc::load_window<enc::StatusEpoch>(a, int64_t(c) - 1, first, lane, win);
-      p = enc::resolve_prefix<enc::StatusEpoch>(a, c, first, agg, lane, win);
+      uint64_t win[kPackLookback];
+      enc::load_window<enc::StatusEpoch, PackLaunch, kPackLookback>(a, int64_t(c) - 1, first, lane,
+                                                                   win);
+      p = enc::resolve_prefix<enc::StatusEpoch, PackLaunch, 32, kPackLookback>(a, c, first, agg,
+                                                                              lane, win);
     }
     if (lane == 0) {
       sm.prefix16 = p;
