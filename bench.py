@@ -329,8 +329,8 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
     flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
              if footprint < 4 * L2_BYTES else None)
     if flush is None:
-        l2_note = (f"inputs ({footprint / 1e9:.3g} GB) larger than L2; "
-                   "prev and w restored untimed before each step")
+        l2_note = (f"step buffers ({footprint / 1e9:.3g} GB: master, prev, w, patch) larger than "
+                   "L2; prev and w restored untimed before each step")
     else:
         l2_note = ("L2 flushed by a 512 MB write after the untimed restore of prev and w, "
                    "before each encode + apply step")
