@@ -47,6 +47,7 @@ import workloads  # noqa: E402
 METRIC = "encode+apply params/s"
 UNIT = "params/s"
 NOMINAL_HBM_GBS = 8000.0
+ONE_THREAD_PARAMS = 100_000_000  # sample of the single-thread oracle timing
 L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 512 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
@@ -469,10 +470,17 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
         chosen, host, total = oracle_sample(specs, cfg["seed"], cfg["eta"], args.cpu_sample_params, dev)
         threads = max(1, min(cores, len(chosen)))
         t, _ = time_oracle(host, threads)
+        del host
+        # the same oracle on one thread, over a smaller sample
+        chosen1, host1, total1 = oracle_sample(specs, cfg["seed"], cfg["eta"],
+                                               min(args.cpu_sample_params, ONE_THREAD_PARAMS), dev)
+        t1, _ = time_oracle(host1, 1)
         out["cpu_baseline"] = {
             "value": total / t, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"first {len(chosen)} tensors ({total} params) of {cfg['name']}, "
-                      f"encode+apply, one oracle call per tensor on {threads} threads"}
+                      f"encode+apply, one oracle call per tensor on {threads} threads",
+            "value_one_thread": total1 / t1,
+            "sample_one_thread": f"first {len(chosen1)} tensors ({total1} params), one thread"}
     return out
 
 
