@@ -373,6 +373,41 @@ def test_multi_apply_both_routes(eta, device_counts):
             np.testing.assert_array_equal(host_u16(s.w), o_prevs[t])
 
 
+@pytest.mark.parametrize("extra", [0, -1])
+@pytest.mark.parametrize("device_counts", [True, False])
+def test_multi_apply_route_boundary(extra, device_counts):
+    """At 64 k = n the chunk-owned route runs, one entry fewer takes the
+    scatter; both write exactly the patch (oracle apply of the same entries)."""
+    dev = _cuda()
+    sizes = [8192 * 5 + 11, 3 * 8192, 8192 + 1]
+    n = sum(sizes)
+    k_total = n // 64 + extra
+    assert (64 * k_total < n) == (extra < 0)
+    rng = np.random.default_rng(321 + extra)
+    ks = [k_total * s // n for s in sizes]
+    ks[0] += k_total - sum(ks)
+    slots, w0s, patches = [], [], []
+    for s, k in zip(sizes, ks):
+        w0 = rng.integers(0, 1 << 16, s, dtype=np.uint64).astype(np.uint16)
+        idx = np.sort(rng.choice(s, size=k, replace=False)).astype(np.uint32)
+        val = rng.integers(0, 1 << 16, k, dtype=np.uint64).astype(np.uint16)
+        slot = pulse.TensorSlot(s, w=dev_u16(w0), idx=dev_u32(idx) if k else
+                                torch.zeros(1, dtype=torch.int32, device=dev),
+                                val=dev_u16(val) if k else torch.zeros(1, dtype=torch.int16, device=dev))
+        slots.append(slot)
+        w0s.append(w0)
+        patches.append((idx, val))
+    with pulse.Plan(slots) as plan:
+        counts = [int(k) for k in ks]
+        plan.apply(torch.tensor(counts, dtype=torch.int64, device=dev) if device_counts else counts)
+        torch.cuda.synchronize()
+        assert plan.get_error() == 0
+        for s, w0, (idx, val) in zip(slots, w0s, patches):
+            want = w0.copy()
+            oracle.apply(want, idx, val)
+            np.testing.assert_array_equal(host_u16(s.w), want)
+
+
 def test_multi_apply_host_counts_and_out_of_range_segment():
     dev = _cuda()
     sizes = [TILE + 3, 2 * TILE]
