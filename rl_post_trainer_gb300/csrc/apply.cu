@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(256)
 //    version (from the partition), asks L2 to prefetch those entries, writes
 //    the chunk's description into the buffer's shared slot and, when the
 //    chunk goes dense, bulk-copies its w into the buffer; it runs up to
-//    kCwBuf chunks ahead of the workers (full / empty mbarriers per buffer),
+//    BUF chunks ahead of the workers (full / empty mbarriers per buffer),
 //    so none of this sits on the workers' path;
 //  * 8 worker warps: per chunk, for each version in order, load the entries
 //    (kCwPre per thread and version in flight at once, for kCwGroup
@@ -330,7 +330,6 @@ __global__ void __launch_bounds__(256)
 //    the changed sectors back whole.
 constexpr int kCwWorkers = 256;                    // 8 worker warps
 constexpr int kCwThreads = kCwWorkers + 32;        // + the producer warp
-constexpr int kCwBuf = 2;                          // chunks staged per CTA
 constexpr int kCwBarrier = 1;                      // the workers' named barrier
 constexpr uint32_t kModeNone = 0, kModeDirect = 1, kModeDense = 2, kModeEnd = 3;
 
@@ -392,11 +391,13 @@ __device__ __forceinline__ bool cw_wait(uint64_t* bar, uint32_t parity, const Cw
 }
 
 // GROUP: versions whose entries are in flight together; PRE: entries per
-// thread and version loaded at once; CTAS: resident CTAs per SM.
-template <int GROUP, int PRE, int CTAS>
+// thread and version loaded at once; CTAS: resident CTAs per SM; BUF: chunks
+// of w staged per CTA (dynamic shared memory, BUF x 16 KB).
+template <int GROUP, int PRE, int CTAS, int BUF>
 __global__ void __launch_bounds__(kCwThreads, CTAS) chunk_apply_kernel(const CwArgs a) {
-  constexpr int kCwGroup = GROUP, kCwPre = PRE;
-  __shared__ __align__(128) uint16_t wsm[kCwBuf][kChunk];
+  constexpr int kCwGroup = GROUP, kCwPre = PRE, kCwBuf = BUF;
+  extern __shared__ __align__(128) uint16_t cw_dyn[];
+  uint16_t(*const wsm)[kChunk] = reinterpret_cast<uint16_t(*)[kChunk]>(cw_dyn);
   __shared__ __align__(16) uint8_t dirty[kChunkSectors];  // one flag byte per 32-byte sector
   __shared__ ChunkSlot slot[kCwBuf];
   __shared__ __align__(8) uint64_t full[kCwBuf], empty[kCwBuf];
@@ -605,23 +606,33 @@ __global__ void __launch_bounds__(kCwThreads, CTAS) chunk_apply_kernel(const CwA
 #define PULSE_CW_PRE_ONE 4
 #endif
 #ifndef PULSE_CW_CTAS_ONE
-#define PULSE_CW_CTAS_ONE 5
+#define PULSE_CW_CTAS_ONE 3
 #endif
 #ifndef PULSE_CW_CTAS_CHAIN
 #define PULSE_CW_CTAS_CHAIN 4
 #endif
+#ifndef PULSE_CW_BUF_ONE
+#define PULSE_CW_BUF_ONE 3
+#endif
+#ifndef PULSE_CW_BUF_CHAIN
+#define PULSE_CW_BUF_CHAIN 2
+#endif
 constexpr int kCwPreOne = PULSE_CW_PRE_ONE, kCwCtasOne = PULSE_CW_CTAS_ONE;
+constexpr int kCwBufOne = PULSE_CW_BUF_ONE, kCwBufChain = PULSE_CW_BUF_CHAIN;
 constexpr int kCwGroupChain = 4, kCwPreChain = 3, kCwCtasChain = PULSE_CW_CTAS_CHAIN;
 
-// Resident CTAs per SM of a persistent kernel (static shared memory only),
-// so that every CTA of the grid is resident from the start.
+// Resident CTAs per SM of a persistent kernel with `dyn` bytes of dynamic
+// shared memory, so that every CTA of the grid is resident from the start.
 template <class K>
-int resident_per_sm(K kernel, int threads, int cap) {
+int resident_per_sm(K kernel, int threads, int cap, size_t dyn) {
+  cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));
   int b = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, 0) != cudaSuccess || b < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, dyn) != cudaSuccess || b < 1)
     b = 1;
   return b < cap ? b : cap;
 }
+
+constexpr size_t cw_smem(int buf) { return size_t(buf) * size_t(kChunk) * sizeof(uint16_t); }
 
 }  // namespace
 
@@ -637,13 +648,13 @@ cudaError_t launch_apply_chunks(const TensorDesc* tensors, int ntensors, uint64_
   cudaGetDevice(&dev);
   apply_partition_kernel<<<unsigned((total_chunks + 255) / 256), 256, 0, stream>>>(
       tensors, chunk_begin, chunk_tensor, counts_dev, total_chunks, chunk_first, error_word, route);
-  auto kernel = chunk_apply_kernel<1, kCwPreOne, kCwCtasOne>;
-  static const int per_sm = resident_per_sm(kernel, kCwThreads, kCwCtasOne);
+  auto kernel = chunk_apply_kernel<1, kCwPreOne, kCwCtasOne, kCwBufOne>;
+  static const int per_sm = resident_per_sm(kernel, kCwThreads, kCwCtasOne, cw_smem(kCwBufOne));
   const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(per_sm);
   const unsigned grid = unsigned(total_chunks < cap ? total_chunks : cap);
   const CwArgs args{tensors, chunk_begin, chunk_tensor, chunk_first, nullptr, counts_dev,
                     0,       1,           total_chunks, error_word, wait_limit_ns, route};
-  kernel<<<grid, kCwThreads, 0, stream>>>(args);
+  kernel<<<grid, kCwThreads, cw_smem(kCwBufOne), stream>>>(args);
   return cudaGetLastError();
 }
 
@@ -673,13 +684,14 @@ cudaError_t launch_apply_chain(const TensorDesc* tensors, const uint64_t* chunk_
   chain_partition_kernel<<<unsigned((parts + 255) / 256), 256, 0, stream>>>(
       tensors, chunk_begin, chunk_tensor, segs, ntensors, nversions, total_chunks, chain_first,
       error_word);
-  auto kernel = chunk_apply_kernel<kCwGroupChain, kCwPreChain, kCwCtasChain>;
-  static const int per_sm = resident_per_sm(kernel, kCwThreads, kCwCtasChain);
+  auto kernel = chunk_apply_kernel<kCwGroupChain, kCwPreChain, kCwCtasChain, kCwBufChain>;
+  static const int per_sm =
+      resident_per_sm(kernel, kCwThreads, kCwCtasChain, cw_smem(kCwBufChain));
   const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(per_sm);
   const unsigned grid = unsigned(total_chunks < cap ? total_chunks : cap);
   const CwArgs args{tensors,  chunk_begin,  chunk_tensor, chain_first, segs, nullptr,
                     ntensors, nversions,    total_chunks, error_word,  wait_limit_ns, nullptr};
-  kernel<<<grid, kCwThreads, 0, stream>>>(args);
+  kernel<<<grid, kCwThreads, cw_smem(kCwBufChain), stream>>>(args);
   return cudaGetLastError();
 }
 

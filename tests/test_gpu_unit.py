@@ -376,12 +376,13 @@ def test_multi_apply_both_routes(eta, device_counts):
 @pytest.mark.parametrize("extra", [0, -1])
 @pytest.mark.parametrize("device_counts", [True, False])
 def test_multi_apply_route_boundary(extra, device_counts):
-    """At 64 k = n the chunk-owned route runs, one entry fewer takes the
-    scatter; both write exactly the patch (oracle apply of the same entries)."""
+    """With the fewest entries for which 64 k >= n the chunk-owned route runs,
+    one entry fewer takes the scatter; both write exactly the patch (oracle
+    apply of the same entries)."""
     dev = _cuda()
     sizes = [8192 * 5 + 11, 3 * 8192, 8192 + 1]
     n = sum(sizes)
-    k_total = n // 64 + extra
+    k_total = (n + 63) // 64 + extra
     assert (64 * k_total < n) == (extra < 0)
     rng = np.random.default_rng(321 + extra)
     ks = [k_total * s // n for s in sizes]
@@ -391,9 +392,10 @@ def test_multi_apply_route_boundary(extra, device_counts):
         w0 = rng.integers(0, 1 << 16, s, dtype=np.uint64).astype(np.uint16)
         idx = np.sort(rng.choice(s, size=k, replace=False)).astype(np.uint32)
         val = rng.integers(0, 1 << 16, k, dtype=np.uint64).astype(np.uint16)
-        slot = pulse.TensorSlot(s, w=dev_u16(w0), idx=dev_u32(idx) if k else
-                                torch.zeros(1, dtype=torch.int32, device=dev),
-                                val=dev_u16(val) if k else torch.zeros(1, dtype=torch.int16, device=dev))
+        # segments with room for n entries (device counts are checked against that)
+        idx_room, val_room = np.zeros(s, np.uint32), np.zeros(s, np.uint16)
+        idx_room[:k], val_room[:k] = idx, val
+        slot = pulse.TensorSlot(s, w=dev_u16(w0), idx=dev_u32(idx_room), val=dev_u16(val_room))
         slots.append(slot)
         w0s.append(w0)
         patches.append((idx, val))
