@@ -601,7 +601,11 @@ __global__ void __launch_bounds__(kCwThreads, CTAS) chunk_apply_kernel(const CwA
   }
 }
 
-// whole-model apply (one version) and chained apply (up to 16 versions)
+// whole-model apply (one version) and chained apply (up to 16 versions).
+// One version: three chunk buffers at three CTAs per SM keep more of w's
+// bulk copies in flight than two at five (8.03B step: 4.99 against 5.53 ms);
+// the chained form, with four versions' entry loads per chunk, measured best
+// at two buffers and four CTAs.
 #ifndef PULSE_CW_PRE_ONE
 #define PULSE_CW_PRE_ONE 4
 #endif
