@@ -11,7 +11,7 @@ model. Before every step prev and the sampler weights are restored from a
 pristine copy (untimed), so every timed step encodes the same real update.
 Inputs (48 GB) are far larger than L2 (129 MB), so no L2 flush is needed;
 a workload whose buffers fit in a few L2s (the single 2^20 tensor) gets a
-512 MB scratch write after the restore, before every step.
+1 GiB scratch write after the restore, before every step.
 
 Printed: one JSON line with params/s (value), the roofline of the encode
 kernel against measured HBM copy bandwidth, the XOR-mask path, the MXFP8,
@@ -49,7 +49,7 @@ UNIT = "params/s"
 NOMINAL_HBM_GBS = 8000.0
 ONE_THREAD_PARAMS = 100_000_000  # sample of the single-thread oracle timing
 L2_BYTES = 129 * 1024 * 1024
-FLUSH_BYTES = 512 * 1024 * 1024
+FLUSH_BYTES = 1024 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "encode_multi_llama3_8b.md")
 ENCODE_SRCS = [os.path.join(ROOT, "rl_post_trainer_gb300", "csrc", f)
@@ -333,7 +333,7 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
         l2_note = (f"step buffers ({footprint / 1e9:.3g} GB: master, prev, w, patch) larger than "
                    "L2; prev and w restored untimed before each step")
     else:
-        l2_note = ("L2 flushed by a 512 MB write after the untimed restore of prev and w, "
+        l2_note = ("L2 flushed by a 1 GiB write after the untimed restore of prev and w, "
                    "before each encode + apply step")
 
     def step(ev=None):
