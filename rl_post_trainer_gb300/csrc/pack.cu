@@ -83,7 +83,7 @@ __device__ __forceinline__ PackSegment segment_of(const PackLaunch& a, const uin
 __device__ __forceinline__ uint32_t bit_width(uint32_t v) { return v ? 32u - __clz(v) : 0u; }
 
 struct PackSmem {
-  uint32_t words[kPackWarps][kPackBlock];  // one block's packed words per warp
+  uint32_t words[kPackWarps][kBlocksPerWarp][kPackBlock];  // every block's packed words
   uint32_t width_of[kPackChunkBlocks];
   uint32_t prefix16;
 };
@@ -132,7 +132,27 @@ __device__ __forceinline__ void pack_chunk(const PackLaunch& a, PackSmem& sm, ui
   }
   __syncthreads();
 
-  // ---- the chunk's payload offset (16-byte units): look-back by warp 0
+  // ---- every block's gaps into shared words; warp 0 first finds the chunk's
+  // payload offset (16-byte units) with the look-back, so the other warps
+  // pack while it waits
+  auto pack_words = [&](int q) {
+    const int lb = warp * kBlocksPerWarp + q;
+    const uint32_t b = sm.width_of[lb];
+    if (b == 0u) return;  // warp-uniform
+    uint32_t* words = sm.words[warp][q];
+    for (uint32_t w = lane; w < 4u * b; w += 32) words[w] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+      if (j >= 1 && j < cnt_blk[q] && gap[q][e] != 0u) {
+        const uint32_t bit = (j - 1u) * b;
+        const uint32_t w0 = bit >> 5, sh = bit & 31u;
+        atomicOr(&words[w0], gap[q][e] << sh);
+        if (sh + b > 32u) atomicOr(&words[w0 + 1], gap[q][e] >> (32u - sh));
+      }
+    }
+  };
   if (warp == 0) {
     const uint32_t wl = sm.width_of[lane];
     const uint32_t agg = __reduce_add_sync(0xFFFFFFFFu, wl);
@@ -154,34 +174,18 @@ __device__ __forceinline__ void pack_chunk(const PackLaunch& a, PackSmem& sm, ui
       if ((lc + 1) * kPackChunk >= sg.count) *sg.payload_bytes = (uint64_t(p) + agg) * 16u;
     }
   }
-  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kBlocksPerWarp; ++q) pack_words(q);
+  __syncthreads();  // the offset and every block's words are in shared memory
 
-  // ---- pack each block's gaps into words and write them out
+  // ---- write the words out
   uint32_t off16 = sm.prefix16;
   for (int q = 0; q < warp * kBlocksPerWarp; ++q) off16 += sm.width_of[q];
 #pragma unroll
   for (int q = 0; q < kBlocksPerWarp; ++q) {
-    const int lb = warp * kBlocksPerWarp + q;
-    const uint32_t b = sm.width_of[lb];
-    if (b != 0u) {  // warp-uniform
-      const uint32_t nwords = 4u * b;
-      for (uint32_t w = lane; w < nwords; w += 32) sm.words[warp][w] = 0u;
-      __syncwarp();
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
-        if (j >= 1 && j < cnt_blk[q] && gap[q][e] != 0u) {
-          const uint32_t bit = (j - 1u) * b;
-          const uint32_t w0 = bit >> 5, sh = bit & 31u;
-          atomicOr(&sm.words[warp][w0], gap[q][e] << sh);
-          if (sh + b > 32u) atomicOr(&sm.words[warp][w0 + 1], gap[q][e] >> (32u - sh));
-        }
-      }
-      __syncwarp();
-      uint32_t* dst = reinterpret_cast<uint32_t*>(sg.payload + uint64_t(off16) * 16u);
-      for (uint32_t w = lane; w < nwords; w += 32) dst[w] = sm.words[warp][w];
-      __syncwarp();
-    }
+    const uint32_t b = sm.width_of[warp * kBlocksPerWarp + q];
+    uint32_t* dst = reinterpret_cast<uint32_t*>(sg.payload + uint64_t(off16) * 16u);
+    for (uint32_t w = lane; w < 4u * b; w += 32) dst[w] = sm.words[warp][q][w];
     off16 += b;
   }
   __syncthreads();  // the shared words and widths are free again
