@@ -181,8 +181,10 @@ __device__ __forceinline__ void cc_producer(const CcArgs& a, CcShared& sh, int l
 // ---------------------------------------------------------- look-back warp
 
 // Copy a parked chunk's entries to positions prefix + k of its tensor's
-// output (16-byte index and 8-byte value stores after a head of up to 3
-// entries). Positions at or past the segment's room are never written.
+// output. Lane l moves entries l, l + 32, l + 64, ...: the ring reads are
+// free of bank conflicts and every store instruction of the warp covers 32
+// consecutive positions (four in flight per lane). Positions at or past the
+// segment's room are never written.
 __device__ __forceinline__ void cc_copy_out(const CcParked& pm, uint32_t prefix,
                                             const uint32_t* ring, int lane) {
   const uint32_t agg = pm.agg;
@@ -190,30 +192,22 @@ __device__ __forceinline__ void cc_copy_out(const CcParked& pm, uint32_t prefix,
   uint32_t* const oi = pm.out.idx;
   uint16_t* const ov = pm.out.val;
   const uint64_t cap = pm.out.cap;
-  const bool vec = (reinterpret_cast<uintptr_t>(oi) % 16u == 0) &&
-                   (reinterpret_cast<uintptr_t>(ov) % 8u == 0) && uint64_t(prefix) + agg <= cap;
-  uint32_t head = vec ? ((4u - (prefix & 3u)) & 3u) : agg;
-  if (head > agg) head = agg;
-  const uint32_t body = vec ? ((agg - head) & ~3u) : 0u;
-  for (uint32_t k = uint32_t(lane); k < head; k += 32) {
-    const uint32_t ent = ring[(pm.ring_start + k) & kCcRingMask];
-    const uint64_t pos = uint64_t(prefix) + k;
-    if (pos < cap) {
-      oi[pos] = base + (ent & 0xFFFFu);
-      ov[pos] = uint16_t(ent >> 16);
+  const bool inb = uint64_t(prefix) + agg <= cap;
+  uint32_t k = uint32_t(lane);
+  if (inb) {
+    for (; k + 96u < agg; k += 128u) {
+      uint32_t e[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) e[q] = ring[(pm.ring_start + k + 32u * q) & kCcRingMask];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint64_t pos = uint64_t(prefix) + k + 32u * q;
+        oi[pos] = base + (e[q] & 0xFFFFu);
+        ov[pos] = uint16_t(e[q] >> 16);
+      }
     }
   }
-  for (uint32_t k = head + uint32_t(lane) * 4u; k < head + body; k += 128u) {
-    uint32_t e[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) e[q] = ring[(pm.ring_start + k + uint32_t(q)) & kCcRingMask];
-    const uint64_t pos = uint64_t(prefix) + k;  // a multiple of 4
-    *reinterpret_cast<uint4*>(oi + pos) = make_uint4(base + (e[0] & 0xFFFFu), base + (e[1] & 0xFFFFu),
-                                                     base + (e[2] & 0xFFFFu), base + (e[3] & 0xFFFFu));
-    *reinterpret_cast<uint2*>(ov + pos) =
-        make_uint2((e[0] >> 16) | (e[1] & 0xFFFF0000u), (e[2] >> 16) | (e[3] & 0xFFFF0000u));
-  }
-  for (uint32_t k = head + body + uint32_t(lane); k < agg; k += 32) {
+  for (; k < agg; k += 32u) {
     const uint32_t ent = ring[(pm.ring_start + k) & kCcRingMask];
     const uint64_t pos = uint64_t(prefix) + k;
     if (pos < cap) {
@@ -423,7 +417,8 @@ __device__ __forceinline__ void cc_compute(const CcArgs& a, CcShared& sh, int ti
     if (lane == 0) mbar_arrive(&sh.agg_ready[q]);
     ++posted;
     ring_head += agg;
-    compute_barrier();  // the image is written again by the next chunk only after every thread parked
+    // the next chunk writes the image only after the barrier at the top of
+    // the loop, which every thread reaches after parking this one
   }
   for (uint32_t e = posted > uint32_t(kPendSlots) ? posted - kPendSlots : 0u; e < posted; ++e)
     wait_or_flag(&sh.slot_free[e % kPendSlots], (e / kPendSlots) & 1u, a);
