@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(kCwThreads, CTAS) chunk_apply_kernel(const CwA
 #endif
 constexpr int kCwPreOne = PULSE_CW_PRE_ONE, kCwCtasOne = PULSE_CW_CTAS_ONE;
 constexpr int kCwBufOne = PULSE_CW_BUF_ONE, kCwBufChain = PULSE_CW_BUF_CHAIN;
-constexpr int kCwGroupChain = 4, kCwPreChain = 3, kCwCtasChain = PULSE_CW_CTAS_CHAIN;
+constexpr int kCwGroupChain = 2, kCwPreChain = 3, kCwCtasChain = PULSE_CW_CTAS_CHAIN;
 
 // Resident CTAs per SM of a persistent kernel with `dyn` bytes of dynamic
 // shared memory, so that every CTA of the grid is resident from the start.
