@@ -35,7 +35,7 @@ constexpr int kCcWords = kCcChunk / 32;      // bitmap words, one per compute th
 static_assert(kCcWords == kEncThreads, "one bitmap word per compute thread");
 static_assert(kCcChunk <= 0x10000, "chunk-local indices fit the ring entry's low half");
 constexpr int kCcStages = 3;                 // chunks prepared ahead by the producer
-constexpr int kCcGroup = 4;                  // versions whose entries are loaded together
+constexpr int kCcGroup = 1;                  // versions whose entries are loaded together
 constexpr int kCcPre = 3;                    // entries per thread and version loaded at once
 constexpr int kCcMinBlocks = 3;              // resident CTAs per SM
 #ifndef PULSE_CC_LB_SLEEP
