@@ -14,7 +14,8 @@ a workload whose buffers fit in a few L2s (the single 2^20 tensor) gets a
 1 GiB scratch write after the restore, before every step.
 
 Printed: one JSON line with params/s (value), the roofline of the encode
-kernel against measured HBM copy bandwidth, the XOR-mask path, the MXFP8,
+kernel against measured HBM copy bandwidth, the same step at eta = 3e-7
+(about 1 % of the view changed, the pages' steady state), the XOR-mask path, the MXFP8,
 MXFP4 and NVFP4 serving views of the same step (their own encode + apply),
 the sidecar catch-up legs, index packing, PULSELoCo, an end-to-end number
 through host buffers, the CPU oracle baseline, and the SM clocks sampled
@@ -47,9 +48,9 @@ import workloads  # noqa: E402
 METRIC = "encode+apply params/s"
 UNIT = "params/s"
 NOMINAL_HBM_GBS = 8000.0
-ONE_THREAD_PARAMS = 100_000_000  # sample of the single-thread oracle timing
 L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 1024 * 1024 * 1024
+SPARSE_ETA = 3e-7
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "encode_multi_llama3_8b.md")
 ENCODE_SRCS = [os.path.join(ROOT, "rl_post_trainer_gb300", "csrc", f)
@@ -268,22 +269,29 @@ def oracle_sample(specs, seed, eta, max_params, dev):
 
 
 def time_oracle(host_pairs, threads):
-    """Wall time of oracle encode + apply over the sample (tensors spread over
-    `threads` host threads; the oracle code itself is single-threaded)."""
+    """Wall time of the oracle's encode + apply over the sample, tensor by
+    tensor. threads == 1: the plain single-threaded calls. Otherwise every
+    tensor is split into 4 x threads contiguous chunks run on `threads` host
+    threads: a count pass, an exclusive scan of the chunk counts, an emit pass
+    into place, then the apply over ranges of the patch (the same scalar C
+    loops; oracle.encode_chunked / apply_chunked)."""
     import oracle
     oracle.build()
     work = [(m, p.copy(), p.copy()) for m, p in host_pairs]
-
-    def one(item):
-        m, prev, w = item
-        idx, val = oracle.encode(m, prev)
-        oracle.apply(w, idx, val)
-        return idx.size
-
+    k = 0
     t0 = time.perf_counter()
-    with ThreadPoolExecutor(max_workers=threads) as ex:
-        ks = list(ex.map(one, work))
-    return time.perf_counter() - t0, sum(ks)
+    if threads == 1:
+        for m, prev, w in work:
+            idx, val = oracle.encode(m, prev)
+            oracle.apply(w, idx, val)
+            k += idx.size
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as pool:
+            for m, prev, w in work:
+                idx, val = oracle.encode_chunked(m, prev, pool, 4 * threads)
+                oracle.apply_chunked(w, idx, val, pool, 4 * threads)
+                k += idx.size
+    return time.perf_counter() - t0, k
 
 
 # ----------------------------------------------------------------- arms
@@ -293,7 +301,7 @@ def run_reference(args, cfg, specs, rank, world, dist_on):
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
     cores = host_cores()
     chosen, host, total = oracle_sample(specs, cfg["seed"], cfg["eta"], args.cpu_sample_params, dev)
-    threads = max(1, min(cores, len(chosen)))
+    threads = cores
     for _ in range(args.warmup):
         time_oracle(host, threads)
     times, ks = [], []
@@ -304,7 +312,8 @@ def run_reference(args, cfg, specs, rank, world, dist_on):
     tt = sum(times)
     value = total * args.steps / tt
     sample = (f"first {len(chosen)} tensors of {cfg['name']} ({total} of "
-              f"{workloads.total_params(specs)} params), encode+apply, {threads} threads")
+              f"{workloads.total_params(specs)} params), encode+apply tensor by tensor, each "
+              f"tensor chunk-parallel on {threads} threads (count pass, scan, emit pass)")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
@@ -413,9 +422,8 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
                   "frac_sector_rmw_measured_peak": app_rmw / app_s / 1e9 / peak,
                   "frac_sector_rmw_nominal_8tbs": app_rmw / app_s / 1e9 / NOMINAL_HBM_GBS},
         "sectors_touched": S,
-        # encode, then the apply's route, partition, chunk-owned and scatter
-        # launches (the route not taken returns at once)
-        "gpu_launches": 5 * args.steps,
+        # one encode launch and one apply launch per step
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),
     }
 
@@ -448,6 +456,8 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
         del wl.prev_x, wl.w_x, wl.mask
         wl.xplan.close()
 
+    if cfg.get("sparse_eta") and not args.no_sparse:
+        out["sparse"] = run_sparse(args, cfg, specs, wl, dev, rank, peak, cfg["sparse_eta"])
     if cfg.get("sweep"):
         out["sweep"] = run_sweep(args, specs, cfg["seed"], dev, peak)
     if not args.no_mx:
@@ -468,20 +478,83 @@ def run_ours(args, cfg, specs, rank, world, dist_on):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = host_cores()
         chosen, host, total = oracle_sample(specs, cfg["seed"], cfg["eta"], args.cpu_sample_params, dev)
-        threads = max(1, min(cores, len(chosen)))
+        threads = cores
         t, _ = time_oracle(host, threads)
+        # the same sample through the plain single-threaded oracle
+        t1, _ = time_oracle(host, 1)
         del host
-        # the same oracle on one thread, over a smaller sample
-        chosen1, host1, total1 = oracle_sample(specs, cfg["seed"], cfg["eta"],
-                                               min(args.cpu_sample_params, ONE_THREAD_PARAMS), dev)
-        t1, _ = time_oracle(host1, 1)
         out["cpu_baseline"] = {
             "value": total / t, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"first {len(chosen)} tensors ({total} params) of {cfg['name']}, "
-                      f"encode+apply, one oracle call per tensor on {threads} threads",
-            "value_one_thread": total1 / t1,
-            "sample_one_thread": f"first {len(chosen1)} tensors ({total1} params), one thread"}
+                      f"encode+apply tensor by tensor, each tensor chunk-parallel on {threads} "
+                      "threads (count pass, scan, emit pass, apply over patch ranges)",
+            "value_one_thread": total / t1,
+            "sample_one_thread": "the same sample, plain single-threaded oracle calls",
+            "speedup": t1 / t}
     return out
+
+
+def regen_masters(wl, specs, seed, eta, dev):
+    """Redraw the FP32 masters in place at update scale `eta`: the generator
+    sequence of the workload (per tensor: w0, then z), so the saved view of
+    w0 (prev0) still holds."""
+    gen = workloads.torch_generator(dev, seed)
+    for m, spec in zip(wl.master, specs):
+        workloads.torch_init_(m, spec, gen)
+        workloads.torch_update_(m, eta, gen)
+
+
+def run_sparse(args, cfg, specs, wl, dev, rank, peak, eta):
+    """The same model and initial weights at a smaller update scale (about
+    1 % of the BF16 view changes at eta = 3e-7, the pages' steady-state
+    regime): encode + apply timed like the headline step (prev and w restored
+    untimed before every step). The masters are redrawn at `eta` first and at
+    the workload's own scale afterwards."""
+    seed = cfg["seed"] + 1000 * rank
+    regen_masters(wl, specs, seed, eta, dev)
+    stream = torch.cuda.current_stream(dev)
+    n = wl.n
+    for _ in range(args.warmup):
+        wl.restore()
+        wl.plan.encode(wl.counts)
+        wl.plan.apply(wl.counts)
+    torch.cuda.synchronize()
+    counts_np = wl.counts.cpu().numpy()
+    k = int(counts_np.sum())
+    te, ta = [], []
+    for _ in range(args.steps):
+        wl.restore()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        wl.plan.encode(wl.counts)
+        ev[1].record(stream)
+        wl.plan.apply(wl.counts)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        te.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+        ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+    if wl.plan.get_error() != 0:
+        raise RuntimeError("device error in the sparse-regime steps")
+    for t in range(len(specs)):
+        if not torch.equal(wl.w[t], wl.prev[t]):
+            raise RuntimeError(f"sampler weights differ from the trainer view (tensor {t})")
+    S = wl.sectors_touched(counts_np)
+    regen_masters(wl, specs, seed, cfg["eta"], dev)
+    e_s, a_s = float(np.mean(te)), float(np.mean(ta))
+    enc_alg, enc_sec = 6.0 * n + 8.0 * k, 6.0 * n + 32.0 * S + 6.0 * k
+    app_rmw = 6.0 * k + 64.0 * S
+    return {
+        "eta": eta, "density": k / n, "patch_entries": k, "sectors_touched": S,
+        "encode_ms": 1e3 * e_s, "apply_ms": 1e3 * a_s, "params_per_s": n / (e_s + a_s),
+        "encode_gbs_algorithmic": enc_alg / e_s / 1e9,
+        "encode_frac_measured_peak": enc_alg / e_s / 1e9 / peak,
+        "encode_frac_sector_measured_peak": enc_sec / e_s / 1e9 / peak,
+        "apply_gbs_sector_rmw": app_rmw / a_s / 1e9,
+        "apply_frac_sector_rmw_measured_peak": app_rmw / a_s / 1e9 / peak,
+        "bytes_model": "encode 6n + 8k (sector 6n + 32S + 6k); apply 6k + 64S",
+        "gpu_launches": 2 * args.steps,
+    }
 
 
 def run_mx(args, cfg, specs, wl, dev, rank, peak, fmt=0):
@@ -602,7 +675,10 @@ def run_mx(args, cfg, specs, wl, dev, rank, peak, fmt=0):
         "encode_frac_measured_peak": enc_alg / e_s / 1e9 / peak,
         "encode_frac_sector_measured_peak": enc_sec / e_s / 1e9 / peak,
         "apply_gbs_sector_rmw": app_rmw / a_s / 1e9,
-        "bytes_model": f"encode {model} + 6k + 6ks (sector: {model} + 32S + 5k + 5ks)",
+        "apply_frac_sector_rmw_measured_peak": app_rmw / a_s / 1e9 / peak,
+        "sectors_touched": sc_codes + sc_scales,
+        "bytes_model": f"encode {model} + 6k + 6ks (sector: {model} + 32S + 5k + 5ks); "
+                       "apply 5k + 5ks + 64S (each touched 32-byte sector read and written)",
         "gpu_launches": (3 if fmt == pulse.MX_NVFP4 else 2) * args.steps,
     }
 
@@ -1069,6 +1145,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-xor", action="store_true")
+    ap.add_argument("--no-sparse", action="store_true",
+                    help="skip the eta = 3e-7 (about 1 %% dense) leg of the 8B workload")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8-, MXFP4- and NVFP4-view legs")
     ap.add_argument("--no-compose", action="store_true", help="skip the patch-chain leg")
     ap.add_argument("--no-loco", action="store_true", help="skip the PULSELoCo leg")
@@ -1087,6 +1165,9 @@ def main():
     if cfg["eta"] is None:  # the density sweep: the headline at the default scale, then every scale
         cfg["eta"] = workloads.ETA_DEFAULT
         cfg["sweep"] = True
+    if args.config == 3:
+        # the same model at the pages' steady-state density (about 1 % changed)
+        cfg["sparse_eta"] = SPARSE_ETA
     specs = cfg["specs"]()
 
     if args.impl == "reference":

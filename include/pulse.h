@@ -61,7 +61,7 @@ extern "C" {
 /* Status codes. */
 #define PULSE_OK           0  /* success */
 #define PULSE_ERR_INVALID  1  /* null pointer where one is required, bad count, overlap */
-#define PULSE_ERR_RANGE    2  /* an element count is >= 2^32 */
+#define PULSE_ERR_RANGE    2  /* an element count is >= 2^32 (past PULSE_NOALLOC_MAX_ELEMS for pulse_encode_noalloc) */
 #define PULSE_ERR_CUDA     3  /* a CUDA runtime call or kernel launch failed */
 #define PULSE_ERR_TIMEOUT  4  /* device: a bounded wait gave up; outputs of that call are invalid */
 #define PULSE_ERR_INDEX    5  /* device: a checked apply met an index >= n and skipped it */
@@ -216,26 +216,20 @@ int pulse_encode_multi(pulse_plan *plan, uint64_t *counts_out, cudaStream_t stre
 /*
  * Apply every tensor's patch segment to the whole model. counts_host (HOST,
  * ntensors uint64) gives each segment's length; it is copied before the call
- * returns. Each segment must list ascending indices (what encode writes).
- * The route follows from the counts (here on the host):
- *  - k = sum of the counts, n = sum of the tensor sizes; when 64 k >= n the
- *    tensor is cut into chunks, each chunk's entries are found by binary
- *    search, and a chunk with many entries is read-modified-written in shared
- *    memory and its changed 32-byte sectors written back whole;
- *  - when 64 k < n (a sparse patch) the entries are scattered straight into
- *    w (each target sector prefetched into L2 first), which moves only the
- *    touched sectors.
- * Entries with idx >= n are skipped and recorded as PULSE_ERR_INDEX in the
- * plan's error word; on the chunk route so are entries outside their chunk
- * (a segment that is not ascending), while the scatter route stores such
- * entries in patch order.
+ * returns. One launch (per 16384 tensors) scatters every entry straight into
+ * w: consecutive entries of a segment go to consecutive threads, so the
+ * partial-sector stores of an ascending segment reach L2 as one request per
+ * 32-byte sector, and only the touched sectors of w move (each read once for
+ * its untouched bytes and written once). Segments from encode are ascending
+ * with distinct indices; in a segment that repeats an index, which of the
+ * repeated entries lands is unspecified. Entries with idx >= n are skipped
+ * and recorded as PULSE_ERR_INDEX in the plan's error word, and a count
+ * larger than its tensor is clamped to n and recorded the same way.
  */
 int pulse_apply_multi(pulse_plan *plan, const uint64_t *counts_host, cudaStream_t stream);
 
 /* As pulse_apply_multi with the counts in DEVICE memory (e.g. counts_out of
- * pulse_encode_multi), so no host round trip is needed: a one-CTA launch
- * picks the route on the device and the launches of the route not taken
- * return at once. */
+ * pulse_encode_multi), so no host round trip is needed. */
 int pulse_apply_multi_device(pulse_plan *plan, const uint64_t *counts_dev, cudaStream_t stream);
 
 /*
@@ -706,12 +700,15 @@ int pulse_nvfp4_encode_multi(pulse_mx_plan *plan, uint64_t *counts_out, float *t
  *  - n may be at most PULSE_NOALLOC_MAX_ELEMS (2^28); larger n returns
  *    PULSE_ERR_RANGE and launches nothing.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress) with that device current and keeps it for the
+ *    rest of the process; make that first call before any stream capture.
+ *    After cudaDeviceReset the kept address is stale: do not call this entry
+ *    point on a device that has been reset.
  *  - All calls share the array and it keeps the previous call's contents;
- *    each call clears the counters it needs. Calls whose work may overlap on
- *    the GPU (different streams without ordering) race on the array: order
- *    them.
+ *    each call clears, on its stream before its kernel, the part it reads
+ *    (8 bytes per 4096 elements plus 256 bytes). Calls whose work may
+ *    overlap on the GPU (different streams without ordering) race on the
+ *    array: order them.
  *  - Device-side errors are not kept for pulse_get_error: a wait that gave
  *    up is reported as *count_out == UINT64_MAX (outputs invalid).
  */

@@ -19,6 +19,8 @@ from .oracle import (  # noqa: F401
     apply_multi,
     xor_mask_multi,
     xor_apply_multi,
+    encode_chunked,
+    apply_chunked,
     MX_BLOCK,
     e4m3_rne,
     mx_block_scale,

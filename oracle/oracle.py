@@ -199,6 +199,68 @@ def xor_mask_multi(masters, prevs):
     return [xor_mask(m, p) for m, p in zip(masters, prevs)]
 
 
+# ------------------------------------------- the same code on many host cores
+
+def _chunks(n: int, parts: int):
+    step = -(-n // max(1, parts))
+    return [(c0, min(n, c0 + step)) for c0 in range(0, n, max(1, step))]
+
+
+def encode_chunked(master: np.ndarray, prev: np.ndarray, pool, parts: int):
+    """The scalar encode spread over host threads, for timing the oracle on
+    every core (not a second definition: it calls the same C loops).
+
+    Count pass: each of ``parts`` contiguous chunks counts its changed
+    elements (``oracle_count_changed``). An exclusive scan of those counts
+    gives each chunk's first patch slot. Emit pass: each chunk runs
+    ``oracle_encode`` on its slice into its slots and shifts the slice-local
+    indices by the chunk's start. Concatenated in chunk order the result is
+    the single-threaded patch. ``pool`` is a thread pool (ctypes releases the
+    interpreter lock during the C calls). Returns (idx, val); refreshes
+    ``prev``."""
+    _check(master, np.float32, "master")
+    _check(prev, np.uint16, "prev", writable=True)
+    if master.size != prev.size:
+        raise ValueError("master and prev differ in length")
+    lib = _load()
+    spans = _chunks(master.size, parts)
+    counts = list(pool.map(
+        lambda s: int(lib.oracle_count_changed(_ptr(master[s[0]:]), _ptr(prev[s[0]:]),
+                                               s[1] - s[0])), spans))
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    k = int(offs[-1])
+    idx = np.empty(max(k, 1), dtype=np.uint32)
+    val = np.empty(max(k, 1), dtype=np.uint16)
+
+    def emit(i):
+        c0, c1 = spans[i]
+        o = int(offs[i])
+        got = lib.oracle_encode(_ptr(master[c0:]), _ptr(prev[c0:]), c1 - c0,
+                                _ptr(idx[o:]), _ptr(val[o:]))
+        if got != counts[i]:
+            raise RuntimeError("emit pass disagrees with the count pass")
+        idx[o:o + got] += np.uint32(c0)
+
+    list(pool.map(emit, range(len(spans))))
+    return idx[:k], val[:k]
+
+
+def apply_chunked(w: np.ndarray, idx: np.ndarray, val: np.ndarray, pool, parts: int) -> None:
+    """``oracle_apply`` over contiguous ranges of the patch on host threads.
+    Patch indices are distinct (an encode patch is strictly ascending), so the
+    ranges write disjoint elements and the order between them is immaterial."""
+    _check(w, np.uint16, "w", writable=True)
+    _check(idx, np.uint32, "idx")
+    _check(val, np.uint16, "val")
+    if idx.size != val.size:
+        raise ValueError("idx and val differ in length")
+    if idx.size and int(idx.max()) >= w.size:
+        raise IndexError("patch index out of range")
+    lib = _load()
+    list(pool.map(lambda s: lib.oracle_apply(_ptr(w), _ptr(idx[s[0]:]), _ptr(val[s[0]:]),
+                                             s[1] - s[0]), _chunks(idx.size, parts)))
+
+
 def xor_apply_multi(ws, masks) -> None:
     for w, m in zip(ws, masks):
         xor_apply(w, m)

@@ -38,7 +38,6 @@ constexpr uint64_t kMaxTiles = 0x7FFFFFFFull;      // tile tickets are uint32
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s per bounded wait
 constexpr size_t kCounterBytes = 256;               // ticket, finished, error (+ padding)
 constexpr int kAmaxWord = 8;  // counters word holding a single-tensor NVFP4 maximum
-constexpr int kRouteWord = 12;  // counters word holding a whole-model apply's route
 constexpr int kMaxTensorsPerApplyLaunch = 16384;     // bound on the apply kernel's smem table
 
 uint64_t div_up(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
@@ -359,7 +358,6 @@ struct pulse_plan {
   uint64_t total_chunks = 0;
   uint64_t* chunk_begin = nullptr;  // device, ntensors + 1
   uint32_t* chunk_tensor = nullptr; // device, total_chunks
-  uint32_t* chunk_first = nullptr;  // device, total_chunks (scratch)
   // chained apply: per-call patch table and partition scratch (grown on demand)
   ChainSeg* chain_segs = nullptr;   // device, chain_seg_cap entries
   uint64_t chain_seg_cap = 0;
@@ -399,7 +397,9 @@ const char* pulse_error_string(int status) {
   switch (status) {
     case PULSE_OK: return "PULSE_OK";
     case PULSE_ERR_INVALID: return "PULSE_ERR_INVALID: invalid argument";
-    case PULSE_ERR_RANGE: return "PULSE_ERR_RANGE: element count must be below 2^32";
+    case PULSE_ERR_RANGE:
+      return "PULSE_ERR_RANGE: element count past the entry point's limit (2^32 - 1, or "
+             "PULSE_NOALLOC_MAX_ELEMS for pulse_encode_noalloc)";
     case PULSE_ERR_CUDA: return "PULSE_ERR_CUDA: CUDA runtime call or launch failed";
     case PULSE_ERR_TIMEOUT: return "PULSE_ERR_TIMEOUT: a bounded device wait gave up";
     case PULSE_ERR_INDEX: return "PULSE_ERR_INDEX: patch index out of range (entry skipped)";
@@ -552,7 +552,7 @@ int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** pl
     st = workspace_reserve(p->ws, tiles, nullptr);
   }
   if (st == PULSE_OK) {
-    // chunk tables of the chunk-owned apply, the chained apply and the k-way compose
+    // chunk tables of the chained apply and the k-way compose
     std::vector<uint64_t> cb(size_t(ntensors) + 1, 0);
     uint64_t chunks = 0;
     for (int i = 0; i < ntensors; ++i) {
@@ -565,8 +565,7 @@ int pulse_plan_create(const pulse_tensor* tensors, int ntensors, pulse_plan** pl
       for (uint64_t g = cb[size_t(i)]; g < cb[size_t(i) + 1]; ++g) ct[size_t(g)] = uint32_t(i);
     p->total_chunks = chunks;
     if (cudaMalloc(&p->chunk_begin, sizeof(uint64_t) * cb.size()) != cudaSuccess ||
-        cudaMalloc(&p->chunk_tensor, sizeof(uint32_t) * ct.size()) != cudaSuccess ||
-        cudaMalloc(&p->chunk_first, sizeof(uint32_t) * ct.size()) != cudaSuccess) {
+        cudaMalloc(&p->chunk_tensor, sizeof(uint32_t) * ct.size()) != cudaSuccess) {
       st = PULSE_ERR_NOMEM;
     } else if (cudaMemcpy(p->chunk_begin, cb.data(), sizeof(uint64_t) * cb.size(),
                           cudaMemcpyHostToDevice) != cudaSuccess ||
@@ -592,7 +591,6 @@ int pulse_plan_destroy(pulse_plan* plan) {
   if (plan->counts) cudaFree(plan->counts);
   if (plan->chunk_begin) cudaFree(plan->chunk_begin);
   if (plan->chunk_tensor) cudaFree(plan->chunk_tensor);
-  if (plan->chunk_first) cudaFree(plan->chunk_first);
   if (plan->chain_segs) cudaFree(plan->chain_segs);
   if (plan->chain_first) cudaFree(plan->chain_first);
   if (plan->cc_outs) cudaFree(plan->cc_outs);
@@ -627,29 +625,15 @@ int pulse_encode_multi(pulse_plan* plan, uint64_t* counts_out, cudaStream_t stre
 }
 
 namespace {
-constexpr int kRouteDevice = -1, kRouteChunks = 0, kRouteScatter = 1;
-
-// Whole-model apply by the given route (kRouteDevice: decided on the device
-// from counts_dev; the launches of the route not taken return at once).
-int apply_multi_routed(pulse_plan* plan, const uint64_t* counts_dev, int how, cudaStream_t stream) {
-  if (plan->chunk_first == nullptr) how = kRouteScatter;  // no chunk tables
-  const uint32_t* run_if = nullptr;
-  if (how != kRouteScatter) {
-    uint32_t* route = how == kRouteDevice ? plan->ws.counters + kRouteWord : nullptr;
-    const cudaError_t e = launch_apply_chunks(
-        plan->desc, plan->ntensors, plan->total_n, plan->chunk_begin, plan->chunk_tensor,
-        plan->chunk_first, counts_dev, plan->total_chunks, route, plan->ws.counters + 2,
-        kDefaultWaitNs, stream);
-    if (e != cudaSuccess) return PULSE_ERR_CUDA;
-    if (how == kRouteChunks) return PULSE_OK;
-    run_if = route;
-  }
+// Whole-model apply: the entry scatter over every segment, in groups of at
+// most kMaxTensorsPerApplyLaunch tensors per launch.
+int apply_multi_launch(pulse_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {
   const int grid = sm_count(plan->device) * 8;
   for (int t0 = 0; t0 < plan->ntensors; t0 += kMaxTensorsPerApplyLaunch) {
     const int nt = plan->ntensors - t0 < kMaxTensorsPerApplyLaunch ? plan->ntensors - t0
                                                                    : kMaxTensorsPerApplyLaunch;
     const cudaError_t e = launch_apply_multi(plan->desc + t0, nt, counts_dev + t0,
-                                             plan->ws.counters + 2, grid, stream, run_if);
+                                             plan->ws.counters + 2, grid, stream);
     if (e != cudaSuccess) return PULSE_ERR_CUDA;
   }
   return PULSE_OK;
@@ -658,24 +642,17 @@ int apply_multi_routed(pulse_plan* plan, const uint64_t* counts_dev, int how, cu
 
 int pulse_apply_multi_device(pulse_plan* plan, const uint64_t* counts_dev, cudaStream_t stream) {
   if (plan == nullptr || counts_dev == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
-  return apply_multi_routed(plan, counts_dev, kRouteDevice, stream);
+  return apply_multi_launch(plan, counts_dev, stream);
 }
 
 int pulse_apply_multi(pulse_plan* plan, const uint64_t* counts_host, cudaStream_t stream) {
   if (plan == nullptr || counts_host == nullptr || !plan->can_apply) return PULSE_ERR_INVALID;
-  // the route from the host counts, by the rule the device would apply
-  uint64_t k = 0;
-  for (int t = 0; t < plan->ntensors; ++t) {
-    const uint64_t n = plan->host_desc[size_t(t)].n;
-    k += counts_host[t] < n ? counts_host[t] : n;
-  }
-  const int how = kApplySparseRatio * k < plan->total_n ? kRouteScatter : kRouteChunks;
   // From pageable memory the copy is staged before this call returns, so the
   // caller may reuse counts_host at once.
   if (cudaMemcpyAsync(plan->counts, counts_host, sizeof(uint64_t) * size_t(plan->ntensors),
                       cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return PULSE_ERR_CUDA;
-  return apply_multi_routed(plan, plan->counts, how, stream);
+  return apply_multi_launch(plan, plan->counts, stream);
 }
 
 namespace {

@@ -14,9 +14,11 @@
 // that array (512 KB of status words + 256 bytes) until the process exits.
 //
 // The array is shared by every call on a device and keeps the previous
-// call's contents: the counters are cleared at the start of each call, and
-// status words are told apart by a per-device launch epoch (cleared only when
-// the epoch wraps). Two calls whose kernels overlap on the GPU (different
+// call's contents, so each call clears, on its stream and before its kernel,
+// the status words of its own tiles and the counters (8 bytes per 4096
+// elements plus 256 bytes; cudaMemsetAsync allocates nothing). Each call's
+// device work then depends only on its arguments, never on how many calls
+// came before it. Two calls whose kernels overlap on the GPU (different
 // streams, no ordering between them) race on the array and give wrong
 // results; callers must order them.
 #include <mutex>
@@ -43,9 +45,11 @@ struct NoallocScratch {
 // for the device symbol: its device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) NoallocScratch g_noalloc_scratch;
 
+// Every call clears the status words it reads, so one fixed epoch serves.
+constexpr uint32_t kNoallocEpoch = 1u;
+
 struct DeviceState {
   NoallocScratch* scratch;  // device address of g_noalloc_scratch on this device
-  uint32_t epoch;
 };
 
 std::mutex g_noalloc_mu;
@@ -89,18 +93,15 @@ extern "C" int pulse_encode_noalloc(const float* master_f32, uint16_t* prev_bf16
         return PULSE_ERR_CUDA;
       st.scratch = static_cast<NoallocScratch*>(ptr);
     }
-    st.epoch += 1;
-    if (st.epoch > kEpochMask) {
-      if (cudaMemsetAsync(st.scratch->status, 0, sizeof(st.scratch->status), stream) != cudaSuccess)
-        return PULSE_ERR_CUDA;
-      st.epoch = 1;
-    }
-    a.epoch = st.epoch;
     a.status = st.scratch->status;
     a.counters = st.scratch->counters;
   }
-  // ticket, finish counter and error word start at zero for this call
-  if (cudaMemsetAsync(a.counters, 0, sizeof(uint32_t) * kNoallocCounterWords, stream) != cudaSuccess)
+  a.epoch = kNoallocEpoch;
+  a.total_tiles = (n + kEncTile - 1) / kEncTile;
+  // this call's status words read "not yet published"; ticket, finish
+  // counter and error word start at zero
+  if (cudaMemsetAsync(a.status, 0, sizeof(uint64_t) * size_t(a.total_tiles), stream) != cudaSuccess ||
+      cudaMemsetAsync(a.counters, 0, sizeof(uint32_t) * kNoallocCounterWords, stream) != cudaSuccess)
     return PULSE_ERR_CUDA;
 
   a.one.master = master_f32;
@@ -117,7 +118,6 @@ extern "C" int pulse_encode_noalloc(const float* master_f32, uint16_t* prev_bf16
   a.tensors = nullptr;
   a.tile_begin = nullptr;
   a.ntensors = 1;
-  a.total_tiles = (n + kEncTile - 1) / kEncTile;
   a.counts_out = count_out;
   a.first_ticket = 0;
   a.wait_limit_ns = kNoallocWaitNs;

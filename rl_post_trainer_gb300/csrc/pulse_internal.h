@@ -230,52 +230,34 @@ cudaError_t launch_compose(const CmpSegment* segs_dev, const CmpSegment& one,
 
 // ---------------------------------------------------------------- apply
 #ifndef PULSE_APPLY_PER_THREAD
-#define PULSE_APPLY_PER_THREAD 8
+#define PULSE_APPLY_PER_THREAD 4
 #endif
 #ifndef PULSE_XOR_ROUNDS
 #define PULSE_XOR_ROUNDS 4
 #endif
 constexpr int kApplyThreads = 256;
 constexpr int kApplyPerThread = PULSE_APPLY_PER_THREAD;     // entries per thread per tile
-constexpr int kApplyTile = kApplyThreads * kApplyPerThread;  // 2048 entries
+constexpr int kApplyTile = kApplyThreads * kApplyPerThread;  // 1024 entries
 
 cudaError_t launch_apply(uint16_t* w, uint64_t n, bool checked, const uint32_t* idx,
                          const uint16_t* val, uint64_t count, uint32_t* error_word,
                          cudaStream_t stream);
-// run_if: null, or a device word; the launch does nothing when it holds 0.
 cudaError_t launch_apply_multi(const TensorDesc* tensors, int ntensors,
                                const uint64_t* counts_dev, uint32_t* error_word,
-                               int grid, cudaStream_t stream, const uint32_t* run_if = nullptr);
+                               int grid, cudaStream_t stream);
 
-// Chunk-owned whole-model apply (ascending segments): kApplyChunk elements
-// per chunk; chunk_begin[t] = first global chunk of tensor t (ntensors + 1),
-// chunk_tensor[g] = tensor of chunk g, chunk_first[g] = scratch (total_chunks).
+// Chained apply: chunks of kApplyChunk elements; chunk_begin[t] = first
+// global chunk of tensor t (ntensors + 1), chunk_tensor[g] = tensor of chunk
+// g. A chunk with at least kApplyDenseMin entries (over all versions) is
+// read into shared memory whole.
 #ifndef PULSE_APPLY_CHUNK
 #define PULSE_APPLY_CHUNK 8192
 #endif
 #ifndef PULSE_APPLY_DENSE_MIN
 #define PULSE_APPLY_DENSE_MIN 64
 #endif
-// A whole-model patch with sparse_ratio * k < n goes to the entry scatter
-// instead of the chunk-owned kernel (reading every touched chunk whole costs
-// more than fetching its few sectors).
-#ifndef PULSE_APPLY_SPARSE_RATIO
-#define PULSE_APPLY_SPARSE_RATIO 64
-#endif
 constexpr int kApplyChunk = PULSE_APPLY_CHUNK;
 constexpr uint32_t kApplyDenseMin = PULSE_APPLY_DENSE_MIN;
-constexpr uint64_t kApplySparseRatio = PULSE_APPLY_SPARSE_RATIO;
-// Route of a whole-model apply, decided on the device from the counts when
-// `route` is not null: *route = 1 when kApplySparseRatio * sum_t min(counts[t],
-// n_t) < total_n (the entry scatter runs), else 0 (partition + chunk-owned
-// kernel run). The partition and chunk-owned launches here do nothing when
-// *route is 1; the caller follows with launch_apply_multi(..., run_if =
-// route). A null `route` runs the chunk-owned route unconditionally.
-cudaError_t launch_apply_chunks(const TensorDesc* tensors, int ntensors, uint64_t total_n,
-                                const uint64_t* chunk_begin, const uint32_t* chunk_tensor,
-                                uint32_t* chunk_first, const uint64_t* counts_dev,
-                                uint64_t total_chunks, uint32_t* route, uint32_t* error_word,
-                                uint64_t wait_limit_ns, cudaStream_t stream);
 
 // Chained apply: one tensor's patch of one version (ascending indices).
 struct ChainSeg {

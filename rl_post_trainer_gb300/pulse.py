@@ -1035,21 +1035,31 @@ PACK_BLOCK = 128
 PACK_CHUNK = 4096
 
 
-def pack_indices(idx: torch.Tensor, count: int):
+def pack_sizes(count: int):
+    """Elements of (firsts, widths, chunk_off, payload) that a packed segment of
+    ``count`` indices needs."""
+    nb = (count + PACK_BLOCK - 1) // PACK_BLOCK
+    nc = (count + PACK_CHUNK - 1) // PACK_CHUNK
+    return max(nb, 1), max(nb, 1), max(nc, 1), max(512 * nb, 16)
+
+
+def pack_indices(idx: torch.Tensor, count: int, alloc=None):
     """pulse_pack_indices on the first ``count`` entries of ``idx``. Returns
     (firsts, widths, chunk_off, payload, payload_bytes); the packed payload is
-    the first ``payload_bytes`` bytes (device int64 tensor) of ``payload``."""
+    the first ``payload_bytes`` bytes (device int64 tensor) of ``payload``.
+    ``alloc(numel, dtype, device)`` makes the output buffers (default
+    torch.empty)."""
     _need(idx, "idx", (torch.int32, torch.uint32))
     dev = idx.device
     count = int(count)
     _need(idx, "idx", (torch.int32, torch.uint32), dev, min_numel=count)
-    nb = (count + PACK_BLOCK - 1) // PACK_BLOCK
-    nc = (count + PACK_CHUNK - 1) // PACK_CHUNK
-    firsts = torch.empty(max(nb, 1), dtype=torch.int32, device=dev)
-    widths = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
-    chunk_off = torch.empty(max(nc, 1), dtype=torch.int64, device=dev)
-    payload = torch.empty(max(512 * nb, 16), dtype=torch.uint8, device=dev)
-    payload_bytes = torch.empty(1, dtype=torch.int64, device=dev)
+    alloc = alloc or (lambda numel, dtype, device: torch.empty(numel, dtype=dtype, device=device))
+    nf, nw, nc, npay = pack_sizes(count)
+    firsts = alloc(nf, torch.int32, dev)
+    widths = alloc(nw, torch.uint8, dev)
+    chunk_off = alloc(nc, torch.int64, dev)
+    payload = alloc(npay, torch.uint8, dev)
+    payload_bytes = alloc(1, torch.int64, dev)
     with torch.cuda.device(dev):
         st = lib().pulse_pack_indices(_ptr(idx), count, _ptr(firsts), _ptr(widths), _ptr(chunk_off),
                                       _ptr(payload), _ptr(payload_bytes), _stream(dev))
@@ -1088,7 +1098,10 @@ class PackJob:
     s, payload_bytes[s] (device int64) its payload size. unpack() rebuilds
     every segment into unpacked[s] (first count entries)."""
 
-    def __init__(self, segments):
+    def __init__(self, segments, alloc=None):
+        """``alloc(numel, dtype, device)`` makes the output buffers (default
+        torch.empty)."""
+        alloc = alloc or (lambda numel, dtype, device: torch.empty(numel, dtype=dtype, device=device))
         if len(segments) == 0:
             raise ValueError("a pack job needs at least one segment")
         dev = None
@@ -1101,13 +1114,12 @@ class PackJob:
             if dev is None:
                 dev = idx.device
             _need(idx, "idx", (torch.int32, torch.uint32), dev, min_numel=count)
-            nb = (count + PACK_BLOCK - 1) // PACK_BLOCK
-            nc = (count + PACK_CHUNK - 1) // PACK_CHUNK
-            firsts = torch.empty(max(nb, 1), dtype=torch.int32, device=dev)
-            widths = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
-            chunk_off = torch.empty(max(nc, 1), dtype=torch.int64, device=dev)
-            payload = torch.empty(max(512 * nb, 16), dtype=torch.uint8, device=dev)
-            out = torch.empty(max(count, 1), dtype=torch.int32, device=dev)
+            nf, nw, nc, npay = pack_sizes(count)
+            firsts = alloc(nf, torch.int32, dev)
+            widths = alloc(nw, torch.uint8, dev)
+            chunk_off = alloc(nc, torch.int64, dev)
+            payload = alloc(npay, torch.uint8, dev)
+            out = alloc(max(count, 1), torch.int32, dev)
             self.counts.append(count)
             self.packed.append((firsts, widths, chunk_off, payload))
             self.unpacked.append(out)

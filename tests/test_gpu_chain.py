@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import rl_post_trainer_gb300 as pulse
-from pulse_testutil import dev_u16, dev_u32, host_u16
+from pulse_testutil import Guarded, dev_u16, dev_u32, host_u16
 
 pytestmark = pytest.mark.gpu
 
@@ -56,10 +56,11 @@ def _dev_patch(p, dev):
 def _run(w0s, chains, dev, offset=0):
     """chains[t] = list of patches of tensor t (oldest first). Returns the
     GPU result per tensor and the plan's error word."""
-    ws = []
+    ws, guards = [], []
     for w0 in w0s:
-        buf = torch.zeros(w0.size + offset, dtype=torch.int16, device=dev)
-        v = buf[offset:]
+        g = Guarded(w0.size + offset, torch.int16, dev)
+        guards.append(g)
+        v = g.t[offset:]
         if w0.size:
             v.copy_(dev_u16(w0, dev))
         ws.append(v)
@@ -70,6 +71,8 @@ def _run(w0s, chains, dev, offset=0):
         plan.apply_chain(patches)
         torch.cuda.synchronize()
         err = plan.get_error()
+    for g in guards:
+        g.check("w")
     return [host_u16(w) for w in ws], err
 
 
@@ -234,12 +237,19 @@ def _compose(w_sizes, chains, dev, offset=0):
              for n in w_sizes]
     nv = len(chains[0])
     patches = [[_dev_patch(chains[t][v], dev) for t in range(len(w_sizes))] for v in range(nv)]
+    # output segments with room for min(n, sum of the versions' counts), guarded
+    need = [min(n, sum(chains[t][v][0].size for v in range(nv))) for t, n in enumerate(w_sizes)]
+    guards = [(Guarded(max(r, 1), torch.int32, dev), Guarded(max(r, 1), torch.int16, dev))
+              for r in need]
     with pulse.Plan(slots) as plan:
-        outs, counts = plan.compose_chain(patches)
+        outs, counts = plan.compose_chain(patches, outs=[(gi.t, gv.t) for gi, gv in guards])
         torch.cuda.synchronize()
         err = plan.get_error()
         cnt = counts.cpu().tolist()
         res = [(host_u32_(oi[:k]), host_u16(ov[:k])) for (oi, ov), k in zip(outs, cnt)]
+    for gi, gv in guards:
+        gi.check("idx_out")
+        gv.check("val_out")
     return res, err
 
 

@@ -9,7 +9,7 @@ import torch
 import oracle
 import rl_post_trainer_gb300 as pulse
 import workloads
-from pulse_testutil import dev_u32, host_u32
+from pulse_testutil import Guarded, dev_u32, host_u32
 
 pytestmark = pytest.mark.gpu
 
@@ -43,8 +43,13 @@ def _host_val(t, dtype):
 def _gpu_compose(a, b, dev):
     ia, va = _to_dev(a, dev)
     ib, vb = _to_dev(b, dev)
-    idx, val, cnt = pulse.compose(ia, va, a[0].size, ib, vb, b[0].size)
+    cap = max(a[0].size + b[0].size, 1)
+    gi, gv = Guarded(cap, torch.int32, dev), Guarded(cap, va.dtype, dev)
+    gc = Guarded(1, torch.int64, dev)
+    idx, val, cnt = pulse.compose(ia, va, a[0].size, ib, vb, b[0].size, gi.t, gv.t, gc.t)
     k = int(cnt.item())
+    for name, g in (("idx", gi), ("val", gv), ("count", gc)):
+        g.check(name)
     return host_u32(idx[:k]), _host_val(val[:k], a[1].dtype)
 
 
@@ -126,15 +131,15 @@ def test_multi_segment(dtype):
     rng = np.random.default_rng(9)
     shapes = [(0, 0, 10), (3, 0, 10), (0, 4, 10), (TILE, TILE + 1, 10 * TILE), (70000, 50000, 200000),
               (1, 1, 2), (5000, 6000, 9000)]
-    segs, host = [], []
+    segs, host, guards = [], [], []
     for ka, kb, n in shapes:
         a, b = _rand_patch(rng, n, ka, dtype), _rand_patch(rng, n, kb, dtype)
         ia, va = _to_dev(a, dev)
         ib, vb = _to_dev(b, dev)
         cap = max(ka + kb, 1)
-        io = torch.empty(cap, dtype=torch.int32, device=dev)
-        vo = torch.empty(cap, dtype=va.dtype, device=dev)
-        segs.append((ia, va, ka, ib, vb, kb, io, vo))
+        gio, gvo = Guarded(cap, torch.int32, dev), Guarded(cap, va.dtype, dev)
+        guards += [gio, gvo]
+        segs.append((ia, va, ka, ib, vb, kb, gio.t, gvo.t))
         host.append((a, b))
     counts = pulse.compose_multi(segs).cpu().tolist()
     for (a, b), s, k in zip(host, segs, counts):
@@ -143,3 +148,5 @@ def test_multi_segment(dtype):
         np.testing.assert_array_equal(host_u32(s[6][:k]), oi)
         np.testing.assert_array_equal(_host_val(s[7][:k], dtype), ov)
     assert pulse.get_error(dev) == 0
+    for g in guards:
+        g.check()

@@ -20,7 +20,7 @@ import torch
 import oracle
 import rl_post_trainer_gb300 as pulse
 import workloads
-from pulse_testutil import host_f32, host_u16, host_u32, patch_of
+from pulse_testutil import Guarded, host_f32, host_u16, host_u32, patch_of
 
 pytestmark = pytest.mark.gpu
 
@@ -40,15 +40,26 @@ class Model:
         pairs = workloads.torch_model(specs, seed, eta, dev)
         self.specs = specs
         self.master = [m for m, _ in pairs]
-        self.prev = [p for _, p in pairs]
+        # every buffer a kernel writes sits between guard zones (checked by close)
+        self.guards = []
+
+        def guarded(init=None, numel=0, dtype=torch.int16):
+            g = Guarded(init.numel() if init is not None else numel, dtype, dev, init=init)
+            self.guards.append(g)
+            return g.t
+
+        self.prev = []
+        for i in range(len(pairs)):
+            self.prev.append(guarded(pairs[i][1]))
+            pairs[i] = None
         self.prev0 = [p.clone() for p in self.prev] if keep_prev0 else None
-        self.w = [p.clone() for p in self.prev]
-        self.idx = [torch.empty(max(s.numel, 1), dtype=torch.int32, device=dev) for s in specs]
-        self.val = [torch.empty(max(s.numel, 1), dtype=torch.int16, device=dev) for s in specs]
+        self.w = [guarded(p) for p in self.prev]
+        self.idx = [guarded(numel=max(s.numel, 1), dtype=torch.int32) for s in specs]
+        self.val = [guarded(numel=max(s.numel, 1)) for s in specs]
         if xor:
-            self.prev_x = [p.clone() for p in self.prev]
-            self.w_x = [p.clone() for p in self.prev]
-            self.mask = [torch.empty(s.numel, dtype=torch.int16, device=dev) for s in specs]
+            self.prev_x = [guarded(p) for p in self.prev]
+            self.w_x = [guarded(p) for p in self.prev]
+            self.mask = [guarded(numel=s.numel) for s in specs]
         slots = [pulse.TensorSlot(s.numel, master=self.master[i], prev=self.prev[i], w=self.w[i],
                                   idx=self.idx[i], val=self.val[i]) for i, s in enumerate(specs)]
         self.plan = pulse.Plan(slots)
@@ -61,6 +72,8 @@ class Model:
         self.plan.close()
         if hasattr(self, "xplan"):
             self.xplan.close()
+        for g in self.guards:
+            g.check()
 
 
 def _check_tensor(model, t, counts, check_xor, prev_before=None):
@@ -106,15 +119,19 @@ def test_config1_single_tensor_2p20():
     dev = _dev()
     spec = workloads.single(1 << 20)[0]
     (m, p0), = workloads.torch_model([spec], seed=0, eta=workloads.ETA_DEFAULT, device=dev)
-    prev = p0.clone()
-    idx, val, cnt = pulse.encode(m, prev)
-    w = p0.clone()
+    n = spec.numel
+    bufs = {name: Guarded(n, dt, dev, init=(p0 if name in ("prev", "w", "prev_x", "w_x") else None))
+            for name, dt in (("prev", torch.int16), ("w", torch.int16), ("prev_x", torch.int16),
+                             ("w_x", torch.int16), ("idx", torch.int32), ("val", torch.int16),
+                             ("mask", torch.int16))}
+    prev, w, prev_x, w_x = (bufs[k].t for k in ("prev", "w", "prev_x", "w_x"))
+    idx, val, cnt = pulse.encode(m, prev, idx_out=bufs["idx"].t, val_out=bufs["val"].t)
     pulse.apply(w, idx, val, int(cnt.item()))
-    prev_x = p0.clone()
-    mask = pulse.xor_mask(m, prev_x)
-    w_x = p0.clone()
+    mask = pulse.xor_mask(m, prev_x, mask_out=bufs["mask"].t)
     pulse.xor_apply(w_x, mask)
     torch.cuda.synchronize()
+    for name, g in bufs.items():
+        g.check(name)
     master_np, p0_np = host_f32(m), host_u16(p0)
     o_prev = p0_np.copy()
     o_idx, o_val = oracle.encode(master_np, o_prev)
@@ -169,17 +186,19 @@ def test_config4_density_sweep_2p28():
     p0 = torch.empty(n, dtype=torch.int16, device=dev)
     workloads.torch_bf16_view_(p0, w0)
     w0_np, p0_np = host_f32(w0), host_u16(p0)
-    idx = torch.empty(n, dtype=torch.int32, device=dev)
-    val = torch.empty(n, dtype=torch.int16, device=dev)
+    gi, gv = Guarded(n, torch.int32, dev), Guarded(n, torch.int16, dev)
+    idx, val = gi.t, gv.t
     last = -1.0
     for i, eta in enumerate(workloads.ETA_SWEEP):
         m = w0.clone()
         workloads.torch_update_(m, eta, workloads.torch_generator(dev, workloads.sweep_seed(i)))
-        prev = p0.clone()
+        gp, gw = Guarded(n, torch.int16, dev, init=p0), Guarded(n, torch.int16, dev, init=p0)
+        prev, w = gp.t, gw.t
         _, _, cnt = pulse.encode(m, prev, idx_out=idx, val_out=val)
-        w = p0.clone()
         pulse.apply(w, idx, val, int(cnt.item()))
         torch.cuda.synchronize()
+        for name, g in (("prev", gp), ("w", gw), ("idx", gi), ("val", gv)):
+            g.check(name)
         m_np = host_f32(m)
         o_prev = p0_np.copy()
         o_idx, o_val = oracle.encode(m_np, o_prev)
@@ -192,7 +211,7 @@ def test_config4_density_sweep_2p28():
         density = k / n
         assert density > last        # the visible fraction grows with the update scale
         last = density
-        del m, prev, w
+        del m, prev, w, gp, gw
     assert pulse.get_error(dev) == 0
 
 

@@ -10,7 +10,7 @@ import torch
 import oracle
 import rl_post_trainer_gb300 as pulse
 import workloads
-from pulse_testutil import dev_f32, host_f32, host_u32
+from pulse_testutil import Guarded, dev_f32, host_f32, host_u32
 
 pytestmark = pytest.mark.gpu
 
@@ -38,14 +38,20 @@ def _round(n, seed, scale=2e-5, err_scale=1e-5):
 def _check(g, w, e, dev, offset=0):
     n = g.size
 
+    guards = []
+
     def placed(a):
-        buf = torch.zeros(n + offset, dtype=torch.float32, device=dev)
-        v = buf[offset:]
+        gb = Guarded(n + offset, torch.float32, dev)
+        guards.append(gb)
+        v = gb.t[offset:]
         v.copy_(torch.from_numpy(a).to(dev))
         return v
 
     gt, wt, et = placed(g), placed(w), placed(e)
-    idx, val, cnt = pulse.loco_gate(gt, wt, et)
+    gi, gv = Guarded(max(n, 1), torch.int32, dev), Guarded(max(n, 1), torch.float32, dev)
+    gc = Guarded(1, torch.int64, dev)
+    guards += [gi, gv, gc]
+    idx, val, cnt = pulse.loco_gate(gt, wt, et, gi.t, gv.t, gc.t)
     torch.cuda.synchronize()
     k = int(cnt.item())
     oe = e.copy()
@@ -55,6 +61,8 @@ def _check(g, w, e, dev, offset=0):
     np.testing.assert_array_equal(_bits(host_f32(val[:k])), _bits(ov))
     np.testing.assert_array_equal(_bits(host_f32(et)), _bits(oe))
     assert pulse.get_error(dev) == 0
+    for gb in guards:
+        gb.check()
     return k
 
 
@@ -116,7 +124,8 @@ def test_accumulate_matches_oracle_and_checks_indices():
     acc = rng.standard_normal(n).astype(np.float32)
     idx = np.sort(rng.choice(n, 30000, replace=False)).astype(np.uint32)
     val = rng.standard_normal(30000).astype(np.float32)
-    at = dev_f32(acc, dev)
+    ga = Guarded(n, torch.float32, dev, init=acc)
+    at = ga.t
     pulse.loco_accumulate(at, torch.from_numpy(idx.view(np.int32)).to(dev), dev_f32(val, dev), idx.size)
     torch.cuda.synchronize()
     exp = acc.copy()
@@ -126,6 +135,7 @@ def test_accumulate_matches_oracle_and_checks_indices():
     bad = torch.tensor([5, n, 7], dtype=torch.int32, device=dev)
     pulse.loco_accumulate(at, bad, torch.ones(3, device=dev), 3)
     assert pulse.get_error(dev) == pulse.pulse.PULSE_ERR_INDEX
+    ga.check("acc")
 
 
 def test_plan_gate_then_accumulate():
@@ -136,13 +146,16 @@ def test_plan_gate_then_accumulate():
     specs = workloads.llama_layer()[-4:] + [workloads.TensorSpec(f"t{i}", (n,), "weight")
                                             for i, n in enumerate([0, 1, 5, TILE + 3])]
     rng = np.random.default_rng(21)
-    host, slots = [], []
+    host, slots, guards = [], [], []
     for s in specs:
         g, w, e = _round(s.numel, int(rng.integers(1 << 30)))
-        gt, wt, et = dev_f32(g, dev), dev_f32(w, dev), dev_f32(e, dev)
-        idx = torch.empty(max(s.numel, 1), dtype=torch.int32, device=dev)
-        val = torch.empty(max(s.numel, 1), dtype=torch.float32, device=dev)
-        acc = gt.clone()
+        gt, wt = dev_f32(g, dev), dev_f32(w, dev)
+        bufs = [Guarded(s.numel, torch.float32, dev, init=e),
+                Guarded(max(s.numel, 1), torch.int32, dev),
+                Guarded(max(s.numel, 1), torch.float32, dev),
+                Guarded(s.numel, torch.float32, dev, init=g)]
+        guards += bufs
+        et, idx, val, acc = (b.t for b in bufs)
         host.append((g, w, e))
         slots.append(pulse.LocoTensorSlot(s.numel, global_w=gt, local_w=wt, err=et, idx=idx, val=val,
                                           acc=acc))
@@ -162,3 +175,5 @@ def test_plan_gate_then_accumulate():
             acc = g.copy()
             oracle.loco_accumulate(acc, oi, ov)
             np.testing.assert_array_equal(_bits(host_f32(sl.acc)), _bits(acc))
+    for b in guards:
+        b.check()

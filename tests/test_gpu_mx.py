@@ -12,7 +12,7 @@ import torch
 import oracle
 import rl_post_trainer_gb300 as pulse
 import workloads
-from pulse_testutil import dev_f32, host_f32, host_u32
+from pulse_testutil import Guarded, dev_f32, guarded_u8, host_f32, host_u32
 
 pytestmark = pytest.mark.gpu
 
@@ -110,10 +110,13 @@ def _special_master(n: int, seed: int) -> np.ndarray:
 def test_quantize_matches_oracle(n):
     dev = _dev()
     m = _special_master(n, 1000 + n)
-    codes, scales = pulse.mx_quantize(dev_f32(m, dev))
+    gc, gs = Guarded(n, torch.uint8, dev), Guarded((n + 31) // 32, torch.uint8, dev)
+    codes, scales = pulse.mx_quantize(dev_f32(m, dev), gc.t, gs.t)
     o_codes, o_scales = oracle.mxfp8_quantize(m)
     np.testing.assert_array_equal(host_u8(scales), o_scales)
     np.testing.assert_array_equal(host_u8(codes), o_codes)
+    gc.check("codes")
+    gs.check("scales")
 
 
 # ------------------------------------------------------------------ encode
@@ -128,19 +131,25 @@ def _encode_both(m_old: np.ndarray, m_new: np.ndarray, dev, offset: int = 0):
     o_pc, o_ps = o_codes.copy(), o_scales.copy()
     o_patch = oracle.mxfp8_encode(m_new, o_pc, o_ps)
 
-    def placed(a, dtype):
-        buf = torch.zeros(a.size + offset, dtype=dtype, device=dev)
-        view = buf[offset:]
-        view.copy_(torch.from_numpy(np.ascontiguousarray(a)).to(dev))
+    guards = {}
+
+    def placed(name, a, dtype, numel=None):
+        # `offset` elements into a guarded allocation; filled from `a` if given
+        numel = a.size if numel is None else numel
+        g = Guarded(numel + offset, dtype, dev)
+        guards[name] = g
+        view = g.t[offset:]
+        if a is not None:
+            view.copy_(torch.from_numpy(np.ascontiguousarray(a)).to(dev))
         return view
 
-    master = placed(m_new, torch.float32)
-    prev_c = placed(o_codes, torch.uint8)
-    prev_s = placed(o_scales, torch.uint8)
-    idx = torch.full((max(n, 1) + offset,), -1, dtype=torch.int32, device=dev)[offset:]
-    val = torch.zeros(max(n, 1) + offset, dtype=torch.uint8, device=dev)[offset:]
-    sidx = torch.full((max(nb, 1) + offset,), -1, dtype=torch.int32, device=dev)[offset:]
-    sval = torch.zeros(max(nb, 1) + offset, dtype=torch.uint8, device=dev)[offset:]
+    master = placed("master", m_new, torch.float32)
+    prev_c = placed("prev_codes", o_codes, torch.uint8)
+    prev_s = placed("prev_scales", o_scales, torch.uint8)
+    idx = placed("idx", None, torch.int32, max(n, 1))
+    val = placed("val", None, torch.uint8, max(n, 1))
+    sidx = placed("sidx", None, torch.int32, max(nb, 1))
+    sval = placed("sval", None, torch.uint8, max(nb, 1))
     _, _, _, _, counts = pulse.mx_encode(master, prev_c, prev_s, idx, val, sidx, sval)
     torch.cuda.synchronize()
     k, ks = (int(c) for c in counts.cpu().tolist())
@@ -150,12 +159,14 @@ def _encode_both(m_old: np.ndarray, m_new: np.ndarray, dev, offset: int = 0):
     np.testing.assert_array_equal(host_u8(prev_c), o_pc)
     np.testing.assert_array_equal(host_u8(prev_s), o_ps)
     # receiver: the old view plus the patch is the new view
-    w_c, w_s = placed(o_codes, torch.uint8), placed(o_scales, torch.uint8)
+    w_c, w_s = placed("codes", o_codes, torch.uint8), placed("scales", o_scales, torch.uint8)
     pulse.mx_apply(w_c, w_s, idx, val, k, sidx, sval, ks)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(host_u8(w_c), o_pc)
     np.testing.assert_array_equal(host_u8(w_s), o_ps)
     assert pulse.get_error(dev) == 0
+    for name, g in guards.items():
+        g.check(name)
     return k, ks
 
 
@@ -265,13 +276,24 @@ class MxModel:
             self.prev_s.append(sc)
         self.c0 = [c.clone() for c in self.prev_c]
         self.s0 = [s.clone() for s in self.prev_s]
-        self.codes = [c.clone() for c in self.prev_c]
-        self.scales = [s.clone() for s in self.prev_s]
-        self.idx = [torch.empty(max(s.numel, 1), dtype=torch.int32, device=dev) for s in specs]
-        self.val = [torch.empty(max(s.numel, 1), dtype=torch.uint8, device=dev) for s in specs]
+        # every buffer the encode or the apply writes sits between guard zones
+        self.guards = []
+
+        def guarded(t=None, numel=0, dtype=torch.uint8):
+            g = Guarded(t.numel() if t is not None else numel, t.dtype if t is not None else dtype,
+                        dev, init=t)
+            self.guards.append(g)
+            return g.t
+
+        self.prev_c = [guarded(c) for c in self.c0]
+        self.prev_s = [guarded(x) for x in self.s0]
+        self.codes = [guarded(c) for c in self.c0]
+        self.scales = [guarded(x) for x in self.s0]
+        self.idx = [guarded(numel=max(s.numel, 1), dtype=torch.int32) for s in specs]
+        self.val = [guarded(numel=max(s.numel, 1)) for s in specs]
         nb = [pulse.mx_blocks(s.numel) for s in specs]
-        self.sidx = [torch.empty(max(b, 1), dtype=torch.int32, device=dev) for b in nb]
-        self.sval = [torch.empty(max(b, 1), dtype=torch.uint8, device=dev) for b in nb]
+        self.sidx = [guarded(numel=max(b, 1), dtype=torch.int32) for b in nb]
+        self.sval = [guarded(numel=max(b, 1)) for b in nb]
         slots = [pulse.MxTensorSlot(s.numel, master=self.master[i], prev_codes=self.prev_c[i],
                                     prev_scales=self.prev_s[i], codes=self.codes[i],
                                     scales=self.scales[i], idx=self.idx[i], val=self.val[i],
@@ -296,6 +318,8 @@ class MxModel:
 
     def close(self):
         self.plan.close()
+        for g in self.guards:
+            g.check()
 
 
 def test_initial_view_matches_oracle_quantize():

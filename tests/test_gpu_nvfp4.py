@@ -11,7 +11,7 @@ import torch
 import oracle
 import rl_post_trainer_gb300 as pulse
 import workloads
-from pulse_testutil import dev_f32, host_f32, host_u32
+from pulse_testutil import Guarded, dev_f32, host_f32, host_u32
 
 pytestmark = pytest.mark.gpu
 
@@ -110,18 +110,23 @@ def _encode_both(m_old, m_new, dev, offset=0):
     o_pc, o_ps = oc.copy(), osc.copy()
     o_patch = oracle.nvfp4_encode(m_new, o_pc, o_ps)
 
-    def placed(a, dtype):
-        buf = torch.zeros(a.size + offset, dtype=dtype, device=dev)
-        view = buf[offset:]
-        view.copy_(torch.from_numpy(np.ascontiguousarray(a)).to(dev))
+    guards = []
+
+    def placed(a, dtype, numel=None):
+        # `offset` elements into a guarded allocation; filled from `a` if given
+        g = Guarded((a.size if numel is None else numel) + offset, dtype, dev)
+        guards.append(g)
+        view = g.t[offset:]
+        if a is not None:
+            view.copy_(torch.from_numpy(np.ascontiguousarray(a)).to(dev))
         return view
 
     master = placed(m_new, torch.float32)
     prev_c, prev_s = placed(oc, torch.uint8), placed(osc, torch.uint8)
-    idx = torch.full((max(ncb, 1) + offset,), -1, dtype=torch.int32, device=dev)[offset:]
-    val = torch.zeros(max(ncb, 1) + offset, dtype=torch.uint8, device=dev)[offset:]
-    sidx = torch.full((max(nb, 1) + offset,), -1, dtype=torch.int32, device=dev)[offset:]
-    sval = torch.zeros(max(nb, 1) + offset, dtype=torch.uint8, device=dev)[offset:]
+    idx = placed(None, torch.int32, max(ncb, 1))
+    val = placed(None, torch.uint8, max(ncb, 1))
+    sidx = placed(None, torch.int32, max(nb, 1))
+    sval = placed(None, torch.uint8, max(nb, 1))
     *_, counts, ts = pulse.nvfp4_encode(master, prev_c, prev_s, idx, val, sidx, sval)
     torch.cuda.synchronize()
     k, ks = (int(c) for c in counts.cpu().tolist())
@@ -137,6 +142,8 @@ def _encode_both(m_old, m_new, dev, offset=0):
     np.testing.assert_array_equal(host_u8(w_c), o_pc)
     np.testing.assert_array_equal(host_u8(w_s), o_ps)
     assert pulse.get_error(dev) == 0
+    for g in guards:
+        g.check()
     return k, ks
 
 
@@ -186,19 +193,28 @@ def test_plan_matches_oracle(device_counts):
                                             enumerate([5, 0, 33, 4096, 4097, 15, 3 * 4096 + 1, 1])]
     states = workloads.torch_model_states(specs, 29, 1e-3, dev)
     prev_c, prev_s, codes, scales, idx, val, sidx, sval, c0, s0 = ([] for _ in range(10))
+    guards = []
+
+    def guard(t, numel=0, dtype=torch.uint8):
+        # a copy of t (or numel elements) between guard zones
+        g = Guarded(t.numel() if t is not None else numel, t.dtype if t is not None else dtype,
+                    dev, init=t)
+        guards.append(g)
+        return g.t
+
     for (w, _), s in zip(states, specs):
         c, sc, _ = pulse.nvfp4_quantize(w)
-        prev_c.append(c.clone())
-        prev_s.append(sc.clone())
+        prev_c.append(guard(c))
+        prev_s.append(guard(sc))
         c0.append(host_u8(c))
         s0.append(host_u8(sc))
-        codes.append(c.clone())
-        scales.append(sc.clone())
+        codes.append(guard(c))
+        scales.append(guard(sc))
         ncb, nb = pulse.mx_code_bytes(s.numel, NV), pulse.mx_scale_count(s.numel, NV)
-        idx.append(torch.empty(max(ncb, 1), dtype=torch.int32, device=dev))
-        val.append(torch.empty(max(ncb, 1), dtype=torch.uint8, device=dev))
-        sidx.append(torch.empty(max(nb, 1), dtype=torch.int32, device=dev))
-        sval.append(torch.empty(max(nb, 1), dtype=torch.uint8, device=dev))
+        idx.append(guard(None, max(ncb, 1), torch.int32))
+        val.append(guard(None, max(ncb, 1)))
+        sidx.append(guard(None, max(nb, 1), torch.int32))
+        sval.append(guard(None, max(nb, 1)))
     slots = [pulse.MxTensorSlot(s.numel, master=states[i][1], prev_codes=prev_c[i],
                                 prev_scales=prev_s[i], codes=codes[i], scales=scales[i],
                                 idx=idx[i], val=val[i], sidx=sidx[i], sval=sval[i])
@@ -223,6 +239,8 @@ def test_plan_matches_oracle(device_counts):
             np.testing.assert_array_equal(host_u8(prev_c[t]), o_c)
             np.testing.assert_array_equal(host_u8(codes[t]), o_c)
             np.testing.assert_array_equal(host_u8(scales[t]), o_s)
+    for g in guards:
+        g.check()
 
 
 def test_mx_calls_refuse_nvfp4():

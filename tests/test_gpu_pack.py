@@ -9,7 +9,7 @@ import torch
 import oracle
 import rl_post_trainer_gb300 as pulse
 import workloads
-from pulse_testutil import dev_u32, host_u32
+from pulse_testutil import Guarded, dev_u32, host_u32
 
 pytestmark = pytest.mark.gpu
 
@@ -28,10 +28,27 @@ def _random_idx(rng, k, mean_gap, big=False):
     return idx.astype(np.uint32)
 
 
+class _GuardedAlloc:
+    """Output buffers between guard zones, checked by check()."""
+
+    def __init__(self):
+        self.guards = []
+
+    def __call__(self, numel, dtype, device):
+        g = Guarded(numel, dtype, device)
+        self.guards.append(g)
+        return g.t
+
+    def check(self):
+        for g in self.guards:
+            g.check()
+
+
 def _check(idx_np, dev):
     k = idx_np.size
     t = dev_u32(idx_np, dev) if k else torch.empty(0, dtype=torch.int32, device=dev)
-    firsts, widths, chunk_off, payload, nbytes = pulse.pack_indices(t, k)
+    alloc = _GuardedAlloc()
+    firsts, widths, chunk_off, payload, nbytes = pulse.pack_indices(t, k, alloc=alloc)
     torch.cuda.synchronize()
     of, ow, oc, op = oracle.pack_indices(idx_np)
     nb, nc = of.size, oc.size
@@ -42,7 +59,8 @@ def _check(idx_np, dev):
     np.testing.assert_array_equal(chunk_off[:nc].cpu().numpy().view(np.uint64), oc)
     np.testing.assert_array_equal(payload[:size].cpu().numpy(), op)
     if k:
-        back = pulse.unpack_indices(firsts, widths, chunk_off, payload, k)
+        back = pulse.unpack_indices(firsts, widths, chunk_off, payload, k,
+                                    idx_out=alloc(k, torch.int32, dev))
         np.testing.assert_array_equal(host_u32(back[:k]), idx_np)
         # the oracle's packing, unpacked on the GPU
         op_dev = torch.zeros(max(op.size, 16), dtype=torch.uint8, device=dev)
@@ -52,6 +70,7 @@ def _check(idx_np, dev):
                                      torch.from_numpy(oc.view(np.int64)).to(dev), op_dev, k)
         np.testing.assert_array_equal(host_u32(back2[:k]), idx_np)
     assert pulse.get_error(dev) == 0
+    alloc.check()
     return size
 
 
@@ -92,7 +111,8 @@ def _check_job(segs_np, dev, offsets=None):
         if a.size:
             buf[off:off + a.size] = dev_u32(a, dev)
         tens.append((buf[off:], a.size))
-    job = pulse.PackJob(tens)
+    alloc = _GuardedAlloc()
+    job = pulse.PackJob(tens, alloc=alloc)
     sizes = job.pack()
     outs = job.unpack()
     torch.cuda.synchronize()
@@ -107,6 +127,7 @@ def _check_job(segs_np, dev, offsets=None):
         np.testing.assert_array_equal(chunk_off[:nc].cpu().numpy().view(np.uint64), oc)
         np.testing.assert_array_equal(payload[:size].cpu().numpy(), op)
         np.testing.assert_array_equal(host_u32(back[:a.size]), a)
+    alloc.check()
 
 
 def test_pack_job_many_segments():

@@ -12,7 +12,8 @@ import torch
 import oracle
 import rl_post_trainer_gb300 as pulse
 import workloads
-from pulse_testutil import dev_f32, dev_u16, dev_u32, host_u16, host_u32, patch_of
+from pulse_testutil import (Guarded, dev_f32, dev_u16, dev_u32, guarded_u16, host_u16, host_u32,
+                            patch_of)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,24 +30,29 @@ def _cuda():
 
 def _encode_both(master_np, prev_np, offset=0):
     """Runs GPU encode (optionally on views misaligned by `offset` elements)
-    and the oracle; returns (gpu_idx, gpu_val, k, gpu_prev, o_idx, o_val, o_prev)."""
+    into guarded buffers and the oracle; returns (gpu_idx, gpu_val, k,
+    gpu_prev, o_idx, o_val, o_prev)."""
     dev = _cuda()
     n = master_np.size
-    if offset:
-        mbuf = torch.zeros(n + offset, dtype=torch.float32, device=dev)
-        pbuf = torch.zeros(n + offset, dtype=torch.int16, device=dev)
-        mbuf[offset:] = dev_f32(master_np)
-        pbuf[offset:] = dev_u16(prev_np)
-        m_t, p_t = mbuf[offset:], pbuf[offset:]
-    else:
-        m_t, p_t = dev_f32(master_np), dev_u16(prev_np)
-    idx_t, val_t, cnt_t = pulse.encode(m_t, p_t)
+    gm = Guarded(n + offset, torch.float32, dev)
+    gp = Guarded(n + offset, torch.int16, dev)
+    gm.t.zero_()
+    gp.t.zero_()
+    gm.t[offset:] = dev_f32(master_np)
+    gp.t[offset:] = dev_u16(prev_np)
+    m_t, p_t = gm.t[offset:], gp.t[offset:]
+    gi = Guarded(max(n, 1), torch.int32, dev)
+    gv = Guarded(max(n, 1), torch.int16, dev)
+    gc = Guarded(1, torch.int64, dev)
+    idx_t, val_t, cnt_t = pulse.encode(m_t, p_t, idx_out=gi.t, val_out=gv.t, count_out=gc.t)
     torch.cuda.synchronize()
     g_idx, g_val, k = patch_of(idx_t, val_t, cnt_t)
     g_prev = host_u16(p_t)
     o_prev = prev_np.copy()
     o_idx, o_val = oracle.encode(master_np, o_prev)
     assert pulse.get_error() == 0
+    for name, g in (("master", gm), ("prev", gp), ("idx", gi), ("val", gv), ("count", gc)):
+        g.check(name)
     return g_idx, g_val, k, g_prev, o_idx, o_val, o_prev
 
 
@@ -149,17 +155,19 @@ def test_apply_parity_and_reconstruction(n):
     o_prev = prev.copy()
     o_idx, o_val = oracle.encode(master, o_prev)
     w_np = prev.copy()
-    w_t = dev_u16(w_np)
-    pulse.apply(w_t, dev_u32(o_idx), dev_u16(o_val), o_idx.size)
+    gw = guarded_u16(w_np)
+    pulse.apply(gw.t, dev_u32(o_idx), dev_u16(o_val), o_idx.size)
     oracle.apply(w_np, o_idx, o_val)
-    got = host_u16(w_t)
+    got = host_u16(gw.t)
     np.testing.assert_array_equal(got, w_np)
     np.testing.assert_array_equal(got, o_prev)   # bit-identical to the new view
     # checked variant on the same inputs
-    w2 = dev_u16(prev)
-    pulse.apply(w2, dev_u32(o_idx), dev_u16(o_val), o_idx.size, checked=True)
-    np.testing.assert_array_equal(host_u16(w2), w_np)
+    gw2 = guarded_u16(prev)
+    pulse.apply(gw2.t, dev_u32(o_idx), dev_u16(o_val), o_idx.size, checked=True)
+    np.testing.assert_array_equal(host_u16(gw2.t), w_np)
     assert pulse.get_error(dev) == 0
+    gw.check("w")
+    gw2.check("w (checked)")
 
 
 def test_apply_misaligned_patch_views():
@@ -173,9 +181,10 @@ def test_apply_misaligned_patch_views():
         vb = torch.zeros(o_idx.size + off, dtype=torch.int16, device=dev)
         ib[off:] = dev_u32(o_idx)
         vb[off:] = dev_u16(o_val)
-        w_t = dev_u16(prev)
-        pulse.apply(w_t, ib[off:], vb[off:], o_idx.size)
-        np.testing.assert_array_equal(host_u16(w_t), o_prev)
+        gw = guarded_u16(prev)
+        pulse.apply(gw.t, ib[off:], vb[off:], o_idx.size)
+        np.testing.assert_array_equal(host_u16(gw.t), o_prev)
+        gw.check("w")
 
 
 def test_apply_checked_reports_out_of_range_and_skips_it():
@@ -184,14 +193,15 @@ def test_apply_checked_reports_out_of_range_and_skips_it():
     w_np = np.arange(n, dtype=np.uint16)
     idx = np.array([3, n + 5, 10, 0xFFFFFFFF], dtype=np.uint32)
     val = np.array([7, 8, 9, 10], dtype=np.uint16)
-    w_t = dev_u16(w_np)
-    pulse.apply(w_t, dev_u32(idx), dev_u16(val), idx.size, checked=True)
+    gw = guarded_u16(w_np)
+    pulse.apply(gw.t, dev_u32(idx), dev_u16(val), idx.size, checked=True)
     assert pulse.get_error(dev) == pulse.pulse.PULSE_ERR_INDEX
     exp = w_np.copy()
     exp[3] = 7
     exp[10] = 9
-    np.testing.assert_array_equal(host_u16(w_t), exp)
+    np.testing.assert_array_equal(host_u16(gw.t), exp)
     assert pulse.get_error(dev) == 0   # cleared
+    gw.check("w")
 
 
 @pytest.mark.parametrize("n", [1, 7, TILE - 1, TILE, TILE + 1, 5 * TILE + 3, (1 << 20) + 3])
@@ -199,27 +209,27 @@ def test_apply_checked_reports_out_of_range_and_skips_it():
 def test_xor_parity(n, offset):
     dev = _cuda()
     master, prev = workloads.np_pair(n, seed=3000 + n)
-    if offset:
-        mb = torch.zeros(n + offset, dtype=torch.float32, device=dev)
-        pb = torch.zeros(n + offset, dtype=torch.int16, device=dev)
-        mb[offset:] = dev_f32(master)
-        pb[offset:] = dev_u16(prev)
-        m_t, p_t = mb[offset:], pb[offset:]
-    else:
-        m_t, p_t = dev_f32(master), dev_u16(prev)
-    mask_t = pulse.xor_mask(m_t, p_t)
+    gm = Guarded(n + offset, torch.float32, dev)
+    gp = Guarded(n + offset, torch.int16, dev)
+    gm.t[offset:] = dev_f32(master)
+    gp.t[offset:] = dev_u16(prev)
+    m_t, p_t = gm.t[offset:], gp.t[offset:]
+    gx = Guarded(n, torch.int16, dev)
+    mask_t = pulse.xor_mask(m_t, p_t, mask_out=gx.t)
     o_prev = prev.copy()
     o_mask = oracle.xor_mask(master, o_prev)
     np.testing.assert_array_equal(host_u16(mask_t), o_mask)
     np.testing.assert_array_equal(host_u16(p_t), o_prev)
-    w_t = dev_u16(prev)
-    pulse.xor_apply(w_t, mask_t)
+    gw = guarded_u16(prev)
+    pulse.xor_apply(gw.t, mask_t)
     w_np = prev.copy()
     oracle.xor_apply(w_np, o_mask)
-    np.testing.assert_array_equal(host_u16(w_t), w_np)
-    np.testing.assert_array_equal(host_u16(w_t), o_prev)
-    pulse.xor_apply(w_t, mask_t)                                  # double XOR restores
-    np.testing.assert_array_equal(host_u16(w_t), prev)
+    np.testing.assert_array_equal(host_u16(gw.t), w_np)
+    np.testing.assert_array_equal(host_u16(gw.t), o_prev)
+    pulse.xor_apply(gw.t, mask_t)                                 # double XOR restores
+    np.testing.assert_array_equal(host_u16(gw.t), prev)
+    for name, g in (("master", gm), ("prev", gp), ("mask", gx), ("w", gw)):
+        g.check(name)
 
 
 def test_xor_and_patch_modes_agree():
@@ -237,27 +247,36 @@ def test_xor_and_patch_modes_agree():
 
 
 def test_exhaustive_fp32_patterns_through_the_gpu_cast():
-    """Every FP32 bit pattern as master, prev = 0: the patch lists exactly the
-    patterns whose RNE view is not +0, with the oracle's values."""
+    """Every FP32 bit pattern as master, twice. Against prev = 0 the patch
+    lists exactly the patterns whose RNE view is not +0, with the oracle's
+    values. Against prev = the oracle's RNE view of the same patterns the
+    patch is empty and prev is left as it was."""
     dev = _cuda()
     chunk = 1 << 28
-    idx_t = torch.empty(chunk, dtype=torch.int32, device=dev)
-    val_t = torch.empty(chunk, dtype=torch.int16, device=dev)
+    gi = Guarded(chunk, torch.int32, dev)
+    gv = Guarded(chunk, torch.int16, dev)
     for start in range(0, 1 << 32, chunk):
         bits = torch.arange(start, start + chunk, dtype=torch.int64, device=dev)
         m_t = bits.to(torch.int32).view(torch.float32)   # wraps to the uint32 pattern
         del bits
         p_t = torch.zeros(chunk, dtype=torch.int16, device=dev)
-        _, _, cnt = pulse.encode(m_t, p_t, idx_out=idx_t, val_out=val_t)
+        _, _, cnt = pulse.encode(m_t, p_t, idx_out=gi.t, val_out=gv.t)
         k = int(cnt.item())
         view = oracle.bf16_rne(np.arange(start, start + chunk, dtype=np.uint64).astype(np.uint32))
         exp_idx = np.nonzero(view)[0].astype(np.uint32)
         assert k == exp_idx.size, hex(start)
-        np.testing.assert_array_equal(host_u32(idx_t[:k]), exp_idx)
-        np.testing.assert_array_equal(host_u16(val_t[:k]), view[exp_idx])
+        np.testing.assert_array_equal(host_u32(gi.t[:k]), exp_idx)
+        np.testing.assert_array_equal(host_u16(gv.t[:k]), view[exp_idx])
+        np.testing.assert_array_equal(host_u16(p_t), view)
+        # prev already holds the oracle's view: nothing changes
+        p_t = dev_u16(view)
+        _, _, cnt = pulse.encode(m_t, p_t, idx_out=gi.t, val_out=gv.t)
+        assert int(cnt.item()) == 0, hex(start)
         np.testing.assert_array_equal(host_u16(p_t), view)
         del m_t, p_t
     assert pulse.get_error(dev) == 0
+    gi.check("idx")
+    gv.check("val")
 
 
 def test_lookback_watchdog_gives_up_and_context_survives():
@@ -283,23 +302,30 @@ def test_lookback_watchdog_gives_up_and_context_survives():
 # ------------------------------------------------------------- multi-tensor
 
 def _slots_from_np(masters, prevs, dev, offsets=None, with_w=True, with_mask=True):
-    slots, keep = [], []
+    """Plan slots over device copies of (master, prev), optionally shifted by
+    `offsets` elements from an aligned start. Every buffer sits between guard
+    zones; returns (slots, guards) and the caller checks the guards."""
+    slots, guards = [], []
     for i, (m, p) in enumerate(zip(masters, prevs)):
         off = 0 if offsets is None else offsets[i]
         n = m.size
-        mb = torch.zeros(n + off, dtype=torch.float32, device=dev)
-        pb = torch.zeros(n + off, dtype=torch.int16, device=dev)
+        gm = Guarded(n + off, torch.float32, dev)
+        gp = Guarded(n + off, torch.int16, dev)
+        gm.t.zero_()
+        gp.t.zero_()
         if n:
-            mb[off:] = dev_f32(m)
-            pb[off:] = dev_u16(p)
-        s = pulse.TensorSlot(n, master=mb[off:], prev=pb[off:],
-                             w=(pb[off:].clone() if with_w else None),
-                             idx=torch.empty(max(n, 1), dtype=torch.int32, device=dev),
-                             val=torch.empty(max(n, 1), dtype=torch.int16, device=dev),
-                             mask=(torch.empty(n, dtype=torch.int16, device=dev) if with_mask else None))
+            gm.t[off:] = dev_f32(m)
+            gp.t[off:] = dev_u16(p)
+        gw = guarded_u16(p) if with_w else None
+        gi = Guarded(max(n, 1), torch.int32, dev)
+        gv = Guarded(max(n, 1), torch.int16, dev)
+        gx = Guarded(n, torch.int16, dev) if with_mask else None
+        s = pulse.TensorSlot(n, master=gm.t[off:], prev=gp.t[off:],
+                             w=(gw.t if gw is not None else None), idx=gi.t, val=gv.t,
+                             mask=(gx.t if gx is not None else None))
         slots.append(s)
-        keep.append((mb, pb))
-    return slots, keep
+        guards += [g for g in (gm, gp, gw, gi, gv, gx) if g is not None]
+    return slots, guards
 
 
 @pytest.mark.parametrize("aligned", [True, False])
@@ -331,15 +357,18 @@ def test_multi_tensor_plan_parity(aligned):
     for t, s in enumerate(slots):
         np.testing.assert_array_equal(host_u16(s.w), o_prevs[t])
     assert plan.get_error() == 0
+    for g in keep:
+        g.check()
     plan.close()
 
 
 @pytest.mark.parametrize("eta", [1e-8, 3e-7, 1e-6, 1e-4])
 @pytest.mark.parametrize("device_counts", [True, False])
-def test_multi_apply_both_routes(eta, device_counts):
-    """A whole-model apply takes the entry scatter when 64 k < n and the
-    chunk-owned kernel otherwise (1e-4 also fills chunks far past the
-    entries a thread loads at once); every route gives the oracle's view."""
+def test_multi_apply_densities(eta, device_counts):
+    """Whole-model apply from about 0.05 % to 70 % of the view changed
+    (1e-4 also fills a tile with consecutive elements), with device and host
+    counts: every segment gives the oracle's view and nothing lands outside
+    w."""
     dev = _cuda()
     sizes = [3 * 8192 + 77, 1, 0, 65536 + 5, 8192, 200003]
     masters, prevs = [], []
@@ -351,9 +380,6 @@ def test_multi_apply_both_routes(eta, device_counts):
     slots, keep = _slots_from_np(masters, prevs, dev, with_mask=False)
     o_prevs = [p.copy() for p in prevs]
     o_patches = oracle.encode_multi(masters, o_prevs)
-    k = sum(o_idx.size for o_idx, _ in o_patches)
-    sparse = 64 * k < sum(sizes)
-    assert sparse == (eta < 1e-6)  # the cases cover both routes
     with pulse.Plan(slots) as plan:
         counts = plan.encode()
         plan.apply(counts if device_counts else counts.cpu().numpy().tolist())
@@ -362,7 +388,7 @@ def test_multi_apply_both_routes(eta, device_counts):
             np.testing.assert_array_equal(host_u16(s.w), o_prevs[t])
         assert plan.get_error() == 0
         # the same patch again changes nothing; an index past its tensor is
-        # skipped and reported on either route
+        # skipped and reported
         plan.apply(counts if device_counts else counts.cpu().numpy().tolist())
         assert plan.get_error() == 0
         if o_patches[0][0].size:
@@ -371,36 +397,36 @@ def test_multi_apply_both_routes(eta, device_counts):
             assert plan.get_error() == pulse.pulse.PULSE_ERR_INDEX
         for t, s in enumerate(slots[1:], start=1):
             np.testing.assert_array_equal(host_u16(s.w), o_prevs[t])
+    for g in keep:
+        g.check()
 
 
-@pytest.mark.parametrize("extra", [0, -1])
+@pytest.mark.parametrize("per_mille", [1, 15, 300])
 @pytest.mark.parametrize("device_counts", [True, False])
-def test_multi_apply_route_boundary(extra, device_counts):
-    """With the fewest entries for which 64 k >= n the chunk-owned route runs,
-    one entry fewer takes the scatter; both write exactly the patch (oracle
-    apply of the same entries)."""
+def test_multi_apply_sorted_random_patch(per_mille, device_counts):
+    """Sorted random patches (arbitrary values, not from an encode) whose
+    segments hold room for n entries: the apply writes exactly the patch
+    (oracle apply of the same entries) and nothing outside w."""
     dev = _cuda()
     sizes = [8192 * 5 + 11, 3 * 8192, 8192 + 1]
-    n = sum(sizes)
-    k_total = (n + 63) // 64 + extra
-    assert (64 * k_total < n) == (extra < 0)
-    rng = np.random.default_rng(321 + extra)
-    ks = [k_total * s // n for s in sizes]
-    ks[0] += k_total - sum(ks)
-    slots, w0s, patches = [], [], []
-    for s, k in zip(sizes, ks):
+    rng = np.random.default_rng(321 + per_mille)
+    slots, w0s, patches, guards = [], [], [], []
+    for s in sizes:
+        k = max(1, s * per_mille // 1000)
         w0 = rng.integers(0, 1 << 16, s, dtype=np.uint64).astype(np.uint16)
         idx = np.sort(rng.choice(s, size=k, replace=False)).astype(np.uint32)
         val = rng.integers(0, 1 << 16, k, dtype=np.uint64).astype(np.uint16)
         # segments with room for n entries (device counts are checked against that)
         idx_room, val_room = np.zeros(s, np.uint32), np.zeros(s, np.uint16)
         idx_room[:k], val_room[:k] = idx, val
-        slot = pulse.TensorSlot(s, w=dev_u16(w0), idx=dev_u32(idx_room), val=dev_u16(val_room))
+        gw = guarded_u16(w0)
+        slot = pulse.TensorSlot(s, w=gw.t, idx=dev_u32(idx_room), val=dev_u16(val_room))
         slots.append(slot)
+        guards.append(gw)
         w0s.append(w0)
         patches.append((idx, val))
     with pulse.Plan(slots) as plan:
-        counts = [int(k) for k in ks]
+        counts = [int(p[0].size) for p in patches]
         plan.apply(torch.tensor(counts, dtype=torch.int64, device=dev) if device_counts else counts)
         torch.cuda.synchronize()
         assert plan.get_error() == 0
@@ -408,6 +434,8 @@ def test_multi_apply_route_boundary(extra, device_counts):
             want = w0.copy()
             oracle.apply(want, idx, val)
             np.testing.assert_array_equal(host_u16(s.w), want)
+    for g in guards:
+        g.check("w")
 
 
 def test_multi_apply_host_counts_and_out_of_range_segment():
@@ -430,6 +458,8 @@ def test_multi_apply_host_counts_and_out_of_range_segment():
     # a count larger than the tensor is clamped and reported
     plan.apply([sizes[0] + 50, 0])
     assert plan.get_error() == pulse.pulse.PULSE_ERR_INDEX
+    for g in keep:
+        g.check()
     plan.close()
 
 
@@ -454,6 +484,8 @@ def test_multi_xor_parity(aligned):
     plan.xor_apply()
     for t, s in enumerate(slots):
         np.testing.assert_array_equal(host_u16(s.w), o_prevs[t])
+    for g in keep:
+        g.check()
     plan.close()
 
 

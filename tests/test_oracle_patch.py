@@ -274,3 +274,21 @@ def test_twenty_step_chain_receiver_stays_bit_identical(eta):
             assert np.count_nonzero(mk) == idx.size
             total_changed += idx.size
     assert total_changed > 0
+
+
+@pytest.mark.parametrize("n,parts", [(0, 4), (1, 4), (4097, 3), (1 << 16, 7), (1 << 16, 64)])
+def test_chunked_encode_and_apply_equal_the_single_thread_oracle(n, parts):
+    # The all-cores CPU baseline runs the same scalar loops on contiguous
+    # chunks (count pass, scan, emit pass); its patch must be the definition's.
+    from concurrent.futures import ThreadPoolExecutor
+    master, prev = workloads.np_pair(n, seed=300 + n)
+    old = prev.copy()
+    e_idx, e_val, b = _expected_patch(master, prev)
+    with ThreadPoolExecutor(max_workers=4) as pool:
+        idx, val = oracle.encode_chunked(master, prev, pool, parts)
+        np.testing.assert_array_equal(idx, e_idx)
+        np.testing.assert_array_equal(val, e_val)
+        np.testing.assert_array_equal(prev, b)
+        w = old.copy()
+        oracle.apply_chunked(w, idx, val, pool, parts)
+    np.testing.assert_array_equal(w, b)
