@@ -248,6 +248,11 @@ int pulse_apply_multi_device(pulse_plan *plan, const uint64_t *counts_dev, cudaS
  * 32-byte sectors are written back once. Needs w for every tensor with n > 0
  * (idx, val and master of the plan are not used). Growing the call's
  * internal tables synchronises `stream`; one stream at a time per plan.
+ * This is the fastest way for a receiver that holds w to catch up: four
+ * 8%-dense versions of an 8.03B-parameter model take about 8.2 ms, against
+ * about 20 ms for four whole-model applies and 17 ms for composing them with
+ * pulse_compose_chain_multi and applying the result. Compose only where the
+ * single patch itself is wanted (to send one patch over the network).
  * Errors: PULSE_ERR_INVALID (NULL plan or patches, nversions < 1, a plan
  * tensor without w, count > 0 with NULL idx or val), PULSE_ERR_RANGE (a
  * count >= 2^32), PULSE_ERR_NOMEM, PULSE_ERR_CUDA; device (plan error word):
@@ -283,7 +288,8 @@ int pulse_apply_chain_multi(pulse_plan *plan, const pulse_patch_ref *patches, in
  * nversions outside 1..16, an output segment without room), PULSE_ERR_RANGE,
  * PULSE_ERR_NOMEM, PULSE_ERR_CUDA; device (plan error word): PULSE_ERR_INDEX
  * (count > n, clamped; an entry outside its chunk, skipped),
- * PULSE_ERR_TIMEOUT.
+ * PULSE_ERR_TIMEOUT. A receiver that holds w catches up faster with
+ * pulse_apply_chain_multi; composing pays where one patch must be sent.
  */
 typedef struct pulse_patch_out {
     uint32_t *idx;  /* device, room entries */
@@ -443,6 +449,9 @@ int pulse_unpack_indices_multi(const pulse_pack_segment *segs, int nsegs, cudaSt
  * every index listed by A or B, with B's value where both list it (the later
  * patch wins), in ascending order. A chain of m patches composes by folding
  * left; applying the result once equals applying the m patches in order.
+ * For a whole model, pulse_compose_chain_multi composes up to 16 versions in
+ * one pass (and pulse_apply_chain_multi applies them without composing),
+ * both far faster than folding pairs with these calls.
  * Preconditions: within each input, indices strictly ascending (what encode
  * produces); output buffers hold count_a + count_b entries and overlap no
  * input. Counts in are HOST values, count out is DEVICE memory.

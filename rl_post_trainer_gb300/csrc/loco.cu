@@ -473,7 +473,9 @@ int loco_blocks_per_sm() {
 
 // ------------------------------------------------------------ accumulate
 // acc[idx[j]] += val[j] (FP32) over one patch segment; an index of a single
-// patch appears once, so no two threads touch the same element.
+// patch appears once, so no two threads touch the same element, and a thread's
+// entries are distinct elements: all of its acc loads are issued before any
+// of its stores (one memory round trip per tile instead of one per entry).
 constexpr int kAccThreads = 256;
 constexpr int kAccPerThread = 8;
 constexpr int kAccTile = kAccThreads * kAccPerThread;
@@ -481,26 +483,26 @@ constexpr int kAccTile = kAccThreads * kAccPerThread;
 __device__ __forceinline__ void acc_tile(float* acc, uint64_t n, const uint32_t* idx,
                                          const float* val, uint64_t count, uint64_t tile,
                                          uint32_t* err) {
-  const uint64_t b = tile * kAccTile;
+  const uint64_t b = tile * kAccTile + threadIdx.x;
   uint32_t ii[kAccPerThread];
-  float vv[kAccPerThread];
+  float vv[kAccPerThread], av[kAccPerThread];
+  bool ok[kAccPerThread];
 #pragma unroll
   for (int k = 0; k < kAccPerThread; ++k) {
-    const uint64_t j = b + uint64_t(k) * kAccThreads + threadIdx.x;
-    ii[k] = j < count ? idx[j] : 0u;
-    vv[k] = j < count ? val[j] : 0.0f;
+    const uint64_t j = b + uint64_t(k) * kAccThreads;
+    ii[k] = j < count ? __ldcs(idx + j) : 0u;
+    vv[k] = j < count ? __ldcs(val + j) : 0.0f;
   }
 #pragma unroll
   for (int k = 0; k < kAccPerThread; ++k) {
-    const uint64_t j = b + uint64_t(k) * kAccThreads + threadIdx.x;
-    if (j < count) {
-      if (uint64_t(ii[k]) >= n) {
-        record_error(err, kErrIndex);
-        continue;
-      }
-      acc[ii[k]] = __fadd_rn(acc[ii[k]], vv[k]);
-    }
+    const uint64_t j = b + uint64_t(k) * kAccThreads;
+    ok[k] = j < count && uint64_t(ii[k]) < n;
+    if (j < count && !ok[k]) record_error(err, kErrIndex);
+    av[k] = ok[k] ? acc[ii[k]] : 0.0f;
   }
+#pragma unroll
+  for (int k = 0; k < kAccPerThread; ++k)
+    if (ok[k]) acc[ii[k]] = __fadd_rn(av[k], vv[k]);
 }
 
 __global__ void __launch_bounds__(kAccThreads)

@@ -101,9 +101,9 @@ def test_pack_an_encode_patch():
 
 
 def _check_job(segs_np, dev, offsets=None):
-    """Pack a list of segments in one launch (PackJob) and compare every
+    """Pack a list of segments in one call (PackJob) and compare every
     segment's arrays with the oracle packing that segment alone; unpack
-    them all in one launch and compare with the input."""
+    them all in one call and compare with the input."""
     tens = []
     for i, a in enumerate(segs_np):
         off = 0 if offsets is None else offsets[i]
@@ -131,7 +131,7 @@ def _check_job(segs_np, dev, offsets=None):
 
 
 def test_pack_job_many_segments():
-    """Segments of every size edge (empty ones included) in one launch: the
+    """Segments of every size edge (empty ones included) in one call: the
     look-back restarts at each segment's first chunk."""
     dev = _dev()
     rng = np.random.default_rng(77)
@@ -165,3 +165,15 @@ def test_pack_job_all_empty():
     job.unpack()
     torch.cuda.synchronize()
     assert pulse.get_error(dev) == 0
+
+
+def test_segments_spanning_several_scan_tiles():
+    """Segments of more than 1024 chunks (4,194,304 entries), alone and in
+    one job: long look-back chains within a segment, restarted at each one."""
+    dev = _dev()
+    rng = np.random.default_rng(99)
+    big = 2 * 1024 * 4096 + 4096 * 3 + 17   # three scan tiles
+    _check(_random_idx(rng, big, 11), dev)
+    segs = [_random_idx(rng, 1024 * 4096 + 1, 5), _random_idx(rng, 300, 1000),
+            _random_idx(rng, big, 0)]
+    _check_job(segs, dev)
