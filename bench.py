@@ -54,7 +54,10 @@ SPARSE_ETA = 3e-7
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "encode_traffic.json")
 ENCODE_SRCS = [os.path.join(ROOT, "rl_post_trainer_gb300", "csrc", f)
-               for f in ("encode.cu", "encode_common.cuh", "pulse_internal.h", "pulse_device.cuh")]
+               for f in ("encode.cu", "encode_common.cuh", "pulse_device.cuh")]
+# the encode kernel's part of the internal header: everything before this line
+INTERNAL_H = os.path.join(ROOT, "rl_post_trainer_gb300", "csrc", "pulse_internal.h")
+INTERNAL_H_ENCODE_END = b"// ------------------------------------------------------- MX view encode"
 
 
 # ------------------------------------------------------------- utilities
@@ -77,11 +80,14 @@ def measured_peak_gbs():
 
 
 def encode_source_hash() -> str:
-    """sha256 over the encode kernel's sources, in a fixed order."""
+    """sha256 over the encode kernel's sources, in a fixed order (the shared
+    internal header up to its encode section's end only)."""
     h = hashlib.sha256()
     for path in ENCODE_SRCS:
         with open(path, "rb") as f:
             h.update(f.read())
+    with open(INTERNAL_H, "rb") as f:
+        h.update(f.read().split(INTERNAL_H_ENCODE_END)[0])
     return h.hexdigest()
 
 
