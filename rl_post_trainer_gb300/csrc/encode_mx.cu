@@ -754,8 +754,18 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
   }
 }
 
+// Resident CTAs per SM the register budget is sized for: the FP4 formats'
+// smaller stages and ring leave shared memory for more CTAs than E4M3's.
+#ifndef PULSE_MX4_MIN_BLOCKS
+#define PULSE_MX4_MIN_BLOCKS 3
+#endif
+template <int F>
+constexpr int mx_min_blocks() {
+  return F == kFmtE4M3 ? kEncMinBlocks : PULSE_MX4_MIN_BLOCKS;
+}
+
 template <int F, bool MULTI>
-__global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
+__global__ void __launch_bounds__(kEncBlockThreads, mx_min_blocks<F>())
     encode_mx_kernel(const __grid_constant__ MxLaunch a) {
   constexpr uint32_t kStageBytes = Stage<F>::kBytes;
   constexpr int kEncStages = Stage<F>::kStages;
