@@ -279,6 +279,62 @@ def test_exhaustive_fp32_patterns_through_the_gpu_cast():
     gv.check("val")
 
 
+def _host_mem_available() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def test_encode_and_apply_at_the_index_limit():
+    """One tensor of 2^32 - 1 elements, the largest a uint32 index can
+    address: the patch's indices reach past 2^31 and up to 2^32 - 2. At a
+    small update (about 0.4 % changed) the whole patch, the refreshed prev and
+    the applied w are compared with the oracle (run chunk-parallel on the host
+    cores: the same scalar loops)."""
+    from concurrent.futures import ThreadPoolExecutor
+    dev = _cuda()
+    n = (1 << 32) - 1
+    if _host_mem_available() < (96 << 30):
+        pytest.skip("needs about 96 GB of host memory for the oracle's copies")
+    spec = workloads.single(n)[0]
+    gen = workloads.torch_generator(dev, 4242)
+    m_t = torch.empty(n, dtype=torch.float32, device=dev)
+    workloads.torch_init_(m_t, spec, gen)
+    p0_t = torch.empty(n, dtype=torch.int16, device=dev)
+    workloads.torch_bf16_view_(p0_t, m_t)
+    workloads.torch_update_(m_t, 1e-7, gen)
+    master = m_t.cpu().numpy()
+    p0 = host_u16(p0_t)
+    prev_t = p0_t.clone()
+    gi = Guarded(n, torch.int32, dev)
+    gv = Guarded(n, torch.int16, dev)
+    _, _, cnt = pulse.encode(m_t, prev_t, idx_out=gi.t, val_out=gv.t)
+    k = int(cnt.item())
+    del m_t
+    w_t = p0_t
+    pulse.apply(w_t, gi.t, gv.t, k)
+    torch.cuda.synchronize()
+    assert pulse.get_error(dev) == 0
+    o_prev = p0.copy()
+    with ThreadPoolExecutor(max_workers=16) as pool:
+        o_idx, o_val = oracle.encode_chunked(master, o_prev, pool, 256)
+    del master
+    assert k == o_idx.size and k > n // 400
+    assert int(o_idx[-1]) > (1 << 31)
+    np.testing.assert_array_equal(host_u32(gi.t[:k]), o_idx)
+    np.testing.assert_array_equal(host_u16(gv.t[:k]), o_val)
+    del o_idx, o_val
+    assert np.array_equal(host_u16(prev_t), o_prev)
+    assert np.array_equal(host_u16(w_t), o_prev)
+    gi.check("idx")
+    gv.check("val")
+
+
 def test_lookback_watchdog_gives_up_and_context_survives():
     # tile 0 is never processed, so tile 1's look-back waits for a word that
     # nothing publishes; the bounded wait must give up (50 ms) and report
