@@ -275,6 +275,31 @@ __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShare
 }
 
 // ------------------------------------------------------------ compute warps
+// Four consecutive elements from element li of a tail or unaligned tile, read
+// from global memory: elements past the end read as +0 with a +0 view, which
+// never counts as a change. Out of line: the bulk path is the hot one, and
+// this one, inlined at every round of both passes, only added to its code.
+struct RoundIn {
+  float4 mv;
+  uint2 pv;
+};
+
+__device__ __noinline__ RoundIn load_round_generic(const float* master, const uint16_t* prev,
+                                                   uint64_t base, uint32_t len, uint32_t li) {
+  float mm[4];
+  uint32_t pp[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const bool valid = li + e < len;
+    mm[e] = valid ? master[base + li + e] : 0.0f;
+    pp[e] = valid ? uint32_t(prev[base + li + e]) : 0u;
+  }
+  RoundIn r;
+  r.mv = make_float4(mm[0], mm[1], mm[2], mm[3]);
+  r.pv = make_uint2(pp[0] | (pp[1] << 16), pp[2] | (pp[3] << 16));
+  return r;
+}
+
 template <bool MULTI>
 __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared& sh,
                                              uint8_t* stages, uint32_t* ring, int tid, int lane,
@@ -303,17 +328,10 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
         mv = sm[j * kEncThreads + tid];
         pv = sp[j * kEncThreads + tid];
       } else {
-        const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
-        float mm[4];
-        uint32_t pp[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const bool valid = li + e < len;
-          mm[e] = valid ? m.master[base + li + e] : 0.0f;
-          pp[e] = valid ? uint32_t(m.prev[base + li + e]) : 0u;
-        }
-        mv = make_float4(mm[0], mm[1], mm[2], mm[3]);
-        pv = make_uint2(pp[0] | (pp[1] << 16), pp[2] | (pp[3] << 16));
+        const RoundIn r = load_round_generic(m.master, m.prev, base, len,
+                                             uint32_t(j * kEncThreads + tid) * 4u);
+        mv = r.mv;
+        pv = r.pv;
       }
     };
     auto compare_round = [&](int j, const uint2& pv) {
