@@ -376,19 +376,7 @@ __device__ __forceinline__ void cc_compute(const CcArgs& a, CcShared& sh, int ti
     const int q = int(posted % kPendSlots);
     if (posted >= uint32_t(kPendSlots))
       failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kPendSlots) / kPendSlots) & 1u, a);
-    if (ring_head + agg - *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) > uint32_t(kCcRing)) {
-      const uint64_t t0 = global_timer_ns();
-      while (ring_head + agg - *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) >
-             uint32_t(kCcRing)) {
-        __nanosleep(256);
-        if (global_timer_ns() - t0 > a.wait_limit_ns ||
-            (ld_volatile_u32(a.counters + 2) & kErrTimeout)) {
-          record_error(a.counters + 2, kErrTimeout);
-          failed = true;
-          break;
-        }
-      }
-    }
+    failed |= !wait_ring_room<256>(&sh.ring_tail, ring_head, agg, uint32_t(kCcRing), a);
 
     // ---- park the chunk's entries in ascending order
     uint32_t r = ring_head + before + (incl - c);

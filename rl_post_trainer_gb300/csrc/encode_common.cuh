@@ -104,6 +104,29 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, con
   return false;
 }
 
+// Bounded wait of a compute thread for room in its CTA's entry ring: until
+// head + need - tail <= cap, with tail advanced by the copy-out warp. The
+// spin reads only shared memory; the clock and the launch's error word (which
+// shares an L2 sector with the tile tickets) are read every 64th turn, so a
+// dense tile's waiting threads do not keep that sector busy for every CTA.
+// Returns false if it gave up (the error is recorded).
+template <unsigned kSleepNs, class L>
+__device__ __forceinline__ bool wait_ring_room(const uint32_t* tail, uint32_t head, uint32_t need,
+                                               uint32_t cap, const L& a) {
+  const volatile uint32_t* t = tail;
+  if (head + need - *t <= cap) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t spin = 0; head + need - *t > cap; ++spin) {
+    __nanosleep(kSleepNs);
+    if ((spin & 63u) == 63u &&
+        (global_timer_ns() - t0 > a.wait_limit_ns || (ld_volatile_u32(a.counters + 2) & kErrTimeout))) {
+      record_error(a.counters + 2, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
 template <class T>
 __device__ __forceinline__ T warp_sum(T v) {
 #pragma unroll

@@ -711,19 +711,7 @@ __device__ __forceinline__ void compute_loop(const MxLaunch& a, MxShared& sh, ui
     const int q = int(posted % kPendSlots);
     if (posted >= uint32_t(kPendSlots))
       failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kPendSlots) / kPendSlots) & 1u, a);
-    if (ring_head + agg_c - *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) > uint32_t(kEncRing)) {
-      const uint64_t t0 = global_timer_ns();
-      while (ring_head + agg_c - *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) >
-             uint32_t(kEncRing)) {
-        __nanosleep(64);
-        if (global_timer_ns() - t0 > a.wait_limit_ns ||
-            (ld_volatile_u32(a.counters + 2) & kErrTimeout)) {
-          record_error(a.counters + 2, kErrTimeout);
-          failed = true;
-          break;
-        }
-      }
-    }
+    failed |= !wait_ring_room<64>(&sh.ring_tail, ring_head, agg_c, uint32_t(kEncRing), a);
 
     // ---- park the compacted tile
 #pragma unroll
