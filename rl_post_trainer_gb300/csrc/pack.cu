@@ -12,14 +12,15 @@
 //  * chunks of 32 blocks (4096 entries): chunk_off[c] = byte offset of the
 //    chunk's first payload, so every chunk decodes on its own.
 //
-// Pack: persistent CTAs (8 per SM) take chunks in ticket order, a ticket
-// when its chunk starts; each warp measures and packs 4 blocks (bits OR-ed
-// into shared-memory words); the chunk's payload offset is the exclusive
-// prefix of the chunk sizes, found with the decoupled look-back shared with
-// the encode kernels (warp 0), counted in 16-byte units.
-// The pack CTAs keep the segments' chunk ranges in shared memory (loaded
-// once per CTA when there are fewer than kSegCache segments), so finding a
-// chunk's segment costs no dependent global loads.
+// Pack: persistent warp-specialized CTAs (3 per SM). A producer warp stages
+// each chunk's indices with a bulk copy; 8 compute warps measure and pack 4
+// blocks each and park the chunk's words in a shared-memory ring; a look-back
+// warp finds the chunk's payload offset (the exclusive prefix of the chunk
+// sizes, in 16-byte units, with the decoupled look-back shared with the
+// encode kernels) and copies the words out, so no compute warp waits on
+// another CTA. The CTAs keep the segments' chunk ranges in shared memory
+// (loaded once per CTA when there are fewer than kSegCache segments), so
+// finding a chunk's segment costs no dependent global loads.
 // Unpack: one CTA per chunk; each warp extracts a block's gaps and rebuilds
 // its indices with a warp scan.
 #include "encode_common.cuh"
@@ -50,24 +51,24 @@ constexpr int kSegCache = 1024;  // segments whose chunk ranges a CTA keeps in s
 #ifndef PULSE_PACK_LOOKBACK
 #define PULSE_PACK_LOOKBACK 1
 #endif
-// Status words per lane and look-back round trip. The whole CTA waits for
-// its chunk's prefix, so the look-back's own latency is what counts: one word
-// per lane (32 predecessors per round trip) measured faster than 2, 4 or 8.
+// Status words per lane and look-back round trip (32 predecessors per round
+// trip with one word per lane).
 constexpr int kPackLookback = PULSE_PACK_LOOKBACK;
-constexpr int kPackCtasPerSm = 8;
 
 // Copy the chunk ranges into shared memory when they fit (multi-segment).
 template <bool MULTI>
-__device__ __forceinline__ void load_seg_begin(const PackLaunch& a, uint64_t* sbeg) {
+__device__ __forceinline__ void load_seg_begin(const PackLaunch& a, uint32_t* sbeg, int nthreads) {
+  // fewer than kSegCache segments of fewer than 2^20 chunks each: the chunk
+  // numbers fit 32 bits
   if (MULTI && a.nsegs < kSegCache)
-    for (int k = threadIdx.x; k <= a.nsegs; k += kPackThreads) sbeg[k] = a.chunk_begin[k];
+    for (int k = threadIdx.x; k <= a.nsegs; k += nthreads) sbeg[k] = uint32_t(a.chunk_begin[k]);
 }
 
 // The segment that global chunk c belongs to: the largest s with
 // chunk_begin[s] <= c (chunk_begin[nsegs] = total > c); sbeg: the shared
 // copy of chunk_begin, or null to search the global one.
 template <bool MULTI>
-__device__ __forceinline__ PackSegment segment_of(const PackLaunch& a, const uint64_t* sbeg,
+__device__ __forceinline__ PackSegment segment_of(const PackLaunch& a, const uint32_t* sbeg,
                                                   uint64_t c) {
   if (!MULTI) return a.one;
   if (sbeg == nullptr || a.nsegs >= kSegCache)
@@ -82,142 +83,407 @@ __device__ __forceinline__ PackSegment segment_of(const PackLaunch& a, const uin
 
 __device__ __forceinline__ uint32_t bit_width(uint32_t v) { return v ? 32u - __clz(v) : 0u; }
 
-struct PackSmem {
-  uint32_t words[kPackWarps][kBlocksPerWarp][kPackBlock];  // every block's packed words
-  uint32_t width_of[kPackChunkBlocks];
-  uint32_t prefix16;
+// ----------------------------------------------------------------- pack
+// Persistent, warp-specialized CTA (the shape of the BF16 encode kernel):
+//  * producer warp (one thread): takes chunk tickets one fill ahead and
+//    stages each chunk's 4096 indices (16 KB) in a kPkStages-deep ring with a
+//    bulk copy (plain loads by the compute threads for a segment's last,
+//    partial chunk or an index array that is not 16-byte aligned);
+//  * 8 compute warps (4 blocks each): form the gaps, take each block's width,
+//    write firsts and widths, publish the chunk's size (16-byte units) in its
+//    status word, and park the chunk's packed words in a shared-memory word
+//    ring (gap bits OR-ed into zeroed words);
+//  * one look-back warp: resolves each parked chunk's payload offset with the
+//    decoupled look-back, writes chunk_off (and the segment's payload size
+//    after its last chunk), copies the words to the payload with 16-byte
+//    stores and frees the ring.
+// The compute warps never wait on another CTA: while a chunk's offset is
+// resolved they pack the next ones (up to kPkSlots parked chunks).
+constexpr int kPkCompute = 256;                     // compute threads (8 warps)
+constexpr int kPkWarps = kPkCompute / 32;
+constexpr int kPkProducerWarp = kPkWarps;
+constexpr int kPkLookbackWarp = kPkWarps + 1;
+constexpr int kPkThreads = kPkCompute + 64;
+#ifndef PULSE_PK_STAGES
+#define PULSE_PK_STAGES 2
+#endif
+#ifndef PULSE_PK_CTAS
+#define PULSE_PK_CTAS 3
+#endif
+constexpr int kPkStages = PULSE_PK_STAGES;
+constexpr int kPkSlots = 8;                         // parked chunks per CTA
+#ifndef PULSE_PK_RING
+#define PULSE_PK_RING 4096
+#endif
+constexpr uint32_t kPkRing = PULSE_PK_RING;         // parked payload words per CTA
+constexpr uint32_t kPkRingMask = kPkRing - 1u;
+constexpr uint32_t kPkStageBytes = kPackChunk * 4;  // 16 KB of indices
+constexpr int kPkCtasPerSm = PULSE_PK_CTAS;
+static_assert(kPkCompute == kEncThreads, "the compute warps use the encode's named barrier");
+static_assert(kBlocksPerWarp * kPkWarps == kPackChunkBlocks, "8 warps x 4 blocks per chunk");
+static_assert(kPkRing >= uint32_t(kPackChunkBlocks) * 4u * 32u, "a chunk of 32-bit gaps fits the ring");
+constexpr size_t kPkDynSmem = size_t(kPkStages) * kPkStageBytes + size_t(kPkRing) * 4 + 128;
+
+enum : uint32_t { kPkEnd = 0, kPkBulk = 1, kPkGeneric = 2 };
+
+struct PkStageMeta {
+  uint64_t c;        // global chunk
+  uint64_t lc;       // chunk within its segment
+  uint32_t mode;
+  uint32_t cnt;      // indices in the chunk
+  PackSegment sg;
 };
 
-// Pack chunk c (of segment sg): firsts, widths, the chunk's payload offset
-// (look-back) and its payload. Ends with every thread done with `sm`.
+struct PkParked {
+  uint64_t c, first, lc;
+  uint32_t agg;      // payload size in 16-byte units
+  uint32_t ring_start;
+  uint32_t last;     // 1: the segment's last chunk; 2: no more chunks
+  uint64_t* chunk_off;
+  uint8_t* payload;
+  uint64_t* payload_bytes;
+};
+
+struct __align__(16) PkShared {
+  uint64_t full[kPkStages];
+  uint64_t empty[kPkStages];
+  uint64_t agg_ready[kPkSlots];
+  uint64_t slot_free[kPkSlots];
+  PkStageMeta meta[kPkStages];
+  PkParked parked[kPkSlots];
+  uint32_t wid[2][kPackChunkBlocks];  // block widths, by iteration parity
+  uint32_t ring_tail;
+};
+
 template <bool MULTI>
-__device__ __forceinline__ void pack_chunk(const PackLaunch& a, PackSmem& sm, uint64_t c,
-                                           const PackSegment& sg) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint64_t lc = c - sg.chunk_begin;  // chunk within the segment
-  const uint64_t chunk_first = lc * kPackChunk;
+__device__ __forceinline__ void pk_producer(const PackLaunch& a, PkShared& sh, uint8_t* stages,
+                                            const uint32_t* sbeg) {
+  const uint64_t pol_stream = l2_policy_evict_first();
+  uint32_t fills_done = 0;
+  uint64_t ticket = atomicAdd(a.counters + 0, 1u);
+  for (uint32_t it = 0;; ++it) {
+    const int s = int(it % kPkStages);
+    const bool end = ticket >= a.total_chunks;
+    const uint64_t next = end ? ticket : uint64_t(atomicAdd(a.counters + 0, 1u));
+    if (it >= uint32_t(kPkStages) &&
+        !enc::helper_wait(&sh.empty[s], ((it / kPkStages) - 1) & 1u, a))
+      break;
+    fills_done = it + 1;
+    PkStageMeta m{};
+    m.c = ticket;
+    if (end) {
+      m.mode = kPkEnd;
+      sh.meta[s] = m;
+      mbar_arrive(&sh.full[s]);
+      break;
+    }
+    m.sg = segment_of<MULTI>(a, sbeg, ticket);
+    m.lc = ticket - m.sg.chunk_begin;
+    const uint64_t start = m.lc * kPackChunk;
+    m.cnt = uint32_t(m.sg.count - start < uint64_t(kPackChunk) ? m.sg.count - start : kPackChunk);
+    const uint32_t* src = m.sg.idx + start;
+    if (m.cnt == uint32_t(kPackChunk) && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+      m.mode = kPkBulk;
+      sh.meta[s] = m;
+      mbar_arrive_expect_tx(&sh.full[s], kPkStageBytes);
+      bulk_g2s(stages + size_t(s) * kPkStageBytes, src, kPkStageBytes, &sh.full[s], pol_stream);
+    } else {
+      m.mode = kPkGeneric;
+      sh.meta[s] = m;
+      mbar_arrive(&sh.full[s]);
+    }
+    ticket = next;
+  }
+  // no bulk copy may still be in flight when the CTA exits
+  for (uint32_t f = fills_done > uint32_t(kPkStages) ? fills_done - kPkStages : 0u; f < fills_done; ++f)
+    mbar_wait_bounded(&sh.full[f % kPkStages], (f / kPkStages) & 1u, a.wait_limit_ns);
+  // the last CTA to stop taking tickets rewinds the counters for the next launch
+  __threadfence();
+  const uint32_t finished = atomicAdd(a.counters + 1, 1u);
+  if (finished == gridDim.x - 1) {
+    atomicExch(a.counters + 0, 0u);
+    atomicExch(a.counters + 1, 0u);
+  }
+}
 
-  // ---- widths and firsts; the gaps stay in registers
-  uint32_t gap[kBlocksPerWarp][4];
-  uint32_t cnt_blk[kBlocksPerWarp];
-#pragma unroll
-  for (int q = 0; q < kBlocksPerWarp; ++q) {
-    const int lb = warp * kBlocksPerWarp + q;
-    const uint64_t start = chunk_first + uint64_t(lb) * kPackBlock;
-    const uint32_t cnt = start < sg.count ? uint32_t(sg.count - start < kPackBlock ? sg.count - start : kPackBlock) : 0u;
-    cnt_blk[q] = cnt;
-    uint32_t v[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
-      v[e] = j < cnt ? sg.idx[start + j] : 0u;
-    }
-    const uint32_t before = __shfl_up_sync(0xFFFFFFFFu, v[3], 1);  // lane - 1's last entry
-    uint32_t mx = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
-      const uint32_t prev = e == 0 ? before : v[e - 1];
-      gap[q][e] = (j >= 1 && j < cnt) ? v[e] - prev - 1u : 0u;
-      mx = max(mx, gap[q][e]);
-    }
-    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+// Copy a parked chunk's words to payload + 16 * prefix (16-byte units; the
+// payload is 16-byte aligned and the chunk's words start at a ring position
+// that is a multiple of 4, so no unit straddles the ring's end).
+__device__ __forceinline__ void pk_copy_out(const PkParked& pm, uint32_t prefix, const uint32_t* ring,
+                                            int lane) {
+  uint4* dst = reinterpret_cast<uint4*>(pm.payload) + prefix;
+  for (uint32_t k = uint32_t(lane); k < pm.agg; k += 32)
+    dst[k] = *reinterpret_cast<const uint4*>(ring + ((pm.ring_start + 4u * k) & kPkRingMask));
+}
+
+__device__ __forceinline__ void pk_lookback(const PackLaunch& a, PkShared& sh, const uint32_t* ring,
+                                            int lane) {
+  for (uint32_t i = 0;;) {
+    const bool ok = enc::helper_wait(&sh.agg_ready[i % kPkSlots], (i / kPkSlots) & 1u, a);
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    int more = 0;
     if (lane == 0) {
-      sm.width_of[lb] = cnt ? bit_width(mx) : 0u;
-      if (cnt) {
-        sg.firsts[start / kPackBlock] = v[0];
-        sg.widths[start / kPackBlock] = uint8_t(bit_width(mx));
+      for (int b = 1; b < enc::kLookbackBatch; ++b) {
+        const uint32_t ii = i + uint32_t(b);
+        if (!mbar_test_wait(&sh.agg_ready[ii % kPkSlots], (ii / kPkSlots) & 1u)) break;
+        more = b;
       }
     }
-  }
-  __syncthreads();
-
-  // ---- every block's gaps into shared words; warp 0 first finds the chunk's
-  // payload offset (16-byte units) with the look-back, so the other warps
-  // pack while it waits
-  auto pack_words = [&](int q) {
-    const int lb = warp * kBlocksPerWarp + q;
-    const uint32_t b = sm.width_of[lb];
-    if (b == 0u) return;  // warp-uniform
-    uint32_t* words = sm.words[warp][q];
-    for (uint32_t w = lane; w < 4u * b; w += 32) words[w] = 0u;
-    __syncwarp();
+    more = __shfl_sync(0xFFFFFFFFu, more, 0);
+    int nb = 0;
+    bool end = false;
+    uint64_t win[enc::kLookbackBatch][kPackLookback];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
-      if (j >= 1 && j < cnt_blk[q] && gap[q][e] != 0u) {
-        const uint32_t bit = (j - 1u) * b;
-        const uint32_t w0 = bit >> 5, sh = bit & 31u;
-        atomicOr(&words[w0], gap[q][e] << sh);
-        if (sh + b > 32u) atomicOr(&words[w0 + 1], gap[q][e] >> (32u - sh));
+    for (int b = 0; b < enc::kLookbackBatch; ++b) {
+      if (b > more || end) continue;
+      const uint32_t ii = i + uint32_t(b);
+      const int q = int(ii % kPkSlots);
+      if (b > 0) mbar_test_wait(&sh.agg_ready[q], (ii / kPkSlots) & 1u);  // acquire for every lane
+      const PkParked& pm = sh.parked[q];
+      if (pm.last == 2u) {
+        end = true;
+        continue;
+      }
+      if (pm.c != pm.first)
+        enc::load_window<enc::StatusEpoch, PackLaunch, kPackLookback>(a, int64_t(pm.c) - 1, pm.first,
+                                                                      lane, win[b]);
+      nb = b + 1;
+    }
+#pragma unroll
+    for (int b = 0; b < enc::kLookbackBatch; ++b) {
+      if (b >= nb) continue;
+      const uint32_t ii = i + uint32_t(b);
+      const int q = int(ii % kPkSlots);
+      const PkParked pm = sh.parked[q];
+      const uint32_t prefix = enc::resolve_prefix<enc::StatusEpoch, PackLaunch, 32, kPackLookback>(
+          a, pm.c, pm.first, pm.agg, lane, win[b]);
+      if (lane == 0) {
+        pm.chunk_off[pm.lc] = uint64_t(prefix) * 16u;
+        if (pm.last == 1u) *pm.payload_bytes = (uint64_t(prefix) + pm.agg) * 16u;
+      }
+      pk_copy_out(pm, prefix, ring, lane);
+      __syncwarp();
+      if (lane == 0) {
+        // chunks are copied out in order: every word before this chunk's end is free
+        __threadfence_block();
+        *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) = pm.ring_start + 4u * pm.agg;
+        mbar_arrive(&sh.slot_free[q]);
       }
     }
-  };
-  if (warp == 0) {
-    const uint32_t wl = sm.width_of[lane];
-    const uint32_t agg = __reduce_add_sync(0xFFFFFFFFu, wl);
-    // the look-back restarts at each segment's first chunk
-    const uint64_t first = sg.chunk_begin;
-    if (lane == 0)
-      st_relaxed_u64(a.status + c, make_status(c == first ? kFlagPrefix : kFlagAggregate, a.epoch, agg));
-    uint32_t p = 0;
-    if (c != first) {
-      uint64_t win[kPackLookback];
-      enc::load_window<enc::StatusEpoch, PackLaunch, kPackLookback>(a, int64_t(c) - 1, first, lane,
-                                                                   win);
-      p = enc::resolve_prefix<enc::StatusEpoch, PackLaunch, 32, kPackLookback>(a, c, first, agg,
-                                                                              lane, win);
-    }
-    if (lane == 0) {
-      sm.prefix16 = p;
-      sg.chunk_off[lc] = uint64_t(p) * 16u;
-      if ((lc + 1) * kPackChunk >= sg.count) *sg.payload_bytes = (uint64_t(p) + agg) * 16u;
-    }
+    if (end) break;
+    i += uint32_t(nb);
   }
-#pragma unroll
-  for (int q = 0; q < kBlocksPerWarp; ++q) pack_words(q);
-  __syncthreads();  // the offset and every block's words are in shared memory
+}
 
-  // ---- write the words out
-  uint32_t off16 = sm.prefix16;
-  for (int q = 0; q < warp * kBlocksPerWarp; ++q) off16 += sm.width_of[q];
+// A block's payload words from its gaps. Lane l holds the gaps of entries
+// 4l .. 4l+3, i.e. bit slots 4l-1 .. 4l+2 of the block's bit string (slot t
+// at bits t*b; lane 0's first gap is the block's first entry, always 0), so
+// its 4b-bit string S_l lies at bit 4lb - b (lane 0: its last 3b bits at bit
+// 0). The block's 4b words (ring positions base + w, masked) are zeroed,
+// then each lane ORs S_l in: at most 2 words for b <= 8, 5 for wider gaps;
+// only non-zero parts are written, and every written word lies inside the
+// block's 4b (its string ends at bit 127b). Whole warp; b warp-uniform.
+__device__ __forceinline__ void pk_block_words(const uint32_t (&g)[4], uint32_t b, uint32_t* ring,
+                                               uint32_t base, int lane) {
+  if (b == 0u) return;
+  const uint32_t L = 4u * b;
+  for (uint32_t w = uint32_t(lane); w < L; w += 32) ring[(base + w) & kPkRingMask] = 0u;
+  __syncwarp();
+  const uint32_t P = lane == 0 ? 0u : uint32_t(lane) * L - b;  // first bit of this lane's string
+  const uint32_t w0 = base + (P >> 5), sh = P & 31u;
+  if (b <= 8u) {
+    uint32_t S = g[0] | (g[1] << b) | (g[2] << (2u * b)) | (g[3] << (3u * b));
+    if (lane == 0) S >>= b;
+    const uint32_t x0 = S << sh, x1 = sh ? S >> (32u - sh) : 0u;
+    if (x0) atomicOr(&ring[w0 & kPkRingMask], x0);
+    if (x1) atomicOr(&ring[(w0 + 1u) & kPkRingMask], x1);
+  } else {
+    // the 128-bit string in four words, then shifted by sh into five
+    uint64_t lo = uint64_t(g[0]) | (uint64_t(g[1]) << b);
+    const uint64_t hi = uint64_t(g[2]) | (uint64_t(g[3]) << b);
+    uint64_t top;
+    if (b == 32u) {
+      top = hi;
+    } else {
+      lo |= hi << (2u * b);
+      top = hi >> (64u - 2u * b);
+    }
+    uint32_t s0 = uint32_t(lo), s1 = uint32_t(lo >> 32), s2 = uint32_t(top), s3 = uint32_t(top >> 32);
+    if (lane == 0) {  // drop the leading b zero bits (9 <= b <= 32)
+      const uint32_t q = b >> 5, r = b & 31u;  // q is 1 only for b == 32
+      if (q) { s0 = s1; s1 = s2; s2 = s3; s3 = 0u; }
+      if (r) {
+        s0 = __funnelshift_r(s0, s1, r);
+        s1 = __funnelshift_r(s1, s2, r);
+        s2 = __funnelshift_r(s2, s3, r);
+        s3 >>= r;
+      }
+    }
+    uint32_t x[5];
+    x[0] = s0 << sh;
+    x[1] = __funnelshift_l(s0, s1, sh);
+    x[2] = __funnelshift_l(s1, s2, sh);
+    x[3] = __funnelshift_l(s2, s3, sh);
+    x[4] = sh ? s3 >> (32u - sh) : 0u;
 #pragma unroll
-  for (int q = 0; q < kBlocksPerWarp; ++q) {
-    const uint32_t b = sm.width_of[warp * kBlocksPerWarp + q];
-    uint32_t* dst = reinterpret_cast<uint32_t*>(sg.payload + uint64_t(off16) * 16u);
-    for (uint32_t w = lane; w < 4u * b; w += 32) dst[w] = sm.words[warp][q][w];
-    off16 += b;
+    for (int k = 0; k < 5; ++k)
+      if (x[k]) atomicOr(&ring[(w0 + uint32_t(k)) & kPkRingMask], x[k]);
   }
-  __syncthreads();  // the shared words and widths are free again
 }
 
 template <bool MULTI>
-__global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm)
-    pack_kernel(const __grid_constant__ PackLaunch a) {
-  __shared__ PackSmem sm;
-  __shared__ uint32_t ticket;
-  __shared__ uint64_t sbeg[MULTI ? kSegCache : 1];
-  const int tid = threadIdx.x;
-  load_seg_begin<MULTI>(a, sbeg);
-  // Chunks are taken in ticket order, so every smaller ticket is held by a
-  // running CTA. A ticket is taken only when its chunk starts: a ticket held
-  // ahead would keep its aggregate from the look-backs behind it meanwhile.
-  for (;;) {
-    if (tid == 0) ticket = atomicAdd(a.counters + 0, 1u);
-    __syncthreads();
-    const uint64_t c = ticket;
-    if (c >= a.total_chunks) break;  // the same shared word for every thread
-    pack_chunk<MULTI>(a, sm, c, segment_of<MULTI>(a, sbeg, c));  // ends in a CTA barrier
-  }
+__device__ __forceinline__ void pk_compute(const PackLaunch& a, PkShared& sh, const uint8_t* stages,
+                                           uint32_t* ring, int tid, int lane, int warp) {
+  uint32_t posted = 0, ring_head = 0;
+  bool failed = false;
+  for (uint32_t it = 0;; ++it) {
+    const int s = int(it % kPkStages);
+    failed |= !enc::wait_or_flag(&sh.full[s], (it / kPkStages) & 1u, a);
+    const PkStageMeta m = sh.meta[s];
+    const bool live = m.mode != kPkEnd;
+    const bool bulk = m.mode == kPkBulk;
+    const uint32_t* sidx = reinterpret_cast<const uint32_t*>(stages + size_t(s) * kPkStageBytes);
+    const uint64_t chunk_first = m.lc * kPackChunk;
+    const int pc = int(it & 1u);
 
-  // the last CTA to finish rewinds the ticket and finish counters
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t done = atomicAdd(a.counters + 1, 1u);
-    if (done == gridDim.x - 1) {
-      atomicExch(a.counters + 0, 0u);
-      atomicExch(a.counters + 1, 0u);
+    // ---- gaps and widths of this warp's 4 blocks (gaps stay in registers)
+    uint32_t gap[kBlocksPerWarp][4];
+    uint32_t wb[kBlocksPerWarp];  // block widths (every lane)
+#pragma unroll
+    for (int q = 0; q < kBlocksPerWarp; ++q) {
+      const int lb = warp * kBlocksPerWarp + q;
+      const uint32_t b0 = uint32_t(lb) * kPackBlock;  // block start within the chunk
+      const uint32_t cnt = live && m.cnt > b0 ? (m.cnt - b0 < uint32_t(kPackBlock) ? m.cnt - b0 : kPackBlock) : 0u;
+      uint32_t v[4];
+      if (bulk) {
+        const uint4 x = reinterpret_cast<const uint4*>(sidx + b0)[lane];
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+          v[e] = j < cnt ? m.sg.idx[chunk_first + b0 + j] : 0u;
+        }
+      }
+      const uint32_t before = __shfl_up_sync(0xFFFFFFFFu, v[3], 1);  // lane - 1's last index
+      uint32_t mx = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+        const uint32_t prev = e == 0 ? before : v[e - 1];
+        gap[q][e] = (j >= 1 && j < cnt) ? v[e] - prev - 1u : 0u;
+        mx = max(mx, gap[q][e]);
+      }
+      mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+      wb[q] = cnt ? bit_width(mx) : 0u;
+      if (lane == 0) {
+        sh.wid[pc][lb] = wb[q];
+        if (cnt) {
+          const uint64_t gb = (chunk_first + b0) / kPackBlock;
+          m.sg.firsts[gb] = v[0];
+          m.sg.widths[gb] = uint8_t(wb[q]);
+        }
+      }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[s]);  // this warp is done with stage s
+    if (enc::compute_barrier_or(failed || !live)) break;
+
+    // ---- block offsets within the chunk (16-byte units) and the chunk's size
+    const uint32_t wl = sh.wid[pc][lane];
+    uint32_t incl = wl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const uint32_t agg = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const uint32_t my_off = __shfl_sync(0xFFFFFFFFu, incl - wl, warp * kBlocksPerWarp);
+    const uint64_t first = m.sg.chunk_begin;  // the look-back restarts at each segment
+    if (tid == 0)
+      st_relaxed_u64(a.status + m.c, make_status(m.c == first ? kFlagPrefix : kFlagAggregate, a.epoch, agg));
+
+    // ---- room: the parked slot must be free and the ring must hold the words
+    const int q = int(posted % kPkSlots);
+    if (posted >= uint32_t(kPkSlots))
+      failed |= !enc::wait_or_flag(&sh.slot_free[q], ((posted - kPkSlots) / kPkSlots) & 1u, a);
+    failed |= !enc::wait_ring_room<64>(&sh.ring_tail, ring_head, 4u * agg, kPkRing, a);
+
+    // ---- park: each block's 4 * width words
+    uint32_t off = my_off;
+#pragma unroll
+    for (int k = 0; k < kBlocksPerWarp; ++k) {
+      pk_block_words(gap[k], wb[k], ring, ring_head + 4u * off, lane);
+      off += wb[k];
+    }
+    if (tid == 0) {
+      PkParked pm;
+      pm.c = m.c;
+      pm.first = first;
+      pm.lc = m.lc;
+      pm.agg = agg;
+      pm.ring_start = ring_head;
+      pm.last = (chunk_first + m.cnt >= m.sg.count) ? 1u : 0u;
+      pm.chunk_off = m.sg.chunk_off;
+      pm.payload = m.sg.payload;
+      pm.payload_bytes = m.sg.payload_bytes;
+      sh.parked[q] = pm;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.agg_ready[q]);  // 8 arrivals: every warp's words are in
+    ++posted;
+    ring_head += 4u * agg;
+  }
+  // no more chunks: wait until every parked chunk is copied out, then send
+  // the look-back warp its end marker
+  for (uint32_t e = posted > uint32_t(kPkSlots) ? posted - kPkSlots : 0u; e < posted; ++e)
+    enc::wait_or_flag(&sh.slot_free[e % kPkSlots], (e / kPkSlots) & 1u, a);
+  enc::compute_barrier();
+  const int q = int(posted % kPkSlots);
+  if (tid == 0) {
+    PkParked pm{};
+    pm.last = 2u;
+    sh.parked[q] = pm;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sh.agg_ready[q]);
+}
+
+template <bool MULTI>
+__global__ void __launch_bounds__(kPkThreads, kPkCtasPerSm)
+    pack_kernel(const __grid_constant__ PackLaunch a) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ PkShared sh;
+  __shared__ uint32_t sbeg[MULTI ? kSegCache : 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~uintptr_t(127));
+  uint32_t* ring = reinterpret_cast<uint32_t*>(stages + size_t(kPkStages) * kPkStageBytes);
+  load_seg_begin<MULTI>(a, sbeg, kPkThreads);
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < kPkStages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], kPkWarps);
+      sh.meta[s] = PkStageMeta{};
+    }
+#pragma unroll
+    for (int q = 0; q < kPkSlots; ++q) {
+      mbar_init(&sh.agg_ready[q], kPkWarps);
+      mbar_init(&sh.slot_free[q], 1);
+      sh.parked[q] = PkParked{};
+      sh.parked[q].last = 2u;
+    }
+    sh.ring_tail = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();  // the last CTA-wide barrier: roles split below
+  if (warp < kPkWarps) {
+    pk_compute<MULTI>(a, sh, stages, ring, tid, lane, warp);
+  } else if (warp == kPkProducerWarp) {
+    if (lane == 0) pk_producer<MULTI>(a, sh, stages, sbeg);
+  } else if (warp == kPkLookbackWarp) {
+    pk_lookback(a, sh, ring, lane);
   }
 }
 
@@ -301,11 +567,21 @@ __global__ void __launch_bounds__(kPackThreads) unpack_kernel(const __grid_const
   unpack_chunk<MULTI>(sm, c, segment_of<MULTI>(a, nullptr, c));
 }
 
-// Persistent pack grid: kPackCtasPerSm CTAs per SM, or fewer chunks.
+// Persistent pack grid: as many CTAs as fit on the GPU, or fewer chunks.
+template <bool MULTI>
 unsigned pack_grid(uint64_t chunks) {
+  static int per_sm = [] {
+    cudaFuncSetAttribute(pack_kernel<MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         int(kPkDynSmem));
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, pack_kernel<MULTI>, kPkThreads,
+                                                      kPkDynSmem) != cudaSuccess || b < 1)
+      b = 1;
+    return b;
+  }();
   int dev = 0;
   cudaGetDevice(&dev);
-  const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(kPackCtasPerSm);
+  const uint64_t cap = uint64_t(sm_count(dev)) * uint64_t(per_sm);
   return unsigned(chunks < cap ? chunks : cap);
 }
 
@@ -327,7 +603,7 @@ cudaError_t launch_pack(const uint32_t* idx, uint64_t count, uint32_t* firsts, u
   a.epoch = epoch;
   a.wait_limit_ns = wait_limit_ns;
   if (a.total_chunks == 0) return cudaSuccess;
-  pack_kernel<false><<<pack_grid(a.total_chunks), kPackThreads, 0, stream>>>(a);
+  pack_kernel<false><<<pack_grid<false>(a.total_chunks), kPkThreads, kPkDynSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -344,7 +620,7 @@ cudaError_t launch_pack_multi(const PackSegment* segs, const uint64_t* chunk_beg
   a.counters = counters;
   a.epoch = epoch;
   a.wait_limit_ns = wait_limit_ns;
-  pack_kernel<true><<<pack_grid(total_chunks), kPackThreads, 0, stream>>>(a);
+  pack_kernel<true><<<pack_grid<true>(total_chunks), kPkThreads, kPkDynSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
