@@ -23,6 +23,8 @@
 // finding a chunk's segment costs no dependent global loads.
 // Unpack: one CTA per chunk; each warp extracts a block's gaps and rebuilds
 // its indices with a warp scan.
+#include <type_traits>
+
 #include "encode_common.cuh"
 
 namespace pulse {
@@ -85,8 +87,8 @@ __device__ __forceinline__ uint32_t bit_width(uint32_t v) { return v ? 32u - __c
 
 // ----------------------------------------------------------------- pack
 // Persistent, warp-specialized CTA (the shape of the BF16 encode kernel):
-//  * producer warp (one thread): takes chunk tickets one fill ahead and
-//    stages each chunk's 4096 indices (16 KB) in a kPkStages-deep ring with a
+//  * producer warp (one thread): takes a chunk ticket whenever a stage is
+//    free and stages the chunk's 4096 indices (16 KB) in a kPkStages-deep ring with a
 //    bulk copy (plain loads by the compute threads for a segment's last,
 //    partial chunk or an index array that is not 16-byte aligned);
 //  * 8 compute warps (4 blocks each): form the gaps, take each block's width,
@@ -160,14 +162,15 @@ __device__ __forceinline__ void pk_producer(const PackLaunch& a, PkShared& sh, u
                                             const uint32_t* sbeg) {
   const uint64_t pol_stream = l2_policy_evict_first();
   uint32_t fills_done = 0;
-  uint64_t ticket = atomicAdd(a.counters + 0, 1u);
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kPkStages);
-    const bool end = ticket >= a.total_chunks;
-    const uint64_t next = end ? ticket : uint64_t(atomicAdd(a.counters + 0, 1u));
     if (it >= uint32_t(kPkStages) &&
         !enc::helper_wait(&sh.empty[s], ((it / kPkStages) - 1) & 1u, a))
       break;
+    // the ticket only once its stage is free: a chunk's count is published
+    // soon after its ticket, so look-backs behind it wait less
+    const uint64_t ticket = atomicAdd(a.counters + 0, 1u);
+    const bool end = ticket >= a.total_chunks;
     fills_done = it + 1;
     PkStageMeta m{};
     m.c = ticket;
@@ -192,7 +195,6 @@ __device__ __forceinline__ void pk_producer(const PackLaunch& a, PkShared& sh, u
       sh.meta[s] = m;
       mbar_arrive(&sh.full[s]);
     }
-    ticket = next;
   }
   // no bulk copy may still be in flight when the CTA exits
   for (uint32_t f = fills_done > uint32_t(kPkStages) ? fills_done - kPkStages : 0u; f < fills_done; ++f)
@@ -346,45 +348,51 @@ __device__ __forceinline__ void pk_compute(const PackLaunch& a, PkShared& sh, co
     const uint64_t chunk_first = m.lc * kPackChunk;
     const int pc = int(it & 1u);
 
-    // ---- gaps and widths of this warp's 4 blocks (gaps stay in registers)
+    // ---- gaps and widths of this warp's 4 blocks (gaps stay in registers);
+    // compiled apart for a full staged chunk, where every block has 128 entries
     uint32_t gap[kBlocksPerWarp][4];
     uint32_t wb[kBlocksPerWarp];  // block widths (every lane)
+    auto widths = [&](auto full_tag) {
+      constexpr bool kFull = decltype(full_tag)::value;
 #pragma unroll
-    for (int q = 0; q < kBlocksPerWarp; ++q) {
-      const int lb = warp * kBlocksPerWarp + q;
-      const uint32_t b0 = uint32_t(lb) * kPackBlock;  // block start within the chunk
-      const uint32_t cnt = live && m.cnt > b0 ? (m.cnt - b0 < uint32_t(kPackBlock) ? m.cnt - b0 : kPackBlock) : 0u;
-      uint32_t v[4];
-      if (bulk) {
-        const uint4 x = reinterpret_cast<const uint4*>(sidx + b0)[lane];
-        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-      } else {
+      for (int q = 0; q < kBlocksPerWarp; ++q) {
+        const int lb = warp * kBlocksPerWarp + q;
+        const uint32_t b0 = uint32_t(lb) * kPackBlock;  // block start within the chunk
+        const uint32_t cnt = kFull ? uint32_t(kPackBlock)
+                                   : (live && m.cnt > b0 ? (m.cnt - b0 < uint32_t(kPackBlock) ? m.cnt - b0 : kPackBlock) : 0u);
+        uint32_t v[4];
+        if constexpr (kFull) {
+          const uint4 x = reinterpret_cast<const uint4*>(sidx + b0)[lane];
+          v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+            v[e] = j < cnt ? m.sg.idx[chunk_first + b0 + j] : 0u;
+          }
+        }
+        const uint32_t before = __shfl_up_sync(0xFFFFFFFFu, v[3], 1);  // lane - 1's last index
+        uint32_t mx = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
-          v[e] = j < cnt ? m.sg.idx[chunk_first + b0 + j] : 0u;
+          const uint32_t prev = e == 0 ? before : v[e - 1];
+          gap[q][e] = (j >= 1 && j < cnt) ? v[e] - prev - 1u : 0u;
+          mx = max(mx, gap[q][e]);
+        }
+        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+        wb[q] = cnt ? bit_width(mx) : 0u;
+        if (lane == 0) {
+          sh.wid[pc][lb] = wb[q];
+          if (cnt) {
+            const uint64_t gb = (chunk_first + b0) / kPackBlock;
+            m.sg.firsts[gb] = v[0];
+            m.sg.widths[gb] = uint8_t(wb[q]);
+          }
         }
       }
-      const uint32_t before = __shfl_up_sync(0xFFFFFFFFu, v[3], 1);  // lane - 1's last index
-      uint32_t mx = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
-        const uint32_t prev = e == 0 ? before : v[e - 1];
-        gap[q][e] = (j >= 1 && j < cnt) ? v[e] - prev - 1u : 0u;
-        mx = max(mx, gap[q][e]);
-      }
-      mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-      wb[q] = cnt ? bit_width(mx) : 0u;
-      if (lane == 0) {
-        sh.wid[pc][lb] = wb[q];
-        if (cnt) {
-          const uint64_t gb = (chunk_first + b0) / kPackBlock;
-          m.sg.firsts[gb] = v[0];
-          m.sg.widths[gb] = uint8_t(wb[q]);
-        }
-      }
-    }
+    };
+    if (bulk) widths(std::true_type{}); else widths(std::false_type{});
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);  // this warp is done with stage s
     if (enc::compute_barrier_or(failed || !live)) break;
