@@ -495,11 +495,17 @@ __global__ void __launch_bounds__(kPkThreads, kPkCtasPerSm)
   }
 }
 
-struct UnpackSmem {
-  uint32_t words[kPackWarps][kPackBlock + 1];
+struct __align__(16) UnpackSmem {
+  // every block's words, then 4 zero words (two-word reads past the end)
+  uint32_t words[kPackWarps][kBlocksPerWarp][kPackBlock + 4];
 };
 
-// Rebuild the indices of chunk c (of segment sg).
+// Rebuild the indices of chunk c (of segment sg). Each warp first copies its
+// 4 blocks' words to shared memory (16-byte loads when the payload is 16-byte
+// aligned), then per block: lane l takes the gaps of entries 4l .. 4l+3 (bit
+// slots 4l-1 .. 4l+2; for widths up to 8 all four come from one 64-bit window
+// of two words), and a warp scan of gap + 1 from the block's first index
+// gives the indices (one 16-byte store per lane for a full, aligned block).
 template <bool MULTI>
 __device__ __forceinline__ void unpack_chunk(UnpackSmem& sm, uint64_t c, const PackSegment& sg) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -521,33 +527,72 @@ __device__ __forceinline__ void unpack_chunk(UnpackSmem& sm, uint64_t c, const P
     if (lane >= o) incl += v;
   }
   const uint64_t base_off = sg.chunk_off[lc];
+  const bool vec_in = (reinterpret_cast<uintptr_t>(payload) & 15u) == 0;
+  uint32_t bw[kBlocksPerWarp], first_idx[kBlocksPerWarp];
+  // ---- every block's words into shared memory
 #pragma unroll
   for (int q = 0; q < kBlocksPerWarp; ++q) {
     const int lb = warp * kBlocksPerWarp + q;
     const uint32_t b = __shfl_sync(0xFFFFFFFFu, wl, lb);
     const uint32_t pre = __shfl_sync(0xFFFFFFFFu, incl - wl, lb);
     const uint64_t start = chunk_first + uint64_t(lb) * kPackBlock;
+    bw[q] = b;
+    first_idx[q] = start < count ? firsts[start / kPackBlock] : 0u;
+    uint32_t* dst = sm.words[warp][q];
+    const uint8_t* src = payload + base_off + uint64_t(pre) * 16u;
+    if (start < count) {
+      if (vec_in) {
+        if (uint32_t(lane) < b)
+          reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(src)[lane];
+      } else {
+        for (uint32_t w = lane; w < 4u * b; w += 32)
+          dst[w] = reinterpret_cast<const uint32_t*>(src)[w];
+      }
+    }
+    if (lane < 4) dst[4u * b + uint32_t(lane)] = 0u;
+  }
+  __syncwarp();
+  // ---- gaps and indices, block by block
+  const bool vec_out = (reinterpret_cast<uintptr_t>(idx_out) & 15u) == 0;
+#pragma unroll
+  for (int q = 0; q < kBlocksPerWarp; ++q) {
+    const int lb = warp * kBlocksPerWarp + q;
+    const uint64_t start = chunk_first + uint64_t(lb) * kPackBlock;
     if (start >= count) break;  // warp-uniform
     const uint32_t cnt = uint32_t(count - start < kPackBlock ? count - start : kPackBlock);
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(payload + base_off + uint64_t(pre) * 16u);
-    for (uint32_t w = lane; w < 4u * b; w += 32) sm.words[warp][w] = src[w];
-    if (lane == 0) sm.words[warp][4u * b] = 0u;  // a zero word past the end for two-word reads
-    __syncwarp();
+    const uint32_t b = bw[q];
+    const uint32_t* words = sm.words[warp][q];
+    const uint32_t mask = b == 32u ? 0xFFFFFFFFu : (1u << b) - 1u;
     // x_j = gap_j + 1 for j >= 1, x_0 = 0; idx_j = first + inclusive sum of x
     uint32_t x[4];
     uint32_t sum = 0;
+    if (b <= 8u) {
+      // the lane's four slots: bits (4l-1)b .. (4l+3)b (lane 0: its three from bit 0)
+      const uint32_t P = lane ? (4u * uint32_t(lane) - 1u) * b : 0u;
+      const uint64_t two = uint64_t(words[P >> 5]) | (uint64_t(words[(P >> 5) + 1]) << 32);
+      const uint32_t window = uint32_t(two >> (P & 31u));
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
-      uint32_t g = 0;
-      if (j >= 1 && j < cnt && b != 0u) {
-        const uint32_t bit = (j - 1u) * b;
-        const uint32_t w0 = bit >> 5, sh = bit & 31u;
-        const uint64_t two = uint64_t(sm.words[warp][w0]) | (uint64_t(sm.words[warp][w0 + 1]) << 32);
-        g = uint32_t((two >> sh) & ((b == 32u) ? 0xFFFFFFFFull : ((1ull << b) - 1ull)));
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+        const int k = lane ? e : e - 1;  // slot within the lane's window
+        const uint32_t g = k < 0 ? 0u : (window >> (uint32_t(k) * b)) & mask;
+        x[e] = (j >= 1 && j < cnt) ? g + 1u : 0u;
+        sum += x[e];
       }
-      x[e] = (j >= 1 && j < cnt) ? g + 1u : 0u;
-      sum += x[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+        uint32_t g = 0;
+        if (j >= 1 && j < cnt) {
+          const uint32_t bit = (j - 1u) * b;
+          const uint32_t w0 = bit >> 5, sh = bit & 31u;
+          const uint64_t two = uint64_t(words[w0]) | (uint64_t(words[w0 + 1]) << 32);
+          g = uint32_t(two >> sh) & mask;
+        }
+        x[e] = (j >= 1 && j < cnt) ? g + 1u : 0u;
+        sum += x[e];
+      }
     }
     uint32_t run = sum;
 #pragma unroll
@@ -555,14 +600,22 @@ __device__ __forceinline__ void unpack_chunk(UnpackSmem& sm, uint64_t c, const P
       const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, run, o);
       if (lane >= o) run += v;
     }
-    uint32_t cur = firsts[start / kPackBlock] + (run - sum);
+    uint32_t cur = first_idx[q] + (run - sum);
+    uint32_t out[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
       cur += x[e];
-      if (j < cnt) idx_out[start + j] = cur;
+      out[e] = cur;
     }
-    __syncwarp();
+    if (vec_out && cnt == uint32_t(kPackBlock)) {
+      reinterpret_cast<uint4*>(idx_out + start)[lane] = make_uint4(out[0], out[1], out[2], out[3]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t j = uint32_t(lane) * 4u + uint32_t(e);
+        if (j < cnt) idx_out[start + j] = out[e];
+      }
+    }
   }
 }
 
