@@ -56,6 +56,10 @@ constexpr int kSegCache = 1024;  // segments whose chunk ranges a CTA keeps in s
 // Status words per lane and look-back round trip (32 predecessors per round
 // trip with one word per lane).
 constexpr int kPackLookback = PULSE_PACK_LOOKBACK;
+#ifndef PULSE_PK_LB_SLEEP
+#define PULSE_PK_LB_SLEEP 32
+#endif
+constexpr unsigned kPkLookbackSleepNs = PULSE_PK_LB_SLEEP;  // look-back poll pause
 
 // Copy the chunk ranges into shared memory when they fit (multi-segment).
 template <bool MULTI>
@@ -257,7 +261,7 @@ __device__ __forceinline__ void pk_lookback(const PackLaunch& a, PkShared& sh, c
       const uint32_t ii = i + uint32_t(b);
       const int q = int(ii % kPkSlots);
       const PkParked pm = sh.parked[q];
-      const uint32_t prefix = enc::resolve_prefix<enc::StatusEpoch, PackLaunch, 32, kPackLookback>(
+      const uint32_t prefix = enc::resolve_prefix<enc::StatusEpoch, PackLaunch, kPkLookbackSleepNs, kPackLookback>(
           a, pm.c, pm.first, pm.agg, lane, win[b]);
       if (lane == 0) {
         pm.chunk_off[pm.lc] = uint64_t(prefix) * 16u;
