@@ -177,3 +177,14 @@ def test_segments_spanning_several_scan_tiles():
     segs = [_random_idx(rng, 1024 * 4096 + 1, 5), _random_idx(rng, 300, 1000),
             _random_idx(rng, big, 0)]
     _check_job(segs, dev)
+
+
+def test_pack_job_more_segments_than_the_shared_table():
+    """1100 segments in one call: past the pack kernel's shared copy of the
+    segments' chunk ranges (1024 entries), each chunk's segment is found by
+    a binary search of the global table."""
+    dev = _dev()
+    rng = np.random.default_rng(1100)
+    ks = [int(k) for k in rng.choice([0, 1, 127, 128, 129, 300, 4096, 4097, 9000], size=1100)]
+    segs = [_random_idx(rng, k, int(rng.choice([0, 11, 1000]))) for k in ks]
+    _check_job(segs, dev)
