@@ -92,13 +92,15 @@ __device__ __forceinline__ uint32_t bit_width(uint32_t v) { return v ? 32u - __c
 // ----------------------------------------------------------------- pack
 // Persistent, warp-specialized CTA (the shape of the BF16 encode kernel):
 //  * producer warp (one thread): takes a chunk ticket whenever a stage is
-//    free and stages the chunk's 4096 indices (16 KB) in a kPkStages-deep ring with a
-//    bulk copy (plain loads by the compute threads for a segment's last,
-//    partial chunk or an index array that is not 16-byte aligned);
+//    free and stages the chunk's 4096 indices (16 KB) in a kPkStages-deep
+//    ring with a bulk copy (plain loads by the compute threads for a
+//    segment's last, partial chunk or an index array that is not 16-byte
+//    aligned);
 //  * 8 compute warps (4 blocks each): form the gaps, take each block's width,
 //    write firsts and widths, publish the chunk's size (16-byte units) in its
 //    status word, and park the chunk's packed words in a shared-memory word
-//    ring (gap bits OR-ed into zeroed words);
+//    ring (each lane ORs its four gaps, as one bit string, into the block's
+//    zeroed words);
 //  * one look-back warp: resolves each parked chunk's payload offset with the
 //    decoupled look-back, writes chunk_off (and the segment's payload size
 //    after its last chunk), copies the words to the payload with 16-byte
@@ -123,6 +125,7 @@ constexpr int kPkSlots = 8;                         // parked chunks per CTA
 #endif
 constexpr uint32_t kPkRing = PULSE_PK_RING;         // parked payload words per CTA
 constexpr uint32_t kPkRingMask = kPkRing - 1u;
+static_assert((kPkRing & (kPkRing - 1u)) == 0u, "the word ring is a power of two");
 constexpr uint32_t kPkStageBytes = kPackChunk * 4;  // 16 KB of indices
 constexpr int kPkCtasPerSm = PULSE_PK_CTAS;
 static_assert(kPkCompute == kEncThreads, "the compute warps use the encode's named barrier");
