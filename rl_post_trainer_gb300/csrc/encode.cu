@@ -66,7 +66,8 @@ struct ParkedMeta {
   uint32_t last;    // 1: last tile of its tensor; 2: no more tiles for this look-back warp
   uint64_t first;   // first global tile of the tensor
   uint64_t n;       // elements of the tensor
-  uint32_t ring_start;
+  uint32_t ring_start;  // ring slot of the tile's first entry
+  uint32_t ring_end;    // entries parked by the CTA up to the tile's last
   uint32_t base;    // first element of the tile within its tensor
   uint32_t* idx;
   uint16_t* val;
@@ -191,7 +192,7 @@ __device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix,
   if (head > agg) head = agg;
   const uint32_t body = vec ? ((agg - head) & ~3u) : 0u;
   for (uint32_t k = uint32_t(lane); k < head; k += 32) {
-    const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
+    const uint32_t ent = ring[ring_slot(pm.ring_start + k)];
     const uint64_t pos = uint64_t(prefix) + k;
     if (pos < pm.n) {
       pm.idx[pos] = pm.base + (ent & 0xFFFFu);
@@ -201,7 +202,7 @@ __device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix,
   for (uint32_t k = head + uint32_t(lane) * 4u; k < head + body; k += 128u) {
     uint32_t e[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) e[q] = ring[(pm.ring_start + k + uint32_t(q)) & kRingMask];
+    for (int q = 0; q < 4; ++q) e[q] = ring[ring_slot(pm.ring_start + k + uint32_t(q))];
     const uint64_t pos = uint64_t(prefix) + k;  // a multiple of 4
     *reinterpret_cast<uint4*>(pm.idx + pos) =
         make_uint4(pm.base + (e[0] & 0xFFFFu), pm.base + (e[1] & 0xFFFFu),
@@ -210,7 +211,7 @@ __device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix,
         make_uint2((e[0] >> 16) | (e[1] & 0xFFFF0000u), (e[2] >> 16) | (e[3] & 0xFFFF0000u));
   }
   for (uint32_t k = head + body + uint32_t(lane); k < agg; k += 32) {
-    const uint32_t ent = ring[(pm.ring_start + k) & kRingMask];
+    const uint32_t ent = ring[ring_slot(pm.ring_start + k)];
     const uint64_t pos = uint64_t(prefix) + k;
     if (pos < pm.n) {
       pm.idx[pos] = pm.base + (ent & 0xFFFFu);
@@ -265,7 +266,7 @@ __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShare
       if (lane == 0) {
         // tiles are copied out in order: everything before this tile's end is free
         __threadfence_block();
-        *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) = pm.ring_start + pm.agg;
+        *reinterpret_cast<volatile uint32_t*>(&sh.ring_tail) = pm.ring_end;
         mbar_arrive(&sh.slot_free[q]);
       }
     }
@@ -305,7 +306,8 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
                                              uint8_t* stages, uint32_t* ring, int tid, int lane,
                                              int warp) {
   // uniform across the compute threads
-  uint32_t posted = 0, ring_head = 0;
+  uint32_t posted = 0, ring_head = 0;  // ring_head: entries parked so far
+  uint32_t ring_pos = 0;               // its ring slot
   bool failed = false;  // this thread saw a wait give up
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kEncStages);
@@ -442,13 +444,13 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
       uint32_t f = (flags >> (j * 4)) & 0xFu;
       if (f == 0u) continue;
       const uint32_t li = uint32_t(j * kEncThreads + tid) * 4u;
-      uint32_t r = ring_head + round_off[j];
+      uint32_t r = ring_pos + round_off[j];
       do {
         const uint32_t e = uint32_t(__ffs(f)) - 1u;
         f &= f - 1u;
         const uint32_t word = (e & 2u) ? nb[j][1] : nb[j][0];
         const uint32_t value = (e & 1u) ? (word >> 16) : (word & 0xFFFFu);
-        ring[r & kRingMask] = (li + e) | (value << 16);
+        ring[ring_slot(r)] = (li + e) | (value << 16);
         ++r;
       } while (f != 0u);
     }
@@ -460,7 +462,8 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
       pm.last = (base + len == m.n) ? 1u : 0u;
       pm.first = m.first;
       pm.n = m.n;
-      pm.ring_start = ring_head;
+      pm.ring_start = ring_pos;
+      pm.ring_end = ring_head + agg;
       pm.base = uint32_t(base);
       pm.idx = m.idx;
       pm.val = m.val;
@@ -470,6 +473,7 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
     if (lane == 0) mbar_arrive(&sh.agg_ready[q]);  // 8 arrivals: every warp's entries are in
     ++posted;
     ring_head += agg;
+    ring_pos = ring_slot(ring_pos + agg);
   }
   // no more tiles (the compute warps left the loop together): wait until
   // every parked tile is copied out, then send each look-back warp its end

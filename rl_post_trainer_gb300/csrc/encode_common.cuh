@@ -28,7 +28,12 @@ constexpr int kPendSlots =
     ((kEncParked > kEncLookbackWarps ? kEncParked : kEncLookbackWarps) + kEncLookbackWarps - 1) /
     kEncLookbackWarps * kEncLookbackWarps;
 constexpr int kComputeBarrier = 1;  // named barrier of the compute warps
-constexpr uint32_t kRingMask = uint32_t(kEncRing) - 1u;
+// Ring slot of position r < 2 * kEncRing (a ring start below kEncRing plus
+// at most one tile): a mask for a power-of-two ring, else one subtraction.
+__device__ __forceinline__ uint32_t ring_slot(uint32_t r) {
+  if constexpr ((kEncRing & (kEncRing - 1)) == 0) return r & uint32_t(kEncRing - 1);
+  else return r >= uint32_t(kEncRing) ? r - uint32_t(kEncRing) : r;
+}
 
 enum : uint32_t { kModeEnd = 0, kModeBulk = 1, kModeGeneric = 2 };
 
