@@ -29,6 +29,11 @@
 namespace pulse {
 namespace {
 
+// Parked tiles per CTA and tiles resolved per look-back round trip (the
+// values this kernel was tuned with).
+constexpr int kCmpSlots = 8;
+constexpr int kCmpBatch = 4;
+
 #ifndef PULSE_CMP_PER_THREAD
 #define PULSE_CMP_PER_THREAD 8
 #endif
@@ -158,10 +163,10 @@ struct CmpParked {
 struct __align__(16) CmpShared {
   uint64_t full[kCmpStages];
   uint64_t empty[kCmpStages];
-  uint64_t agg_ready[enc::kPendSlots];
-  uint64_t slot_free[enc::kPendSlots];
+  uint64_t agg_ready[kCmpSlots];
+  uint64_t slot_free[kCmpSlots];
   CmpStageMeta meta[kCmpStages];
-  CmpParked parked[enc::kPendSlots];
+  CmpParked parked[kCmpSlots];
   uint32_t warp_tot[2][kCmpWarps];
   uint32_t ring_tail;
 };
@@ -376,26 +381,26 @@ __device__ __forceinline__ void cmp_lookback(const CmpLaunch& a, CmpShared& sh,
                                              int lane) {
   using namespace enc;
   for (uint32_t i = 0;;) {
-    const bool ok = helper_wait(&sh.agg_ready[i % kPendSlots], (i / kPendSlots) & 1u, a);
+    const bool ok = helper_wait(&sh.agg_ready[i % kCmpSlots], (i / kCmpSlots) & 1u, a);
     if (!__all_sync(0xFFFFFFFFu, ok)) break;
     int more = 0;
     if (lane == 0) {
-      for (int b = 1; b < kLookbackBatch; ++b) {
+      for (int b = 1; b < kCmpBatch; ++b) {
         const uint32_t ii = i + uint32_t(b);
-        if (!mbar_test_wait(&sh.agg_ready[ii % kPendSlots], (ii / kPendSlots) & 1u)) break;
+        if (!mbar_test_wait(&sh.agg_ready[ii % kCmpSlots], (ii / kCmpSlots) & 1u)) break;
         more = b;
       }
     }
     more = __shfl_sync(0xFFFFFFFFu, more, 0);
     int nb = 0;
     bool end = false;
-    uint64_t win[kLookbackBatch][kLookbackPerLane];
+    uint64_t win[kCmpBatch][kLookbackPerLane];
 #pragma unroll
-    for (int b = 0; b < kLookbackBatch; ++b) {
+    for (int b = 0; b < kCmpBatch; ++b) {
       if (b > more || end) continue;
       const uint32_t ii = i + uint32_t(b);
-      const int q = int(ii % kPendSlots);
-      if (b > 0) mbar_test_wait(&sh.agg_ready[q], (ii / kPendSlots) & 1u);  // acquire for every lane
+      const int q = int(ii % kCmpSlots);
+      if (b > 0) mbar_test_wait(&sh.agg_ready[q], (ii / kCmpSlots) & 1u);  // acquire for every lane
       const CmpParked& pm = sh.parked[q];
       if (pm.last == 2u) {
         end = true;
@@ -405,10 +410,10 @@ __device__ __forceinline__ void cmp_lookback(const CmpLaunch& a, CmpShared& sh,
       nb = b + 1;
     }
 #pragma unroll
-    for (int b = 0; b < kLookbackBatch; ++b) {
+    for (int b = 0; b < kCmpBatch; ++b) {
       if (b >= nb) continue;
       const uint32_t ii = i + uint32_t(b);
-      const int q = int(ii % kPendSlots);
+      const int q = int(ii % kCmpSlots);
       const CmpParked pm = sh.parked[q];
       const uint32_t prefix = resolve_prefix<StatusEpoch>(a, pm.tile, pm.first, pm.agg, lane, win[b]);
       if (lane == 0 && pm.last == 1u) a.counts_out[MULTI ? pm.seg : 0] = uint64_t(prefix) + pm.agg;
@@ -541,9 +546,9 @@ __device__ __forceinline__ void cmp_compute(const CmpLaunch& a, CmpShared& sh, u
                      make_status(uint64_t(m.tile) == m.first ? kFlagPrefix : kFlagAggregate, a.epoch, agg));
 
     // ---- room: the parked slot must be free and the ring must hold agg more
-    const int q = int(posted % kPendSlots);
-    if (posted >= uint32_t(kPendSlots))
-      failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kPendSlots) / kPendSlots) & 1u, a);
+    const int q = int(posted % kCmpSlots);
+    if (posted >= uint32_t(kCmpSlots))
+      failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kCmpSlots) / kCmpSlots) & 1u, a);
     failed |= !wait_ring_room<64>(&sh.ring_tail, ring_head, agg, kCmpRing, a);
 
     // ---- park the kept entries
@@ -574,10 +579,10 @@ __device__ __forceinline__ void cmp_compute(const CmpLaunch& a, CmpShared& sh, u
     ++posted;
     ring_head += agg;
   }
-  for (uint32_t e = posted > uint32_t(kPendSlots) ? posted - kPendSlots : 0u; e < posted; ++e)
-    wait_or_flag(&sh.slot_free[e % kPendSlots], (e / kPendSlots) & 1u, a);
+  for (uint32_t e = posted > uint32_t(kCmpSlots) ? posted - kCmpSlots : 0u; e < posted; ++e)
+    wait_or_flag(&sh.slot_free[e % kCmpSlots], (e / kCmpSlots) & 1u, a);
   compute_barrier();
-  const int q = int(posted % kPendSlots);
+  const int q = int(posted % kCmpSlots);
   if (tid == 0) {
     CmpParked pm{};
     pm.last = 2u;
@@ -607,7 +612,7 @@ __global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
       sh.meta[s].mode = enc::kModeEnd;
     }
 #pragma unroll
-    for (int q = 0; q < enc::kPendSlots; ++q) {
+    for (int q = 0; q < kCmpSlots; ++q) {
       mbar_init(&sh.agg_ready[q], kCmpWarps);
       mbar_init(&sh.slot_free[q], 1);
       sh.parked[q] = CmpParked{};

@@ -30,6 +30,11 @@ namespace {
 
 using namespace enc;
 
+// Parked chunks per CTA and chunks resolved per look-back round trip: 8 and 4
+// (16 and 2, the other kernels' choice, measured 0.4 % slower here).
+constexpr int kCcSlots = 8;
+constexpr int kCcBatch = 4;
+
 constexpr int kCcChunk = kApplyChunk;        // positions per chunk
 constexpr int kCcWords = kCcChunk / 32;      // bitmap words, one per compute thread
 static_assert(kCcWords == kEncThreads, "one bitmap word per compute thread");
@@ -84,10 +89,10 @@ struct CcParked {
 struct __align__(16) CcShared {
   uint64_t full[kCcStages];
   uint64_t empty[kCcStages];
-  uint64_t agg_ready[kPendSlots];
-  uint64_t slot_free[kPendSlots];
+  uint64_t agg_ready[kCcSlots];
+  uint64_t slot_free[kCcSlots];
   CcMeta meta[kCcStages];
-  CcParked parked[kPendSlots];
+  CcParked parked[kCcSlots];
   uint32_t warp_tot[2][kWarps];
   uint32_t ring_tail;
   uint32_t bits[kCcWords];
@@ -219,27 +224,27 @@ __device__ __forceinline__ void cc_copy_out(const CcParked& pm, uint32_t prefix,
 
 __device__ __forceinline__ void cc_lookback(const CcArgs& a, CcShared& sh, int lane) {
   for (uint32_t i = 0;;) {
-    const bool ok = helper_wait(&sh.agg_ready[i % kPendSlots], (i / kPendSlots) & 1u, a);
+    const bool ok = helper_wait(&sh.agg_ready[i % kCcSlots], (i / kCcSlots) & 1u, a);
     if (!__all_sync(0xFFFFFFFFu, ok)) break;
     // how many more chunks are already parked (lane 0 decides)
     int more = 0;
     if (lane == 0) {
-      for (int b = 1; b < kLookbackBatch; ++b) {
+      for (int b = 1; b < kCcBatch; ++b) {
         const uint32_t ii = i + uint32_t(b);
-        if (!mbar_test_wait(&sh.agg_ready[ii % kPendSlots], (ii / kPendSlots) & 1u)) break;
+        if (!mbar_test_wait(&sh.agg_ready[ii % kCcSlots], (ii / kCcSlots) & 1u)) break;
         more = b;
       }
     }
     more = __shfl_sync(0xFFFFFFFFu, more, 0);
     int nb = 0;
     bool end = false;
-    uint64_t win[kLookbackBatch][kLookbackPerLane];
+    uint64_t win[kCcBatch][kLookbackPerLane];
 #pragma unroll
-    for (int b = 0; b < kLookbackBatch; ++b) {
+    for (int b = 0; b < kCcBatch; ++b) {
       if (b > more || end) continue;
       const uint32_t ii = i + uint32_t(b);
-      const int q = int(ii % kPendSlots);
-      if (b > 0) mbar_test_wait(&sh.agg_ready[q], (ii / kPendSlots) & 1u);  // acquire for every lane
+      const int q = int(ii % kCcSlots);
+      if (b > 0) mbar_test_wait(&sh.agg_ready[q], (ii / kCcSlots) & 1u);  // acquire for every lane
       const CcParked& pm = sh.parked[q];
       if (pm.last == 2u) {
         end = true;
@@ -249,10 +254,10 @@ __device__ __forceinline__ void cc_lookback(const CcArgs& a, CcShared& sh, int l
       nb = b + 1;
     }
 #pragma unroll
-    for (int b = 0; b < kLookbackBatch; ++b) {
+    for (int b = 0; b < kCcBatch; ++b) {
       if (b >= nb) continue;
       const uint32_t ii = i + uint32_t(b);
-      const int q = int(ii % kPendSlots);
+      const int q = int(ii % kCcSlots);
       const CcParked pm = sh.parked[q];
       const uint32_t prefix = resolve_prefix<StatusEpoch, CcArgs, kCcLookbackSleepNs>(
           a, pm.tile, pm.first, pm.agg, lane, win[b]);
@@ -373,9 +378,9 @@ __device__ __forceinline__ void cc_compute(const CcArgs& a, CcShared& sh, int ti
                                                a.epoch, agg));
 
     // ---- room: the parked slot must be free and the ring must hold agg more
-    const int q = int(posted % kPendSlots);
-    if (posted >= uint32_t(kPendSlots))
-      failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kPendSlots) / kPendSlots) & 1u, a);
+    const int q = int(posted % kCcSlots);
+    if (posted >= uint32_t(kCcSlots))
+      failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kCcSlots) / kCcSlots) & 1u, a);
     failed |= !wait_ring_room<256>(&sh.ring_tail, ring_head, agg, uint32_t(kCcRing), a);
 
     // ---- park the chunk's entries in ascending order
@@ -408,10 +413,10 @@ __device__ __forceinline__ void cc_compute(const CcArgs& a, CcShared& sh, int ti
     // the next chunk writes the image only after the barrier at the top of
     // the loop, which every thread reaches after parking this one
   }
-  for (uint32_t e = posted > uint32_t(kPendSlots) ? posted - kPendSlots : 0u; e < posted; ++e)
-    wait_or_flag(&sh.slot_free[e % kPendSlots], (e / kPendSlots) & 1u, a);
+  for (uint32_t e = posted > uint32_t(kCcSlots) ? posted - kCcSlots : 0u; e < posted; ++e)
+    wait_or_flag(&sh.slot_free[e % kCcSlots], (e / kCcSlots) & 1u, a);
   compute_barrier();
-  const int q = int(posted % kPendSlots);
+  const int q = int(posted % kCcSlots);
   if (tid == 0) {
     CcParked pm{};
     pm.last = 2u;
@@ -438,7 +443,7 @@ __global__ void __launch_bounds__(kEncBlockThreads, kCcMinBlocks)
       sh.meta[s].mode = kModeEnd;
     }
 #pragma unroll
-    for (int q = 0; q < kPendSlots; ++q) {
+    for (int q = 0; q < kCcSlots; ++q) {
       mbar_init(&sh.agg_ready[q], kWarps);
       mbar_init(&sh.slot_free[q], 1);
       sh.parked[q].last = 2u;

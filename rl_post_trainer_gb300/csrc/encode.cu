@@ -26,7 +26,7 @@
 //    round trip, publishes the inclusive prefix, copies the parked entries to
 //    the patch with contiguous coalesced stores, and frees the slot. An L2
 //    round trip to the status words costs microseconds while HBM is
-//    saturated, so up to kSlots tiles per CTA wait in the ring while the
+//    saturated, so up to kPendSlots tiles per CTA wait in the ring while the
 //    compute warps stream on.
 // Every wait is bounded; a wait that gives up records PULSE_ERR_TIMEOUT and
 // the kernel still finishes with all writes inside the caller's buffers.
@@ -36,20 +36,6 @@ namespace pulse {
 namespace {
 
 using namespace enc;
-
-// Parked tiles per CTA and tiles resolved per look-back round trip. The BF16
-// encode keeps more tiles parked than the other kernels built on the same
-// pipeline and resolves them two at a time: 16 / 2 measured 0.3 % faster on
-// the 8.03B step at 8 % density and 1.6 % at 1.2 % than 8 / 4.
-#ifndef PULSE_BF16_PARKED
-#define PULSE_BF16_PARKED 16
-#endif
-#ifndef PULSE_BF16_LB_BATCH
-#define PULSE_BF16_LB_BATCH 2
-#endif
-constexpr int kSlots = PULSE_BF16_PARKED;
-constexpr int kBatch = PULSE_BF16_LB_BATCH;
-static_assert(kEncLookbackWarps == 1 && kSlots >= kBatch, "one look-back warp takes up to kBatch parked tiles");
 
 constexpr uint32_t kStageMasterBytes = kEncTile * 4;
 constexpr uint32_t kStagePrevBytes = kEncTile * 2;
@@ -90,10 +76,10 @@ struct ParkedMeta {
 struct __align__(16) EncodeShared {
   uint64_t full[kEncStages];       // producer -> compute: stage filled
   uint64_t empty[kEncStages];      // compute -> producer: stage consumed
-  uint64_t agg_ready[kSlots];  // compute -> look-back: tile parked and counted
-  uint64_t slot_free[kSlots];  // look-back -> compute: tile copied out
+  uint64_t agg_ready[kPendSlots];  // compute -> look-back: tile parked and counted
+  uint64_t slot_free[kPendSlots];  // look-back -> compute: tile copied out
   StageMeta meta[kEncStages];
-  ParkedMeta parked[kSlots];
+  ParkedMeta parked[kPendSlots];
   uint32_t warp_tot[2][kWarps];  // per warp: changed elements per round, one byte each
   uint32_t ring_tail;            // ring entries before this position are copied out
 };
@@ -186,7 +172,7 @@ __device__ __forceinline__ void producer_loop(const EncodeLaunch& a, EncodeShare
 // ---------------------------------------------------------- look-back warps
 // Look-back warp w handles parked tiles w, w + W, w + 2W, ... of its CTA
 // (W = kEncLookbackWarps), each in its own slot. It takes every such tile
-// that is already counted, up to kBatch, issues all their look-back
+// that is already counted, up to kLookbackBatch, issues all their look-back
 // windows at once (one L2 round trip for the batch), then for each tile:
 // resolves its global offset, publishes its inclusive prefix, copies its
 // parked entries to the patch (entry k to position offset + k: contiguous,
@@ -237,28 +223,28 @@ __device__ __forceinline__ void copy_out(const ParkedMeta& pm, uint32_t prefix,
 __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShared& sh,
                                               const uint32_t* ring, int w, int lane, bool multi) {
   for (uint32_t i = uint32_t(w);;) {
-    const bool ok = helper_wait(&sh.agg_ready[i % kSlots], (i / kSlots) & 1u, a);
+    const bool ok = helper_wait(&sh.agg_ready[i % kPendSlots], (i / kPendSlots) & 1u, a);
     // the warp leaves together: everything below uses full-warp collectives
     if (!__all_sync(0xFFFFFFFFu, ok)) break;
     // how many more of this warp's tiles are already parked (lane 0 decides)
     int more = 0;
     if (lane == 0) {
-      for (int b = 1; b < kBatch; ++b) {
+      for (int b = 1; b < kLookbackBatch; ++b) {
         const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
-        if (!mbar_test_wait(&sh.agg_ready[ii % kSlots], (ii / kSlots) & 1u)) break;
+        if (!mbar_test_wait(&sh.agg_ready[ii % kPendSlots], (ii / kPendSlots) & 1u)) break;
         more = b;
       }
     }
     more = __shfl_sync(0xFFFFFFFFu, more, 0);
     int nb = 0;
     bool end = false;
-    uint64_t win[kBatch][kLookbackPerLane];
+    uint64_t win[kLookbackBatch][kLookbackPerLane];
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
+    for (int b = 0; b < kLookbackBatch; ++b) {
       if (b > more || end) continue;
       const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
-      const int q = int(ii % kSlots);
-      if (b > 0) mbar_test_wait(&sh.agg_ready[q], (ii / kSlots) & 1u);  // acquire for every lane
+      const int q = int(ii % kPendSlots);
+      if (b > 0) mbar_test_wait(&sh.agg_ready[q], (ii / kPendSlots) & 1u);  // acquire for every lane
       const ParkedMeta& pm = sh.parked[q];
       if (pm.last == 2u) {
         end = true;
@@ -268,10 +254,10 @@ __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShare
       nb = b + 1;
     }
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
+    for (int b = 0; b < kLookbackBatch; ++b) {
       if (b >= nb) continue;
       const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
-      const int q = int(ii % kSlots);
+      const int q = int(ii % kPendSlots);
       const ParkedMeta pm = sh.parked[q];
       const uint32_t prefix = resolve_prefix<StatusEpoch>(a, pm.tile, pm.first, pm.agg, lane, win[b]);
       if (lane == 0 && pm.last == 1u) a.counts_out[multi ? pm.tensor : 0] = uint64_t(prefix) + pm.agg;
@@ -446,9 +432,9 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
     // ---- room for the tile: its parked slot must have been copied out (the
     // look-back warp frees slots in order) and the ring must hold agg more
     // entries. Each thread checks for itself; no CTA barrier is needed.
-    const int q = int(posted % kSlots);
-    if (posted >= uint32_t(kSlots))
-      failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kSlots) / kSlots) & 1u, a);
+    const int q = int(posted % kPendSlots);
+    if (posted >= uint32_t(kPendSlots))
+      failed |= !wait_or_flag(&sh.slot_free[q], ((posted - kPendSlots) / kPendSlots) & 1u, a);
     failed |= !wait_ring_room<64>(&sh.ring_tail, ring_head, agg, uint32_t(kEncRing), a);
 
     // ---- park the compacted tile: (local index | value << 16) per entry,
@@ -492,12 +478,12 @@ __device__ __forceinline__ void compute_loop(const EncodeLaunch& a, EncodeShared
   // no more tiles (the compute warps left the loop together): wait until
   // every parked tile is copied out, then send each look-back warp its end
   // marker
-  for (uint32_t e = posted > uint32_t(kSlots) ? posted - kSlots : 0u; e < posted; ++e)
-    wait_or_flag(&sh.slot_free[e % kSlots], (e / kSlots) & 1u, a);
+  for (uint32_t e = posted > uint32_t(kPendSlots) ? posted - kPendSlots : 0u; e < posted; ++e)
+    wait_or_flag(&sh.slot_free[e % kPendSlots], (e / kPendSlots) & 1u, a);
   compute_barrier();
   for (int k = 0; k < kEncLookbackWarps; ++k) {
     const uint32_t i = posted + uint32_t(k);
-    const int q = int(i % kSlots);
+    const int q = int(i % kPendSlots);
     if (tid == 0) {
       ParkedMeta pm{};
       pm.last = 2u;
@@ -536,7 +522,7 @@ __global__ void __launch_bounds__(kEncBlockThreads, kEncMinBlocks)
       sh.meta[s].mode = kModeEnd;
     }
 #pragma unroll
-    for (int q = 0; q < kSlots; ++q) {
+    for (int q = 0; q < kPendSlots; ++q) {
       mbar_init(&sh.agg_ready[q], kWarps);
       mbar_init(&sh.slot_free[q], 1);
       sh.parked[q] = ParkedMeta{};
