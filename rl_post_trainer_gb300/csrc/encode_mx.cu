@@ -62,7 +62,6 @@ struct Fmt<kFmtE2M1> {
 };
 template <>
 struct Fmt<kFmtNvfp4> {
-  static constexpr uint32_t kEmax = 0;  // unused: the block scale is an E4M3 value
   static constexpr uint32_t kElemsPerByte = 2;
   static constexpr uint32_t kBlock = 16;
 };

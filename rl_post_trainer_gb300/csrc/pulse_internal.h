@@ -22,10 +22,11 @@ constexpr int kEncTile = kEncThreads * kEncRounds * 4;  // 4096 elements
 #endif
 // Parked tiles per CTA awaiting copy-out, and parked tiles resolved per
 // look-back round trip (PULSE_ENC_LB_BATCH), for the kernels built on the
-// encode pipeline. 16 and 2 measured faster than 8 and 4 on the 8.03B step:
-// BF16 encode 0.3 % at 8 % density and 1.6 % at 1.2 %, MXFP8 2.9 %, MXFP4
-// 5.6 %, LoCo gate 1.1 %, index packing 1.7 %; the two composition kernels
-// keep 8 and 4 of their own.
+// encode pipeline. On the 8.03B step 16 and 2 measured faster than 8 and 4
+// (BF16 encode 0.3 % at 8 % density and 1.6 % at 1.2 %, MXFP8 2.9 %, MXFP4
+// 5.6 %, LoCo gate 1.1 %, index packing 1.7 %), and 16 and 1 faster again
+// (BF16 encode 0.5 %, MXFP8 1.8 %, MXFP4 1.2 %); 32 slots cost MXFP8 its
+// third CTA per SM. The two composition kernels keep 8 and 4 of their own.
 #ifndef PULSE_ENC_PARKED
 #define PULSE_ENC_PARKED 16
 #endif
@@ -39,7 +40,7 @@ constexpr int kEncTile = kEncThreads * kEncRounds * 4;  // 4096 elements
 #define PULSE_ENC_LOOKBACK 2
 #endif
 #ifndef PULSE_ENC_LB_BATCH
-#define PULSE_ENC_LB_BATCH 2
+#define PULSE_ENC_LB_BATCH 1
 #endif
 
 constexpr int kEncStages = PULSE_ENC_STAGES;                // bulk-copy ring depth
