@@ -33,6 +33,7 @@ namespace {
 // values this kernel was tuned with).
 constexpr int kCmpSlots = 8;
 constexpr int kCmpBatch = 4;
+constexpr int kCmpWindow = 2;  // look-back words per lane and round trip
 
 #ifndef PULSE_CMP_PER_THREAD
 #define PULSE_CMP_PER_THREAD 8
@@ -394,7 +395,7 @@ __device__ __forceinline__ void cmp_lookback(const CmpLaunch& a, CmpShared& sh,
     more = __shfl_sync(0xFFFFFFFFu, more, 0);
     int nb = 0;
     bool end = false;
-    uint64_t win[kCmpBatch][kLookbackPerLane];
+    uint64_t win[kCmpBatch][kCmpWindow];
 #pragma unroll
     for (int b = 0; b < kCmpBatch; ++b) {
       if (b > more || end) continue;
@@ -406,7 +407,8 @@ __device__ __forceinline__ void cmp_lookback(const CmpLaunch& a, CmpShared& sh,
         end = true;
         continue;
       }
-      if (pm.tile != pm.first) load_window<StatusEpoch>(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
+      if (pm.tile != pm.first)
+        load_window<StatusEpoch, CmpLaunch, kCmpWindow>(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
       nb = b + 1;
     }
 #pragma unroll
@@ -415,7 +417,8 @@ __device__ __forceinline__ void cmp_lookback(const CmpLaunch& a, CmpShared& sh,
       const uint32_t ii = i + uint32_t(b);
       const int q = int(ii % kCmpSlots);
       const CmpParked pm = sh.parked[q];
-      const uint32_t prefix = resolve_prefix<StatusEpoch>(a, pm.tile, pm.first, pm.agg, lane, win[b]);
+      const uint32_t prefix = resolve_prefix<StatusEpoch, CmpLaunch, 32, kCmpWindow>(
+          a, pm.tile, pm.first, pm.agg, lane, win[b]);
       if (lane == 0 && pm.last == 1u) a.counts_out[MULTI ? pm.seg : 0] = uint64_t(prefix) + pm.agg;
       cmp_copy_out<V>(pm, prefix, ring_idx, ring_val, lane);
       __syncwarp();

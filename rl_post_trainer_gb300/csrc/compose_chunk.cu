@@ -32,8 +32,15 @@ using namespace enc;
 
 // Parked chunks per CTA and chunks resolved per look-back round trip: 8 and 4
 // (16 and 2, the other kernels' choice, measured 0.4 % slower here).
-constexpr int kCcSlots = 8;
-constexpr int kCcBatch = 4;
+#ifndef PULSE_CC_PARKED
+#define PULSE_CC_PARKED 8
+#endif
+#ifndef PULSE_CC_LB_BATCH
+#define PULSE_CC_LB_BATCH 4
+#endif
+constexpr int kCcSlots = PULSE_CC_PARKED;
+constexpr int kCcBatch = PULSE_CC_LB_BATCH;
+constexpr int kCcWindow = 2;  // look-back words per lane and round trip
 
 constexpr int kCcChunk = kApplyChunk;        // positions per chunk
 constexpr int kCcWords = kCcChunk / 32;      // bitmap words, one per compute thread
@@ -238,7 +245,7 @@ __device__ __forceinline__ void cc_lookback(const CcArgs& a, CcShared& sh, int l
     more = __shfl_sync(0xFFFFFFFFu, more, 0);
     int nb = 0;
     bool end = false;
-    uint64_t win[kCcBatch][kLookbackPerLane];
+    uint64_t win[kCcBatch][kCcWindow];
 #pragma unroll
     for (int b = 0; b < kCcBatch; ++b) {
       if (b > more || end) continue;
@@ -250,7 +257,8 @@ __device__ __forceinline__ void cc_lookback(const CcArgs& a, CcShared& sh, int l
         end = true;
         continue;
       }
-      if (pm.tile != pm.first) load_window<StatusEpoch>(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
+      if (pm.tile != pm.first)
+        load_window<StatusEpoch, CcArgs, kCcWindow>(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
       nb = b + 1;
     }
 #pragma unroll
@@ -259,7 +267,7 @@ __device__ __forceinline__ void cc_lookback(const CcArgs& a, CcShared& sh, int l
       const uint32_t ii = i + uint32_t(b);
       const int q = int(ii % kCcSlots);
       const CcParked pm = sh.parked[q];
-      const uint32_t prefix = resolve_prefix<StatusEpoch, CcArgs, kCcLookbackSleepNs>(
+      const uint32_t prefix = resolve_prefix<StatusEpoch, CcArgs, kCcLookbackSleepNs, kCcWindow>(
           a, pm.tile, pm.first, pm.agg, lane, win[b]);
       if (lane == 0 && pm.last == 1u) a.counts_out[pm.tensor] = uint64_t(prefix) + pm.agg;
       cc_copy_out(pm, prefix, sh.ring, lane);

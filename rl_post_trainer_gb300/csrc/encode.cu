@@ -37,6 +37,15 @@ namespace {
 
 using namespace enc;
 
+// Look-back words per lane and round trip. A dense tile's look-back sits on
+// its CTA's critical path, where 4 words a lane measured much slower than 2
+// (2^28 flat at 40 / 70 % density: 0.75 / 1.03 ms against 0.64 / 0.88) for
+// 0.7 % at 8 %; the sparser kernels of the pipeline take the default of 4.
+#ifndef PULSE_BF16_LOOKBACK
+#define PULSE_BF16_LOOKBACK 2
+#endif
+constexpr int kWindow = PULSE_BF16_LOOKBACK;
+
 constexpr uint32_t kStageMasterBytes = kEncTile * 4;
 constexpr uint32_t kStagePrevBytes = kEncTile * 2;
 constexpr uint32_t kStageBytes = kStageMasterBytes + kStagePrevBytes;
@@ -238,7 +247,7 @@ __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShare
     more = __shfl_sync(0xFFFFFFFFu, more, 0);
     int nb = 0;
     bool end = false;
-    uint64_t win[kLookbackBatch][kLookbackPerLane];
+    uint64_t win[kLookbackBatch][kWindow];
 #pragma unroll
     for (int b = 0; b < kLookbackBatch; ++b) {
       if (b > more || end) continue;
@@ -250,7 +259,8 @@ __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShare
         end = true;
         continue;
       }
-      if (pm.tile != pm.first) load_window<StatusEpoch>(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
+      if (pm.tile != pm.first)
+        load_window<StatusEpoch, EncodeLaunch, kWindow>(a, int64_t(pm.tile) - 1, pm.first, lane, win[b]);
       nb = b + 1;
     }
 #pragma unroll
@@ -259,7 +269,8 @@ __device__ __forceinline__ void lookback_loop(const EncodeLaunch& a, EncodeShare
       const uint32_t ii = i + uint32_t(b * kEncLookbackWarps);
       const int q = int(ii % kPendSlots);
       const ParkedMeta pm = sh.parked[q];
-      const uint32_t prefix = resolve_prefix<StatusEpoch>(a, pm.tile, pm.first, pm.agg, lane, win[b]);
+      const uint32_t prefix = resolve_prefix<StatusEpoch, EncodeLaunch, 32, kWindow>(
+          a, pm.tile, pm.first, pm.agg, lane, win[b]);
       if (lane == 0 && pm.last == 1u) a.counts_out[multi ? pm.tensor : 0] = uint64_t(prefix) + pm.agg;
       copy_out(pm, prefix, ring, lane);
       __syncwarp();

@@ -119,7 +119,10 @@ constexpr int kPkThreads = kPkCompute + 64;
 #define PULSE_PK_CTAS 3
 #endif
 constexpr int kPkStages = PULSE_PK_STAGES;
-constexpr int kPkSlots = 8;                         // parked chunks per CTA
+#ifndef PULSE_PK_PARKED
+#define PULSE_PK_PARKED 16  // 0.962 against 0.966 ms with 8 on the 8.03B patch
+#endif
+constexpr int kPkSlots = PULSE_PK_PARKED;           // parked chunks per CTA
 #ifndef PULSE_PK_RING
 #define PULSE_PK_RING 4096
 #endif
