@@ -69,13 +69,18 @@ struct Fmt<kFmtNvfp4> {
 // previous scales.
 // Stages in flight per CTA and parked-entry ring per format: a tile holds at
 // most kEncTile / elements-per-byte code entries, so the FP4 formats need
-// half the ring. (A third stage measured the same: the compute warps' per-tile
-// bookkeeping, not the prefetch depth, sets the pace.)
+// half the ring. A third stage costs MXFP8 its third CTA per SM (10.95
+// against 9.20 ms on the 8.03B step) and leaves MXFP4 unchanged (8.21 against
+// 8.19); NVFP4, whose tiles take longer to quantize, gains from it (13.94
+// against 14.05 ms).
 #ifndef PULSE_MX8_STAGES
 #define PULSE_MX8_STAGES 2
 #endif
 #ifndef PULSE_MX4_STAGES
 #define PULSE_MX4_STAGES 2
+#endif
+#ifndef PULSE_NV4_STAGES
+#define PULSE_NV4_STAGES 3
 #endif
 constexpr int kMaxMxStages = 4;
 
@@ -84,7 +89,8 @@ struct Stage {
   static constexpr uint32_t kCodeBytes = kEncTile / Fmt<F>::kElemsPerByte;
   static constexpr uint32_t kScaleBytes = kEncTile / Fmt<F>::kBlock;  // one per block
   static constexpr uint32_t kBytes = kStageMasterBytes + kCodeBytes + kScaleBytes;
-  static constexpr int kStages = F == kFmtE4M3 ? PULSE_MX8_STAGES : PULSE_MX4_STAGES;
+  static constexpr int kStages =
+      F == kFmtE4M3 ? PULSE_MX8_STAGES : (F == kFmtNvfp4 ? PULSE_NV4_STAGES : PULSE_MX4_STAGES);
   static constexpr uint32_t kRing = kCodeBytes;  // parked code entries per CTA
   static constexpr uint32_t kRingMask = kRing - 1u;
   static constexpr size_t kDynSmem = size_t(kStages) * kBytes + size_t(kRing) * 4 + 128;
