@@ -466,7 +466,10 @@ int loco_blocks_per_sm() {
 // entries are distinct elements: all of its acc loads are issued before any
 // of its stores (one memory round trip per tile instead of one per entry).
 constexpr int kAccThreads = 256;
-constexpr int kAccPerThread = 8;
+#ifndef PULSE_ACC_PER_THREAD
+#define PULSE_ACC_PER_THREAD 8  // 9.8 ms on the 8.03B step against 10.3-10.4 with 2 or 4
+#endif
+constexpr int kAccPerThread = PULSE_ACC_PER_THREAD;
 constexpr int kAccTile = kAccThreads * kAccPerThread;
 
 __device__ __forceinline__ void acc_tile(float* acc, uint64_t n, const uint32_t* idx,
