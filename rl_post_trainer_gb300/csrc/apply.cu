@@ -25,13 +25,22 @@
 namespace pulse {
 namespace {
 
+// The scatter's stores carry the evict-first hint: no sector of w is read
+// again in the launch (8 % density, 8.03B step: 4.68 against 4.75 ms).
+#ifndef PULSE_APPLY_STREAM_STORES
+#define PULSE_APPLY_STREAM_STORES 1
+#endif
 template <bool CHECKED, class V>
 __device__ __forceinline__ void scatter1(V* w, uint64_t n, uint32_t i, uint32_t v, uint32_t* err) {
   if (CHECKED && uint64_t(i) >= n) {
     record_error(err, kErrIndex);
     return;
   }
+#if PULSE_APPLY_STREAM_STORES
+  __stcs(&w[i], V(v));
+#else
   w[i] = V(v);
+#endif
 }
 
 // Apply entries [0, count) of one segment, tile `tile` of kApplyTile entries.
